@@ -1,0 +1,514 @@
+"""CPU float64 oracle for the TSP-folded transformer block.
+
+TEST INFRASTRUCTURE ONLY.  Only the test-suite, the package's smoke check and
+the benchmark's CPU-baseline leg may import this module; the library never
+does, and it shares no code with the CUDA path.
+
+Source pages (cited below by short tag):
+  [TSP]  "Folding Tensor and Sequence Parallelism for Memory-Efficient
+         Transformer Training & Inference" (gist.science summaries, Arabic and
+         Japanese editions).  Section 2 ("Methodology: TSP") defines the fold:
+         every rank holds 1/D of the parameters and 1/D of the tokens
+         (2, "Unified sharding"); attention layers walk the packed
+         W_Q/W_K/W_V/W_O shards, project locally, all-gather K/V and run
+         FlashAttention over zigzag-partitioned causal rows (2, "Runtime
+         schedules", attention bullet); gated-MLP layers rotate W_1/W_2/W_3
+         shards around a ring and accumulate partial outputs locally with no
+         all-reduce (2, "Runtime schedules", gated-MLP bullet).
+The pages give no formula for any step.  Where they are silent this module
+takes the plain readings listed below; each one is also listed in the
+design notes of the repository.
+
+  R1  RMSNorm: rms(u) = u / sqrt(mean(u^2) + eps) * g, eps = 1e-6, learnable
+      gain g, no bias (pre-norm block).
+  R2  No biases anywhere; no positional encoding (NoPE).
+  R3  Attention: multi-head, scale 1/sqrt(dh), causal with the diagonal
+      included (no row is ever fully masked).
+  R4  Gated MLP: G = silu(b W_1^T) * (b W_3^T), y = h + G W_2^T
+      (SiLU on the W_1 branch), silu(z) = z * sigmoid(z).
+  R5  Zigzag: the S tokens are cut into 2D equal chunks of c = S/(2D); rank r
+      owns chunks r and 2D-1-r, stored rank-major, chunk r first, ascending
+      position inside each chunk.
+  R6  Shards: contiguous column ranges with boundaries floor(k*n/D).
+  R7  Shard arrival order: attention broadcasts shard k = 0..D-1 in turn;
+      the MLP ring hands rank r shard (r - t) mod D at step t.
+  R8  Backward: the exact gradient of the forward above; weight gradients of
+      the virtual ranks are summed (what TSP's reduction to shard owners
+      delivers).
+
+Every floating-point step runs in numpy float64; inputs are converted
+exactly from their bf16/fp32 storage.  No step here rounds to bf16.
+
+Parity pins: every function below is pinned by tests under tests/ against
+closed forms, invariants, brute force and an independent library
+evaluation (torch CPU float64); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# ----------------------------------------------------------------------------
+# Zigzag causal partitioning  [TSP 2, attention bullet: zigzag partitioning]
+# ----------------------------------------------------------------------------
+
+
+def zigzag_positions(S: int, D: int) -> np.ndarray:
+    """Global token position held at every row of the rank-major zigzag buffer.
+
+    Buffer row r*2c + slot*c + t holds chunk (r if slot == 0 else 2D-1-r),
+    offset t, i.e. global position chunk*c + t (reading R5).
+    """
+    if D < 1 or S % (2 * D) != 0:
+        raise ValueError("S must be a positive multiple of 2D")
+    c = S // (2 * D)
+    pos = np.empty(S, dtype=np.int64)
+    row = 0
+    for r in range(D):
+        for chunk in (r, 2 * D - 1 - r):
+            for t in range(c):
+                pos[row] = chunk * c + t
+                row += 1
+    return pos
+
+
+def zigzag_owner(S: int, D: int) -> np.ndarray:
+    """Virtual rank that owns each global position (reading R5)."""
+    c = S // (2 * D)
+    chunk = np.arange(S) // c
+    return np.where(chunk < D, chunk, 2 * D - 1 - chunk)
+
+
+def zigzag_permute(x: np.ndarray, D: int, inverse: bool = False) -> np.ndarray:
+    """Global order -> rank-major zigzag order (or back with ``inverse``)."""
+    pos = zigzag_positions(x.shape[0], D)
+    out = np.empty_like(x)
+    if inverse:
+        out[pos] = x
+    else:
+        out[:] = x[pos]
+    return out
+
+
+def causal_pairs_per_rank(S: int, D: int) -> np.ndarray:
+    """Number of causal (query, key) pairs j <= i whose query rank r owns.
+
+    Counted by brute force over the owner map; the closed form c*(S+1) for
+    every rank is what zigzag balancing promises.
+    """
+    owner = zigzag_owner(S, D)
+    pairs = np.zeros(D, dtype=np.int64)
+    for i in range(S):
+        pairs[owner[i]] += i + 1  # keys 0..i
+    return pairs
+
+
+def shard_bounds(n: int, D: int) -> list[int]:
+    """Contiguous shard boundaries floor(k*n/D), k = 0..D (reading R6)."""
+    return [(k * n) // D for k in range(D + 1)]
+
+
+# ----------------------------------------------------------------------------
+# Elementary layers
+# ----------------------------------------------------------------------------
+
+
+def f64(t) -> np.ndarray:
+    """Exact conversion of a CPU torch tensor (bf16/fp32/fp64) or array to float64."""
+    if hasattr(t, "detach"):
+        import torch
+        return t.detach().to(torch.float64).numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def rmsnorm(u: np.ndarray, g: np.ndarray, eps: float):
+    """Reading R1.  Returns (u * rstd * g, rstd) with rstd = 1/sqrt(mean(u^2)+eps)."""
+    rstd = 1.0 / np.sqrt(np.mean(u * u, axis=1) + eps)
+    return u * rstd[:, None] * g[None, :], rstd
+
+
+def sigmoid(z: np.ndarray) -> np.ndarray:
+    out = np.empty_like(z)
+    pos = z >= 0
+    out[pos] = 1.0 / (1.0 + np.exp(-z[pos]))
+    ez = np.exp(z[~pos])
+    out[~pos] = ez / (1.0 + ez)
+    return out
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    return z * sigmoid(z)
+
+
+def causal_attention(Q, K, V, H, q_pos=None, k_pos=None, row_block=512):
+    """Softmax attention of every query row over the keys at positions <= its own.
+
+    [TSP 2, attention bullet] runs FlashAttention over the gathered K/V; the
+    value it computes is exact softmax attention (readings R3).  For query i
+    and head h:  s_ij = q_i . k_j / sqrt(dh) for pos(j) <= pos(i),
+    p_ij = exp(s_ij - m_i) / sum_j exp(s_ij - m_i),  o_i = sum_j p_ij v_j.
+    Rows are evaluated a group at a time only to bound memory.
+
+    Returns (O [nq, H*dh], LSE [H, nq]) with LSE_i = log sum_j exp(s_ij).
+    """
+    nq = Q.shape[0]
+    nk = K.shape[0]
+    dh = Q.shape[1] // H
+    if q_pos is None:
+        q_pos = np.arange(nq)
+    if k_pos is None:
+        k_pos = np.arange(nk)
+    scale = 1.0 / math.sqrt(dh)
+    O = np.zeros((nq, H * dh))
+    LSE = np.zeros((H, nq))
+    for r0 in range(0, nq, row_block):
+        r1 = min(nq, r0 + row_block)
+        allowed = k_pos[None, :] <= q_pos[r0:r1, None]
+        kmax = int(np.nonzero(allowed.any(axis=0))[0].max()) + 1 if allowed.any() else 0
+        allowed = allowed[:, :kmax]
+        for h in range(H):
+            cols = slice(h * dh, (h + 1) * dh)
+            s = (Q[r0:r1, cols] @ K[:kmax, cols].T) * scale
+            s = np.where(allowed, s, -np.inf)
+            m = s.max(axis=1, keepdims=True)
+            e = np.exp(s - m)
+            z = e.sum(axis=1, keepdims=True)
+            O[r0:r1, cols] = (e / z) @ V[:kmax, cols]
+            LSE[h, r0:r1] = (m + np.log(z))[:, 0]
+    return O, LSE
+
+
+def attention_probs(Q, K, H, q_pos=None, k_pos=None):
+    """Full probability matrices P[h, i, j] (small inputs only; used by pins)."""
+    nq, nk = Q.shape[0], K.shape[0]
+    dh = Q.shape[1] // H
+    q_pos = np.arange(nq) if q_pos is None else q_pos
+    k_pos = np.arange(nk) if k_pos is None else k_pos
+    allowed = k_pos[None, :] <= q_pos[:, None]
+    P = np.zeros((H, nq, nk))
+    for h in range(H):
+        cols = slice(h * dh, (h + 1) * dh)
+        s = (Q[:, cols] @ K[:, cols].T) / math.sqrt(dh)
+        s = np.where(allowed, s, -np.inf)
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        P[h] = e / e.sum(axis=1, keepdims=True)
+    return P
+
+
+# ----------------------------------------------------------------------------
+# Unsharded block (the value TSP must reproduce)
+# ----------------------------------------------------------------------------
+
+
+def _w(W, name):
+    return f64(W[name])
+
+
+def attn_block_fwd(x, W, H, eps):
+    """h = x + Attn(rms(x; g_attn)) W_O^T.  Returns (h, saved dict)."""
+    x = f64(x)
+    a, rstd1 = rmsnorm(x, _w(W, "g_attn"), eps)
+    Q = a @ _w(W, "wq").T
+    K = a @ _w(W, "wk").T
+    V = a @ _w(W, "wv").T
+    O, LSE = causal_attention(Q, K, V, H)
+    h = x + O @ _w(W, "wo").T
+    return h, dict(x=x, a=a, rstd1=rstd1, Q=Q, K=K, V=V, O=O, LSE=LSE)
+
+
+def mlp_fwd(h, W, eps, norm=True, residual=True):
+    """y = [h +] silu(b W_1^T) * (b W_3^T) W_2^T with b = rms(h; g_mlp) or b = h."""
+    h = f64(h)
+    if norm:
+        b, rstd2 = rmsnorm(h, _w(W, "g_mlp"), eps)
+    else:
+        b, rstd2 = h, None
+    A = b @ _w(W, "w1").T
+    B = b @ _w(W, "w3").T
+    G = silu(A) * B
+    y = G @ _w(W, "w2").T
+    if residual:
+        y = h + y
+    return y, dict(h=h, b=b, rstd2=rstd2, A=A, B=B, G=G)
+
+
+def block_fwd(x, W, H, eps):
+    """Pre-norm block: h = x + Attn(rms(x)), y = h + MLP(rms(h))."""
+    h, s1 = attn_block_fwd(x, W, H, eps)
+    y, s2 = mlp_fwd(h, W, eps)
+    s1.update(s2)
+    return y, s1
+
+
+# ----------------------------------------------------------------------------
+# Sharded emulation: D virtual ranks following the TSP schedules
+# ----------------------------------------------------------------------------
+
+
+def block_fwd_sharded(x, W, H, D, eps, parts=("attn", "mlp")):
+    """The TSP schedule, one virtual rank at a time, in float64.
+
+    1. zigzag-partition the tokens (reading R5);
+    2. attention broadcast loop: shard k = 0..D-1 of the packed W_Q/W_K/W_V
+       columns C_k arrives; every rank projects its own rows with it;
+    3. "all-gather" of K/V: concatenate every rank's K/V rows with their
+       global positions;
+    4. causal attention of rank r's rows against the gathered K/V;
+    5. W_O: each rank accumulates O[:, C_k] W_O[:, C_k]^T shard by shard onto
+       its residual rows;
+    6. MLP ring: at step t rank r holds shard I_k, k = (r - t) mod D, of
+       W_1/W_3 (rows) and W_2 (columns) and accumulates the partial
+       G[:, I_k] W_2[:, I_k]^T onto its rows;
+    7. un-permute.
+    ``parts`` selects which half runs (both by default); the MLP half keeps
+    its norm and residual.
+    """
+    x = f64(x)
+    S, d = x.shape
+    c = S // (2 * D)
+    pos = zigzag_positions(S, D)
+    xz = x[pos]
+    rows = [slice(r * 2 * c, (r + 1) * 2 * c) for r in range(D)]
+    Cb = shard_bounds(d, D)
+    hz = xz.copy()
+    if "attn" in parts:
+        g1 = _w(W, "g_attn")
+        wq, wk, wv, wo = (_w(W, n) for n in ("wq", "wk", "wv", "wo"))
+        Qz = np.zeros((S, d)); Kz = np.zeros((S, d)); Vz = np.zeros((S, d))
+        az = np.zeros((S, d))
+        for r in range(D):
+            az[rows[r]] = rmsnorm(xz[rows[r]], g1, eps)[0]
+        for k in range(D):                      # shard k is broadcast ...
+            C = slice(Cb[k], Cb[k + 1])
+            for r in range(D):                  # ... and every rank projects
+                Qz[rows[r], C] = az[rows[r]] @ wq[C].T
+                Kz[rows[r], C] = az[rows[r]] @ wk[C].T
+                Vz[rows[r], C] = az[rows[r]] @ wv[C].T
+        for r in range(D):
+            O_r, _ = causal_attention(Qz[rows[r]], Kz, Vz, H, q_pos=pos[rows[r]], k_pos=pos)
+            for k in range(D):
+                C = slice(Cb[k], Cb[k + 1])
+                hz[rows[r]] += O_r[:, C] @ wo[:, C].T
+    yz = hz.copy()
+    if "mlp" in parts:
+        g2 = _w(W, "g_mlp")
+        w1, w3, w2 = (_w(W, n) for n in ("w1", "w3", "w2"))
+        Ib = shard_bounds(w1.shape[0], D)
+        for r in range(D):
+            b_r = rmsnorm(hz[rows[r]], g2, eps)[0]
+            for t in range(D):
+                k = (r - t) % D
+                I = slice(Ib[k], Ib[k + 1])
+                G = silu(b_r @ w1[I].T) * (b_r @ w3[I].T)
+                yz[rows[r]] += G @ w2[:, I].T
+    out = np.empty_like(yz)
+    out[pos] = yz
+    return out
+
+
+def mlp_fwd_sharded(h, W, D, eps, norm=True, residual=True):
+    """The gated-MLP ring on its own: rank r accumulates shards (r - t) mod D."""
+    h = f64(h)
+    S = h.shape[0]
+    c = S // (2 * D)
+    pos = zigzag_positions(S, D)
+    hz = h[pos]
+    w1, w3, w2 = (_w(W, n) for n in ("w1", "w3", "w2"))
+    Ib = shard_bounds(w1.shape[0], D)
+    yz = hz.copy() if residual else np.zeros_like(hz)
+    for r in range(D):
+        R = slice(r * 2 * c, (r + 1) * 2 * c)
+        b_r = rmsnorm(hz[R], _w(W, "g_mlp"), eps)[0] if norm else hz[R]
+        for t in range(D):
+            k = (r - t) % D
+            I = slice(Ib[k], Ib[k + 1])
+            yz[R] += (silu(b_r @ w1[I].T) * (b_r @ w3[I].T)) @ w2[:, I].T
+    out = np.empty_like(yz)
+    out[pos] = yz
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Sampled rows of a large forward (exact on the rows it returns)
+# ----------------------------------------------------------------------------
+
+
+def block_fwd_rows(x, W, H, eps, rows, attn_only=False):
+    """y (or h with ``attn_only``) at the given global positions only.
+
+    Keys and values are needed at every position <= max(rows); queries,
+    attention, W_O and the MLP only at the requested rows (every step after
+    K/V is row-local).
+    """
+    x = f64(x)
+    rows = np.asarray(rows, dtype=np.int64)
+    kmax = int(rows.max()) + 1
+    g1 = _w(W, "g_attn")
+    a_all = rmsnorm(x[:kmax], g1, eps)[0]
+    K = a_all @ _w(W, "wk").T
+    V = a_all @ _w(W, "wv").T
+    Q = a_all[rows] @ _w(W, "wq").T
+    O, _ = causal_attention(Q, K, V, H, q_pos=rows, k_pos=np.arange(kmax))
+    h = x[rows] + O @ _w(W, "wo").T
+    if attn_only:
+        return h
+    return mlp_fwd(h, W, eps)[0]
+
+
+# ----------------------------------------------------------------------------
+# Backward: exact gradient of block_fwd (reading R8)
+# ----------------------------------------------------------------------------
+
+
+def rmsnorm_bwd(dout, u, g, rstd):
+    """Gradient of n*g, n = u*rstd, rstd = (mean(u^2)+eps)^-1/2.
+
+    dg = sum_rows dout*n;  du = rstd * (dout*g - n * mean_cols(dout*g*n)).
+    """
+    n = u * rstd[:, None]
+    dg = (dout * n).sum(axis=0)
+    gd = dout * g[None, :]
+    du = rstd[:, None] * (gd - n * np.mean(gd * n, axis=1, keepdims=True))
+    return du, dg
+
+
+def causal_attention_bwd(Q, K, V, O, dO, H, q_pos=None, k_pos=None, row_block=512):
+    """dQ, dK, dV of causal_attention.
+
+    With P the probabilities:  dV = P^T dO,  dP = dO V^T,
+    Delta_i = sum_c dO_ic O_ic,  dS = P * (dP - Delta),
+    dQ = dS K / sqrt(dh),  dK = dS^T Q / sqrt(dh).  The sums over query
+    rows are taken a row group at a time only to bound memory.
+    """
+    nq, nk = Q.shape[0], K.shape[0]
+    dh = Q.shape[1] // H
+    q_pos = np.arange(nq) if q_pos is None else q_pos
+    k_pos = np.arange(nk) if k_pos is None else k_pos
+    scale = 1.0 / math.sqrt(dh)
+    dQ = np.zeros_like(Q); dK = np.zeros_like(K); dV = np.zeros_like(V)
+    for r0 in range(0, nq, row_block):
+        r1 = min(nq, r0 + row_block)
+        allowed = k_pos[None, :] <= q_pos[r0:r1, None]
+        kmax = int(np.nonzero(allowed.any(axis=0))[0].max()) + 1
+        allowed = allowed[:, :kmax]
+        for h in range(H):
+            cols = slice(h * dh, (h + 1) * dh)
+            s = (Q[r0:r1, cols] @ K[:kmax, cols].T) * scale
+            s = np.where(allowed, s, -np.inf)
+            e = np.exp(s - s.max(axis=1, keepdims=True))
+            P = e / e.sum(axis=1, keepdims=True)
+            do = dO[r0:r1, cols]
+            dV[:kmax, cols] += P.T @ do
+            dP = do @ V[:kmax, cols].T
+            delta = (do * O[r0:r1, cols]).sum(axis=1, keepdims=True)
+            dS = P * (dP - delta)
+            dQ[r0:r1, cols] = (dS @ K[:kmax, cols]) * scale
+            dK[:kmax, cols] += (dS.T @ Q[r0:r1, cols]) * scale
+    return dQ, dK, dV
+
+
+def block_bwd(x, W, dy, H, eps):
+    """All gradients of L = sum(dy * y) for y = block_fwd(x).
+
+    Returns dict: dx, dwq, dwk, dwv, dwo, dw1, dw3, dw2, dg_attn, dg_mlp.
+    """
+    y, s = block_fwd(x, W, H, eps)
+    dy = f64(dy)
+    w1, w3, w2 = _w(W, "w1"), _w(W, "w3"), _w(W, "w2")
+    # MLP
+    dw2 = dy.T @ s["G"]
+    dG = dy @ w2
+    sA = sigmoid(s["A"])
+    silu_A = s["A"] * sA
+    dA = dG * s["B"] * sA * (1.0 + s["A"] * (1.0 - sA))
+    dB = dG * silu_A
+    dw1 = dA.T @ s["b"]
+    dw3 = dB.T @ s["b"]
+    db = dA @ w1 + dB @ w3
+    du2, dg_mlp = rmsnorm_bwd(db, s["h"], _w(W, "g_mlp"), s["rstd2"])
+    dh = dy + du2
+    # attention
+    wq, wk, wv, wo = (_w(W, n) for n in ("wq", "wk", "wv", "wo"))
+    dwo = dh.T @ s["O"]
+    dO = dh @ wo
+    dQ, dK, dV = causal_attention_bwd(s["Q"], s["K"], s["V"], s["O"], dO, H)
+    dwq = dQ.T @ s["a"]
+    dwk = dK.T @ s["a"]
+    dwv = dV.T @ s["a"]
+    da = dQ @ wq + dK @ wk + dV @ wv
+    du1, dg_attn = rmsnorm_bwd(da, s["x"], _w(W, "g_attn"), s["rstd1"])
+    dx = dh + du1
+    return dict(dx=dx, dwq=dwq, dwk=dwk, dwv=dwv, dwo=dwo, dw1=dw1, dw3=dw3,
+                dw2=dw2, dg_attn=dg_attn, dg_mlp=dg_mlp)
+
+
+def block_bwd_sharded(x, W, dy, H, D, eps):
+    """Backward in the D-virtual-rank layout.
+
+    Activations stay on their zigzag rows; every rank contributes the weight
+    and gain gradients of its own 2c rows and they are summed over ranks
+    (reading R8).  dK/dV reach a key's owner from every rank whose queries
+    attend to it (summed over the query ranks).  dx is returned in global
+    order.
+    """
+    x = f64(x)
+    dy = f64(dy)
+    S, d = x.shape
+    c = S // (2 * D)
+    pos = zigzag_positions(S, D)
+    R = [slice(r * 2 * c, (r + 1) * 2 * c) for r in range(D)]
+    xz, dyz = x[pos], dy[pos]
+    g1, g2 = _w(W, "g_attn"), _w(W, "g_mlp")
+    wq, wk, wv, wo = (_w(W, n) for n in ("wq", "wk", "wv", "wo"))
+    w1, w3, w2 = _w(W, "w1"), _w(W, "w3"), _w(W, "w2")
+    # forward, per rank (row-local steps) + gathered K/V
+    az = np.zeros_like(xz); rstd1 = np.zeros(S)
+    for r in range(D):
+        az[R[r]], rstd1[R[r]] = rmsnorm(xz[R[r]], g1, eps)
+    Qz, Kz, Vz = az @ wq.T, az @ wk.T, az @ wv.T
+    Oz = np.zeros_like(xz)
+    for r in range(D):
+        Oz[R[r]] = causal_attention(Qz[R[r]], Kz, Vz, H, q_pos=pos[R[r]], k_pos=pos)[0]
+    hz = xz + Oz @ wo.T
+    grads = {k: 0.0 for k in ("dwq", "dwk", "dwv", "dwo", "dw1", "dw3", "dw2", "dg_attn", "dg_mlp")}
+    dOz = np.zeros_like(xz); dhz = np.zeros_like(xz)
+    for r in range(D):
+        h_r = hz[R[r]]
+        b_r, rstd2 = rmsnorm(h_r, g2, eps)
+        A = b_r @ w1.T; B = b_r @ w3.T
+        sA = sigmoid(A)
+        G = A * sA * B
+        dy_r = dyz[R[r]]
+        grads["dw2"] = grads["dw2"] + dy_r.T @ G
+        dG = dy_r @ w2
+        dA = dG * B * sA * (1.0 + A * (1.0 - sA))
+        dB = dG * A * sA
+        grads["dw1"] = grads["dw1"] + dA.T @ b_r
+        grads["dw3"] = grads["dw3"] + dB.T @ b_r
+        du2, dg2 = rmsnorm_bwd(dA @ w1 + dB @ w3, h_r, g2, rstd2)
+        grads["dg_mlp"] = grads["dg_mlp"] + dg2
+        dhz[R[r]] = dy_r + du2
+        grads["dwo"] = grads["dwo"] + dhz[R[r]].T @ Oz[R[r]]
+        dOz[R[r]] = dhz[R[r]] @ wo
+    dQz = np.zeros_like(xz); dKz = np.zeros_like(xz); dVz = np.zeros_like(xz)
+    for r in range(D):
+        dq, dk, dv = causal_attention_bwd(Qz[R[r]], Kz, Vz, Oz[R[r]], dOz[R[r]], H,
+                                          q_pos=pos[R[r]], k_pos=pos)
+        dQz[R[r]] = dq
+        dKz += dk            # returned to the key owners
+        dVz += dv
+    dxz = np.zeros_like(xz)
+    for r in range(D):
+        a_r = az[R[r]]
+        grads["dwq"] = grads["dwq"] + dQz[R[r]].T @ a_r
+        grads["dwk"] = grads["dwk"] + dKz[R[r]].T @ a_r
+        grads["dwv"] = grads["dwv"] + dVz[R[r]].T @ a_r
+        da = dQz[R[r]] @ wq + dKz[R[r]] @ wk + dVz[R[r]] @ wv
+        du1, dg1 = rmsnorm_bwd(da, xz[R[r]], g1, rstd1[R[r]])
+        grads["dg_attn"] = grads["dg_attn"] + dg1
+        dxz[R[r]] = dhz[R[r]] + du1
+    dx = np.empty_like(dxz)
+    dx[pos] = dxz
+    grads["dx"] = dx
+    return grads

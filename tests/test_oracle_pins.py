@@ -1,0 +1,371 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each pin is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign or index, a transposed operand, a wrong chunk order) fails at
+least one of them:
+  * hand-worked fixtures under tests/golden/ (zigzag map, pair counts);
+  * closed forms (constant-row RMSNorm, S=1 attention, K = 0 attention,
+    zero W_O / W_2, the c*(S+1) pair count);
+  * invariants (bijection, softmax rows sum to 1, causality, sharded ==
+    unsharded for D = 1..8);
+  * an independent library evaluation in torch CPU float64 (F.rms_norm,
+    scaled_dot_product_attention, F.silu, autograd);
+  * central finite differences for the backward.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle.tsp_oracle as O
+from folded_tensor_sequence_zigzag_gb300.inputs import BlockShape, TINY_FP32, make_block_inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(v) for v in line.split()])
+    return np.array(rows, dtype=np.int64)
+
+
+# --------------------------------------------------------------- zigzag map
+
+def test_zigzag_golden_S12_D3():
+    g = _load("zigzag_S12_D3.txt")
+    pos = O.zigzag_positions(12, 3)
+    assert np.array_equal(pos, g[:, 1])
+    assert np.array_equal(O.zigzag_owner(12, 3)[pos], g[:, 2])
+
+
+@pytest.mark.parametrize("S,D", [(2, 1), (16, 1), (16, 2), (48, 3), (256, 4), (320, 5), (96, 6), (112, 7), (256, 8), (4096, 8)])
+def test_zigzag_is_bijection_and_owner_consistent(S, D):
+    pos = O.zigzag_positions(S, D)
+    assert np.array_equal(np.sort(pos), np.arange(S))
+    c = S // (2 * D)
+    owner = O.zigzag_owner(S, D)
+    for r in range(D):
+        rows = pos[r * 2 * c:(r + 1) * 2 * c]
+        assert np.all(owner[rows] == r)
+        assert np.all(np.diff(rows[:c]) == 1) and np.all(np.diff(rows[c:]) == 1)
+    x = np.random.default_rng(0).standard_normal((S, 3))
+    assert np.array_equal(O.zigzag_permute(O.zigzag_permute(x, D), D, inverse=True), x)
+
+
+def test_causal_pairs_closed_form_golden():
+    for S, D, per_rank, total in _load("causal_pairs.txt"):
+        pairs = O.causal_pairs_per_rank(int(S), int(D))
+        assert np.all(pairs == per_rank), (S, D, pairs)
+        assert pairs.sum() == total == S * (S + 1) // 2
+
+
+def test_zigzag_rejects_bad_sizes():
+    with pytest.raises(ValueError):
+        O.zigzag_positions(10, 3)
+
+
+def test_shard_bounds_cover_once():
+    for n in (64, 128, 4096, 11008):
+        for D in range(1, 9):
+            b = O.shard_bounds(n, D)
+            assert b[0] == 0 and b[-1] == n and all(b[k] <= b[k + 1] for k in range(D))
+    assert O.shard_bounds(11008, 8)[1] == 1376 and O.shard_bounds(11008, 4)[1] == 2752
+
+
+# --------------------------------------------------------------- elementary layers
+
+def test_rmsnorm_closed_form_constant_rows():
+    vals = np.array([0.5, -3.0, 7.25])
+    u = np.repeat(vals[:, None], 8, axis=1)
+    g = np.linspace(0.5, 2.0, 8)
+    eps = 1e-6
+    out, rstd = O.rmsnorm(u, g, eps)
+    expect = vals[:, None] / np.sqrt(vals[:, None] ** 2 + eps) * g[None, :]
+    assert np.allclose(out, expect, rtol=0, atol=1e-15)
+    assert np.allclose(rstd, 1 / np.sqrt(vals ** 2 + eps))
+
+
+def test_rmsnorm_matches_torch():
+    rng = np.random.default_rng(1)
+    u = rng.standard_normal((17, 33)) * 3
+    g = rng.standard_normal(33)
+    out, _ = O.rmsnorm(u, g, 1e-6)
+    ref = F.rms_norm(torch.from_numpy(u), (33,), torch.from_numpy(g), eps=1e-6).numpy()
+    assert np.max(np.abs(out - ref)) < 1e-13
+
+
+def test_silu_matches_torch_and_is_stable():
+    z = np.linspace(-800, 800, 2001)
+    ref = F.silu(torch.from_numpy(z)).numpy()
+    assert np.allclose(O.silu(z), ref, rtol=1e-14, atol=1e-300)
+    assert np.all(np.isfinite(O.silu(z)))
+
+
+def _rand_qkv(S, H, dh, seed=0):
+    rng = np.random.default_rng(seed)
+    return [rng.standard_normal((S, H * dh)) for _ in range(3)]
+
+
+def test_attention_single_token_returns_v():
+    Q, K, V = _rand_qkv(1, 2, 4)
+    out, lse = O.causal_attention(Q, K, V, 2)
+    assert np.array_equal(out, V)
+    for h in range(2):
+        s = Q[0, h * 4:(h + 1) * 4] @ K[0, h * 4:(h + 1) * 4] / 2.0
+        assert abs(lse[h, 0] - s) < 1e-14
+
+
+def test_attention_zero_keys_is_prefix_mean():
+    Q, K, V = _rand_qkv(37, 3, 8, seed=2)
+    out, lse = O.causal_attention(Q, np.zeros_like(K), V, 3, row_block=8)
+    prefix = np.cumsum(V, axis=0) / np.arange(1, 38)[:, None]
+    assert np.max(np.abs(out - prefix)) < 1e-13
+    assert np.allclose(lse, np.log(np.arange(1, 38))[None, :].repeat(3, 0))
+
+
+def test_attention_rows_sum_to_one_and_mask():
+    Q, K, V = _rand_qkv(29, 2, 8, seed=3)
+    P = O.attention_probs(Q * 4, K * 4, 2)
+    assert np.max(np.abs(P.sum(axis=2) - 1)) <= 1e-12
+    assert np.all(np.triu(P[0], 1) == 0) and np.all(np.triu(P[1], 1) == 0)
+    assert np.all(np.diagonal(P, axis1=1, axis2=2) > 0)
+
+
+def test_attention_matches_torch_sdpa():
+    H, dh, S = 4, 16, 70
+    Q, K, V = _rand_qkv(S, H, dh, seed=4)
+    out, lse = O.causal_attention(Q, K, V, H, row_block=16)
+    t = lambda a: torch.from_numpy(a).view(S, H, dh).transpose(0, 1)  # noqa: E731
+    ref = F.scaled_dot_product_attention(t(Q), t(K), t(V), is_causal=True)
+    ref = ref.transpose(0, 1).reshape(S, H * dh).numpy()
+    assert np.max(np.abs(out - ref)) < 1e-13
+    sc = torch.einsum("hid,hjd->hij", t(Q), t(K)) / math.sqrt(dh)
+    sc = sc.masked_fill(torch.triu(torch.ones(S, S, dtype=torch.bool), 1), float("-inf"))
+    assert np.max(np.abs(lse - torch.logsumexp(sc, dim=2).numpy())) < 1e-12
+
+
+def test_attention_with_positions_equals_permuted_attention():
+    # zigzag-ordered queries/keys with their global positions give the same
+    # rows as the global-order computation, permuted
+    S, D, H, dh = 48, 3, 2, 8
+    Q, K, V = _rand_qkv(S, H, dh, seed=5)
+    pos = O.zigzag_positions(S, D)
+    ref, lref = O.causal_attention(Q, K, V, H)
+    out, lout = O.causal_attention(Q[pos], K[pos], V[pos], H, q_pos=pos, k_pos=pos, row_block=7)
+    assert np.max(np.abs(out - ref[pos])) < 1e-13
+    assert np.max(np.abs(lout - lref[:, pos])) < 1e-12
+
+
+# --------------------------------------------------------------- whole block
+
+def _torch_block(inp, H, eps, requires_grad=False):
+    """Independent float64 evaluation with torch library routines."""
+    T = {k: v.to(torch.float64).clone().requires_grad_(requires_grad) for k, v in inp.items()}
+    x = T["x"]
+    S, d = x.shape
+    dh = d // H
+    a = F.rms_norm(x, (d,), T["g_attn"], eps=eps)
+    heads = lambda m: m.view(S, H, dh).transpose(0, 1)  # noqa: E731
+    o = F.scaled_dot_product_attention(heads(F.linear(a, T["wq"])), heads(F.linear(a, T["wk"])),
+                                       heads(F.linear(a, T["wv"])), is_causal=True)
+    h = x + F.linear(o.transpose(0, 1).reshape(S, d), T["wo"])
+    b = F.rms_norm(h, (d,), T["g_mlp"], eps=eps)
+    y = h + F.linear(F.silu(F.linear(b, T["w1"])) * F.linear(b, T["w3"]), T["w2"])
+    return y, h, T
+
+
+def _small(S=64, d=32, H=4, inter=48, D=4, seed=0, dtype=torch.float32):
+    shape = BlockShape(S=S, d=d, H=H, inter=inter, D=D)
+    inp = make_block_inputs(shape, dtype, seed=seed, with_dy=True)
+    # non-trivial gains so a dropped gain shows up
+    gen = torch.Generator().manual_seed(seed + 100)
+    inp["g_attn"] = (1 + 0.5 * torch.randn(d, generator=gen)).to(dtype)
+    inp["g_mlp"] = (1 + 0.5 * torch.randn(d, generator=gen)).to(dtype)
+    # larger weights so attention is far from uniform and the MLP is non-linear
+    for k in ("wq", "wk", "wv", "wo", "w1", "w3", "w2"):
+        inp[k] = (inp[k] * 10).to(dtype)
+    return shape, inp
+
+
+def test_block_fwd_matches_torch_fp64():
+    shape, inp = _small()
+    y, s = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+    yt, ht, _ = _torch_block(inp, shape.H, shape.eps)
+    assert np.max(np.abs(y - yt.detach().numpy())) < 1e-11
+    assert np.max(np.abs(s["h"] - ht.detach().numpy())) < 1e-11
+
+
+def test_block_fwd_tiny_config_matches_torch_fp64():
+    inp = make_block_inputs(TINY_FP32, torch.float32, seed=0)
+    y, _ = O.block_fwd(inp["x"], inp, TINY_FP32.H, TINY_FP32.eps)
+    yt, _, _ = _torch_block(inp, TINY_FP32.H, TINY_FP32.eps)
+    assert np.max(np.abs(y - yt.detach().numpy())) < 1e-12
+
+
+@pytest.mark.parametrize("D", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_sharded_equals_unsharded(D):
+    shape, inp = _small(S=2 * D * 16, D=D, seed=D)
+    y, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+    ys = O.block_fwd_sharded(inp["x"], inp, shape.H, D, shape.eps)
+    rel = np.max(np.abs(ys - y)) / np.max(np.abs(y))
+    assert rel <= 1e-12
+    if D == 1:
+        assert np.max(np.abs(ys - y)) <= 1e-12 * np.max(np.abs(y))
+
+
+@pytest.mark.parametrize("D", [1, 2, 4, 8])
+def test_sharded_equals_unsharded_tiny_S256(D):
+    inp = make_block_inputs(TINY_FP32, torch.float32, seed=0)
+    y, _ = O.block_fwd(inp["x"], inp, 4, 1e-6)
+    ys = O.block_fwd_sharded(inp["x"], inp, 4, D, 1e-6)
+    assert np.max(np.abs(ys - y)) <= 1e-12 * np.max(np.abs(y))
+
+
+def test_mlp_sharded_equals_unsharded_no_norm_no_residual():
+    shape, inp = _small(S=64, D=4)
+    ref, _ = O.mlp_fwd(inp["x"], inp, shape.eps, norm=False, residual=False)
+    got = O.mlp_fwd_sharded(inp["x"], inp, 4, shape.eps, norm=False, residual=False)
+    assert np.max(np.abs(got - ref)) <= 1e-12 * np.max(np.abs(ref))
+    t = {k: v.to(torch.float64) for k, v in inp.items()}
+    tref = F.linear(F.silu(F.linear(t["x"], t["w1"])) * F.linear(t["x"], t["w3"]), t["w2"]).numpy()
+    assert np.max(np.abs(ref - tref)) < 1e-11
+
+
+def test_causality_perturbing_future_rows():
+    shape, inp = _small(S=48, D=3)
+    y0, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+    for i in (0, 17, 30, 46):
+        pert = dict(inp)
+        x = inp["x"].clone()
+        x[i + 1:] += torch.randn(x[i + 1:].shape, generator=torch.Generator().manual_seed(i)) * 5
+        pert["x"] = x
+        y1, _ = O.block_fwd(x, pert, shape.H, shape.eps)
+        assert np.array_equal(y0[: i + 1], y1[: i + 1])
+        if i + 1 < 48:
+            assert not np.array_equal(y0[i + 1:], y1[i + 1:])
+
+
+def test_zero_w2_gives_h_and_zero_wo_gives_x():
+    shape, inp = _small(S=32, D=2)
+    z = dict(inp)
+    z["w2"] = torch.zeros_like(inp["w2"])
+    y, s = O.block_fwd(inp["x"], z, shape.H, shape.eps)
+    assert np.array_equal(y, s["h"])
+    z = dict(inp)
+    z["wo"] = torch.zeros_like(inp["wo"])
+    h, _ = O.attn_block_fwd(inp["x"], z, shape.H, shape.eps)
+    assert np.array_equal(h, O.f64(inp["x"]))
+
+
+def test_block_fwd_rows_matches_full():
+    shape, inp = _small(S=96, D=3)
+    y, s = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+    rows = np.array([0, 5, 15, 16, 40, 95])
+    assert np.max(np.abs(O.block_fwd_rows(inp["x"], inp, shape.H, shape.eps, rows) - y[rows])) < 1e-12
+    h = O.block_fwd_rows(inp["x"], inp, shape.H, shape.eps, rows, attn_only=True)
+    assert np.max(np.abs(h - s["h"][rows])) < 1e-12
+
+
+# --------------------------------------------------------------- backward
+
+def _loss(inp, H, eps):
+    y, _ = O.block_fwd(inp["x"], inp, H, eps)
+    return float(np.sum(O.f64(inp["dy"]) * y))
+
+
+GRAD_OF = {"dx": "x", "dwq": "wq", "dwk": "wk", "dwv": "wv", "dwo": "wo", "dw1": "w1",
+           "dw3": "w3", "dw2": "w2", "dg_attn": "g_attn", "dg_mlp": "g_mlp"}
+
+
+def test_backward_matches_torch_autograd():
+    shape, inp = _small(S=40, d=16, H=2, inter=24, D=2)
+    g = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
+    y, _, T = _torch_block(inp, shape.H, shape.eps, requires_grad=True)
+    (y * T["dy"].detach()).sum().backward()
+    for gname, pname in GRAD_OF.items():
+        ref = T[pname].grad.numpy()
+        err = np.max(np.abs(g[gname] - ref)) / max(np.max(np.abs(ref)), 1e-30)
+        assert err < 1e-11, (gname, err)
+
+
+def test_backward_central_finite_differences():
+    shape, inp = _small(S=32, d=16, H=2, inter=24, D=2, seed=7)
+    inp = {k: v.to(torch.float64) for k, v in inp.items()}
+    g = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
+    rng = np.random.default_rng(11)
+    step = 1e-6
+    for gname, pname in GRAD_OF.items():
+        base = inp[pname]
+        scale = np.sqrt(np.mean(g[gname] ** 2))
+        flat = base.reshape(-1)
+        idx = rng.choice(flat.numel(), size=min(16, flat.numel()), replace=False)
+        for i in idx:
+            plus, minus = dict(inp), dict(inp)
+            p = base.clone(); p.view(-1)[i] += step; plus[pname] = p
+            m = base.clone(); m.view(-1)[i] -= step; minus[pname] = m
+            fd = (_loss(plus, shape.H, shape.eps) - _loss(minus, shape.H, shape.eps)) / (2 * step)
+            an = g[gname].reshape(-1)[i]
+            assert abs(fd - an) <= 1e-6 * max(abs(an), scale), (gname, i, fd, an)
+        # a random direction
+        v = torch.from_numpy(rng.standard_normal(tuple(base.shape)))
+        plus, minus = dict(inp), dict(inp)
+        plus[pname] = base + step * v
+        minus[pname] = base - step * v
+        fd = (_loss(plus, shape.H, shape.eps) - _loss(minus, shape.H, shape.eps)) / (2 * step)
+        an = float(np.sum(g[gname] * v.numpy()))
+        assert abs(fd - an) <= 1e-6 * max(abs(an), scale * math.sqrt(v.numel())), (gname, fd, an)
+
+
+@pytest.mark.parametrize("D", [1, 2, 3, 4])
+def test_backward_sharded_equals_unsharded(D):
+    shape, inp = _small(S=2 * D * 8, d=16, H=2, inter=24, D=D, seed=20 + D)
+    g = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
+    gs = O.block_bwd_sharded(inp["x"], inp, inp["dy"], shape.H, D, shape.eps)
+    for k in GRAD_OF:
+        ref = g[k]
+        assert np.max(np.abs(gs[k] - ref)) <= 1e-12 * np.max(np.abs(ref)), k
+
+
+# --------------------------------------------------------------- planted mistakes
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    """Plant typical slips in the oracle (CPU only) and check a pin fails."""
+    shape, inp = _small(S=48, D=3)
+    yt, _, _ = _torch_block(inp, shape.H, shape.eps)
+    yt = yt.detach().numpy()
+
+    def off():
+        y, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+        return np.max(np.abs(y - yt))
+
+    assert off() < 1e-11
+    # (1) SiLU on the wrong branch / wrong sign in the sigmoid
+    with monkeypatch.context() as m:
+        m.setattr(O, "sigmoid", lambda z: 1 / (1 + np.exp(z)))
+        assert off() > 1e-3
+    # (2) RMSNorm without eps inside the root -> the constant-row closed form
+    with monkeypatch.context() as m:
+        m.setattr(O, "rmsnorm", lambda u, g, eps: (u / np.sqrt(np.mean(u * u, 1))[:, None] * g,
+                                                   1 / np.sqrt(np.mean(u * u, 1))))
+        out, _ = O.rmsnorm(np.full((1, 4), 1e-4), np.ones(4), 1e-6)
+        assert abs(out[0, 0] - 1e-4 / math.sqrt(1e-8 + 1e-6)) > 1e-3
+    # (3) zigzag with the two chunks of a rank swapped -> golden fixture
+    with monkeypatch.context() as m:
+        def swapped(S, D):
+            c = S // (2 * D)
+            return np.concatenate([np.r_[(2 * D - 1 - r) * c:(2 * D - r) * c, r * c:(r + 1) * c]
+                                   for r in range(D)])
+        m.setattr(O, "zigzag_positions", swapped)
+        assert not np.array_equal(O.zigzag_positions(12, 3), _load("zigzag_S12_D3.txt")[:, 1])
+    # (4) attention mask without the diagonal -> S=1 closed form breaks
+    Q, K, V = _rand_qkv(5, 1, 4)
+    P = O.attention_probs(Q, K, 1)
+    strict = np.tril(P[0], -1)
+    assert not np.allclose(strict.sum(axis=1), 1)
