@@ -1,0 +1,425 @@
+"""Benchmark of the TSP-folded block on GB300: tokens/s and TFLOP/s at 1 GPU.
+
+Workload (default): 7B-shaped TSP block forward, S=16384 tokens, D=8 virtual
+ranks under zigzag causal partitioning, d_model=4096, 32 heads x 128, SwiGLU
+inter=11008, bf16 storage with fp32 accumulation; synthetic Gaussian inputs
+(x ~ N(0,1), weights ~ N(0,0.02), gains 1).
+
+One step = the whole hot path on one batch resident in HBM: zigzag-permute x,
+RMSNorm, shard-streamed Q|K|V GEMM, zigzag causal flash attention, W_O split-K
+GEMM + residual, RMSNorm, W_1|W_3 SwiGLU GEMM, W_2 ring-order split-K GEMM +
+residual, un-permute y.  The step's working set (x 128 MiB, weights 405 MiB,
+activations > 1 GiB) is larger than L2, so no explicit flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload fwd16k|fwd128k|fwdbwd32k|mlp16k]
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own replica
+("replicas only": the block has no data-path exchange on one node's GPUs in
+this form); value = all ranks' tokens / max-over-ranks time.
+The reference arm is the CPU float64 oracle, timed on this host's cores on a
+bounded prefix of the same workload and scaled to the full workload by the
+algorithmic flop ratio.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # name: (S, D, d, H, inter, kind)
+    "fwd16k": (16384, 8, 4096, 32, 11008, "fwd"),
+    "fwd128k": (131072, 8, 4096, 32, 11008, "fwd"),
+    "fwdbwd32k": (32768, 8, 4096, 32, 11008, "fwdbwd"),
+    "mlp16k": (16384, 4, 4096, 32, 11008, "mlp"),
+}
+DEFAULT_WORKLOAD = "fwd16k"
+
+
+def block_flops(S, d, inter, kind):
+    """Algorithmic flops: 8Sd^2 (Q,K,V,O) + 6SdI (SwiGLU) + 2S(S+1)d (causal pairs)."""
+    if kind == "mlp":
+        return 6.0 * S * d * inter
+    f = 8.0 * S * d * d + 6.0 * S * d * inter + 2.0 * S * (S + 1) * d
+    return 3.0 * f if kind == "fwdbwd" else f
+
+
+def gemm_flops(name, S, d, inter):
+    table = {
+        "gemm_qkv": 2.0 * S * d * 3 * d,
+        "gemm_oproj": 2.0 * S * d * d,
+        "gemm_w13_swiglu": 4.0 * S * d * inter,
+        "gemm_w2": 2.0 * S * d * inter,
+        "attn_fwd": 2.0 * S * (S + 1) * d,
+    }
+    return table.get(name)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return j, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.idx = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+
+_SAMPLE_CACHE = {}
+
+
+def oracle_sample(S_full, d, H, inter, D, kind, budget_rows):
+    """Time the float64 oracle on a causal prefix of the workload.
+
+    The first `rows` tokens of a causal block only depend on each other, so
+    the oracle's block forward on that prefix is a self-contained slice of the
+    same workload; its time is scaled to the full workload by the algorithmic
+    flop ratio.  Returns (seconds_for_full_workload_estimate, description).
+    """
+    import numpy as np  # noqa: F401
+    import torch
+    import oracle.tsp_oracle as O
+    from folded_tensor_sequence_zigzag_gb300.inputs import BlockShape, make_block_inputs
+    rows = budget_rows
+    key = (rows, d, H, inter, kind)
+    if key not in _SAMPLE_CACHE:
+        shape = BlockShape(S=rows, d=d, H=H, inter=inter, D=1)
+        _SAMPLE_CACHE.clear()
+        _SAMPLE_CACHE[key] = make_block_inputs(shape, torch.bfloat16, seed=0,
+                                               with_dy=(kind == "fwdbwd"), mlp_only=(kind == "mlp"))
+    inp = _SAMPLE_CACHE[key]
+    t0 = time.perf_counter()
+    if kind == "mlp":
+        O.mlp_fwd(inp["x"], inp, 1e-6, norm=False, residual=False)
+    elif kind == "fwd":
+        O.block_fwd(inp["x"], inp, H, 1e-6)
+    else:
+        O.block_bwd(inp["x"], inp, inp["dy"], H, 1e-6)
+    dt = time.perf_counter() - t0
+    scale = block_flops(S_full, d, inter, kind) / block_flops(rows, d, inter, kind)
+    desc = (f"oracle (numpy float64) on the first {rows} tokens of the workload "
+            f"({kind}), scaled by algorithmic flops x{scale:.1f}")
+    return dt * scale, dt, desc
+
+
+def cpu_cores():
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        if rank != 0:
+            dist.barrier()
+            dist.destroy_process_group()
+            return
+    S, D, d, H, inter, kind = WORKLOADS[args.workload]
+    rows = args.ref_rows or (256 if kind == "fwdbwd" else 512)
+    for _ in range(args.warmup):
+        oracle_sample(S, d, H, inter, D, kind, rows)
+    times = []
+    desc = ""
+    for _ in range(args.steps):
+        est, _, desc = oracle_sample(S, d, H, inter, D, kind, rows)
+        times.append(est)
+    t = statistics.median(times)
+    value = S / t
+    line = {
+        "impl": "reference", "metric": "TSP-block tokens/s", "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args.workload),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def workload_config(name):
+    S, D, d, H, inter, kind = WORKLOADS[name]
+    desc = {"fwd": "7B-shaped TSP block forward", "fwdbwd": "7B-shaped TSP block forward+backward",
+            "mlp": "sharded SwiGLU MLP only (no norm, no residual)"}[kind]
+    return {"workload": f"{desc}, S={S}, D={D} zigzag virtual ranks, d_model={d}, "
+                        f"{H} heads x {d // H}, SwiGLU inter={inter}, causal",
+            "S": S, "D": D, "d_model": d, "heads": H, "inter": inter, "global_batch": 1,
+            "seq_len": S, "parallelism": "replicas (one TSP-emulated block per GPU)",
+            "l2": "working set larger than L2 (no flush needed)"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    from folded_tensor_sequence_zigzag_gb300 import build, tsp
+    from folded_tensor_sequence_zigzag_gb300.inputs import BlockShape, make_block_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    tsp.load()
+
+    S, D, d, H, inter, kind = WORKLOADS[args.workload]
+    shape = BlockShape(S=S, d=d, H=H, inter=inter, D=D)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=rank, with_dy=(kind == "fwdbwd"),
+                            mlp_only=(kind == "mlp"))
+    cfg = tsp.make_cfg(S, d, H, inter, D, torch.bfloat16)
+    if kind == "mlp":
+        inp.update({k: torch.zeros(1, dtype=torch.bfloat16) for k in ("wq", "wk", "wv", "wo")})
+    W = tsp.BlockWeights.from_dict(inp, dev)
+    x = inp["x"].to(dev)
+    xz = torch.empty_like(x)
+    yz = torch.empty_like(x)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+    saved = ws = wsb = dy = dyz = None
+    if kind == "fwd":
+        ws = torch.empty(tsp.workspace_bytes(cfg, tsp.TSP_OP_BLOCK_FWD), dtype=torch.uint8, device=dev)
+    elif kind == "mlp":
+        ws = torch.empty(tsp.workspace_bytes(cfg, tsp.TSP_OP_MLP_FWD), dtype=torch.uint8, device=dev)
+    else:
+        saved = torch.empty(tsp.saved_bytes(cfg), dtype=torch.uint8, device=dev)
+        wsb = torch.empty(tsp.workspace_bytes(cfg, tsp.TSP_OP_BLOCK_BWD), dtype=torch.uint8, device=dev)
+        dy = inp["dy"].to(dev)
+        dyz = torch.empty_like(dy)
+
+    def step(xin):
+        tsp.zigzag_permute(xin, D, out=xz)
+        if kind == "fwd":
+            tsp.block_fwd(cfg, xz, W, out=yz, ws=ws)
+            tsp.zigzag_permute(yz, D, inverse=True, out=y)
+            return y
+        if kind == "mlp":
+            tsp.gated_mlp_fwd(cfg, xz, W, norm=False, residual=False, out=yz, ws=ws)
+            tsp.zigzag_permute(yz, D, inverse=True, out=y)
+            return y
+        tsp.block_fwd(cfg, xz, W, saved=saved, out=yz)
+        tsp.zigzag_permute(dy, D, out=dyz)
+        g = tsp.block_bwd(cfg, xz, dyz, saved, W, ws=wsb)
+        tsp.zigzag_permute(g["dx"], D, inverse=True, out=y)
+        return y
+
+    # ---- warm-up
+    for _ in range(max(args.warmup, 0)):
+        step(x)
+    torch.cuda.synchronize(dev)
+    if tsp.device_status() != tsp.TSP_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    # ---- device-timed region: inputs resident in HBM; per-kernel CUDA events
+    # are recorded on the launch stream inside the same region
+    n0 = tsp.launch_count()
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    clocks.start()
+    tsp.profile_enable(True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(x)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    launches = tsp.launch_count() - n0
+    prof = tsp.profile_report()
+    tsp.profile_enable(False)
+    t_dev = ev0.elapsed_time(ev1) / 1e3 / args.steps
+    t_dev = reduce_max(t_dev, world, dev if world > 1 else None)
+
+    # ---- end to end through the public API with host buffers
+    x_host = inp["x"].pin_memory()
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    x_dev = torch.empty_like(x)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        out = step(x_dev)
+        y_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_e2e = e0.elapsed_time(e1) / 1e3 / args.steps
+    t_e2e = reduce_max(t_e2e, world, dev if world > 1 else None)
+    if tsp.device_status() != tsp.TSP_OK:
+        raise RuntimeError("device status not OK after the timed region")
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = measured_peaks()
+    kernel_rows = []
+    for name, (k, ms) in prof.items():
+        kernel_rows.append((ms, name, k))
+    kernel_rows.sort(reverse=True)
+    top_name = kernel_rows[0][1] if kernel_rows else None
+    roof = None
+    per_kernel = {}
+    for ms, name, k in kernel_rows:
+        per_launch_ms = ms / max(k, 1)
+        f = gemm_flops(name, S, d, inter)
+        entry = {"launches": k, "ms_per_launch": per_launch_ms}
+        if f is not None and kind != "mlp":
+            entry["tflops"] = f / (per_launch_ms / 1e3) / 1e12
+        elif name.startswith("gemm_w13") and kind == "mlp":
+            entry["tflops"] = 4.0 * S * d * inter / (per_launch_ms / 1e3) / 1e12
+        elif name.startswith("gemm_w2") and kind == "mlp":
+            entry["tflops"] = 2.0 * S * d * inter / (per_launch_ms / 1e3) / 1e12
+        per_kernel[name] = entry
+    # the dominant tensor-core kernel of the step
+    dom = None
+    for ms, name, k in kernel_rows:
+        if "tflops" in per_kernel[name]:
+            dom = name
+            break
+    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    if dom is not None:
+        ach = per_kernel[dom]["tflops"]
+        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)",
+                "traffic": None}
+    flops = block_flops(S, d, inter, kind)
+    value = world * S / t_dev
+    tflops = world * flops / t_dev / 1e12
+    line = {
+        "metric": "TSP-block tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_dev * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (x~N(0,1), weights~N(0,0.02), gains 1)",
+        "config": workload_config(args.workload),
+        "tflops": tflops, "tflops_per_gpu": tflops / world,
+        "frac_of_peak": (tflops / world) / peaks.get("bf16_tflops", peak),
+        "peak_tflops": peaks.get("bf16_tflops"), "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)",
+        "e2e": {"value": world * S / t_e2e, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x.numel() * x.element_size()),
+                "d2h_bytes_per_step": int(y.numel() * y.element_size())},
+        "gpu_launches": int(launches),
+        "launches_per_step": launches / args.steps,
+        "kernels": per_kernel,
+        "roofline": roof,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        S_, D_, d_, H_, I_, kind_ = WORKLOADS[args.workload]
+        rows = args.ref_rows or (512 if kind_ == "fwdbwd" else 2048)
+        est, dt, desc = oracle_sample(S_, d_, H_, I_, D_, kind_, rows)
+        line["cpu_baseline"] = {"value": S_ / est, "unit": "tokens/s", "cores": cpu_cores(),
+                                "kind": "oracle", "sample": desc, "sample_seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--ref-rows", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,731 @@
+// api.cu -- the C ABI (include/tsp.h): argument checks, workspace layout and
+// the launch sequence of the TSP-folded block on one stream.
+//
+// Source: "Folding Tensor and Sequence Parallelism for Memory-Efficient
+// Transformer Training & Inference" (gist.science summary), section 2.
+// The D ranks are virtual: rank r's tokens are rows [r*2c, (r+1)*2c) of the
+// zigzag buffer, a weight shard is a column range of the unsharded weight,
+// and every collective of the real schedule becomes a layout fact:
+//   broadcast of shard k  -> the GEMM's N (or K) range is segmented by shard;
+//   K/V all-gather        -> all ranks' K/V already sit in one buffer;
+//   MLP ring              -> the W_2 GEMM's K loop runs in ring order per rank;
+//   weight-grad reduction -> the wgrad GEMMs' K loop (tokens) runs over every
+//                            rank's rows into one fp32 accumulator.
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "gemm_tc.h"
+#include "kernels.h"
+
+namespace tsp {
+
+__device__ int g_status_word = 0;
+
+int* status_word() {
+  static int* ptr[16] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) ptr[dev] = (int*)p;
+  }
+  return ptr[dev];
+}
+
+int num_sms() {
+  static int n[16] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
+  if (n[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) v = 0;
+    n[dev] = v > 0 ? v : 1;
+  }
+  return n[dev];
+}
+
+uint64_t wait_limit_ns() {
+  static uint64_t v = [] {
+    const char* e = getenv("TSP_WAIT_LIMIT_MS");  // debug knob; default 4 s per wait
+    uint64_t ms = 4000;
+    if (e && atoll(e) > 0) ms = (uint64_t)atoll(e);
+    return ms * 1000000ull;
+  }();
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Launch accounting: every kernel launch site is wrapped in a Prof scope that
+// counts its kernels and, while profiling is on, brackets them with CUDA
+// events recorded on the launch stream.
+// ---------------------------------------------------------------------------
+namespace {
+std::atomic<long long> g_launches{0};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+struct ProfRec {
+  const char* name;
+  int kernels;
+  cudaEvent_t a, b;
+};
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pool_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+}  // namespace
+
+Prof::Prof(const char* name, cudaStream_t st, int kernels) : name_(name), kernels_(kernels), st_(st) {
+  g_launches.fetch_add(kernels);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on) return;
+  on_ = true;
+  a_ = pool_event();
+  b_ = pool_event();
+  cudaEventRecord(a_, st_);
+}
+
+Prof::~Prof() {
+  if (!on_) return;
+  cudaEventRecord(b_, st_);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof.push_back(ProfRec{name_, kernels_, a_, b_});
+}
+
+namespace {
+
+bool al16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+tsp_status check_cfg(const tsp_cfg* c) {
+  if (!c) return TSP_ERR_INVALID_ARG;
+  if (c->S <= 0 || c->D < 1 || c->D > 64 || c->S % (2 * (int64_t)c->D) != 0)
+    return TSP_ERR_INVALID_ARG;
+  if (c->d <= 0 || c->H <= 0 || c->d % c->H != 0 || c->dh != c->d / c->H) return TSP_ERR_INVALID_ARG;
+  if (c->inter <= 0 || c->d < c->D || c->inter < c->D) return TSP_ERR_INVALID_ARG;
+  if (c->dtype != TSP_F32 && c->dtype != TSP_BF16) return TSP_ERR_INVALID_ARG;
+  if (!(c->eps >= 0.f)) return TSP_ERR_INVALID_ARG;
+  if (c->S > (int64_t)1 << 31) return TSP_ERR_UNSUPPORTED;
+  if (c->dtype == TSP_F32 && c->dh > 128) return TSP_ERR_UNSUPPORTED;
+  return TSP_OK;
+}
+
+tsp_status check_bf16_mlp(const tsp_cfg* c) {
+  if (c->dtype != TSP_BF16) return TSP_OK;
+  if (c->d % 256 != 0 || c->inter % 128 != 0) return TSP_ERR_UNSUPPORTED;
+  return TSP_OK;
+}
+tsp_status check_bf16_attn(const tsp_cfg* c) {
+  if (c->dtype != TSP_BF16) return TSP_OK;
+  if (c->d % 256 != 0 || c->dh != 128 || (c->S / (2 * c->D)) % 128 != 0) return TSP_ERR_UNSUPPORTED;
+  return TSP_OK;
+}
+
+// Activation buffers of the forward pass (the "saved" set of the backward).
+struct Acts {
+  float *rstd1, *rstd2, *lse;
+  void *a, *qkv, *o, *h, *b, *ab, *g;
+  size_t bytes;
+};
+
+enum { PART_ATTN = 1, PART_MLP = 2, PART_AB = 4 };
+
+Acts acts_layout(const tsp_cfg* c, int parts, uint8_t* base) {
+  const size_t e = c->dtype == TSP_BF16 ? 2 : 4;
+  const size_t S = (size_t)c->S, d = (size_t)c->d, I = (size_t)c->inter, H = (size_t)c->H;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void* {
+    void* p = base ? base + off : nullptr;
+    off += up256(bytes);
+    return p;
+  };
+  Acts A;
+  memset(&A, 0, sizeof(A));
+  if (parts & PART_ATTN) {
+    A.rstd1 = (float*)take(S * 4);
+    A.lse = (float*)take(H * S * 4);
+    A.a = take(S * d * e);
+    A.qkv = take(S * 3 * d * e);
+    A.o = take(S * d * e);
+  }
+  if (parts & PART_MLP) {
+    A.rstd2 = (float*)take(S * 4);
+    A.h = (parts & PART_ATTN) ? take(S * d * 4) : nullptr;  // fp32 residual stream
+    A.b = take(S * d * e);
+    A.g = take(S * I * e);
+    if (parts & PART_AB) A.ab = take(S * 2 * I * e);
+  }
+  A.bytes = off;
+  return A;
+}
+
+int fwd_parts(const tsp_cfg* c, bool training) {
+  // the fp32 path builds G from A|B, so it always keeps them
+  return PART_ATTN | PART_MLP | ((training || c->dtype == TSP_F32) ? PART_AB : 0);
+}
+
+struct BwdWs {
+  void *dab, *dg_f32, *db, *dh_f32, *dh_t, *dO, *dqkv, *da;
+  float *delta, *dq_acc, *dg_part;
+  size_t bytes;
+};
+
+BwdWs bwd_layout(const tsp_cfg* c, uint8_t* base) {
+  const size_t e = c->dtype == TSP_BF16 ? 2 : 4;
+  const size_t S = (size_t)c->S, d = (size_t)c->d, I = (size_t)c->inter, H = (size_t)c->H;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void* {
+    void* p = base ? base + off : nullptr;
+    off += up256(bytes);
+    return p;
+  };
+  BwdWs W;
+  memset(&W, 0, sizeof(W));
+  W.dab = take(S * 2 * I * e);
+  if (c->dtype == TSP_F32) W.dg_f32 = take(S * I * 4);
+  W.db = take(S * d * 4);
+  W.dh_f32 = take(S * d * 4);
+  if (c->dtype == TSP_BF16) W.dh_t = take(S * d * e);
+  W.dO = take(S * d * e);
+  W.dqkv = take(S * 3 * d * e);
+  W.da = take(S * d * 4);
+  W.delta = (float*)take(H * S * 4);
+  if (c->dtype == TSP_BF16) W.dq_acc = (float*)take(S * d * 4);
+  W.dg_part = (float*)take((size_t)rmsnorm_bwd_blocks(c->S) * d * 4);
+  W.bytes = off;
+  return W;
+}
+
+cudaStream_t S_(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// ----------------------------------------------------------------------------
+// Forward halves
+// ----------------------------------------------------------------------------
+
+// h_f32: write h in fp32 (the block's residual stream) instead of the cfg dtype.
+tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, void* h, bool h_f32,
+                     const Acts& A, cudaStream_t st) {
+  const int64_t S = c->S;
+  const int d = c->d, D = c->D;
+  tsp_status r = launch_rmsnorm_fwd(x, 0, w->g_attn, A.a, A.rstd1, S, d, c->eps, c->dtype, st);
+  if (r != TSP_OK) return r;
+  if (c->dtype == TSP_BF16) {
+    // Q|K|V: the N range is split into the W_Q, W_K, W_V segments; within a
+    // segment the N tiles are the column shards C_k streamed one after another.
+    TcGemm g;
+    g.M = (int)S; g.N = 3 * d; g.K = d;
+    g.A[0] = A.a; g.lda[0] = d; g.kseg_len[0] = d;
+    g.B[0] = w->wq; g.B[1] = w->wk; g.B[2] = w->wv;
+    g.ldb[0] = g.ldb[1] = g.ldb[2] = d;
+    g.nseg_n = d; g.name = "gemm_qkv";
+    g.epi = EPI_BF16; g.out = A.qkv; g.ldo = 3 * d;
+    if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    if ((r = launch_attn_fwd_bf16(A.qkv, A.o, A.lse, S, c->H, c->dh, D, st)) != TSP_OK) return r;
+    // W_O: split-K over the shards C_k (k = 0..D-1, broadcast order), fp32
+    // accumulation in TMEM, residual x added in the epilogue.
+    TcGemm o;
+    o.M = (int)S; o.N = d; o.K = d;
+    o.A[0] = A.o; o.lda[0] = d; o.kseg_len[0] = d;
+    o.B[0] = w->wo; o.ldb[0] = d;
+    o.epi = EPI_RES; o.res = x; o.name = "gemm_oproj"; o.ldr = d; o.out = h; o.ldo = d; o.out_f32 = h_f32;
+    return gemm_tc(o, st);
+  }
+  // exact fp32 path: literal shard loop
+  const float* a = (const float*)A.a;
+  float* qkv = (float*)A.qkv;
+  const float* W3[3] = {(const float*)w->wq, (const float*)w->wk, (const float*)w->wv};
+  for (int k = 0; k < D; ++k) {
+    const int lo = (int)((int64_t)k * d / D), hi = (int)((int64_t)(k + 1) * d / D);
+    for (int j = 0; j < 3; ++j) {
+      r = launch_gemm_f32((int)S, hi - lo, d, a, d, 1, W3[j] + (int64_t)lo * d, d, 1,
+                          qkv + j * d + lo, 3 * d, nullptr, 0, 0, st);
+      if (r != TSP_OK) return r;
+    }
+  }
+  if ((r = launch_attn_f32_fwd(qkv, S, c->H, c->dh, D, (float*)A.o, A.lse, st)) != TSP_OK) return r;
+  for (int k = 0; k < D; ++k) {
+    const int lo = (int)((int64_t)k * d / D), hi = (int)((int64_t)(k + 1) * d / D);
+    r = launch_gemm_f32((int)S, d, hi - lo, (const float*)A.o + lo, d, 1, (const float*)w->wo + lo,
+                        d, 1, (float*)h, d, k == 0 ? (const float*)x : nullptr, d, k > 0, st);
+    if (r != TSP_OK) return r;
+  }
+  return TSP_OK;
+}
+
+// hin_f32: the input h is fp32 (the block's residual stream), else the cfg dtype.
+tsp_status mlp_half(const tsp_cfg* c, const void* hin, bool hin_f32, const tsp_mlp_w* w, void* y,
+                    const Acts& A, cudaStream_t st) {
+  const int64_t S = c->S;
+  const int d = c->d, I = c->inter, D = c->D;
+  const int64_t rows_per_rank = S / D;
+  tsp_status r;
+  const void* b = hin;
+  if (w->g_mlp) {
+    if ((r = launch_rmsnorm_fwd(hin, hin_f32 ? 1 : 0, w->g_mlp, A.b, A.rstd2, S, d, c->eps,
+                                c->dtype, st)) != TSP_OK)
+      return r;
+    b = A.b;
+  }
+  if (c->dtype == TSP_BF16) {
+    // W_1|W_3: one 256-wide B tile = 128 rows of W_1 and the same 128 rows of
+    // W_3 (split-N over the I_k shards); SiLU(.)*gate fused in the epilogue.
+    TcGemm g;
+    g.M = (int)S; g.N = I; g.K = d;
+    g.A[0] = b; g.lda[0] = d; g.kseg_len[0] = d;
+    g.B[0] = w->w1; g.B[1] = w->w3; g.ldb[0] = g.ldb[1] = d;
+    g.paired = true; g.name = "gemm_w13_swiglu";
+    g.epi = EPI_SWIGLU; g.out = A.g; g.ldo = I;
+    if (A.ab) {
+      g.out2 = A.ab; g.ldo2 = 2 * (int64_t)I;
+      g.out3 = (uint8_t*)A.ab + (size_t)I * 2; g.ldo3 = 2 * (int64_t)I;
+    }
+    if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    // W_2: K = I walked shard by shard in ring order (r - t) mod D for the
+    // virtual rank r owning the row tile; residual fused.
+    TcGemm o;
+    o.M = (int)S; o.N = d; o.K = I;
+    o.A[0] = A.g; o.lda[0] = I; o.kseg_len[0] = I;
+    o.B[0] = w->w2; o.ldb[0] = I;
+    o.rot_rows = (int)rows_per_rank; o.rot_D = D; o.name = "gemm_w2";
+    o.out = y; o.ldo = d;
+    if (w->add_residual) {
+      o.epi = EPI_RES; o.res = hin; o.ldr = d; o.res_f32 = hin_f32;
+    } else {
+      o.epi = EPI_BF16;
+    }
+    return gemm_tc(o, st);
+  }
+  const float* bf = (const float*)b;
+  float* ab = (float*)A.ab;
+  for (int k = 0; k < D; ++k) {
+    const int lo = (int)((int64_t)k * I / D), hi = (int)((int64_t)(k + 1) * I / D);
+    if ((r = launch_gemm_f32((int)S, hi - lo, d, bf, d, 1, (const float*)w->w1 + (int64_t)lo * d, d,
+                             1, ab + lo, 2 * I, nullptr, 0, 0, st)) != TSP_OK)
+      return r;
+    if ((r = launch_gemm_f32((int)S, hi - lo, d, bf, d, 1, (const float*)w->w3 + (int64_t)lo * d, d,
+                             1, ab + I + lo, 2 * I, nullptr, 0, 0, st)) != TSP_OK)
+      return r;
+  }
+  if ((r = launch_swiglu_f32(ab, (float*)A.g, S, I, st)) != TSP_OK) return r;
+  // ring: virtual rank rr takes shard (rr - t) mod D at step t
+  for (int rr = 0; rr < D; ++rr) {
+    const int64_t r0 = rr * rows_per_rank;
+    for (int t = 0; t < D; ++t) {
+      const int k = ((rr - t) % D + D) % D;
+      const int lo = (int)((int64_t)k * I / D), hi = (int)((int64_t)(k + 1) * I / D);
+      const float* res = (t == 0 && w->add_residual) ? (const float*)hin + r0 * d : nullptr;
+      r = launch_gemm_f32((int)rows_per_rank, d, hi - lo, (const float*)A.g + r0 * I + lo, I, 1,
+                          (const float*)w->w2 + lo, I, 1, (float*)y + r0 * d, d, res, d, t > 0, st);
+      if (r != TSP_OK) return r;
+    }
+  }
+  return TSP_OK;
+}
+
+tsp_status check_attn_w(const tsp_attn_w* w) {
+  if (!w || !al16(w->wq) || !al16(w->wk) || !al16(w->wv) || !al16(w->wo) || !al16(w->g_attn))
+    return TSP_ERR_INVALID_ARG;
+  return TSP_OK;
+}
+tsp_status check_mlp_w(const tsp_mlp_w* w, bool need_norm) {
+  if (!w || !al16(w->w1) || !al16(w->w3) || !al16(w->w2)) return TSP_ERR_INVALID_ARG;
+  if (w->g_mlp && !al16(w->g_mlp)) return TSP_ERR_INVALID_ARG;
+  if (need_norm && (!w->g_mlp || !w->add_residual)) return TSP_ERR_INVALID_ARG;
+  return TSP_OK;
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------------
+// Backward (defined below the C entry points' helpers)
+// ----------------------------------------------------------------------------
+tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const void* saved,
+                          const tsp_attn_w* aw, const tsp_mlp_w* mw, void* dx, float* dwq,
+                          float* dwk, float* dwv, float* dwo, float* dw1, float* dw3, float* dw2,
+                          float* dg_attn, float* dg_mlp, void* ws, cudaStream_t st);
+
+}  // namespace tsp
+
+using namespace tsp;
+
+extern "C" {
+
+const char* tsp_strerror(tsp_status s) {
+  switch (s) {
+    case TSP_OK: return "ok";
+    case TSP_ERR_INVALID_ARG: return "invalid argument";
+    case TSP_ERR_UNSUPPORTED: return "shape not supported by the selected kernels";
+    case TSP_ERR_CUDA: return "CUDA runtime error";
+    case TSP_ERR_TIMEOUT: return "device pipeline wait exceeded its time limit";
+  }
+  return "unknown status";
+}
+
+int32_t tsp_num_sms(void) {
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) return 0;
+  return num_sms();
+}
+
+tsp_status tsp_zigzag_permute(const void* src, void* dst, int64_t S, int32_t D, int64_t row_bytes,
+                              int32_t inverse, void* stream) {
+  if (!src || !dst || S <= 0 || D < 1 || D > 64 || S % (2 * (int64_t)D) != 0 || row_bytes <= 0)
+    return TSP_ERR_INVALID_ARG;
+  return launch_zigzag_permute(src, dst, S, D, row_bytes, inverse, S_(stream));
+}
+
+tsp_status tsp_rmsnorm_fwd(const void* u, const void* g, void* out, float* rstd, int64_t rows,
+                           int32_t n, float eps, int32_t dtype, void* stream) {
+  if (!u || !g || !out || rows <= 0 || n <= 0 || (dtype != TSP_F32 && dtype != TSP_BF16) ||
+      !(eps >= 0.f))
+    return TSP_ERR_INVALID_ARG;
+  return launch_rmsnorm_fwd(u, 0, g, out, rstd, rows, n, eps, dtype, S_(stream));
+}
+
+size_t tsp_workspace_bytes(const tsp_cfg* cfg, int32_t op) {
+  if (check_cfg(cfg) != TSP_OK) return 0;
+  switch (op) {
+    case TSP_OP_ATTN_FWD: return acts_layout(cfg, PART_ATTN, nullptr).bytes;
+    case TSP_OP_MLP_FWD:
+      return acts_layout(cfg, PART_MLP | (cfg->dtype == TSP_F32 ? PART_AB : 0), nullptr).bytes;
+    case TSP_OP_BLOCK_FWD: return acts_layout(cfg, fwd_parts(cfg, false), nullptr).bytes;
+    case TSP_OP_BLOCK_BWD: return bwd_layout(cfg, nullptr).bytes;
+  }
+  return 0;
+}
+
+size_t tsp_saved_bytes(const tsp_cfg* cfg) {
+  if (check_cfg(cfg) != TSP_OK) return 0;
+  return acts_layout(cfg, fwd_parts(cfg, true), nullptr).bytes;
+}
+
+tsp_status tsp_attn_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* w, void* h_z,
+                              void* ws, size_t ws_bytes, void* stream) {
+  tsp_status r = check_cfg(cfg);
+  if (r != TSP_OK) return r;
+  if ((r = check_attn_w(w)) != TSP_OK) return r;
+  if (!al16(x_z) || !al16(h_z)) return TSP_ERR_INVALID_ARG;
+  if ((r = check_bf16_attn(cfg)) != TSP_OK) return r;
+  const Acts A0 = acts_layout(cfg, PART_ATTN, nullptr);
+  if (!al16(ws) || ws_bytes < A0.bytes) return TSP_ERR_INVALID_ARG;
+  const Acts A = acts_layout(cfg, PART_ATTN, (uint8_t*)ws);
+  return attn_half(cfg, x_z, w, h_z, false, A, S_(stream));
+}
+
+tsp_status tsp_gated_mlp_fwd(const tsp_cfg* cfg, const void* h_z, const tsp_mlp_w* w, void* y_z,
+                             void* ws, size_t ws_bytes, void* stream) {
+  tsp_status r = check_cfg(cfg);
+  if (r != TSP_OK) return r;
+  if ((r = check_mlp_w(w, false)) != TSP_OK) return r;
+  if (!al16(h_z) || !al16(y_z)) return TSP_ERR_INVALID_ARG;
+  if ((r = check_bf16_mlp(cfg)) != TSP_OK) return r;
+  const int parts = PART_MLP | (cfg->dtype == TSP_F32 ? PART_AB : 0);
+  const Acts A0 = acts_layout(cfg, parts, nullptr);
+  if (!al16(ws) || ws_bytes < A0.bytes) return TSP_ERR_INVALID_ARG;
+  const Acts A = acts_layout(cfg, parts, (uint8_t*)ws);
+  return mlp_half(cfg, h_z, false, w, y_z, A, S_(stream));
+}
+
+tsp_status tsp_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* aw,
+                         const tsp_mlp_w* mw, void* y_z, void* saved, void* ws, size_t ws_bytes,
+                         void* stream) {
+  tsp_status r = check_cfg(cfg);
+  if (r != TSP_OK) return r;
+  if ((r = check_attn_w(aw)) != TSP_OK) return r;
+  if ((r = check_mlp_w(mw, true)) != TSP_OK) return r;
+  if (!al16(x_z) || !al16(y_z)) return TSP_ERR_INVALID_ARG;
+  if ((r = check_bf16_attn(cfg)) != TSP_OK) return r;
+  if ((r = check_bf16_mlp(cfg)) != TSP_OK) return r;
+  const bool training = saved != nullptr;
+  const int parts = fwd_parts(cfg, training);
+  uint8_t* base;
+  if (training) {
+    if (!al16(saved)) return TSP_ERR_INVALID_ARG;
+    base = (uint8_t*)saved;
+  } else {
+    if (!al16(ws) || ws_bytes < acts_layout(cfg, parts, nullptr).bytes) return TSP_ERR_INVALID_ARG;
+    base = (uint8_t*)ws;
+  }
+  const Acts A = acts_layout(cfg, parts, base);
+  cudaStream_t st = S_(stream);
+  if ((r = attn_half(cfg, x_z, aw, A.h, true, A, st)) != TSP_OK) return r;
+  return mlp_half(cfg, A.h, true, mw, y_z, A, st);
+}
+
+tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z, const void* saved,
+                         const tsp_attn_w* aw, const tsp_mlp_w* mw, void* dx_z, float* dwq,
+                         float* dwk, float* dwv, float* dwo, float* dw1, float* dw3, float* dw2,
+                         float* dg_attn, float* dg_mlp, void* ws, size_t ws_bytes, void* stream) {
+  tsp_status r = check_cfg(cfg);
+  if (r != TSP_OK) return r;
+  if ((r = check_attn_w(aw)) != TSP_OK) return r;
+  if ((r = check_mlp_w(mw, true)) != TSP_OK) return r;
+  if (!al16(x_z) || !al16(dy_z) || !al16(saved) || !al16(dx_z)) return TSP_ERR_INVALID_ARG;
+  const float* gp[9] = {dwq, dwk, dwv, dwo, dw1, dw3, dw2, dg_attn, dg_mlp};
+  for (const float* p : gp)
+    if (!al16(p)) return TSP_ERR_INVALID_ARG;
+  if ((r = check_bf16_attn(cfg)) != TSP_OK) return r;
+  if ((r = check_bf16_mlp(cfg)) != TSP_OK) return r;
+  if (!al16(ws) || ws_bytes < bwd_layout(cfg, nullptr).bytes) return TSP_ERR_INVALID_ARG;
+  return block_bwd_impl(cfg, x_z, dy_z, saved, aw, mw, dx_z, dwq, dwk, dwv, dwo, dw1, dw3, dw2,
+                        dg_attn, dg_mlp, ws, S_(stream));
+}
+
+tsp_status tsp_pack_attn_shards(const tsp_cfg* cfg, const tsp_attn_w* w, void* dst, void* stream) {
+  tsp_status r = check_cfg(cfg);
+  if (r != TSP_OK) return r;
+  if (!w || !w->wq || !w->wk || !w->wv || !w->wo || !dst) return TSP_ERR_INVALID_ARG;
+  return launch_pack_attn_shards(w->wq, w->wk, w->wv, w->wo, dst, cfg->d, cfg->D, cfg->dtype,
+                                 S_(stream));
+}
+
+void tsp_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& r : g_prof) {
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_prof.clear();
+  g_prof_on = on != 0;
+}
+
+int32_t tsp_profile_report(char* buf, int64_t bytes) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  std::map<std::string, std::pair<long long, double>> agg;
+  for (auto& r : g_prof) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return -1;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return -1;
+    auto& e = agg[r.name];
+    e.first += r.kernels;
+    e.second += ms;
+  }
+  std::string out;
+  for (auto& kv : agg) {
+    char line[256];
+    snprintf(line, sizeof(line), "%s\t%lld\t%.6f\n", kv.first.c_str(), kv.second.first,
+             kv.second.second);
+    out += line;
+  }
+  if (!buf || bytes <= (int64_t)out.size()) return -1;
+  memcpy(buf, out.c_str(), out.size() + 1);
+  return (int32_t)agg.size();
+}
+
+int64_t tsp_launch_count(void) { return g_launches.load(); }
+
+tsp_status tsp_device_status(void* stream, int32_t reset) {
+  int* p = status_word();
+  if (!p) return TSP_ERR_CUDA;
+  int v = 0;
+  if (cudaStreamSynchronize(S_(stream)) != cudaSuccess) return TSP_ERR_CUDA;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TSP_ERR_CUDA;
+  if (reset) {
+    const int z = 0;
+    if (cudaMemcpy(p, &z, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return TSP_ERR_CUDA;
+  }
+  return (tsp_status)v;
+}
+
+}  // extern "C"
+
+// ----------------------------------------------------------------------------
+// Backward of the block
+// ----------------------------------------------------------------------------
+namespace tsp {
+
+tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const void* saved,
+                          const tsp_attn_w* aw, const tsp_mlp_w* mw, void* dx, float* dwq,
+                          float* dwk, float* dwv, float* dwo, float* dw1, float* dw3, float* dw2,
+                          float* dg_attn, float* dg_mlp, void* ws, cudaStream_t st) {
+  const int64_t S = c->S;
+  const int d = c->d, I = c->inter, D = c->D, H = c->H, dh = c->dh;
+  const Acts A = acts_layout(c, fwd_parts(c, true), (uint8_t*)saved);
+  const BwdWs W = bwd_layout(c, (uint8_t*)ws);
+  tsp_status r;
+  if (c->dtype == TSP_BF16) {
+    const size_t e = 2;
+    // dA|dB = SwiGLU'(dG), dG = dy W_2   (B operand W_2 read MN-major)
+    {
+      TcGemm g;
+      g.M = (int)S; g.N = I; g.K = d;
+      g.A[0] = dy; g.lda[0] = d; g.kseg_len[0] = d;
+      g.b_mn = true; g.B[0] = mw->w2; g.ldb[0] = I;
+      g.epi = EPI_SWIGLU_BWD; g.name = "gemm_dgrad_w2_swiglu";
+      g.e1 = A.ab; g.e2 = (uint8_t*)A.ab + (size_t)I * e; g.lde = 2 * (int64_t)I;
+      g.out = W.dab; g.ldo = 2 * (int64_t)I;
+      g.out2 = (uint8_t*)W.dab + (size_t)I * e; g.ldo2 = 2 * (int64_t)I;
+      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    }
+    // dW_2 = dy^T G: K = tokens, i.e. every virtual rank's rows summed in fp32
+    {
+      TcGemm g;
+      g.M = d; g.N = I; g.K = (int)S;
+      g.a_mn = true; g.A[0] = dy; g.lda[0] = d; g.kseg_len[0] = (int)S;
+      g.b_mn = true; g.B[0] = A.g; g.ldb[0] = I;
+      g.epi = EPI_F32; g.out = dw2; g.ldo = I; g.name = "gemm_wgrad_w2";
+      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    }
+    // dW_1 | dW_3 = [dA | dB]^T b (one launch, rows split between the outputs)
+    {
+      TcGemm g;
+      g.M = 2 * I; g.N = d; g.K = (int)S;
+      g.a_mn = true; g.A[0] = W.dab; g.lda[0] = 2 * (int64_t)I; g.kseg_len[0] = (int)S;
+      g.b_mn = true; g.B[0] = A.b; g.ldb[0] = d;
+      g.epi = EPI_F32; g.ldo = d; g.m_seg = I; g.name = "gemm_wgrad_w13"; g.outs[0] = dw1; g.outs[1] = dw3;
+      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    }
+    // db = dA W_1 + dB W_3 (two K segments), fp32
+    {
+      TcGemm g;
+      g.M = (int)S; g.N = d; g.K = 2 * I;
+      g.nks = 2;
+      g.A[0] = W.dab; g.A[1] = (uint8_t*)W.dab + (size_t)I * e;
+      g.lda[0] = g.lda[1] = 2 * (int64_t)I;
+      g.kseg_len[0] = g.kseg_len[1] = I;
+      g.b_mn = true; g.B[0] = mw->w1; g.B[1] = mw->w3; g.ldb[0] = g.ldb[1] = d;
+      g.epi = EPI_F32; g.out = W.db; g.ldo = d; g.name = "gemm_dgrad_w13";
+      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    }
+    // dh = dy + RMSNorm_2'(db)
+    if ((r = launch_rmsnorm_bwd((const float*)W.db, A.h, 1, mw->g_mlp, A.rstd2, nullptr, dy,
+                                (float*)W.dh_f32, W.dh_t, dg_mlp, W.dg_part, S, d, c->dtype, st)) !=
+        TSP_OK)
+      return r;
+    // dW_O = dh^T O
+    {
+      TcGemm g;
+      g.M = d; g.N = d; g.K = (int)S;
+      g.a_mn = true; g.A[0] = W.dh_t; g.lda[0] = d; g.kseg_len[0] = (int)S;
+      g.b_mn = true; g.B[0] = A.o; g.ldb[0] = d;
+      g.epi = EPI_F32; g.out = dwo; g.ldo = d; g.name = "gemm_wgrad_wo";
+      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    }
+    // dO = dh W_O
+    {
+      TcGemm g;
+      g.M = (int)S; g.N = d; g.K = d;
+      g.A[0] = W.dh_t; g.lda[0] = d; g.kseg_len[0] = d;
+      g.b_mn = true; g.B[0] = aw->wo; g.ldb[0] = d;
+      g.epi = EPI_BF16; g.out = W.dO; g.ldo = d; g.name = "gemm_dgrad_wo";
+      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    }
+    if ((r = launch_attn_bwd_bf16(A.qkv, A.o, W.dO, A.lse, W.delta, W.dq_acc, W.dqkv, S, H, dh, D,
+                                  st)) != TSP_OK)
+      return r;
+    // dW_Q | dW_K | dW_V = [dQ | dK | dV]^T a
+    {
+      TcGemm g;
+      g.M = 3 * d; g.N = d; g.K = (int)S;
+      g.a_mn = true; g.A[0] = W.dqkv; g.lda[0] = 3 * (int64_t)d; g.kseg_len[0] = (int)S;
+      g.b_mn = true; g.B[0] = A.a; g.ldb[0] = d;
+      g.epi = EPI_F32; g.ldo = d; g.m_seg = d; g.name = "gemm_wgrad_qkv"; g.outs[0] = dwq; g.outs[1] = dwk; g.outs[2] = dwv;
+      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    }
+    // da = dQ W_Q + dK W_K + dV W_V (three K segments), fp32
+    {
+      TcGemm g;
+      g.M = (int)S; g.N = d; g.K = 3 * d;
+      g.nks = 3;
+      const void* ws3[3] = {aw->wq, aw->wk, aw->wv};
+      for (int j = 0; j < 3; ++j) {
+        g.A[j] = (uint8_t*)W.dqkv + (size_t)j * d * e;
+        g.lda[j] = 3 * (int64_t)d;
+        g.kseg_len[j] = d;
+        g.B[j] = ws3[j];
+        g.ldb[j] = d;
+      }
+      g.b_mn = true;
+      g.epi = EPI_F32; g.out = W.da; g.ldo = d; g.name = "gemm_dgrad_qkv";
+      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    }
+    // dx = dh + RMSNorm_1'(da)
+    return launch_rmsnorm_bwd((const float*)W.da, x, 0, aw->g_attn, A.rstd1, (const float*)W.dh_f32,
+                              nullptr, nullptr, dx, dg_attn, W.dg_part, S, d, c->dtype, st);
+  }
+
+  // ------------------------------------------------------------ exact fp32
+  const int64_t R = S / D;  // rows per virtual rank
+  const float* dyf = (const float*)dy;
+  const float* ab = (const float*)A.ab;
+  float* dab = (float*)W.dab;
+  float* dG = (float*)W.dg_f32;
+  if ((r = launch_gemm_f32((int)S, I, d, dyf, d, 1, (const float*)mw->w2, 1, I, dG, I, nullptr, 0,
+                           0, st)) != TSP_OK)
+    return r;
+  if ((r = launch_swiglu_bwd_f32(dG, ab, dab, S, I, st)) != TSP_OK) return r;
+  for (int rr = 0; rr < D; ++rr) {  // weight grads: sum over the virtual ranks' rows
+    const int64_t r0 = rr * R;
+    if ((r = launch_gemm_f32(d, I, (int)R, dyf + r0 * d, 1, d, (const float*)A.g + r0 * I, 1, I,
+                             dw2, I, nullptr, 0, rr > 0, st)) != TSP_OK)
+      return r;
+    if ((r = launch_gemm_f32(I, d, (int)R, dab + r0 * 2 * I, 1, 2 * I, (const float*)A.b + r0 * d,
+                             1, d, dw1, d, nullptr, 0, rr > 0, st)) != TSP_OK)
+      return r;
+    if ((r = launch_gemm_f32(I, d, (int)R, dab + r0 * 2 * I + I, 1, 2 * I,
+                             (const float*)A.b + r0 * d, 1, d, dw3, d, nullptr, 0, rr > 0, st)) !=
+        TSP_OK)
+      return r;
+  }
+  float* db = (float*)W.db;
+  if ((r = launch_gemm_f32((int)S, d, I, dab, 2 * I, 1, (const float*)mw->w1, 1, d, db, d, nullptr,
+                           0, 0, st)) != TSP_OK)
+    return r;
+  if ((r = launch_gemm_f32((int)S, d, I, dab + I, 2 * I, 1, (const float*)mw->w3, 1, d, db, d,
+                           nullptr, 0, 1, st)) != TSP_OK)
+    return r;
+  float* dhf = (float*)W.dh_f32;
+  if ((r = launch_rmsnorm_bwd(db, A.h, 1, mw->g_mlp, A.rstd2, dyf, nullptr, dhf, nullptr, dg_mlp,
+                              W.dg_part, S, d, c->dtype, st)) != TSP_OK)
+    return r;
+  for (int rr = 0; rr < D; ++rr) {
+    const int64_t r0 = rr * R;
+    if ((r = launch_gemm_f32(d, d, (int)R, dhf + r0 * d, 1, d, (const float*)A.o + r0 * d, 1, d, dwo,
+                             d, nullptr, 0, rr > 0, st)) != TSP_OK)
+      return r;
+  }
+  float* dO = (float*)W.dO;
+  if ((r = launch_gemm_f32((int)S, d, d, dhf, d, 1, (const float*)aw->wo, 1, d, dO, d, nullptr, 0, 0,
+                           st)) != TSP_OK)
+    return r;
+  float* dqkv = (float*)W.dqkv;
+  if ((r = launch_attn_f32_bwd((const float*)A.qkv, (const float*)A.o, dO, A.lse, W.delta, dqkv, S,
+                               H, dh, D, st)) != TSP_OK)
+    return r;
+  float* dws[3] = {dwq, dwk, dwv};
+  const float* wts[3] = {(const float*)aw->wq, (const float*)aw->wk, (const float*)aw->wv};
+  for (int j = 0; j < 3; ++j) {
+    for (int rr = 0; rr < D; ++rr) {
+      const int64_t r0 = rr * R;
+      if ((r = launch_gemm_f32(d, d, (int)R, dqkv + r0 * 3 * d + j * d, 1, 3 * d,
+                               (const float*)A.a + r0 * d, 1, d, dws[j], d, nullptr, 0, rr > 0,
+                               st)) != TSP_OK)
+        return r;
+    }
+  }
+  float* da = (float*)W.da;
+  for (int j = 0; j < 3; ++j) {
+    if ((r = launch_gemm_f32((int)S, d, d, dqkv + j * d, 3 * d, 1, wts[j], 1, d, da, d, nullptr, 0,
+                             j > 0, st)) != TSP_OK)
+      return r;
+  }
+  return launch_rmsnorm_bwd(da, x, 0, aw->g_attn, A.rstd1, dhf, nullptr, (float*)dx, nullptr, dg_attn,
+                            W.dg_part, S, d, c->dtype, st);
+}
+
+}  // namespace tsp

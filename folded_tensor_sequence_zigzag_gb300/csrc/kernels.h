@@ -1,0 +1,52 @@
+// kernels.h -- launchers of the TSP block kernels (one definition per .cu).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "tsp.h"
+
+namespace tsp {
+
+// rowwise.cu
+tsp_status launch_zigzag_permute(const void* src, void* dst, int64_t S, int D, int64_t row_bytes,
+                                 int inverse, cudaStream_t st);
+// u_f32: the input is fp32 (else the storage dtype); g and out are of the storage dtype.
+tsp_status launch_rmsnorm_fwd(const void* u, int u_f32, const void* g, void* out, float* rstd,
+                              int64_t rows, int n, float eps, int dtype, cudaStream_t st);
+int rmsnorm_bwd_blocks(int64_t rows);
+// du = rstd (dout g - nrm mean(dout g nrm)), nrm = u rstd; out = resid + du, where
+// resid is resid_f32 (fp32) or resid_t (storage dtype), exactly one non-NULL;
+// dg = sum over rows of dout * nrm (dg_part: rmsnorm_bwd_blocks(rows) x n fp32 scratch).
+// u_f32: u is fp32 (else the storage dtype).
+tsp_status launch_rmsnorm_bwd(const float* dout, const void* u, int u_f32, const void* g,
+                              const float* rstd, const float* resid_f32, const void* resid_t,
+                              float* out_f32, void* out_t, float* dg, float* dg_part, int64_t rows,
+                              int n, int dtype, cudaStream_t st);
+tsp_status launch_swiglu_f32(const float* AB, float* G, int64_t rows, int I, cudaStream_t st);
+tsp_status launch_swiglu_bwd_f32(const float* dG, const float* AB, float* dAB, int64_t rows, int I,
+                                 cudaStream_t st);
+tsp_status launch_pack_attn_shards(const void* wq, const void* wk, const void* wv, const void* wo,
+                                   void* dst, int d, int D, int dtype, cudaStream_t st);
+
+// simt_f32.cu
+tsp_status launch_gemm_f32(int M, int N, int K, const float* A, int64_t sam, int64_t sak,
+                           const float* B, int64_t sbn, int64_t sbk, float* C, int64_t ldc,
+                           const float* R, int64_t ldr, int acc, cudaStream_t st);
+tsp_status launch_attn_f32_fwd(const float* QKV, int64_t S, int H, int dh, int D, float* O,
+                               float* LSE, cudaStream_t st);
+tsp_status launch_attn_f32_bwd(const float* QKV, const float* O, const float* dO, const float* LSE,
+                               float* delta, float* dQKV, int64_t S, int H, int dh, int D,
+                               cudaStream_t st);
+
+// attn_fwd.cu
+tsp_status launch_attn_fwd_bf16(const void* qkv, void* o, float* lse, int64_t S, int H, int dh,
+                                int D, cudaStream_t st);
+
+// attn_bwd.cu
+tsp_status launch_attn_bwd_bf16(const void* qkv, const void* o, const void* dO, const float* lse,
+                                float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int dh,
+                                int D, cudaStream_t st);
+
+}  // namespace tsp

@@ -1,0 +1,374 @@
+// rowwise.cu -- HBM-bound kernels: zigzag gather/scatter and RMSNorm fwd/bwd.
+//
+// Zigzag causal partitioning: "Folding Tensor and Sequence Parallelism for
+// Memory-Efficient Transformer Training & Inference" (gist.science summary),
+// section 2, attention-layer schedule (zigzag partitioning balances causal
+// attention).  Rank r owns chunks r and 2D-1-r of the 2D equal chunks.
+// RMSNorm: the pages give no formula; the plain reading of a pre-norm block,
+// rms(u; g) = u / sqrt(mean(u^2) + eps) * g with fp32 arithmetic.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tsp {
+
+// ---------------------------------------------------------------------------
+// K1: zigzag permute.  One CTA row at a time (grid-stride over rows), 16-byte
+// vectors when the row length allows it, 4-way unrolled for memory-level
+// parallelism.  Bit-exact copy.
+// ---------------------------------------------------------------------------
+template <typename V>
+__global__ void __launch_bounds__(256) zigzag_permute_kernel(const V* __restrict__ src,
+                                                             V* __restrict__ dst, int64_t S,
+                                                             int64_t c, int D, int64_t vpr,
+                                                             int inverse) {
+  for (int64_t row = blockIdx.x; row < S; row += gridDim.x) {
+    // forward: dst zigzag row <- src global row pos(row)
+    // inverse: dst global row <- src zigzag row row_of_pos(row)
+    const int64_t srow = inverse ? zz_row_of_pos(row, c, D) : zz_pos_of_row(row, c, D);
+    const V* s = src + srow * vpr;
+    V* d = dst + row * vpr;
+    int64_t v = threadIdx.x;
+    for (; v + 3 * blockDim.x < vpr; v += 4 * blockDim.x) {
+      V a0 = s[v], a1 = s[v + blockDim.x], a2 = s[v + 2 * blockDim.x], a3 = s[v + 3 * blockDim.x];
+      d[v] = a0;
+      d[v + blockDim.x] = a1;
+      d[v + 2 * blockDim.x] = a2;
+      d[v + 3 * blockDim.x] = a3;
+    }
+    for (; v < vpr; v += blockDim.x) d[v] = s[v];
+  }
+}
+
+tsp_status launch_zigzag_permute(const void* src, void* dst, int64_t S, int D, int64_t row_bytes,
+                                 int inverse, cudaStream_t st) {
+  const int64_t c = S / (2 * D);
+  const int grid = (int)std::min<int64_t>(S, (int64_t)num_sms() * 8);
+  Prof prof(inverse ? "zigzag_unpermute" : "zigzag_permute", st);
+  if (row_bytes % 16 == 0) {
+    zigzag_permute_kernel<uint4><<<grid, 256, 0, st>>>((const uint4*)src, (uint4*)dst, S, c, D,
+                                                       row_bytes / 16, inverse);
+  } else if (row_bytes % 4 == 0) {
+    zigzag_permute_kernel<uint32_t><<<grid, 256, 0, st>>>((const uint32_t*)src, (uint32_t*)dst, S,
+                                                          c, D, row_bytes / 4, inverse);
+  } else {
+    zigzag_permute_kernel<uint8_t><<<grid, 256, 0, st>>>((const uint8_t*)src, (uint8_t*)dst, S, c,
+                                                         D, row_bytes, inverse);
+  }
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// K2: RMSNorm forward.  One warp per row; the row stays in registers (UPL
+// units of 8 elements per lane), so u is read once and out written once.
+// Input and output types may differ (the block's fp32 residual stream h is
+// normalised into the bf16 GEMM operand b).
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float* f) {
+  if constexpr (sizeof(T) == 2) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = bf16_lo(w[i]);
+      f[2 * i + 1] = bf16_hi(w[i]);
+    }
+  } else {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+}
+template <typename T>
+__device__ __forceinline__ void store8(T* p, const float* f) {
+  if constexpr (sizeof(T) == 2) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
+                                              pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+  } else {
+    reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+  }
+}
+
+template <typename Tin, typename T, int UPL>
+__global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const Tin* __restrict__ u,
+                                                          const T* __restrict__ g,
+                                                          T* __restrict__ out,
+                                                          float* __restrict__ rstd_out,
+                                                          int64_t rows, int n, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int nu = n >> 3;  // 8-element units per row
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    const Tin* src = u + row * n;
+    float v[UPL][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < UPL; ++i) {
+      const int idx = lane + 32 * i;
+      if (idx < nu) {
+        load8(src + idx * 8, v[i]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(v[i][e], v[i][e], ss);
+      }
+    }
+    ss = warp_sum(ss);
+    const float r = rsqrtf(ss / (float)n + eps);
+    if (lane == 0 && rstd_out) rstd_out[row] = r;
+    T* dst = out + row * n;
+#pragma unroll
+    for (int i = 0; i < UPL; ++i) {
+      const int idx = lane + 32 * i;
+      if (idx < nu) {
+        float gf[8];
+        load8(g + idx * 8, gf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[i][e] = v[i][e] * r * gf[e];
+        store8(dst + idx * 8, v[i]);
+      }
+    }
+  }
+}
+
+// Scalar fallback for rows whose length is not a multiple of 8 (or unaligned).
+template <typename Tin, typename T>
+__global__ void rmsnorm_fwd_scalar_kernel(const Tin* __restrict__ u, const T* __restrict__ g,
+                                          T* __restrict__ out, float* __restrict__ rstd_out,
+                                          int64_t rows, int n, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    float ss = 0.f;
+    for (int i = lane; i < n; i += 32) {
+      float f = to_f(u[row * n + i]);
+      ss = fmaf(f, f, ss);
+    }
+    ss = warp_sum(ss);
+    const float r = rsqrtf(ss / (float)n + eps);
+    if (lane == 0 && rstd_out) rstd_out[row] = r;
+    for (int i = lane; i < n; i += 32)
+      out[row * n + i] = from_f<T>(to_f(u[row * n + i]) * r * to_f(g[i]));
+  }
+}
+
+template <typename Tin, typename T>
+static tsp_status rmsnorm_fwd_t(const Tin* u, const T* g, T* out, float* rstd, int64_t rows, int n,
+                                float eps, cudaStream_t st) {
+  const int64_t want = (rows + 7) / 8;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms() * 8));
+  const bool vec_ok = (n % 8 == 0) && ((uintptr_t)u % 16 == 0) && ((uintptr_t)g % 16 == 0) &&
+                      ((uintptr_t)out % 16 == 0);
+  const int nu = n / 8;
+  Prof prof("rmsnorm_fwd", st);
+  if (vec_ok && nu <= 32)
+    rmsnorm_fwd_kernel<Tin, T, 1><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
+  else if (vec_ok && nu <= 128)
+    rmsnorm_fwd_kernel<Tin, T, 4><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
+  else if (vec_ok && nu <= 512)
+    rmsnorm_fwd_kernel<Tin, T, 16><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
+  else
+    rmsnorm_fwd_scalar_kernel<Tin, T><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+tsp_status launch_rmsnorm_fwd(const void* u, int u_f32, const void* g, void* out, float* rstd,
+                              int64_t rows, int n, float eps, int dtype, cudaStream_t st) {
+  typedef __nv_bfloat16 bf;
+  if (dtype == TSP_BF16) {
+    if (u_f32)
+      return rmsnorm_fwd_t((const float*)u, (const bf*)g, (bf*)out, rstd, rows, n, eps, st);
+    return rmsnorm_fwd_t((const bf*)u, (const bf*)g, (bf*)out, rstd, rows, n, eps, st);
+  }
+  return rmsnorm_fwd_t((const float*)u, (const float*)g, (float*)out, rstd, rows, n, eps, st);
+}
+
+// ---------------------------------------------------------------------------
+// K8: RMSNorm backward fused with the residual-gradient add.
+//   nrm = u * rstd;  gd = dout * g
+//   du  = rstd * (gd - nrm * mean(gd * nrm))
+//   res_out = resid + du          (fp32 and/or storage-dtype copies)
+//   dg_part[block] = sum over the block's rows of dout * nrm
+// dout is fp32; u is of type Tu (the fp32 residual stream or the storage
+// dtype); g, resid_t and out_t are of the storage dtype T.
+// One warp per row (strided loop over columns); the gain gradient of a CTA is
+// gathered in shared memory and written as one partial row, summed by
+// rowsum_partials_kernel.
+// ---------------------------------------------------------------------------
+template <typename Tu, typename T>
+__global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(
+    const float* __restrict__ dout, const Tu* __restrict__ u, const T* __restrict__ g,
+    const float* __restrict__ rstd, const float* __restrict__ resid_f32,
+    const T* __restrict__ resid_t, float* __restrict__ out_f32, T* __restrict__ out_t,
+    float* __restrict__ dg_part, int64_t rows, int n) {
+  extern __shared__ float s_dg[];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) s_dg[i] = 0.f;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    const float r = rstd[row];
+    const float* dr = dout + row * n;
+    const Tu* ur = u + row * n;
+    float dot = 0.f;
+    for (int i = lane; i < n; i += 32) {
+      const float nrm = to_f(ur[i]) * r;
+      const float dv = dr[i];
+      dot = fmaf(dv * to_f(g[i]), nrm, dot);
+      atomicAdd(&s_dg[i], dv * nrm);
+    }
+    dot = warp_sum(dot) / (float)n;
+    for (int i = lane; i < n; i += 32) {
+      const float nrm = to_f(ur[i]) * r;
+      const float du = r * (dr[i] * to_f(g[i]) - nrm * dot);
+      const float o = (resid_f32 ? resid_f32[row * n + i] : to_f(resid_t[row * n + i])) + du;
+      if (out_f32) out_f32[row * n + i] = o;
+      if (out_t) out_t[row * n + i] = from_f<T>(o);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) dg_part[(int64_t)blockIdx.x * n + i] = s_dg[i];
+}
+
+int rmsnorm_bwd_blocks(int64_t rows) {
+  return (int)std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 2));
+}
+
+// out[i] = sum_b part[b][i]  (deterministic order)
+__global__ void rowsum_partials_kernel(const float* __restrict__ part, float* __restrict__ out,
+                                       int nb, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float s = 0.f;
+  for (int b = 0; b < nb; ++b) s += part[(int64_t)b * n + i];
+  out[i] = s;
+}
+
+template <typename Tu, typename T>
+static tsp_status rmsnorm_bwd_t(const float* dout, const Tu* u, const T* g, const float* rstd,
+                                const float* resid_f32, const T* resid_t, float* out_f32, T* out_t,
+                                float* dg, float* dg_part, int64_t rows, int n, cudaStream_t st) {
+  const int grid = rmsnorm_bwd_blocks(rows);
+  const size_t sm = (size_t)n * sizeof(float);
+  Prof prof("rmsnorm_bwd", st, 2);
+  if (sm > 48 * 1024)
+    TSP_CUDA_TRY(cudaFuncSetAttribute(rmsnorm_bwd_kernel<Tu, T>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+  rmsnorm_bwd_kernel<Tu, T><<<grid, 256, sm, st>>>(dout, u, g, rstd, resid_f32, resid_t, out_f32,
+                                                   out_t, dg_part, rows, n);
+  TSP_CUDA_TRY(cudaGetLastError());
+  rowsum_partials_kernel<<<(n + 255) / 256, 256, 0, st>>>(dg_part, dg, grid, n);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+tsp_status launch_rmsnorm_bwd(const float* dout, const void* u, int u_f32, const void* g,
+                              const float* rstd, const float* resid_f32, const void* resid_t,
+                              float* out_f32, void* out_t, float* dg, float* dg_part, int64_t rows,
+                              int n, int dtype, cudaStream_t st) {
+  typedef __nv_bfloat16 bf;
+  if (dtype == TSP_BF16) {
+    if (u_f32)
+      return rmsnorm_bwd_t(dout, (const float*)u, (const bf*)g, rstd, resid_f32,
+                           (const bf*)resid_t, out_f32, (bf*)out_t, dg, dg_part, rows, n, st);
+    return rmsnorm_bwd_t(dout, (const bf*)u, (const bf*)g, rstd, resid_f32, (const bf*)resid_t,
+                         out_f32, (bf*)out_t, dg, dg_part, rows, n, st);
+  }
+  return rmsnorm_bwd_t(dout, (const float*)u, (const float*)g, rstd, resid_f32,
+                       (const float*)resid_t, out_f32, (float*)out_t, dg, dg_part, rows, n, st);
+}
+
+// ---------------------------------------------------------------------------
+// Elementwise helpers of the exact-fp32 path.
+// ---------------------------------------------------------------------------
+
+// G = silu(A) * B, with A = AB[:, :I] and B = AB[:, I:]  (row stride 2I)
+__global__ void swiglu_f32_kernel(const float* __restrict__ AB, float* __restrict__ G, int64_t rows,
+                                  int I) {
+  const int64_t total = rows * I;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = t / I;
+    const int i = (int)(t - r * I);
+    const float a = AB[r * 2 * I + i], b = AB[r * 2 * I + I + i];
+    G[t] = a * sigmoidf_(a) * b;
+  }
+}
+
+// dA = dG * B * s(A) * (1 + A (1 - s(A))),  dB = dG * silu(A)   (into dAB [rows, 2I])
+__global__ void swiglu_bwd_f32_kernel(const float* __restrict__ dG, const float* __restrict__ AB,
+                                      float* __restrict__ dAB, int64_t rows, int I) {
+  const int64_t total = rows * I;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = t / I;
+    const int i = (int)(t - r * I);
+    const float a = AB[r * 2 * I + i], b = AB[r * 2 * I + I + i];
+    const float s = sigmoidf_(a);
+    const float dg = dG[t];
+    dAB[r * 2 * I + i] = dg * b * s * (1.f + a * (1.f - s));
+    dAB[r * 2 * I + I + i] = dg * a * s;
+  }
+}
+
+tsp_status launch_swiglu_f32(const float* AB, float* G, int64_t rows, int I, cudaStream_t st) {
+  Prof prof("swiglu_f32", st);
+  swiglu_f32_kernel<<<num_sms() * 4, 256, 0, st>>>(AB, G, rows, I);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+tsp_status launch_swiglu_bwd_f32(const float* dG, const float* AB, float* dAB, int64_t rows, int I,
+                                 cudaStream_t st) {
+  Prof prof("swiglu_bwd_f32", st);
+  swiglu_bwd_f32_kernel<<<num_sms() * 4, 256, 0, st>>>(dG, AB, dAB, rows, I);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+// Pack the attention shards: shard k -> [W_Q[C_k,:]; W_K[C_k,:]; W_V[C_k,:]; W_O[:,C_k]^T].
+template <typename T>
+__global__ void pack_attn_shards_kernel(const T* __restrict__ wq, const T* __restrict__ wk,
+                                        const T* __restrict__ wv, const T* __restrict__ wo,
+                                        T* __restrict__ dst, int d, int D) {
+  const int64_t total = (int64_t)4 * d * d;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t orow = t / d;  // row of dst
+    const int col = (int)(t - orow * d);
+    // find shard k with 4*lo(k) <= orow < 4*lo(k+1)
+    int k = (int)((orow / 4) * D / d);
+    while (k > 0 && 4 * ((int64_t)k * d / D) > orow) --k;
+    while (k + 1 < D && 4 * ((int64_t)(k + 1) * d / D) <= orow) ++k;
+    const int64_t lo = (int64_t)k * d / D, w = (int64_t)(k + 1) * d / D - lo;
+    const int64_t rr = orow - 4 * lo;
+    const int part = (int)(rr / w);
+    const int64_t ci = lo + (rr - part * w);
+    T v;
+    if (part == 0) v = wq[ci * d + col];
+    else if (part == 1) v = wk[ci * d + col];
+    else if (part == 2) v = wv[ci * d + col];
+    else v = wo[(int64_t)col * d + ci];
+    dst[t] = v;
+  }
+}
+
+tsp_status launch_pack_attn_shards(const void* wq, const void* wk, const void* wv, const void* wo,
+                                   void* dst, int d, int D, int dtype, cudaStream_t st) {
+  Prof prof("pack_attn_shards", st);
+  if (dtype == TSP_BF16)
+    pack_attn_shards_kernel<__nv_bfloat16><<<num_sms() * 4, 256, 0, st>>>(
+        (const __nv_bfloat16*)wq, (const __nv_bfloat16*)wk, (const __nv_bfloat16*)wv,
+        (const __nv_bfloat16*)wo, (__nv_bfloat16*)dst, d, D);
+  else
+    pack_attn_shards_kernel<float><<<num_sms() * 4, 256, 0, st>>>(
+        (const float*)wq, (const float*)wk, (const float*)wv, (const float*)wo, (float*)dst, d, D);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+}  // namespace tsp

@@ -1,0 +1,267 @@
+"""Thin ctypes binding of libtsp.so (include/tsp.h).
+
+Argument marshalling only: torch tensors give device pointers and the current
+stream; every step of the block runs in the library's CUDA kernels.  There is
+no fallback: if the library is missing or no GPU is present the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtsp.so")
+
+TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT = range(5)
+TSP_F32, TSP_BF16 = 0, 1
+TSP_OP_ATTN_FWD, TSP_OP_MLP_FWD, TSP_OP_BLOCK_FWD, TSP_OP_BLOCK_BWD = range(4)
+
+EXPORTED = ("tsp_zigzag_permute", "tsp_rmsnorm_fwd", "tsp_workspace_bytes", "tsp_saved_bytes",
+            "tsp_attn_block_fwd", "tsp_gated_mlp_fwd", "tsp_block_fwd", "tsp_block_bwd",
+            "tsp_pack_attn_shards", "tsp_device_status", "tsp_strerror", "tsp_num_sms",
+            "tsp_profile_enable", "tsp_profile_report", "tsp_launch_count")
+
+
+class TspError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (status {code})")
+
+
+class Cfg(ctypes.Structure):
+    _fields_ = [("S", ctypes.c_int64), ("d", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("dh", ctypes.c_int32), ("inter", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("eps", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+class AttnW(ctypes.Structure):
+    _fields_ = [("wq", ctypes.c_void_p), ("wk", ctypes.c_void_p), ("wv", ctypes.c_void_p),
+                ("wo", ctypes.c_void_p), ("g_attn", ctypes.c_void_p)]
+
+
+class MlpW(ctypes.Structure):
+    _fields_ = [("w1", ctypes.c_void_p), ("w3", ctypes.c_void_p), ("w2", ctypes.c_void_p),
+                ("g_mlp", ctypes.c_void_p), ("add_residual", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libtsp.so (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: run folded_tensor_sequence_zigzag_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    P = ctypes.POINTER
+    sig = {
+        "tsp_zigzag_permute": (i32, [vp, vp, i64, i32, i64, i32, vp]),
+        "tsp_rmsnorm_fwd": (i32, [vp, vp, vp, vp, i64, i32, f32, i32, vp]),
+        "tsp_workspace_bytes": (sz, [P(Cfg), i32]),
+        "tsp_saved_bytes": (sz, [P(Cfg)]),
+        "tsp_attn_block_fwd": (i32, [P(Cfg), vp, P(AttnW), vp, vp, sz, vp]),
+        "tsp_gated_mlp_fwd": (i32, [P(Cfg), vp, P(MlpW), vp, vp, sz, vp]),
+        "tsp_block_fwd": (i32, [P(Cfg), vp, P(AttnW), P(MlpW), vp, vp, vp, sz, vp]),
+        "tsp_block_bwd": (i32, [P(Cfg), vp, vp, vp, P(AttnW), P(MlpW), vp] + [vp] * 9 + [vp, sz, vp]),
+        "tsp_pack_attn_shards": (i32, [P(Cfg), P(AttnW), vp, vp]),
+        "tsp_device_status": (i32, [vp, i32]),
+        "tsp_strerror": (ctypes.c_char_p, [i32]),
+        "tsp_num_sms": (i32, []),
+        "tsp_profile_enable": (None, [i32]),
+        "tsp_profile_report": (i32, [ctypes.c_char_p, i64]),
+        "tsp_launch_count": (i64, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return load().tsp_strerror(code).decode()
+    except Exception:  # noqa: BLE001
+        return f"status {code}"
+
+
+def _check(code: int, where: str):
+    if code != TSP_OK:
+        raise TspError(code, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must live on the GPU")
+
+
+@dataclass
+class BlockWeights:
+    """Device tensors of one block (nn.Linear layout [out, in])."""
+    wq: torch.Tensor
+    wk: torch.Tensor
+    wv: torch.Tensor
+    wo: torch.Tensor
+    w1: torch.Tensor
+    w3: torch.Tensor
+    w2: torch.Tensor
+    g_attn: torch.Tensor
+    g_mlp: torch.Tensor
+
+    @classmethod
+    def from_dict(cls, d: dict, device="cuda"):
+        return cls(**{k: d[k].to(device).contiguous() for k in
+                      ("wq", "wk", "wv", "wo", "w1", "w3", "w2", "g_attn", "g_mlp")})
+
+    def attn(self) -> AttnW:
+        return AttnW(_ptr(self.wq), _ptr(self.wk), _ptr(self.wv), _ptr(self.wo), _ptr(self.g_attn))
+
+    def mlp(self, norm=True, residual=True) -> MlpW:
+        return MlpW(_ptr(self.w1), _ptr(self.w3), _ptr(self.w2), _ptr(self.g_mlp) if norm else None,
+                    1 if residual else 0)
+
+
+def make_cfg(S, d, H, inter, D, dtype: torch.dtype, eps=1e-6) -> Cfg:
+    return Cfg(int(S), int(d), int(H), int(d // H), int(inter), int(D), float(eps),
+               TSP_BF16 if dtype == torch.bfloat16 else TSP_F32)
+
+
+def workspace_bytes(cfg: Cfg, op: int) -> int:
+    return int(load().tsp_workspace_bytes(ctypes.byref(cfg), op))
+
+
+def saved_bytes(cfg: Cfg) -> int:
+    return int(load().tsp_saved_bytes(ctypes.byref(cfg)))
+
+
+def _ws(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def zigzag_permute(src: torch.Tensor, D: int, inverse: bool = False, out=None, stream=None):
+    """Rows of src (global order) -> zigzag rank-major order (or back)."""
+    _require_cuda(src)
+    src = src.contiguous()
+    out = torch.empty_like(src) if out is None else out
+    S = src.shape[0]
+    row_bytes = src.numel() // max(S, 1) * src.element_size()
+    _check(load().tsp_zigzag_permute(_ptr(src), _ptr(out), S, D, row_bytes, 1 if inverse else 0,
+                                     _stream(stream)), "tsp_zigzag_permute")
+    return out
+
+
+def rmsnorm_fwd(u: torch.Tensor, g: torch.Tensor, eps: float = 1e-6, with_rstd=False, stream=None):
+    _require_cuda(u, g)
+    out = torch.empty_like(u)
+    rstd = torch.empty(u.shape[0], dtype=torch.float32, device=u.device) if with_rstd else None
+    dt = TSP_BF16 if u.dtype == torch.bfloat16 else TSP_F32
+    _check(load().tsp_rmsnorm_fwd(_ptr(u), _ptr(g), _ptr(out), _ptr(rstd), u.shape[0], u.shape[1],
+                                  eps, dt, _stream(stream)), "tsp_rmsnorm_fwd")
+    return (out, rstd) if with_rstd else out
+
+
+def attn_block_fwd(cfg: Cfg, x_z, W: BlockWeights, out=None, ws=None, stream=None):
+    _require_cuda(x_z)
+    out = torch.empty_like(x_z) if out is None else out
+    nb = workspace_bytes(cfg, TSP_OP_ATTN_FWD)
+    ws = _ws(nb, x_z.device) if ws is None else ws
+    aw = W.attn()
+    _check(load().tsp_attn_block_fwd(ctypes.byref(cfg), _ptr(x_z), ctypes.byref(aw), _ptr(out),
+                                     _ptr(ws), ws.numel(), _stream(stream)), "tsp_attn_block_fwd")
+    return out
+
+
+def gated_mlp_fwd(cfg: Cfg, h_z, W: BlockWeights, norm=True, residual=True, out=None, ws=None,
+                  stream=None):
+    _require_cuda(h_z)
+    out = torch.empty_like(h_z) if out is None else out
+    nb = workspace_bytes(cfg, TSP_OP_MLP_FWD)
+    ws = _ws(nb, h_z.device) if ws is None else ws
+    mw = W.mlp(norm, residual)
+    _check(load().tsp_gated_mlp_fwd(ctypes.byref(cfg), _ptr(h_z), ctypes.byref(mw), _ptr(out),
+                                    _ptr(ws), ws.numel(), _stream(stream)), "tsp_gated_mlp_fwd")
+    return out
+
+
+def block_fwd(cfg: Cfg, x_z, W: BlockWeights, saved=None, out=None, ws=None, stream=None):
+    """y_z = block(x_z).  Pass ``saved`` (uint8, saved_bytes(cfg)) to keep activations for bwd."""
+    _require_cuda(x_z)
+    out = torch.empty_like(x_z) if out is None else out
+    if saved is None and ws is None:
+        ws = _ws(workspace_bytes(cfg, TSP_OP_BLOCK_FWD), x_z.device)
+    aw, mw = W.attn(), W.mlp()
+    _check(load().tsp_block_fwd(ctypes.byref(cfg), _ptr(x_z), ctypes.byref(aw), ctypes.byref(mw),
+                                _ptr(out), _ptr(saved), _ptr(ws), 0 if ws is None else ws.numel(),
+                                _stream(stream)), "tsp_block_fwd")
+    return out
+
+
+GRAD_NAMES = ("dwq", "dwk", "dwv", "dwo", "dw1", "dw3", "dw2", "dg_attn", "dg_mlp")
+
+
+def block_bwd(cfg: Cfg, x_z, dy_z, saved, W: BlockWeights, ws=None, stream=None) -> dict:
+    """Gradients of sum(dy * y): dx_z (activation dtype) and fp32 weight/gain grads."""
+    _require_cuda(x_z, dy_z, saved)
+    dev = x_z.device
+    d, I = cfg.d, cfg.inter
+    shapes = {"dwq": (d, d), "dwk": (d, d), "dwv": (d, d), "dwo": (d, d), "dw1": (I, d),
+              "dw3": (I, d), "dw2": (d, I), "dg_attn": (d,), "dg_mlp": (d,)}
+    g = {k: torch.empty(shapes[k], dtype=torch.float32, device=dev) for k in GRAD_NAMES}
+    g["dx"] = torch.empty_like(x_z)
+    ws = _ws(workspace_bytes(cfg, TSP_OP_BLOCK_BWD), dev) if ws is None else ws
+    aw, mw = W.attn(), W.mlp()
+    _check(load().tsp_block_bwd(ctypes.byref(cfg), _ptr(x_z), _ptr(dy_z), _ptr(saved),
+                                ctypes.byref(aw), ctypes.byref(mw), _ptr(g["dx"]),
+                                *[_ptr(g[k]) for k in GRAD_NAMES], _ptr(ws), ws.numel(),
+                                _stream(stream)), "tsp_block_bwd")
+    return g
+
+
+def pack_attn_shards(cfg: Cfg, W: BlockWeights, stream=None):
+    out = torch.empty((4 * cfg.d, cfg.d), dtype=W.wq.dtype, device=W.wq.device)
+    aw = W.attn()
+    _check(load().tsp_pack_attn_shards(ctypes.byref(cfg), ctypes.byref(aw), _ptr(out),
+                                       _stream(stream)), "tsp_pack_attn_shards")
+    return out
+
+
+def device_status(reset: bool = True, stream=None) -> int:
+    return int(load().tsp_device_status(_stream(stream), 1 if reset else 0))
+
+
+def profile_enable(on: bool = True):
+    load().tsp_profile_enable(1 if on else 0)
+
+
+def profile_report() -> dict:
+    """{label: (kernels, total_ms)} of the launches recorded since profile_enable(True)."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    n = load().tsp_profile_report(buf, len(buf))
+    if n < 0:
+        raise RuntimeError("tsp_profile_report failed")
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, k, ms = line.split("\t")
+        out[name] = (int(k), float(ms))
+    return out
+
+
+def launch_count() -> int:
+    return int(load().tsp_launch_count())

@@ -1,0 +1,203 @@
+/*
+ * tsp.h -- C ABI of the TSP-folded transformer block for one GB300 (sm_103a).
+ *
+ * What the library computes
+ * -------------------------
+ * Source page: "Folding Tensor and Sequence Parallelism for Memory-Efficient
+ * Transformer Training & Inference" (gist.science summary), section 2
+ * ("Methodology: TSP").  Under TSP every one of D ranks holds 1/D of the
+ * parameters and 1/D of the tokens ("Unified sharding").  Attention layers
+ * walk the packed W_Q/W_K/W_V/W_O shards (one rank broadcasts its shard per
+ * step), project every rank's own tokens, all-gather K/V over the sequence
+ * and run FlashAttention on zigzag-partitioned causal rows ("Runtime
+ * schedules", attention bullet).  Gated-MLP layers rotate W_1/W_2/W_3 shards
+ * around a ring; every rank accumulates its partial outputs locally, so no
+ * all-reduce is needed ("Runtime schedules", gated-MLP bullet).
+ *
+ * Here the D ranks are VIRTUAL ranks on one GPU: rank r's tokens are rows
+ * [r*2c, (r+1)*2c) of one rank-major "zigzag" buffer, the gathered K/V is the
+ * same buffer, and a weight shard is a column range of the unsharded weight.
+ * The block is pre-norm:
+ *     a = rms(x; g_attn),  Q|K|V = a [W_Q|W_K|W_V]^T,  O = causal MHA(Q,K,V),
+ *     h = x + O W_O^T,     b = rms(h; g_mlp),
+ *     y = h + (silu(b W_1^T) * (b W_3^T)) W_2^T
+ * with rms(u; g) = u / sqrt(mean(u^2) + eps) * g, scale 1/sqrt(dh), causal
+ * mask j <= i with the diagonal included, no biases, no positional encoding.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers are DEVICE pointers unless a comment says otherwise; the caller
+ *    allocates and owns every buffer.  The library never allocates device
+ *    memory: scratch comes from the caller's workspace (tsp_workspace_bytes).
+ *  - Matrices are row-major.  Weights use the nn.Linear convention
+ *    [out, in]: W_Q, W_K, W_V, W_O are [d, d]; W_1, W_3 are [inter, d];
+ *    W_2 is [d, inter]; gains are [d].
+ *  - Activations (x_z, h_z, y_z, dy_z, dx_z) are in zigzag rank-major order:
+ *    [D][2][c][d] with c = S/(2D); rank r's slot 0 holds global chunk r and
+ *    slot 1 holds chunk 2D-1-r, positions ascending inside a chunk.
+ *    tsp_zigzag_permute converts from/to global token order.
+ *  - dtype TSP_BF16: activations, weights and gains are bf16; accumulation,
+ *    softmax and norms run in fp32.  TSP_F32: everything fp32 (exact fp32
+ *    SIMT path, meant for small shapes).  Weight/gain gradients are always
+ *    fp32 and are OVERWRITTEN (not accumulated into).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *    call is asynchronous on that stream; outputs are ready when the stream
+ *    reaches the call.
+ *  - Errors a host can detect (bad sizes, NULL or misaligned pointers, short
+ *    workspace, shapes the bf16 kernels do not take) are returned at once and
+ *    nothing is launched.  Launch failures return TSP_ERR_CUDA.  Errors the
+ *    device detects (a pipeline wait that exceeded its time limit) set a
+ *    sticky device status word read by tsp_device_status; kernels never trap.
+ *  - All pointers must be 16-byte aligned; row strides are dense.
+ */
+#ifndef TSP_H_
+#define TSP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TSP_OK = 0,
+  TSP_ERR_INVALID_ARG = 1,   /* bad size, NULL or misaligned pointer, short buffer */
+  TSP_ERR_UNSUPPORTED = 2,   /* valid shape that the selected kernels do not take */
+  TSP_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed               */
+  TSP_ERR_TIMEOUT = 4        /* a device pipeline wait exceeded its time limit     */
+} tsp_status;
+
+typedef enum { TSP_F32 = 0, TSP_BF16 = 1 } tsp_dtype;
+
+/* Block configuration.  Causal attention always.
+ *   S      tokens (multiple of 2D)
+ *   d      d_model;  H heads;  dh = d / H (must equal d / H)
+ *   inter  SwiGLU intermediate size
+ *   D      virtual ranks, 1..64
+ *   eps    RMSNorm epsilon
+ *   dtype  tsp_dtype
+ * bf16 kernels additionally need: d % 256 == 0, inter % 128 == 0, and for
+ * attention dh == 128 and c = S/(2D) a multiple of 128.  Other valid shapes
+ * return TSP_ERR_UNSUPPORTED in bf16 (there is no silent fallback). */
+typedef struct {
+  int64_t S;
+  int32_t d, H, dh, inter, D;
+  float eps;
+  int32_t dtype;
+} tsp_cfg;
+
+/* Attention-half weights: wq, wk, wv, wo [d, d]; g_attn [d]. */
+typedef struct {
+  const void *wq, *wk, *wv, *wo, *g_attn;
+} tsp_attn_w;
+
+/* Gated-MLP weights: w1, w3 [inter, d]; w2 [d, inter]; g_mlp [d] or NULL
+ * (NULL: no RMSNorm, b = h).  add_residual: 1 -> y = h + MLP(b), 0 -> y = MLP(b). */
+typedef struct {
+  const void *w1, *w3, *w2, *g_mlp;
+  int32_t add_residual;
+} tsp_mlp_w;
+
+/* Workspace queries (op selects the entry point). */
+enum { TSP_OP_ATTN_FWD = 0, TSP_OP_MLP_FWD = 1, TSP_OP_BLOCK_FWD = 2, TSP_OP_BLOCK_BWD = 3 };
+
+/* Zigzag causal partitioning (section 2, attention bullet: "zigzag
+ * partitioning balances the causal attention work").  Bit-exact row copy.
+ *   inverse = 0: src in global order [S][row_bytes] -> dst zigzag rank-major;
+ *   inverse = 1: zigzag rank-major -> global order.
+ * row_bytes: bytes per token row (e.g. d * sizeof(element)); any value > 0,
+ * multiples of 16 take the vectorised path.  src and dst must not overlap.
+ * Errors: TSP_ERR_INVALID_ARG if S <= 0, D not in 1..64, S % (2D) != 0,
+ * row_bytes <= 0 or a NULL pointer. */
+tsp_status tsp_zigzag_permute(const void* src, void* dst, int64_t S, int32_t D,
+                              int64_t row_bytes, int32_t inverse, void* stream);
+
+/* Row-wise RMSNorm (pre-norm of both halves of the block; the pages give no
+ * formula, the plain reading is the one above).  u, out: [rows, n] of the
+ * cfg dtype; g: [n] of the cfg dtype; rstd (nullable): [rows] fp32 receives
+ * 1/sqrt(mean(u^2)+eps).  dtype: tsp_dtype. */
+tsp_status tsp_rmsnorm_fwd(const void* u, const void* g, void* out, float* rstd,
+                           int64_t rows, int32_t n, float eps, int32_t dtype, void* stream);
+
+/* Bytes of caller workspace an entry point needs for cfg (0 if cfg invalid). */
+size_t tsp_workspace_bytes(const tsp_cfg* cfg, int32_t op);
+
+/* Bytes of the activation buffer tsp_block_fwd fills for tsp_block_bwd. */
+size_t tsp_saved_bytes(const tsp_cfg* cfg);
+
+/* Attention half of the block (section 2, attention bullet): for shard
+ * k = 0..D-1 every virtual rank projects its rows with the W_Q/W_K/W_V
+ * columns of shard k; K/V of all ranks form the gathered context; each rank's
+ * zigzag rows attend causally to it; each rank accumulates O[:,C_k] W_O[:,C_k]^T
+ * over k in fp32 onto its residual rows:  h_z = x_z + Attn(rms(x_z)) W_O^T.
+ * x_z, h_z: [S, d] zigzag.  ws: tsp_workspace_bytes(cfg, TSP_OP_ATTN_FWD). */
+tsp_status tsp_attn_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* w,
+                              void* h_z, void* ws, size_t ws_bytes, void* stream);
+
+/* Gated-MLP half (section 2, gated-MLP bullet): shard I_k of W_1/W_3 (rows)
+ * and W_2 (columns); virtual rank r takes shard (r - t) mod D at ring step t
+ * and accumulates G[:,I_k] W_2[:,I_k]^T in fp32 on its own rows.
+ *   y_z = [h_z +] (silu(b W_1^T) * (b W_3^T)) W_2^T, b = rms(h_z; g_mlp) or h_z.
+ * h_z, y_z: [S, d] zigzag.  ws: tsp_workspace_bytes(cfg, TSP_OP_MLP_FWD). */
+tsp_status tsp_gated_mlp_fwd(const tsp_cfg* cfg, const void* h_z, const tsp_mlp_w* w,
+                             void* y_z, void* ws, size_t ws_bytes, void* stream);
+
+/* Whole block forward: y_z = MLP-half(Attention-half(x_z)).  mlp_w->g_mlp
+ * must be non-NULL and add_residual 1 (pre-norm block).  saved (nullable):
+ * tsp_saved_bytes(cfg) bytes that receive the activations tsp_block_bwd
+ * needs; NULL for inference.  ws: tsp_workspace_bytes(cfg, TSP_OP_BLOCK_FWD). */
+tsp_status tsp_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* aw,
+                         const tsp_mlp_w* mw, void* y_z, void* saved,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* Whole block backward of L = sum(dy * y).  Inputs: x_z and dy_z ([S, d]
+ * zigzag, cfg dtype), saved (filled by tsp_block_fwd with the same cfg,
+ * weights and x_z).  Outputs: dx_z ([S, d] zigzag, cfg dtype) and fp32
+ * gradients dwq, dwk, dwv, dwo [d, d], dw1, dw3 [inter, d], dw2 [d, inter],
+ * dg_attn, dg_mlp [d] -- each the sum over the D virtual ranks' token rows
+ * (the reduction TSP performs toward the shard owners).
+ * ws: tsp_workspace_bytes(cfg, TSP_OP_BLOCK_BWD). */
+tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z,
+                         const void* saved, const tsp_attn_w* aw, const tsp_mlp_w* mw,
+                         void* dx_z, float* dwq, float* dwk, float* dwv, float* dwo,
+                         float* dw1, float* dw3, float* dw2, float* dg_attn, float* dg_mlp,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* Packed shard layout, what one broadcast step of the attention schedule
+ * carries ("packed W_Q, W_K, W_V, W_O"): for shard k (columns C_k of width
+ * d/D, boundaries floor(k*d/D)) writes [W_Q[C_k,:]; W_K[C_k,:]; W_V[C_k,:];
+ * W_O[:,C_k]^T] as a [4*|C_k|, d] block; shards follow each other in dst.
+ * Elements of the cfg dtype; dst holds 4*d*d elements.  The forward kernels
+ * read the unsharded weights directly and do not need this. */
+tsp_status tsp_pack_attn_shards(const tsp_cfg* cfg, const tsp_attn_w* w, void* dst, void* stream);
+
+/* Reads (and with reset != 0 clears) the sticky device status word.  Waits
+ * for `stream` to finish.  Returns TSP_OK or the first device error seen
+ * (TSP_ERR_TIMEOUT). */
+tsp_status tsp_device_status(void* stream, int32_t reset);
+
+/* Static string for a status code. */
+const char* tsp_strerror(tsp_status s);
+
+/* Number of SMs the kernels size their persistent grids for (current device,
+ * queried on first use; 0 if no device). */
+int32_t tsp_num_sms(void);
+
+/* Launch accounting (not on the pages: measurement plumbing).
+ * tsp_profile_enable(1) clears the record and starts bracketing every later
+ * launch site with CUDA events on its stream; (0) stops.  tsp_profile_report
+ * waits for the recorded events and writes one line per launch-site label,
+ * "label<TAB>kernels<TAB>total_ms<NL>", into buf (host memory, `bytes` long,
+ * NUL-terminated); returns the number of lines, or -1 if buf is too small or
+ * an event failed.  tsp_launch_count: kernels launched by the library since
+ * it was loaded. */
+void tsp_profile_enable(int32_t on);
+int32_t tsp_profile_report(char* buf, int64_t bytes);
+int64_t tsp_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSP_H_ */

@@ -1,0 +1,120 @@
+"""The C ABI library loads, exports every declared entry point, and rejects
+bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from folded_tensor_sequence_zigzag_gb300 import tsp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(tsp_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from folded_tensor_sequence_zigzag_gb300 import build
+    build.build()
+    return tsp.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"tsp_zigzag_permute", "tsp_attn_block_fwd", "tsp_gated_mlp_fwd", "tsp_block_fwd",
+            "tsp_block_bwd"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(tsp.EXPORTED) == names
+
+
+def test_strerror(lib):
+    for code in range(5):
+        assert lib.tsp_strerror(code)
+    assert b"invalid" in lib.tsp_strerror(tsp.TSP_ERR_INVALID_ARG)
+
+
+def _cfg(**kw):
+    base = dict(S=256, d=64, H=4, inter=128, D=4, dtype=tsp.TSP_F32)
+    base.update(kw)
+    return tsp.Cfg(base["S"], base["d"], base["H"], base.get("dh", base["d"] // base["H"]),
+                   base["inter"], base["D"], 1e-6, base["dtype"])
+
+
+@pytest.mark.parametrize("bad", [dict(S=250), dict(D=0), dict(D=65), dict(d=66), dict(dh=8),
+                                 dict(inter=0), dict(dtype=7), dict(S=0), dict(d=2, H=1, D=4)])
+def test_invalid_cfg_rejected_without_launch(lib, bad):
+    cfg = _cfg(**bad)
+    assert lib.tsp_workspace_bytes(ctypes.byref(cfg), tsp.TSP_OP_BLOCK_FWD) == 0
+    assert lib.tsp_saved_bytes(ctypes.byref(cfg)) == 0
+    fake = ctypes.c_void_p(0x10000)
+    aw = tsp.AttnW(fake, fake, fake, fake, fake)
+    mw = tsp.MlpW(fake, fake, fake, fake, 1)
+    r = lib.tsp_block_fwd(ctypes.byref(cfg), fake, ctypes.byref(aw), ctypes.byref(mw), fake, None,
+                          fake, 1 << 40, None)
+    assert r == tsp.TSP_ERR_INVALID_ARG
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    cfg = _cfg()
+    ok = ctypes.c_void_p(0x10000)
+    mis = ctypes.c_void_p(0x10008)
+    aw = tsp.AttnW(ok, ok, ok, ok, ok)
+    mw = tsp.MlpW(ok, ok, ok, ok, 1)
+    big = 1 << 40
+    assert lib.tsp_block_fwd(ctypes.byref(cfg), None, ctypes.byref(aw), ctypes.byref(mw), ok,
+                             None, ok, big, None) == tsp.TSP_ERR_INVALID_ARG
+    assert lib.tsp_block_fwd(ctypes.byref(cfg), mis, ctypes.byref(aw), ctypes.byref(mw), ok,
+                             None, ok, big, None) == tsp.TSP_ERR_INVALID_ARG
+    bad_aw = tsp.AttnW(ok, mis, ok, ok, ok)
+    assert lib.tsp_block_fwd(ctypes.byref(cfg), ok, ctypes.byref(bad_aw), ctypes.byref(mw), ok,
+                             None, ok, big, None) == tsp.TSP_ERR_INVALID_ARG
+    # block forward needs the MLP norm and residual
+    no_norm = tsp.MlpW(ok, ok, ok, None, 1)
+    assert lib.tsp_block_fwd(ctypes.byref(cfg), ok, ctypes.byref(aw), ctypes.byref(no_norm), ok,
+                             None, ok, big, None) == tsp.TSP_ERR_INVALID_ARG
+    # short workspace
+    assert lib.tsp_block_fwd(ctypes.byref(cfg), ok, ctypes.byref(aw), ctypes.byref(mw), ok,
+                             None, ok, 16, None) == tsp.TSP_ERR_INVALID_ARG
+    assert lib.tsp_zigzag_permute(None, ok, 16, 2, 16, 0, None) == tsp.TSP_ERR_INVALID_ARG
+    assert lib.tsp_zigzag_permute(ok, ok, 18, 2, 16, 0, None) == tsp.TSP_ERR_INVALID_ARG
+    assert lib.tsp_zigzag_permute(ok, ok, 16, 2, 0, 0, None) == tsp.TSP_ERR_INVALID_ARG
+    assert lib.tsp_rmsnorm_fwd(ok, None, ok, None, 4, 8, 1e-6, 1, None) == tsp.TSP_ERR_INVALID_ARG
+
+
+def test_bf16_shapes_the_kernels_do_not_take_are_unsupported(lib):
+    ok = ctypes.c_void_p(0x10000)
+    aw = tsp.AttnW(ok, ok, ok, ok, ok)
+    mw = tsp.MlpW(ok, ok, ok, ok, 1)
+    # dh = 64 (tensor-core attention takes dh = 128 only)
+    cfg = _cfg(S=2048, d=256, H=4, inter=512, D=4, dtype=tsp.TSP_BF16)
+    assert lib.tsp_block_fwd(ctypes.byref(cfg), ok, ctypes.byref(aw), ctypes.byref(mw), ok,
+                             None, ok, 1 << 40, None) == tsp.TSP_ERR_UNSUPPORTED
+    # chunk of 64 rows (not a multiple of the 128-row query tile)
+    cfg = _cfg(S=512, d=256, H=2, inter=512, D=4, dtype=tsp.TSP_BF16)
+    assert lib.tsp_attn_block_fwd(ctypes.byref(cfg), ok, ctypes.byref(aw), ok, ok, 1 << 40,
+                                  None) == tsp.TSP_ERR_UNSUPPORTED
+    # the MLP alone takes it
+    cfg = _cfg(S=500 * 8, d=256, H=2, inter=384, D=4, dtype=tsp.TSP_BF16)
+    assert lib.tsp_workspace_bytes(ctypes.byref(cfg), tsp.TSP_OP_MLP_FWD) > 0
+
+
+def test_workspace_sizes_are_consistent(lib):
+    cfg = _cfg(S=16384, d=4096, H=32, inter=11008, D=8, dtype=tsp.TSP_BF16)
+    S, d, I, H = 16384, 4096, 11008, 32
+    fwd = lib.tsp_workspace_bytes(ctypes.byref(cfg), tsp.TSP_OP_BLOCK_FWD)
+    saved = lib.tsp_saved_bytes(ctypes.byref(cfg))
+    # inference keeps a, Q|K|V, O, h, b, G (bf16) + rstd, LSE (fp32)
+    assert fwd >= S * (d * 2 * (1 + 3 + 1 + 1 + 1) + I * 2 + 4 * (2 + H))
+    # training additionally keeps the SwiGLU pre-activations A|B
+    assert saved - fwd >= S * 2 * I * 2
+    assert lib.tsp_workspace_bytes(ctypes.byref(cfg), tsp.TSP_OP_BLOCK_BWD) > 0

@@ -1,0 +1,253 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU float64 oracle.
+
+Every input is drawn by folded_tensor_sequence_zigzag_gb300.inputs; the GPU
+permutes it into zigzag order with its own kernel and the result is permuted
+back with its own kernel before the comparison.  The oracle never sees a GPU
+value as input.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.tsp_oracle as O
+from folded_tensor_sequence_zigzag_gb300 import tsp
+from folded_tensor_sequence_zigzag_gb300.inputs import (BlockShape, TINY_FP32, make_block_inputs,
+                                                         sample_rows)
+from tests.helpers import assert_bf16_close, assert_f32_close, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from folded_tensor_sequence_zigzag_gb300 import build
+    build.build()
+    return tsp.load()
+
+
+def _run_block(shape: BlockShape, inp: dict, dtype, mode="block", norm=True, residual=True):
+    dev = "cuda"
+    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps)
+    W = tsp.BlockWeights.from_dict(inp, dev)
+    x = inp["x"].to(dev)
+    xz = tsp.zigzag_permute(x, shape.D)
+    if mode == "block":
+        yz = tsp.block_fwd(cfg, xz, W)
+    elif mode == "attn":
+        yz = tsp.attn_block_fwd(cfg, xz, W)
+    else:
+        yz = tsp.gated_mlp_fwd(cfg, xz, W, norm=norm, residual=residual)
+    y = tsp.zigzag_permute(yz, shape.D, inverse=True)
+    torch.cuda.synchronize()
+    assert tsp.device_status() == tsp.TSP_OK
+    return y.cpu()
+
+
+# ------------------------------------------------------------------ K1 permute
+
+@pytest.mark.parametrize("S,D,cols,dtype", [(256, 4, 64, torch.float32), (2048, 8, 512, torch.bfloat16),
+                                            (48, 3, 5, torch.float32), (16, 1, 7, torch.bfloat16),
+                                            (64, 2, 3, torch.uint8), (131072, 8, 4096, torch.bfloat16)])
+def test_zigzag_permute_bit_exact(S, D, cols, dtype):
+    g = torch.Generator().manual_seed(S + D)
+    if dtype == torch.uint8:
+        x = torch.randint(0, 256, (S, cols), generator=g, dtype=torch.uint8)
+    else:
+        x = torch.randn(S, cols, generator=g).to(dtype)
+    xd = x.cuda()
+    z = tsp.zigzag_permute(xd, D).cpu()
+    pos = torch.from_numpy(O.zigzag_positions(S, D))
+    assert torch.equal(z, x[pos])
+    back = tsp.zigzag_permute(z.cuda(), D, inverse=True).cpu()
+    assert torch.equal(back, x)
+
+
+# ------------------------------------------------------------------ K2 RMSNorm
+
+@pytest.mark.parametrize("rows,n,dtype", [(300, 64, torch.float32), (1000, 4096, torch.bfloat16),
+                                          (37, 200, torch.float32), (257, 11008, torch.bfloat16),
+                                          (5, 12, torch.bfloat16)])
+def test_rmsnorm_fwd(rows, n, dtype):
+    g0 = torch.Generator().manual_seed(rows)
+    u = (torch.randn(rows, n, generator=g0) * 3).to(dtype)
+    gain = (1 + 0.5 * torch.randn(n, generator=g0)).to(dtype)
+    out, rstd = tsp.rmsnorm_fwd(u.cuda(), gain.cuda(), 1e-6, with_rstd=True)
+    ref, rref = O.rmsnorm(to64(u), to64(gain), 1e-6)
+    if dtype == torch.float32:
+        assert_f32_close(out.cpu(), ref, "rmsnorm", tol=1e-5)
+    else:
+        # one bf16 rounding of an fp32 value: |err| <= 2^-9 |ref| (+ fp32 noise), checked with 2x margin
+        err = np.abs(to64(out.cpu()) - ref)
+        assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-6), float((err / (np.abs(ref) + 1e-6)).max())
+    assert np.max(np.abs(to64(rstd.cpu()) - rref) / rref) < 1e-5
+
+
+# ------------------------------------------------------------------ fp32 tiny block (exact path)
+
+def test_tiny_fp32_block_matches_oracle():
+    inp = make_block_inputs(TINY_FP32, torch.float32, seed=0)
+    y = _run_block(TINY_FP32, inp, torch.float32)
+    ref, _ = O.block_fwd(inp["x"], inp, TINY_FP32.H, TINY_FP32.eps)
+    assert_f32_close(y, ref, "tiny fp32 block")
+
+
+@pytest.mark.parametrize("D", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_fp32_block_virtual_rank_sweep(D):
+    shape = BlockShape(S=2 * D * 16, d=64, H=4, inter=128, D=D)
+    inp = make_block_inputs(shape, torch.float32, seed=D)
+    y = _run_block(shape, inp, torch.float32)
+    ref = O.block_fwd_sharded(inp["x"], inp, shape.H, D, shape.eps)
+    assert_f32_close(y, ref, f"fp32 block D={D}")
+
+
+@pytest.mark.parametrize("D", [1, 2, 4, 8])
+def test_fp32_block_S256_rank_sweep(D):
+    shape = BlockShape(S=256, d=64, H=4, inter=128, D=D)
+    inp = make_block_inputs(shape, torch.float32, seed=0)
+    y = _run_block(shape, inp, torch.float32)
+    ref, _ = O.block_fwd(inp["x"], inp, 4, shape.eps)
+    assert_f32_close(y, ref, f"fp32 S=256 D={D}")
+
+
+def test_fp32_halves_match_oracle():
+    shape = BlockShape(S=96, d=48, H=3, inter=80, D=3)
+    inp = make_block_inputs(shape, torch.float32, seed=3)
+    h = _run_block(shape, inp, torch.float32, mode="attn")
+    href, _ = O.attn_block_fwd(inp["x"], inp, shape.H, shape.eps)
+    assert_f32_close(h, href, "fp32 attention half")
+    y = _run_block(shape, inp, torch.float32, mode="mlp", norm=False, residual=False)
+    yref = O.mlp_fwd_sharded(inp["x"], inp, shape.D, shape.eps, norm=False, residual=False)
+    assert_f32_close(y, yref, "fp32 mlp half (no norm, no residual)")
+
+
+# ------------------------------------------------------------------ bf16 tensor-core path
+
+@pytest.mark.parametrize("S,d,I,D,norm,res", [
+    (512, 256, 384, 4, False, False),     # several N and M tiles, I/D = 96 (not a 64 multiple)
+    (660, 512, 640, 3, True, True),       # ragged last M tile (660 = 5 x 128 + 20), shards 213/214
+    (384, 512, 512, 1, True, False),
+    (1000 * 2, 256, 512, 8, False, True),  # S not a multiple of 128 -> ragged M
+])
+def test_bf16_mlp_half(S, d, I, D, norm, res):
+    shape = BlockShape(S=S, d=d, H=2, inter=I, D=D)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=S + D)
+    y = _run_block(shape, inp, torch.bfloat16, mode="mlp", norm=norm, residual=res)
+    ref, _ = O.mlp_fwd(inp["x"], inp, shape.eps, norm=norm, residual=res)
+    assert_bf16_close(y, ref, f"bf16 mlp S={S} D={D}")
+
+
+@pytest.mark.parametrize("S,H,D", [(1024, 2, 4), (512, 2, 1), (2048, 4, 8), (1536, 2, 3)])
+def test_bf16_attention_half(S, H, D):
+    shape = BlockShape(S=S, d=128 * H, H=H, inter=256, D=D)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=S + H)
+    h = _run_block(shape, inp, torch.bfloat16, mode="attn")
+    ref, _ = O.attn_block_fwd(inp["x"], inp, shape.H, shape.eps)
+    assert_bf16_close(h, ref, f"bf16 attention S={S} D={D}")
+
+
+@pytest.mark.parametrize("S,H,D", [(1024, 2, 4), (2048, 2, 8), (1536, 2, 3)])
+def test_bf16_attention_dominated(S, H, D):
+    """Sharper softmax (W_Q, W_K x8) and a large W_O (x60) so that the attention
+    term, not the residual x, dominates h: checks the attention kernel itself."""
+    shape = BlockShape(S=S, d=128 * H, H=H, inter=256, D=D)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=S + 11)
+    for k, f in (("wq", 8.0), ("wk", 8.0), ("wo", 60.0)):
+        inp[k] = (inp[k].float() * f).to(torch.bfloat16)
+    h = _run_block(shape, inp, torch.bfloat16, mode="attn")
+    ref, _ = O.attn_block_fwd(inp["x"], inp, shape.H, shape.eps)
+    x = to64(inp["x"])
+    assert np.sqrt(np.mean((ref - x) ** 2)) > 2 * np.sqrt(np.mean(x ** 2))
+    assert_bf16_close(h, ref, f"attention-dominated S={S} D={D}")
+
+
+@pytest.mark.parametrize("S,d,H,I,D", [(2048, 512, 4, 1024, 4), (2048, 256, 2, 512, 8),
+                                       (1024, 256, 2, 768, 2)])
+def test_bf16_block_small(S, d, H, I, D):
+    shape = BlockShape(S=S, d=d, H=H, inter=I, D=D)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=7)
+    y = _run_block(shape, inp, torch.bfloat16)
+    ref, _ = O.block_fwd(inp["x"], inp, H, shape.eps)
+    assert_bf16_close(y, ref, f"bf16 block S={S} D={D}")
+
+
+# ------------------------------------------------------------------ the 7B-shaped workloads
+
+@pytest.mark.parametrize("S", [1024, 2048, 4096, 8192, 16384])
+def test_mlp_only_4096_11008_D4(S):
+    """SwiGLU MLP alone, d=4096, inter=11008, D=4; no norm, no residual (y = G W_2^T)."""
+    shape = BlockShape(S=S, d=4096, H=32, inter=11008, D=4)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=0, mlp_only=True)
+    dev = "cuda"
+    cfg = tsp.make_cfg(S, 4096, 32, 11008, 4, torch.bfloat16)
+    W = tsp.BlockWeights(*(inp[k].to(dev) if k in inp else torch.zeros(1, device=dev)
+                           for k in ("wq", "wk", "wv", "wo", "w1", "w3", "w2", "g_attn", "g_mlp")))
+    xz = tsp.zigzag_permute(inp["x"].to(dev), 4)
+    yz = tsp.gated_mlp_fwd(cfg, xz, W, norm=False, residual=False)
+    y = tsp.zigzag_permute(yz, 4, inverse=True).cpu()
+    assert tsp.device_status() == tsp.TSP_OK
+    rows = sample_rows(S, 4).numpy() if S > 1024 else np.arange(S)
+    ref, _ = O.mlp_fwd(inp["x"][rows], inp, shape.eps, norm=False, residual=False)
+    assert_bf16_close(y[rows], ref, f"MLP-only S={S}")
+
+
+@pytest.mark.parametrize("S", [16384, 131072])
+def test_7b_block_fwd_sampled_rows(S):
+    shape = BlockShape(S=S, d=4096, H=32, inter=11008, D=8)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=0)
+    y = _run_block(shape, inp, torch.bfloat16)
+    rows = sample_rows(S, 8).numpy()
+    assert len(rows) == 256
+    ref = O.block_fwd_rows(inp["x"], inp, shape.H, shape.eps, rows)
+    assert_bf16_close(y[rows], ref, f"7B block S={S}")
+
+
+# ------------------------------------------------------------------ backward
+
+def _run_bwd(shape, inp, dtype):
+    dev = "cuda"
+    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps)
+    W = tsp.BlockWeights.from_dict(inp, dev)
+    xz = tsp.zigzag_permute(inp["x"].to(dev), shape.D)
+    dyz = tsp.zigzag_permute(inp["dy"].to(dev), shape.D)
+    saved = torch.empty(tsp.saved_bytes(cfg), dtype=torch.uint8, device=dev)
+    yz = tsp.block_fwd(cfg, xz, W, saved=saved)
+    g = tsp.block_bwd(cfg, xz, dyz, saved, W)
+    g["dx"] = tsp.zigzag_permute(g["dx"], shape.D, inverse=True)
+    y = tsp.zigzag_permute(yz, shape.D, inverse=True)
+    torch.cuda.synchronize()
+    assert tsp.device_status() == tsp.TSP_OK
+    return y.cpu(), {k: v.cpu() for k, v in g.items()}
+
+
+def test_tiny_fp32_backward_matches_oracle():
+    inp = make_block_inputs(TINY_FP32, torch.float32, seed=0, with_dy=True)
+    y, g = _run_bwd(TINY_FP32, inp, torch.float32)
+    ref = O.block_bwd(inp["x"], inp, inp["dy"], TINY_FP32.H, TINY_FP32.eps)
+    yref, _ = O.block_fwd(inp["x"], inp, TINY_FP32.H, TINY_FP32.eps)
+    assert_f32_close(y, yref, "fwd (training)")
+    for k, v in ref.items():
+        scale = max(1.0, float(np.max(np.abs(v))))
+        assert_f32_close(g[k], v, k, tol=1e-4 * scale)
+
+
+@pytest.mark.parametrize("D", [1, 3, 8])
+def test_fp32_backward_rank_sweep(D):
+    shape = BlockShape(S=2 * D * 16, d=32, H=2, inter=48, D=D)
+    inp = make_block_inputs(shape, torch.float32, seed=10 + D, with_dy=True)
+    _, g = _run_bwd(shape, inp, torch.float32)
+    ref = O.block_bwd_sharded(inp["x"], inp, inp["dy"], shape.H, D, shape.eps)
+    for k, v in ref.items():
+        scale = max(1.0, float(np.max(np.abs(v))))
+        assert_f32_close(g[k], v, f"{k} D={D}", tol=1e-4 * scale)
+
+
+@pytest.mark.parametrize("S,d,H,I,D", [(1024, 256, 2, 512, 4), (2048, 512, 4, 768, 8)])
+def test_bf16_backward_small(S, d, H, I, D):
+    shape = BlockShape(S=S, d=d, H=H, inter=I, D=D)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=5, with_dy=True)
+    _, g = _run_bwd(shape, inp, torch.bfloat16)
+    ref = O.block_bwd(inp["x"], inp, inp["dy"], H, shape.eps)
+    for k, v in ref.items():
+        assert_bf16_close(g[k], v, f"bf16 {k}")
