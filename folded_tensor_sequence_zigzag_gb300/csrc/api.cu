@@ -180,7 +180,7 @@ int fwd_parts(const tsp_cfg* c, bool training) {
 }
 
 struct BwdWs {
-  void *dab, *dg_f32, *db, *dh_f32, *dh_t, *dO, *dqkv, *da;
+  void *dab, *dg_f32, *db, *dh_f32, *dh_t, *dO, *dqkv, *da, *dy16;
   float *delta, *dq_acc, *dg_part;
   size_t bytes;
 };
@@ -207,8 +207,62 @@ BwdWs bwd_layout(const tsp_cfg* c, uint8_t* base) {
   W.delta = (float*)take(H * S * 4);
   if (c->dtype == TSP_BF16) W.dq_acc = (float*)take(S * d * 4);
   W.dg_part = (float*)take((size_t)rmsnorm_bwd_blocks(c->S) * d * 4);
+  if (c->dtype == TSP_BF16) W.dy16 = take(S * d * 2);
   W.bytes = off;
   return W;
+}
+
+// fp16 copies of the bf16 weights (the internal tensor-core operand type);
+// refreshed from the caller's weights on every call.
+struct WCache {
+  void *wq, *wk, *wv, *wo, *w1, *w3, *w2;
+  size_t bytes;
+};
+
+enum { WC_ATTN = 1, WC_MLP = 2 };
+
+WCache wcache_layout(const tsp_cfg* c, int which, uint8_t* base) {
+  WCache W;
+  memset(&W, 0, sizeof(W));
+  if (c->dtype != TSP_BF16) return W;
+  const size_t d = (size_t)c->d, I = (size_t)c->inter;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void* {
+    void* p = base ? base + off : nullptr;
+    off += up256(bytes);
+    return p;
+  };
+  if (which & WC_ATTN) {
+    W.wq = take(d * d * 2);
+    W.wk = take(d * d * 2);
+    W.wv = take(d * d * 2);
+    W.wo = take(d * d * 2);
+  }
+  if (which & WC_MLP) {
+    W.w1 = take(I * d * 2);
+    W.w3 = take(I * d * 2);
+    W.w2 = take(d * I * 2);
+  }
+  W.bytes = off;
+  return W;
+}
+
+tsp_status fill_wcache(const tsp_cfg* c, const WCache& W, const tsp_attn_w* aw, const tsp_mlp_w* mw,
+                       cudaStream_t st) {
+  const int64_t dd = (int64_t)c->d * c->d, Id = (int64_t)c->inter * c->d;
+  tsp_status r;
+  if (W.wq) {
+    if ((r = launch_convert_bf16_f16(aw->wq, W.wq, dd, st)) != TSP_OK) return r;
+    if ((r = launch_convert_bf16_f16(aw->wk, W.wk, dd, st)) != TSP_OK) return r;
+    if ((r = launch_convert_bf16_f16(aw->wv, W.wv, dd, st)) != TSP_OK) return r;
+    if ((r = launch_convert_bf16_f16(aw->wo, W.wo, dd, st)) != TSP_OK) return r;
+  }
+  if (W.w1) {
+    if ((r = launch_convert_bf16_f16(mw->w1, W.w1, Id, st)) != TSP_OK) return r;
+    if ((r = launch_convert_bf16_f16(mw->w3, W.w3, Id, st)) != TSP_OK) return r;
+    if ((r = launch_convert_bf16_f16(mw->w2, W.w2, Id, st)) != TSP_OK) return r;
+  }
+  return TSP_OK;
 }
 
 cudaStream_t S_(void* s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -218,11 +272,14 @@ cudaStream_t S_(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 // ----------------------------------------------------------------------------
 
 // h_f32: write h in fp32 (the block's residual stream) instead of the cfg dtype.
-tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, void* h, bool h_f32,
-                     const Acts& A, cudaStream_t st) {
+// WC: fp16 weight copies (bf16 configuration; filled by the caller of this function).
+tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, const WCache& WC,
+                     void* h, bool h_f32, const Acts& A, cudaStream_t st) {
   const int64_t S = c->S;
   const int d = c->d, D = c->D;
-  tsp_status r = launch_rmsnorm_fwd(x, 0, w->g_attn, A.a, A.rstd1, S, d, c->eps, c->dtype, st);
+  tsp_status r = launch_rmsnorm_fwd(x, c->dtype == TSP_BF16 ? TY_BF16 : TY_F32, w->g_attn, A.a,
+                                    c->dtype == TSP_BF16 ? TY_F16 : TY_F32, A.rstd1, S, d, c->eps,
+                                    c->dtype, st);
   if (r != TSP_OK) return r;
   if (c->dtype == TSP_BF16) {
     // Q|K|V: the N range is split into the W_Q, W_K, W_V segments; within a
@@ -230,19 +287,20 @@ tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, void*
     TcGemm g;
     g.M = (int)S; g.N = 3 * d; g.K = d;
     g.A[0] = A.a; g.lda[0] = d; g.kseg_len[0] = d;
-    g.B[0] = w->wq; g.B[1] = w->wk; g.B[2] = w->wv;
+    g.B[0] = WC.wq; g.B[1] = WC.wk; g.B[2] = WC.wv;
     g.ldb[0] = g.ldb[1] = g.ldb[2] = d;
     g.nseg_n = d; g.name = "gemm_qkv";
-    g.epi = EPI_BF16; g.out = A.qkv; g.ldo = 3 * d;
+    g.epi = EPI_STORE; g.out_type = OUT_F16; g.out = A.qkv; g.ldo = 3 * d;
     if ((r = gemm_tc(g, st)) != TSP_OK) return r;
-    if ((r = launch_attn_fwd_bf16(A.qkv, A.o, A.lse, S, c->H, c->dh, D, st)) != TSP_OK) return r;
+    if ((r = launch_attn_fwd_f16(A.qkv, A.o, A.lse, S, c->H, c->dh, D, st)) != TSP_OK) return r;
     // W_O: split-K over the shards C_k (k = 0..D-1, broadcast order), fp32
     // accumulation in TMEM, residual x added in the epilogue.
     TcGemm o;
     o.M = (int)S; o.N = d; o.K = d;
     o.A[0] = A.o; o.lda[0] = d; o.kseg_len[0] = d;
-    o.B[0] = w->wo; o.ldb[0] = d;
-    o.epi = EPI_RES; o.res = x; o.name = "gemm_oproj"; o.ldr = d; o.out = h; o.ldo = d; o.out_f32 = h_f32;
+    o.B[0] = WC.wo; o.ldb[0] = d;
+    o.epi = EPI_RES; o.res = x; o.ldr = d; o.name = "gemm_oproj";
+    o.out = h; o.ldo = d; o.out_type = h_f32 ? OUT_F32 : OUT_BF16;
     return gemm_tc(o, st);
   }
   // exact fp32 path: literal shard loop
@@ -268,26 +326,33 @@ tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, void*
 }
 
 // hin_f32: the input h is fp32 (the block's residual stream), else the cfg dtype.
-tsp_status mlp_half(const tsp_cfg* c, const void* hin, bool hin_f32, const tsp_mlp_w* w, void* y,
-                    const Acts& A, cudaStream_t st) {
+tsp_status mlp_half(const tsp_cfg* c, const void* hin, bool hin_f32, const tsp_mlp_w* w,
+                    const WCache& WC, void* y, const Acts& A, cudaStream_t st) {
   const int64_t S = c->S;
   const int d = c->d, I = c->inter, D = c->D;
   const int64_t rows_per_rank = S / D;
   tsp_status r;
   const void* b = hin;
+  const bool bf = c->dtype == TSP_BF16;
   if (w->g_mlp) {
-    if ((r = launch_rmsnorm_fwd(hin, hin_f32 ? 1 : 0, w->g_mlp, A.b, A.rstd2, S, d, c->eps,
-                                c->dtype, st)) != TSP_OK)
+    if ((r = launch_rmsnorm_fwd(hin, bf ? (hin_f32 ? TY_F32 : TY_BF16) : TY_F32, w->g_mlp, A.b,
+                                bf ? TY_F16 : TY_F32, A.rstd2, S, d, c->eps, c->dtype, st)) !=
+        TSP_OK)
       return r;
     b = A.b;
+  } else if (bf) {
+    // no norm: the GEMM operand is h itself, in the internal fp16 type
+    if (hin_f32) return TSP_ERR_UNSUPPORTED;
+    if ((r = launch_convert_bf16_f16(hin, A.b, S * d, st)) != TSP_OK) return r;
+    b = A.b;
   }
-  if (c->dtype == TSP_BF16) {
+  if (bf) {
     // W_1|W_3: one 256-wide B tile = 128 rows of W_1 and the same 128 rows of
     // W_3 (split-N over the I_k shards); SiLU(.)*gate fused in the epilogue.
     TcGemm g;
     g.M = (int)S; g.N = I; g.K = d;
     g.A[0] = b; g.lda[0] = d; g.kseg_len[0] = d;
-    g.B[0] = w->w1; g.B[1] = w->w3; g.ldb[0] = g.ldb[1] = d;
+    g.B[0] = WC.w1; g.B[1] = WC.w3; g.ldb[0] = g.ldb[1] = d;
     g.paired = true; g.name = "gemm_w13_swiglu";
     g.epi = EPI_SWIGLU; g.out = A.g; g.ldo = I;
     if (A.ab) {
@@ -300,24 +365,24 @@ tsp_status mlp_half(const tsp_cfg* c, const void* hin, bool hin_f32, const tsp_m
     TcGemm o;
     o.M = (int)S; o.N = d; o.K = I;
     o.A[0] = A.g; o.lda[0] = I; o.kseg_len[0] = I;
-    o.B[0] = w->w2; o.ldb[0] = I;
+    o.B[0] = WC.w2; o.ldb[0] = I;
     o.rot_rows = (int)rows_per_rank; o.rot_D = D; o.name = "gemm_w2";
-    o.out = y; o.ldo = d;
+    o.out = y; o.ldo = d; o.out_type = OUT_BF16;
     if (w->add_residual) {
       o.epi = EPI_RES; o.res = hin; o.ldr = d; o.res_f32 = hin_f32;
     } else {
-      o.epi = EPI_BF16;
+      o.epi = EPI_STORE;
     }
     return gemm_tc(o, st);
   }
-  const float* bf = (const float*)b;
+  const float* bin = (const float*)b;
   float* ab = (float*)A.ab;
   for (int k = 0; k < D; ++k) {
     const int lo = (int)((int64_t)k * I / D), hi = (int)((int64_t)(k + 1) * I / D);
-    if ((r = launch_gemm_f32((int)S, hi - lo, d, bf, d, 1, (const float*)w->w1 + (int64_t)lo * d, d,
+    if ((r = launch_gemm_f32((int)S, hi - lo, d, bin, d, 1, (const float*)w->w1 + (int64_t)lo * d, d,
                              1, ab + lo, 2 * I, nullptr, 0, 0, st)) != TSP_OK)
       return r;
-    if ((r = launch_gemm_f32((int)S, hi - lo, d, bf, d, 1, (const float*)w->w3 + (int64_t)lo * d, d,
+    if ((r = launch_gemm_f32((int)S, hi - lo, d, bin, d, 1, (const float*)w->w3 + (int64_t)lo * d, d,
                              1, ab + I + lo, 2 * I, nullptr, 0, 0, st)) != TSP_OK)
       return r;
   }
@@ -394,17 +459,23 @@ tsp_status tsp_rmsnorm_fwd(const void* u, const void* g, void* out, float* rstd,
   if (!u || !g || !out || rows <= 0 || n <= 0 || (dtype != TSP_F32 && dtype != TSP_BF16) ||
       !(eps >= 0.f))
     return TSP_ERR_INVALID_ARG;
-  return launch_rmsnorm_fwd(u, 0, g, out, rstd, rows, n, eps, dtype, S_(stream));
+  const int ty = dtype == TSP_BF16 ? TY_BF16 : TY_F32;
+  return launch_rmsnorm_fwd(u, ty, g, out, ty, rstd, rows, n, eps, dtype, S_(stream));
 }
 
 size_t tsp_workspace_bytes(const tsp_cfg* cfg, int32_t op) {
   if (check_cfg(cfg) != TSP_OK) return 0;
   switch (op) {
-    case TSP_OP_ATTN_FWD: return acts_layout(cfg, PART_ATTN, nullptr).bytes;
+    case TSP_OP_ATTN_FWD:
+      return acts_layout(cfg, PART_ATTN, nullptr).bytes + wcache_layout(cfg, WC_ATTN, nullptr).bytes;
     case TSP_OP_MLP_FWD:
-      return acts_layout(cfg, PART_MLP | (cfg->dtype == TSP_F32 ? PART_AB : 0), nullptr).bytes;
-    case TSP_OP_BLOCK_FWD: return acts_layout(cfg, fwd_parts(cfg, false), nullptr).bytes;
-    case TSP_OP_BLOCK_BWD: return bwd_layout(cfg, nullptr).bytes;
+      return acts_layout(cfg, PART_MLP | (cfg->dtype == TSP_F32 ? PART_AB : 0), nullptr).bytes +
+             wcache_layout(cfg, WC_MLP, nullptr).bytes;
+    case TSP_OP_BLOCK_FWD:
+      return acts_layout(cfg, fwd_parts(cfg, false), nullptr).bytes +
+             wcache_layout(cfg, WC_ATTN | WC_MLP, nullptr).bytes;
+    case TSP_OP_BLOCK_BWD:
+      return bwd_layout(cfg, nullptr).bytes + wcache_layout(cfg, WC_ATTN | WC_MLP, nullptr).bytes;
   }
   return 0;
 }
@@ -421,10 +492,13 @@ tsp_status tsp_attn_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_att
   if ((r = check_attn_w(w)) != TSP_OK) return r;
   if (!al16(x_z) || !al16(h_z)) return TSP_ERR_INVALID_ARG;
   if ((r = check_bf16_attn(cfg)) != TSP_OK) return r;
-  const Acts A0 = acts_layout(cfg, PART_ATTN, nullptr);
-  if (!al16(ws) || ws_bytes < A0.bytes) return TSP_ERR_INVALID_ARG;
+  const size_t na = acts_layout(cfg, PART_ATTN, nullptr).bytes;
+  if (!al16(ws) || ws_bytes < tsp_workspace_bytes(cfg, TSP_OP_ATTN_FWD)) return TSP_ERR_INVALID_ARG;
   const Acts A = acts_layout(cfg, PART_ATTN, (uint8_t*)ws);
-  return attn_half(cfg, x_z, w, h_z, false, A, S_(stream));
+  const WCache WC = wcache_layout(cfg, WC_ATTN, (uint8_t*)ws + na);
+  cudaStream_t st = S_(stream);
+  if ((r = fill_wcache(cfg, WC, w, nullptr, st)) != TSP_OK) return r;
+  return attn_half(cfg, x_z, w, WC, h_z, false, A, st);
 }
 
 tsp_status tsp_gated_mlp_fwd(const tsp_cfg* cfg, const void* h_z, const tsp_mlp_w* w, void* y_z,
@@ -435,10 +509,13 @@ tsp_status tsp_gated_mlp_fwd(const tsp_cfg* cfg, const void* h_z, const tsp_mlp_
   if (!al16(h_z) || !al16(y_z)) return TSP_ERR_INVALID_ARG;
   if ((r = check_bf16_mlp(cfg)) != TSP_OK) return r;
   const int parts = PART_MLP | (cfg->dtype == TSP_F32 ? PART_AB : 0);
-  const Acts A0 = acts_layout(cfg, parts, nullptr);
-  if (!al16(ws) || ws_bytes < A0.bytes) return TSP_ERR_INVALID_ARG;
+  const size_t na = acts_layout(cfg, parts, nullptr).bytes;
+  if (!al16(ws) || ws_bytes < tsp_workspace_bytes(cfg, TSP_OP_MLP_FWD)) return TSP_ERR_INVALID_ARG;
   const Acts A = acts_layout(cfg, parts, (uint8_t*)ws);
-  return mlp_half(cfg, h_z, false, w, y_z, A, S_(stream));
+  const WCache WC = wcache_layout(cfg, WC_MLP, (uint8_t*)ws + na);
+  cudaStream_t st = S_(stream);
+  if ((r = fill_wcache(cfg, WC, nullptr, w, st)) != TSP_OK) return r;
+  return mlp_half(cfg, h_z, false, w, WC, y_z, A, st);
 }
 
 tsp_status tsp_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* aw,
@@ -453,18 +530,25 @@ tsp_status tsp_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* 
   if ((r = check_bf16_mlp(cfg)) != TSP_OK) return r;
   const bool training = saved != nullptr;
   const int parts = fwd_parts(cfg, training);
-  uint8_t* base;
+  const size_t nwc = wcache_layout(cfg, WC_ATTN | WC_MLP, nullptr).bytes;
+  uint8_t *abase, *wbase;
   if (training) {
+    // activations go to `saved`; the workspace holds the fp16 weight copies
     if (!al16(saved)) return TSP_ERR_INVALID_ARG;
-    base = (uint8_t*)saved;
+    if (nwc > 0 && (!al16(ws) || ws_bytes < nwc)) return TSP_ERR_INVALID_ARG;
+    abase = (uint8_t*)saved;
+    wbase = (uint8_t*)ws;
   } else {
-    if (!al16(ws) || ws_bytes < acts_layout(cfg, parts, nullptr).bytes) return TSP_ERR_INVALID_ARG;
-    base = (uint8_t*)ws;
+    if (!al16(ws) || ws_bytes < tsp_workspace_bytes(cfg, TSP_OP_BLOCK_FWD)) return TSP_ERR_INVALID_ARG;
+    abase = (uint8_t*)ws;
+    wbase = (uint8_t*)ws + acts_layout(cfg, parts, nullptr).bytes;
   }
-  const Acts A = acts_layout(cfg, parts, base);
+  const Acts A = acts_layout(cfg, parts, abase);
+  const WCache WC = wcache_layout(cfg, WC_ATTN | WC_MLP, wbase);
   cudaStream_t st = S_(stream);
-  if ((r = attn_half(cfg, x_z, aw, A.h, true, A, st)) != TSP_OK) return r;
-  return mlp_half(cfg, A.h, true, mw, y_z, A, st);
+  if ((r = fill_wcache(cfg, WC, aw, mw, st)) != TSP_OK) return r;
+  if ((r = attn_half(cfg, x_z, aw, WC, A.h, true, A, st)) != TSP_OK) return r;
+  return mlp_half(cfg, A.h, true, mw, WC, y_z, A, st);
 }
 
 tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z, const void* saved,
@@ -481,7 +565,7 @@ tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z, 
     if (!al16(p)) return TSP_ERR_INVALID_ARG;
   if ((r = check_bf16_attn(cfg)) != TSP_OK) return r;
   if ((r = check_bf16_mlp(cfg)) != TSP_OK) return r;
-  if (!al16(ws) || ws_bytes < bwd_layout(cfg, nullptr).bytes) return TSP_ERR_INVALID_ARG;
+  if (!al16(ws) || ws_bytes < tsp_workspace_bytes(cfg, TSP_OP_BLOCK_BWD)) return TSP_ERR_INVALID_ARG;
   return block_bwd_impl(cfg, x_z, dy_z, saved, aw, mw, dx_z, dwq, dwk, dwv, dwo, dw1, dw3, dw2,
                         dg_attn, dg_mlp, ws, S_(stream));
 }
@@ -560,12 +644,16 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
   tsp_status r;
   if (c->dtype == TSP_BF16) {
     const size_t e = 2;
+    const WCache WC = wcache_layout(c, WC_ATTN | WC_MLP, (uint8_t*)ws + W.bytes);
+    if ((r = fill_wcache(c, WC, aw, mw, st)) != TSP_OK) return r;
+    // the upstream gradient in the internal fp16 operand type
+    if ((r = launch_convert_bf16_f16(dy, W.dy16, S * d, st)) != TSP_OK) return r;
     // dA|dB = SwiGLU'(dG), dG = dy W_2   (B operand W_2 read MN-major)
     {
       TcGemm g;
       g.M = (int)S; g.N = I; g.K = d;
-      g.A[0] = dy; g.lda[0] = d; g.kseg_len[0] = d;
-      g.b_mn = true; g.B[0] = mw->w2; g.ldb[0] = I;
+      g.A[0] = W.dy16; g.lda[0] = d; g.kseg_len[0] = d;
+      g.b_mn = true; g.B[0] = WC.w2; g.ldb[0] = I;
       g.epi = EPI_SWIGLU_BWD; g.name = "gemm_dgrad_w2_swiglu";
       g.e1 = A.ab; g.e2 = (uint8_t*)A.ab + (size_t)I * e; g.lde = 2 * (int64_t)I;
       g.out = W.dab; g.ldo = 2 * (int64_t)I;
@@ -576,7 +664,7 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
     {
       TcGemm g;
       g.M = d; g.N = I; g.K = (int)S;
-      g.a_mn = true; g.A[0] = dy; g.lda[0] = d; g.kseg_len[0] = (int)S;
+      g.a_mn = true; g.A[0] = W.dy16; g.lda[0] = d; g.kseg_len[0] = (int)S;
       g.b_mn = true; g.B[0] = A.g; g.ldb[0] = I;
       g.epi = EPI_F32; g.out = dw2; g.ldo = I; g.name = "gemm_wgrad_w2";
       if ((r = gemm_tc(g, st)) != TSP_OK) return r;
@@ -587,7 +675,8 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
       g.M = 2 * I; g.N = d; g.K = (int)S;
       g.a_mn = true; g.A[0] = W.dab; g.lda[0] = 2 * (int64_t)I; g.kseg_len[0] = (int)S;
       g.b_mn = true; g.B[0] = A.b; g.ldb[0] = d;
-      g.epi = EPI_F32; g.ldo = d; g.m_seg = I; g.name = "gemm_wgrad_w13"; g.outs[0] = dw1; g.outs[1] = dw3;
+      g.epi = EPI_F32; g.ldo = d; g.m_seg = I; g.name = "gemm_wgrad_w13";
+      g.outs[0] = dw1; g.outs[1] = dw3;
       if ((r = gemm_tc(g, st)) != TSP_OK) return r;
     }
     // db = dA W_1 + dB W_3 (two K segments), fp32
@@ -598,14 +687,14 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
       g.A[0] = W.dab; g.A[1] = (uint8_t*)W.dab + (size_t)I * e;
       g.lda[0] = g.lda[1] = 2 * (int64_t)I;
       g.kseg_len[0] = g.kseg_len[1] = I;
-      g.b_mn = true; g.B[0] = mw->w1; g.B[1] = mw->w3; g.ldb[0] = g.ldb[1] = d;
+      g.b_mn = true; g.B[0] = WC.w1; g.B[1] = WC.w3; g.ldb[0] = g.ldb[1] = d;
       g.epi = EPI_F32; g.out = W.db; g.ldo = d; g.name = "gemm_dgrad_w13";
       if ((r = gemm_tc(g, st)) != TSP_OK) return r;
     }
-    // dh = dy + RMSNorm_2'(db)
-    if ((r = launch_rmsnorm_bwd((const float*)W.db, A.h, 1, mw->g_mlp, A.rstd2, nullptr, dy,
-                                (float*)W.dh_f32, W.dh_t, dg_mlp, W.dg_part, S, d, c->dtype, st)) !=
-        TSP_OK)
+    // dh = dy + RMSNorm_2'(db)   (fp32, plus an fp16 copy for the GEMMs)
+    if ((r = launch_rmsnorm_bwd((const float*)W.db, A.h, TY_F32, mw->g_mlp, A.rstd2, nullptr, dy,
+                                (float*)W.dh_f32, W.dh_t, TY_F16, dg_mlp, W.dg_part, S, d,
+                                c->dtype, st)) != TSP_OK)
       return r;
     // dW_O = dh^T O
     {
@@ -621,12 +710,12 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
       TcGemm g;
       g.M = (int)S; g.N = d; g.K = d;
       g.A[0] = W.dh_t; g.lda[0] = d; g.kseg_len[0] = d;
-      g.b_mn = true; g.B[0] = aw->wo; g.ldb[0] = d;
-      g.epi = EPI_BF16; g.out = W.dO; g.ldo = d; g.name = "gemm_dgrad_wo";
+      g.b_mn = true; g.B[0] = WC.wo; g.ldb[0] = d;
+      g.epi = EPI_STORE; g.out_type = OUT_F16; g.out = W.dO; g.ldo = d; g.name = "gemm_dgrad_wo";
       if ((r = gemm_tc(g, st)) != TSP_OK) return r;
     }
-    if ((r = launch_attn_bwd_bf16(A.qkv, A.o, W.dO, A.lse, W.delta, W.dq_acc, W.dqkv, S, H, dh, D,
-                                  st)) != TSP_OK)
+    if ((r = launch_attn_bwd_f16(A.qkv, A.o, W.dO, A.lse, W.delta, W.dq_acc, W.dqkv, S, H, dh, D,
+                                 st)) != TSP_OK)
       return r;
     // dW_Q | dW_K | dW_V = [dQ | dK | dV]^T a
     {
@@ -634,7 +723,8 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
       g.M = 3 * d; g.N = d; g.K = (int)S;
       g.a_mn = true; g.A[0] = W.dqkv; g.lda[0] = 3 * (int64_t)d; g.kseg_len[0] = (int)S;
       g.b_mn = true; g.B[0] = A.a; g.ldb[0] = d;
-      g.epi = EPI_F32; g.ldo = d; g.m_seg = d; g.name = "gemm_wgrad_qkv"; g.outs[0] = dwq; g.outs[1] = dwk; g.outs[2] = dwv;
+      g.epi = EPI_F32; g.ldo = d; g.m_seg = d; g.name = "gemm_wgrad_qkv";
+      g.outs[0] = dwq; g.outs[1] = dwk; g.outs[2] = dwv;
       if ((r = gemm_tc(g, st)) != TSP_OK) return r;
     }
     // da = dQ W_Q + dK W_K + dV W_V (three K segments), fp32
@@ -642,7 +732,7 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
       TcGemm g;
       g.M = (int)S; g.N = d; g.K = 3 * d;
       g.nks = 3;
-      const void* ws3[3] = {aw->wq, aw->wk, aw->wv};
+      const void* ws3[3] = {WC.wq, WC.wk, WC.wv};
       for (int j = 0; j < 3; ++j) {
         g.A[j] = (uint8_t*)W.dqkv + (size_t)j * d * e;
         g.lda[j] = 3 * (int64_t)d;
@@ -655,8 +745,9 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
       if ((r = gemm_tc(g, st)) != TSP_OK) return r;
     }
     // dx = dh + RMSNorm_1'(da)
-    return launch_rmsnorm_bwd((const float*)W.da, x, 0, aw->g_attn, A.rstd1, (const float*)W.dh_f32,
-                              nullptr, nullptr, dx, dg_attn, W.dg_part, S, d, c->dtype, st);
+    return launch_rmsnorm_bwd((const float*)W.da, x, TY_BF16, aw->g_attn, A.rstd1,
+                              (const float*)W.dh_f32, nullptr, nullptr, dx, TY_BF16, dg_attn,
+                              W.dg_part, S, d, c->dtype, st);
   }
 
   // ------------------------------------------------------------ exact fp32
@@ -690,8 +781,8 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
                            nullptr, 0, 1, st)) != TSP_OK)
     return r;
   float* dhf = (float*)W.dh_f32;
-  if ((r = launch_rmsnorm_bwd(db, A.h, 1, mw->g_mlp, A.rstd2, dyf, nullptr, dhf, nullptr, dg_mlp,
-                              W.dg_part, S, d, c->dtype, st)) != TSP_OK)
+  if ((r = launch_rmsnorm_bwd(db, A.h, TY_F32, mw->g_mlp, A.rstd2, dyf, nullptr, dhf, nullptr,
+                              TY_F32, dg_mlp, W.dg_part, S, d, c->dtype, st)) != TSP_OK)
     return r;
   for (int rr = 0; rr < D; ++rr) {
     const int64_t r0 = rr * R;
@@ -724,8 +815,8 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
                              j > 0, st)) != TSP_OK)
       return r;
   }
-  return launch_rmsnorm_bwd(da, x, 0, aw->g_attn, A.rstd1, dhf, nullptr, (float*)dx, nullptr, dg_attn,
-                            W.dg_part, S, d, c->dtype, st);
+  return launch_rmsnorm_bwd(da, x, TY_F32, aw->g_attn, A.rstd1, dhf, nullptr, (float*)dx, nullptr,
+                            TY_F32, dg_attn, W.dg_part, S, d, c->dtype, st);
 }
 
 }  // namespace tsp

@@ -1,4 +1,5 @@
-// attn_bwd.cu -- causal flash-attention backward over the zigzag layout (bf16).
+// attn_bwd.cu -- causal flash-attention backward over the zigzag layout (fp16
+// tensor-core operands, fp32 accumulation).
 //
 // Source: "Folding Tensor and Sequence Parallelism for Memory-Efficient
 // Transformer Training & Inference" (gist.science summary), section 2: the
@@ -16,7 +17,7 @@
 // Per CTA: 8 warps, warp w owns keys 16w..16w+15 of the tile and keeps its
 // dK, dV accumulators in registers; S^T and dP^T are computed key-major on
 // mma.sync m16n8k16; dS goes through shared memory for dQ, which is
-// accumulated in fp32 with vector atomics and converted to bf16 at the end.
+// accumulated in fp32 with vector atomics and converted to fp16 at the end.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -58,15 +59,15 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void load_rows(uint32_t sdst, const __nv_bfloat16* g, int64_t ld,
+__device__ __forceinline__ void load_rows(uint32_t sdst, const ct_t* g, int64_t ld,
                                           int nrows) {
   for (int i = threadIdx.x; i < nrows * 16; i += NTHR) {
     const int row = i >> 4, ch = i & 15;
@@ -75,12 +76,12 @@ __device__ __forceinline__ void load_rows(uint32_t sdst, const __nv_bfloat16* g,
 }
 
 struct BwdArgs {
-  const __nv_bfloat16* qkv;  // [S, 3d]
-  const __nv_bfloat16* dO;   // [S, d]
+  const ct_t* qkv;  // [S, 3d]
+  const ct_t* dO;   // [S, d]
   const float* lse;          // [H, S] natural log
   const float* delta;        // [H, S]
   float* dq_acc;             // [S, d] fp32, zeroed
-  __nv_bfloat16* dqkv;       // [S, 3d]: dK, dV written here
+  ct_t* dqkv;       // [S, 3d]: dK, dV written here
   int64_t S, c;
   int D, d, n_kt;            // n_kt = c / 128
   float scale, scale_log2;
@@ -94,7 +95,7 @@ __device__ void key_tile(const BwdArgs& a, int h, int64_t k0, uint8_t* smem) {
   float* sL = reinterpret_cast<float*>(smem + OFF_L);   // [2][64]
   float* sDl = sL + 2 * BR;                             // [2][64]
   const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
-  const __nv_bfloat16* kg = a.qkv + krow0 * ld + a.d + h * DH;
+  const ct_t* kg = a.qkv + krow0 * ld + a.d + h * DH;
   const int nq = (int)((a.S - k0) / BR);
 
   auto load_q = [&](int j, int b) {
@@ -154,11 +155,11 @@ __device__ void key_tile(const BwdArgs& a, int h, int64_t k0, uint8_t* smem) {
           const int q = np * 16 + (lane & 7) + ((lane >> 4) << 3);
           const int bc = ks * 16 + ((lane >> 3) & 1) * 8;
           ldsm_x4(sQ + swz(q, bc), b0, b1, b2, b3);
-          mma_bf16(st[2 * np], ka, b0, b1);
-          mma_bf16(st[2 * np + 1], ka, b2, b3);
+          mma_f16(st[2 * np], ka, b0, b1);
+          mma_f16(st[2 * np + 1], ka, b2, b3);
           ldsm_x4(sdO + swz(q, bc), b0, b1, b2, b3);
-          mma_bf16(dp[2 * np], va, b0, b1);
-          mma_bf16(dp[2 * np + 1], va, b2, b3);
+          mma_f16(dp[2 * np], va, b0, b1);
+          mma_f16(dp[2 * np + 1], va, b2, b3);
         }
       }
       // P^T and dS^T in place (st -> P, dp -> dS)
@@ -182,44 +183,44 @@ __device__ void key_tile(const BwdArgs& a, int h, int64_t k0, uint8_t* smem) {
       // dV += P^T dO ; dK += dS^T Q   (k-dimension = 64 queries)
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        const uint32_t pa[4] = {pack_bf16(st[2 * ks][0], st[2 * ks][1]),
-                                pack_bf16(st[2 * ks][2], st[2 * ks][3]),
-                                pack_bf16(st[2 * ks + 1][0], st[2 * ks + 1][1]),
-                                pack_bf16(st[2 * ks + 1][2], st[2 * ks + 1][3])};
-        const uint32_t da[4] = {pack_bf16(dp[2 * ks][0], dp[2 * ks][1]),
-                                pack_bf16(dp[2 * ks][2], dp[2 * ks][3]),
-                                pack_bf16(dp[2 * ks + 1][0], dp[2 * ks + 1][1]),
-                                pack_bf16(dp[2 * ks + 1][2], dp[2 * ks + 1][3])};
+        const uint32_t pa[4] = {pack_f16(st[2 * ks][0], st[2 * ks][1]),
+                                pack_f16(st[2 * ks][2], st[2 * ks][3]),
+                                pack_f16(st[2 * ks + 1][0], st[2 * ks + 1][1]),
+                                pack_f16(st[2 * ks + 1][2], st[2 * ks + 1][3])};
+        const uint32_t da[4] = {pack_f16(dp[2 * ks][0], dp[2 * ks][1]),
+                                pack_f16(dp[2 * ks][2], dp[2 * ks][3]),
+                                pack_f16(dp[2 * ks + 1][0], dp[2 * ks + 1][1]),
+                                pack_f16(dp[2 * ks + 1][2], dp[2 * ks + 1][3])};
         const int q = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
         for (int dpi = 0; dpi < 8; ++dpi) {
           uint32_t b0, b1, b2, b3;
           const int col = dpi * 16 + (lane >> 4) * 8;
           ldsm_x4_t(sdO + swz(q, col), b0, b1, b2, b3);
-          mma_bf16(dv[2 * dpi], pa, b0, b1);
-          mma_bf16(dv[2 * dpi + 1], pa, b2, b3);
+          mma_f16(dv[2 * dpi], pa, b0, b1);
+          mma_f16(dv[2 * dpi + 1], pa, b2, b3);
           ldsm_x4_t(sQ + swz(q, col), b0, b1, b2, b3);
-          mma_bf16(dk[2 * dpi], da, b0, b1);
-          mma_bf16(dk[2 * dpi + 1], da, b2, b3);
+          mma_f16(dk[2 * dpi], da, b0, b1);
+          mma_f16(dk[2 * dpi + 1], da, b2, b3);
         }
       }
       // dS (query-major) into shared memory for dQ
-      __nv_bfloat16* ds = reinterpret_cast<__nv_bfloat16*>(smem + OFF_DS);
+      ct_t* ds = reinterpret_cast<ct_t*>(smem + OFF_DS);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int ql = i * 8 + (lane & 3) * 2 + e;
           const int kl = warp * 16 + (lane >> 2);
-          ds[swz(ql, kl) >> 1] = __float2bfloat16_rn(dp[i][e]);
-          ds[swz(ql, kl + 8) >> 1] = __float2bfloat16_rn(dp[i][2 + e]);
+          ds[swz(ql, kl) >> 1] = __float2half_rn(dp[i][e]);
+          ds[swz(ql, kl + 8) >> 1] = __float2half_rn(dp[i][2 + e]);
         }
       }
     } else {
-      __nv_bfloat16* ds = reinterpret_cast<__nv_bfloat16*>(smem + OFF_DS);
+      ct_t* ds = reinterpret_cast<ct_t*>(smem + OFF_DS);
       for (int i = lane; i < BR * 16; i += 32) {
         const int ql = i >> 4, kl = warp * 16 + (i & 15);
-        ds[swz(ql, kl) >> 1] = __float2bfloat16_rn(0.f);
+        ds[swz(ql, kl) >> 1] = __float2half_rn(0.f);
       }
     }
     __syncthreads();
@@ -239,8 +240,8 @@ __device__ void key_tile(const BwdArgs& a, int h, int64_t k0, uint8_t* smem) {
         for (int dpi = 0; dpi < 4; ++dpi) {
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(sK + swz(key, cw + dpi * 16 + (lane >> 4) * 8), b0, b1, b2, b3);
-          mma_bf16(acc[2 * dpi], af, b0, b1);
-          mma_bf16(acc[2 * dpi + 1], af, b2, b3);
+          mma_f16(acc[2 * dpi], af, b0, b1);
+          mma_f16(acc[2 * dpi + 1], af, b2, b3);
         }
       }
       const int64_t qrow = zz_row_of_pos(q0, a.c, a.D) + qw + (lane >> 2);
@@ -257,17 +258,17 @@ __device__ void key_tile(const BwdArgs& a, int h, int64_t k0, uint8_t* smem) {
     cp_async_wait_all();
     __syncthreads();
   }
-  // dK (scaled), dV -> bf16 rows of the key tile
+  // dK (scaled), dV -> fp16 rows of the key tile
   const int64_t row_lo = krow0 + warp * 16 + (lane >> 2), row_hi = row_lo + 8;
-  __nv_bfloat16* dk_lo = a.dqkv + row_lo * ld + a.d + h * DH;
-  __nv_bfloat16* dk_hi = a.dqkv + row_hi * ld + a.d + h * DH;
+  ct_t* dk_lo = a.dqkv + row_lo * ld + a.d + h * DH;
+  ct_t* dk_hi = a.dqkv + row_hi * ld + a.d + h * DH;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int col = i * 8 + (lane & 3) * 2;
-    *reinterpret_cast<uint32_t*>(dk_lo + col) = pack_bf16(dk[i][0] * a.scale, dk[i][1] * a.scale);
-    *reinterpret_cast<uint32_t*>(dk_hi + col) = pack_bf16(dk[i][2] * a.scale, dk[i][3] * a.scale);
-    *reinterpret_cast<uint32_t*>(dk_lo + a.d + col) = pack_bf16(dv[i][0], dv[i][1]);
-    *reinterpret_cast<uint32_t*>(dk_hi + a.d + col) = pack_bf16(dv[i][2], dv[i][3]);
+    *reinterpret_cast<uint32_t*>(dk_lo + col) = pack_f16(dk[i][0] * a.scale, dk[i][1] * a.scale);
+    *reinterpret_cast<uint32_t*>(dk_hi + col) = pack_f16(dk[i][2] * a.scale, dk[i][3] * a.scale);
+    *reinterpret_cast<uint32_t*>(dk_lo + a.d + col) = pack_f16(dv[i][0], dv[i][1]);
+    *reinterpret_cast<uint32_t*>(dk_hi + a.d + col) = pack_f16(dv[i][2], dv[i][3]);
   }
   __syncthreads();
 }
@@ -284,8 +285,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_zigzag_kernel(const BwdArgs 
 }
 
 // Delta[h][row] = dO[row, head h] . O[row, head h]  (warp per row and head)
-__global__ void attn_delta_kernel(const __nv_bfloat16* __restrict__ o,
-                                  const __nv_bfloat16* __restrict__ dO, float* __restrict__ delta,
+__global__ void attn_delta_kernel(const ct_t* __restrict__ o,
+                                  const ct_t* __restrict__ dO, float* __restrict__ delta,
                                   int64_t S, int H, int d) {
   const int lane = threadIdx.x & 31;
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -294,15 +295,15 @@ __global__ void attn_delta_kernel(const __nv_bfloat16* __restrict__ o,
     const int h = (int)(w - row * H);
     const uint2 ov = *reinterpret_cast<const uint2*>(o + row * d + h * DH + lane * 4);
     const uint2 gv = *reinterpret_cast<const uint2*>(dO + row * d + h * DH + lane * 4);
-    float s = bf16_lo(ov.x) * bf16_lo(gv.x) + bf16_hi(ov.x) * bf16_hi(gv.x) +
-              bf16_lo(ov.y) * bf16_lo(gv.y) + bf16_hi(ov.y) * bf16_hi(gv.y);
+    float s = f16_lo(ov.x) * f16_lo(gv.x) + f16_hi(ov.x) * f16_hi(gv.x) +
+              f16_lo(ov.y) * f16_lo(gv.y) + f16_hi(ov.y) * f16_hi(gv.y);
     s = warp_sum(s);
     if (lane == 0) delta[(int64_t)h * S + row] = s;
   }
 }
 
-// dQKV[:, 0:d] = bf16(dq_acc)
-__global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dqkv,
+// dQKV[:, 0:d] = fp16(dq_acc)
+__global__ void dq_convert_kernel(const float* __restrict__ acc, ct_t* __restrict__ dqkv,
                                   int64_t S, int d) {
   const int64_t total4 = S * d / 4;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total4;
@@ -312,15 +313,15 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* 
     const int col = (int)(e - row * d);
     const float4 v = reinterpret_cast<const float4*>(acc)[t];
     uint2 o;
-    o.x = pack_bf16(v.x, v.y);
-    o.y = pack_bf16(v.z, v.w);
+    o.x = pack_f16(v.x, v.y);
+    o.y = pack_f16(v.z, v.w);
     *reinterpret_cast<uint2*>(dqkv + row * 3 * (int64_t)d + col) = o;
   }
 }
 
 }  // namespace
 
-tsp_status launch_attn_bwd_bf16(const void* qkv, const void* o, const void* dO, const float* lse,
+tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, const float* lse,
                                 float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int dh,
                                 int D, cudaStream_t st) {
   if (dh != DH) return TSP_ERR_UNSUPPORTED;
@@ -329,18 +330,18 @@ tsp_status launch_attn_bwd_bf16(const void* qkv, const void* o, const void* dO, 
   const int d = H * dh;
   {
   Prof prof("attn_bwd_prep", st);
-  attn_delta_kernel<<<num_sms() * 8, 256, 0, st>>>((const __nv_bfloat16*)o,
-                                                   (const __nv_bfloat16*)dO, delta, S, H, d);
+  attn_delta_kernel<<<num_sms() * 8, 256, 0, st>>>((const ct_t*)o,
+                                                   (const ct_t*)dO, delta, S, H, d);
   TSP_CUDA_TRY(cudaGetLastError());
   TSP_CUDA_TRY(cudaMemsetAsync(dq_acc, 0, (size_t)S * d * sizeof(float), st));
   }
   BwdArgs a;
-  a.qkv = (const __nv_bfloat16*)qkv;
-  a.dO = (const __nv_bfloat16*)dO;
+  a.qkv = (const ct_t*)qkv;
+  a.dO = (const ct_t*)dO;
   a.lse = lse;
   a.delta = delta;
   a.dq_acc = dq_acc;
-  a.dqkv = (__nv_bfloat16*)dqkv;
+  a.dqkv = (ct_t*)dqkv;
   a.S = S;
   a.c = c;
   a.D = D;
@@ -361,7 +362,7 @@ tsp_status launch_attn_bwd_bf16(const void* qkv, const void* o, const void* dO, 
     TSP_CUDA_TRY(cudaGetLastError());
   }
   Prof prof("attn_bwd_dq_convert", st);
-  dq_convert_kernel<<<num_sms() * 8, 256, 0, st>>>(dq_acc, (__nv_bfloat16*)dqkv, S, d);
+  dq_convert_kernel<<<num_sms() * 8, 256, 0, st>>>(dq_acc, (ct_t*)dqkv, S, d);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }

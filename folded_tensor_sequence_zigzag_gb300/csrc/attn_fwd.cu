@@ -1,4 +1,5 @@
-// attn_fwd.cu -- causal flash-attention forward over the zigzag layout (bf16).
+// attn_fwd.cu -- causal flash-attention forward over the zigzag layout (fp16
+// tensor-core operands, fp32 softmax and accumulation).
 //
 // Source: "Folding Tensor and Sequence Parallelism for Memory-Efficient
 // Transformer Training & Inference" (gist.science summary), section 2,
@@ -15,7 +16,7 @@
 // 64-key tiles on the diagonal are masked element-wise.
 //
 // Inner loop (per warp: 16 query rows, dh = 128; per CTA: 8 warps, 128 rows):
-// S = Q K^T on mma.sync m16n8k16 bf16 -> fp32, online softmax in the log2
+// S = Q K^T on mma.sync m16n8k16 fp16 -> fp32, online softmax in the log2
 // domain with exp2f, O += P V with P re-packed from the accumulator
 // registers.  K/V tiles (64 keys) are double-buffered with cp.async.
 #include "common.cuh"
@@ -31,7 +32,7 @@ constexpr int SQ_BYTES = BQ * TILE_ROW_BYTES;
 constexpr int SKV_BYTES = BKV * TILE_ROW_BYTES;
 constexpr int SMEM = SQ_BYTES + 4 * SKV_BYTES;  // Q + 2 x (K, V)
 
-// byte offset of (row, col) in a [rows][128] bf16 tile, 16-byte chunks XOR-swizzled by row
+// byte offset of (row, col) in a [rows][128] 16-bit tile, 16-byte chunks XOR-swizzled by row
 __device__ __forceinline__ uint32_t swz(int row, int col) {
   return (uint32_t)(row * TILE_ROW_BYTES + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
 }
@@ -55,17 +56,17 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// rows [0, nrows) x 128 bf16 columns from global (row stride ld elements) into a swizzled tile
-__device__ __forceinline__ void load_tile(uint32_t sdst, const __nv_bfloat16* g, int64_t ld,
+// rows [0, nrows) x 128 16-bit columns from global (row stride ld elements) into a swizzled tile
+__device__ __forceinline__ void load_tile(uint32_t sdst, const ct_t* g, int64_t ld,
                                           int nrows) {
   for (int i = threadIdx.x; i < nrows * 16; i += NTHR) {
     const int row = i >> 4, ch = i & 15;
@@ -74,8 +75,8 @@ __device__ __forceinline__ void load_tile(uint32_t sdst, const __nv_bfloat16* g,
 }
 
 struct AttnArgs {
-  const __nv_bfloat16* qkv;  // [S, 3d]
-  __nv_bfloat16* o;          // [S, d]
+  const ct_t* qkv;  // [S, 3d]
+  ct_t* o;          // [S, d]
   float* lse;                // [H, S]
   int64_t S;
   int64_t c;
@@ -90,7 +91,7 @@ __device__ void attend_tile(const AttnArgs& a, int h, int64_t p0, uint8_t* smem)
   const uint32_t sK0 = sQ + SQ_BYTES;
   // buffer b: K at sK0 + b*2*SKV, V at +SKV
   const int64_t qrow0 = zz_row_of_pos(p0, a.c, a.D);
-  const __nv_bfloat16* qg = a.qkv + qrow0 * ld + h * DH;
+  const ct_t* qg = a.qkv + qrow0 * ld + h * DH;
   const int nt = (int)((p0 + BQ) / BKV);
 
   auto kv_src = [&](int j) {
@@ -99,7 +100,7 @@ __device__ void attend_tile(const AttnArgs& a, int h, int64_t p0, uint8_t* smem)
   };
   load_tile(sQ, qg, ld, BQ);
   {
-    const __nv_bfloat16* ks = kv_src(0);
+    const ct_t* ks = kv_src(0);
     load_tile(sK0, ks, ld, BKV);
     load_tile(sK0 + SKV_BYTES, ks + a.d, ld, BKV);
   }
@@ -129,7 +130,7 @@ __device__ void attend_tile(const AttnArgs& a, int h, int64_t p0, uint8_t* smem)
     const uint32_t sV = sK + SKV_BYTES;
     if (j + 1 < nt) {
       const uint32_t nK = sK0 + (uint32_t)((j + 1) & 1) * 2 * SKV_BYTES;
-      const __nv_bfloat16* ks = kv_src(j + 1);
+      const ct_t* ks = kv_src(j + 1);
       load_tile(nK, ks, ld, BKV);
       load_tile(nK + SKV_BYTES, ks + a.d, ld, BKV);
     }
@@ -147,8 +148,8 @@ __device__ void attend_tile(const AttnArgs& a, int h, int64_t p0, uint8_t* smem)
           const int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
           const int col = ks * 16 + ((lane >> 3) & 1) * 8;
           ldsm_x4(sK + swz(key, col), b0, b1, b2, b3);
-          mma_bf16(s[2 * np], qf[ks], b0, b1);
-          mma_bf16(s[2 * np + 1], qf[ks], b2, b3);
+          mma_f16(s[2 * np], qf[ks], b0, b1);
+          mma_f16(s[2 * np + 1], qf[ks], b2, b3);
         }
       }
       const bool diag = k0 + BKV - 1 > wq0;
@@ -186,8 +187,8 @@ __device__ void attend_tile(const AttnArgs& a, int h, int64_t p0, uint8_t* smem)
         sum_lo += p0v + p1v;
         sum_hi += p2v + p3v;
         // C fragment of n-tile i -> A fragment of k-step i/2
-        pf[i >> 1][(i & 1) * 2 + 0] = pack_bf16(p0v, p1v);
-        pf[i >> 1][(i & 1) * 2 + 1] = pack_bf16(p2v, p3v);
+        pf[i >> 1][(i & 1) * 2 + 0] = pack_f16(p0v, p1v);
+        pf[i >> 1][(i & 1) * 2 + 1] = pack_f16(p2v, p3v);
       }
       l_lo = l_lo * c_lo + sum_lo;
       l_hi = l_hi * c_hi + sum_hi;
@@ -208,8 +209,8 @@ __device__ void attend_tile(const AttnArgs& a, int h, int64_t p0, uint8_t* smem)
           const int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
           const int col = dp * 16 + (lane >> 4) * 8;
           ldsm_x4_t(sV + swz(key, col), b0, b1, b2, b3);
-          mma_bf16(o[2 * dp], af, b0, b1);
-          mma_bf16(o[2 * dp + 1], af, b2, b3);
+          mma_f16(o[2 * dp], af, b0, b1);
+          mma_f16(o[2 * dp + 1], af, b2, b3);
         }
       }
     }
@@ -223,13 +224,13 @@ __device__ void attend_tile(const AttnArgs& a, int h, int64_t p0, uint8_t* smem)
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
   const float inv_lo = 1.f / l_lo, inv_hi = 1.f / l_hi;
   const int64_t row_lo = qrow0 + warp * 16 + (lane >> 2), row_hi = row_lo + 8;
-  __nv_bfloat16* out_lo = a.o + row_lo * a.d + h * DH;
-  __nv_bfloat16* out_hi = a.o + row_hi * a.d + h * DH;
+  ct_t* out_lo = a.o + row_lo * a.d + h * DH;
+  ct_t* out_hi = a.o + row_hi * a.d + h * DH;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int col = i * 8 + (lane & 3) * 2;
-    *reinterpret_cast<uint32_t*>(out_lo + col) = pack_bf16(o[i][0] * inv_lo, o[i][1] * inv_lo);
-    *reinterpret_cast<uint32_t*>(out_hi + col) = pack_bf16(o[i][2] * inv_hi, o[i][3] * inv_hi);
+    *reinterpret_cast<uint32_t*>(out_lo + col) = pack_f16(o[i][0] * inv_lo, o[i][1] * inv_lo);
+    *reinterpret_cast<uint32_t*>(out_hi + col) = pack_f16(o[i][2] * inv_hi, o[i][3] * inv_hi);
   }
   if ((lane & 3) == 0) {
     constexpr float LN2 = 0.69314718055994530942f;
@@ -254,14 +255,14 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_zigzag_kernel(const AttnArgs
 
 int attn_fwd_smem_bytes() { return SMEM; }
 
-tsp_status launch_attn_fwd_bf16(const void* qkv, void* o, float* lse, int64_t S, int H, int dh,
+tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, int H, int dh,
                                 int D, cudaStream_t st) {
   if (dh != DH) return TSP_ERR_UNSUPPORTED;
   const int64_t c = S / (2 * D);
   if (c % BQ != 0) return TSP_ERR_UNSUPPORTED;
   AttnArgs a;
-  a.qkv = (const __nv_bfloat16*)qkv;
-  a.o = (__nv_bfloat16*)o;
+  a.qkv = (const ct_t*)qkv;
+  a.o = (ct_t*)o;
   a.lse = lse;
   a.S = S;
   a.c = c;

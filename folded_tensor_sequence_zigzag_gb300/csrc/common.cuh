@@ -7,6 +7,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -214,12 +215,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
-                                                      bool b_mn_major) {
+// Instruction descriptor, kind::f16 with 16-bit A/B (fp16: format 0, bf16:
+// format 1; A and B always of the same type) and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                     bool bf16 = false) {
   return (1u << 4)                          // D format: f32
-         | (1u << 7)                        // A format: bf16
-         | (1u << 10)                       // B format: bf16
+         | ((bf16 ? 1u : 0u) << 7)          // A format
+         | ((bf16 ? 1u : 0u) << 10)         // B format
          | ((a_mn_major ? 1u : 0u) << 15)   // A major-ness
          | ((b_mn_major ? 1u : 0u) << 16)   // B major-ness
          | ((uint32_t)(N >> 3) << 17)       // N / 8
@@ -236,6 +238,39 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 p = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+__device__ __forceinline__ float f16_lo(uint32_t v) {
+  return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t v) {
+  return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+}
+
+// Internal tensor-core operand type of the bf16 configuration: activations
+// and weights enter and leave the library as bf16, but every intermediate
+// that feeds a tensor-core MMA is held in fp16 (10-bit mantissa against
+// bf16's 7), with fp32 accumulation.  Same tcgen05 rate, 8x smaller rounding
+// steps inside the block.
+typedef __half ct_t;
+
+// Pack/unpack two values of a 16-bit storage type T (bf16 or fp16).
+template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  return pack_bf16(lo, hi);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  return pack_f16(lo, hi);
+}
+template <typename T> __device__ __forceinline__ float lo2(uint32_t v);
+template <typename T> __device__ __forceinline__ float hi2(uint32_t v);
+template <> __device__ __forceinline__ float lo2<__nv_bfloat16>(uint32_t v) { return bf16_lo(v); }
+template <> __device__ __forceinline__ float hi2<__nv_bfloat16>(uint32_t v) { return bf16_hi(v); }
+template <> __device__ __forceinline__ float lo2<__half>(uint32_t v) { return f16_lo(v); }
+template <> __device__ __forceinline__ float hi2<__half>(uint32_t v) { return f16_hi(v); }
+
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
 
 template <typename T> __device__ __forceinline__ float to_f(T v);
@@ -243,8 +278,10 @@ template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
   return __bfloat162float(v);
 }
+template <> __device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
 template <typename T> __device__ __forceinline__ T from_f(float v);
 template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }

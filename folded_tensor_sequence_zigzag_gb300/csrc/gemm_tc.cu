@@ -14,6 +14,7 @@
 //    running sum kept in the fp32 TMEM accumulator.
 //
 // Kernel structure (one CTA per SM, persistent over output tiles):
+// Operands are fp16 (the block's internal tensor-core type, see common.cuh).
 //   warps 0-3  epilogue: tcgen05.ld the 128x256 fp32 accumulator (one TMEM
 //              lane = one output row per thread), fused epilogue, stores;
 //   warp 4     TMA producer: 4-stage ring of A (128x64) + B (256x64) tiles
@@ -64,7 +65,7 @@ struct KParams {
   int64_t ldo3;
   const void* res;
   int64_t ldr;
-  int res_f32, out_f32;
+  int res_f32, out_type;
   const void* e1;
   const void* e2;
   int64_t lde;
@@ -99,23 +100,36 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* f) {
+template <typename T>
+__device__ __forceinline__ void store16x32(T* dst, const float* f) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    d4[q] = make_uint4(pack_bf16(f[8 * q + 0], f[8 * q + 1]), pack_bf16(f[8 * q + 2], f[8 * q + 3]),
-                       pack_bf16(f[8 * q + 4], f[8 * q + 5]), pack_bf16(f[8 * q + 6], f[8 * q + 7]));
+    d4[q] = make_uint4(pack2<T>(f[8 * q + 0], f[8 * q + 1]), pack2<T>(f[8 * q + 2], f[8 * q + 3]),
+                       pack2<T>(f[8 * q + 4], f[8 * q + 5]), pack2<T>(f[8 * q + 6], f[8 * q + 7]));
 }
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* f) {
+template <typename T>
+__device__ __forceinline__ void load16x32(const T* src, float* f) {
   const uint4* s4 = reinterpret_cast<const uint4*>(src);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const uint4 v = s4[q];
-    f[8 * q + 0] = bf16_lo(v.x); f[8 * q + 1] = bf16_hi(v.x);
-    f[8 * q + 2] = bf16_lo(v.y); f[8 * q + 3] = bf16_hi(v.y);
-    f[8 * q + 4] = bf16_lo(v.z); f[8 * q + 5] = bf16_hi(v.z);
-    f[8 * q + 6] = bf16_lo(v.w); f[8 * q + 7] = bf16_hi(v.w);
+    f[8 * q + 0] = lo2<T>(v.x); f[8 * q + 1] = hi2<T>(v.x);
+    f[8 * q + 2] = lo2<T>(v.y); f[8 * q + 3] = hi2<T>(v.y);
+    f[8 * q + 4] = lo2<T>(v.z); f[8 * q + 5] = hi2<T>(v.z);
+    f[8 * q + 6] = lo2<T>(v.w); f[8 * q + 7] = hi2<T>(v.w);
   }
+}
+__device__ __forceinline__ void store_f32x32(float* dst, const float* f) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) d4[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+}
+// out_type: OUT_F16 (internal operand), OUT_BF16 (API output), OUT_F32
+__device__ __forceinline__ void store_any32(void* base, int64_t off, const float* f, int out_type) {
+  if (out_type == OUT_F32) store_f32x32((float*)base + off, f);
+  else if (out_type == OUT_BF16) store16x32((__nv_bfloat16*)base + off, f);
+  else store16x32((ct_t*)base + off, f);
 }
 
 template <int EPI, bool A_MN, bool B_MN, bool PAIRED>
@@ -244,7 +258,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      constexpr uint32_t idesc = idesc_f16_f32(BM, BN, A_MN, B_MN, false);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -322,9 +336,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
               fb[j] = __uint_as_float(vb[j]);
               g[j] = fa[j] * sigmoidf_(fa[j]) * fb[j];
             }
-            store_bf16x32((__nv_bfloat16*)p.out + (int64_t)m * p.ldo + n, g);
-            if (p.out2) store_bf16x32((__nv_bfloat16*)p.out2 + (int64_t)m * p.ldo2 + n, fa);
-            if (p.out3) store_bf16x32((__nv_bfloat16*)p.out3 + (int64_t)m * p.ldo3 + n, fb);
+            store16x32((ct_t*)p.out + (int64_t)m * p.ldo + n, g);
+            if (p.out2) store16x32((ct_t*)p.out2 + (int64_t)m * p.ldo2 + n, fa);
+            if (p.out3) store16x32((ct_t*)p.out3 + (int64_t)m * p.ldo3 + n, fb);
           }
         }
       } else {
@@ -338,8 +352,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
           float f[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-          if constexpr (EPI == EPI_BF16) {
-            store_bf16x32((__nv_bfloat16*)p.out + (int64_t)m * p.ldo + n, f);
+          if constexpr (EPI == EPI_STORE) {
+            store_any32(p.out, (int64_t)m * p.ldo + n, f, p.out_type);
           } else if constexpr (EPI == EPI_RES) {
             float r[32];
             if (p.res_f32) {
@@ -351,18 +365,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
                 r[4 * q] = t4.x; r[4 * q + 1] = t4.y; r[4 * q + 2] = t4.z; r[4 * q + 3] = t4.w;
               }
             } else {
-              load_bf16x32((const __nv_bfloat16*)p.res + (int64_t)m * p.ldr + n, r);
+              load16x32((const __nv_bfloat16*)p.res + (int64_t)m * p.ldr + n, r);
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) f[j] += r[j];
-            if (p.out_f32) {
-              float4* d4 = reinterpret_cast<float4*>((float*)p.out + (int64_t)m * p.ldo + n);
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                d4[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
-            } else {
-              store_bf16x32((__nv_bfloat16*)p.out + (int64_t)m * p.ldo + n, f);
-            }
+            store_any32(p.out, (int64_t)m * p.ldo + n, f, p.out_type);
           } else if constexpr (EPI == EPI_F32) {
             float* dst;
             if (p.m_seg > 0) {
@@ -371,23 +378,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
             } else {
               dst = (float*)p.out + (int64_t)m * p.ldo + n;
             }
-            float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              d4[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+            store_f32x32(dst, f);
           } else if constexpr (EPI == EPI_SWIGLU_BWD) {
             // f = dG;  e1 = A, e2 = B (pre-activations, bf16)
             float a[32], b[32], da[32], db[32];
-            load_bf16x32((const __nv_bfloat16*)p.e1 + (int64_t)m * p.lde + n, a);
-            load_bf16x32((const __nv_bfloat16*)p.e2 + (int64_t)m * p.lde + n, b);
+            load16x32((const ct_t*)p.e1 + (int64_t)m * p.lde + n, a);
+            load16x32((const ct_t*)p.e2 + (int64_t)m * p.lde + n, b);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float s = sigmoidf_(a[j]);
               da[j] = f[j] * b[j] * s * (1.f + a[j] * (1.f - s));
               db[j] = f[j] * a[j] * s;
             }
-            store_bf16x32((__nv_bfloat16*)p.out + (int64_t)m * p.ldo + n, da);
-            store_bf16x32((__nv_bfloat16*)p.out2 + (int64_t)m * p.ldo2 + n, db);
+            store16x32((ct_t*)p.out + (int64_t)m * p.ldo + n, da);
+            store16x32((ct_t*)p.out2 + (int64_t)m * p.ldo2 + n, db);
           }
         }
       }
@@ -433,7 +437,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [outer, inner] with row stride ld elements; box
+// Row-major fp16 matrix [outer, inner] with row stride ld elements; box
 // {box_inner = 64, box_outer}; 128-byte swizzle; zero fill out of bounds.
 bool make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld,
               int box_outer) {
@@ -443,7 +447,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int
   const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
   const cuuint32_t box[2] = {64u, (cuuint32_t)box_outer};
   const cuuint32_t estr[2] = {1u, 1u};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -533,7 +537,7 @@ tsp_status gemm_tc(const TcGemm& g, cudaStream_t st) {
   kp->res = g.res;
   kp->ldr = g.ldr;
   kp->res_f32 = g.res_f32 ? 1 : 0;
-  kp->out_f32 = g.out_f32 ? 1 : 0;
+  kp->out_type = g.out_type;
   kp->e1 = g.e1;
   kp->e2 = g.e2;
   kp->lde = g.lde;
@@ -544,9 +548,9 @@ tsp_status gemm_tc(const TcGemm& g, cudaStream_t st) {
   const int tiles = kp->tiles_m * kp->tiles_n;
   const int grid = std::min(tiles, num_sms());
   switch (g.epi) {
-    case EPI_BF16:
-      if (!g.a_mn && !g.b_mn) return launch_t<EPI_BF16, false, false, false>(*kp, grid, st, g.name);
-      if (!g.a_mn && g.b_mn) return launch_t<EPI_BF16, false, true, false>(*kp, grid, st, g.name);
+    case EPI_STORE:
+      if (!g.a_mn && !g.b_mn) return launch_t<EPI_STORE, false, false, false>(*kp, grid, st, g.name);
+      if (!g.a_mn && g.b_mn) return launch_t<EPI_STORE, false, true, false>(*kp, grid, st, g.name);
       break;
     case EPI_RES:
       if (!g.a_mn && !g.b_mn) return launch_t<EPI_RES, false, false, false>(*kp, grid, st, g.name);

@@ -6,9 +6,10 @@
 
 namespace tsp {
 
-enum { EPI_BF16 = 0, EPI_RES = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_SWIGLU_BWD = 4 };
+enum { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 2 };
+enum { EPI_STORE = 0, EPI_RES = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_SWIGLU_BWD = 4 };
 
-// C[M, N] = sum over K of A(m, k) * B(n, k), bf16 operands, fp32 accumulation.
+// C[M, N] = sum over K of A(m, k) * B(n, k), fp16 operands, fp32 accumulation.
 //   A K-major: stored [M, K] (row stride lda);  A MN-major: stored [K, M].
 //   B K-major: stored [N, K] (nn.Linear weight); B MN-major: stored [K, N].
 // K may be split into up to 3 segments, each with its own A and B pointer
@@ -20,12 +21,12 @@ enum { EPI_BF16 = 0, EPI_RES = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_SWIGLU_BWD = 
 // (boundaries floor(s*K/rot_D), k-block granularity) in ring order
 // (r - t) mod rot_D.
 // Epilogues (out/out2/out3 row strides ldo/ldo2/ldo3, elements):
-//   EPI_BF16       out = bf16(C)
-//   EPI_RES        out = C + res, res bf16 or fp32 (res_f32), out bf16 or fp32 (out_f32)
+//   EPI_STORE      out = C stored as out_type (OUT_F16 / OUT_BF16 / OUT_F32)
+//   EPI_RES        out = C + res, res bf16 or fp32 (res_f32), stored as out_type
 //   EPI_F32        out = C (fp32); with m_seg > 0 rows go to outs[m / m_seg]
-//   EPI_SWIGLU     out = bf16(silu(C_1) * C_3); out2/out3 (nullable) = bf16(C_1), bf16(C_3)
-//   EPI_SWIGLU_BWD C = dG; e1 = A, e2 = B (bf16, stride lde):
-//                  out = bf16(dG * B * s(A) (1 + A (1 - s(A)))), out2 = bf16(dG * silu(A))
+//   EPI_SWIGLU     out = f16(silu(C_1) * C_3); out2/out3 (nullable) = f16(C_1), f16(C_3)
+//   EPI_SWIGLU_BWD C = dG; e1 = A, e2 = B (fp16, stride lde):
+//                  out = f16(dG * B * s(A) (1 + A (1 - s(A)))), out2 = f16(dG * silu(A))
 struct TcGemm {
   const char* name = "gemm_tc";  // label for launch accounting
   int M = 0, N = 0, K = 0;
@@ -39,7 +40,7 @@ struct TcGemm {
   int nseg_n = 0;
   bool paired = false;
   int rot_rows = 0, rot_D = 0;
-  int epi = EPI_BF16;
+  int epi = EPI_STORE;
   void* out = nullptr;
   int64_t ldo = 0;
   void* out2 = nullptr;
@@ -48,7 +49,8 @@ struct TcGemm {
   int64_t ldo3 = 0;
   const void* res = nullptr;
   int64_t ldr = 0;
-  bool res_f32 = false, out_f32 = false;
+  bool res_f32 = false;
+  int out_type = OUT_F16;
   const void* e1 = nullptr;
   const void* e2 = nullptr;
   int64_t lde = 0;

@@ -12,18 +12,24 @@ namespace tsp {
 // rowwise.cu
 tsp_status launch_zigzag_permute(const void* src, void* dst, int64_t S, int D, int64_t row_bytes,
                                  int inverse, cudaStream_t st);
-// u_f32: the input is fp32 (else the storage dtype); g and out are of the storage dtype.
-tsp_status launch_rmsnorm_fwd(const void* u, int u_f32, const void* g, void* out, float* rstd,
-                              int64_t rows, int n, float eps, int dtype, cudaStream_t st);
+// Element types of internal buffers.
+enum { TY_F32 = 0, TY_BF16 = 1, TY_F16 = 2 };
+
+// dtype TSP_F32: everything fp32.  dtype TSP_BF16: g is bf16; (u, out) is one
+// of (fp32, fp16), (bf16, fp16), (bf16, bf16).
+tsp_status launch_rmsnorm_fwd(const void* u, int u_ty, const void* g, void* out, int out_ty,
+                              float* rstd, int64_t rows, int n, float eps, int dtype,
+                              cudaStream_t st);
 int rmsnorm_bwd_blocks(int64_t rows);
 // du = rstd (dout g - nrm mean(dout g nrm)), nrm = u rstd; out = resid + du, where
 // resid is resid_f32 (fp32) or resid_t (storage dtype), exactly one non-NULL;
 // dg = sum over rows of dout * nrm (dg_part: rmsnorm_bwd_blocks(rows) x n fp32 scratch).
-// u_f32: u is fp32 (else the storage dtype).
-tsp_status launch_rmsnorm_bwd(const float* dout, const void* u, int u_f32, const void* g,
+// dtype TSP_BF16: g and resid_t are bf16; (u, out_t) is (fp32, fp16) or (bf16, bf16).
+tsp_status launch_rmsnorm_bwd(const float* dout, const void* u, int u_ty, const void* g,
                               const float* rstd, const float* resid_f32, const void* resid_t,
-                              float* out_f32, void* out_t, float* dg, float* dg_part, int64_t rows,
-                              int n, int dtype, cudaStream_t st);
+                              float* out_f32, void* out_t, int out_ty, float* dg, float* dg_part,
+                              int64_t rows, int n, int dtype, cudaStream_t st);
+tsp_status launch_convert_bf16_f16(const void* src, void* dst, int64_t n, cudaStream_t st);
 tsp_status launch_swiglu_f32(const float* AB, float* G, int64_t rows, int I, cudaStream_t st);
 tsp_status launch_swiglu_bwd_f32(const float* dG, const float* AB, float* dAB, int64_t rows, int I,
                                  cudaStream_t st);
@@ -41,11 +47,11 @@ tsp_status launch_attn_f32_bwd(const float* QKV, const float* O, const float* dO
                                cudaStream_t st);
 
 // attn_fwd.cu
-tsp_status launch_attn_fwd_bf16(const void* qkv, void* o, float* lse, int64_t S, int H, int dh,
+tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, int H, int dh,
                                 int D, cudaStream_t st);
 
 // attn_bwd.cu
-tsp_status launch_attn_bwd_bf16(const void* qkv, const void* o, const void* dO, const float* lse,
+tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, const float* lse,
                                 float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int dh,
                                 int D, cudaStream_t st);
 

@@ -71,8 +71,8 @@ __device__ __forceinline__ void load8(const T* p, float* f) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      f[2 * i] = bf16_lo(w[i]);
-      f[2 * i + 1] = bf16_hi(w[i]);
+      f[2 * i] = lo2<T>(w[i]);
+      f[2 * i + 1] = hi2<T>(w[i]);
     }
   } else {
     const float4 a = reinterpret_cast<const float4*>(p)[0];
@@ -84,17 +84,17 @@ __device__ __forceinline__ void load8(const T* p, float* f) {
 template <typename T>
 __device__ __forceinline__ void store8(T* p, const float* f) {
   if constexpr (sizeof(T) == 2) {
-    *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
-                                              pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+    *reinterpret_cast<uint4*>(p) = make_uint4(pack2<T>(f[0], f[1]), pack2<T>(f[2], f[3]),
+                                              pack2<T>(f[4], f[5]), pack2<T>(f[6], f[7]));
   } else {
     reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
     reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
   }
 }
 
-template <typename Tin, typename T, int UPL>
+template <typename Tin, typename Tg, typename T, int UPL>
 __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const Tin* __restrict__ u,
-                                                          const T* __restrict__ g,
+                                                          const Tg* __restrict__ g,
                                                           T* __restrict__ out,
                                                           float* __restrict__ rstd_out,
                                                           int64_t rows, int n, float eps) {
@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const Tin* __restrict_
 }
 
 // Scalar fallback for rows whose length is not a multiple of 8 (or unaligned).
-template <typename Tin, typename T>
-__global__ void rmsnorm_fwd_scalar_kernel(const Tin* __restrict__ u, const T* __restrict__ g,
+template <typename Tin, typename Tg, typename T>
+__global__ void rmsnorm_fwd_scalar_kernel(const Tin* __restrict__ u, const Tg* __restrict__ g,
                                           T* __restrict__ out, float* __restrict__ rstd_out,
                                           int64_t rows, int n, float eps) {
   const int lane = threadIdx.x & 31;
@@ -155,8 +155,8 @@ __global__ void rmsnorm_fwd_scalar_kernel(const Tin* __restrict__ u, const T* __
   }
 }
 
-template <typename Tin, typename T>
-static tsp_status rmsnorm_fwd_t(const Tin* u, const T* g, T* out, float* rstd, int64_t rows, int n,
+template <typename Tin, typename Tg, typename T>
+static tsp_status rmsnorm_fwd_t(const Tin* u, const Tg* g, T* out, float* rstd, int64_t rows, int n,
                                 float eps, cudaStream_t st) {
   const int64_t want = (rows + 7) / 8;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms() * 8));
@@ -165,26 +165,31 @@ static tsp_status rmsnorm_fwd_t(const Tin* u, const T* g, T* out, float* rstd, i
   const int nu = n / 8;
   Prof prof("rmsnorm_fwd", st);
   if (vec_ok && nu <= 32)
-    rmsnorm_fwd_kernel<Tin, T, 1><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
+    rmsnorm_fwd_kernel<Tin, Tg, T, 1><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
   else if (vec_ok && nu <= 128)
-    rmsnorm_fwd_kernel<Tin, T, 4><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
+    rmsnorm_fwd_kernel<Tin, Tg, T, 4><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
   else if (vec_ok && nu <= 512)
-    rmsnorm_fwd_kernel<Tin, T, 16><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
+    rmsnorm_fwd_kernel<Tin, Tg, T, 16><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
   else
-    rmsnorm_fwd_scalar_kernel<Tin, T><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
+    rmsnorm_fwd_scalar_kernel<Tin, Tg, T><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }
 
-tsp_status launch_rmsnorm_fwd(const void* u, int u_f32, const void* g, void* out, float* rstd,
-                              int64_t rows, int n, float eps, int dtype, cudaStream_t st) {
+tsp_status launch_rmsnorm_fwd(const void* u, int u_ty, const void* g, void* out, int out_ty,
+                              float* rstd, int64_t rows, int n, float eps, int dtype,
+                              cudaStream_t st) {
   typedef __nv_bfloat16 bf;
-  if (dtype == TSP_BF16) {
-    if (u_f32)
-      return rmsnorm_fwd_t((const float*)u, (const bf*)g, (bf*)out, rstd, rows, n, eps, st);
-    return rmsnorm_fwd_t((const bf*)u, (const bf*)g, (bf*)out, rstd, rows, n, eps, st);
-  }
-  return rmsnorm_fwd_t((const float*)u, (const float*)g, (float*)out, rstd, rows, n, eps, st);
+  if (dtype != TSP_BF16)
+    return rmsnorm_fwd_t((const float*)u, (const float*)g, (float*)out, rstd, rows, n, eps, st);
+  const bf* gb = (const bf*)g;
+  if (u_ty == TY_F32 && out_ty == TY_F16)
+    return rmsnorm_fwd_t((const float*)u, gb, (ct_t*)out, rstd, rows, n, eps, st);
+  if (u_ty == TY_BF16 && out_ty == TY_F16)
+    return rmsnorm_fwd_t((const bf*)u, gb, (ct_t*)out, rstd, rows, n, eps, st);
+  if (u_ty == TY_BF16 && out_ty == TY_BF16)
+    return rmsnorm_fwd_t((const bf*)u, gb, (bf*)out, rstd, rows, n, eps, st);
+  return TSP_ERR_UNSUPPORTED;
 }
 
 // ---------------------------------------------------------------------------
@@ -199,11 +204,11 @@ tsp_status launch_rmsnorm_fwd(const void* u, int u_f32, const void* g, void* out
 // gathered in shared memory and written as one partial row, summed by
 // rowsum_partials_kernel.
 // ---------------------------------------------------------------------------
-template <typename Tu, typename T>
+template <typename Tu, typename T, typename Tr, typename To>
 __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(
     const float* __restrict__ dout, const Tu* __restrict__ u, const T* __restrict__ g,
     const float* __restrict__ rstd, const float* __restrict__ resid_f32,
-    const T* __restrict__ resid_t, float* __restrict__ out_f32, T* __restrict__ out_t,
+    const Tr* __restrict__ resid_t, float* __restrict__ out_f32, To* __restrict__ out_t,
     float* __restrict__ dg_part, int64_t rows, int n) {
   extern __shared__ float s_dg[];
   for (int i = threadIdx.x; i < n; i += blockDim.x) s_dg[i] = 0.f;
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(
       const float du = r * (dr[i] * to_f(g[i]) - nrm * dot);
       const float o = (resid_f32 ? resid_f32[row * n + i] : to_f(resid_t[row * n + i])) + du;
       if (out_f32) out_f32[row * n + i] = o;
-      if (out_t) out_t[row * n + i] = from_f<T>(o);
+      if (out_t) out_t[row * n + i] = from_f<To>(o);
     }
   }
   __syncthreads();
@@ -249,38 +254,63 @@ __global__ void rowsum_partials_kernel(const float* __restrict__ part, float* __
   out[i] = s;
 }
 
-template <typename Tu, typename T>
+template <typename Tu, typename T, typename Tr, typename To>
 static tsp_status rmsnorm_bwd_t(const float* dout, const Tu* u, const T* g, const float* rstd,
-                                const float* resid_f32, const T* resid_t, float* out_f32, T* out_t,
+                                const float* resid_f32, const Tr* resid_t, float* out_f32, To* out_t,
                                 float* dg, float* dg_part, int64_t rows, int n, cudaStream_t st) {
   const int grid = rmsnorm_bwd_blocks(rows);
   const size_t sm = (size_t)n * sizeof(float);
   Prof prof("rmsnorm_bwd", st, 2);
   if (sm > 48 * 1024)
-    TSP_CUDA_TRY(cudaFuncSetAttribute(rmsnorm_bwd_kernel<Tu, T>,
+    TSP_CUDA_TRY(cudaFuncSetAttribute(rmsnorm_bwd_kernel<Tu, T, Tr, To>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-  rmsnorm_bwd_kernel<Tu, T><<<grid, 256, sm, st>>>(dout, u, g, rstd, resid_f32, resid_t, out_f32,
-                                                   out_t, dg_part, rows, n);
+  rmsnorm_bwd_kernel<Tu, T, Tr, To><<<grid, 256, sm, st>>>(dout, u, g, rstd, resid_f32, resid_t,
+                                                           out_f32, out_t, dg_part, rows, n);
   TSP_CUDA_TRY(cudaGetLastError());
   rowsum_partials_kernel<<<(n + 255) / 256, 256, 0, st>>>(dg_part, dg, grid, n);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }
 
-tsp_status launch_rmsnorm_bwd(const float* dout, const void* u, int u_f32, const void* g,
+tsp_status launch_rmsnorm_bwd(const float* dout, const void* u, int u_ty, const void* g,
                               const float* rstd, const float* resid_f32, const void* resid_t,
-                              float* out_f32, void* out_t, float* dg, float* dg_part, int64_t rows,
-                              int n, int dtype, cudaStream_t st) {
+                              float* out_f32, void* out_t, int out_ty, float* dg, float* dg_part,
+                              int64_t rows, int n, int dtype, cudaStream_t st) {
   typedef __nv_bfloat16 bf;
-  if (dtype == TSP_BF16) {
-    if (u_f32)
-      return rmsnorm_bwd_t(dout, (const float*)u, (const bf*)g, rstd, resid_f32,
-                           (const bf*)resid_t, out_f32, (bf*)out_t, dg, dg_part, rows, n, st);
-    return rmsnorm_bwd_t(dout, (const bf*)u, (const bf*)g, rstd, resid_f32, (const bf*)resid_t,
-                         out_f32, (bf*)out_t, dg, dg_part, rows, n, st);
+  if (dtype != TSP_BF16)
+    return rmsnorm_bwd_t(dout, (const float*)u, (const float*)g, rstd, resid_f32,
+                         (const float*)resid_t, out_f32, (float*)out_t, dg, dg_part, rows, n, st);
+  const bf* gb = (const bf*)g;
+  // MLP norm: u = h (fp32 residual stream), resid = dy (bf16), out = dh (fp32) + fp16 copy
+  if (u_ty == TY_F32 && out_ty == TY_F16)
+    return rmsnorm_bwd_t(dout, (const float*)u, gb, rstd, resid_f32, (const bf*)resid_t, out_f32,
+                         (ct_t*)out_t, dg, dg_part, rows, n, st);
+  // attention norm: u = x (bf16), resid = dh (fp32), out = dx (bf16)
+  if (u_ty == TY_BF16 && out_ty == TY_BF16)
+    return rmsnorm_bwd_t(dout, (const bf*)u, gb, rstd, resid_f32, (const bf*)resid_t, out_f32,
+                         (bf*)out_t, dg, dg_part, rows, n, st);
+  return TSP_ERR_UNSUPPORTED;
+}
+
+// bf16 -> fp16, 8 elements per thread-iteration (n % 8 == 0, 16-byte aligned)
+__global__ void convert_bf16_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                        int64_t n8) {
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n8;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 v = src[t];
+    dst[t] = make_uint4(pack_f16(bf16_lo(v.x), bf16_hi(v.x)), pack_f16(bf16_lo(v.y), bf16_hi(v.y)),
+                        pack_f16(bf16_lo(v.z), bf16_hi(v.z)), pack_f16(bf16_lo(v.w), bf16_hi(v.w)));
   }
-  return rmsnorm_bwd_t(dout, (const float*)u, (const float*)g, rstd, resid_f32,
-                       (const float*)resid_t, out_f32, (float*)out_t, dg, dg_part, rows, n, st);
+}
+
+tsp_status launch_convert_bf16_f16(const void* src, void* dst, int64_t n, cudaStream_t st) {
+  if (n % 8 != 0 || ((uintptr_t)src & 15u) || ((uintptr_t)dst & 15u)) return TSP_ERR_UNSUPPORTED;
+  Prof prof("convert_bf16_f16", st);
+  const int64_t n8 = n / 8;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((n8 + 255) / 256, (int64_t)num_sms() * 8));
+  convert_bf16_f16_kernel<<<grid, 256, 0, st>>>((const uint4*)src, (uint4*)dst, n8);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
 }
 
 // ---------------------------------------------------------------------------

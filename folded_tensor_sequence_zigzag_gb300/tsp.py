@@ -201,10 +201,13 @@ def gated_mlp_fwd(cfg: Cfg, h_z, W: BlockWeights, norm=True, residual=True, out=
 
 
 def block_fwd(cfg: Cfg, x_z, W: BlockWeights, saved=None, out=None, ws=None, stream=None):
-    """y_z = block(x_z).  Pass ``saved`` (uint8, saved_bytes(cfg)) to keep activations for bwd."""
+    """y_z = block(x_z).  Pass ``saved`` (uint8, saved_bytes(cfg)) to keep activations for bwd.
+
+    The workspace always holds the fp16 operand copies of the weights; without
+    ``saved`` it also holds the activations."""
     _require_cuda(x_z)
     out = torch.empty_like(x_z) if out is None else out
-    if saved is None and ws is None:
+    if ws is None:
         ws = _ws(workspace_bytes(cfg, TSP_OP_BLOCK_FWD), x_z.device)
     aw, mw = W.attn(), W.mlp()
     _check(load().tsp_block_fwd(ctypes.byref(cfg), _ptr(x_z), ctypes.byref(aw), ctypes.byref(mw),
