@@ -820,3 +820,53 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
 }
 
 }  // namespace tsp
+
+// ----------------------------------------------------------------------------
+// Gated-MLP forward for callers that cannot allocate: the scratch is this
+// fixed device array instead of a caller workspace.
+// ----------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_noalloc_scratch[TSP_NOALLOC_SCRATCH_BYTES];
+
+namespace tsp {
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {nullptr};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current.  (In host code the array's name is
+// only a host-side stand-in, never a device pointer.)
+tsp_status noalloc_scratch(uint8_t** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TSP_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return TSP_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = (uint8_t*)g_noalloc_addr[dev];
+  return TSP_OK;
+}
+}  // namespace
+}  // namespace tsp
+
+extern "C" tsp_status tsp_gated_mlp_fwd_noalloc(const tsp_cfg* cfg, const void* h_z,
+                                                const tsp_mlp_w* w, void* y_z, void* stream) {
+  tsp_status r = check_cfg(cfg);
+  if (r != TSP_OK) return r;
+  if ((r = check_mlp_w(w, false)) != TSP_OK) return r;
+  if (!al16(h_z) || !al16(y_z)) return TSP_ERR_INVALID_ARG;
+  if ((r = check_bf16_mlp(cfg)) != TSP_OK) return r;
+  const size_t need = tsp_workspace_bytes(cfg, TSP_OP_MLP_FWD);
+  if (need == 0 || need > (size_t)TSP_NOALLOC_SCRATCH_BYTES) return TSP_ERR_INVALID_ARG;
+  uint8_t* scratch = nullptr;
+  if ((r = noalloc_scratch(&scratch)) != TSP_OK) return r;
+  const int parts = PART_MLP | (cfg->dtype == TSP_F32 ? PART_AB : 0);
+  const size_t na = acts_layout(cfg, parts, nullptr).bytes;
+  const Acts A = acts_layout(cfg, parts, scratch);
+  const WCache WC = wcache_layout(cfg, WC_MLP, scratch + na);
+  cudaStream_t st = S_(stream);
+  if ((r = fill_wcache(cfg, WC, nullptr, w, st)) != TSP_OK) return r;
+  return mlp_half(cfg, h_z, false, w, WC, y_z, A, st);
+}

@@ -22,7 +22,8 @@ TSP_OP_ATTN_FWD, TSP_OP_MLP_FWD, TSP_OP_BLOCK_FWD, TSP_OP_BLOCK_BWD = range(4)
 EXPORTED = ("tsp_zigzag_permute", "tsp_rmsnorm_fwd", "tsp_workspace_bytes", "tsp_saved_bytes",
             "tsp_attn_block_fwd", "tsp_gated_mlp_fwd", "tsp_block_fwd", "tsp_block_bwd",
             "tsp_pack_attn_shards", "tsp_device_status", "tsp_strerror", "tsp_num_sms",
-            "tsp_profile_enable", "tsp_profile_report", "tsp_launch_count")
+            "tsp_profile_enable", "tsp_profile_report", "tsp_launch_count",
+            "tsp_gated_mlp_fwd_noalloc")
 
 
 class TspError(RuntimeError):
@@ -76,6 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "tsp_profile_enable": (None, [i32]),
         "tsp_profile_report": (i32, [ctypes.c_char_p, i64]),
         "tsp_launch_count": (i64, []),
+        "tsp_gated_mlp_fwd_noalloc": (i32, [P(Cfg), vp, P(MlpW), vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -268,3 +270,20 @@ def profile_report() -> dict:
 
 def launch_count() -> int:
     return int(load().tsp_launch_count())
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def gated_mlp_fwd_noalloc(cfg: Cfg, h_z, W: BlockWeights, out, norm=True, residual=True,
+                          stream=None):
+    """tsp_gated_mlp_fwd without a workspace: for callers that must not allocate
+    device memory during the call.  ``out`` must be preallocated by the caller;
+    the library works in its fixed 32 MiB device scratch and allocates nothing.
+    Calls that overlap on the GPU share that scratch and race."""
+    _require_cuda(h_z, out)
+    mw = W.mlp(norm, residual)
+    _check(load().tsp_gated_mlp_fwd_noalloc(ctypes.byref(cfg), _ptr(h_z), ctypes.byref(mw),
+                                            _ptr(out), _stream(stream)),
+           "tsp_gated_mlp_fwd_noalloc")
+    return out

@@ -143,6 +143,34 @@ tsp_status tsp_attn_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_att
 tsp_status tsp_gated_mlp_fwd(const tsp_cfg* cfg, const void* h_z, const tsp_mlp_w* w,
                              void* y_z, void* ws, size_t ws_bytes, void* stream);
 
+/* Size of the device scratch that tsp_gated_mlp_fwd_noalloc works in: 32 MiB.
+ * Every GPU that loads this library holds it until the process exits. */
+#define TSP_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* Gated-MLP half without a caller workspace.  The pages have no counterpart
+ * for this entry point: it exists for callers that cannot allocate device
+ * memory at the point of the call -- for example a plugin whose execute hook
+ * runs inside an inference engine that has already planned every byte of
+ * device memory (an extra allocation could fail or break that plan), or a
+ * latency-critical loop that cannot afford the device-wide synchronisation a
+ * cudaMalloc/cudaFree may imply.  It computes exactly what tsp_gated_mlp_fwd
+ * computes, with the same arguments minus (ws, ws_bytes); its scratch (the
+ * normalised input, G, and the fp16 weight copies) lives in one fixed
+ * TSP_NOALLOC_SCRATCH_BYTES array compiled into the library.  It allocates
+ * nothing.
+ *  - Limit: if tsp_workspace_bytes(cfg, TSP_OP_MLP_FWD) exceeds
+ *    TSP_NOALLOC_SCRATCH_BYTES it returns TSP_ERR_INVALID_ARG and launches
+ *    nothing (other argument errors as for tsp_gated_mlp_fwd).
+ *  - The first call on a device looks up the array's device address with that
+ *    device current (cudaGetSymbolAddress; TSP_ERR_CUDA if that fails).  Make
+ *    that first call before any stream capture.
+ *  - Every call shares the one array, which keeps the previous call's
+ *    contents; no part of it needs to start at zero (each call writes every
+ *    byte it reads).  Calls that overlap on the GPU (other streams, other host
+ *    threads) race on it: order them on one stream or synchronise them. */
+tsp_status tsp_gated_mlp_fwd_noalloc(const tsp_cfg* cfg, const void* h_z, const tsp_mlp_w* w,
+                                     void* y_z, void* stream);
+
 /* Whole block forward: y_z = MLP-half(Attention-half(x_z)).  mlp_w->g_mlp
  * must be non-NULL and add_residual 1 (pre-norm block).  saved (nullable):
  * tsp_saved_bytes(cfg) bytes that receive the activations tsp_block_bwd
