@@ -1,5 +1,6 @@
-// attn_fwd.cu -- causal flash-attention forward over the zigzag layout (fp16
-// tensor-core operands, fp32 softmax and accumulation).
+// attn_fwd.cu -- causal flash-attention forward over the zigzag layout on the
+// 5th-generation tensor cores (tcgen05.mma kind::f16, fp16 operands, fp32
+// accumulators in TMEM, softmax in fp32).
 //
 // Source: "Folding Tensor and Sequence Parallelism for Memory-Efficient
 // Transformer Training & Inference" (gist.science summary), section 2,
@@ -8,17 +9,28 @@
 // work of the ranks equal.  On one GPU the gathered K/V is the zigzag buffer
 // itself: key position p is read from buffer row zz_row_of_pos(p).
 //
-// Work unit = one CTA = (head h, virtual rank r, q-tile t): it processes the
-// 128 query rows of tile t in chunk r AND the mirrored tile n-1-t of chunk
-// 2D-1-r (n = c/128 tiles per chunk).  Their causal key ranges add up to
-// S + 128 keys for every (r, t), so every CTA carries the same work.
-// Key tiles past a query tile's last row are never visited; only the two
-// 64-key tiles on the diagonal are masked element-wise.
+// Work unit = one CTA = (head h, virtual rank r, q-tile t): the 128 query rows
+// of tile t in chunk r AND the mirrored tile n-1-t of chunk 2D-1-r
+// (n = c/128).  Their causal key ranges add up to S + 128 keys for every
+// (r, t), so every CTA carries the same work.  Key tiles past a query tile's
+// last row are never visited; only the diagonal 128-key tile is masked.
 //
-// Inner loop (per warp: 16 query rows, dh = 128; per CTA: 8 warps, 128 rows):
-// S = Q K^T on mma.sync m16n8k16 fp16 -> fp32, online softmax in the log2
-// domain with exp2f, O += P V with P re-packed from the accumulator
-// registers.  K/V tiles (64 keys) are double-buffered with cp.async.
+// Per KV tile j (128 keys), warp-specialised:
+//   warp 4   TMA producer: Q once per q-tile, K_j and V_j into a 2-stage ring
+//            (128-byte swizzle; Q, K, V are column boxes of the Q|K|V buffer);
+//   warp 5   TMEM allocator + MMA issuer: S_j = Q K_j^T into one of two
+//            128-column TMEM buffers (issued one tile ahead), then
+//            O += P_j V_j into a 128-column TMEM accumulator, with V read
+//            MN-major (dh contiguous) straight from the buffer;
+//   warps 0-3 softmax: thread = query row = TMEM lane; loads its S row,
+//            p = 2^(s*scale*log2e - m), writes P_j as fp16 into swizzled
+//            shared memory (double-buffered, the A operand of the PV MMA).
+// The running max m is only raised (and O rescaled in TMEM) when a warp's
+// row max grows by more than 2^8 -- the result O/l is exact either way and
+// p stays below 256.  All mbarrier waits are bounded (TSP_ERR_TIMEOUT).
+#include <cstring>
+#include <memory>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -26,260 +38,365 @@ namespace tsp {
 
 namespace {
 
-constexpr int BQ = 128, BKV = 64, DH = 128, NTHR = 256;
-constexpr int TILE_ROW_BYTES = DH * 2;  // 256
-constexpr int SQ_BYTES = BQ * TILE_ROW_BYTES;
-constexpr int SKV_BYTES = BKV * TILE_ROW_BYTES;
-constexpr int SMEM = SQ_BYTES + 4 * SKV_BYTES;  // Q + 2 x (K, V)
+constexpr int BQ = 128, BKV = 128, DH = 128;
+constexpr int NTHR = 192;
+constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128x128 fp16 tile (two 64-column boxes)
+constexpr int BOX_BYTES = TILE_BYTES / 2;  // 128 rows x 64 columns
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + TILE_BYTES;        // 2 stages
+constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;    // 2 stages
+constexpr int OFF_P = OFF_V + 2 * TILE_BYTES;    // 2 buffers
+constexpr int OFF_BAR = OFF_P + 2 * TILE_BYTES;
+constexpr int SMEM = OFF_BAR + 256 + 1024;       // + 1 KB alignment slack
+constexpr uint32_t TMEM_COLS = 512;              // S0 | S1 | O | (unused)
+constexpr uint32_t TM_S = 0, TM_O = 256;
+constexpr float RESCALE_LOG2 = 8.0f;             // lazy-rescale threshold (log2 units)
 
-// byte offset of (row, col) in a [rows][128] 16-bit tile, 16-byte chunks XOR-swizzled by row
-__device__ __forceinline__ uint32_t swz(int row, int col) {
-  return (uint32_t)(row * TILE_ROW_BYTES + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// rows [0, nrows) x 128 16-bit columns from global (row stride ld elements) into a swizzled tile
-__device__ __forceinline__ void load_tile(uint32_t sdst, const ct_t* g, int64_t ld,
-                                          int nrows) {
-  for (int i = threadIdx.x; i < nrows * 16; i += NTHR) {
-    const int row = i >> 4, ch = i & 15;
-    cp_async16(sdst + swz(row, ch * 8), g + (int64_t)row * ld + ch * 8);
-  }
-}
-
-struct AttnArgs {
-  const ct_t* qkv;  // [S, 3d]
-  ct_t* o;          // [S, d]
-  float* lse;                // [H, S]
-  int64_t S;
-  int64_t c;
-  int D, H, d, n_tiles;      // n_tiles = c / 128
-  float scale_log2;          // log2(e) / sqrt(dh)
+struct TcAttnArgs {
+  CUtensorMap tm;       // Q|K|V buffer [S rows, 3d cols] fp16, box {64, 128}, 128B swizzle
+  ct_t* o;              // [S, d]
+  float* lse;           // [H, S]
+  int64_t S, c;
+  int D, d, n_tiles;    // n_tiles = c / 128
+  float scale_log2;
+  int* status;
+  uint64_t limit_ns;
 };
 
-__device__ void attend_tile(const AttnArgs& a, int h, int64_t p0, uint8_t* smem) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t ld = 3 * (int64_t)a.d;
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK0 = sQ + SQ_BYTES;
-  // buffer b: K at sK0 + b*2*SKV, V at +SKV
-  const int64_t qrow0 = zz_row_of_pos(p0, a.c, a.D);
-  const ct_t* qg = a.qkv + qrow0 * ld + h * DH;
-  const int nt = (int)((p0 + BQ) / BKV);
-
-  auto kv_src = [&](int j) {
-    const int64_t k0 = (int64_t)j * BKV;
-    return a.qkv + zz_row_of_pos(k0, a.c, a.D) * ld + a.d + h * DH;
-  };
-  load_tile(sQ, qg, ld, BQ);
-  {
-    const ct_t* ks = kv_src(0);
-    load_tile(sK0, ks, ld, BKV);
-    load_tile(sK0 + SKV_BYTES, ks + a.d, ld, BKV);
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > limit_ns) return;
   }
-  cp_async_commit();
-  cp_async_wait_all();
-  __syncthreads();
-
-  // Q fragments for this warp's 16 rows, 8 k-steps over dh
-  uint32_t qf[8][4];
-  {
-    const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int col = ks * 16 + (lane >> 4) * 8;
-      ldsm_x4(sQ + swz(r, col), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
-    }
-  }
-  float o[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
-  const int64_t wq0 = p0 + warp * 16;                 // first query position of this warp
-  const int64_t q_lo = wq0 + (lane >> 2), q_hi = q_lo + 8;
-
-  for (int j = 0; j < nt; ++j) {
-    const uint32_t sK = sK0 + (uint32_t)(j & 1) * 2 * SKV_BYTES;
-    const uint32_t sV = sK + SKV_BYTES;
-    if (j + 1 < nt) {
-      const uint32_t nK = sK0 + (uint32_t)((j + 1) & 1) * 2 * SKV_BYTES;
-      const ct_t* ks = kv_src(j + 1);
-      load_tile(nK, ks, ld, BKV);
-      load_tile(nK + SKV_BYTES, ks + a.d, ld, BKV);
-    }
-    cp_async_commit();
-    const int64_t k0 = (int64_t)j * BKV;
-    if (k0 <= wq0 + 15) {
-      float s[8][4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          uint32_t b0, b1, b2, b3;
-          const int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-          const int col = ks * 16 + ((lane >> 3) & 1) * 8;
-          ldsm_x4(sK + swz(key, col), b0, b1, b2, b3);
-          mma_f16(s[2 * np], qf[ks], b0, b1);
-          mma_f16(s[2 * np + 1], qf[ks], b2, b3);
-        }
-      }
-      const bool diag = k0 + BKV - 1 > wq0;
-      float mx_lo = -INFINITY, mx_hi = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float v0 = s[i][e] * a.scale_log2, v1 = s[i][2 + e] * a.scale_log2;
-          if (diag) {
-            const int64_t kp = k0 + i * 8 + (lane & 3) * 2 + e;
-            if (kp > q_lo) v0 = -INFINITY;
-            if (kp > q_hi) v1 = -INFINITY;
-          }
-          s[i][e] = v0;
-          s[i][2 + e] = v1;
-          mx_lo = fmaxf(mx_lo, v0);
-          mx_hi = fmaxf(mx_hi, v1);
-        }
-      }
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-      const float c_lo = exp2f(m_lo - mn_lo), c_hi = exp2f(m_hi - mn_hi);
-      m_lo = mn_lo;
-      m_hi = mn_hi;
-      float sum_lo = 0.f, sum_hi = 0.f;
-      uint32_t pf[4][4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float p0v = exp2f(s[i][0] - mn_lo), p1v = exp2f(s[i][1] - mn_lo);
-        const float p2v = exp2f(s[i][2] - mn_hi), p3v = exp2f(s[i][3] - mn_hi);
-        sum_lo += p0v + p1v;
-        sum_hi += p2v + p3v;
-        // C fragment of n-tile i -> A fragment of k-step i/2
-        pf[i >> 1][(i & 1) * 2 + 0] = pack_f16(p0v, p1v);
-        pf[i >> 1][(i & 1) * 2 + 1] = pack_f16(p2v, p3v);
-      }
-      l_lo = l_lo * c_lo + sum_lo;
-      l_hi = l_hi * c_hi + sum_hi;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        o[i][0] *= c_lo;
-        o[i][1] *= c_lo;
-        o[i][2] *= c_hi;
-        o[i][3] *= c_hi;
-      }
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        // A fragment order: (rows lo, k 0-7), (rows hi, k 0-7), (rows lo, k 8-15), (rows hi, k 8-15)
-        const uint32_t af[4] = {pf[ks][0], pf[ks][1], pf[ks][2], pf[ks][3]};
-#pragma unroll
-        for (int dp = 0; dp < 8; ++dp) {
-          uint32_t b0, b1, b2, b3;
-          const int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int col = dp * 16 + (lane >> 4) * 8;
-          ldsm_x4_t(sV + swz(key, col), b0, b1, b2, b3);
-          mma_f16(o[2 * dp], af, b0, b1);
-          mma_f16(o[2 * dp + 1], af, b2, b3);
-        }
-      }
-    }
-    cp_async_wait_all();
-    __syncthreads();
-  }
-  // finalize: full row sums across the quad
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  const float inv_lo = 1.f / l_lo, inv_hi = 1.f / l_hi;
-  const int64_t row_lo = qrow0 + warp * 16 + (lane >> 2), row_hi = row_lo + 8;
-  ct_t* out_lo = a.o + row_lo * a.d + h * DH;
-  ct_t* out_hi = a.o + row_hi * a.d + h * DH;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int col = i * 8 + (lane & 3) * 2;
-    *reinterpret_cast<uint32_t*>(out_lo + col) = pack_f16(o[i][0] * inv_lo, o[i][1] * inv_lo);
-    *reinterpret_cast<uint32_t*>(out_hi + col) = pack_f16(o[i][2] * inv_hi, o[i][3] * inv_hi);
-  }
-  if ((lane & 3) == 0) {
-    constexpr float LN2 = 0.69314718055994530942f;
-    a.lse[(int64_t)h * a.S + row_lo] = (m_lo + log2f(l_lo)) * LN2;
-    a.lse[(int64_t)h * a.S + row_hi] = (m_hi + log2f(l_hi)) * LN2;
-  }
-  __syncthreads();  // smem is reused by the next tile
 }
 
-__global__ void __launch_bounds__(NTHR, 1) attn_fwd_zigzag_kernel(const AttnArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_constant__ TcAttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + OFF_BAR;
+  // barrier map (8 bytes each)
+  const uint32_t q_full = bars + 0;
+  auto k_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto v_full = [&](int s) { return bars + 8u * (3 + s); };
+  auto kv_empty = [&](int s) { return bars + 8u * (5 + s); };
+  auto s_full = [&](int b) { return bars + 8u * (7 + b); };
+  auto p_full = [&](int b) { return bars + 8u * (9 + b); };
+  auto p_free = [&](int b) { return bars + 8u * (11 + b); };
+  const uint32_t o_final = bars + 8u * 13;
+  const uint32_t drain_bar = bars + 8u * 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 160);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_BAR + 168);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
-  const int pair = blockIdx.x;          // r * n_tiles + t
+  const int pair = blockIdx.x;
   const int r = pair / a.n_tiles, t = pair - r * a.n_tiles;
-  const int64_t pA = (int64_t)r * a.c + (int64_t)t * BQ;                                  // chunk r
-  const int64_t pB = (int64_t)(2 * a.D - 1 - r) * a.c + (int64_t)(a.n_tiles - 1 - t) * BQ;  // mirror
-  attend_tile(a, h, pB, smem);
-  attend_tile(a, h, pA, smem);
+  int64_t p0s[2];
+  p0s[0] = (int64_t)(2 * a.D - 1 - r) * a.c + (int64_t)(a.n_tiles - 1 - t) * BQ;  // mirror tile
+  p0s[1] = (int64_t)r * a.c + (int64_t)t * BQ;                                      // own tile
+
+  // a device error recorded earlier (sticky until the host resets it) skips the work
+  if (*(volatile int*)a.status != 0) return;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+      mbar_init(s_full(s), 1);
+      mbar_init(p_full(s), 128);
+      mbar_init(p_free(s), 1);
+    }
+    mbar_init(o_final, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) tma_prefetch_desc(&a.tm);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  uint32_t it = 0;          // KV tiles processed by this CTA so far (both q-tiles)
+  uint32_t k_issued = 0;    // producer: K/V stages issued
+  uint32_t q_issued = 0;    // producer: Q tiles issued
+  for (int tile = 0; tile < 2; ++tile) {
+    const int64_t p0 = p0s[tile];
+    const int n = (int)(p0 / BKV) + 1;
+    const int64_t qrow0 = zz_row_of_pos(p0, a.c, a.D);
+    if (warp == 4) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0 && !*abort_flag) {
+        mbar_arrive_expect_tx(q_full, TILE_BYTES);
+        tma_load_2d(base + OFF_Q, &a.tm, h * DH, (int)qrow0, q_full);
+        tma_load_2d(base + OFF_Q + BOX_BYTES, &a.tm, h * DH + 64, (int)qrow0, q_full);
+        ++q_issued;
+        for (int j = 0; j < n; ++j) {
+          const uint32_t cur = it + j, st = cur & 1u;
+          if (!mbar_wait(kv_empty(st), ((cur >> 1) & 1u) ^ 1u, a.status, abort_flag, a.limit_ns))
+            break;
+          const int krow = (int)zz_row_of_pos((int64_t)j * BKV, a.c, a.D);
+          const uint32_t sk = base + OFF_K + st * TILE_BYTES, sv = base + OFF_V + st * TILE_BYTES;
+          mbar_arrive_expect_tx(k_full(st), TILE_BYTES);
+          tma_load_2d(sk, &a.tm, a.d + h * DH, krow, k_full(st));
+          tma_load_2d(sk + BOX_BYTES, &a.tm, a.d + h * DH + 64, krow, k_full(st));
+          mbar_arrive_expect_tx(v_full(st), TILE_BYTES);
+          tma_load_2d(sv, &a.tm, 2 * a.d + h * DH, krow, v_full(st));
+          tma_load_2d(sv + BOX_BYTES, &a.tm, 2 * a.d + h * DH + 64, krow, v_full(st));
+          ++k_issued;
+        }
+      }
+    } else if (warp == 5) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0 && !*abort_flag) {
+        constexpr uint32_t idesc_s = idesc_f16_f32(BQ, BKV, false, false, false);
+        constexpr uint32_t idesc_o = idesc_f16_f32(BQ, DH, false, true, false);
+        bool ok = mbar_wait(q_full, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
+        auto issue_s = [&](uint32_t cur) -> bool {
+          const uint32_t st = cur & 1u;
+          if (!mbar_wait(k_full(st), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns)) return false;
+          tc_fence_after();
+          const uint32_t sq = base + OFF_Q, sk = base + OFF_K + st * TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < DH / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+            umma_f16_ss(tmem + TM_S + st * 128, sdesc_sw128(sq + off, 16, 1024),
+                        sdesc_sw128(sk + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full(st));
+          return true;
+        };
+        if (ok) ok = issue_s(it);
+        for (int j = 0; j < n && ok; ++j) {
+          const uint32_t cur = it + j, b = cur & 1u;
+          if (j + 1 < n && !(ok = issue_s(cur + 1))) break;
+          if (!mbar_wait(p_full(b), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns) ||
+              !mbar_wait(v_full(b), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sp = base + OFF_P + b * TILE_BYTES, sv = base + OFF_V + b * TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BKV / 16; ++kk) {
+            const uint32_t poff = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+            umma_f16_ss(tmem + TM_O, sdesc_sw128(sp + poff, 16, 1024),
+                        sdesc_sw128(sv + kk * 2048, BOX_BYTES, 1024), idesc_o,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(kv_empty(b));
+          umma_commit(p_free(b));
+        }
+        if (ok) {
+          umma_commit(o_final);
+        } else {
+          umma_commit(drain_bar);
+          drain_wait(drain_bar, 0, a.limit_ns);
+        }
+      }
+    } else {
+      // ------------------------------------------------------------ softmax
+      const int row = warp * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        const uint32_t cur = it + j, b = cur & 1u;
+        if (!mbar_wait(s_full(b), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(lane_base + TM_S + b * 128 + q * 32, sr[q]);
+        tmem_wait_ld();
+        const bool diag = (j == n - 1);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float v = __uint_as_float(sr[q][e]) * a.scale_log2;
+            if (diag && q * 32 + e > row) v = -INFINITY;
+            sr[q][e] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
+          }
+        // lazy rescale, decided per warp (TMEM access is warp-collective)
+        const bool mine = mx > m_used + RESCALE_LOG2;
+        if (__any_sync(0xffffffffu, mine)) {
+          const float m_new = mine ? mx : m_used;
+          const float alpha = ex2_approx(m_used - m_new);   // 0 on the first tile, 1 if unchanged
+          l *= alpha;
+          m_used = m_new;
+          if (j > 0) {
+            // O must hold PV(cur-1) before it is rescaled
+            const uint32_t pb = (cur - 1) & 1u;
+            if (!mbar_wait(p_free(pb), ((cur - 1) >> 1) & 1u, a.status, abort_flag, a.limit_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+              uint32_t ov[32];
+              tmem_ld32(lane_base + TM_O + q * 32, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              tmem_st32(lane_base + TM_O + q * 32, ov);
+            }
+            tmem_wait_st();
+          }
+        }
+        // P buffer b was last read by PV(cur-2)
+        if (cur >= 2 &&
+            !mbar_wait(p_free(b), (((cur - 2) >> 1) & 1u), a.status, abort_flag, a.limit_ns)) {
+          ok = false;
+          break;
+        }
+        float sum = 0.f;
+        uint8_t* prow = gbase + OFF_P + b * TILE_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0v = ex2_approx(__uint_as_float(sr[q][e]) - m_used);
+            const float p1v = ex2_approx(__uint_as_float(sr[q][e + 1]) - m_used);
+            sum += p0v + p1v;
+            pk[e >> 1] = pack_f16(p0v, p1v);
+          }
+          // keys q*32 .. q*32+31 -> box (q >> 1), 16-byte chunks 4*(q&1) .. +3
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int chunk = (q & 1) * 4 + c;
+            uint4* dst = reinterpret_cast<uint4*>(prow + (q >> 1) * BOX_BYTES +
+                                                  ((chunk ^ (row & 7)) << 4));
+            *dst = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          }
+        }
+        l += sum;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(p_full(b));
+      }
+      // epilogue: O / l -> fp16 rows, LSE
+      if (ok && mbar_wait(o_final, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns)) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        ct_t* orow = a.o + (qrow0 + row) * (int64_t)a.d + h * DH;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          uint32_t ov[32];
+          tmem_ld32(lane_base + TM_O + q * 32, ov);
+          tmem_wait_ld();
+          uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            dst[c] = make_uint4(
+                pack_f16(__uint_as_float(ov[8 * c + 0]) * inv, __uint_as_float(ov[8 * c + 1]) * inv),
+                pack_f16(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv),
+                pack_f16(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv),
+                pack_f16(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv));
+        }
+        constexpr float LN2 = 0.69314718055994530942f;
+        a.lse[(int64_t)h * a.S + qrow0 + row] = (m_used + __log2f(l)) * LN2;
+      }
+      tc_fence_before();
+    }
+    it += (uint32_t)n;
+    __syncthreads();  // Q, O and the barriers' phases are reused by the next q-tile
+    tc_fence_after();
+  }
+  // drain: copies the producer issued that nobody consumed (abort path only)
+  if (warp == 4 && lane == 0 && *abort_flag) {
+    const uint32_t n_out = k_issued < 2u ? k_issued : 2u;
+    for (uint32_t jj = k_issued - n_out; jj < k_issued; ++jj) {
+      drain_wait(k_full(jj & 1u), (jj >> 1) & 1u, a.limit_ns);
+      drain_wait(v_full(jj & 1u), (jj >> 1) & 1u, a.limit_ns);
+    }
+    if (q_issued > 0) drain_wait(q_full, (q_issued - 1) & 1u, a.limit_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn_attn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
 }
 
 }  // namespace
 
-int attn_fwd_smem_bytes() { return SMEM; }
-
 tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, int H, int dh,
-                                int D, cudaStream_t st) {
+                               int D, cudaStream_t st) {
   if (dh != DH) return TSP_ERR_UNSUPPORTED;
   const int64_t c = S / (2 * D);
   if (c % BQ != 0) return TSP_ERR_UNSUPPORTED;
-  AttnArgs a;
-  a.qkv = (const ct_t*)qkv;
-  a.o = (ct_t*)o;
-  a.lse = lse;
-  a.S = S;
-  a.c = c;
-  a.D = D;
-  a.H = H;
-  a.d = H * dh;
-  a.n_tiles = (int)(c / BQ);
-  a.scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
+  if (S > (int64_t)INT32_MAX) return TSP_ERR_UNSUPPORTED;
+  const int d = H * dh;
+  if (((uintptr_t)qkv & 15u) || ((3 * d * 2) % 16)) return TSP_ERR_INVALID_ARG;
+  TcAttnArgs* a = new TcAttnArgs();
+  std::unique_ptr<TcAttnArgs> guard(a);
+  memset(a, 0, sizeof(TcAttnArgs));
+  EncodeTiledFn fn = encode_fn_attn();
+  if (!fn) return TSP_ERR_CUDA;
+  const cuuint64_t dims[2] = {(cuuint64_t)(3 * d), (cuuint64_t)S};
+  const cuuint64_t strides[1] = {(cuuint64_t)(3 * d * 2)};
+  const cuuint32_t box[2] = {64u, 128u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  if (fn(&a->tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(qkv), dims, strides, box,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return TSP_ERR_CUDA;
+  a->o = (ct_t*)o;
+  a->lse = lse;
+  a->S = S;
+  a->c = c;
+  a->D = D;
+  a->d = d;
+  a->n_tiles = (int)(c / BQ);
+  a->scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
+  a->status = status_word();
+  a->limit_ns = wait_limit_ns();
   static bool attr = false;
   if (!attr) {
-    TSP_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_zigzag_kernel,
+    TSP_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_tc_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM));
     attr = true;
   }
-  dim3 grid((unsigned)(D * a.n_tiles), (unsigned)H);
+  dim3 grid((unsigned)(D * a->n_tiles), (unsigned)H);
   Prof prof("attn_fwd", st);
-  attn_fwd_zigzag_kernel<<<grid, NTHR, SMEM, st>>>(a);
+  attn_fwd_tc_kernel<<<grid, NTHR, SMEM, st>>>(*a);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }

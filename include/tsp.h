@@ -48,6 +48,8 @@
  *    nothing is launched.  Launch failures return TSP_ERR_CUDA.  Errors the
  *    device detects (a pipeline wait that exceeded its time limit) set a
  *    sticky device status word read by tsp_device_status; kernels never trap.
+ *    While the word holds an error, the tensor-core kernels return without
+ *    doing their work, until tsp_device_status(stream, 1) clears it.
  *  - All pointers must be 16-byte aligned; row strides are dense.
  */
 #ifndef TSP_H_
