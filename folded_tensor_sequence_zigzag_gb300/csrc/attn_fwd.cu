@@ -16,15 +16,17 @@
 // last row are never visited; only the diagonal 128-key tile is masked.
 //
 // Per KV tile j (128 keys), warp-specialised:
-//   warp 4   TMA producer: Q once per q-tile, K_j and V_j into a 2-stage ring
+//   warp 8   TMA producer: Q once per q-tile, K_j and V_j into a 2-stage ring
 //            (128-byte swizzle; Q, K, V are column boxes of the Q|K|V buffer);
-//   warp 5   TMEM allocator + MMA issuer: S_j = Q K_j^T into one of two
+//   warp 9   TMEM allocator + MMA issuer: S_j = Q K_j^T into one of two
 //            128-column TMEM buffers (issued one tile ahead), then
 //            O += P_j V_j into a 128-column TMEM accumulator, with V read
 //            MN-major (dh contiguous) straight from the buffer;
-//   warps 0-3 softmax: thread = query row = TMEM lane; loads its S row,
-//            p = 2^(s*scale*log2e - m), writes P_j as fp16 into swizzled
-//            shared memory (double-buffered, the A operand of the PV MMA).
+//   warps 0-7 softmax: query row = TMEM lane; warps w and w+4 share 32 rows,
+//            each thread owning 64 of the 128 key columns (the row max is
+//            exchanged through shared memory); p = 2^(s*scale*log2e - m) with
+//            one FFMA + MUFU ex2 per score, written as fp16 into swizzled
+//            shared memory (the A operand of the PV MMA).
 // The running max m is only raised (and O rescaled in TMEM) when a warp's
 // row max grows by more than 2^8 -- the result O/l is exact either way and
 // p stays below 256.  All mbarrier waits are bounded (TSP_ERR_TIMEOUT).
@@ -39,18 +41,37 @@ namespace tsp {
 namespace {
 
 constexpr int BQ = 128, BKV = 128, DH = 128;
-constexpr int NTHR = 192;
+constexpr int NSOFT = 256;                 // 8 softmax warps: two threads per query row
+constexpr int NTHR = NSOFT + 64;           // + producer warp + MMA warp
+constexpr int WARP_PROD = 8, WARP_MMA = 9;
 constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128x128 fp16 tile (two 64-column boxes)
 constexpr int BOX_BYTES = TILE_BYTES / 2;  // 128 rows x 64 columns
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + TILE_BYTES;        // 2 stages
 constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;    // 2 stages
-constexpr int OFF_P = OFF_V + 2 * TILE_BYTES;    // 2 buffers
-constexpr int OFF_BAR = OFF_P + 2 * TILE_BYTES;
+constexpr int OFF_P = OFF_V + 2 * TILE_BYTES;    // 1 buffer
+constexpr int OFF_X = OFF_P + TILE_BYTES;        // row-max exchange [2][2][128] + row-sum [2][128]
+constexpr int OFF_BAR = OFF_X + 3 * 1024;
 constexpr int SMEM = OFF_BAR + 256 + 1024;       // + 1 KB alignment slack
 constexpr uint32_t TMEM_COLS = 512;              // S0 | S1 | O | (unused)
 constexpr uint32_t TM_S = 0, TM_O = 256;
 constexpr float RESCALE_LOG2 = 8.0f;             // lazy-rescale threshold (log2 units)
+
+// Named barrier over the softmax warps that also ANDs a predicate: every
+// participant leaves with the same verdict, so a loop exit taken on a failed
+// (timed-out) wait is uniform and nobody is left at a barrier.
+__device__ __forceinline__ bool softmax_bar_and(bool pred) {
+  uint32_t res;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(res)
+      : "r"(pred ? 1u : 0u), "r"(NSOFT)
+      : "memory");
+  return res != 0;
+}
 
 struct TcAttnArgs {
   CUtensorMap tm;       // Q|K|V buffer [S rows, 3d cols] fp16, box {64, 128}, 128B swizzle
@@ -82,8 +103,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
   auto v_full = [&](int s) { return bars + 8u * (3 + s); };
   auto kv_empty = [&](int s) { return bars + 8u * (5 + s); };
   auto s_full = [&](int b) { return bars + 8u * (7 + b); };
-  auto p_full = [&](int b) { return bars + 8u * (9 + b); };
-  auto p_free = [&](int b) { return bars + 8u * (11 + b); };
+  const uint32_t p_full = bars + 8u * 9;
+  const uint32_t p_free = bars + 8u * 10;
   const uint32_t o_final = bars + 8u * 13;
   const uint32_t drain_bar = bars + 8u * 14;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 160);
@@ -106,20 +127,20 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
       mbar_init(v_full(s), 1);
       mbar_init(kv_empty(s), 1);
       mbar_init(s_full(s), 1);
-      mbar_init(p_full(s), 128);
-      mbar_init(p_free(s), 1);
     }
+    mbar_init(p_full, NSOFT);
+    mbar_init(p_free, 1);
     mbar_init(o_final, 1);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 5) {
+  if (warp == WARP_MMA) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) tma_prefetch_desc(&a.tm);
+  if (warp == WARP_PROD && lane == 0) tma_prefetch_desc(&a.tm);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -132,7 +153,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
     const int64_t p0 = p0s[tile];
     const int n = (int)(p0 / BKV) + 1;
     const int64_t qrow0 = zz_row_of_pos(p0, a.c, a.D);
-    if (warp == 4) {
+    if (warp == WARP_PROD) {
       // ------------------------------------------------------------ producer
       if (lane == 0 && !*abort_flag) {
         mbar_arrive_expect_tx(q_full, TILE_BYTES);
@@ -154,7 +175,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
           ++k_issued;
         }
       }
-    } else if (warp == 5) {
+    } else if (warp == WARP_MMA) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0 && !*abort_flag) {
         constexpr uint32_t idesc_s = idesc_f16_f32(BQ, BKV, false, false, false);
@@ -178,13 +199,13 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
         for (int j = 0; j < n && ok; ++j) {
           const uint32_t cur = it + j, b = cur & 1u;
           if (j + 1 < n && !(ok = issue_s(cur + 1))) break;
-          if (!mbar_wait(p_full(b), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns) ||
+          if (!mbar_wait(p_full, cur & 1u, a.status, abort_flag, a.limit_ns) ||
               !mbar_wait(v_full(b), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sp = base + OFF_P + b * TILE_BYTES, sv = base + OFF_V + b * TILE_BYTES;
+          const uint32_t sp = base + OFF_P, sv = base + OFF_V + b * TILE_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk) {
             const uint32_t poff = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
@@ -193,7 +214,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
                         (j > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(kv_empty(b));
-          umma_commit(p_free(b));
+          umma_commit(p_free);
         }
         if (ok) {
           umma_commit(o_final);
@@ -204,100 +225,112 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
       }
     } else {
       // ------------------------------------------------------------ softmax
-      const int row = warp * 32 + lane;
-      const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+      const int quarter = warp & 3, half = warp >> 2;
+      const int row = quarter * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+      float* xmax = reinterpret_cast<float*>(gbase + OFF_X);  // [2 parity][2 half][128 rows]
+      float* lsum = xmax + 512;                               // [2 half][128 rows]
+      uint8_t* prow = gbase + OFF_P + half * BOX_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
-      for (int j = 0; j < n && ok; ++j) {
+      for (int j = 0; j < n; ++j) {
         const uint32_t cur = it + j, b = cur & 1u;
-        if (!mbar_wait(s_full(b), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t sr[4][32];
+        bool okl = ok && mbar_wait(s_full(b), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns);
+        okl = __all_sync(0xffffffffu, okl);
+        uint32_t sr[2][32];
+        float mxp = -INFINITY;
+        if (okl) {
+          tc_fence_after();
+          tmem_ld32(lane_base + TM_S + b * 128 + half * 64, sr[0]);
+          tmem_ld32(lane_base + TM_S + b * 128 + half * 64 + 32, sr[1]);
+          tmem_wait_ld();
+          if (j == n - 1) {  // diagonal tile: key index > query index is masked
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(lane_base + TM_S + b * 128 + q * 32, sr[q]);
-        tmem_wait_ld();
-        const bool diag = (j == n - 1);
-        float mx = -INFINITY;
+            for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float v = __uint_as_float(sr[q][e]) * a.scale_log2;
-            if (diag && q * 32 + e > row) v = -INFINITY;
-            sr[q][e] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
+              for (int e = 0; e < 32; ++e)
+                if (half * 64 + q * 32 + e > row) sr[q][e] = __float_as_uint(-INFINITY);
           }
-        // lazy rescale, decided per warp (TMEM access is warp-collective)
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mxp = fmaxf(mxp, __uint_as_float(sr[q][e]));
+          xmax[b * 256 + half * 128 + row] = mxp;
+        }
+        ok = softmax_bar_and(okl);
+        if (!ok) break;
+        const float mx = fmaxf(mxp, xmax[b * 256 + (1 - half) * 128 + row]) * a.scale_log2;
+        // lazy rescale, decided per warp (TMEM access is warp-collective); the
+        // two warps of a row pair see the same maxima and decide alike
         const bool mine = mx > m_used + RESCALE_LOG2;
-        if (__any_sync(0xffffffffu, mine)) {
+        const bool resc = __any_sync(0xffffffffu, mine);
+        float alpha = 1.f;
+        if (resc) {
           const float m_new = mine ? mx : m_used;
-          const float alpha = ex2_approx(m_used - m_new);   // 0 on the first tile, 1 if unchanged
+          alpha = ex2_approx(m_used - m_new);   // 0 on the first tile, 1 if unchanged
           l *= alpha;
           m_used = m_new;
-          if (j > 0) {
-            // O must hold PV(cur-1) before it is rescaled
-            const uint32_t pb = (cur - 1) & 1u;
-            if (!mbar_wait(p_free(pb), ((cur - 1) >> 1) & 1u, a.status, abort_flag, a.limit_ns)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-              uint32_t ov[32];
-              tmem_ld32(lane_base + TM_O + q * 32, ov);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-              tmem_st32(lane_base + TM_O + q * 32, ov);
-            }
-            tmem_wait_st();
+        }
+        // PV(cur-1) must have finished before P is overwritten or O rescaled
+        if (cur >= 1) {
+          bool wok = mbar_wait(p_free, (cur - 1) & 1u, a.status, abort_flag, a.limit_ns);
+          if (!__all_sync(0xffffffffu, wok)) {
+            ok = false;
+            continue;  // the next vote (or the epilogue's) takes everyone out
           }
+          tc_fence_after();
         }
-        // P buffer b was last read by PV(cur-2)
-        if (cur >= 2 &&
-            !mbar_wait(p_free(b), (((cur - 2) >> 1) & 1u), a.status, abort_flag, a.limit_ns)) {
-          ok = false;
-          break;
-        }
-        float sum = 0.f;
-        uint8_t* prow = gbase + OFF_P + b * TILE_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
+        if (resc && j > 0) {
+#pragma unroll 1
+          for (int q = 0; q < 2; ++q) {
+            uint32_t ov[32];
+            tmem_ld32(lane_base + TM_O + half * 64 + q * 32, ov);
+            tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(lane_base + TM_O + half * 64 + q * 32, ov);
+          }
+          tmem_wait_st();
+        }
+        const float neg_m = -m_used;
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float p0v = ex2_approx(__uint_as_float(sr[q][e]) - m_used);
-            const float p1v = ex2_approx(__uint_as_float(sr[q][e + 1]) - m_used);
+            const float p0v = ex2_approx(fmaf(__uint_as_float(sr[q][e]), a.scale_log2, neg_m));
+            const float p1v = ex2_approx(fmaf(__uint_as_float(sr[q][e + 1]), a.scale_log2, neg_m));
             sum += p0v + p1v;
             pk[e >> 1] = pack_f16(p0v, p1v);
           }
-          // keys q*32 .. q*32+31 -> box (q >> 1), 16-byte chunks 4*(q&1) .. +3
+          // keys half*64 + q*32 .. +31 -> 16-byte chunks 4q .. 4q+3 of box `half`
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const int chunk = (q & 1) * 4 + c;
-            uint4* dst = reinterpret_cast<uint4*>(prow + (q >> 1) * BOX_BYTES +
-                                                  ((chunk ^ (row & 7)) << 4));
-            *dst = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            const int chunk = q * 4 + c;
+            *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
           }
         }
         l += sum;
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(p_full(b));
+        mbar_arrive(p_full);
       }
       // epilogue: O / l -> fp16 rows, LSE
-      if (ok && mbar_wait(o_final, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns)) {
+      bool eok = ok && mbar_wait(o_final, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
+      eok = __all_sync(0xffffffffu, eok);
+      if (eok) lsum[half * 128 + row] = l;
+      eok = softmax_bar_and(eok);
+      if (eok) {
         tc_fence_after();
-        const float inv = 1.f / l;
-        ct_t* orow = a.o + (qrow0 + row) * (int64_t)a.d + h * DH;
+        const float l_tot = l + lsum[(1 - half) * 128 + row];
+        const float inv = 1.f / l_tot;
+        ct_t* orow = a.o + (qrow0 + row) * (int64_t)a.d + h * DH + half * 64;
 #pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
           uint32_t ov[32];
-          tmem_ld32(lane_base + TM_O + q * 32, ov);
+          tmem_ld32(lane_base + TM_O + half * 64 + q * 32, ov);
           tmem_wait_ld();
           uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
 #pragma unroll
@@ -308,8 +341,10 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
                 pack_f16(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv),
                 pack_f16(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv));
         }
-        constexpr float LN2 = 0.69314718055994530942f;
-        a.lse[(int64_t)h * a.S + qrow0 + row] = (m_used + __log2f(l)) * LN2;
+        if (half == 0) {
+          constexpr float LN2 = 0.69314718055994530942f;
+          a.lse[(int64_t)h * a.S + qrow0 + row] = (m_used + __log2f(l_tot)) * LN2;
+        }
       }
       tc_fence_before();
     }
@@ -318,7 +353,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
     tc_fence_after();
   }
   // drain: copies the producer issued that nobody consumed (abort path only)
-  if (warp == 4 && lane == 0 && *abort_flag) {
+  if (warp == WARP_PROD && lane == 0 && *abort_flag) {
     const uint32_t n_out = k_issued < 2u ? k_issued : 2u;
     for (uint32_t jj = k_issued - n_out; jj < k_issued; ++jj) {
       drain_wait(k_full(jj & 1u), (jj >> 1) & 1u, a.limit_ns);
@@ -328,7 +363,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == WARP_MMA) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
