@@ -271,6 +271,7 @@ def run_gpu(args):
         wsb = torch.empty(tsp.workspace_bytes(cfg, tsp.TSP_OP_BLOCK_BWD), dtype=torch.uint8, device=dev)
         dy = inp["dy"].to(dev)
         dyz = torch.empty_like(dy)
+        y = torch.empty(x.shape, dtype=torch.float32, device=dev)  # dx (fp32) in global order
 
     def step(xin):
         tsp.zigzag_permute(xin, D, out=xz)

@@ -420,7 +420,7 @@ tsp_status check_mlp_w(const tsp_mlp_w* w, bool need_norm) {
 // Backward (defined below the C entry points' helpers)
 // ----------------------------------------------------------------------------
 tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const void* saved,
-                          const tsp_attn_w* aw, const tsp_mlp_w* mw, void* dx, float* dwq,
+                          const tsp_attn_w* aw, const tsp_mlp_w* mw, float* dx, float* dwq,
                           float* dwk, float* dwv, float* dwo, float* dw1, float* dw3, float* dw2,
                           float* dg_attn, float* dg_mlp, void* ws, cudaStream_t st);
 
@@ -552,7 +552,7 @@ tsp_status tsp_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* 
 }
 
 tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z, const void* saved,
-                         const tsp_attn_w* aw, const tsp_mlp_w* mw, void* dx_z, float* dwq,
+                         const tsp_attn_w* aw, const tsp_mlp_w* mw, float* dx_z, float* dwq,
                          float* dwk, float* dwv, float* dwo, float* dw1, float* dw3, float* dw2,
                          float* dg_attn, float* dg_mlp, void* ws, size_t ws_bytes, void* stream) {
   tsp_status r = check_cfg(cfg);
@@ -634,7 +634,7 @@ tsp_status tsp_device_status(void* stream, int32_t reset) {
 namespace tsp {
 
 tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const void* saved,
-                          const tsp_attn_w* aw, const tsp_mlp_w* mw, void* dx, float* dwq,
+                          const tsp_attn_w* aw, const tsp_mlp_w* mw, float* dx, float* dwq,
                           float* dwk, float* dwv, float* dwo, float* dw1, float* dw3, float* dw2,
                           float* dg_attn, float* dg_mlp, void* ws, cudaStream_t st) {
   const int64_t S = c->S;
@@ -744,9 +744,9 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
       g.epi = EPI_F32; g.out = W.da; g.ldo = d; g.name = "gemm_dgrad_qkv";
       if ((r = gemm_tc(g, st)) != TSP_OK) return r;
     }
-    // dx = dh + RMSNorm_1'(da)
+    // dx = dh + RMSNorm_1'(da), fp32
     return launch_rmsnorm_bwd((const float*)W.da, x, TY_BF16, aw->g_attn, A.rstd1,
-                              (const float*)W.dh_f32, nullptr, nullptr, dx, TY_BF16, dg_attn,
+                              (const float*)W.dh_f32, nullptr, dx, nullptr, TY_BF16, dg_attn,
                               W.dg_part, S, d, c->dtype, st);
   }
 
@@ -815,7 +815,7 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
                              j > 0, st)) != TSP_OK)
       return r;
   }
-  return launch_rmsnorm_bwd(da, x, TY_F32, aw->g_attn, A.rstd1, dhf, nullptr, (float*)dx, nullptr,
+  return launch_rmsnorm_bwd(da, x, TY_F32, aw->g_attn, A.rstd1, dhf, nullptr, dx, nullptr,
                             TY_F32, dg_attn, W.dg_part, S, d, c->dtype, st);
 }
 

@@ -35,6 +35,8 @@ constexpr int OFF_DO = OFF_Q + 2 * SQ_BYTES;
 constexpr int OFF_DS = OFF_DO + 2 * SQ_BYTES;
 constexpr int OFF_L = OFF_DS + SDS_BYTES;    // float L[2][64], Dl[2][64]
 constexpr int SMEM = OFF_L + 4 * BR * 4;
+constexpr float kOperandScale = 256.f;            // P, dS scaling into fp16's normal range
+constexpr float kOperandUnscale = 1.f / 256.f;
 
 __device__ __forceinline__ uint32_t swz(int row, int col) {
   return (uint32_t)(row * ROWB + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
@@ -180,7 +182,16 @@ __device__ void key_tile(const BwdArgs& a, int h, int64_t k0, uint8_t* smem) {
           dp[i][2 + e] = p1 * (dp[i][2 + e] - dl);
         }
       }
-      // dV += P^T dO ; dK += dS^T Q   (k-dimension = 64 queries)
+      // dV += P^T dO ; dK += dS^T Q   (k-dimension = 64 queries).  P and dS
+      // enter the fp16 MMAs scaled by 2^8 so that small probabilities stay in
+      // fp16's normal range; the accumulators are scaled back at the end.
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          st[i][e] *= kOperandScale;
+          dp[i][e] *= kOperandScale;
+        }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         const uint32_t pa[4] = {pack_f16(st[2 * ks][0], st[2 * ks][1]),
@@ -249,10 +260,9 @@ __device__ void key_tile(const BwdArgs& a, int h, int64_t k0, uint8_t* smem) {
       float* dst_hi = dst_lo + 8 * (int64_t)a.d;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        atomicAdd(reinterpret_cast<float2*>(dst_lo + i * 8),
-                  make_float2(acc[i][0] * a.scale, acc[i][1] * a.scale));
-        atomicAdd(reinterpret_cast<float2*>(dst_hi + i * 8),
-                  make_float2(acc[i][2] * a.scale, acc[i][3] * a.scale));
+        const float sc = a.scale * kOperandUnscale;
+        atomicAdd(reinterpret_cast<float2*>(dst_lo + i * 8), make_float2(acc[i][0] * sc, acc[i][1] * sc));
+        atomicAdd(reinterpret_cast<float2*>(dst_hi + i * 8), make_float2(acc[i][2] * sc, acc[i][3] * sc));
       }
     }
     cp_async_wait_all();
@@ -262,13 +272,16 @@ __device__ void key_tile(const BwdArgs& a, int h, int64_t k0, uint8_t* smem) {
   const int64_t row_lo = krow0 + warp * 16 + (lane >> 2), row_hi = row_lo + 8;
   ct_t* dk_lo = a.dqkv + row_lo * ld + a.d + h * DH;
   ct_t* dk_hi = a.dqkv + row_hi * ld + a.d + h * DH;
+  const float skk = a.scale * kOperandUnscale;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int col = i * 8 + (lane & 3) * 2;
-    *reinterpret_cast<uint32_t*>(dk_lo + col) = pack_f16(dk[i][0] * a.scale, dk[i][1] * a.scale);
-    *reinterpret_cast<uint32_t*>(dk_hi + col) = pack_f16(dk[i][2] * a.scale, dk[i][3] * a.scale);
-    *reinterpret_cast<uint32_t*>(dk_lo + a.d + col) = pack_f16(dv[i][0], dv[i][1]);
-    *reinterpret_cast<uint32_t*>(dk_hi + a.d + col) = pack_f16(dv[i][2], dv[i][3]);
+    *reinterpret_cast<uint32_t*>(dk_lo + col) = pack_f16(dk[i][0] * skk, dk[i][1] * skk);
+    *reinterpret_cast<uint32_t*>(dk_hi + col) = pack_f16(dk[i][2] * skk, dk[i][3] * skk);
+    *reinterpret_cast<uint32_t*>(dk_lo + a.d + col) =
+        pack_f16(dv[i][0] * kOperandUnscale, dv[i][1] * kOperandUnscale);
+    *reinterpret_cast<uint32_t*>(dk_hi + a.d + col) =
+        pack_f16(dv[i][2] * kOperandUnscale, dv[i][3] * kOperandUnscale);
   }
   __syncthreads();
 }

@@ -222,14 +222,14 @@ GRAD_NAMES = ("dwq", "dwk", "dwv", "dwo", "dw1", "dw3", "dw2", "dg_attn", "dg_ml
 
 
 def block_bwd(cfg: Cfg, x_z, dy_z, saved, W: BlockWeights, ws=None, stream=None) -> dict:
-    """Gradients of sum(dy * y): dx_z (activation dtype) and fp32 weight/gain grads."""
+    """Gradients of sum(dy * y), all fp32: dx_z (zigzag order) and the weight/gain grads."""
     _require_cuda(x_z, dy_z, saved)
     dev = x_z.device
     d, I = cfg.d, cfg.inter
     shapes = {"dwq": (d, d), "dwk": (d, d), "dwv": (d, d), "dwo": (d, d), "dw1": (I, d),
               "dw3": (I, d), "dw2": (d, I), "dg_attn": (d,), "dg_mlp": (d,)}
     g = {k: torch.empty(shapes[k], dtype=torch.float32, device=dev) for k in GRAD_NAMES}
-    g["dx"] = torch.empty_like(x_z)
+    g["dx"] = torch.empty(x_z.shape, dtype=torch.float32, device=dev)
     ws = _ws(workspace_bytes(cfg, TSP_OP_BLOCK_BWD), dev) if ws is None else ws
     aw, mw = W.attn(), W.mlp()
     _check(load().tsp_block_bwd(ctypes.byref(cfg), _ptr(x_z), _ptr(dy_z), _ptr(saved),

@@ -183,14 +183,17 @@ tsp_status tsp_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* 
 
 /* Whole block backward of L = sum(dy * y).  Inputs: x_z and dy_z ([S, d]
  * zigzag, cfg dtype), saved (filled by tsp_block_fwd with the same cfg,
- * weights and x_z).  Outputs: dx_z ([S, d] zigzag, cfg dtype) and fp32
- * gradients dwq, dwk, dwv, dwo [d, d], dw1, dw3 [inter, d], dw2 [d, inter],
- * dg_attn, dg_mlp [d] -- each the sum over the D virtual ranks' token rows
- * (the reduction TSP performs toward the shard owners).
+ * weights and x_z).  Outputs, all fp32: dx_z ([S, d] zigzag -- the gradient
+ * of the residual stream, kept in fp32 like the stream itself: at early
+ * positions, which every later query attends, it reaches ~10x its RMS, where
+ * a bf16 result would lose more than the bf16 path's error budget to its own
+ * rounding) and the gradients dwq, dwk, dwv, dwo [d, d], dw1, dw3 [inter, d],
+ * dw2 [d, inter], dg_attn, dg_mlp [d] -- each the sum over the D virtual
+ * ranks' token rows (the reduction TSP performs toward the shard owners).
  * ws: tsp_workspace_bytes(cfg, TSP_OP_BLOCK_BWD). */
 tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z,
                          const void* saved, const tsp_attn_w* aw, const tsp_mlp_w* mw,
-                         void* dx_z, float* dwq, float* dwk, float* dwv, float* dwo,
+                         float* dx_z, float* dwq, float* dwk, float* dwv, float* dwo,
                          float* dw1, float* dw3, float* dw2, float* dg_attn, float* dg_mlp,
                          void* ws, size_t ws_bytes, void* stream);
 

@@ -512,3 +512,44 @@ def block_bwd_sharded(x, W, dy, H, D, eps):
     dx[pos] = dxz
     grads["dx"] = dx
     return grads
+
+
+def block_bwd_tail(x, W, dy, H, eps, n_tail):
+    """dx of L = sum(dy * y) at the last n_tail positions, exactly.
+
+    A key at position >= S - n_tail is attended only by queries at positions
+    >= its own, all inside the tail, so its dK and dV are complete once the
+    tail queries are back-propagated; dQ of a tail query needs every key, which
+    only takes the K/V projections of all rows.  Everything else is row-local.
+    Returns dx[S - n_tail:] (global order).
+    """
+    x = f64(x)
+    dy = f64(dy)
+    S = x.shape[0]
+    t0 = S - n_tail
+    g1, g2 = _w(W, "g_attn"), _w(W, "g_mlp")
+    wq, wk, wv, wo = (_w(W, n) for n in ("wq", "wk", "wv", "wo"))
+    w1, w3, w2 = _w(W, "w1"), _w(W, "w3"), _w(W, "w2")
+    a_all, rstd1 = rmsnorm(x, g1, eps)
+    K = a_all @ wk.T
+    V = a_all @ wv.T
+    tail = np.arange(t0, S)
+    keys = np.arange(S)
+    Q_t = a_all[t0:] @ wq.T
+    O_t, _ = causal_attention(Q_t, K, V, H, q_pos=tail, k_pos=keys)
+    h_t = x[t0:] + O_t @ wo.T
+    b_t, rstd2 = rmsnorm(h_t, g2, eps)
+    A = b_t @ w1.T
+    B = b_t @ w3.T
+    sA = sigmoid(A)
+    dG = dy[t0:] @ w2
+    dA = dG * B * sA * (1.0 + A * (1.0 - sA))
+    dB = dG * A * sA
+    du2, _ = rmsnorm_bwd(dA @ w1 + dB @ w3, h_t, g2, rstd2)
+    dh_t = dy[t0:] + du2
+    dO_t = dh_t @ wo
+    dQ_t, dK, dV = causal_attention_bwd(Q_t, K, V, O_t, dO_t, H, q_pos=tail, k_pos=keys)
+    da = dQ_t @ wq + dK[t0:] @ wk + dV[t0:] @ wv
+    du1, _ = rmsnorm_bwd(da, x[t0:], g1, rstd1[t0:])
+    return dh_t + du1
+

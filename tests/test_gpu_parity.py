@@ -251,3 +251,35 @@ def test_bf16_backward_small(S, d, H, I, D):
     ref = O.block_bwd(inp["x"], inp, inp["dy"], H, shape.eps)
     for k, v in ref.items():
         assert_bf16_close(g[k], v, f"bf16 {k}")
+
+
+# ------------------------------------------------------------------ training step at 7B shapes
+
+def test_7b_fwd_bwd_S8192_all_outputs():
+    """Config-5 shapes (d=4096, 32x128 heads, inter=11008, D=8) at S=8192:
+    every output of the training step against the dense float64 backward."""
+    shape = BlockShape(S=8192, d=4096, H=32, inter=11008, D=8)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=0, with_dy=True)
+    y, g = _run_bwd(shape, inp, torch.bfloat16)
+    yref, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+    assert_bf16_close(y, yref, "y (S=8192)")
+    ref = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
+    for k, v in ref.items():
+        assert_bf16_close(g[k], v, f"{k} (S=8192)")
+
+
+def test_7b_fwd_bwd_S32768_sampled():
+    """Config 5 at full size (S=32768, D=8): y on 256 seeded rows and dx on the
+    last 256 positions (both exact in the oracle), every gradient finite."""
+    S, D = 32768, 8
+    shape = BlockShape(S=S, d=4096, H=32, inter=11008, D=D)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=0, with_dy=True)
+    y, g = _run_bwd(shape, inp, torch.bfloat16)
+    rows = sample_rows(S, D).numpy()
+    assert_bf16_close(y[rows], O.block_fwd_rows(inp["x"], inp, shape.H, shape.eps, rows),
+                      "y (S=32768, sampled rows)")
+    n_tail = 256
+    dx_ref = O.block_bwd_tail(inp["x"], inp, inp["dy"], shape.H, shape.eps, n_tail)
+    assert_bf16_close(g["dx"][S - n_tail:], dx_ref, "dx (S=32768, last 256 positions)")
+    for k in ("dwq", "dwk", "dwv", "dwo", "dw1", "dw3", "dw2", "dg_attn", "dg_mlp"):
+        assert torch.isfinite(g[k]).all(), k

@@ -333,6 +333,14 @@ def test_backward_sharded_equals_unsharded(D):
         assert np.max(np.abs(gs[k] - ref)) <= 1e-12 * np.max(np.abs(ref)), k
 
 
+@pytest.mark.parametrize("n_tail", [1, 7, 24])
+def test_backward_tail_rows_equal_full_backward(n_tail):
+    shape, inp = _small(S=48, d=16, H=2, inter=24, D=3, seed=31)
+    full = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)["dx"]
+    tail = O.block_bwd_tail(inp["x"], inp, inp["dy"], shape.H, shape.eps, n_tail)
+    assert np.max(np.abs(tail - full[48 - n_tail:])) <= 1e-12 * np.max(np.abs(full))
+
+
 # --------------------------------------------------------------- planted mistakes
 
 def test_planted_mistakes_are_caught(monkeypatch):
