@@ -1,5 +1,6 @@
-// attn_bwd.cu -- causal flash-attention backward over the zigzag layout (fp16
-// tensor-core operands, fp32 accumulation).
+// attn_bwd.cu -- causal flash-attention backward over the zigzag layout on the
+// 5th-generation tensor cores (tcgen05.mma kind::f16, fp16 operands, fp32
+// accumulators in TMEM).
 //
 // Source: "Folding Tensor and Sequence Parallelism for Memory-Efficient
 // Transformer Training & Inference" (gist.science summary), section 2: the
@@ -10,14 +11,28 @@
 //   dS_ij = P_ij (dP_ij - Delta_i),
 //   dQ_i = scale sum_j dS_ij K_j,   dK_j = scale sum_i dS_ij Q_i.
 //
-// Work unit = one CTA = (head, virtual rank r, key tile t of 128 keys): it
-// owns key tile t of chunk r and the mirrored tile of chunk 2D-1-r, and walks
-// the 64-row query tiles at positions >= the key tile.  The two causal query
-// ranges add up to S + 128 rows for every (r, t), so CTAs are balanced.
-// Per CTA: 8 warps, warp w owns keys 16w..16w+15 of the tile and keeps its
-// dK, dV accumulators in registers; S^T and dP^T are computed key-major on
-// mma.sync m16n8k16; dS goes through shared memory for dQ, which is
-// accumulated in fp32 with vector atomics and converted to fp16 at the end.
+// Work unit = one CTA = (head, virtual rank r, key tile t of 128 keys): key
+// tile t of chunk r and the mirrored tile of chunk 2D-1-r, each walking the
+// 64-row query tiles at positions >= the tile; the two query ranges add up to
+// S + 128 rows for every (r, t), so CTAs are balanced.  Per query tile:
+//   warp 8   TMA producer: K, V once per key tile; Q_i, dO_i (+ LSE_i, Delta_i
+//            by bulk copy) into a 2-stage ring;
+//   warp 9   MMA issuer: S^T = K Q_i^T and dP^T = V dO_i^T (M = 128 keys,
+//            N = 64 queries) for tile i+1 as soon as tile i's were read; then
+//            dV += P^T dO_i, dK += dS^T Q_i (TMEM accumulators across every
+//            query tile) and dQ_i^T = K^T dS^T (M = 128 dh, N = 64 queries);
+//   warps 0-3 (thread = key = TMEM lane): P = 2^(s*scale*log2e - LSE*log2e),
+//            dS = P (dP - Delta), both written as fp16 (scaled by 2^8 to keep
+//            small probabilities in fp16's normal range) into swizzled smem,
+//            which serves as the K-major A operand of dV/dK and, unchanged, as
+//            the MN-major B operand of dQ^T; at the end dK, dV -> fp16 rows;
+//   warps 4-7 (thread = dh = TMEM lane): drain dQ_i^T from TMEM into the fp32
+//            dQ accumulator with warp-coalesced atomics.
+// All mbarrier waits are bounded (TSP_ERR_TIMEOUT) and every loop exit is
+// uniform across the threads that share a barrier.
+#include <cstring>
+#include <memory>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -25,282 +40,386 @@ namespace tsp {
 
 namespace {
 
-constexpr int BC = 128, BR = 64, DH = 128, NTHR = 256;
-constexpr int ROWB = DH * 2;                 // 256 bytes per row
-constexpr int SK_BYTES = BC * ROWB;          // 32 KB
-constexpr int SQ_BYTES = BR * ROWB;          // 16 KB
-constexpr int SDS_BYTES = BR * BC * 2;       // 16 KB
-constexpr int OFF_K = 0, OFF_V = SK_BYTES, OFF_Q = 2 * SK_BYTES;   // Q[2], dO[2] follow
-constexpr int OFF_DO = OFF_Q + 2 * SQ_BYTES;
-constexpr int OFF_DS = OFF_DO + 2 * SQ_BYTES;
-constexpr int OFF_L = OFF_DS + SDS_BYTES;    // float L[2][64], Dl[2][64]
-constexpr int SMEM = OFF_L + 4 * BR * 4;
-constexpr float kOperandScale = 256.f;            // P, dS scaling into fp16's normal range
+constexpr int BC = 128, BR = 64, DH = 128;
+constexpr int NTHR = 320;
+constexpr int WARP_PROD = 8, WARP_MMA = 9;
+constexpr int KT_BYTES = BC * DH * 2;      // 32 KB: 128 keys x 128 dh
+constexpr int QT_BYTES = BR * DH * 2;      // 16 KB: 64 queries x 128 dh
+constexpr int PT_BYTES = BC * BR * 2;      // 16 KB: 128 keys x 64 queries
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + KT_BYTES;
+constexpr int OFF_Q = OFF_V + KT_BYTES;          // 2 stages
+constexpr int OFF_DO = OFF_Q + 2 * QT_BYTES;     // 2 stages
+constexpr int OFF_P = OFF_DO + 2 * QT_BYTES;     // 2 buffers
+constexpr int OFF_DS = OFF_P + 2 * PT_BYTES;     // 2 buffers
+constexpr int OFF_L = OFF_DS + 2 * PT_BYTES;     // [2 stages][LSE 64 | Delta 64] floats
+constexpr int OFF_BAR = OFF_L + 2 * 2 * BR * 4;
+constexpr int SMEM = OFF_BAR + 256 + 1024;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DQ = 128, TM_DV = 256, TM_DK = 384;
+constexpr float kOperandScale = 256.f;           // P, dS scaling into fp16's normal range
 constexpr float kOperandUnscale = 1.f / 256.f;
 
-__device__ __forceinline__ uint32_t swz(int row, int col) {
-  return (uint32_t)(row * ROWB + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void load_rows(uint32_t sdst, const ct_t* g, int64_t ld,
-                                          int nrows) {
-  for (int i = threadIdx.x; i < nrows * 16; i += NTHR) {
-    const int row = i >> 4, ch = i & 15;
-    cp_async16(sdst + swz(row, ch * 8), g + (int64_t)row * ld + ch * 8);
-  }
-}
-
-struct BwdArgs {
-  const ct_t* qkv;  // [S, 3d]
-  const ct_t* dO;   // [S, d]
-  const float* lse;          // [H, S] natural log
-  const float* delta;        // [H, S]
-  float* dq_acc;             // [S, d] fp32, zeroed
-  ct_t* dqkv;       // [S, 3d]: dK, dV written here
+struct TcBwdArgs {
+  CUtensorMap tm_qkv;   // Q|K|V [S, 3d] fp16, box {64, 64}, 128B swizzle
+  CUtensorMap tm_do;    // dO [S, d] fp16, box {64, 64}, 128B swizzle
+  const float* lse;     // [H, S]
+  const float* delta;   // [H, S]
+  float* dq_acc;        // [S, d] fp32, zeroed
+  ct_t* dqkv;           // [S, 3d]: dK, dV written here
   int64_t S, c;
-  int D, d, n_kt;            // n_kt = c / 128
+  int D, d, n_kt;       // n_kt = c / 128
   float scale, scale_log2;
+  int* status;
+  uint64_t limit_ns;
 };
 
-__device__ void key_tile(const BwdArgs& a, int h, int64_t k0, uint8_t* smem) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t ld = 3 * (int64_t)a.d;
-  const uint32_t s0 = smem_u32(smem);
-  const uint32_t sK = s0 + OFF_K, sV = s0 + OFF_V, sDS = s0 + OFF_DS;
-  float* sL = reinterpret_cast<float*>(smem + OFF_L);   // [2][64]
-  float* sDl = sL + 2 * BR;                             // [2][64]
-  const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
-  const ct_t* kg = a.qkv + krow0 * ld + a.d + h * DH;
-  const int nq = (int)((a.S - k0) / BR);
-
-  auto load_q = [&](int j, int b) {
-    const int64_t q0 = k0 + (int64_t)j * BR;
-    const int64_t qrow = zz_row_of_pos(q0, a.c, a.D);
-    load_rows(s0 + OFF_Q + b * SQ_BYTES, a.qkv + qrow * ld + h * DH, ld, BR);
-    load_rows(s0 + OFF_DO + b * SQ_BYTES, a.dO + qrow * a.d + h * DH, a.d, BR);
-    if (threadIdx.x < BR) {
-      cp_async4(smem_u32(sL + b * BR + threadIdx.x), a.lse + (int64_t)h * a.S + qrow + threadIdx.x);
-    } else if (threadIdx.x < 2 * BR) {
-      const int t = threadIdx.x - BR;
-      cp_async4(smem_u32(sDl + b * BR + t), a.delta + (int64_t)h * a.S + qrow + t);
-    }
-  };
-  load_rows(sK, kg, ld, BC);
-  load_rows(sV, kg + a.d, ld, BC);
-  load_q(0, 0);
-  cp_async_commit();
-  cp_async_wait_all();
-  __syncthreads();
-
-  float dk[16][4], dv[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) dk[i][e] = dv[i][e] = 0.f;
-  const int64_t kw0 = k0 + warp * 16;
-  const int64_t kp_lo = kw0 + (lane >> 2), kp_hi = kp_lo + 8;
-  const int arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;  // A-fragment row (key)
-  constexpr float LOG2E = 1.4426950408889634f;
-
-  for (int j = 0; j < nq; ++j) {
-    const int b = j & 1;
-    if (j + 1 < nq) load_q(j + 1, b ^ 1);
-    cp_async_commit();
-    const uint32_t sQ = s0 + OFF_Q + b * SQ_BYTES, sdO = s0 + OFF_DO + b * SQ_BYTES;
-    const float* L = sL + b * BR;
-    const float* Dl = sDl + b * BR;
-    const int64_t q0 = k0 + (int64_t)j * BR;
-    const bool active = q0 + BR - 1 >= kw0;
-    if (active) {
-      float st[8][4], dp[8][4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) st[i][e] = dp[i][e] = 0.f;
-      // S^T = K Q^T and dP^T = V dO^T  (16 keys x 64 queries)
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t ka[4], va[4];
-        const int col = ks * 16 + (lane >> 4) * 8;
-        ldsm_x4(sK + swz(arow, col), ka[0], ka[1], ka[2], ka[3]);
-        ldsm_x4(sV + swz(arow, col), va[0], va[1], va[2], va[3]);
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          uint32_t b0, b1, b2, b3;
-          const int q = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-          const int bc = ks * 16 + ((lane >> 3) & 1) * 8;
-          ldsm_x4(sQ + swz(q, bc), b0, b1, b2, b3);
-          mma_f16(st[2 * np], ka, b0, b1);
-          mma_f16(st[2 * np + 1], ka, b2, b3);
-          ldsm_x4(sdO + swz(q, bc), b0, b1, b2, b3);
-          mma_f16(dp[2 * np], va, b0, b1);
-          mma_f16(dp[2 * np + 1], va, b2, b3);
-        }
-      }
-      // P^T and dS^T in place (st -> P, dp -> dS)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int ql = i * 8 + (lane & 3) * 2 + e;
-          const int64_t qp = q0 + ql;
-          const float l2 = L[ql] * LOG2E, dl = Dl[ql];
-          float p0 = exp2f(st[i][e] * a.scale_log2 - l2);
-          float p1 = exp2f(st[i][2 + e] * a.scale_log2 - l2);
-          if (kp_lo > qp) p0 = 0.f;
-          if (kp_hi > qp) p1 = 0.f;
-          st[i][e] = p0;
-          st[i][2 + e] = p1;
-          dp[i][e] = p0 * (dp[i][e] - dl);
-          dp[i][2 + e] = p1 * (dp[i][2 + e] - dl);
-        }
-      }
-      // dV += P^T dO ; dK += dS^T Q   (k-dimension = 64 queries).  P and dS
-      // enter the fp16 MMAs scaled by 2^8 so that small probabilities stay in
-      // fp16's normal range; the accumulators are scaled back at the end.
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          st[i][e] *= kOperandScale;
-          dp[i][e] *= kOperandScale;
-        }
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint32_t pa[4] = {pack_f16(st[2 * ks][0], st[2 * ks][1]),
-                                pack_f16(st[2 * ks][2], st[2 * ks][3]),
-                                pack_f16(st[2 * ks + 1][0], st[2 * ks + 1][1]),
-                                pack_f16(st[2 * ks + 1][2], st[2 * ks + 1][3])};
-        const uint32_t da[4] = {pack_f16(dp[2 * ks][0], dp[2 * ks][1]),
-                                pack_f16(dp[2 * ks][2], dp[2 * ks][3]),
-                                pack_f16(dp[2 * ks + 1][0], dp[2 * ks + 1][1]),
-                                pack_f16(dp[2 * ks + 1][2], dp[2 * ks + 1][3])};
-        const int q = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-        for (int dpi = 0; dpi < 8; ++dpi) {
-          uint32_t b0, b1, b2, b3;
-          const int col = dpi * 16 + (lane >> 4) * 8;
-          ldsm_x4_t(sdO + swz(q, col), b0, b1, b2, b3);
-          mma_f16(dv[2 * dpi], pa, b0, b1);
-          mma_f16(dv[2 * dpi + 1], pa, b2, b3);
-          ldsm_x4_t(sQ + swz(q, col), b0, b1, b2, b3);
-          mma_f16(dk[2 * dpi], da, b0, b1);
-          mma_f16(dk[2 * dpi + 1], da, b2, b3);
-        }
-      }
-      // dS (query-major) into shared memory for dQ
-      ct_t* ds = reinterpret_cast<ct_t*>(smem + OFF_DS);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int ql = i * 8 + (lane & 3) * 2 + e;
-          const int kl = warp * 16 + (lane >> 2);
-          ds[swz(ql, kl) >> 1] = __float2half_rn(dp[i][e]);
-          ds[swz(ql, kl + 8) >> 1] = __float2half_rn(dp[i][2 + e]);
-        }
-      }
-    } else {
-      ct_t* ds = reinterpret_cast<ct_t*>(smem + OFF_DS);
-      for (int i = lane; i < BR * 16; i += 32) {
-        const int ql = i >> 4, kl = warp * 16 + (i & 15);
-        ds[swz(ql, kl) >> 1] = __float2half_rn(0.f);
-      }
-    }
-    __syncthreads();
-    // dQ partial = dS K: warp -> 16 queries x 64 dh columns
-    {
-      const int qw = (warp & 3) * 16, cw = (warp >> 2) * 64;
-      float acc[8][4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-      const int qa = qw + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {   // 128 keys
-        uint32_t af[4];
-        ldsm_x4(sDS + swz(qa, ks * 16 + (lane >> 4) * 8), af[0], af[1], af[2], af[3]);
-        const int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-        for (int dpi = 0; dpi < 4; ++dpi) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(sK + swz(key, cw + dpi * 16 + (lane >> 4) * 8), b0, b1, b2, b3);
-          mma_f16(acc[2 * dpi], af, b0, b1);
-          mma_f16(acc[2 * dpi + 1], af, b2, b3);
-        }
-      }
-      const int64_t qrow = zz_row_of_pos(q0, a.c, a.D) + qw + (lane >> 2);
-      float* dst_lo = a.dq_acc + qrow * a.d + h * DH + cw + (lane & 3) * 2;
-      float* dst_hi = dst_lo + 8 * (int64_t)a.d;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float sc = a.scale * kOperandUnscale;
-        atomicAdd(reinterpret_cast<float2*>(dst_lo + i * 8), make_float2(acc[i][0] * sc, acc[i][1] * sc));
-        atomicAdd(reinterpret_cast<float2*>(dst_hi + i * 8), make_float2(acc[i][2] * sc, acc[i][3] * sc));
-      }
-    }
-    cp_async_wait_all();
-    __syncthreads();
-  }
-  // dK (scaled), dV -> fp16 rows of the key tile
-  const int64_t row_lo = krow0 + warp * 16 + (lane >> 2), row_hi = row_lo + 8;
-  ct_t* dk_lo = a.dqkv + row_lo * ld + a.d + h * DH;
-  ct_t* dk_hi = a.dqkv + row_hi * ld + a.d + h * DH;
-  const float skk = a.scale * kOperandUnscale;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int col = i * 8 + (lane & 3) * 2;
-    *reinterpret_cast<uint32_t*>(dk_lo + col) = pack_f16(dk[i][0] * skk, dk[i][1] * skk);
-    *reinterpret_cast<uint32_t*>(dk_hi + col) = pack_f16(dk[i][2] * skk, dk[i][3] * skk);
-    *reinterpret_cast<uint32_t*>(dk_lo + a.d + col) =
-        pack_f16(dv[i][0] * kOperandUnscale, dv[i][1] * kOperandUnscale);
-    *reinterpret_cast<uint32_t*>(dk_hi + a.d + col) =
-        pack_f16(dv[i][2] * kOperandUnscale, dv[i][3] * kOperandUnscale);
-  }
-  __syncthreads();
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
-__global__ void __launch_bounds__(NTHR, 1) attn_bwd_zigzag_kernel(const BwdArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > limit_ns) return;
+  }
+}
+
+// Named barrier of warps 0-3 (id 1) or 4-7 (id 2) that ANDs a predicate: a
+// loop exit taken on a failed (timed-out) wait is the same for all of them.
+__device__ __forceinline__ bool group_bar_and(int id, bool pred) {
+  uint32_t res;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(res)
+      : "r"(pred ? 1u : 0u), "r"(id)
+      : "memory");
+  return res != 0;
+}
+
+__global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_constant__ TcBwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + OFF_BAR;
+  const uint32_t kv_full = bars;
+  auto qd_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto qd_empty = [&](int s) { return bars + 8u * (3 + s); };
+  const uint32_t s_full = bars + 8u * 5;
+  const uint32_t s_free = bars + 8u * 6;
+  auto p_full = [&](int b) { return bars + 8u * (7 + b); };
+  auto p_free = [&](int b) { return bars + 8u * (9 + b); };
+  const uint32_t dq_full = bars + 8u * 11;
+  const uint32_t dq_empty = bars + 8u * 12;
+  const uint32_t kv_done = bars + 8u * 13;
+  const uint32_t drain_bar = bars + 8u * 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 160);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_BAR + 168);
+
+  if (*(volatile int*)a.status != 0) return;  // an earlier device error skips the work
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
   const int pair = blockIdx.x;
   const int r = pair / a.n_kt, t = pair - r * a.n_kt;
-  const int64_t kA = (int64_t)r * a.c + (int64_t)t * BC;
-  const int64_t kB = (int64_t)(2 * a.D - 1 - r) * a.c + (int64_t)(a.n_kt - 1 - t) * BC;
-  key_tile(a, h, kA, smem);   // long query range first
-  key_tile(a, h, kB, smem);
+  int64_t k0s[2];
+  k0s[0] = (int64_t)r * a.c + (int64_t)t * BC;                                      // long range
+  k0s[1] = (int64_t)(2 * a.D - 1 - r) * a.c + (int64_t)(a.n_kt - 1 - t) * BC;      // mirror
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(qd_full(s), 1);
+      mbar_init(qd_empty(s), 1);
+      mbar_init(p_full(s), 128);
+      mbar_init(p_free(s), 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(kv_done, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == WARP_PROD && lane == 0) {
+    tma_prefetch_desc(&a.tm_qkv);
+    tma_prefetch_desc(&a.tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  float* sLD = reinterpret_cast<float*>(gbase + OFF_L);  // [stage][LSE 64 | Delta 64]
+
+  uint32_t it = 0;        // query tiles processed by this CTA so far
+  uint32_t q_issued = 0, kv_issued = 0;
+  for (int tile = 0; tile < 2; ++tile) {
+    const int64_t k0 = k0s[tile];
+    const int nq = (int)((a.S - k0) / BR);
+    const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
+    if (warp == WARP_PROD) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0 && !*abort_flag) {
+        mbar_arrive_expect_tx(kv_full, 2 * KT_BYTES);
+#pragma unroll
+        for (int jh = 0; jh < 2; ++jh)
+#pragma unroll
+          for (int rh = 0; rh < 2; ++rh) {
+            const uint32_t off = jh * (KT_BYTES / 2) + rh * (KT_BYTES / 4);
+            tma_load_2d(base + OFF_K + off, &a.tm_qkv, a.d + h * DH + 64 * jh,
+                        (int)(krow0 + 64 * rh), kv_full);
+            tma_load_2d(base + OFF_V + off, &a.tm_qkv, 2 * a.d + h * DH + 64 * jh,
+                        (int)(krow0 + 64 * rh), kv_full);
+          }
+        ++kv_issued;
+        for (int j = 0; j < nq; ++j) {
+          const uint32_t cur = it + j, st = cur & 1u;
+          if (!mbar_wait(qd_empty(st), ((cur >> 1) & 1u) ^ 1u, a.status, abort_flag, a.limit_ns))
+            break;
+          const int64_t qrow = zz_row_of_pos(k0 + (int64_t)j * BR, a.c, a.D);
+          const uint32_t fb = qd_full(st);
+          mbar_arrive_expect_tx(fb, 2 * QT_BYTES + 2 * BR * 4);
+#pragma unroll
+          for (int jh = 0; jh < 2; ++jh) {
+            tma_load_2d(base + OFF_Q + st * QT_BYTES + jh * (QT_BYTES / 2), &a.tm_qkv,
+                        h * DH + 64 * jh, (int)qrow, fb);
+            tma_load_2d(base + OFF_DO + st * QT_BYTES + jh * (QT_BYTES / 2), &a.tm_do,
+                        h * DH + 64 * jh, (int)qrow, fb);
+          }
+          const uint32_t sl = smem_u32(sLD + st * 2 * BR);
+          bulk_load(sl, a.lse + (int64_t)h * a.S + qrow, BR * 4, fb);
+          bulk_load(sl + BR * 4, a.delta + (int64_t)h * a.S + qrow, BR * 4, fb);
+          ++q_issued;
+        }
+      }
+    } else if (warp == WARP_MMA) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0 && !*abort_flag) {
+        constexpr uint32_t id_s = idesc_f16_f32(BC, BR, false, false, false);   // S^T, dP^T
+        constexpr uint32_t id_kv = idesc_f16_f32(BC, DH, false, true, false);   // dV, dK
+        constexpr uint32_t id_q = idesc_f16_f32(DH, BR, true, true, false);     // dQ^T
+        bool ok = mbar_wait(kv_full, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
+        auto issue_s = [&](uint32_t cur) -> bool {
+          const uint32_t st = cur & 1u;
+          if (!mbar_wait(qd_full(st), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns))
+            return false;
+          if (cur >= 1 && !mbar_wait(s_free, (cur - 1) & 1u, a.status, abort_flag, a.limit_ns))
+            return false;
+          tc_fence_after();
+          const uint32_t sq = base + OFF_Q + st * QT_BYTES, sdo = base + OFF_DO + st * QT_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < DH / 16; ++kk) {
+            const uint32_t aoff = (kk >> 2) * (KT_BYTES / 2) + (kk & 3) * 32;
+            const uint32_t boff = (kk >> 2) * (QT_BYTES / 2) + (kk & 3) * 32;
+            umma_f16_ss(tmem + TM_S, sdesc_sw128(base + OFF_K + aoff, 16, 1024),
+                        sdesc_sw128(sq + boff, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+            umma_f16_ss(tmem + TM_DP, sdesc_sw128(base + OFF_V + aoff, 16, 1024),
+                        sdesc_sw128(sdo + boff, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full);
+          return true;
+        };
+        if (ok) ok = issue_s(it);
+        for (int j = 0; j < nq && ok; ++j) {
+          const uint32_t cur = it + j, st = cur & 1u, pb = cur & 1u;
+          if (j + 1 < nq && !(ok = issue_s(cur + 1))) break;
+          if (!mbar_wait(p_full(pb), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sp = base + OFF_P + pb * PT_BYTES, sds = base + OFF_DS + pb * PT_BYTES;
+          const uint32_t sq = base + OFF_Q + st * QT_BYTES, sdo = base + OFF_DO + st * QT_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BR / 16; ++kk) {
+            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+            umma_f16_ss(tmem + TM_DV, sdesc_sw128(sp + kk * 32, 16, 1024),
+                        sdesc_sw128(sdo + kk * 2048, QT_BYTES / 2, 1024), id_kv, acc);
+            umma_f16_ss(tmem + TM_DK, sdesc_sw128(sds + kk * 32, 16, 1024),
+                        sdesc_sw128(sq + kk * 2048, QT_BYTES / 2, 1024), id_kv, acc);
+          }
+          umma_commit(qd_empty(st));
+          if (cur >= 1 && !mbar_wait(dq_empty, (cur - 1) & 1u, a.status, abort_flag, a.limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BC / 16; ++kk)
+            umma_f16_ss(tmem + TM_DQ, sdesc_sw128(base + OFF_K + kk * 2048, KT_BYTES / 2, 1024),
+                        sdesc_sw128(sds + kk * 2048, PT_BYTES, 1024), id_q, kk > 0 ? 1u : 0u);
+          umma_commit(dq_full);
+          umma_commit(p_free(pb));
+        }
+        if (ok) {
+          umma_commit(kv_done);
+        } else {
+          umma_commit(drain_bar);
+          drain_wait(drain_bar, 0, a.limit_ns);
+        }
+      }
+    } else if (warp < 4) {
+      // ------------------------------------------------------------ P, dS (thread = key)
+      const int row = warp * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+      const int64_t kp = k0 + row;
+      constexpr float LOG2E = 1.4426950408889634f;
+      bool ok = true;
+      for (int j = 0; j < nq; ++j) {
+        const uint32_t cur = it + j, st = cur & 1u, pb = cur & 1u;
+        bool okl = ok && mbar_wait(s_full, cur & 1u, a.status, abort_flag, a.limit_ns);
+        okl = okl && mbar_wait(qd_full(st), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns);
+        okl = __all_sync(0xffffffffu, okl);
+        uint32_t sv[2][32], dv[2][32];
+        if (okl) {
+          tc_fence_after();
+          tmem_ld32(lane_base + TM_S, sv[0]);
+          tmem_ld32(lane_base + TM_S + 32, sv[1]);
+          tmem_ld32(lane_base + TM_DP, dv[0]);
+          tmem_ld32(lane_base + TM_DP + 32, dv[1]);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(s_free);
+        }
+        // buffer pb was last read by the MMAs of query tile cur-2
+        if (okl && cur >= 2)
+          okl = mbar_wait(p_free(pb), ((cur - 2) >> 1) & 1u, a.status, abort_flag, a.limit_ns);
+        ok = group_bar_and(1, okl);
+        if (!ok) break;
+        const float* L = sLD + st * 2 * BR;
+        const float* Dl = L + BR;
+        const int64_t q0 = k0 + (int64_t)j * BR;
+        const bool diag = q0 < k0 + BC;
+        uint8_t* prow = gbase + OFF_P + pb * PT_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
+        uint8_t* drow = gbase + OFF_DS + pb * PT_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float pp[2], dd[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int qi = q * 32 + e + u;
+              float p = ex2_approx(fmaf(__uint_as_float(sv[q][e + u]), a.scale_log2, -L[qi] * LOG2E));
+              if (diag && kp > q0 + qi) p = 0.f;
+              pp[u] = p * kOperandScale;
+              dd[u] = pp[u] * (__uint_as_float(dv[q][e + u]) - Dl[qi]);
+            }
+            pk[e >> 1] = pack_f16(pp[0], pp[1]);
+            dk[e >> 1] = pack_f16(dd[0], dd[1]);
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int chunk = q * 4 + c;
+            const uint32_t off = (uint32_t)((chunk ^ (row & 7)) << 4);
+            *reinterpret_cast<uint4*>(prow + off) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            *reinterpret_cast<uint4*>(drow + off) =
+                make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(p_full(pb));
+      }
+      // dK, dV of this key tile -> fp16 rows
+      bool eok = ok && mbar_wait(kv_done, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
+      eok = __all_sync(0xffffffffu, eok);
+      if (eok) {
+        tc_fence_after();
+        ct_t* dkrow = a.dqkv + (krow0 + row) * 3 * (int64_t)a.d + a.d + h * DH;
+        const float skk = a.scale * kOperandUnscale;
+#pragma unroll 1
+        for (int part = 0; part < 2; ++part) {   // 0: dK, 1: dV
+          const float mul = part == 0 ? skk : kOperandUnscale;
+          ct_t* out = dkrow + part * a.d;
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            uint32_t v[32];
+            tmem_ld32(lane_base + (part == 0 ? TM_DK : TM_DV) + q * 32, v);
+            tmem_wait_ld();
+            uint4* dst = reinterpret_cast<uint4*>(out + q * 32);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              dst[c] = make_uint4(
+                  pack_f16(__uint_as_float(v[8 * c]) * mul, __uint_as_float(v[8 * c + 1]) * mul),
+                  pack_f16(__uint_as_float(v[8 * c + 2]) * mul, __uint_as_float(v[8 * c + 3]) * mul),
+                  pack_f16(__uint_as_float(v[8 * c + 4]) * mul, __uint_as_float(v[8 * c + 5]) * mul),
+                  pack_f16(__uint_as_float(v[8 * c + 6]) * mul, __uint_as_float(v[8 * c + 7]) * mul));
+          }
+        }
+      }
+      tc_fence_before();
+    } else {
+      // ------------------------------------------------------------ dQ drain (thread = dh)
+      const int quarter = warp & 3;
+      const int dh = quarter * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+      const float sc = a.scale * kOperandUnscale;
+      bool ok = true;
+      for (int j = 0; j < nq; ++j) {
+        const uint32_t cur = it + j;
+        bool okl = ok && mbar_wait(dq_full, cur & 1u, a.status, abort_flag, a.limit_ns);
+        okl = __all_sync(0xffffffffu, okl);
+        uint32_t v[2][32];
+        if (okl) {
+          tc_fence_after();
+          tmem_ld32(lane_base + TM_DQ, v[0]);
+          tmem_ld32(lane_base + TM_DQ + 32, v[1]);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(dq_empty);
+        }
+        ok = group_bar_and(2, okl);
+        if (!ok) break;
+        const int64_t qrow = zz_row_of_pos(k0 + (int64_t)j * BR, a.c, a.D);
+        float* dst = a.dq_acc + qrow * a.d + h * DH + dh;
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            atomicAdd(dst + (int64_t)(q * 32 + e) * a.d, __uint_as_float(v[q][e]) * sc);
+      }
+      tc_fence_before();
+    }
+    it += (uint32_t)nq;
+    __syncthreads();   // K/V tiles, TMEM accumulators and barrier phases move on
+    tc_fence_after();
+  }
+  if (warp == WARP_PROD && lane == 0 && *abort_flag) {
+    const uint32_t n_out = q_issued < 2u ? q_issued : 2u;
+    for (uint32_t jj = q_issued - n_out; jj < q_issued; ++jj)
+      drain_wait(qd_full(jj & 1u), (jj >> 1) & 1u, a.limit_ns);
+    if (kv_issued > 0) drain_wait(kv_full, (kv_issued - 1) & 1u, a.limit_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
 }
 
 // Delta[h][row] = dO[row, head h] . O[row, head h]  (warp per row and head)
-__global__ void attn_delta_kernel(const ct_t* __restrict__ o,
-                                  const ct_t* __restrict__ dO, float* __restrict__ delta,
-                                  int64_t S, int H, int d) {
+__global__ void attn_delta_kernel(const ct_t* __restrict__ o, const ct_t* __restrict__ dO,
+                                  float* __restrict__ delta, int64_t S, int H, int d) {
   const int lane = threadIdx.x & 31;
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < S * H; w += nw) {
@@ -332,46 +451,86 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, ct_t* __restric
   }
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn_bwd() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Row-major fp16 [rows, cols] with box {64 columns, 64 rows}, 128-byte swizzle.
+bool map_2d(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows) {
+  EncodeTiledFn fn = encode_fn_bwd();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
+  const cuuint32_t box[2] = {64u, 64u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, const float* lse,
-                                float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int dh,
-                                int D, cudaStream_t st) {
+                               float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int dh,
+                               int D, cudaStream_t st) {
   if (dh != DH) return TSP_ERR_UNSUPPORTED;
   const int64_t c = S / (2 * D);
-  if (c % BC != 0) return TSP_ERR_UNSUPPORTED;
+  if (c % BC != 0 || S > (int64_t)INT32_MAX) return TSP_ERR_UNSUPPORTED;
   const int d = H * dh;
+  if (((uintptr_t)qkv & 15u) || ((uintptr_t)dO & 15u) || ((uintptr_t)lse & 15u) ||
+      ((uintptr_t)delta & 15u) || (S * 4) % 16 != 0)
+    return TSP_ERR_INVALID_ARG;
   {
-  Prof prof("attn_bwd_prep", st);
-  attn_delta_kernel<<<num_sms() * 8, 256, 0, st>>>((const ct_t*)o,
-                                                   (const ct_t*)dO, delta, S, H, d);
-  TSP_CUDA_TRY(cudaGetLastError());
-  TSP_CUDA_TRY(cudaMemsetAsync(dq_acc, 0, (size_t)S * d * sizeof(float), st));
+    Prof prof("attn_bwd_prep", st);
+    attn_delta_kernel<<<num_sms() * 8, 256, 0, st>>>((const ct_t*)o, (const ct_t*)dO, delta, S, H,
+                                                     d);
+    TSP_CUDA_TRY(cudaGetLastError());
+    TSP_CUDA_TRY(cudaMemsetAsync(dq_acc, 0, (size_t)S * d * sizeof(float), st));
   }
-  BwdArgs a;
-  a.qkv = (const ct_t*)qkv;
-  a.dO = (const ct_t*)dO;
-  a.lse = lse;
-  a.delta = delta;
-  a.dq_acc = dq_acc;
-  a.dqkv = (ct_t*)dqkv;
-  a.S = S;
-  a.c = c;
-  a.D = D;
-  a.d = d;
-  a.n_kt = (int)(c / BC);
-  a.scale = 1.0f / sqrtf((float)dh);
-  a.scale_log2 = 1.4426950408889634f * a.scale;
+  TcBwdArgs* a = new TcBwdArgs();
+  std::unique_ptr<TcBwdArgs> guard(a);
+  memset(a, 0, sizeof(TcBwdArgs));
+  if (!map_2d(&a->tm_qkv, qkv, 3 * (int64_t)d, S) || !map_2d(&a->tm_do, dO, d, S))
+    return TSP_ERR_CUDA;
+  a->lse = lse;
+  a->delta = delta;
+  a->dq_acc = dq_acc;
+  a->dqkv = (ct_t*)dqkv;
+  a->S = S;
+  a->c = c;
+  a->D = D;
+  a->d = d;
+  a->n_kt = (int)(c / BC);
+  a->scale = 1.0f / sqrtf((float)dh);
+  a->scale_log2 = 1.4426950408889634f * a->scale;
+  a->status = status_word();
+  a->limit_ns = wait_limit_ns();
   static bool attr = false;
   if (!attr) {
-    TSP_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_zigzag_kernel,
+    TSP_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_tc_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM));
     attr = true;
   }
-  dim3 grid((unsigned)(D * a.n_kt), (unsigned)H);
+  dim3 grid((unsigned)(D * a->n_kt), (unsigned)H);
   {
     Prof prof("attn_bwd", st);
-    attn_bwd_zigzag_kernel<<<grid, NTHR, SMEM, st>>>(a);
+    attn_bwd_tc_kernel<<<grid, NTHR, SMEM, st>>>(*a);
     TSP_CUDA_TRY(cudaGetLastError());
   }
   Prof prof("attn_bwd_dq_convert", st);
