@@ -15,18 +15,19 @@
 // tile t of chunk r and the mirrored tile of chunk 2D-1-r, each walking the
 // 64-row query tiles at positions >= the tile; the two query ranges add up to
 // S + 128 rows for every (r, t), so CTAs are balanced.  Per query tile:
-//   warp 8   TMA producer: K, V once per key tile; Q_i, dO_i (+ LSE_i, Delta_i
-//            by bulk copy) into a 2-stage ring;
-//   warp 9   MMA issuer: S^T = K Q_i^T and dP^T = V dO_i^T (M = 128 keys,
+//   warp 12  TMA producer: K, V once per key tile; Q_i, dO_i (+ LSE_i, Delta_i
+//            by bulk copy) into a 3-stage ring;
+//   warp 13  MMA issuer: S^T = K Q_i^T and dP^T = V dO_i^T (M = 128 keys,
 //            N = 64 queries) for tile i+1 as soon as tile i's were read; then
 //            dV += P^T dO_i, dK += dS^T Q_i (TMEM accumulators across every
 //            query tile) and dQ_i^T = K^T dS^T (M = 128 dh, N = 64 queries);
-//   warps 0-3 (thread = key = TMEM lane): P = 2^(s*scale*log2e - LSE*log2e),
+//   warps 0-7 (key = TMEM lane; warps w and w+4 share 32 keys, each thread
+//            owning 32 of the 64 query columns): P = 2^(s*scale*log2e - LSE*log2e),
 //            dS = P (dP - Delta), both written as fp16 (scaled by 2^8 to keep
 //            small probabilities in fp16's normal range) into swizzled smem,
 //            which serves as the K-major A operand of dV/dK and, unchanged, as
 //            the MN-major B operand of dQ^T; at the end dK, dV -> fp16 rows;
-//   warps 4-7 (thread = dh = TMEM lane): drain dQ_i^T from TMEM into the fp32
+//   warps 8-11 (thread = dh = TMEM lane): drain dQ_i^T from TMEM into the fp32
 //            dQ accumulator with warp-coalesced atomics.
 // All mbarrier waits are bounded (TSP_ERR_TIMEOUT) and every loop exit is
 // uniform across the threads that share a barrier.
@@ -41,19 +42,21 @@ namespace tsp {
 namespace {
 
 constexpr int BC = 128, BR = 64, DH = 128;
-constexpr int NTHR = 320;
-constexpr int WARP_PROD = 8, WARP_MMA = 9;
+constexpr int NSOFT = 256;                 // 8 warps: two threads per key row
+constexpr int NTHR = NSOFT + 128 + 64;     // + 4 dQ-drain warps + producer + MMA
+constexpr int WARP_PROD = 12, WARP_MMA = 13;   // warps 8-11 drain dQ
 constexpr int KT_BYTES = BC * DH * 2;      // 32 KB: 128 keys x 128 dh
 constexpr int QT_BYTES = BR * DH * 2;      // 16 KB: 64 queries x 128 dh
 constexpr int PT_BYTES = BC * BR * 2;      // 16 KB: 128 keys x 64 queries
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + KT_BYTES;
-constexpr int OFF_Q = OFF_V + KT_BYTES;          // 2 stages
-constexpr int OFF_DO = OFF_Q + 2 * QT_BYTES;     // 2 stages
-constexpr int OFF_P = OFF_DO + 2 * QT_BYTES;     // 2 buffers
-constexpr int OFF_DS = OFF_P + 2 * PT_BYTES;     // 2 buffers
-constexpr int OFF_L = OFF_DS + 2 * PT_BYTES;     // [2 stages][LSE 64 | Delta 64] floats
-constexpr int OFF_BAR = OFF_L + 2 * 2 * BR * 4;
+constexpr int QSTAGES = 3;                        // Q/dO ring depth (covers TMA latency)
+constexpr int OFF_Q = OFF_V + KT_BYTES;            // QSTAGES stages
+constexpr int OFF_DO = OFF_Q + QSTAGES * QT_BYTES; // QSTAGES stages
+constexpr int OFF_P = OFF_DO + QSTAGES * QT_BYTES; // 2 buffers
+constexpr int OFF_DS = OFF_P + 2 * PT_BYTES;       // 2 buffers
+constexpr int OFF_L = OFF_DS + 2 * PT_BYTES;       // [QSTAGES][LSE 64 | Delta 64] floats
+constexpr int OFF_BAR = OFF_L + QSTAGES * 2 * BR * 4;
 constexpr int SMEM = OFF_BAR + 256 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DQ = 128, TM_DV = 256, TM_DK = 384;
@@ -90,17 +93,18 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-// Named barrier of warps 0-3 (id 1) or 4-7 (id 2) that ANDs a predicate: a
-// loop exit taken on a failed (timed-out) wait is the same for all of them.
-__device__ __forceinline__ bool group_bar_and(int id, bool pred) {
+// Named barrier of the P/dS warps (id 1, 256 threads) or of the dQ warps
+// (id 2, 128 threads) that ANDs a predicate: a loop exit taken on a failed
+// (timed-out) wait is the same for all of them.
+__device__ __forceinline__ bool group_bar_and(int id, int nthreads, bool pred) {
   uint32_t res;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, 128, p;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(res)
-      : "r"(pred ? 1u : 0u), "r"(id)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
       : "memory");
   return res != 0;
 }
@@ -112,16 +116,16 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + OFF_BAR;
   const uint32_t kv_full = bars;
-  auto qd_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto qd_empty = [&](int s) { return bars + 8u * (3 + s); };
-  const uint32_t s_full = bars + 8u * 5;
-  const uint32_t s_free = bars + 8u * 6;
-  auto p_full = [&](int b) { return bars + 8u * (7 + b); };
-  auto p_free = [&](int b) { return bars + 8u * (9 + b); };
-  const uint32_t dq_full = bars + 8u * 11;
-  const uint32_t dq_empty = bars + 8u * 12;
-  const uint32_t kv_done = bars + 8u * 13;
-  const uint32_t drain_bar = bars + 8u * 14;
+  auto qd_full = [&](uint32_t s) { return bars + 8u * (1 + s); };       // 1..3
+  auto qd_empty = [&](uint32_t s) { return bars + 8u * (4 + s); };      // 4..6
+  const uint32_t s_full = bars + 8u * 7;
+  const uint32_t s_free = bars + 8u * 8;
+  auto p_full = [&](uint32_t b) { return bars + 8u * (9 + b); };
+  auto p_free = [&](uint32_t b) { return bars + 8u * (11 + b); };
+  const uint32_t dq_full = bars + 8u * 13;
+  const uint32_t dq_empty = bars + 8u * 14;
+  const uint32_t kv_done = bars + 8u * 15;
+  const uint32_t drain_bar = bars + 8u * 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 160);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_BAR + 168);
 
@@ -137,14 +141,16 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < QSTAGES; ++s) {
       mbar_init(qd_full(s), 1);
       mbar_init(qd_empty(s), 1);
-      mbar_init(p_full(s), 128);
-      mbar_init(p_free(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(p_full(b), NSOFT);
+      mbar_init(p_free(b), 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 128);
+    mbar_init(s_free, NSOFT);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(kv_done, 1);
@@ -166,6 +172,9 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   float* sLD = reinterpret_cast<float*>(gbase + OFF_L);  // [stage][LSE 64 | Delta 64]
+  // Q/dO ring position of query tile `cur` (CTA-wide counter)
+  auto qst = [](uint32_t cur) { return cur % QSTAGES; };
+  auto qph = [](uint32_t cur) { return (cur / QSTAGES) & 1u; };
 
   uint32_t it = 0;        // query tiles processed by this CTA so far
   uint32_t q_issued = 0, kv_issued = 0;
@@ -189,8 +198,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           }
         ++kv_issued;
         for (int j = 0; j < nq; ++j) {
-          const uint32_t cur = it + j, st = cur & 1u;
-          if (!mbar_wait(qd_empty(st), ((cur >> 1) & 1u) ^ 1u, a.status, abort_flag, a.limit_ns))
+          const uint32_t cur = it + j, st = qst(cur);
+          if (!mbar_wait(qd_empty(st), qph(cur) ^ 1u, a.status, abort_flag, a.limit_ns))
             break;
           const int64_t qrow = zz_row_of_pos(k0 + (int64_t)j * BR, a.c, a.D);
           const uint32_t fb = qd_full(st);
@@ -216,8 +225,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
         constexpr uint32_t id_q = idesc_f16_f32(DH, BR, true, true, false);     // dQ^T
         bool ok = mbar_wait(kv_full, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
         auto issue_s = [&](uint32_t cur) -> bool {
-          const uint32_t st = cur & 1u;
-          if (!mbar_wait(qd_full(st), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns))
+          const uint32_t st = qst(cur);
+          if (!mbar_wait(qd_full(st), qph(cur), a.status, abort_flag, a.limit_ns))
             return false;
           if (cur >= 1 && !mbar_wait(s_free, (cur - 1) & 1u, a.status, abort_flag, a.limit_ns))
             return false;
@@ -237,7 +246,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
         };
         if (ok) ok = issue_s(it);
         for (int j = 0; j < nq && ok; ++j) {
-          const uint32_t cur = it + j, st = cur & 1u, pb = cur & 1u;
+          const uint32_t cur = it + j, st = qst(cur), pb = cur & 1u;
           if (j + 1 < nq && !(ok = issue_s(cur + 1))) break;
           if (!mbar_wait(p_full(pb), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns)) {
             ok = false;
@@ -274,66 +283,66 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           drain_wait(drain_bar, 0, a.limit_ns);
         }
       }
-    } else if (warp < 4) {
+    } else if (warp < 8) {
       // ------------------------------------------------------------ P, dS (thread = key)
-      const int row = warp * 32 + lane;
-      const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+      const int quarter = warp & 3, half = warp >> 2;
+      const int row = quarter * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
       const int64_t kp = k0 + row;
       constexpr float LOG2E = 1.4426950408889634f;
       bool ok = true;
       for (int j = 0; j < nq; ++j) {
-        const uint32_t cur = it + j, st = cur & 1u, pb = cur & 1u;
+        const uint32_t cur = it + j, st = qst(cur), pb = cur & 1u;
         bool okl = ok && mbar_wait(s_full, cur & 1u, a.status, abort_flag, a.limit_ns);
-        okl = okl && mbar_wait(qd_full(st), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns);
-        okl = __all_sync(0xffffffffu, okl);
-        uint32_t sv[2][32], dv[2][32];
-        if (okl) {
-          tc_fence_after();
-          tmem_ld32(lane_base + TM_S, sv[0]);
-          tmem_ld32(lane_base + TM_S + 32, sv[1]);
-          tmem_ld32(lane_base + TM_DP, dv[0]);
-          tmem_ld32(lane_base + TM_DP + 32, dv[1]);
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(s_free);
-        }
+        okl = okl && mbar_wait(qd_full(st), qph(cur), a.status, abort_flag, a.limit_ns);
         // buffer pb was last read by the MMAs of query tile cur-2
         if (okl && cur >= 2)
           okl = mbar_wait(p_free(pb), ((cur - 2) >> 1) & 1u, a.status, abort_flag, a.limit_ns);
-        ok = group_bar_and(1, okl);
+        ok = group_bar_and(1, NSOFT, okl);
         if (!ok) break;
+        uint32_t sv[32], dv[32];
+        tc_fence_after();
+        tmem_ld32(lane_base + TM_S + half * 32, sv);
+        tmem_ld32(lane_base + TM_DP + half * 32, dv);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(s_free);
         const float* L = sLD + st * 2 * BR;
         const float* Dl = L + BR;
         const int64_t q0 = k0 + (int64_t)j * BR;
         const bool diag = q0 < k0 + BC;
         uint8_t* prow = gbase + OFF_P + pb * PT_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
         uint8_t* drow = gbase + OFF_DS + pb * PT_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
+        // this thread's 32 query columns, 8 at a time (LSE, Delta read as float4)
+        const float neg_l_scale = -LOG2E;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t pk[16], dk[16];
+        for (int c = 0; c < 4; ++c) {
+          const int qb = half * 32 + c * 8;
+          const float4 l0 = *reinterpret_cast<const float4*>(L + qb);
+          const float4 l1 = *reinterpret_cast<const float4*>(L + qb + 4);
+          const float4 d0 = *reinterpret_cast<const float4*>(Dl + qb);
+          const float4 d1 = *reinterpret_cast<const float4*>(Dl + qb + 4);
+          const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+          const float dlv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+          uint32_t pk[4], dk[4];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
+          for (int e = 0; e < 8; e += 2) {
             float pp[2], dd[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const int qi = q * 32 + e + u;
-              float p = ex2_approx(fmaf(__uint_as_float(sv[q][e + u]), a.scale_log2, -L[qi] * LOG2E));
-              if (diag && kp > q0 + qi) p = 0.f;
+              const int x = c * 8 + e + u;
+              float p = ex2_approx(fmaf(__uint_as_float(sv[x]), a.scale_log2, lv[e + u] * neg_l_scale));
+              if (diag && kp > q0 + qb + e + u) p = 0.f;
               pp[u] = p * kOperandScale;
-              dd[u] = pp[u] * (__uint_as_float(dv[q][e + u]) - Dl[qi]);
+              dd[u] = pp[u] * (__uint_as_float(dv[x]) - dlv[e + u]);
             }
             pk[e >> 1] = pack_f16(pp[0], pp[1]);
             dk[e >> 1] = pack_f16(dd[0], dd[1]);
           }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int chunk = q * 4 + c;
-            const uint32_t off = (uint32_t)((chunk ^ (row & 7)) << 4);
-            *reinterpret_cast<uint4*>(prow + off) =
-                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            *reinterpret_cast<uint4*>(drow + off) =
-                make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
-          }
+          const int chunk = half * 4 + c;
+          const uint32_t off = (uint32_t)((chunk ^ (row & 7)) << 4);
+          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(drow + off) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
         }
         fence_proxy_async_smem();
         mbar_arrive(p_full(pb));
@@ -345,8 +354,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
         tc_fence_after();
         ct_t* dkrow = a.dqkv + (krow0 + row) * 3 * (int64_t)a.d + a.d + h * DH;
         const float skk = a.scale * kOperandUnscale;
-#pragma unroll 1
-        for (int part = 0; part < 2; ++part) {   // 0: dK, 1: dV
+        {
+          const int part = half;   // warps 0-3 write dK, warps 4-7 write dV
           const float mul = part == 0 ? skk : kOperandUnscale;
           ct_t* out = dkrow + part * a.d;
 #pragma unroll 1
@@ -376,18 +385,15 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
       for (int j = 0; j < nq; ++j) {
         const uint32_t cur = it + j;
         bool okl = ok && mbar_wait(dq_full, cur & 1u, a.status, abort_flag, a.limit_ns);
-        okl = __all_sync(0xffffffffu, okl);
-        uint32_t v[2][32];
-        if (okl) {
-          tc_fence_after();
-          tmem_ld32(lane_base + TM_DQ, v[0]);
-          tmem_ld32(lane_base + TM_DQ + 32, v[1]);
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(dq_empty);
-        }
-        ok = group_bar_and(2, okl);
+        ok = group_bar_and(2, 128, okl);
         if (!ok) break;
+        uint32_t v[2][32];
+        tc_fence_after();
+        tmem_ld32(lane_base + TM_DQ, v[0]);
+        tmem_ld32(lane_base + TM_DQ + 32, v[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(dq_empty);
         const int64_t qrow = zz_row_of_pos(k0 + (int64_t)j * BR, a.c, a.D);
         float* dst = a.dq_acc + qrow * a.d + h * DH + dh;
 #pragma unroll
@@ -403,9 +409,9 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
     tc_fence_after();
   }
   if (warp == WARP_PROD && lane == 0 && *abort_flag) {
-    const uint32_t n_out = q_issued < 2u ? q_issued : 2u;
+    const uint32_t n_out = q_issued < (uint32_t)QSTAGES ? q_issued : (uint32_t)QSTAGES;
     for (uint32_t jj = q_issued - n_out; jj < q_issued; ++jj)
-      drain_wait(qd_full(jj & 1u), (jj >> 1) & 1u, a.limit_ns);
+      drain_wait(qd_full(qst(jj)), qph(jj), a.limit_ns);
     if (kv_issued > 0) drain_wait(kv_full, (kv_issued - 1) & 1u, a.limit_ns);
   }
   tc_fence_before();
