@@ -25,6 +25,7 @@
 // that runs out records TSP_ERR_TIMEOUT, drains the CTA's copies and MMAs,
 // frees TMEM and returns.
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <memory>
 #include <mutex>
@@ -73,6 +74,7 @@ struct KParams {
   void* outs[3];
   int* status;
   uint64_t limit_ns;
+  int debug_skip;  // failure-detection test: CTA 0 never loads its first stage
   int shard_kb[65];
 };
 
@@ -211,6 +213,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.status, abort_flag, p.limit_ns)) {
             ok = false;
             break;
+          }
+          if (p.debug_skip && blockIdx.x == 0 && issued == 0 && i == 0) {
+            // test knob: this stage is never filled, so the MMA's wait on it runs out
+            ++issued;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            ++kb;
+            continue;
           }
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
@@ -547,6 +559,14 @@ tsp_status gemm_tc(const TcGemm& g, cudaStream_t st) {
   for (int i = 0; i < 3; ++i) kp->outs[i] = g.outs[i];
   kp->status = status_word();
   kp->limit_ns = wait_limit_ns();
+  {
+    // TSP_DEBUG_SKIP_STAGE=1 (read on every call): CTA 0 of the next GEMM never
+    // fills its first pipeline stage, which exercises the bounded-wait path
+    // (TSP_ERR_TIMEOUT in the status word after TSP_WAIT_LIMIT_MS) without a
+    // fault or a hang.  Used by the failure-detection test only.
+    const char* e = getenv("TSP_DEBUG_SKIP_STAGE");
+    kp->debug_skip = (e && atoi(e) > 0) ? 1 : 0;
+  }
   const int tiles = kp->tiles_m * kp->tiles_n;
   const int grid = std::min(tiles, num_sms());
   switch (g.epi) {
