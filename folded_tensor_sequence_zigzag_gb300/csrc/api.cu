@@ -132,7 +132,7 @@ tsp_status check_bf16_mlp(const tsp_cfg* c) {
 }
 tsp_status check_bf16_attn(const tsp_cfg* c) {
   if (c->dtype != TSP_BF16) return TSP_OK;
-  if (c->d % 256 != 0 || c->dh != 128 || (c->S / (2 * c->D)) % 128 != 0) return TSP_ERR_UNSUPPORTED;
+  if (c->d % 256 != 0 || c->dh != 128 || (c->S / (2 * c->D)) % 256 != 0) return TSP_ERR_UNSUPPORTED;
   return TSP_OK;
 }
 

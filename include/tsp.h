@@ -80,7 +80,7 @@ typedef enum { TSP_F32 = 0, TSP_BF16 = 1 } tsp_dtype;
  *   eps    RMSNorm epsilon
  *   dtype  tsp_dtype
  * bf16 kernels additionally need: d % 256 == 0, inter % 128 == 0, and for
- * attention dh == 128 and c = S/(2D) a multiple of 128.  Other valid shapes
+ * attention dh == 128 and c = S/(2D) a multiple of 256.  Other valid shapes
  * return TSP_ERR_UNSUPPORTED in bf16 (there is no silent fallback). */
 typedef struct {
   int64_t S;

@@ -99,7 +99,7 @@ def test_bf16_shapes_the_kernels_do_not_take_are_unsupported(lib):
     cfg = _cfg(S=2048, d=256, H=4, inter=512, D=4, dtype=tsp.TSP_BF16)
     assert lib.tsp_block_fwd(ctypes.byref(cfg), ok, ctypes.byref(aw), ctypes.byref(mw), ok,
                              None, ok, 1 << 40, None) == tsp.TSP_ERR_UNSUPPORTED
-    # chunk of 64 rows (not a multiple of the 128-row query tile)
+    # chunk of 64 rows (not a multiple of the 256-row attention block)
     cfg = _cfg(S=512, d=256, H=2, inter=512, D=4, dtype=tsp.TSP_BF16)
     assert lib.tsp_attn_block_fwd(ctypes.byref(cfg), ok, ctypes.byref(aw), ok, ok, 1 << 40,
                                   None) == tsp.TSP_ERR_UNSUPPORTED

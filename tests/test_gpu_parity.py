@@ -138,7 +138,7 @@ def test_bf16_mlp_half(S, d, I, D, norm, res):
     assert_bf16_close(y, ref, f"bf16 mlp S={S} D={D}")
 
 
-@pytest.mark.parametrize("S,H,D", [(1024, 2, 4), (512, 2, 1), (2048, 4, 8), (1536, 2, 3)])
+@pytest.mark.parametrize("S,H,D", [(2048, 2, 4), (512, 2, 1), (4096, 4, 8), (1536, 2, 3)])
 def test_bf16_attention_half(S, H, D):
     shape = BlockShape(S=S, d=128 * H, H=H, inter=256, D=D)
     inp = make_block_inputs(shape, torch.bfloat16, seed=S + H)
@@ -147,7 +147,7 @@ def test_bf16_attention_half(S, H, D):
     assert_bf16_close(h, ref, f"bf16 attention S={S} D={D}")
 
 
-@pytest.mark.parametrize("S,H,D", [(1024, 2, 4), (2048, 2, 8), (1536, 2, 3)])
+@pytest.mark.parametrize("S,H,D", [(2048, 2, 4), (4096, 2, 8), (1536, 2, 3)])
 def test_bf16_attention_dominated(S, H, D):
     """Sharper softmax (W_Q, W_K x8) and a large W_O (x60) so that the attention
     term, not the residual x, dominates h: checks the attention kernel itself."""
@@ -162,7 +162,7 @@ def test_bf16_attention_dominated(S, H, D):
     assert_bf16_close(h, ref, f"attention-dominated S={S} D={D}")
 
 
-@pytest.mark.parametrize("S,d,H,I,D", [(2048, 512, 4, 1024, 4), (2048, 256, 2, 512, 8),
+@pytest.mark.parametrize("S,d,H,I,D", [(2048, 512, 4, 1024, 4), (4096, 256, 2, 512, 8),
                                        (1024, 256, 2, 768, 2)])
 def test_bf16_block_small(S, d, H, I, D):
     shape = BlockShape(S=S, d=d, H=H, inter=I, D=D)
@@ -243,7 +243,7 @@ def test_fp32_backward_rank_sweep(D):
         assert_f32_close(g[k], v, f"{k} D={D}", tol=1e-4 * scale)
 
 
-@pytest.mark.parametrize("S,d,H,I,D", [(1024, 256, 2, 512, 4), (2048, 512, 4, 768, 8)])
+@pytest.mark.parametrize("S,d,H,I,D", [(2048, 256, 2, 512, 4), (4096, 512, 4, 768, 8)])
 def test_bf16_backward_small(S, d, H, I, D):
     shape = BlockShape(S=S, d=d, H=H, inter=I, D=D)
     inp = make_block_inputs(shape, torch.bfloat16, seed=5, with_dy=True)
