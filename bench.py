@@ -12,7 +12,7 @@ residual, un-permute y.  The step's working set (x 128 MiB, weights 405 MiB,
 activations > 1 GiB) is larger than L2, so no explicit flush is needed.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload fwd16k|fwd128k|fwdbwd32k|mlp16k]
+                    [--workload fwd16k|fwd128k|fwdbwd32k|fwdbwd8k|mlp16k]
 
 With N > 1 (torchrun, one rank per GPU) every rank runs its own replica
 ("replicas only": the block has no data-path exchange on one node's GPUs in
@@ -41,6 +41,7 @@ WORKLOADS = {
     "fwd16k": (16384, 8, 4096, 32, 11008, "fwd"),
     "fwd128k": (131072, 8, 4096, 32, 11008, "fwd"),
     "fwdbwd32k": (32768, 8, 4096, 32, 11008, "fwdbwd"),
+    "fwdbwd8k": (8192, 8, 4096, 32, 11008, "fwdbwd"),   # small case for profiler captures
     "mlp16k": (16384, 4, 4096, 32, 11008, "mlp"),
 }
 DEFAULT_WORKLOAD = "fwd16k"
@@ -61,8 +62,43 @@ def gemm_flops(name, S, d, inter):
         "gemm_w13_swiglu": 4.0 * S * d * inter,
         "gemm_w2": 2.0 * S * d * inter,
         "attn_fwd": 2.0 * S * (S + 1) * d,
+        # backward: dgrad and wgrad of every projection, and the attention
+        # backward's five causal products (S recomputed, dP, dV, dK, dQ)
+        "gemm_dgrad_w2_swiglu": 2.0 * S * d * inter,
+        "gemm_wgrad_w2": 2.0 * S * d * inter,
+        "gemm_wgrad_w13": 4.0 * S * d * inter,
+        "gemm_dgrad_w13": 4.0 * S * d * inter,
+        "gemm_wgrad_wo": 2.0 * S * d * d,
+        "gemm_dgrad_wo": 2.0 * S * d * d,
+        "gemm_wgrad_qkv": 6.0 * S * d * d,
+        "gemm_dgrad_qkv": 6.0 * S * d * d,
+        "attn_bwd": 5.0 * S * (S + 1) * d,
     }
     return table.get(name)
+
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# dominant kernel, from one ncu capture of `bench.py --workload <w>`; each entry
+# holds the SHA-256 of the kernel's source file at capture time, and the figure
+# is reported only while that source is unchanged (otherwise traffic is null).
+MEASURED_TRAFFIC = {
+    # (kernel, workload): (bytes per launch, source file, sha256 of the source)
+}
+
+
+def measured_traffic(kernel, workload):
+    import hashlib
+    ent = MEASURED_TRAFFIC.get((kernel, workload))
+    if ent is None:
+        return None
+    nbytes, src, sha = ent
+    try:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != sha:
+                return None
+    except OSError:
+        return None
+    return nbytes
 
 
 def measured_peaks():
@@ -371,7 +407,7 @@ def run_gpu(args):
         ach = per_kernel[dom]["tflops"]
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                 "frac": ach / peak, "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)",
-                "traffic": None}
+                "traffic": measured_traffic(dom, args.workload)}
     flops = block_flops(S, d, inter, kind)
     value = world * S / t_dev
     tflops = world * flops / t_dev / 1e12

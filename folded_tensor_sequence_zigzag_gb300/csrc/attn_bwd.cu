@@ -224,6 +224,17 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
         constexpr uint32_t id_kv = idesc_f16_f32(BC, DH, false, true, false);   // dV, dK
         constexpr uint32_t id_q = idesc_f16_f32(DH, BR, true, true, false);     // dQ^T
         bool ok = mbar_wait(kv_full, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
+        // base descriptors, computed once: the issue loops only add constants
+        const uint64_t dK_k = sdesc_sw128(base + OFF_K, 16, 1024);            // K, K-major
+        const uint64_t dV_k = sdesc_sw128(base + OFF_V, 16, 1024);            // V, K-major
+        const uint64_t dK_mn = sdesc_sw128(base + OFF_K, KT_BYTES / 2, 1024); // K^T, MN-major
+        const uint64_t dQ_k = sdesc_sw128(base + OFF_Q, 16, 1024);            // Q stages, K-major
+        const uint64_t dDO_k = sdesc_sw128(base + OFF_DO, 16, 1024);          // dO stages, K-major
+        const uint64_t dQ_mn = sdesc_sw128(base + OFF_Q, QT_BYTES / 2, 1024); // Q stages, MN-major
+        const uint64_t dDO_mn = sdesc_sw128(base + OFF_DO, QT_BYTES / 2, 1024);
+        const uint64_t dP_k = sdesc_sw128(base + OFF_P, 16, 1024);            // P^T buffers
+        const uint64_t dDS_k = sdesc_sw128(base + OFF_DS, 16, 1024);          // dS^T buffers
+        const uint64_t dDS_mn = sdesc_sw128(base + OFF_DS, PT_BYTES, 1024);   // dS, MN-major
         auto issue_s = [&](uint32_t cur) -> bool {
           const uint32_t st = qst(cur);
           if (!mbar_wait(qd_full(st), qph(cur), a.status, abort_flag, a.limit_ns))
@@ -231,15 +242,15 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           if (cur >= 1 && !mbar_wait(s_free, (cur - 1) & 1u, a.status, abort_flag, a.limit_ns))
             return false;
           tc_fence_after();
-          const uint32_t sq = base + OFF_Q + st * QT_BYTES, sdo = base + OFF_DO + st * QT_BYTES;
+          const uint64_t bq = sdesc_add(dQ_k, st * QT_BYTES), bdo = sdesc_add(dDO_k, st * QT_BYTES);
 #pragma unroll
           for (int kk = 0; kk < DH / 16; ++kk) {
             const uint32_t aoff = (kk >> 2) * (KT_BYTES / 2) + (kk & 3) * 32;
             const uint32_t boff = (kk >> 2) * (QT_BYTES / 2) + (kk & 3) * 32;
-            umma_f16_ss(tmem + TM_S, sdesc_sw128(base + OFF_K + aoff, 16, 1024),
-                        sdesc_sw128(sq + boff, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-            umma_f16_ss(tmem + TM_DP, sdesc_sw128(base + OFF_V + aoff, 16, 1024),
-                        sdesc_sw128(sdo + boff, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+            umma_f16_ss_hot(tmem + TM_S, sdesc_add(dK_k, aoff), sdesc_add(bq, boff), id_s,
+                            kk > 0 ? 1u : 0u);
+            umma_f16_ss_hot(tmem + TM_DP, sdesc_add(dV_k, aoff), sdesc_add(bdo, boff), id_s,
+                            kk > 0 ? 1u : 0u);
           }
           umma_commit(s_full);
           return true;
@@ -253,15 +264,16 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
             break;
           }
           tc_fence_after();
-          const uint32_t sp = base + OFF_P + pb * PT_BYTES, sds = base + OFF_DS + pb * PT_BYTES;
-          const uint32_t sq = base + OFF_Q + st * QT_BYTES, sdo = base + OFF_DO + st * QT_BYTES;
+          const uint64_t ap = sdesc_add(dP_k, pb * PT_BYTES), ads = sdesc_add(dDS_k, pb * PT_BYTES);
+          const uint64_t bdo = sdesc_add(dDO_mn, st * QT_BYTES), bq = sdesc_add(dQ_mn, st * QT_BYTES);
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < BR / 16; ++kk) {
-            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-            umma_f16_ss(tmem + TM_DV, sdesc_sw128(sp + kk * 32, 16, 1024),
-                        sdesc_sw128(sdo + kk * 2048, QT_BYTES / 2, 1024), id_kv, acc);
-            umma_f16_ss(tmem + TM_DK, sdesc_sw128(sds + kk * 32, 16, 1024),
-                        sdesc_sw128(sq + kk * 2048, QT_BYTES / 2, 1024), id_kv, acc);
+            const uint32_t acc = kk > 0 ? 1u : acc0;
+            umma_f16_ss_hot(tmem + TM_DV, sdesc_add(ap, kk * 32), sdesc_add(bdo, kk * 2048), id_kv,
+                            acc);
+            umma_f16_ss_hot(tmem + TM_DK, sdesc_add(ads, kk * 32), sdesc_add(bq, kk * 2048), id_kv,
+                            acc);
           }
           umma_commit(qd_empty(st));
           if (cur >= 1 && !mbar_wait(dq_empty, (cur - 1) & 1u, a.status, abort_flag, a.limit_ns)) {
@@ -269,10 +281,11 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
             break;
           }
           tc_fence_after();
+          const uint64_t bds = sdesc_add(dDS_mn, pb * PT_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BC / 16; ++kk)
-            umma_f16_ss(tmem + TM_DQ, sdesc_sw128(base + OFF_K + kk * 2048, KT_BYTES / 2, 1024),
-                        sdesc_sw128(sds + kk * 2048, PT_BYTES, 1024), id_q, kk > 0 ? 1u : 0u);
+            umma_f16_ss_hot(tmem + TM_DQ, sdesc_add(dK_mn, kk * 2048), sdesc_add(bds, kk * 2048),
+                            id_q, kk > 0 ? 1u : 0u);
           umma_commit(dq_full);
           umma_commit(p_free(pb));
         }

@@ -21,7 +21,7 @@
 // 128x128 scores into probabilities, the tensor core runs the other tile's
 // MMAs, so the MUFU/FMA work of the softmax hides behind tcgen05 work.
 //   warps 8-11 (one warpgroup, registers handed to the softmax warpgroups):
-//   warp 8   TMA producer: Q_A, Q_B once per block; K_j, V_j through a 3-slot
+//   warp 8   TMA producer: Q_A, Q_B once per block; K_j, V_j through a 4-slot
 //            ring of 128x128 fp16 tiles (128-byte swizzle, column boxes of
 //            the Q|K|V buffer);
 //   warp 9   TMEM allocator + MMA issuer, in the order
@@ -31,7 +31,12 @@
 //            (V read MN-major, dh contiguous, straight from the buffer);
 //   warps 0-3 / 4-7  softmax of tile A / B: thread = query row = TMEM lane;
 //            p = 2^(s*scale*log2e - m) with one FFMA + MUFU ex2 per score,
-//            written as fp16 into swizzled shared memory (A operand of PV).
+//            written as fp16 pairs into TMEM over the scores just read: PV
+//            takes P as its A operand from tensor memory.
+// Shared memory feeds the tensor core at about 128 bytes a clock per SM,
+// which an M=128, N=128 MMA with both operands in shared memory uses up on
+// its own; with P in TMEM, PV reads only V there, and no P store competes
+// with the operand reads.
 // The running max m is only raised (and O rescaled in TMEM) when a warp's row
 // max grows by more than 2^8; O/l is exact either way and p stays below 256.
 // All mbarrier waits are bounded (TSP_ERR_TIMEOUT); loop exits are
@@ -58,11 +63,14 @@ constexpr int REG_TOTAL = 2 * 128 * REG_SOFT + 128 * REG_CTRL;
 constexpr int WARP_PROD = 8, WARP_MMA = 9;
 constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128x128 fp16 tile (two 64-column boxes)
 constexpr int BOX_BYTES = TILE_BYTES / 2;  // 128 rows x 64 columns
-constexpr int NSLOT = 3;                   // K/V ring: K_0 V_0 K_1 V_1 ... in 3 slots
+constexpr int NSLOT = 4;                   // K/V ring: K_0 V_0 K_1 V_1 ... in 4 slots
 constexpr int OFF_Q = 0;                         // Q_A, Q_B
-constexpr int OFF_P = OFF_Q + 2 * TILE_BYTES;    // P_A, P_B
-constexpr int OFF_KV = OFF_P + 2 * TILE_BYTES;   // ring slots
+constexpr int OFF_KV = OFF_Q + 2 * TILE_BYTES;   // ring slots
 constexpr int OFF_BAR = OFF_KV + NSLOT * TILE_BYTES;
+// mbarrier indices
+constexpr int B_QFULL = 0, B_SFULL = 1, B_SEMPTY = B_SFULL + NSLOT, B_S = B_SEMPTY + NSLOT,
+              B_P = B_S + 2, B_O = B_P + 2, B_DRAIN = B_O + 2, N_BARS = B_DRAIN + 1;
+static_assert(N_BARS * 8 <= 160, "barriers overlap the TMEM slot");
 constexpr int SMEM = OFF_BAR + 256 + 1024;       // + 1 KB alignment slack
 constexpr uint32_t TMEM_COLS = 512;              // S_A | S_B | O_A | O_B
 constexpr float RESCALE_LOG2 = 8.0f;             // lazy-rescale threshold (log2 units)
@@ -96,13 +104,13 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + OFF_BAR;
-  const uint32_t q_full = bars;
-  auto slot_full = [&](uint32_t s) { return bars + 8u * (1 + s); };    // 1..3
-  auto slot_empty = [&](uint32_t s) { return bars + 8u * (4 + s); };   // 4..6
-  auto s_full = [&](int x) { return bars + 8u * (7 + x); };            // 7, 8
-  auto p_full = [&](int x) { return bars + 8u * (9 + x); };            // 9, 10
-  auto o_done = [&](int x) { return bars + 8u * (11 + x); };           // 11, 12
-  const uint32_t drain_bar = bars + 8u * 13;
+  const uint32_t q_full = bars + 8u * B_QFULL;
+  auto slot_full = [&](uint32_t s) { return bars + 8u * (B_SFULL + s); };
+  auto slot_empty = [&](uint32_t s) { return bars + 8u * (B_SEMPTY + s); };
+  auto s_full = [&](int x) { return bars + 8u * (B_S + x); };
+  auto p_full = [&](int x) { return bars + 8u * (B_P + x); };
+  auto o_done = [&](int x) { return bars + 8u * (B_O + x); };
+  const uint32_t drain_bar = bars + 8u * B_DRAIN;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 160);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_BAR + 168);
 
@@ -205,14 +213,18 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
             tc_fence_after();
             return true;
           };
+          // base descriptors, computed once: the issue loops only add constants
+          const uint64_t dq0 = sdesc_sw128(base + OFF_Q, 16, 1024);     // Q, K-major
+          const uint64_t dk0 = sdesc_sw128(base + OFF_KV, 16, 1024);    // K, K-major
+          const uint64_t dv0 = sdesc_sw128(base + OFF_KV, BOX_BYTES, 1024);   // V, MN-major
           auto mma_s = [&](int x, uint32_t kslot) {
-            const uint32_t sq = base + OFF_Q + x * TILE_BYTES;
-            const uint32_t sk = base + OFF_KV + kslot * TILE_BYTES;
+            const uint64_t da = sdesc_add(dq0, x * TILE_BYTES);
+            const uint64_t db = sdesc_add(dk0, kslot * TILE_BYTES);
 #pragma unroll
             for (int kk = 0; kk < DH / 16; ++kk) {
               const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-              umma_f16_ss(tmem + x * 128, sdesc_sw128(sq + off, 16, 1024),
-                          sdesc_sw128(sk + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+              umma_f16_ss_hot(tmem + x * 128, sdesc_add(da, off), sdesc_add(db, off), idesc_s,
+                              kk > 0 ? 1u : 0u);
             }
             umma_commit(s_full(x));
           };
@@ -220,15 +232,15 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
             const uint32_t cx = x == 0 ? cnt_a : cnt_b;
             if (!mbar_wait(p_full(x), cx & 1u, a.status, abort_flag, a.limit_ns)) return false;
             tc_fence_after();
-            const uint32_t sp = base + OFF_P + x * TILE_BYTES;
-            const uint32_t sv = base + OFF_KV + vslot * TILE_BYTES;
+            // P_x sits in TMEM (the first 64 columns of S_x, fp16 pairs): A from
+            // tensor memory, only V is read from shared memory
+            const uint32_t ta = tmem + x * 128;
+            const uint64_t db = sdesc_add(dv0, vslot * TILE_BYTES);
+            const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
-            for (int kk = 0; kk < BKV / 16; ++kk) {
-              const uint32_t poff = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-              umma_f16_ss(tmem + 256 + x * 128, sdesc_sw128(sp + poff, 16, 1024),
-                          sdesc_sw128(sv + kk * 2048, BOX_BYTES, 1024), idesc_o,
-                          (!first || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < BKV / 16; ++kk)
+              umma_f16_ts_hot(tmem + 256 + x * 128, ta + kk * 8, sdesc_add(db, kk * 2048), idesc_o,
+                              kk > 0 ? 1u : acc0);
             umma_commit(o_done(x));
             if (x == 0) ++cnt_a; else ++cnt_b;
             return true;
@@ -293,7 +305,6 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
         const int nX = x == 0 ? nA : nB;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const uint32_t tm_s = lane_base + x * 128, tm_o = lane_base + 256 + x * 128;
-        uint8_t* prow = gbase + OFF_P + x * TILE_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nX; ++j) {
@@ -315,12 +326,20 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
               for (int e = 0; e < 32; ++e)
                 if (q * 32 + e > row) sr[q][e] = __float_as_uint(-INFINITY);
           }
-          float mx = -INFINITY;
+          // row max over 16 independent partial maxima (short dependency chains)
+          float mp[16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
+          for (int k = 0; k < 16; ++k)
+            mp[k] = fmaxf(__uint_as_float(sr[0][k]), __uint_as_float(sr[0][k + 16]));
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[q][e]));
-          mx *= a.scale_log2;
+          for (int q = 1; q < 4; ++q)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mp[e & 15] = fmaxf(mp[e & 15], __uint_as_float(sr[q][e]));
+#pragma unroll
+          for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) mp[k] = fmaxf(mp[k], mp[k + w]);
+          const float mx = mp[0] * a.scale_log2;
           const bool mine = mx > m_used + RESCALE_LOG2;
           const bool resc = __any_sync(0xffffffffu, mine);
           float alpha = 1.f;
@@ -333,17 +352,18 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
           // probabilities first (fp16 pairs), so the scores' registers are free
           // before O is touched
           const float neg_m = -m_used;
-          float sum = 0.f;
-          uint32_t pk[64];
+          float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // partial row sums
+          uint32_t pk[2][32];   // column i of P_x holds keys 2i (low half) and 2i+1
 #pragma unroll
           for (int q = 0; q < 4; ++q)
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               const float p0v = ex2_approx(fmaf(__uint_as_float(sr[q][e]), a.scale_log2, neg_m));
               const float p1v = ex2_approx(fmaf(__uint_as_float(sr[q][e + 1]), a.scale_log2, neg_m));
-              sum += p0v + p1v;
-              pk[q * 16 + (e >> 1)] = pack_f16(p0v, p1v);
+              ps[(e >> 1) & 7] += p0v + p1v;
+              pk[q >> 1][(q & 1) * 16 + (e >> 1)] = pack_f16(p0v, p1v);
             }
+          const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
           // PV_x(j-1) must have finished before P_x is overwritten or O_x rescaled
           if (j > 0) {
             okl = mbar_wait(o_done(x), (c_now - 1) & 1u, a.status, abort_flag, a.limit_ns);
@@ -365,18 +385,12 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
               tmem_wait_st();
             }
           }
-          // keys q*32 .. q*32+31 -> box (q >> 1), 16-byte chunks 4*(q&1) .. +3
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int chunk = (q & 1) * 4 + c;
-              *reinterpret_cast<uint4*>(prow + (q >> 1) * BOX_BYTES + ((chunk ^ (row & 7)) << 4)) =
-                  make_uint4(pk[q * 16 + 4 * c], pk[q * 16 + 4 * c + 1], pk[q * 16 + 4 * c + 2],
-                             pk[q * 16 + 4 * c + 3]);
-            }
+          // P_x into TMEM over the scores just read (columns 0..63 of S_x); the
+          // next S_x MMA is issued after PV_x, which reads P_x first
+          tmem_st32(tm_s, pk[0]);
+          tmem_st32(tm_s + 32, pk[1]);
+          tmem_wait_st();
           l += sum;
-          fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(p_full(x));
           rounds = c_now + 1;

@@ -172,6 +172,34 @@ __device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// Same MMA for hot issue loops: no memory clobber, so the issuing thread's
+// descriptor arithmetic is scheduled freely around it.  Ordering against the
+// mbarrier waits that guard the operands still holds (volatile asm statements
+// keep their order), and the MMA touches no memory the compiler tracks.
+// One thread issues every MMA of a CTA, so its per-instruction cost adds up:
+// a K=16 step of an M=128 x N=128 MMA takes 64 tensor-core cycles, which the
+// issue path (descriptor arithmetic included) must stay under.
+__device__ __forceinline__ void umma_f16_ss_hot(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16: A (M rows = TMEM lanes,
+// K = 16 fp16 values packed two per 32-bit column, lower index in the low
+// half) is read from tensor memory, so only B is fetched from shared memory.
+__device__ __forceinline__ void umma_f16_ts_hot(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
 // Arrives once on `bar` when every tcgen05.mma issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -236,6 +264,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= 1ull << 46;
   d |= 2ull << 61;
   return d;
+}
+
+// A descriptor advanced by `bytes` (a multiple of 16): the start-address field
+// holds address >> 4 in its low bits, and shared-memory addresses stay far
+// below the field's 256 KB range, so the advance is a plain add.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
 }
 
 // Instruction descriptor, kind::f16 with 16-bit A/B (fp16: format 0, bf16:

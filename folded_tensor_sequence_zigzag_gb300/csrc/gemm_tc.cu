@@ -273,6 +273,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(BM, BN, A_MN, B_MN, false);
+      // stage-0 descriptors, computed once: the issue loop only adds constants
+      const uint64_t da0 = A_MN ? sdesc_sw128(base, 8192, 1024) : sdesc_sw128(base, 16, 1024);
+      const uint64_t db0 = B_MN ? sdesc_sw128(base + A_BYTES, 8192, 1024)
+                                : sdesc_sw128(base + A_BYTES, 16, 1024);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -291,16 +295,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
             break;
           }
           tc_fence_after();
-          const uint32_t sa = base + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          const uint64_t da = sdesc_add(da0, stage * STAGE_BYTES);
+          const uint64_t db = sdesc_add(db0, stage * STAGE_BYTES);
+          const uint32_t acc0 = i != 0 ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
-                                     : sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
-                                     : sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma_f16_ss(d_tmem, ad, bd, idesc, (i | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_f16_ss_hot(d_tmem, sdesc_add(da, A_MN ? kk * 2048 : kk * 32),
+                            sdesc_add(db, B_MN ? kk * 2048 : kk * 32), idesc, kk > 0 ? 1u : acc0);
           umma_commit(empty_bar(stage));
           if (++stage == STAGES) {
             stage = 0;

@@ -244,14 +244,131 @@ int rmsnorm_bwd_blocks(int64_t rows) {
   return (int)std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 2));
 }
 
-// out[i] = sum_b part[b][i]  (deterministic order)
-__global__ void rowsum_partials_kernel(const float* __restrict__ part, float* __restrict__ out,
-                                       int nb, int n) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
+// Fast path of K8 for n = 1024*K: 256 threads a CTA, thread t owns the
+// columns k*1024 + 4t .. +3 (k < K) of every row the CTA visits, so its share
+// of the gain gradient stays in registers and every load is a 16-byte (fp32)
+// or 8-byte (16-bit) vector.  Rows are read once; the row dot product is
+// reduced across the CTA with one barrier per row (double-buffered partials).
+template <typename T> __device__ __forceinline__ float4 load4(const T* p);
+template <> __device__ __forceinline__ float4 load4<float>(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+template <> __device__ __forceinline__ float4 load4<__half>(const __half* p) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+template <typename T> __device__ __forceinline__ void store4(T* p, float4 v);
+template <> __device__ __forceinline__ void store4<float>(float* p, float4 v) {
+  *reinterpret_cast<float4*>(p) = v;
+}
+template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 o;
+  o.x = *reinterpret_cast<const uint32_t*>(&a);
+  o.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = o;
+}
+template <> __device__ __forceinline__ void store4<__half>(__half* p, float4 v) {
+  const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+  uint2 o;
+  o.x = *reinterpret_cast<const uint32_t*>(&a);
+  o.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = o;
+}
+__device__ __forceinline__ float f4(const float4& v, int e) {
+  return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+template <int K, typename Tu, typename T, typename Tr, typename To>
+__global__ void __launch_bounds__(256) rmsnorm_bwd_vec_kernel(
+    const float* __restrict__ dout, const Tu* __restrict__ u, const T* __restrict__ g,
+    const float* __restrict__ rstd, const float* __restrict__ resid_f32,
+    const Tr* __restrict__ resid_t, float* __restrict__ out_f32, To* __restrict__ out_t,
+    float* __restrict__ dg_part, int64_t rows) {
+  constexpr int n = 1024 * K;
+  __shared__ float red[2][8];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  float4 gv[K], dg[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    gv[k] = load4(g + k * 1024 + 4 * t);
+    dg[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  int it = 0;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, ++it) {
+    const float r = rstd[row];
+    const int64_t base = row * n + 4 * t;
+    float4 dv[K], nv[K];
+    float dot = 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      dv[k] = load4(dout + base + k * 1024);
+      nv[k] = load4(u + base + k * 1024);
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      nv[k] = make_float4(nv[k].x * r, nv[k].y * r, nv[k].z * r, nv[k].w * r);
+      dot = fmaf(dv[k].x * gv[k].x, nv[k].x, dot);
+      dot = fmaf(dv[k].y * gv[k].y, nv[k].y, dot);
+      dot = fmaf(dv[k].z * gv[k].z, nv[k].z, dot);
+      dot = fmaf(dv[k].w * gv[k].w, nv[k].w, dot);
+      dg[k].x = fmaf(dv[k].x, nv[k].x, dg[k].x);
+      dg[k].y = fmaf(dv[k].y, nv[k].y, dg[k].y);
+      dg[k].z = fmaf(dv[k].z, nv[k].z, dg[k].z);
+      dg[k].w = fmaf(dv[k].w, nv[k].w, dg[k].w);
+    }
+    dot = warp_sum(dot);
+    if (lane == 0) red[it & 1][warp] = dot;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[it & 1][w];
+    tot *= 1.f / (float)n;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const float4 res = resid_f32 ? load4(resid_f32 + base + k * 1024)
+                                   : load4(resid_t + base + k * 1024);
+      float4 o;
+      o.x = res.x + r * (dv[k].x * gv[k].x - nv[k].x * tot);
+      o.y = res.y + r * (dv[k].y * gv[k].y - nv[k].y * tot);
+      o.z = res.z + r * (dv[k].z * gv[k].z - nv[k].z * tot);
+      o.w = res.w + r * (dv[k].w * gv[k].w - nv[k].w * tot);
+      if (out_f32) store4(out_f32 + base + k * 1024, o);
+      if (out_t) store4(out_t + base + k * 1024, o);
+    }
+  }
+  float* part = dg_part + (int64_t)blockIdx.x * n + 4 * t;
+#pragma unroll
+  for (int k = 0; k < K; ++k) store4(part + k * 1024, dg[k]);
+}
+
+// out[i] = sum_b part[b][i], b in a fixed order: 32 columns a CTA, the
+// partial rows split 8 ways and combined in shared memory (deterministic).
+__global__ void __launch_bounds__(256) rowsum_partials_kernel(const float* __restrict__ part,
+                                                              float* __restrict__ out, int nb,
+                                                              int n) {
+  __shared__ float acc[8][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int i = blockIdx.x * 32 + tx;
   float s = 0.f;
-  for (int b = 0; b < nb; ++b) s += part[(int64_t)b * n + i];
-  out[i] = s;
+  if (i < n)
+    for (int b = ty; b < nb; b += 8) s += part[(int64_t)b * n + i];
+  acc[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && i < n) {
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) o += acc[w][tx];
+    out[i] = o;
+  }
 }
 
 template <typename Tu, typename T, typename Tr, typename To>
@@ -259,15 +376,34 @@ static tsp_status rmsnorm_bwd_t(const float* dout, const Tu* u, const T* g, cons
                                 const float* resid_f32, const Tr* resid_t, float* out_f32, To* out_t,
                                 float* dg, float* dg_part, int64_t rows, int n, cudaStream_t st) {
   const int grid = rmsnorm_bwd_blocks(rows);
-  const size_t sm = (size_t)n * sizeof(float);
   Prof prof("rmsnorm_bwd", st, 2);
-  if (sm > 48 * 1024)
-    TSP_CUDA_TRY(cudaFuncSetAttribute(rmsnorm_bwd_kernel<Tu, T, Tr, To>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-  rmsnorm_bwd_kernel<Tu, T, Tr, To><<<grid, 256, sm, st>>>(dout, u, g, rstd, resid_f32, resid_t,
-                                                           out_f32, out_t, dg_part, rows, n);
+  auto al16 = [](const void* p) { return ((uintptr_t)p & 15u) == 0; };
+  const bool vec = n % 1024 == 0 && (n / 1024 == 1 || n / 1024 == 2 || n / 1024 == 4 ||
+                                     n / 1024 == 8) &&
+                   al16(dout) && al16(u) && al16(g) && al16(resid_f32) && al16(resid_t) &&
+                   al16(out_f32) && al16(out_t) && al16(dg_part);
+  if (vec) {
+#define TSP_RMSB_VEC(K)                                                                     \
+  rmsnorm_bwd_vec_kernel<K, Tu, T, Tr, To><<<grid, 256, 0, st>>>(dout, u, g, rstd, resid_f32, \
+                                                                 resid_t, out_f32, out_t,     \
+                                                                 dg_part, rows)
+    switch (n / 1024) {
+      case 1: TSP_RMSB_VEC(1); break;
+      case 2: TSP_RMSB_VEC(2); break;
+      case 4: TSP_RMSB_VEC(4); break;
+      default: TSP_RMSB_VEC(8); break;
+    }
+#undef TSP_RMSB_VEC
+  } else {
+    const size_t sm = (size_t)n * sizeof(float);
+    if (sm > 48 * 1024)
+      TSP_CUDA_TRY(cudaFuncSetAttribute(rmsnorm_bwd_kernel<Tu, T, Tr, To>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+    rmsnorm_bwd_kernel<Tu, T, Tr, To><<<grid, 256, sm, st>>>(dout, u, g, rstd, resid_f32, resid_t,
+                                                             out_f32, out_t, dg_part, rows, n);
+  }
   TSP_CUDA_TRY(cudaGetLastError());
-  rowsum_partials_kernel<<<(n + 255) / 256, 256, 0, st>>>(dg_part, dg, grid, n);
+  rowsum_partials_kernel<<<(n + 31) / 32, 256, 0, st>>>(dg_part, dg, grid, n);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }

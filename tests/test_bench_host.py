@@ -21,6 +21,34 @@ def test_flop_counts():
     assert bench.block_flops(S, d, I, "mlp") == 6 * S * d * I
 
 
+def test_kernel_flop_table_adds_up():
+    """The per-kernel table covers the step: forward kernels sum to the block's
+    forward flops, backward GEMMs to twice the forward projections."""
+    S, d, I = 8192, 4096, 11008
+    fwd = ["gemm_qkv", "gemm_oproj", "gemm_w13_swiglu", "gemm_w2", "attn_fwd"]
+    assert sum(bench.gemm_flops(k, S, d, I) for k in fwd) == bench.block_flops(S, d, I, "fwd")
+    bwd_gemms = ["gemm_dgrad_w2_swiglu", "gemm_wgrad_w2", "gemm_wgrad_w13", "gemm_dgrad_w13",
+                 "gemm_wgrad_wo", "gemm_dgrad_wo", "gemm_wgrad_qkv", "gemm_dgrad_qkv"]
+    proj = sum(bench.gemm_flops(k, S, d, I) for k in fwd[:4])
+    assert sum(bench.gemm_flops(k, S, d, I) for k in bwd_gemms) == 2 * proj
+    assert bench.gemm_flops("attn_bwd", S, d, I) == 2.5 * bench.gemm_flops("attn_fwd", S, d, I)
+
+
+def test_traffic_figure_tracks_its_source(tmp_path, monkeypatch):
+    """A stored ncu traffic figure is reported only while the kernel source
+    it was taken on is unchanged."""
+    import hashlib
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    sha = hashlib.sha256(b"kernel v1").hexdigest()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "MEASURED_TRAFFIC", {("k", "w"): (1234, "k.cu", sha)})
+    assert bench.measured_traffic("k", "w") == 1234
+    assert bench.measured_traffic("k", "other") is None
+    src.write_text("kernel v2")
+    assert bench.measured_traffic("k", "w") is None
+
+
 def _rank(rank, world, port, q):
     import torch.distributed as dist
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),

@@ -243,7 +243,9 @@ def test_fp32_backward_rank_sweep(D):
         assert_f32_close(g[k], v, f"{k} D={D}", tol=1e-4 * scale)
 
 
-@pytest.mark.parametrize("S,d,H,I,D", [(2048, 256, 2, 512, 4), (4096, 512, 4, 768, 8)])
+@pytest.mark.parametrize("S,d,H,I,D", [(2048, 256, 2, 512, 4), (4096, 512, 4, 768, 8),
+                                       # d = 1024 and 2048: the vectorised RMSNorm backward
+                                       (2048, 1024, 8, 1024, 4), (1024, 2048, 16, 512, 2)])
 def test_bf16_backward_small(S, d, H, I, D):
     shape = BlockShape(S=S, d=d, H=H, inter=I, D=D)
     inp = make_block_inputs(shape, torch.bfloat16, seed=5, with_dy=True)
