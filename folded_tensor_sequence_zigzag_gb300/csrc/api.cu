@@ -204,7 +204,7 @@ BwdWs bwd_layout(const tsp_cfg* c, uint8_t* base) {
   W.dO = take(S * d * e);
   W.dqkv = take(S * 3 * d * e);
   W.da = take(S * d * 4);
-  W.delta = (float*)take(H * S * 4);
+  W.delta = (float*)take(2 * H * S * 4);   // Delta [H, S], then (bf16 path) LSE*log2(e) - 8
   if (c->dtype == TSP_BF16) W.dq_acc = (float*)take(S * d * 4);
   W.dg_part = (float*)take((size_t)rmsnorm_bwd_blocks(c->S) * d * 4);
   if (c->dtype == TSP_BF16) W.dy16 = take(S * d * 2);

@@ -13,24 +13,37 @@
 //
 // Work unit = one CTA = (head, virtual rank r, key tile t of 128 keys): key
 // tile t of chunk r and the mirrored tile of chunk 2D-1-r, each walking the
-// 64-row query tiles at positions >= the tile; the two query ranges add up to
-// S + 128 rows for every (r, t), so CTAs are balanced.  Per query tile:
-//   warp 12  TMA producer: K, V once per key tile; Q_i, dO_i (+ LSE_i, Delta_i
-//            by bulk copy) into a 3-stage ring;
-//   warp 13  MMA issuer: S^T = K Q_i^T and dP^T = V dO_i^T (M = 128 keys,
-//            N = 64 queries) for tile i+1 as soon as tile i's were read; then
-//            dV += P^T dO_i, dK += dS^T Q_i (TMEM accumulators across every
-//            query tile) and dQ_i^T = K^T dS^T (M = 128 dh, N = 64 queries);
-//   warps 0-7 (key = TMEM lane; warps w and w+4 share 32 keys, each thread
-//            owning 32 of the 64 query columns): P = 2^(s*scale*log2e - LSE*log2e),
-//            dS = P (dP - Delta), both written as fp16 (scaled by 2^8 to keep
-//            small probabilities in fp16's normal range) into swizzled smem,
-//            which serves as the K-major A operand of dV/dK and, unchanged, as
-//            the MN-major B operand of dQ^T; at the end dK, dV -> fp16 rows;
-//   warps 8-11 (thread = dh = TMEM lane): drain dQ_i^T from TMEM into the fp32
-//            dQ accumulator with warp-coalesced atomics.
-// All mbarrier waits are bounded (TSP_ERR_TIMEOUT) and every loop exit is
-// uniform across the threads that share a barrier.
+// 128-row query tiles at positions >= the tile; the two query ranges add up to
+// S + 128 rows for every (r, t), so CTAs are balanced.  Every MMA is
+// M = 128, N = 128 (an N = 64 MMA costs three quarters of an N = 128 one).
+//
+// Tensor memory (512 columns) is time-shared per query tile c:
+//   cols   0..127  S^T(c) = K Q_c^T, then dQ^T(c) = K^T dS^T(c);
+//   cols 128..255  dP^T(c) = V dO_c^T; the P/dS warps overwrite it with
+//                  P^T(c) as fp16 pairs (each thread only over columns it has
+//                  read), the A operand of dV;
+//   cols 256..511  dV, dK accumulated over all query tiles of the key tile.
+// One issue burst per query tile, in tensor-core order
+//   dK(c) | dQ^T(c) | dV(c) | dP^T(c+1) | S^T(c+1)
+// (dP^T(c+1) follows dV(c), which read P^T(c) from the same columns; S^T(c+1)
+// waits until the dQ drain has read dQ^T(c), which the three MMA groups in
+// between leave time for).  All MMAs of a tile are issued while the FFMA-heavy
+// P/dS warps wait: a tcgen05.mma issue needs scheduler slots that those warps
+// would otherwise take.
+//   warps 0-7  P/dS: thread = key = TMEM lane, warps w and w+4 share 32 keys
+//              and take 64 query columns each: 2^8 P = 2^(s*scale*log2e - L2)
+//              with L2 = LSE*log2e - 8 precomputed per query (the 2^8 keeps
+//              small probabilities in fp16's normal range), dS = P (dP - Delta)
+//              at the same scale; P^T into TMEM, dS^T into swizzled shared memory (the
+//              K-major A operand of dK and the MN-major B operand of dQ^T);
+//              at the end of a key tile dK (warps 0-3), dV (4-7) -> fp16 rows;
+//   warps 8-11 dQ drain (thread = dh = TMEM lane): dQ^T(c) into the fp32 dQ
+//              accumulator with warp-coalesced atomics;
+//   warp 12    TMA producer: K, V once per key tile; Q_c, dO_c (+ LSE_c,
+//              Delta_c by bulk copy) through a 2-stage ring;
+//   warp 13    TMEM allocator + MMA issuer.
+// All mbarrier waits are bounded (TSP_ERR_TIMEOUT); TMEM accesses and loop
+// exits are warp-uniform.
 #include <cstring>
 #include <memory>
 
@@ -41,32 +54,40 @@ namespace tsp {
 
 namespace {
 
-constexpr int BC = 128, BR = 64, DH = 128;
-constexpr int NSOFT = 256;                 // 8 warps: two threads per key row
-constexpr int NTHR = NSOFT + 128 + 64;     // + 4 dQ-drain warps + producer + MMA
-constexpr int WARP_PROD = 12, WARP_MMA = 13;   // warps 8-11 drain dQ
-constexpr int KT_BYTES = BC * DH * 2;      // 32 KB: 128 keys x 128 dh
-constexpr int QT_BYTES = BR * DH * 2;      // 16 KB: 64 queries x 128 dh
-constexpr int PT_BYTES = BC * BR * 2;      // 16 KB: 128 keys x 64 queries
+constexpr int BC = 128, BR = 128, DH = 128;
+constexpr int NTHR = 512;                  // P/dS x8, dQ drain x4, producer, MMA, 2 idle
+// Register split (setmaxnreg): the dQ drain holds a whole dQ^T row of 128 fp32
+// values, so its warpgroup takes REG_DRAIN registers a thread from the
+// producer/MMA warpgroup; the P/dS warpgroups keep the launch count.  The host
+// checks the sum against the launch allocation before every launch.
+constexpr int REG_CTRL = 96, REG_DRAIN = 160;
+constexpr int WARP_DRAIN = 8, WARP_PROD = 12, WARP_MMA = 13;
+constexpr int TILE_BYTES = 128 * 128 * 2;  // 32 KB: 128 rows x 128 fp16
+constexpr int BOX_BYTES = TILE_BYTES / 2;  // 128 rows x 64 columns (one TMA box)
+constexpr int QSTAGES = 2;                 // Q/dO ring depth
 constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + KT_BYTES;
-constexpr int QSTAGES = 3;                        // Q/dO ring depth (covers TMA latency)
-constexpr int OFF_Q = OFF_V + KT_BYTES;            // QSTAGES stages
-constexpr int OFF_DO = OFF_Q + QSTAGES * QT_BYTES; // QSTAGES stages
-constexpr int OFF_P = OFF_DO + QSTAGES * QT_BYTES; // 2 buffers
-constexpr int OFF_DS = OFF_P + 2 * PT_BYTES;       // 2 buffers
-constexpr int OFF_L = OFF_DS + 2 * PT_BYTES;       // [QSTAGES][LSE 64 | Delta 64] floats
+constexpr int OFF_V = OFF_K + TILE_BYTES;
+constexpr int OFF_Q = OFF_V + TILE_BYTES;               // QSTAGES stages
+constexpr int OFF_DO = OFF_Q + QSTAGES * TILE_BYTES;    // QSTAGES stages
+constexpr int OFF_DS = OFF_DO + QSTAGES * TILE_BYTES;   // dS^T, one buffer
+constexpr int OFF_L = OFF_DS + TILE_BYTES;              // [stage][LSE 128 | Delta 128] floats
 constexpr int OFF_BAR = OFF_L + QSTAGES * 2 * BR * 4;
-constexpr int SMEM = OFF_BAR + 256 + 1024;
+constexpr int SMEM = OFF_BAR + 256;        // the dynamic base must be 1024-byte aligned
+static_assert(SMEM <= 232448, "shared memory above the per-block limit");
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DQ = 128, TM_DV = 256, TM_DK = 384;
-constexpr float kOperandScale = 256.f;           // P, dS scaling into fp16's normal range
+constexpr uint32_t TM_SQ = 0, TM_DPP = 128, TM_DV = 256, TM_DK = 384;
+constexpr float kOperandLog2Scale = 8.f;         // P, dS scaled by 2^8 into fp16's normal range
 constexpr float kOperandUnscale = 1.f / 256.f;
+// mbarrier indices
+constexpr int B_KV = 0, B_QFULL = 1, B_QEMPTY = B_QFULL + QSTAGES, B_DP = B_QEMPTY + QSTAGES,
+              B_P = B_DP + 1, B_DQF = B_P + 1, B_DQE = B_DQF + 1, B_KVDONE = B_DQE + 1,
+              B_DRAIN = B_KVDONE + 1, N_BARS = B_DRAIN + 1;
+static_assert(N_BARS * 8 <= 160, "barriers overlap the TMEM slot");
 
 struct TcBwdArgs {
-  CUtensorMap tm_qkv;   // Q|K|V [S, 3d] fp16, box {64, 64}, 128B swizzle
-  CUtensorMap tm_do;    // dO [S, d] fp16, box {64, 64}, 128B swizzle
-  const float* lse;     // [H, S]
+  CUtensorMap tm_qkv;   // Q|K|V [S, 3d] fp16, box {64, 128}, 128B swizzle
+  CUtensorMap tm_do;    // dO [S, d] fp16, box {64, 128}, 128B swizzle
+  const float* lse2;    // [H, S]: LSE * log2(e) - 8
   const float* delta;   // [H, S]
   float* dq_acc;        // [S, d] fp32, zeroed
   ct_t* dqkv;           // [S, 3d]: dK, dV written here
@@ -86,6 +107,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// barrier `id` over `nthreads` threads (whole warps), independent of barrier 0
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
@@ -93,43 +119,30 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-// Named barrier of the P/dS warps (id 1, 256 threads) or of the dQ warps
-// (id 2, 128 threads) that ANDs a predicate: a loop exit taken on a failed
-// (timed-out) wait is the same for all of them.
-__device__ __forceinline__ bool group_bar_and(int id, int nthreads, bool pred) {
-  uint32_t res;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(res)
-      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
-      : "memory");
-  return res != 0;
-}
-
 __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_constant__ TcBwdArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (base - raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base = smem_u32(smem_raw);
+  uint8_t* gbase = smem_raw;
   const uint32_t bars = base + OFF_BAR;
-  const uint32_t kv_full = bars;
-  auto qd_full = [&](uint32_t s) { return bars + 8u * (1 + s); };       // 1..3
-  auto qd_empty = [&](uint32_t s) { return bars + 8u * (4 + s); };      // 4..6
-  const uint32_t s_full = bars + 8u * 7;
-  const uint32_t s_free = bars + 8u * 8;
-  auto p_full = [&](uint32_t b) { return bars + 8u * (9 + b); };
-  auto p_free = [&](uint32_t b) { return bars + 8u * (11 + b); };
-  const uint32_t dq_full = bars + 8u * 13;
-  const uint32_t dq_empty = bars + 8u * 14;
-  const uint32_t kv_done = bars + 8u * 15;
-  const uint32_t drain_bar = bars + 8u * 16;
+  const uint32_t kv_full = bars + 8u * B_KV;
+  auto qd_full = [&](uint32_t s) { return bars + 8u * (B_QFULL + s); };
+  auto qd_empty = [&](uint32_t s) { return bars + 8u * (B_QEMPTY + s); };
+  const uint32_t dp_full = bars + 8u * B_DP;     // S^T(c), dP^T(c) and all earlier MMAs done
+  const uint32_t p_full = bars + 8u * B_P;       // P^T(c) in TMEM, dS^T(c) in shared memory
+  const uint32_t dq_full = bars + 8u * B_DQF;
+  const uint32_t dq_empty = bars + 8u * B_DQE;
+  const uint32_t kv_done = bars + 8u * B_KVDONE;
+  const uint32_t drain_bar = bars + 8u * B_DRAIN;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 160);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_BAR + 168);
 
   if (*(volatile int*)a.status != 0) return;  // an earlier device error skips the work
+  // the 128-byte-swizzled tiles need a 1024-byte aligned base; the layout has
+  // no slack to realign it
+  if (base & 1023u) {
+    if (threadIdx.x == 0) report_status(a.status, (int)TSP_ERR_UNSUPPORTED);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
@@ -145,12 +158,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
       mbar_init(qd_full(s), 1);
       mbar_init(qd_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(p_full(b), NSOFT);
-      mbar_init(p_free(b), 1);
-    }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, NSOFT);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(kv_done, 1);
@@ -171,210 +180,263 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  float* sLD = reinterpret_cast<float*>(gbase + OFF_L);  // [stage][LSE 64 | Delta 64]
+  float* sLD = reinterpret_cast<float*>(gbase + OFF_L);  // [stage][LSE 128 | Delta 128]
   // Q/dO ring position of query tile `cur` (CTA-wide counter)
   auto qst = [](uint32_t cur) { return cur % QSTAGES; };
   auto qph = [](uint32_t cur) { return (cur / QSTAGES) & 1u; };
 
-  uint32_t it = 0;        // query tiles processed by this CTA so far
-  uint32_t q_issued = 0, kv_issued = 0;
-  for (int tile = 0; tile < 2; ++tile) {
-    const int64_t k0 = k0s[tile];
-    const int nq = (int)((a.S - k0) / BR);
-    const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
-    if (warp == WARP_PROD) {
-      // ------------------------------------------------------------ producer
-      if (lane == 0 && !*abort_flag) {
-        mbar_arrive_expect_tx(kv_full, 2 * KT_BYTES);
-#pragma unroll
-        for (int jh = 0; jh < 2; ++jh)
-#pragma unroll
-          for (int rh = 0; rh < 2; ++rh) {
-            const uint32_t off = jh * (KT_BYTES / 2) + rh * (KT_BYTES / 4);
-            tma_load_2d(base + OFF_K + off, &a.tm_qkv, a.d + h * DH + 64 * jh,
-                        (int)(krow0 + 64 * rh), kv_full);
-            tma_load_2d(base + OFF_V + off, &a.tm_qkv, 2 * a.d + h * DH + 64 * jh,
-                        (int)(krow0 + 64 * rh), kv_full);
-          }
-        ++kv_issued;
-        for (int j = 0; j < nq; ++j) {
-          const uint32_t cur = it + j, st = qst(cur);
-          if (!mbar_wait(qd_empty(st), qph(cur) ^ 1u, a.status, abort_flag, a.limit_ns))
-            break;
-          const int64_t qrow = zz_row_of_pos(k0 + (int64_t)j * BR, a.c, a.D);
-          const uint32_t fb = qd_full(st);
-          mbar_arrive_expect_tx(fb, 2 * QT_BYTES + 2 * BR * 4);
+  // Each role runs its own loop over the two key tiles, so the register limit
+  // that setmaxnreg sets covers all code of that role.
+  uint32_t it = 0;        // query tiles processed by this CTA so far (one copy per role)
+  auto tile_sync = [&]() {  // K/V tiles, TMEM accumulators and barrier phases move on
+    tc_fence_before();
+    named_bar_sync(1, NTHR);
+    tc_fence_after();
+  };
+  if (warp >= WARP_PROD) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(REG_CTRL));
+    uint32_t q_issued = 0, kv_issued = 0;
+    for (int tile = 0; tile < 2; ++tile) {
+      const int64_t k0 = k0s[tile];
+      const int nq = (int)((a.S - k0) / BR);
+      const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
+      if (warp == WARP_PROD) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && !*abort_flag) {
+          mbar_arrive_expect_tx(kv_full, 2 * TILE_BYTES);
 #pragma unroll
           for (int jh = 0; jh < 2; ++jh) {
-            tma_load_2d(base + OFF_Q + st * QT_BYTES + jh * (QT_BYTES / 2), &a.tm_qkv,
-                        h * DH + 64 * jh, (int)qrow, fb);
-            tma_load_2d(base + OFF_DO + st * QT_BYTES + jh * (QT_BYTES / 2), &a.tm_do,
-                        h * DH + 64 * jh, (int)qrow, fb);
+            tma_load_2d(base + OFF_K + jh * BOX_BYTES, &a.tm_qkv, a.d + h * DH + 64 * jh, (int)krow0,
+                        kv_full);
+            tma_load_2d(base + OFF_V + jh * BOX_BYTES, &a.tm_qkv, 2 * a.d + h * DH + 64 * jh,
+                        (int)krow0, kv_full);
           }
-          const uint32_t sl = smem_u32(sLD + st * 2 * BR);
-          bulk_load(sl, a.lse + (int64_t)h * a.S + qrow, BR * 4, fb);
-          bulk_load(sl + BR * 4, a.delta + (int64_t)h * a.S + qrow, BR * 4, fb);
-          ++q_issued;
-        }
-      }
-    } else if (warp == WARP_MMA) {
-      // ------------------------------------------------------------ MMA issuer
-      if (lane == 0 && !*abort_flag) {
-        constexpr uint32_t id_s = idesc_f16_f32(BC, BR, false, false, false);   // S^T, dP^T
-        constexpr uint32_t id_kv = idesc_f16_f32(BC, DH, false, true, false);   // dV, dK
-        constexpr uint32_t id_q = idesc_f16_f32(DH, BR, true, true, false);     // dQ^T
-        bool ok = mbar_wait(kv_full, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
-        // base descriptors, computed once: the issue loops only add constants
-        const uint64_t dK_k = sdesc_sw128(base + OFF_K, 16, 1024);            // K, K-major
-        const uint64_t dV_k = sdesc_sw128(base + OFF_V, 16, 1024);            // V, K-major
-        const uint64_t dK_mn = sdesc_sw128(base + OFF_K, KT_BYTES / 2, 1024); // K^T, MN-major
-        const uint64_t dQ_k = sdesc_sw128(base + OFF_Q, 16, 1024);            // Q stages, K-major
-        const uint64_t dDO_k = sdesc_sw128(base + OFF_DO, 16, 1024);          // dO stages, K-major
-        const uint64_t dQ_mn = sdesc_sw128(base + OFF_Q, QT_BYTES / 2, 1024); // Q stages, MN-major
-        const uint64_t dDO_mn = sdesc_sw128(base + OFF_DO, QT_BYTES / 2, 1024);
-        const uint64_t dP_k = sdesc_sw128(base + OFF_P, 16, 1024);            // P^T buffers
-        const uint64_t dDS_k = sdesc_sw128(base + OFF_DS, 16, 1024);          // dS^T buffers
-        const uint64_t dDS_mn = sdesc_sw128(base + OFF_DS, PT_BYTES, 1024);   // dS, MN-major
-        auto issue_s = [&](uint32_t cur) -> bool {
-          const uint32_t st = qst(cur);
-          if (!mbar_wait(qd_full(st), qph(cur), a.status, abort_flag, a.limit_ns))
-            return false;
-          if (cur >= 1 && !mbar_wait(s_free, (cur - 1) & 1u, a.status, abort_flag, a.limit_ns))
-            return false;
-          tc_fence_after();
-          const uint64_t bq = sdesc_add(dQ_k, st * QT_BYTES), bdo = sdesc_add(dDO_k, st * QT_BYTES);
+          ++kv_issued;
+          for (int j = 0; j < nq; ++j) {
+            const uint32_t cur = it + j, st = qst(cur);
+            if (!mbar_wait(qd_empty(st), qph(cur) ^ 1u, a.status, abort_flag, a.limit_ns)) break;
+            const int64_t qrow = zz_row_of_pos(k0 + (int64_t)j * BR, a.c, a.D);
+            const uint32_t fb = qd_full(st);
+            mbar_arrive_expect_tx(fb, 2 * TILE_BYTES + 2 * BR * 4);
 #pragma unroll
-          for (int kk = 0; kk < DH / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * (KT_BYTES / 2) + (kk & 3) * 32;
-            const uint32_t boff = (kk >> 2) * (QT_BYTES / 2) + (kk & 3) * 32;
-            umma_f16_ss_hot(tmem + TM_S, sdesc_add(dK_k, aoff), sdesc_add(bq, boff), id_s,
-                            kk > 0 ? 1u : 0u);
-            umma_f16_ss_hot(tmem + TM_DP, sdesc_add(dV_k, aoff), sdesc_add(bdo, boff), id_s,
-                            kk > 0 ? 1u : 0u);
-          }
-          umma_commit(s_full);
-          return true;
-        };
-        if (ok) ok = issue_s(it);
-        for (int j = 0; j < nq && ok; ++j) {
-          const uint32_t cur = it + j, st = qst(cur), pb = cur & 1u;
-          if (j + 1 < nq && !(ok = issue_s(cur + 1))) break;
-          if (!mbar_wait(p_full(pb), (cur >> 1) & 1u, a.status, abort_flag, a.limit_ns)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t ap = sdesc_add(dP_k, pb * PT_BYTES), ads = sdesc_add(dDS_k, pb * PT_BYTES);
-          const uint64_t bdo = sdesc_add(dDO_mn, st * QT_BYTES), bq = sdesc_add(dQ_mn, st * QT_BYTES);
-          const uint32_t acc0 = j > 0 ? 1u : 0u;
-#pragma unroll
-          for (int kk = 0; kk < BR / 16; ++kk) {
-            const uint32_t acc = kk > 0 ? 1u : acc0;
-            umma_f16_ss_hot(tmem + TM_DV, sdesc_add(ap, kk * 32), sdesc_add(bdo, kk * 2048), id_kv,
-                            acc);
-            umma_f16_ss_hot(tmem + TM_DK, sdesc_add(ads, kk * 32), sdesc_add(bq, kk * 2048), id_kv,
-                            acc);
-          }
-          umma_commit(qd_empty(st));
-          if (cur >= 1 && !mbar_wait(dq_empty, (cur - 1) & 1u, a.status, abort_flag, a.limit_ns)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t bds = sdesc_add(dDS_mn, pb * PT_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BC / 16; ++kk)
-            umma_f16_ss_hot(tmem + TM_DQ, sdesc_add(dK_mn, kk * 2048), sdesc_add(bds, kk * 2048),
-                            id_q, kk > 0 ? 1u : 0u);
-          umma_commit(dq_full);
-          umma_commit(p_free(pb));
-        }
-        if (ok) {
-          umma_commit(kv_done);
-        } else {
-          umma_commit(drain_bar);
-          drain_wait(drain_bar, 0, a.limit_ns);
-        }
-      }
-    } else if (warp < 8) {
-      // ------------------------------------------------------------ P, dS (thread = key)
-      const int quarter = warp & 3, half = warp >> 2;
-      const int row = quarter * 32 + lane;
-      const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-      const int64_t kp = k0 + row;
-      constexpr float LOG2E = 1.4426950408889634f;
-      bool ok = true;
-      for (int j = 0; j < nq; ++j) {
-        const uint32_t cur = it + j, st = qst(cur), pb = cur & 1u;
-        bool okl = ok && mbar_wait(s_full, cur & 1u, a.status, abort_flag, a.limit_ns);
-        okl = okl && mbar_wait(qd_full(st), qph(cur), a.status, abort_flag, a.limit_ns);
-        // buffer pb was last read by the MMAs of query tile cur-2
-        if (okl && cur >= 2)
-          okl = mbar_wait(p_free(pb), ((cur - 2) >> 1) & 1u, a.status, abort_flag, a.limit_ns);
-        ok = group_bar_and(1, NSOFT, okl);
-        if (!ok) break;
-        uint32_t sv[32], dv[32];
-        tc_fence_after();
-        tmem_ld32(lane_base + TM_S + half * 32, sv);
-        tmem_ld32(lane_base + TM_DP + half * 32, dv);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(s_free);
-        const float* L = sLD + st * 2 * BR;
-        const float* Dl = L + BR;
-        const int64_t q0 = k0 + (int64_t)j * BR;
-        const bool diag = q0 < k0 + BC;
-        uint8_t* prow = gbase + OFF_P + pb * PT_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
-        uint8_t* drow = gbase + OFF_DS + pb * PT_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
-        // this thread's 32 query columns, 8 at a time (LSE, Delta read as float4)
-        const float neg_l_scale = -LOG2E;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int qb = half * 32 + c * 8;
-          const float4 l0 = *reinterpret_cast<const float4*>(L + qb);
-          const float4 l1 = *reinterpret_cast<const float4*>(L + qb + 4);
-          const float4 d0 = *reinterpret_cast<const float4*>(Dl + qb);
-          const float4 d1 = *reinterpret_cast<const float4*>(Dl + qb + 4);
-          const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-          const float dlv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-          uint32_t pk[4], dk[4];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            float pp[2], dd[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int x = c * 8 + e + u;
-              float p = ex2_approx(fmaf(__uint_as_float(sv[x]), a.scale_log2, lv[e + u] * neg_l_scale));
-              if (diag && kp > q0 + qb + e + u) p = 0.f;
-              pp[u] = p * kOperandScale;
-              dd[u] = pp[u] * (__uint_as_float(dv[x]) - dlv[e + u]);
+            for (int jh = 0; jh < 2; ++jh) {
+              tma_load_2d(base + OFF_Q + st * TILE_BYTES + jh * BOX_BYTES, &a.tm_qkv,
+                          h * DH + 64 * jh, (int)qrow, fb);
+              tma_load_2d(base + OFF_DO + st * TILE_BYTES + jh * BOX_BYTES, &a.tm_do,
+                          h * DH + 64 * jh, (int)qrow, fb);
             }
-            pk[e >> 1] = pack_f16(pp[0], pp[1]);
-            dk[e >> 1] = pack_f16(dd[0], dd[1]);
+            const uint32_t sl = smem_u32(sLD + st * 2 * BR);
+            bulk_load(sl, a.lse2 + (int64_t)h * a.S + qrow, BR * 4, fb);
+            bulk_load(sl + BR * 4, a.delta + (int64_t)h * a.S + qrow, BR * 4, fb);
+            ++q_issued;
           }
-          const int chunk = half * 4 + c;
-          const uint32_t off = (uint32_t)((chunk ^ (row & 7)) << 4);
-          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(drow + off) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(p_full(pb));
+      } else if (warp == WARP_MMA) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && !*abort_flag) {
+          constexpr uint32_t id_f = idesc_f16_f32(128, 128, false, false, false);  // S^T, dP^T
+          constexpr uint32_t id_kv = idesc_f16_f32(128, 128, false, true, false);  // dV, dK
+          constexpr uint32_t id_q = idesc_f16_f32(128, 128, true, true, false);    // dQ^T
+          // base descriptors, computed once: the issue loops only add constants
+          const uint64_t dK_k = sdesc_sw128(base + OFF_K, 16, 1024);           // K, K-major
+          const uint64_t dV_k = sdesc_sw128(base + OFF_V, 16, 1024);           // V, K-major
+          const uint64_t dK_mn = sdesc_sw128(base + OFF_K, BOX_BYTES, 1024);   // K^T, MN-major
+          const uint64_t dQ_k = sdesc_sw128(base + OFF_Q, 16, 1024);           // Q stages
+          const uint64_t dDO_k = sdesc_sw128(base + OFF_DO, 16, 1024);         // dO stages
+          const uint64_t dQ_mn = sdesc_sw128(base + OFF_Q, BOX_BYTES, 1024);
+          const uint64_t dDO_mn = sdesc_sw128(base + OFF_DO, BOX_BYTES, 1024);
+          const uint64_t dDS_k = sdesc_sw128(base + OFF_DS, 16, 1024);         // dS^T, K-major
+          const uint64_t dDS_mn = sdesc_sw128(base + OFF_DS, BOX_BYTES, 1024); // dS^T, MN-major
+          bool ok = mbar_wait(kv_full, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
+          // S^T(cur) = K Q^T or dP^T(cur) = V dO^T: M = 128 keys, N = 128 queries, K = dh
+          auto issue_sdp = [&](uint32_t d_tmem, uint64_t a0, uint64_t b0) {
+#pragma unroll
+            for (int kk = 0; kk < DH / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+              umma_f16_ss_hot(tmem + d_tmem, sdesc_add(a0, off), sdesc_add(b0, off), id_f,
+                              kk > 0 ? 1u : 0u);
+            }
+          };
+          if (ok) ok = mbar_wait(qd_full(qst(it)), qph(it), a.status, abort_flag, a.limit_ns);
+          if (ok) {
+            tc_fence_after();
+            const uint32_t so = qst(it) * TILE_BYTES;
+            issue_sdp(TM_SQ, dK_k, sdesc_add(dQ_k, so));
+            issue_sdp(TM_DPP, dV_k, sdesc_add(dDO_k, so));
+            umma_commit(dp_full);
+          }
+          for (int j = 0; j < nq && ok; ++j) {
+            const uint32_t cur = it + j, so = qst(cur) * TILE_BYTES;
+            if (!(ok = mbar_wait(p_full, cur & 1u, a.status, abort_flag, a.limit_ns))) break;
+            tc_fence_after();
+            // dK += dS^T Q: M = 128 keys, N = 128 dh, K = 128 queries
+            const uint64_t bdo = sdesc_add(dDO_mn, so), bq = sdesc_add(dQ_mn, so);
+            const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < BR / 16; ++kk)
+              umma_f16_ss_hot(tmem + TM_DK,
+                              sdesc_add(dDS_k, (kk >> 2) * BOX_BYTES + (kk & 3) * 32),
+                              sdesc_add(bq, kk * 2048), id_kv, kk > 0 ? 1u : acc0);
+            // dQ^T(cur) = K^T dS^T: M = 128 dh, N = 128 queries, K = 128 keys
+#pragma unroll
+            for (int kk = 0; kk < BC / 16; ++kk)
+              umma_f16_ss_hot(tmem + TM_SQ, sdesc_add(dK_mn, kk * 2048), sdesc_add(dDS_mn, kk * 2048),
+                              id_q, kk > 0 ? 1u : 0u);
+            umma_commit(dq_full);
+            // dV += P^T dO (A = P^T from TMEM: queries 64g + 16m.. at column 64g + 8m)
+#pragma unroll
+            for (int kk = 0; kk < BR / 16; ++kk)
+              umma_f16_ts_hot(tmem + TM_DV, tmem + TM_DPP + 64 * (kk >> 2) + 8 * (kk & 3),
+                              sdesc_add(bdo, kk * 2048), id_kv, kk > 0 ? 1u : acc0);
+            umma_commit(qd_empty(qst(cur)));
+            if (j + 1 < nq) {
+              const uint32_t nx = cur + 1, so1 = qst(nx) * TILE_BYTES;
+              if (!(ok = mbar_wait(qd_full(qst(nx)), qph(nx), a.status, abort_flag, a.limit_ns)))
+                break;
+              tc_fence_after();
+              issue_sdp(TM_DPP, dV_k, sdesc_add(dDO_k, so1));
+              // S^T(cur+1) reuses the dQ^T columns once the drain has read them
+              if (!(ok = mbar_wait(dq_empty, cur & 1u, a.status, abort_flag, a.limit_ns))) break;
+              tc_fence_after();
+              issue_sdp(TM_SQ, dK_k, sdesc_add(dQ_k, so1));
+              umma_commit(dp_full);
+            }
+          }
+          if (ok) {
+            umma_commit(kv_done);
+          } else {
+            umma_commit(drain_bar);
+            drain_wait(drain_bar, 0, a.limit_ns);
+          }
+        }
       }
-      // dK, dV of this key tile -> fp16 rows
-      bool eok = ok && mbar_wait(kv_done, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
-      eok = __all_sync(0xffffffffu, eok);
-      if (eok) {
-        tc_fence_after();
-        ct_t* dkrow = a.dqkv + (krow0 + row) * 3 * (int64_t)a.d + a.d + h * DH;
-        const float skk = a.scale * kOperandUnscale;
-        {
-          const int part = half;   // warps 0-3 write dK, warps 4-7 write dV
-          const float mul = part == 0 ? skk : kOperandUnscale;
-          ct_t* out = dkrow + part * a.d;
+      it += (uint32_t)nq;
+      tile_sync();
+    }
+    if (warp == WARP_PROD && lane == 0 && *abort_flag) {
+      const uint32_t n_out = q_issued < (uint32_t)QSTAGES ? q_issued : (uint32_t)QSTAGES;
+      for (uint32_t jj = q_issued - n_out; jj < q_issued; ++jj)
+        drain_wait(qd_full(qst(jj)), qph(jj), a.limit_ns);
+      if (kv_issued > 0) drain_wait(kv_full, (kv_issued - 1) & 1u, a.limit_ns);
+    }
+  } else if (warp >= WARP_DRAIN) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(REG_DRAIN));
+    for (int tile = 0; tile < 2; ++tile) {
+      const int64_t k0 = k0s[tile];
+      const int nq = (int)((a.S - k0) / BR);
+      const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
+      {
+        // ------------------------------------------------------------ dQ drain (thread = dh)
+        // all 128 query columns are read before the TMEM columns are released, so
+        // S^T(cur+1) never waits for the atomics (which take ~2700 clocks a tile:
+        // 64 KB at the ~24 bytes a clock an SM gets for global reductions)
+        const int quarter = warp & 3;
+        const int dh = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const float sc = a.scale * kOperandUnscale;
+        bool ok = true;
+        for (int j = 0; j < nq; ++j) {
+          const uint32_t cur = it + j;
+          const bool okl = ok && mbar_wait(dq_full, cur & 1u, a.status, abort_flag, a.limit_ns);
+          if (!(ok = __all_sync(0xffffffffu, okl))) break;
+          tc_fence_after();
+          uint32_t v[4][32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tmem_ld32(lane_base + TM_SQ + q * 32, v[q]);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(dq_empty);   // dQ^T(cur) read: its columns may take S^T(cur+1)
+          const int64_t qrow = zz_row_of_pos(k0 + (int64_t)j * BR, a.c, a.D);
+          float* dst = a.dq_acc + qrow * a.d + h * DH + dh;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              atomicAdd(dst + (int64_t)(q * 32 + e) * a.d, __uint_as_float(v[q][e]) * sc);
+        }
+        tc_fence_before();
+      }
+      it += (uint32_t)nq;
+      tile_sync();
+    }
+  } else {
+    for (int tile = 0; tile < 2; ++tile) {
+      const int64_t k0 = k0s[tile];
+      const int nq = (int)((a.S - k0) / BR);
+      const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
+      {
+        // ------------------------------------------------------------ P, dS (thread = key)
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        uint8_t* drow = gbase + OFF_DS + half * BOX_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
+        bool ok = true;
+        for (int j = 0; j < nq; ++j) {
+          const uint32_t cur = it + j, st = qst(cur);
+          bool okl = ok && mbar_wait(dp_full, cur & 1u, a.status, abort_flag, a.limit_ns);
+          okl = okl && mbar_wait(qd_full(st), qph(cur), a.status, abort_flag, a.limit_ns);
+          if (!(ok = __all_sync(0xffffffffu, okl))) break;
+          tc_fence_after();
+          const float* L = sLD + st * 2 * BR;
+          const float* Dl = L + BR;
+          const bool diag = j == 0;   // query tile == key tile: key index > query index is masked
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            const int qb = half * 64 + ch * 32;    // this chunk's 32 query columns
+            uint32_t sv[32], dv[32];
+            tmem_ld32(lane_base + TM_SQ + qb, sv);
+            tmem_ld32(lane_base + TM_DPP + qb, dv);
+            tmem_wait_ld();
+            uint32_t pk[16], dk[16];
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+              const float4 l0 = *reinterpret_cast<const float4*>(L + qb + c8 * 8);
+              const float4 l1 = *reinterpret_cast<const float4*>(L + qb + c8 * 8 + 4);
+              const float4 d0 = *reinterpret_cast<const float4*>(Dl + qb + c8 * 8);
+              const float4 d1 = *reinterpret_cast<const float4*>(Dl + qb + c8 * 8 + 4);
+              const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+              const float dlv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+              for (int e = 0; e < 8; e += 2) {
+                float pp[2], dd[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int x = c8 * 8 + e + u;
+                  float p = ex2_approx(fmaf(__uint_as_float(sv[x]), a.scale_log2, -lv[e + u]));
+                  if (diag && row > qb + x) p = 0.f;
+                  pp[u] = p;
+                  dd[u] = p * (__uint_as_float(dv[x]) - dlv[e + u]);
+                }
+                pk[c8 * 4 + (e >> 1)] = pack_f16(pp[0], pp[1]);
+                dk[c8 * 4 + (e >> 1)] = pack_f16(dd[0], dd[1]);
+              }
+            }
+            // P^T over this thread's own dP^T columns: queries qb.. -> column half*64 + ch*16
+            tmem_st16(lane_base + TM_DPP + half * 64 + ch * 16, pk);
+            // dS^T row `row`, queries qb.. -> box `half`, 16-byte chunks 4*ch .. 4*ch+3
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int chunk = ch * 4 + c;
+              *reinterpret_cast<uint4*>(drow + ((chunk ^ (row & 7)) << 4)) =
+                  make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+            }
+          }
+          tmem_wait_st();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(p_full);
+        }
+        // dK, dV of this key tile -> fp16 rows
+        bool eok = ok && mbar_wait(kv_done, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
+        if (__all_sync(0xffffffffu, eok)) {
+          tc_fence_after();
+          ct_t* dkrow = a.dqkv + (krow0 + row) * 3 * (int64_t)a.d + a.d + h * DH;
+          const float mul = half == 0 ? a.scale * kOperandUnscale : kOperandUnscale;
+          ct_t* out = dkrow + half * a.d;     // warps 0-3 write dK, warps 4-7 write dV
 #pragma unroll 1
           for (int q = 0; q < 4; ++q) {
             uint32_t v[32];
-            tmem_ld32(lane_base + (part == 0 ? TM_DK : TM_DV) + q * 32, v);
+            tmem_ld32(lane_base + (half == 0 ? TM_DK : TM_DV) + q * 32, v);
             tmem_wait_ld();
             uint4* dst = reinterpret_cast<uint4*>(out + q * 32);
 #pragma unroll
@@ -386,46 +448,11 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
                   pack_f16(__uint_as_float(v[8 * c + 6]) * mul, __uint_as_float(v[8 * c + 7]) * mul));
           }
         }
-      }
-      tc_fence_before();
-    } else {
-      // ------------------------------------------------------------ dQ drain (thread = dh)
-      const int quarter = warp & 3;
-      const int dh = quarter * 32 + lane;
-      const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-      const float sc = a.scale * kOperandUnscale;
-      bool ok = true;
-      for (int j = 0; j < nq; ++j) {
-        const uint32_t cur = it + j;
-        bool okl = ok && mbar_wait(dq_full, cur & 1u, a.status, abort_flag, a.limit_ns);
-        ok = group_bar_and(2, 128, okl);
-        if (!ok) break;
-        uint32_t v[2][32];
-        tc_fence_after();
-        tmem_ld32(lane_base + TM_DQ, v[0]);
-        tmem_ld32(lane_base + TM_DQ + 32, v[1]);
-        tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(dq_empty);
-        const int64_t qrow = zz_row_of_pos(k0 + (int64_t)j * BR, a.c, a.D);
-        float* dst = a.dq_acc + qrow * a.d + h * DH + dh;
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            atomicAdd(dst + (int64_t)(q * 32 + e) * a.d, __uint_as_float(v[q][e]) * sc);
       }
-      tc_fence_before();
+      it += (uint32_t)nq;
+      tile_sync();
     }
-    it += (uint32_t)nq;
-    __syncthreads();   // K/V tiles, TMEM accumulators and barrier phases move on
-    tc_fence_after();
-  }
-  if (warp == WARP_PROD && lane == 0 && *abort_flag) {
-    const uint32_t n_out = q_issued < (uint32_t)QSTAGES ? q_issued : (uint32_t)QSTAGES;
-    for (uint32_t jj = q_issued - n_out; jj < q_issued; ++jj)
-      drain_wait(qd_full(qst(jj)), qph(jj), a.limit_ns);
-    if (kv_issued > 0) drain_wait(kv_full, (kv_issued - 1) & 1u, a.limit_ns);
   }
   tc_fence_before();
   __syncthreads();
@@ -436,9 +463,12 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
   }
 }
 
-// Delta[h][row] = dO[row, head h] . O[row, head h]  (warp per row and head)
+// Delta[h][row] = dO[row, head h] . O[row, head h] and
+// L2[h][row] = LSE[h][row] * log2(e) - 8 (the exponent offset of 2^8 P)
+// (warp per row and head)
 __global__ void attn_delta_kernel(const ct_t* __restrict__ o, const ct_t* __restrict__ dO,
-                                  float* __restrict__ delta, int64_t S, int H, int d) {
+                                  const float* __restrict__ lse, float* __restrict__ delta,
+                                  float* __restrict__ lse2, int64_t S, int H, int d) {
   const int lane = threadIdx.x & 31;
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < S * H; w += nw) {
@@ -449,7 +479,11 @@ __global__ void attn_delta_kernel(const ct_t* __restrict__ o, const ct_t* __rest
     float s = f16_lo(ov.x) * f16_lo(gv.x) + f16_hi(ov.x) * f16_hi(gv.x) +
               f16_lo(ov.y) * f16_lo(gv.y) + f16_hi(ov.y) * f16_hi(gv.y);
     s = warp_sum(s);
-    if (lane == 0) delta[(int64_t)h * S + row] = s;
+    if (lane == 0) {
+      delta[(int64_t)h * S + row] = s;
+      lse2[(int64_t)h * S + row] =
+          fmaf(lse[(int64_t)h * S + row], 1.4426950408889634f, -kOperandLog2Scale);
+    }
   }
 }
 
@@ -490,13 +524,13 @@ EncodeTiledFn encode_fn_bwd() {
   return fn;
 }
 
-// Row-major fp16 [rows, cols] with box {64 columns, 64 rows}, 128-byte swizzle.
+// Row-major fp16 [rows, cols] with box {64 columns, 128 rows}, 128-byte swizzle.
 bool map_2d(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows) {
   EncodeTiledFn fn = encode_fn_bwd();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
-  const cuuint32_t box[2] = {64u, 64u};
+  const cuuint32_t box[2] = {64u, 128u};
   const cuuint32_t estr[2] = {1u, 1u};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -511,14 +545,15 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
   if (dh != DH) return TSP_ERR_UNSUPPORTED;
   const int64_t c = S / (2 * D);
   if (c % BC != 0 || S > (int64_t)INT32_MAX) return TSP_ERR_UNSUPPORTED;
+  if (S % 4 != 0) return TSP_ERR_UNSUPPORTED;
   const int d = H * dh;
   if (((uintptr_t)qkv & 15u) || ((uintptr_t)dO & 15u) || ((uintptr_t)lse & 15u) ||
       ((uintptr_t)delta & 15u) || (S * 4) % 16 != 0)
     return TSP_ERR_INVALID_ARG;
   {
     Prof prof("attn_bwd_prep", st);
-    attn_delta_kernel<<<num_sms() * 8, 256, 0, st>>>((const ct_t*)o, (const ct_t*)dO, delta, S, H,
-                                                     d);
+    attn_delta_kernel<<<num_sms() * 8, 256, 0, st>>>((const ct_t*)o, (const ct_t*)dO, lse, delta,
+                                                     delta + (int64_t)H * S, S, H, d);
     TSP_CUDA_TRY(cudaGetLastError());
     TSP_CUDA_TRY(cudaMemsetAsync(dq_acc, 0, (size_t)S * d * sizeof(float), st));
   }
@@ -527,7 +562,7 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
   memset(a, 0, sizeof(TcBwdArgs));
   if (!map_2d(&a->tm_qkv, qkv, 3 * (int64_t)d, S) || !map_2d(&a->tm_do, dO, d, S))
     return TSP_ERR_CUDA;
-  a->lse = lse;
+  a->lse2 = delta + (int64_t)H * S;
   a->delta = delta;
   a->dq_acc = dq_acc;
   a->dqkv = (ct_t*)dqkv;
@@ -541,11 +576,18 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
   a->status = status_word();
   a->limit_ns = wait_limit_ns();
   static bool attr = false;
+  static int launch_regs = 0;
   if (!attr) {
     TSP_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_tc_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM));
+    cudaFuncAttributes fa;
+    TSP_CUDA_TRY(cudaFuncGetAttributes(&fa, attn_bwd_tc_kernel));
+    launch_regs = fa.numRegs;
     attr = true;
   }
+  // setmaxnreg.inc would wait forever if the split exceeded the launch allocation
+  if ((int64_t)launch_regs * NTHR < (int64_t)launch_regs * 256 + 128 * (REG_DRAIN + REG_CTRL))
+    return TSP_ERR_UNSUPPORTED;
   dim3 grid((unsigned)(D * a->n_kt), (unsigned)H);
   {
     Prof prof("attn_bwd", st);

@@ -50,7 +50,7 @@ tsp_status launch_attn_f32_bwd(const float* QKV, const float* O, const float* dO
 tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, int H, int dh,
                                 int D, cudaStream_t st);
 
-// attn_bwd.cu
+// attn_bwd.cu (delta: 2 x H x S fp32 scratch, Delta then the scaled LSE)
 tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, const float* lse,
                                 float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int dh,
                                 int D, cudaStream_t st);
