@@ -82,7 +82,17 @@ def gemm_flops(name, S, d, inter):
 # holds the SHA-256 of the kernel's source file at capture time, and the figure
 # is reported only while that source is unchanged (otherwise traffic is null).
 MEASURED_TRAFFIC = {
-    # (kernel, workload): (bytes per launch, source file, sha256 of the source)
+    # (kernel, workload): (bytes per launch, source file, sha256 of the source);
+    # first (cold) launch of the process, from the captures summarised under profiles/
+    ("gemm_w13_swiglu", "fwd16k"): (
+        1576974000 + 347252224, "folded_tensor_sequence_zigzag_gb300/csrc/gemm_tc.cu",
+        "6746a2f317f37a9b17dbeb4daeab63797c4d6d5208f6bb042b02d22c3a573bf4"),
+    ("attn_fwd", "fwd16k"): (
+        423326976 + 119269888, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
+        "cf9ba7748c5011b937e86fd91099f1f659aa90ce593c79bc15d0b984fe17529e"),
+    ("attn_bwd", "fwdbwd8k"): (
+        408379392 + 229071616, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
+        "8173d044cd43f05ef9db6dab64e8a65e29e59339a80da34bc75f7d5cf7436d9d"),
 }
 
 
@@ -431,7 +441,7 @@ def run_gpu(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         S_, D_, d_, H_, I_, kind_ = WORKLOADS[args.workload]
-        rows = args.ref_rows or (512 if kind_ == "fwdbwd" else 2048)
+        rows = args.ref_rows or (512 if kind_ == "fwdbwd" else 8192)   # ~10 s on 16 cores
         est, dt, desc = oracle_sample(S_, d_, H_, I_, D_, kind_, rows)
         line["cpu_baseline"] = {"value": S_ / est, "unit": "tokens/s", "cores": cpu_cores(),
                                 "kind": "oracle", "sample": desc, "sample_seconds": dt}
