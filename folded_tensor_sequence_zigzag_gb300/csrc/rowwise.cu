@@ -133,6 +133,50 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const Tin* __restrict_
   }
 }
 
+// Row-per-CTA variant for n % 512 == 0, n <= 16384: n/16 threads, 16 elements
+// (two 8-element units) per thread, the row sum reduced through shared memory
+// with one barrier per row (double-buffered partials).  Few registers, so many
+// CTAs share an SM and many rows are in flight: the warp-per-row kernel above
+// holds a whole row per warp in registers and runs latency-bound.
+template <typename Tin, typename Tg, typename T>
+__global__ void __launch_bounds__(1024) rmsnorm_fwd_cta_kernel(const Tin* __restrict__ u,
+                                                               const Tg* __restrict__ g,
+                                                               T* __restrict__ out,
+                                                               float* __restrict__ rstd_out,
+                                                               int64_t rows, int n, float eps) {
+  __shared__ float part[2][32];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nw = blockDim.x >> 5;
+  const int c0 = t * 8, c1 = (t + blockDim.x) * 8;   // this thread's two units
+  float gf0[8], gf1[8];
+  load8(g + c0, gf0);
+  load8(g + c1, gf1);
+  int it = 0;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, ++it) {
+    const Tin* src = u + row * n;
+    float v0[8], v1[8];
+    load8(src + c0, v0);
+    load8(src + c1, v1);
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(v0[e], v0[e], fmaf(v1[e], v1[e], ss));
+    ss = warp_sum(ss);
+    if (lane == 0) part[it & 1][warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < nw; ++w) tot += part[it & 1][w];
+    const float r = rsqrtf(tot / (float)n + eps);
+    if (t == 0 && rstd_out) rstd_out[row] = r;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      v0[e] = v0[e] * r * gf0[e];
+      v1[e] = v1[e] * r * gf1[e];
+    }
+    T* dst = out + row * n;
+    store8(dst + c0, v0);
+    store8(dst + c1, v1);
+  }
+}
+
 // Scalar fallback for rows whose length is not a multiple of 8 (or unaligned).
 template <typename Tin, typename Tg, typename T>
 __global__ void rmsnorm_fwd_scalar_kernel(const Tin* __restrict__ u, const Tg* __restrict__ g,
@@ -164,7 +208,12 @@ static tsp_status rmsnorm_fwd_t(const Tin* u, const Tg* g, T* out, float* rstd, 
                       ((uintptr_t)out % 16 == 0);
   const int nu = n / 8;
   Prof prof("rmsnorm_fwd", st);
-  if (vec_ok && nu <= 32)
+  if (vec_ok && n % 512 == 0 && n <= 16384) {
+    const int threads = n / 16;
+    const int per_sm = std::max(1, 2048 / threads);
+    const int grid2 = (int)std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)num_sms() * per_sm));
+    rmsnorm_fwd_cta_kernel<Tin, Tg, T><<<grid2, threads, 0, st>>>(u, g, out, rstd, rows, n, eps);
+  } else if (vec_ok && nu <= 32)
     rmsnorm_fwd_kernel<Tin, Tg, T, 1><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
   else if (vec_ok && nu <= 128)
     rmsnorm_fwd_kernel<Tin, Tg, T, 4><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
