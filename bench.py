@@ -319,21 +319,22 @@ def run_gpu(args):
         dyz = torch.empty_like(dy)
         y = torch.empty(x.shape, dtype=torch.float32, device=dev)  # dx (fp32) in global order
 
-    def step(xin):
+    def step(xin, yout=None):
+        yout = y if yout is None else yout
         tsp.zigzag_permute(xin, D, out=xz)
         if kind == "fwd":
             tsp.block_fwd(cfg, xz, W, out=yz, ws=ws)
-            tsp.zigzag_permute(yz, D, inverse=True, out=y)
-            return y
+            tsp.zigzag_permute(yz, D, inverse=True, out=yout)
+            return yout
         if kind == "mlp":
             tsp.gated_mlp_fwd(cfg, xz, W, norm=False, residual=False, out=yz, ws=ws)
-            tsp.zigzag_permute(yz, D, inverse=True, out=y)
-            return y
+            tsp.zigzag_permute(yz, D, inverse=True, out=yout)
+            return yout
         tsp.block_fwd(cfg, xz, W, saved=saved, out=yz)
         tsp.zigzag_permute(dy, D, out=dyz)
         g = tsp.block_bwd(cfg, xz, dyz, saved, W, ws=wsb)
-        tsp.zigzag_permute(g["dx"], D, inverse=True, out=y)
-        return y
+        tsp.zigzag_permute(g["dx"], D, inverse=True, out=yout)
+        return yout
 
     # ---- warm-up
     for _ in range(max(args.warmup, 0)):
@@ -368,18 +369,41 @@ def run_gpu(args):
     t_dev = ev0.elapsed_time(ev1) / 1e3 / args.steps
     t_dev = reduce_max(t_dev, world, dev if world > 1 else None)
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: every step
+    # uploads its input from pinned host memory and reads its result back.
+    # Uploads and read-backs run on streams of their own with double-buffered
+    # device copies, so step i+1's upload and step i-1's read-back overlap step
+    # i's compute; the timed region runs from the first upload to the last
+    # read-back.
     x_host = inp["x"].pin_memory()
-    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-    x_dev = torch.empty_like(x)
+    y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    y_dev = [torch.empty_like(y) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    h2d_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    d2h_done = [torch.cuda.Event() for _ in range(2)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for _ in range(args.steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        out = step(x_dev)
-        y_host.copy_(out, non_blocking=True)
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(args.steps):
+        p = i & 1
+        if i >= 2:
+            s_in.wait_event(comp_done[p])      # x_dev[p] no longer read
+        with torch.cuda.stream(s_in):
+            x_dev[p].copy_(x_host, non_blocking=True)
+        h2d_done[p].record(s_in)
+        stream.wait_event(h2d_done[p])
+        if i >= 2:
+            stream.wait_event(d2h_done[p])     # y_dev[p] read back
+        with torch.cuda.stream(stream):
+            step(x_dev[p], y_dev[p])
+        comp_done[p].record(stream)
+        s_out.wait_event(comp_done[p])
+        with torch.cuda.stream(s_out):
+            y_host[p].copy_(y_dev[p], non_blocking=True)
+        d2h_done[p].record(s_out)
+    e1.record(s_out)
     torch.cuda.synchronize(dev)
     t_e2e = e0.elapsed_time(e1) / 1e3 / args.steps
     t_e2e = reduce_max(t_e2e, world, dev if world > 1 else None)

@@ -250,19 +250,28 @@ WCache wcache_layout(const tsp_cfg* c, int which, uint8_t* base) {
 tsp_status fill_wcache(const tsp_cfg* c, const WCache& W, const tsp_attn_w* aw, const tsp_mlp_w* mw,
                        cudaStream_t st) {
   const int64_t dd = (int64_t)c->d * c->d, Id = (int64_t)c->inter * c->d;
-  tsp_status r;
+  const void* src[kMaxConvert];
+  void* dst[kMaxConvert];
+  int64_t n[kMaxConvert];
+  int k = 0;
+  auto add = [&](const void* s_, void* d_, int64_t n_) {
+    src[k] = s_;
+    dst[k] = d_;
+    n[k] = n_;
+    ++k;
+  };
   if (W.wq) {
-    if ((r = launch_convert_bf16_f16(aw->wq, W.wq, dd, st)) != TSP_OK) return r;
-    if ((r = launch_convert_bf16_f16(aw->wk, W.wk, dd, st)) != TSP_OK) return r;
-    if ((r = launch_convert_bf16_f16(aw->wv, W.wv, dd, st)) != TSP_OK) return r;
-    if ((r = launch_convert_bf16_f16(aw->wo, W.wo, dd, st)) != TSP_OK) return r;
+    add(aw->wq, W.wq, dd);
+    add(aw->wk, W.wk, dd);
+    add(aw->wv, W.wv, dd);
+    add(aw->wo, W.wo, dd);
   }
   if (W.w1) {
-    if ((r = launch_convert_bf16_f16(mw->w1, W.w1, Id, st)) != TSP_OK) return r;
-    if ((r = launch_convert_bf16_f16(mw->w3, W.w3, Id, st)) != TSP_OK) return r;
-    if ((r = launch_convert_bf16_f16(mw->w2, W.w2, Id, st)) != TSP_OK) return r;
+    add(mw->w1, W.w1, Id);
+    add(mw->w3, W.w3, Id);
+    add(mw->w2, W.w2, Id);
   }
-  return TSP_OK;
+  return k == 0 ? TSP_OK : launch_convert_bf16_f16_many(src, dst, n, k, st);
 }
 
 cudaStream_t S_(void* s) { return reinterpret_cast<cudaStream_t>(s); }

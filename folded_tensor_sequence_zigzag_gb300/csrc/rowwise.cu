@@ -6,6 +6,8 @@
 // attention).  Rank r owns chunks r and 2D-1-r of the 2D equal chunks.
 // RMSNorm: the pages give no formula; the plain reading of a pre-norm block,
 // rms(u; g) = u / sqrt(mean(u^2) + eps) * g with fp32 arithmetic.
+#include <cstring>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -494,6 +496,52 @@ tsp_status launch_convert_bf16_f16(const void* src, void* dst, int64_t n, cudaSt
   const int64_t n8 = n / 8;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((n8 + 255) / 256, (int64_t)num_sms() * 8));
   convert_bf16_f16_kernel<<<grid, 256, 0, st>>>((const uint4*)src, (uint4*)dst, n8);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+// Several bf16 -> fp16 conversions in one launch: the buffers are laid end to
+// end in one index space of 8-element units; a thread walks its grid-stride
+// indices upward, so its buffer index only moves forward.
+struct ConvertList {
+  const uint4* src[kMaxConvert];
+  uint4* dst[kMaxConvert];
+  int64_t end8[kMaxConvert];   // exclusive prefix ends, in 8-element units
+  int count;
+};
+
+__global__ void convert_bf16_f16_many_kernel(const __grid_constant__ ConvertList L) {
+  const int64_t total = L.end8[L.count - 1];
+  int seg = 0;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    while (t >= L.end8[seg]) ++seg;
+    const int64_t i = t - (seg > 0 ? L.end8[seg - 1] : 0);
+    const uint4 v = L.src[seg][i];
+    L.dst[seg][i] = make_uint4(pack_f16(bf16_lo(v.x), bf16_hi(v.x)), pack_f16(bf16_lo(v.y), bf16_hi(v.y)),
+                               pack_f16(bf16_lo(v.z), bf16_hi(v.z)), pack_f16(bf16_lo(v.w), bf16_hi(v.w)));
+  }
+}
+
+tsp_status launch_convert_bf16_f16_many(const void* const* src, void* const* dst, const int64_t* n,
+                                        int count, cudaStream_t st) {
+  if (count < 1 || count > kMaxConvert) return TSP_ERR_INVALID_ARG;
+  ConvertList L;
+  memset(&L, 0, sizeof(L));
+  int64_t acc = 0;
+  for (int k = 0; k < count; ++k) {
+    if (n[k] % 8 != 0 || ((uintptr_t)src[k] & 15u) || ((uintptr_t)dst[k] & 15u))
+      return TSP_ERR_UNSUPPORTED;
+    L.src[k] = (const uint4*)src[k];
+    L.dst[k] = (uint4*)dst[k];
+    acc += n[k] / 8;
+    L.end8[k] = acc;
+  }
+  L.count = count;
+  if (acc == 0) return TSP_OK;
+  Prof prof("convert_bf16_f16", st);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((acc + 255) / 256, (int64_t)num_sms() * 8));
+  convert_bf16_f16_many_kernel<<<grid, 256, 0, st>>>(L);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }
