@@ -12,7 +12,8 @@ residual, un-permute y.  The step's working set (x 128 MiB, weights 405 MiB,
 activations > 1 GiB) is larger than L2, so no explicit flush is needed.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload fwd16k|fwd128k|fwdbwd32k|fwdbwd8k|mlp16k]
+                    [--workload fwd16k|fwd128k|fwdbwd32k|fwdbwd8k|mlp16k|
+                                fwd512k|fwd1m|fwdbwd512k]
 
 With N > 1 (torchrun, one rank per GPU) every rank runs its own replica
 ("replicas only": the block has no data-path exchange on one node's GPUs in
@@ -42,6 +43,11 @@ WORKLOADS = {
     "fwd128k": (131072, 8, 4096, 32, 11008, "fwd"),
     "fwdbwd32k": (32768, 8, 4096, 32, 11008, "fwdbwd"),
     "fwdbwd8k": (8192, 8, 4096, 32, 11008, "fwdbwd"),   # small case for profiler captures
+    # long context on one GPU without sequence tiling: the forward fits up to
+    # ~1M tokens (92 GB of workspace), the training step up to 512K (179 GB)
+    "fwd512k": (524288, 8, 4096, 32, 11008, "fwd"),
+    "fwd1m": (1048576, 8, 4096, 32, 11008, "fwd"),
+    "fwdbwd512k": (524288, 8, 4096, 32, 11008, "fwdbwd"),
     "mlp16k": (16384, 4, 4096, 32, 11008, "mlp"),
 }
 DEFAULT_WORKLOAD = "fwd16k"

@@ -192,7 +192,7 @@ def test_mlp_only_4096_11008_D4(S):
     assert_bf16_close(y[rows], ref, f"MLP-only S={S}")
 
 
-@pytest.mark.parametrize("S", [16384, 131072])
+@pytest.mark.parametrize("S", [16384, 131072, 262144])
 def test_7b_block_fwd_sampled_rows(S):
     shape = BlockShape(S=S, d=4096, H=32, inter=11008, D=8)
     inp = make_block_inputs(shape, torch.bfloat16, seed=0)
@@ -268,6 +268,21 @@ def test_7b_fwd_bwd_S8192_all_outputs():
     ref = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
     for k, v in ref.items():
         assert_bf16_close(g[k], v, f"{k} (S=8192)")
+
+
+def test_long_context_training_step_S262144_tail():
+    """Beyond 131K tokens on one GPU with no sequence tiling: the training step
+    at S=262144 (D=8, 7B shapes); dx at the last 256 positions is exact in the
+    oracle, every gradient finite."""
+    S, D = 262144, 8
+    shape = BlockShape(S=S, d=4096, H=32, inter=11008, D=D)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=1, with_dy=True)
+    _, g = _run_bwd(shape, inp, torch.bfloat16)
+    n_tail = 256
+    dx_ref = O.block_bwd_tail(inp["x"], inp, inp["dy"], shape.H, shape.eps, n_tail)
+    assert_bf16_close(g["dx"][S - n_tail:], dx_ref, "dx (S=262144, last 256 positions)")
+    for k in ("dwq", "dwk", "dwv", "dwo", "dw1", "dw3", "dw2", "dg_attn", "dg_mlp"):
+        assert torch.isfinite(g[k]).all(), k
 
 
 def test_7b_fwd_bwd_S32768_sampled():
