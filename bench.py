@@ -13,7 +13,7 @@ activations > 1 GiB) is larger than L2, so no explicit flush is needed.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                     [--workload fwd16k|fwd128k|fwdbwd32k|fwdbwd8k|mlp16k|
-                                fwd512k|fwd1m|fwdbwd512k]
+                                fwd512k|fwd1m|fwdbwd512k|stack32_16k|stack32train_16k]
 
 With N > 1 (torchrun, one rank per GPU) every rank runs its own replica
 ("replicas only": the block has no data-path exchange on one node's GPUs in
@@ -49,7 +49,11 @@ WORKLOADS = {
     "fwd1m": (1048576, 8, 4096, 32, 11008, "fwd"),
     "fwdbwd512k": (524288, 8, 4096, 32, 11008, "fwdbwd"),
     "mlp16k": (16384, 4, 4096, 32, 11008, "mlp"),
+    # 32-layer stacks of the 7B-shaped block (each layer its own weights)
+    "stack32_16k": (16384, 8, 4096, 32, 11008, "fwd"),
+    "stack32train_16k": (16384, 8, 4096, 32, 11008, "fwdbwd"),
 }
+LAYERS = {"stack32_16k": 32, "stack32train_16k": 32}   # other workloads: one block
 DEFAULT_WORKLOAD = "fwd16k"
 
 
@@ -243,6 +247,7 @@ def run_reference(args):
             dist.destroy_process_group()
             return
     S, D, d, H, inter, kind = WORKLOADS[args.workload]
+    L = LAYERS.get(args.workload, 1)
     rows = args.ref_rows or (256 if kind == "fwdbwd" else 512)
     for _ in range(args.warmup):
         oracle_sample(S, d, H, inter, D, kind, rows)
@@ -250,7 +255,9 @@ def run_reference(args):
     desc = ""
     for _ in range(args.steps):
         est, _, desc = oracle_sample(S, d, H, inter, D, kind, rows)
-        times.append(est)
+        times.append(est * L)
+    if L > 1:
+        desc += f", x{L} layers"
     t = statistics.median(times)
     value = S / t
     line = {
@@ -274,6 +281,9 @@ def workload_config(name):
     S, D, d, H, inter, kind = WORKLOADS[name]
     desc = {"fwd": "7B-shaped TSP block forward", "fwdbwd": "7B-shaped TSP block forward+backward",
             "mlp": "sharded SwiGLU MLP only (no norm, no residual)"}[kind]
+    L = LAYERS.get(name, 1)
+    if L > 1:
+        desc = f"{L}-layer stack of the {desc}"
     return {"workload": f"{desc}, S={S}, D={D} zigzag virtual ranks, d_model={d}, "
                         f"{H} heads x {d // H}, SwiGLU inter={inter}, causal",
             "S": S, "D": D, "d_model": d, "heads": H, "inter": inter, "global_batch": 1,
@@ -308,13 +318,36 @@ def run_gpu(args):
     if kind == "mlp":
         inp.update({k: torch.zeros(1, dtype=torch.bfloat16) for k in ("wq", "wk", "wv", "wo")})
     W = tsp.BlockWeights.from_dict(inp, dev)
+    L = LAYERS.get(args.workload, 1)
+    Ws = [W]
+    gen = torch.Generator(device=dev).manual_seed(1000 + rank)
+    for _ in range(1, L):   # further layers drawn on the device, same distributions
+        def rnd(*shp):
+            return (torch.randn(*shp, generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+        Ws.append(tsp.BlockWeights(rnd(d, d), rnd(d, d), rnd(d, d), rnd(d, d), rnd(inter, d),
+                                   rnd(inter, d), rnd(d, inter),
+                                   torch.ones(d, dtype=torch.bfloat16, device=dev),
+                                   torch.ones(d, dtype=torch.bfloat16, device=dev)))
     x = inp["x"].to(dev)
     xz = torch.empty_like(x)
     yz = torch.empty_like(x)
     y = torch.empty_like(x)
     stream = torch.cuda.current_stream(dev)
     saved = ws = wsb = dy = dyz = None
-    if kind == "fwd":
+    if L > 1:
+        if kind == "fwd":
+            ws = torch.empty(tsp.stack_workspace_bytes(cfg, L, tsp.TSP_OP_BLOCK_FWD),
+                             dtype=torch.uint8, device=dev)
+        else:
+            saved = torch.empty(tsp.stack_saved_bytes(cfg, L), dtype=torch.uint8, device=dev)
+            ws = torch.empty(tsp.stack_workspace_bytes(cfg, L, tsp.TSP_OP_BLOCK_FWD),
+                             dtype=torch.uint8, device=dev)
+            wsb = torch.empty(tsp.stack_workspace_bytes(cfg, L, tsp.TSP_OP_BLOCK_BWD),
+                              dtype=torch.uint8, device=dev)
+            dy = inp["dy"].to(dev)
+            dyz = torch.empty_like(dy)
+            y = torch.empty(x.shape, dtype=torch.float32, device=dev)
+    elif kind == "fwd":
         ws = torch.empty(tsp.workspace_bytes(cfg, tsp.TSP_OP_BLOCK_FWD), dtype=torch.uint8, device=dev)
     elif kind == "mlp":
         ws = torch.empty(tsp.workspace_bytes(cfg, tsp.TSP_OP_MLP_FWD), dtype=torch.uint8, device=dev)
@@ -328,6 +361,16 @@ def run_gpu(args):
     def step(xin, yout=None):
         yout = y if yout is None else yout
         tsp.zigzag_permute(xin, D, out=xz)
+        if L > 1 and kind == "fwd":
+            tsp.stack_fwd(cfg, xz, Ws, out=yz, ws=ws)
+            tsp.zigzag_permute(yz, D, inverse=True, out=yout)
+            return yout
+        if L > 1:
+            tsp.stack_fwd(cfg, xz, Ws, saved=saved, out=yz, ws=ws)
+            tsp.zigzag_permute(dy, D, out=dyz)
+            dx, _ = tsp.stack_bwd(cfg, dyz, saved, Ws, ws=wsb)
+            tsp.zigzag_permute(dx, D, inverse=True, out=yout)
+            return yout
         if kind == "fwd":
             tsp.block_fwd(cfg, xz, W, out=yz, ws=ws)
             tsp.zigzag_permute(yz, D, inverse=True, out=yout)
@@ -448,7 +491,7 @@ def run_gpu(args):
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                 "frac": ach / peak, "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)",
                 "traffic": measured_traffic(dom, args.workload)}
-    flops = block_flops(S, d, inter, kind)
+    flops = block_flops(S, d, inter, kind) * L
     value = world * S / t_dev
     tflops = world * flops / t_dev / 1e12
     line = {
@@ -468,11 +511,22 @@ def run_gpu(args):
         "kernels": per_kernel,
         "roofline": roof,
         "clocks": clk,
+        "memory": {
+            "layers": L, "device_peak_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
+            # bytes one rank would hold for this many layers (the fold against the
+            # layouts the pages compare), from the kernels' own buffer plan
+            "per_rank_gb": {nm: tsp.rank_memory(cfg, L, kind == "fwdbwd", sch)["total"] / 1e9
+                            for nm, sch in (("tsp", tsp.TSP_MEM_TSP), ("dp", tsp.TSP_MEM_DP),
+                                            ("tp", tsp.TSP_MEM_TP), ("sp", tsp.TSP_MEM_SP),
+                                            ("tp_sp_on_D2_devices", tsp.TSP_MEM_TP_SP))}},
     }
     if rank == 0 and not args.no_cpu_baseline:
         S_, D_, d_, H_, I_, kind_ = WORKLOADS[args.workload]
         rows = args.ref_rows or (512 if kind_ == "fwdbwd" else 8192)   # ~10 s on 16 cores
         est, dt, desc = oracle_sample(S_, d_, H_, I_, D_, kind_, rows)
+        if L > 1:
+            est *= L
+            desc += f", x{L} layers"
         line["cpu_baseline"] = {"value": S_ / est, "unit": "tokens/s", "cores": cpu_cores(),
                                 "kind": "oracle", "sample": desc, "sample_seconds": dt}
     if rank == 0:

@@ -30,6 +30,7 @@ tsp_status launch_rmsnorm_bwd(const float* dout, const void* u, int u_ty, const 
                               float* out_f32, void* out_t, int out_ty, float* dg, float* dg_part,
                               int64_t rows, int n, int dtype, cudaStream_t st);
 tsp_status launch_convert_bf16_f16(const void* src, void* dst, int64_t n, cudaStream_t st);
+tsp_status launch_convert_f32_bf16(const float* src, void* dst, int64_t n, cudaStream_t st);
 // up to kMaxConvert conversions (n[k] elements each, multiples of 8) in one launch
 constexpr int kMaxConvert = 8;
 tsp_status launch_convert_bf16_f16_many(const void* const* src, void* const* dst, const int64_t* n,

@@ -546,6 +546,27 @@ tsp_status launch_convert_bf16_f16_many(const void* const* src, void* const* dst
   return TSP_OK;
 }
 
+// fp32 -> bf16 (round to nearest), 8 elements per thread-iteration
+__global__ void convert_f32_bf16_kernel(const float4* __restrict__ src, uint4* __restrict__ dst,
+                                        int64_t n8) {
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n8;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const float4 a = src[2 * t], b = src[2 * t + 1];
+    dst[t] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
+                        pack_bf16(b.z, b.w));
+  }
+}
+
+tsp_status launch_convert_f32_bf16(const float* src, void* dst, int64_t n, cudaStream_t st) {
+  if (n % 8 != 0 || ((uintptr_t)src & 15u) || ((uintptr_t)dst & 15u)) return TSP_ERR_UNSUPPORTED;
+  Prof prof("convert_f32_bf16", st);
+  const int64_t n8 = n / 8;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((n8 + 255) / 256, (int64_t)num_sms() * 8));
+  convert_f32_bf16_kernel<<<grid, 256, 0, st>>>((const float4*)src, (uint4*)dst, n8);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Elementwise helpers of the exact-fp32 path.
 // ---------------------------------------------------------------------------

@@ -23,7 +23,8 @@ EXPORTED = ("tsp_zigzag_permute", "tsp_rmsnorm_fwd", "tsp_workspace_bytes", "tsp
             "tsp_attn_block_fwd", "tsp_gated_mlp_fwd", "tsp_block_fwd", "tsp_block_bwd",
             "tsp_pack_attn_shards", "tsp_device_status", "tsp_strerror", "tsp_num_sms",
             "tsp_profile_enable", "tsp_profile_report", "tsp_launch_count",
-            "tsp_gated_mlp_fwd_noalloc")
+            "tsp_gated_mlp_fwd_noalloc", "tsp_stack_saved_bytes", "tsp_stack_workspace_bytes",
+            "tsp_stack_fwd", "tsp_stack_bwd", "tsp_rank_memory")
 
 
 class TspError(RuntimeError):
@@ -78,6 +79,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "tsp_profile_report": (i32, [ctypes.c_char_p, i64]),
         "tsp_launch_count": (i64, []),
         "tsp_gated_mlp_fwd_noalloc": (i32, [P(Cfg), vp, P(MlpW), vp, vp]),
+        "tsp_stack_saved_bytes": (sz, [P(Cfg), i32]),
+        "tsp_stack_workspace_bytes": (sz, [P(Cfg), i32, i32]),
+        "tsp_stack_fwd": (i32, [P(Cfg), i32, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "tsp_stack_bwd": (i32, [P(Cfg), i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "tsp_rank_memory": (i32, [P(Cfg), i32, i32, i32, P(RankMem)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -112,6 +118,15 @@ def _require_cuda(*ts):
     for t in ts:
         if t is not None and not t.is_cuda:
             raise ValueError("tensors must live on the GPU")
+
+
+class RankMem(ctypes.Structure):
+    _fields_ = [("weights", ctypes.c_double), ("activations", ctypes.c_double),
+                ("transient", ctypes.c_double), ("total", ctypes.c_double),
+                ("devices", ctypes.c_double)]
+
+
+TSP_MEM_TSP, TSP_MEM_DP, TSP_MEM_TP, TSP_MEM_SP, TSP_MEM_TP_SP = range(5)
 
 
 @dataclass
@@ -237,6 +252,63 @@ def block_bwd(cfg: Cfg, x_z, dy_z, saved, W: BlockWeights, ws=None, stream=None)
                                 *[_ptr(g[k]) for k in GRAD_NAMES], _ptr(ws), ws.numel(),
                                 _stream(stream)), "tsp_block_bwd")
     return g
+
+
+def stack_saved_bytes(cfg: Cfg, L: int) -> int:
+    return int(load().tsp_stack_saved_bytes(ctypes.byref(cfg), int(L)))
+
+
+def stack_workspace_bytes(cfg: Cfg, L: int, op: int) -> int:
+    return int(load().tsp_stack_workspace_bytes(ctypes.byref(cfg), int(L), op))
+
+
+def _weight_arrays(Ws):
+    L = len(Ws)
+    aws = (AttnW * L)(*[W.attn() for W in Ws])
+    mws = (MlpW * L)(*[W.mlp() for W in Ws])
+    return aws, mws
+
+
+def stack_fwd(cfg: Cfg, x_z, Ws, saved=None, out=None, ws=None, stream=None):
+    """y_z of the L-block stack with weights Ws[0..L-1].  ``saved`` (uint8,
+    stack_saved_bytes(cfg, L)) keeps every layer's input and activations."""
+    _require_cuda(x_z)
+    L = len(Ws)
+    out = torch.empty_like(x_z) if out is None else out
+    if ws is None:
+        ws = _ws(stack_workspace_bytes(cfg, L, TSP_OP_BLOCK_FWD), x_z.device)
+    aws, mws = _weight_arrays(Ws)
+    _check(load().tsp_stack_fwd(ctypes.byref(cfg), L, _ptr(x_z), aws, mws, _ptr(out), _ptr(saved),
+                                _ptr(ws), ws.numel(), _stream(stream)), "tsp_stack_fwd")
+    return out
+
+
+def stack_bwd(cfg: Cfg, dy_z, saved, Ws, ws=None, stream=None):
+    """Gradients of sum(dy * y) through the stack: (dx_z fp32, [grads of layer l])."""
+    _require_cuda(dy_z, saved)
+    dev = dy_z.device
+    L = len(Ws)
+    d, I = cfg.d, cfg.inter
+    shapes = {"dwq": (d, d), "dwk": (d, d), "dwv": (d, d), "dwo": (d, d), "dw1": (I, d),
+              "dw3": (I, d), "dw2": (d, I), "dg_attn": (d,), "dg_mlp": (d,)}
+    grads = [{k: torch.empty(shapes[k], dtype=torch.float32, device=dev) for k in GRAD_NAMES}
+             for _ in range(L)]
+    ptrs = (ctypes.c_void_p * (9 * L))(*[g[k].data_ptr() for g in grads for k in GRAD_NAMES])
+    dx = torch.empty(dy_z.shape, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = _ws(stack_workspace_bytes(cfg, L, TSP_OP_BLOCK_BWD), dev)
+    aws, mws = _weight_arrays(Ws)
+    _check(load().tsp_stack_bwd(ctypes.byref(cfg), L, _ptr(dy_z), _ptr(saved), aws, mws, _ptr(dx),
+                                ptrs, _ptr(ws), ws.numel(), _stream(stream)), "tsp_stack_bwd")
+    return dx, grads
+
+
+def rank_memory(cfg: Cfg, L: int, training: bool, scheme: int) -> dict:
+    """Bytes one rank holds for an L-layer stack under a parallel scheme (host only)."""
+    m = RankMem()
+    _check(load().tsp_rank_memory(ctypes.byref(cfg), int(L), 1 if training else 0, int(scheme),
+                                  ctypes.byref(m)), "tsp_rank_memory")
+    return {k: getattr(m, k) for k, _ in RankMem._fields_}
 
 
 def pack_attn_shards(cfg: Cfg, W: BlockWeights, stream=None):

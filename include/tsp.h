@@ -197,6 +197,55 @@ tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z,
                          float* dw1, float* dw3, float* dw2, float* dg_attn, float* dg_mlp,
                          void* ws, size_t ws_bytes, void* stream);
 
+/* ---- Stack of L blocks (the multi-layer model the fold is applied to) ----
+ * y = B_{L-1}(... B_0(x)), B_l = the block above with weights aw[l], mw[l];
+ * every layer runs tsp_block_fwd / tsp_block_bwd, so the kernels are the
+ * block's.  aw, mw: host arrays of L weight sets (each as for tsp_block_fwd).
+ *
+ * tsp_stack_saved_bytes: training record of L layers (each layer's input
+ *   plus its block's saved activations); 0 if cfg is invalid or L < 1.
+ * tsp_stack_workspace_bytes: op = TSP_OP_BLOCK_FWD (forward, with or without
+ *   the training record) or TSP_OP_BLOCK_BWD; 0 if invalid.
+ * tsp_stack_fwd: x_z, y_z [S, d] zigzag (cfg dtype); saved = NULL for
+ *   inference or tsp_stack_saved_bytes(cfg, L) bytes for training.
+ * tsp_stack_bwd: backward of L = sum(dy * y) through the stack.  dy_z [S, d]
+ *   (cfg dtype), saved as filled by tsp_stack_fwd, dx_z [S, d] fp32 out.
+ *   grads: host array of 9*L fp32 device pointers, layer l at 9*l in the
+ *   order dwq, dwk, dwv, dwo, dw1, dw3, dw2, dg_attn, dg_mlp (each sized as
+ *   for tsp_block_bwd, overwritten).  The gradient between layers is passed
+ *   in the cfg dtype (bf16 for bf16 configurations), as the block's dy is.
+ * Errors: TSP_ERR_INVALID_ARG for L < 1, NULL or misaligned pointers or a
+ *   short workspace; otherwise as for the block calls, stopping at the first
+ *   failing layer. */
+size_t tsp_stack_saved_bytes(const tsp_cfg* cfg, int32_t L);
+size_t tsp_stack_workspace_bytes(const tsp_cfg* cfg, int32_t L, int32_t op);
+tsp_status tsp_stack_fwd(const tsp_cfg* cfg, int32_t L, const void* x_z, const tsp_attn_w* aw,
+                         const tsp_mlp_w* mw, void* y_z, void* saved, void* ws,
+                         size_t ws_bytes, void* stream);
+tsp_status tsp_stack_bwd(const tsp_cfg* cfg, int32_t L, const void* dy_z, const void* saved,
+                         const tsp_attn_w* aw, const tsp_mlp_w* mw, float* dx_z,
+                         float* const* grads, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- Per-rank memory account (sections 1-3: the fold cuts both weight and
+ * activation memory per rank by D; TP cuts only weights, SP only
+ * activations, TP+SP both but on D^2 devices, DP neither).  Bytes one rank
+ * holds for an L-layer stack of cfg's block at cfg->S tokens and degree
+ * cfg->D:
+ *   weights      L layers' parameters (cfg dtype) times the scheme's share;
+ *   activations  training: L x (block saved buffer + layer input), i.e. the
+ *                tsp_stack_saved_bytes record, times the scheme's token
+ *                share; inference: one layer's forward workspace;
+ *   transient    TSP only: the larger of one broadcast attention shard plus
+ *                the gathered K and V of all S tokens, and one MLP ring shard;
+ *   devices      devices the scheme occupies (D, or D*D for TP+SP).
+ * Shares come from the same buffer plan the kernels use.  Host-only; no GPU. */
+enum { TSP_MEM_TSP = 0, TSP_MEM_DP = 1, TSP_MEM_TP = 2, TSP_MEM_SP = 3, TSP_MEM_TP_SP = 4 };
+typedef struct {
+  double weights, activations, transient, total, devices;
+} tsp_rank_mem;
+tsp_status tsp_rank_memory(const tsp_cfg* cfg, int32_t L, int32_t training, int32_t scheme,
+                           tsp_rank_mem* out);
+
 /* Packed shard layout, what one broadcast step of the attention schedule
  * carries ("packed W_Q, W_K, W_V, W_O"): for shard k (columns C_k of width
  * d/D, boundaries floor(k*d/D)) writes [W_Q[C_k,:]; W_K[C_k,:]; W_V[C_k,:];

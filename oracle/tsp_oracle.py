@@ -35,9 +35,14 @@ design notes of the repository.
   R8  Backward: the exact gradient of the forward above; weight gradients of
       the virtual ranks are summed (what TSP's reduction to shard owners
       delivers).
+  R11 Stack of L layers: plain composition, each layer its own weights; a
+      stack whose activations live in bf16 hands each layer's output (and, in
+      the backward, each layer's input gradient) to the next layer rounded to
+      bf16.
 
 Every floating-point step runs in numpy float64; inputs are converted
-exactly from their bf16/fp32 storage.  No step here rounds to bf16.
+exactly from their bf16/fp32 storage.  No step here rounds to bf16, except
+the stack's explicit bf16 storage between layers (R11, ``store="bf16"``).
 
 Parity pins: every function below is pinned by tests under tests/ against
 closed forms, invariants, brute force and an independent library
@@ -48,6 +53,7 @@ from __future__ import annotations
 import math
 
 import numpy as np
+import torch
 
 # ----------------------------------------------------------------------------
 # Zigzag causal partitioning  [TSP 2, attention bullet: zigzag partitioning]
@@ -406,6 +412,50 @@ def causal_attention_bwd(Q, K, V, O, dO, H, q_pos=None, k_pos=None, row_block=51
             dQ[r0:r1, cols] = (dS @ K[:kmax, cols]) * scale
             dK[:kmax, cols] += (dS.T @ Q[r0:r1, cols]) * scale
     return dQ, dK, dV
+
+
+def _store(v, store):
+    """A value the way the stack stores it between layers: unchanged (None)
+    or rounded to bfloat16 ("bf16", the storage dtype of the bf16 API)."""
+    if store is None:
+        return v
+    if store == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(v)).to(torch.bfloat16).to(torch.float64).numpy()
+    raise ValueError(store)
+
+
+def stack_fwd(x, Ws, H, eps, store=None):
+    """y of an L-layer stack: the blocks applied in order, each with its own
+    weights Ws[l] ([TSP] sections 1-3: the fold is applied to every layer of
+    the model; the stack is plain composition).  ``store="bf16"`` rounds each
+    layer's output to bfloat16 before the next layer reads it, as a stack
+    whose activations are stored in bf16 does (reading R11)."""
+    y = f64(x)
+    for l, W in enumerate(Ws):
+        y, _ = block_fwd(y, W, H, eps)
+        if l + 1 < len(Ws):
+            y = _store(y, store)
+    return y
+
+
+def stack_bwd(x, Ws, dy, H, eps, store=None):
+    """dx and per-layer gradients of L = sum(dy * y), y = stack_fwd(x): the
+    chain rule through the layers, the dx of layer l being the dy of layer
+    l - 1 (rounded to bfloat16 with ``store="bf16"``, like the forward's
+    layer outputs).  Returns (dx, [dict of layer l's weight and gain
+    gradients])."""
+    xs = [f64(x)]
+    for W in Ws[:-1]:
+        xs.append(_store(block_fwd(xs[-1], W, H, eps)[0], store))
+    g = f64(dy)
+    grads = [None] * len(Ws)
+    for l in range(len(Ws) - 1, -1, -1):
+        gl = block_bwd(xs[l], Ws[l], g, H, eps)
+        g = gl.pop("dx")
+        grads[l] = gl
+        if l > 0:
+            g = _store(g, store)
+    return g, grads
 
 
 def block_bwd(x, W, dy, H, eps):

@@ -377,3 +377,87 @@ def test_planted_mistakes_are_caught(monkeypatch):
     P = O.attention_probs(Q, K, 1)
     strict = np.tril(P[0], -1)
     assert not np.allclose(strict.sum(axis=1), 1)
+
+
+# ------------------------------------------------------------------ stack of blocks
+
+def _layers(shape, seeds):
+    """Weight sets of the _small kind (non-trivial gains, larger weights)."""
+    ws = []
+    for sd in seeds:
+        _, inp = _small(S=shape.S, d=shape.d, H=shape.H, inter=shape.inter, D=shape.D, seed=sd)
+        ws.append({k: inp[k].to(torch.float64) for k in GRAD_OF.values() if k != "x"})
+    return ws
+
+
+def test_stack_of_one_is_the_block():
+    shape, inp = _small(S=24, d=16, H=2, inter=24, D=3, seed=41)
+    y1 = O.stack_fwd(inp["x"], [inp], shape.H, shape.eps)
+    yb, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+    assert np.array_equal(y1, yb)
+
+
+def test_stack_identity_layer_is_transparent():
+    """A layer with W_O = 0 and W_2 = 0 adds nothing to either residual, so it
+    passes its input through unchanged wherever it sits in the stack."""
+    shape, inp = _small(S=24, d=16, H=2, inter=24, D=3, seed=42)
+    ident = dict(inp)
+    ident["wo"] = torch.zeros_like(inp["wo"])
+    ident["w2"] = torch.zeros_like(inp["w2"])
+    yb, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+    for Ws in ([inp, ident], [ident, inp], [ident, inp, ident]):
+        y = O.stack_fwd(inp["x"], Ws, shape.H, shape.eps)
+        assert np.max(np.abs(y - yb)) <= 1e-13 * np.max(np.abs(yb))
+
+
+def test_stack_backward_central_finite_differences():
+    """dx and one weight of every layer of a 3-layer stack against central
+    differences of sum(dy * y): a dropped or misplaced link of the chain rule
+    between layers fails."""
+    shape, inp = _small(S=16, d=8, H=2, inter=12, D=2, seed=43)
+    inp = {k: v.to(torch.float64) for k, v in inp.items()}
+    Ws = _layers(shape, [43, 44, 45])
+    x, dy = inp["x"], inp["dy"]
+    dx, grads = O.stack_bwd(x, Ws, dy, shape.H, shape.eps)
+
+    def loss(xx, WW):
+        return float(np.sum(O.f64(dy) * O.stack_fwd(xx, WW, shape.H, shape.eps)))
+
+    rng = np.random.default_rng(5)
+    step = 1e-6
+    v = torch.from_numpy(rng.standard_normal(tuple(x.shape)))
+    fd = (loss(x + step * v, Ws) - loss(x - step * v, Ws)) / (2 * step)
+    an = float(np.sum(dx * v.numpy()))
+    assert abs(fd - an) <= 1e-6 * abs(an), ("dx", fd, an)
+    for l in range(3):
+        for gname, pname in (("dwq", "wq"), ("dw2", "w2"), ("dg_mlp", "g_mlp")):
+            base = Ws[l][pname]
+            u = torch.from_numpy(rng.standard_normal(tuple(base.shape)))
+            plus = [dict(W) for W in Ws]
+            minus = [dict(W) for W in Ws]
+            plus[l][pname] = base + step * u
+            minus[l][pname] = base - step * u
+            fd = (loss(x, plus) - loss(x, minus)) / (2 * step)
+            an = float(np.sum(grads[l][gname] * u.numpy()))
+            assert abs(fd - an) <= 1e-6 * max(abs(an), 1e-8), (l, gname, fd, an)
+
+
+def test_stack_bf16_storage_rounds_only_between_layers():
+    """With bf16 storage a one-layer stack is still the block exactly, and an
+    identity layer after a block returns exactly the block's output rounded
+    to bf16 (the rounding happens at the layer boundary and nowhere else)."""
+    shape, inp = _small(S=24, d=16, H=2, inter=24, D=3, seed=46)
+    ident = dict(inp)
+    ident["wo"] = torch.zeros_like(inp["wo"])
+    ident["w2"] = torch.zeros_like(inp["w2"])
+    yb, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+    y1 = O.stack_fwd(inp["x"], [inp], shape.H, shape.eps, store="bf16")
+    assert np.array_equal(y1, yb)
+    y2 = O.stack_fwd(inp["x"], [inp, ident], shape.H, shape.eps, store="bf16")
+    rounded = torch.from_numpy(yb).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(y2, rounded)
+    assert not np.array_equal(y2, yb)
+    # backward: the gradient handed down is rounded, the top layer's is not
+    dx1, _ = O.stack_bwd(inp["x"], [inp], inp["dy"], shape.H, shape.eps, store="bf16")
+    g = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
+    assert np.array_equal(dx1, g["dx"])
