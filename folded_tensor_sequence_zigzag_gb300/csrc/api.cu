@@ -120,6 +120,7 @@ tsp_status check_cfg(const tsp_cfg* c) {
   if (c->inter <= 0 || c->d < c->D || c->inter < c->D) return TSP_ERR_INVALID_ARG;
   if (c->dtype != TSP_F32 && c->dtype != TSP_BF16) return TSP_ERR_INVALID_ARG;
   if (!(c->eps >= 0.f)) return TSP_ERR_INVALID_ARG;
+  if (!(c->rope_base >= 0.f) || (c->rope_base > 0.f && c->dh % 2 != 0)) return TSP_ERR_INVALID_ARG;
   if (c->S > (int64_t)1 << 31) return TSP_ERR_UNSUPPORTED;
   if (c->dtype == TSP_F32 && c->dh > 128) return TSP_ERR_UNSUPPORTED;
   return TSP_OK;
@@ -140,6 +141,7 @@ tsp_status check_bf16_attn(const tsp_cfg* c) {
 struct Acts {
   float *rstd1, *rstd2, *lse;
   void *a, *qkv, *o, *h, *b, *ab, *g;
+  float2* rope;   // (cos, sin) per zigzag row and frequency, when cfg->rope_base > 0
   size_t bytes;
 };
 
@@ -162,6 +164,7 @@ Acts acts_layout(const tsp_cfg* c, int parts, uint8_t* base) {
     A.a = take(S * d * e);
     A.qkv = take(S * 3 * d * e);
     A.o = take(S * d * e);
+    if (c->rope_base > 0.f) A.rope = (float2*)take(S * (size_t)(c->dh / 2) * sizeof(float2));
   }
   if (parts & PART_MLP) {
     A.rstd2 = (float*)take(S * 4);
@@ -276,6 +279,20 @@ tsp_status fill_wcache(const tsp_cfg* c, const WCache& W, const tsp_attn_w* aw, 
 
 cudaStream_t S_(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Rotary embedding of the Q and K column blocks of a [S, 3d] Q|K|V buffer
+// (inverse = 1: the transposed rotation, which maps gradients of the rotated
+// Q, K back to gradients of the projections).  The forward fills the table of
+// (cos, sin) per zigzag row first; the backward reuses the saved one.
+tsp_status rope_qk(const tsp_cfg* c, const Acts& A, void* qkv, int ty, int inverse,
+                   cudaStream_t st) {
+  if (c->rope_base <= 0.f) return TSP_OK;
+  tsp_status r;
+  if (!inverse &&
+      (r = launch_rope_table(A.rope, c->S, c->D, c->dh, c->rope_base, st)) != TSP_OK)
+    return r;
+  return launch_rope(qkv, ty, c->S, 3 * c->d, c->d, c->H, c->dh, A.rope, inverse, st);
+}
+
 // ----------------------------------------------------------------------------
 // Forward halves
 // ----------------------------------------------------------------------------
@@ -301,6 +318,7 @@ tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, const
     g.nseg_n = d; g.name = "gemm_qkv";
     g.epi = EPI_STORE; g.out_type = OUT_F16; g.out = A.qkv; g.ldo = 3 * d;
     if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    if ((r = rope_qk(c, A, A.qkv, TY_F16, 0, st)) != TSP_OK) return r;
     if ((r = launch_attn_fwd_f16(A.qkv, A.o, A.lse, S, c->H, c->dh, D, st)) != TSP_OK) return r;
     // W_O: split-K over the shards C_k (k = 0..D-1, broadcast order), fp32
     // accumulation in TMEM, residual x added in the epilogue.
@@ -324,6 +342,7 @@ tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, const
       if (r != TSP_OK) return r;
     }
   }
+  if ((r = rope_qk(c, A, qkv, TY_F32, 0, st)) != TSP_OK) return r;
   if ((r = launch_attn_f32_fwd(qkv, S, c->H, c->dh, D, (float*)A.o, A.lse, st)) != TSP_OK) return r;
   for (int k = 0; k < D; ++k) {
     const int lo = (int)((int64_t)k * d / D), hi = (int)((int64_t)(k + 1) * d / D);
@@ -726,6 +745,8 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
     if ((r = launch_attn_bwd_f16(A.qkv, A.o, W.dO, A.lse, W.delta, W.dq_acc, W.dqkv, S, H, dh, D,
                                  st)) != TSP_OK)
       return r;
+    // gradients of the rotated Q, K -> gradients of the projections
+    if ((r = rope_qk(c, A, W.dqkv, TY_F16, 1, st)) != TSP_OK) return r;
     // dW_Q | dW_K | dW_V = [dQ | dK | dV]^T a
     {
       TcGemm g;
@@ -807,6 +828,7 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
   if ((r = launch_attn_f32_bwd((const float*)A.qkv, (const float*)A.o, dO, A.lse, W.delta, dqkv, S,
                                H, dh, D, st)) != TSP_OK)
     return r;
+  if ((r = rope_qk(c, A, dqkv, TY_F32, 1, st)) != TSP_OK) return r;
   float* dws[3] = {dwq, dwk, dwv};
   const float* wts[3] = {(const float*)aw->wq, (const float*)aw->wk, (const float*)aw->wv};
   for (int j = 0; j < 3; ++j) {

@@ -31,6 +31,12 @@ tsp_status launch_rmsnorm_bwd(const float* dout, const void* u, int u_ty, const 
                               int64_t rows, int n, int dtype, cudaStream_t st);
 tsp_status launch_convert_bf16_f16(const void* src, void* dst, int64_t n, cudaStream_t st);
 tsp_status launch_convert_f32_bf16(const float* src, void* dst, int64_t n, cudaStream_t st);
+// rotary embedding: table[row][j] = (cos, sin) of pos(row) * base^(-2j/dh), j < dh/2,
+// pos(row) the global position of zigzag row `row`; then rotate the Q (cols
+// [0, d)) and K (cols [d, 2d)) blocks of a [S, ld] buffer of type ty in place
+tsp_status launch_rope_table(float2* table, int64_t S, int D, int dh, float base, cudaStream_t st);
+tsp_status launch_rope(void* qkv, int ty, int64_t S, int ld, int d, int H, int dh,
+                       const float2* table, int inverse, cudaStream_t st);
 // up to kMaxConvert conversions (n[k] elements each, multiples of 8) in one launch
 constexpr int kMaxConvert = 8;
 tsp_status launch_convert_bf16_f16_many(const void* const* src, void* const* dst, const int64_t* n,

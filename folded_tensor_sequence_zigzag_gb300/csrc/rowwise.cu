@@ -6,6 +6,7 @@
 // attention).  Rank r owns chunks r and 2D-1-r of the 2D equal chunks.
 // RMSNorm: the pages give no formula; the plain reading of a pre-norm block,
 // rms(u; g) = u / sqrt(mean(u^2) + eps) * g with fp32 arithmetic.
+#include <cmath>
 #include <cstring>
 
 #include "common.cuh"
@@ -563,6 +564,90 @@ tsp_status launch_convert_f32_bf16(const float* src, void* dst, int64_t n, cudaS
   const int64_t n8 = n / 8;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((n8 + 255) / 256, (int64_t)num_sms() * 8));
   convert_f32_bf16_kernel<<<grid, 256, 0, st>>>((const float4*)src, (uint4*)dst, n8);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Rotary position embedding (a variant; the pages' block has none).
+// Rotate-half form: within each head, element j < dh/2 pairs with j + dh/2 and
+// the pair turns by the angle pos * f_j, f_j = base^(-2j/dh).  The angle is
+// formed and reduced modulo 2*pi in fp64 (at a million positions an fp32
+// product would be off by a twentieth of a radian); sin and cos of the
+// reduced angle are taken in fp32.  The frequencies come from the host in
+// fp64.
+// ---------------------------------------------------------------------------
+constexpr int kRopeMaxHalf = 128;
+struct RopeFreq {
+  double f[kRopeMaxHalf];
+};
+
+__global__ void rope_table_kernel(float2* __restrict__ tab, int64_t S, int64_t c, int D, int half,
+                                  const __grid_constant__ RopeFreq F) {
+  const int64_t total = S * half;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = t / half;
+    const int j = (int)(t - row * half);
+    const double ang = (double)zz_pos_of_row(row, c, D) * F.f[j];
+    const double two_pi = 6.283185307179586476925287;
+    const double red = ang - two_pi * rint(ang / two_pi);
+    float sv, cv;
+    sincosf((float)red, &sv, &cv);
+    tab[t] = make_float2(cv, sv);
+  }
+}
+
+tsp_status launch_rope_table(float2* table, int64_t S, int D, int dh, float base, cudaStream_t st) {
+  const int half = dh / 2;
+  if (!table || half < 1 || half > kRopeMaxHalf) return TSP_ERR_UNSUPPORTED;
+  RopeFreq F;
+  for (int j = 0; j < half; ++j) F.f[j] = std::pow((double)base, -2.0 * j / (double)dh);
+  Prof prof("rope_table", st);
+  const int64_t total = S * half;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 8));
+  rope_table_kernel<<<grid, 256, 0, st>>>(table, S, S / (2 * D), D, half, F);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+// one thread = one (row, Q or K, head, pair j); consecutive threads take
+// consecutive j of one head, so both halves of a head are read coalesced
+template <typename T>
+__global__ void rope_kernel(T* __restrict__ qkv, int64_t S, int ld, int d, int H, int half,
+                            const float2* __restrict__ tab, float sgn) {
+  const int64_t per_row = 2LL * H * half;
+  const int64_t total = S * per_row;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = t / per_row;
+    int64_t rem = t - row * per_row;
+    const int which = (int)(rem / ((int64_t)H * half));   // 0: Q, 1: K
+    rem -= (int64_t)which * H * half;
+    const int h = (int)(rem / half), j = (int)(rem - (int64_t)h * half);
+    T* p = qkv + row * ld + (int64_t)which * d + (int64_t)h * 2 * half + j;
+    const float2 cs = tab[row * half + j];
+    const float s = sgn * cs.y;
+    const float x1 = to_f(p[0]), x2 = to_f(p[half]);
+    p[0] = from_f<T>(x1 * cs.x - x2 * s);
+    p[half] = from_f<T>(x1 * s + x2 * cs.x);
+  }
+}
+
+tsp_status launch_rope(void* qkv, int ty, int64_t S, int ld, int d, int H, int dh,
+                       const float2* table, int inverse, cudaStream_t st) {
+  const int half = dh / 2;
+  if (!qkv || !table || half < 1) return TSP_ERR_INVALID_ARG;
+  Prof prof("rope", st);
+  const int64_t total = S * 2LL * H * half;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 8));
+  const float sgn = inverse ? -1.f : 1.f;
+  if (ty == TY_F16)
+    rope_kernel<__half><<<grid, 256, 0, st>>>((__half*)qkv, S, ld, d, H, half, table, sgn);
+  else if (ty == TY_F32)
+    rope_kernel<float><<<grid, 256, 0, st>>>((float*)qkv, S, ld, d, H, half, table, sgn);
+  else
+    return TSP_ERR_UNSUPPORTED;
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }

@@ -36,7 +36,7 @@ class TspError(RuntimeError):
 class Cfg(ctypes.Structure):
     _fields_ = [("S", ctypes.c_int64), ("d", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("dh", ctypes.c_int32), ("inter", ctypes.c_int32), ("D", ctypes.c_int32),
-                ("eps", ctypes.c_float), ("dtype", ctypes.c_int32)]
+                ("eps", ctypes.c_float), ("dtype", ctypes.c_int32), ("rope_base", ctypes.c_float)]
 
 
 class AttnW(ctypes.Structure):
@@ -155,9 +155,9 @@ class BlockWeights:
                     1 if residual else 0)
 
 
-def make_cfg(S, d, H, inter, D, dtype: torch.dtype, eps=1e-6) -> Cfg:
+def make_cfg(S, d, H, inter, D, dtype: torch.dtype, eps=1e-6, rope_base=0.0) -> Cfg:
     return Cfg(int(S), int(d), int(H), int(d // H), int(inter), int(D), float(eps),
-               TSP_BF16 if dtype == torch.bfloat16 else TSP_F32)
+               TSP_BF16 if dtype == torch.bfloat16 else TSP_F32, float(rope_base))
 
 
 def workspace_bytes(cfg: Cfg, op: int) -> int:

@@ -87,6 +87,11 @@ typedef struct {
   int32_t d, H, dh, inter, D;
   float eps;
   int32_t dtype;
+  /* Rotary position embedding of Q and K (not on the pages; a variant):
+   * 0 = none (the pages' block); > 0 = the rotate-half rotation with
+   * frequencies rope_base^(-2j/dh), j < dh/2, at each token's global
+   * position (the zigzag layout only moves rows).  Needs an even dh. */
+  float rope_base;
 } tsp_cfg;
 
 /* Attention-half weights: wq, wk, wv, wo [d, d]; g_attn [d]. */

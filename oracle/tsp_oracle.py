@@ -35,6 +35,10 @@ design notes of the repository.
   R8  Backward: the exact gradient of the forward above; weight gradients of
       the virtual ranks are summed (what TSP's reduction to shard owners
       delivers).
+  R12 Rotary position embedding (a variant, off by default): rotate-half
+      form, pair (j, j + dh/2) of every head turned by pos * base^(-2j/dh)
+      at the token's global position; Q and K only.  Selected by a
+      "rope_base" entry next to the weights (0 or absent: none).
   R11 Stack of L layers: plain composition, each layer its own weights; a
       stack whose activations live in bf16 hands each layer's output (and, in
       the backward, each layer's input gradient) to the next layer rounded to
@@ -211,12 +215,43 @@ def _w(W, name):
     return f64(W[name])
 
 
+def _rope_base(W):
+    return float(W.get("rope_base", 0.0)) if hasattr(W, "get") else 0.0
+
+
+def rope(X, pos, H, base, inverse=False):
+    """Rotary position embedding (a variant; the pages' block has none,
+    reading R12): within each head of width dh, element j < dh/2 pairs with
+    element j + dh/2 and the pair turns by the angle pos * base^(-2j/dh);
+    ``inverse`` applies the transposed rotation (the map of gradients).
+    base = 0 leaves X as it is."""
+    if not base:
+        return X
+    X = np.asarray(X, dtype=np.float64)
+    d = X.shape[1]
+    dh = d // H
+    half = dh // 2
+    f = float(base) ** (-2.0 * np.arange(half) / dh)
+    ang = np.asarray(pos, dtype=np.float64)[:, None] * f[None, :]
+    cs, sn = np.cos(ang), np.sin(ang)
+    if inverse:
+        sn = -sn
+    Y = X.copy()
+    for h in range(H):
+        a = X[:, h * dh:h * dh + half]
+        b = X[:, h * dh + half:(h + 1) * dh]
+        Y[:, h * dh:h * dh + half] = a * cs - b * sn
+        Y[:, h * dh + half:(h + 1) * dh] = a * sn + b * cs
+    return Y
+
+
 def attn_block_fwd(x, W, H, eps):
     """h = x + Attn(rms(x; g_attn)) W_O^T.  Returns (h, saved dict)."""
     x = f64(x)
     a, rstd1 = rmsnorm(x, _w(W, "g_attn"), eps)
-    Q = a @ _w(W, "wq").T
-    K = a @ _w(W, "wk").T
+    p = np.arange(x.shape[0])
+    Q = rope(a @ _w(W, "wq").T, p, H, _rope_base(W))
+    K = rope(a @ _w(W, "wk").T, p, H, _rope_base(W))
     V = a @ _w(W, "wv").T
     O, LSE = causal_attention(Q, K, V, H)
     h = x + O @ _w(W, "wo").T
@@ -291,6 +326,8 @@ def block_fwd_sharded(x, W, H, D, eps, parts=("attn", "mlp")):
                 Qz[rows[r], C] = az[rows[r]] @ wq[C].T
                 Kz[rows[r], C] = az[rows[r]] @ wk[C].T
                 Vz[rows[r], C] = az[rows[r]] @ wv[C].T
+        Qz = rope(Qz, pos, H, _rope_base(W))        # whole heads, global positions
+        Kz = rope(Kz, pos, H, _rope_base(W))
         for r in range(D):
             O_r, _ = causal_attention(Qz[rows[r]], Kz, Vz, H, q_pos=pos[rows[r]], k_pos=pos)
             for k in range(D):
@@ -352,9 +389,9 @@ def block_fwd_rows(x, W, H, eps, rows, attn_only=False):
     kmax = int(rows.max()) + 1
     g1 = _w(W, "g_attn")
     a_all = rmsnorm(x[:kmax], g1, eps)[0]
-    K = a_all @ _w(W, "wk").T
+    K = rope(a_all @ _w(W, "wk").T, np.arange(kmax), H, _rope_base(W))
     V = a_all @ _w(W, "wv").T
-    Q = a_all[rows] @ _w(W, "wq").T
+    Q = rope(a_all[rows] @ _w(W, "wq").T, rows, H, _rope_base(W))
     O, _ = causal_attention(Q, K, V, H, q_pos=rows, k_pos=np.arange(kmax))
     h = x[rows] + O @ _w(W, "wo").T
     if attn_only:
@@ -483,6 +520,9 @@ def block_bwd(x, W, dy, H, eps):
     dwo = dh.T @ s["O"]
     dO = dh @ wo
     dQ, dK, dV = causal_attention_bwd(s["Q"], s["K"], s["V"], s["O"], dO, H)
+    p = np.arange(s["x"].shape[0])
+    dQ = rope(dQ, p, H, _rope_base(W), inverse=True)   # back through the rotation
+    dK = rope(dK, p, H, _rope_base(W), inverse=True)
     dwq = dQ.T @ s["a"]
     dwk = dK.T @ s["a"]
     dwv = dV.T @ s["a"]
@@ -517,6 +557,8 @@ def block_bwd_sharded(x, W, dy, H, D, eps):
     for r in range(D):
         az[R[r]], rstd1[R[r]] = rmsnorm(xz[R[r]], g1, eps)
     Qz, Kz, Vz = az @ wq.T, az @ wk.T, az @ wv.T
+    Qz = rope(Qz, pos, H, _rope_base(W))
+    Kz = rope(Kz, pos, H, _rope_base(W))
     Oz = np.zeros_like(xz)
     for r in range(D):
         Oz[R[r]] = causal_attention(Qz[R[r]], Kz, Vz, H, q_pos=pos[R[r]], k_pos=pos)[0]
@@ -548,6 +590,8 @@ def block_bwd_sharded(x, W, dy, H, D, eps):
         dQz[R[r]] = dq
         dKz += dk            # returned to the key owners
         dVz += dv
+    dQz = rope(dQz, pos, H, _rope_base(W), inverse=True)
+    dKz = rope(dKz, pos, H, _rope_base(W), inverse=True)
     dxz = np.zeros_like(xz)
     for r in range(D):
         a_r = az[R[r]]
@@ -581,11 +625,11 @@ def block_bwd_tail(x, W, dy, H, eps, n_tail):
     wq, wk, wv, wo = (_w(W, n) for n in ("wq", "wk", "wv", "wo"))
     w1, w3, w2 = _w(W, "w1"), _w(W, "w3"), _w(W, "w2")
     a_all, rstd1 = rmsnorm(x, g1, eps)
-    K = a_all @ wk.T
-    V = a_all @ wv.T
     tail = np.arange(t0, S)
     keys = np.arange(S)
-    Q_t = a_all[t0:] @ wq.T
+    K = rope(a_all @ wk.T, keys, H, _rope_base(W))
+    V = a_all @ wv.T
+    Q_t = rope(a_all[t0:] @ wq.T, tail, H, _rope_base(W))
     O_t, _ = causal_attention(Q_t, K, V, H, q_pos=tail, k_pos=keys)
     h_t = x[t0:] + O_t @ wo.T
     b_t, rstd2 = rmsnorm(h_t, g2, eps)
@@ -599,7 +643,9 @@ def block_bwd_tail(x, W, dy, H, eps, n_tail):
     dh_t = dy[t0:] + du2
     dO_t = dh_t @ wo
     dQ_t, dK, dV = causal_attention_bwd(Q_t, K, V, O_t, dO_t, H, q_pos=tail, k_pos=keys)
-    da = dQ_t @ wq + dK[t0:] @ wk + dV[t0:] @ wv
+    dQ_t = rope(dQ_t, tail, H, _rope_base(W), inverse=True)
+    dK_t = rope(dK[t0:], tail, H, _rope_base(W), inverse=True)
+    da = dQ_t @ wq + dK_t @ wk + dV[t0:] @ wv
     du1, _ = rmsnorm_bwd(da, x[t0:], g1, rstd1[t0:])
     return dh_t + du1
 

@@ -44,14 +44,15 @@ def test_strerror(lib):
 
 
 def _cfg(**kw):
-    base = dict(S=256, d=64, H=4, inter=128, D=4, dtype=tsp.TSP_F32)
+    base = dict(S=256, d=64, H=4, inter=128, D=4, dtype=tsp.TSP_F32, rope_base=0.0)
     base.update(kw)
     return tsp.Cfg(base["S"], base["d"], base["H"], base.get("dh", base["d"] // base["H"]),
-                   base["inter"], base["D"], 1e-6, base["dtype"])
+                   base["inter"], base["D"], 1e-6, base["dtype"], base["rope_base"])
 
 
 @pytest.mark.parametrize("bad", [dict(S=250), dict(D=0), dict(D=65), dict(d=66), dict(dh=8),
-                                 dict(inter=0), dict(dtype=7), dict(S=0), dict(d=2, H=1, D=4)])
+                                 dict(inter=0), dict(dtype=7), dict(S=0), dict(d=2, H=1, D=4),
+                                 dict(rope_base=-1.0), dict(d=60, H=4, rope_base=10000.0)])
 def test_invalid_cfg_rejected_without_launch(lib, bad):
     cfg = _cfg(**bad)
     assert lib.tsp_workspace_bytes(ctypes.byref(cfg), tsp.TSP_OP_BLOCK_FWD) == 0

@@ -27,9 +27,10 @@ def lib():
     return tsp.load()
 
 
-def _run_block(shape: BlockShape, inp: dict, dtype, mode="block", norm=True, residual=True):
+def _run_block(shape: BlockShape, inp: dict, dtype, mode="block", norm=True, residual=True,
+               rope_base=0.0):
     dev = "cuda"
-    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps)
+    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps, rope_base)
     W = tsp.BlockWeights.from_dict(inp, dev)
     x = inp["x"].to(dev)
     xz = tsp.zigzag_permute(x, shape.D)
@@ -205,9 +206,9 @@ def test_7b_block_fwd_sampled_rows(S):
 
 # ------------------------------------------------------------------ backward
 
-def _run_bwd(shape, inp, dtype):
+def _run_bwd(shape, inp, dtype, rope_base=0.0):
     dev = "cuda"
-    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps)
+    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps, rope_base)
     W = tsp.BlockWeights.from_dict(inp, dev)
     xz = tsp.zigzag_permute(inp["x"].to(dev), shape.D)
     dyz = tsp.zigzag_permute(inp["dy"].to(dev), shape.D)
@@ -300,3 +301,47 @@ def test_7b_fwd_bwd_S32768_sampled():
     assert_bf16_close(g["dx"][S - n_tail:], dx_ref, "dx (S=32768, last 256 positions)")
     for k in ("dwq", "dwk", "dwv", "dwo", "dw1", "dw3", "dw2", "dg_attn", "dg_mlp"):
         assert torch.isfinite(g[k]).all(), k
+
+
+# ------------------------------------------------------------------ rotary embedding (variant)
+
+def _with_rope(inp, base):
+    out = dict(inp)
+    out["rope_base"] = base
+    return out
+
+
+def test_tiny_fp32_rope_forward_backward():
+    base = 10000.0
+    inp = make_block_inputs(TINY_FP32, torch.float32, seed=4, with_dy=True)
+    y, g = _run_bwd(TINY_FP32, inp, torch.float32, rope_base=base)
+    ref_in = _with_rope(inp, base)
+    yref, _ = O.block_fwd(inp["x"], ref_in, TINY_FP32.H, TINY_FP32.eps)
+    assert_f32_close(y, yref, "rope fwd")
+    ref = O.block_bwd(inp["x"], ref_in, inp["dy"], TINY_FP32.H, TINY_FP32.eps)
+    for k, v in ref.items():
+        scale = max(1.0, float(np.max(np.abs(v))))
+        assert_f32_close(g[k], v, f"rope {k}", tol=1e-4 * scale)
+
+
+def test_bf16_rope_forward_backward_small():
+    base = 10000.0
+    shape = BlockShape(S=2048, d=256, H=2, inter=512, D=4)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=6, with_dy=True)
+    y, g = _run_bwd(shape, inp, torch.bfloat16, rope_base=base)
+    ref_in = _with_rope(inp, base)
+    yref, _ = O.block_fwd(inp["x"], ref_in, shape.H, shape.eps)
+    assert_bf16_close(y, yref, "bf16 rope y")
+    ref = O.block_bwd(inp["x"], ref_in, inp["dy"], shape.H, shape.eps)
+    for k, v in ref.items():
+        assert_bf16_close(g[k], v, f"bf16 rope {k}")
+
+
+def test_7b_rope_block_fwd_sampled_rows():
+    base, S = 500000.0, 16384
+    shape = BlockShape(S=S, d=4096, H=32, inter=11008, D=8)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=2)
+    y = _run_block(shape, inp, torch.bfloat16, rope_base=base)
+    rows = sample_rows(S, 8).numpy()
+    ref = O.block_fwd_rows(inp["x"], _with_rope(inp, base), shape.H, shape.eps, rows)
+    assert_bf16_close(y[rows], ref, "7B rope block S=16384")

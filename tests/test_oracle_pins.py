@@ -461,3 +461,91 @@ def test_stack_bf16_storage_rounds_only_between_layers():
     dx1, _ = O.stack_bwd(inp["x"], [inp], inp["dy"], shape.H, shape.eps, store="bf16")
     g = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
     assert np.array_equal(dx1, g["dx"])
+
+
+# ------------------------------------------------------------------ rotary embedding (variant)
+
+def _rope_rand(n=12, H=2, dh=8, seed=0):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((n, H * dh)), rng.integers(0, 5000, size=n)
+
+
+def test_rope_closed_form_on_unit_vectors():
+    """Element j of a head alone turns into (cos, sin) of pos * base^(-2j/dh)
+    at positions j and j + dh/2: pins the frequency formula and the pairing."""
+    H, dh, base = 2, 8, 10000.0
+    half = dh // 2
+    pos = np.array([0, 1, 7, 4095])
+    for h in range(H):
+        for j in range(half):
+            X = np.zeros((len(pos), H * dh))
+            X[:, h * dh + j] = 1.0
+            Y = O.rope(X, pos, H, base)
+            ang = pos * base ** (-2.0 * j / dh)
+            assert np.allclose(Y[:, h * dh + j], np.cos(ang), atol=1e-15)
+            assert np.allclose(Y[:, h * dh + j + half], np.sin(ang), atol=1e-15)
+            others = np.delete(Y, [h * dh + j, h * dh + j + half], axis=1)
+            assert np.all(others == 0)
+
+
+def test_rope_norms_roundtrip_and_identity():
+    X, pos = _rope_rand()
+    Y = O.rope(X, pos, 2, 10000.0)
+    assert np.allclose(np.linalg.norm(Y, axis=1), np.linalg.norm(X, axis=1), rtol=1e-14)
+    assert np.allclose(O.rope(Y, pos, 2, 10000.0, inverse=True), X, atol=1e-13)
+    assert np.array_equal(O.rope(X, np.zeros_like(pos), 2, 10000.0), X)
+    assert O.rope(X, pos, 2, 0.0) is X
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    q, _ = _rope_rand(n=1, seed=1)
+    k, _ = _rope_rand(n=1, seed=2)
+    H, dh = 2, 8
+    for m, n in ((5, 3), (100, 100), (17, 2000)):
+        for t in (0, 1, 999):
+            a = O.rope(q, [m + t], H, 500.0)
+            b = O.rope(k, [n + t], H, 500.0)
+            ref = O.rope(q, [m], H, 500.0), O.rope(k, [n], H, 500.0)
+            for h in range(H):
+                sl = slice(h * dh, (h + 1) * dh)
+                assert np.isclose(a[0, sl] @ b[0, sl], ref[0][0, sl] @ ref[1][0, sl], rtol=1e-12)
+
+
+def _rope_small(seed, D=2, S=32):
+    shape, inp = _small(S=S, d=16, H=2, inter=24, D=D, seed=seed)
+    inp = {k: v.to(torch.float64) for k, v in inp.items()}
+    inp["rope_base"] = 1000.0
+    return shape, inp
+
+
+def test_rope_block_backward_central_finite_differences():
+    shape, inp = _rope_small(51)
+    g = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
+    rng = np.random.default_rng(3)
+    step = 1e-6
+    for gname, pname in (("dx", "x"), ("dwq", "wq"), ("dwk", "wk"), ("dwv", "wv")):
+        base = inp[pname]
+        v = torch.from_numpy(rng.standard_normal(tuple(base.shape)))
+        plus, minus = dict(inp), dict(inp)
+        plus[pname] = base + step * v
+        minus[pname] = base - step * v
+        fd = (_loss(plus, shape.H, shape.eps) - _loss(minus, shape.H, shape.eps)) / (2 * step)
+        an = float(np.sum(g[gname] * v.numpy()))
+        assert abs(fd - an) <= 1e-6 * abs(an), (gname, fd, an)
+
+
+@pytest.mark.parametrize("D", [1, 2, 4])
+def test_rope_sharded_and_tail_equal_unsharded(D):
+    shape, inp = _rope_small(60 + D, D=D, S=2 * D * 8)
+    y, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+    ys = O.block_fwd_sharded(inp["x"], inp, shape.H, D, shape.eps)
+    assert np.max(np.abs(ys - y)) <= 1e-12 * np.max(np.abs(y))
+    rows = np.array([0, 3, shape.S - 1])
+    yr = O.block_fwd_rows(inp["x"], inp, shape.H, shape.eps, rows)
+    assert np.max(np.abs(yr - y[rows])) <= 1e-12 * np.max(np.abs(y))
+    g = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
+    gs = O.block_bwd_sharded(inp["x"], inp, inp["dy"], shape.H, D, shape.eps)
+    for k in GRAD_OF:
+        assert np.max(np.abs(gs[k] - g[k])) <= 1e-12 * np.max(np.abs(g[k])), k
+    tail = O.block_bwd_tail(inp["x"], inp, inp["dy"], shape.H, shape.eps, 5)
+    assert np.max(np.abs(tail - g["dx"][-5:])) <= 1e-12 * np.max(np.abs(g["dx"]))
