@@ -21,7 +21,7 @@ design notes of the repository.
 
   R1  RMSNorm: rms(u) = u / sqrt(mean(u^2) + eps) * g, eps = 1e-6, learnable
       gain g, no bias (pre-norm block).
-  R2  No biases anywhere; no positional encoding (NoPE).
+  R2  No biases anywhere; no positional encoding (NoPE) unless R12 is selected.
   R3  Attention: multi-head, scale 1/sqrt(dh), causal with the diagonal
       included (no row is ever fully masked).
   R4  Gated MLP: G = silu(b W_1^T) * (b W_3^T), y = h + G W_2^T
