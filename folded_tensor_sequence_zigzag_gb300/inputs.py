@@ -7,7 +7,9 @@ tensors in a fixed order and rounds them to the storage dtype.
 Workload recipe (the pages print no dataset; every input is synthetic):
   * activations x  ~ N(0, 1), shape [S, d], in global token order;
   * weight matrices ~ N(0, 0.02), nn.Linear convention [out, in]:
-      W_Q, W_K, W_V, W_O : [d, d];  W_1, W_3 : [inter, d];  W_2 : [d, inter];
+      W_Q, W_O : [d, d];  W_K, W_V : [Hkv*dh, d] ([d, d] unless the shape
+      sets Hkv, grouped-query attention);  W_1, W_3 : [inter, d];
+      W_2 : [d, inter];
   * RMSNorm gains g_attn, g_mlp = 1 (learnable; not drawn);
   * upstream gradient dy ~ N(0, 1), shape [S, d] (training step only).
 Draw order on one ``torch.Generator('cpu')``: x, W_Q, W_K, W_V, W_O, W_1,
@@ -30,10 +32,15 @@ class BlockShape:
     inter: int      # SwiGLU intermediate size
     D: int          # virtual ranks
     eps: float = 1e-6
+    Hkv: int = 0    # K/V heads (0: as many as query heads)
 
     @property
     def dh(self) -> int:
         return self.d // self.H
+
+    @property
+    def dkv(self) -> int:
+        return (self.Hkv or self.H) * self.dh
 
 
 # The five workloads the method is exercised on (7B-shaped unless noted).
@@ -64,7 +71,8 @@ def make_block_inputs(shape: BlockShape, dtype: torch.dtype, seed: int = 0,
     out = {"x": _normal(gen, (S, d), 1.0, dtype)}
     if not mlp_only:
         for name in ("wq", "wk", "wv", "wo"):
-            out[name] = _normal(gen, (d, d), 0.02, dtype)
+            rows = shape.dkv if name in ("wk", "wv") else d
+            out[name] = _normal(gen, (rows, d), 0.02, dtype)
     out["w1"] = _normal(gen, (inter, d), 0.02, dtype)
     out["w3"] = _normal(gen, (inter, d), 0.02, dtype)
     out["w2"] = _normal(gen, (d, inter), 0.02, dtype)

@@ -39,6 +39,11 @@ design notes of the repository.
       form, pair (j, j + dh/2) of every head turned by pos * base^(-2j/dh)
       at the token's global position; Q and K only.  Selected by a
       "rope_base" entry next to the weights (0 or absent: none).
+  R13 Grouped-query attention (a variant, off by default): H query heads
+      share Hkv K/V heads, Hkv dividing H; query head h reads K/V head
+      floor(h / (H / Hkv)), so consecutive query heads form a group.  The K/V
+      head count follows from the shapes (W_K, W_V have Hkv*dh rows); Hkv = H
+      is plain multi-head attention.
   R11 Stack of L layers: plain composition, each layer its own weights; a
       stack whose activations live in bf16 hands each layer's output (and, in
       the backward, each layer's input gradient) to the next layer rounded to
@@ -160,11 +165,15 @@ def causal_attention(Q, K, V, H, q_pos=None, k_pos=None, row_block=512):
     p_ij = exp(s_ij - m_i) / sum_j exp(s_ij - m_i),  o_i = sum_j p_ij v_j.
     Rows are evaluated a group at a time only to bound memory.
 
+    With fewer K/V heads than query heads (reading R13) query head h reads
+    K/V head h // (H / Hkv), Hkv = K.shape[1] / dh.
+
     Returns (O [nq, H*dh], LSE [H, nq]) with LSE_i = log sum_j exp(s_ij).
     """
     nq = Q.shape[0]
     nk = K.shape[0]
     dh = Q.shape[1] // H
+    grp = H // (K.shape[1] // dh)
     if q_pos is None:
         q_pos = np.arange(nq)
     if k_pos is None:
@@ -179,12 +188,13 @@ def causal_attention(Q, K, V, H, q_pos=None, k_pos=None, row_block=512):
         allowed = allowed[:, :kmax]
         for h in range(H):
             cols = slice(h * dh, (h + 1) * dh)
-            s = (Q[r0:r1, cols] @ K[:kmax, cols].T) * scale
+            kc = slice((h // grp) * dh, (h // grp + 1) * dh)
+            s = (Q[r0:r1, cols] @ K[:kmax, kc].T) * scale
             s = np.where(allowed, s, -np.inf)
             m = s.max(axis=1, keepdims=True)
             e = np.exp(s - m)
             z = e.sum(axis=1, keepdims=True)
-            O[r0:r1, cols] = (e / z) @ V[:kmax, cols]
+            O[r0:r1, cols] = (e / z) @ V[:kmax, kc]
             LSE[h, r0:r1] = (m + np.log(z))[:, 0]
     return O, LSE
 
@@ -193,13 +203,15 @@ def attention_probs(Q, K, H, q_pos=None, k_pos=None):
     """Full probability matrices P[h, i, j] (small inputs only; used by pins)."""
     nq, nk = Q.shape[0], K.shape[0]
     dh = Q.shape[1] // H
+    grp = H // (K.shape[1] // dh)
     q_pos = np.arange(nq) if q_pos is None else q_pos
     k_pos = np.arange(nk) if k_pos is None else k_pos
     allowed = k_pos[None, :] <= q_pos[:, None]
     P = np.zeros((H, nq, nk))
     for h in range(H):
         cols = slice(h * dh, (h + 1) * dh)
-        s = (Q[:, cols] @ K[:, cols].T) / math.sqrt(dh)
+        kc = slice((h // grp) * dh, (h // grp + 1) * dh)
+        s = (Q[:, cols] @ K[:, kc].T) / math.sqrt(dh)
         s = np.where(allowed, s, -np.inf)
         e = np.exp(s - s.max(axis=1, keepdims=True))
         P[h] = e / e.sum(axis=1, keepdims=True)
@@ -217,6 +229,11 @@ def _w(W, name):
 
 def _rope_base(W):
     return float(W.get("rope_base", 0.0)) if hasattr(W, "get") else 0.0
+
+
+def _kv_heads(W, H):
+    """K/V head count of the weights: W_K rows / dh (reading R13)."""
+    return W["wk"].shape[0] // (W["wq"].shape[0] // H)
 
 
 def rope(X, pos, H, base, inverse=False):
@@ -251,7 +268,7 @@ def attn_block_fwd(x, W, H, eps):
     a, rstd1 = rmsnorm(x, _w(W, "g_attn"), eps)
     p = np.arange(x.shape[0])
     Q = rope(a @ _w(W, "wq").T, p, H, _rope_base(W))
-    K = rope(a @ _w(W, "wk").T, p, H, _rope_base(W))
+    K = rope(a @ _w(W, "wk").T, p, _kv_heads(W, H), _rope_base(W))
     V = a @ _w(W, "wv").T
     O, LSE = causal_attention(Q, K, V, H)
     h = x + O @ _w(W, "wo").T
@@ -292,7 +309,9 @@ def block_fwd_sharded(x, W, H, D, eps, parts=("attn", "mlp")):
 
     1. zigzag-partition the tokens (reading R5);
     2. attention broadcast loop: shard k = 0..D-1 of the packed W_Q/W_K/W_V
-       columns C_k arrives; every rank projects its own rows with it;
+       columns C_k arrives (K/V columns cut the same way over their own
+       width, which is d unless reading R13 applies); every rank projects its
+       own rows with it;
     3. "all-gather" of K/V: concatenate every rank's K/V rows with their
        global positions;
     4. causal attention of rank r's rows against the gathered K/V;
@@ -316,18 +335,21 @@ def block_fwd_sharded(x, W, H, D, eps, parts=("attn", "mlp")):
     if "attn" in parts:
         g1 = _w(W, "g_attn")
         wq, wk, wv, wo = (_w(W, n) for n in ("wq", "wk", "wv", "wo"))
-        Qz = np.zeros((S, d)); Kz = np.zeros((S, d)); Vz = np.zeros((S, d))
+        dkv = wk.shape[0]
+        Kb = shard_bounds(dkv, D)
+        Qz = np.zeros((S, d)); Kz = np.zeros((S, dkv)); Vz = np.zeros((S, dkv))
         az = np.zeros((S, d))
         for r in range(D):
             az[rows[r]] = rmsnorm(xz[rows[r]], g1, eps)[0]
         for k in range(D):                      # shard k is broadcast ...
             C = slice(Cb[k], Cb[k + 1])
+            Ck = slice(Kb[k], Kb[k + 1])
             for r in range(D):                  # ... and every rank projects
                 Qz[rows[r], C] = az[rows[r]] @ wq[C].T
-                Kz[rows[r], C] = az[rows[r]] @ wk[C].T
-                Vz[rows[r], C] = az[rows[r]] @ wv[C].T
+                Kz[rows[r], Ck] = az[rows[r]] @ wk[Ck].T
+                Vz[rows[r], Ck] = az[rows[r]] @ wv[Ck].T
         Qz = rope(Qz, pos, H, _rope_base(W))        # whole heads, global positions
-        Kz = rope(Kz, pos, H, _rope_base(W))
+        Kz = rope(Kz, pos, _kv_heads(W, H), _rope_base(W))
         for r in range(D):
             O_r, _ = causal_attention(Qz[rows[r]], Kz, Vz, H, q_pos=pos[rows[r]], k_pos=pos)
             for k in range(D):
@@ -389,7 +411,7 @@ def block_fwd_rows(x, W, H, eps, rows, attn_only=False):
     kmax = int(rows.max()) + 1
     g1 = _w(W, "g_attn")
     a_all = rmsnorm(x[:kmax], g1, eps)[0]
-    K = rope(a_all @ _w(W, "wk").T, np.arange(kmax), H, _rope_base(W))
+    K = rope(a_all @ _w(W, "wk").T, np.arange(kmax), _kv_heads(W, H), _rope_base(W))
     V = a_all @ _w(W, "wv").T
     Q = rope(a_all[rows] @ _w(W, "wq").T, rows, H, _rope_base(W))
     O, _ = causal_attention(Q, K, V, H, q_pos=rows, k_pos=np.arange(kmax))
@@ -422,10 +444,13 @@ def causal_attention_bwd(Q, K, V, O, dO, H, q_pos=None, k_pos=None, row_block=51
     With P the probabilities:  dV = P^T dO,  dP = dO V^T,
     Delta_i = sum_c dO_ic O_ic,  dS = P * (dP - Delta),
     dQ = dS K / sqrt(dh),  dK = dS^T Q / sqrt(dh).  The sums over query
-    rows are taken a row group at a time only to bound memory.
+    rows are taken a row group at a time only to bound memory; with grouped
+    K/V heads (reading R13) a K/V head's dK and dV sum over its group's query
+    heads.
     """
     nq, nk = Q.shape[0], K.shape[0]
     dh = Q.shape[1] // H
+    grp = H // (K.shape[1] // dh)
     q_pos = np.arange(nq) if q_pos is None else q_pos
     k_pos = np.arange(nk) if k_pos is None else k_pos
     scale = 1.0 / math.sqrt(dh)
@@ -437,17 +462,18 @@ def causal_attention_bwd(Q, K, V, O, dO, H, q_pos=None, k_pos=None, row_block=51
         allowed = allowed[:, :kmax]
         for h in range(H):
             cols = slice(h * dh, (h + 1) * dh)
-            s = (Q[r0:r1, cols] @ K[:kmax, cols].T) * scale
+            kc = slice((h // grp) * dh, (h // grp + 1) * dh)
+            s = (Q[r0:r1, cols] @ K[:kmax, kc].T) * scale
             s = np.where(allowed, s, -np.inf)
             e = np.exp(s - s.max(axis=1, keepdims=True))
             P = e / e.sum(axis=1, keepdims=True)
             do = dO[r0:r1, cols]
-            dV[:kmax, cols] += P.T @ do
-            dP = do @ V[:kmax, cols].T
+            dV[:kmax, kc] += P.T @ do
+            dP = do @ V[:kmax, kc].T
             delta = (do * O[r0:r1, cols]).sum(axis=1, keepdims=True)
             dS = P * (dP - delta)
-            dQ[r0:r1, cols] = (dS @ K[:kmax, cols]) * scale
-            dK[:kmax, cols] += (dS.T @ Q[r0:r1, cols]) * scale
+            dQ[r0:r1, cols] = (dS @ K[:kmax, kc]) * scale
+            dK[:kmax, kc] += (dS.T @ Q[r0:r1, cols]) * scale
     return dQ, dK, dV
 
 
@@ -522,7 +548,7 @@ def block_bwd(x, W, dy, H, eps):
     dQ, dK, dV = causal_attention_bwd(s["Q"], s["K"], s["V"], s["O"], dO, H)
     p = np.arange(s["x"].shape[0])
     dQ = rope(dQ, p, H, _rope_base(W), inverse=True)   # back through the rotation
-    dK = rope(dK, p, H, _rope_base(W), inverse=True)
+    dK = rope(dK, p, _kv_heads(W, H), _rope_base(W), inverse=True)
     dwq = dQ.T @ s["a"]
     dwk = dK.T @ s["a"]
     dwv = dV.T @ s["a"]
@@ -558,7 +584,7 @@ def block_bwd_sharded(x, W, dy, H, D, eps):
         az[R[r]], rstd1[R[r]] = rmsnorm(xz[R[r]], g1, eps)
     Qz, Kz, Vz = az @ wq.T, az @ wk.T, az @ wv.T
     Qz = rope(Qz, pos, H, _rope_base(W))
-    Kz = rope(Kz, pos, H, _rope_base(W))
+    Kz = rope(Kz, pos, _kv_heads(W, H), _rope_base(W))
     Oz = np.zeros_like(xz)
     for r in range(D):
         Oz[R[r]] = causal_attention(Qz[R[r]], Kz, Vz, H, q_pos=pos[R[r]], k_pos=pos)[0]
@@ -583,7 +609,7 @@ def block_bwd_sharded(x, W, dy, H, D, eps):
         dhz[R[r]] = dy_r + du2
         grads["dwo"] = grads["dwo"] + dhz[R[r]].T @ Oz[R[r]]
         dOz[R[r]] = dhz[R[r]] @ wo
-    dQz = np.zeros_like(xz); dKz = np.zeros_like(xz); dVz = np.zeros_like(xz)
+    dQz = np.zeros_like(xz); dKz = np.zeros_like(Kz); dVz = np.zeros_like(Vz)
     for r in range(D):
         dq, dk, dv = causal_attention_bwd(Qz[R[r]], Kz, Vz, Oz[R[r]], dOz[R[r]], H,
                                           q_pos=pos[R[r]], k_pos=pos)
@@ -591,7 +617,7 @@ def block_bwd_sharded(x, W, dy, H, D, eps):
         dKz += dk            # returned to the key owners
         dVz += dv
     dQz = rope(dQz, pos, H, _rope_base(W), inverse=True)
-    dKz = rope(dKz, pos, H, _rope_base(W), inverse=True)
+    dKz = rope(dKz, pos, _kv_heads(W, H), _rope_base(W), inverse=True)
     dxz = np.zeros_like(xz)
     for r in range(D):
         a_r = az[R[r]]
@@ -627,7 +653,7 @@ def block_bwd_tail(x, W, dy, H, eps, n_tail):
     a_all, rstd1 = rmsnorm(x, g1, eps)
     tail = np.arange(t0, S)
     keys = np.arange(S)
-    K = rope(a_all @ wk.T, keys, H, _rope_base(W))
+    K = rope(a_all @ wk.T, keys, _kv_heads(W, H), _rope_base(W))
     V = a_all @ wv.T
     Q_t = rope(a_all[t0:] @ wq.T, tail, H, _rope_base(W))
     O_t, _ = causal_attention(Q_t, K, V, H, q_pos=tail, k_pos=keys)
@@ -644,7 +670,7 @@ def block_bwd_tail(x, W, dy, H, eps, n_tail):
     dO_t = dh_t @ wo
     dQ_t, dK, dV = causal_attention_bwd(Q_t, K, V, O_t, dO_t, H, q_pos=tail, k_pos=keys)
     dQ_t = rope(dQ_t, tail, H, _rope_base(W), inverse=True)
-    dK_t = rope(dK[t0:], tail, H, _rope_base(W), inverse=True)
+    dK_t = rope(dK[t0:], tail, _kv_heads(W, H), _rope_base(W), inverse=True)
     da = dQ_t @ wq + dK_t @ wk + dV[t0:] @ wv
     du1, _ = rmsnorm_bwd(da, x[t0:], g1, rstd1[t0:])
     return dh_t + du1

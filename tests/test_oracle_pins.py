@@ -171,18 +171,21 @@ def _torch_block(inp, H, eps, requires_grad=False):
     x = T["x"]
     S, d = x.shape
     dh = d // H
+    Hk = T["wk"].shape[0] // dh          # K/V heads (grouped-query attention if < H)
     a = F.rms_norm(x, (d,), T["g_attn"], eps=eps)
-    heads = lambda m: m.view(S, H, dh).transpose(0, 1)  # noqa: E731
-    o = F.scaled_dot_product_attention(heads(F.linear(a, T["wq"])), heads(F.linear(a, T["wk"])),
-                                       heads(F.linear(a, T["wv"])), is_causal=True)
+    heads = lambda m, n: m.view(S, n, dh).transpose(0, 1)  # noqa: E731
+    o = F.scaled_dot_product_attention(heads(F.linear(a, T["wq"]), H),
+                                       heads(F.linear(a, T["wk"]), Hk),
+                                       heads(F.linear(a, T["wv"]), Hk), is_causal=True,
+                                       enable_gqa=Hk != H)
     h = x + F.linear(o.transpose(0, 1).reshape(S, d), T["wo"])
     b = F.rms_norm(h, (d,), T["g_mlp"], eps=eps)
     y = h + F.linear(F.silu(F.linear(b, T["w1"])) * F.linear(b, T["w3"]), T["w2"])
     return y, h, T
 
 
-def _small(S=64, d=32, H=4, inter=48, D=4, seed=0, dtype=torch.float32):
-    shape = BlockShape(S=S, d=d, H=H, inter=inter, D=D)
+def _small(S=64, d=32, H=4, inter=48, D=4, seed=0, dtype=torch.float32, Hkv=0):
+    shape = BlockShape(S=S, d=d, H=H, inter=inter, D=D, Hkv=Hkv)
     inp = make_block_inputs(shape, dtype, seed=seed, with_dy=True)
     # non-trivial gains so a dropped gain shows up
     gen = torch.Generator().manual_seed(seed + 100)
@@ -549,3 +552,79 @@ def test_rope_sharded_and_tail_equal_unsharded(D):
         assert np.max(np.abs(gs[k] - g[k])) <= 1e-12 * np.max(np.abs(g[k])), k
     tail = O.block_bwd_tail(inp["x"], inp, inp["dy"], shape.H, shape.eps, 5)
     assert np.max(np.abs(tail - g["dx"][-5:])) <= 1e-12 * np.max(np.abs(g["dx"]))
+
+
+# ------------------------------------------------------------------ grouped-query attention (variant)
+
+@pytest.mark.parametrize("Hkv", [1, 2])
+def test_gqa_block_matches_torch_fp64_forward_and_autograd(Hkv):
+    """torch's own grouped-query attention (query head h on K/V head
+    h // (H / Hkv)) pins the head mapping, the forward and every gradient,
+    including dW_K / dW_V, which sum over a group's query heads."""
+    shape, inp = _small(S=40, d=32, H=4, inter=24, D=2, seed=70 + Hkv, Hkv=Hkv)
+    assert inp["wk"].shape == (Hkv * 8, 32)
+    y, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+    yt, _, T = _torch_block(inp, shape.H, shape.eps, requires_grad=True)
+    assert np.max(np.abs(y - yt.detach().numpy())) < 1e-11
+    g = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
+    (yt * T["dy"].detach()).sum().backward()
+    for gname, pname in GRAD_OF.items():
+        ref = T[pname].grad.numpy()
+        assert g[gname].shape == ref.shape, gname
+        err = np.max(np.abs(g[gname] - ref)) / max(np.max(np.abs(ref)), 1e-30)
+        assert err < 1e-11, (gname, err)
+
+
+def test_gqa_equals_mha_with_each_kv_head_repeated_over_its_group():
+    rng = np.random.default_rng(5)
+    S, H, Hkv, dh = 24, 6, 2, 8
+    Q = rng.standard_normal((S, H * dh))
+    K = rng.standard_normal((S, Hkv * dh))
+    V = rng.standard_normal((S, Hkv * dh))
+    grp = H // Hkv
+    rep = lambda M: np.concatenate(  # noqa: E731
+        [M[:, (h // grp) * dh:(h // grp + 1) * dh] for h in range(H)], axis=1)
+    O1, L1 = O.causal_attention(Q, K, V, H)
+    O2, L2 = O.causal_attention(Q, rep(K), rep(V), H)
+    assert np.allclose(O1, O2, atol=1e-14) and np.allclose(L1, L2, atol=1e-14)
+    dO = rng.standard_normal(O1.shape)
+    dq1, dk1, dv1 = O.causal_attention_bwd(Q, K, V, O1, dO, H)
+    dq2, dk2, dv2 = O.causal_attention_bwd(Q, rep(K), rep(V), O2, dO, H)
+    assert np.allclose(dq1, dq2, atol=1e-13)
+    for g in range(Hkv):      # a K/V head's gradient = the sum over its group
+        sl = slice(g * dh, (g + 1) * dh)
+        want_k = sum(dk2[:, h * dh:(h + 1) * dh] for h in range(g * grp, (g + 1) * grp))
+        want_v = sum(dv2[:, h * dh:(h + 1) * dh] for h in range(g * grp, (g + 1) * grp))
+        assert np.allclose(dk1[:, sl], want_k, atol=1e-13)
+        assert np.allclose(dv1[:, sl], want_v, atol=1e-13)
+
+
+@pytest.mark.parametrize("D", [1, 2, 4])
+def test_gqa_with_rope_sharded_rows_and_tail_equal_unsharded(D):
+    shape, inp = _small(S=2 * D * 8, d=32, H=4, inter=24, D=D, seed=80 + D, Hkv=2)
+    inp = {k: v.to(torch.float64) for k, v in inp.items()}
+    inp["rope_base"] = 1000.0
+    y, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+    ys = O.block_fwd_sharded(inp["x"], inp, shape.H, D, shape.eps)
+    assert np.max(np.abs(ys - y)) <= 1e-12 * np.max(np.abs(y))
+    rows = np.array([0, 3, shape.S - 1])
+    yr = O.block_fwd_rows(inp["x"], inp, shape.H, shape.eps, rows)
+    assert np.max(np.abs(yr - y[rows])) <= 1e-12 * np.max(np.abs(y))
+    g = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
+    gs = O.block_bwd_sharded(inp["x"], inp, inp["dy"], shape.H, D, shape.eps)
+    for k in GRAD_OF:
+        assert np.max(np.abs(gs[k] - g[k])) <= 1e-12 * np.max(np.abs(g[k])), k
+    tail = O.block_bwd_tail(inp["x"], inp, inp["dy"], shape.H, shape.eps, 5)
+    assert np.max(np.abs(tail - g["dx"][-5:])) <= 1e-12 * np.max(np.abs(g["dx"]))
+    # finite differences through RoPE on grouped K heads
+    rng = np.random.default_rng(9)
+    step = 1e-6
+    for gname, pname in (("dwk", "wk"), ("dwv", "wv")):
+        base = inp[pname]
+        v = torch.from_numpy(rng.standard_normal(tuple(base.shape)))
+        plus, minus = dict(inp), dict(inp)
+        plus[pname] = base + step * v
+        minus[pname] = base - step * v
+        fd = (_loss(plus, shape.H, shape.eps) - _loss(minus, shape.H, shape.eps)) / (2 * step)
+        an = float(np.sum(g[gname] * v.numpy()))
+        assert abs(fd - an) <= 1e-6 * abs(an), (gname, fd, an)
