@@ -52,22 +52,38 @@ WORKLOADS = {
     # 32-layer stacks of the 7B-shaped block (each layer its own weights)
     "stack32_16k": (16384, 8, 4096, 32, 11008, "fwd"),
     "stack32train_16k": (16384, 8, 4096, 32, 11008, "fwdbwd"),
+    # the 7B-shaped block with grouped-query attention (8 K/V heads, four
+    # query heads per group) and rotary embedding
+    "fwd16k_gqa8": (16384, 8, 4096, 32, 11008, "fwd"),
+    "fwdbwd8k_gqa8": (8192, 8, 4096, 32, 11008, "fwdbwd"),
 }
 LAYERS = {"stack32_16k": 32, "stack32train_16k": 32}   # other workloads: one block
+# block variants of a workload (default: multi-head attention, no positional encoding)
+VARIANTS = {"fwd16k_gqa8": {"Hkv": 8, "rope_base": 500000.0},
+            "fwdbwd8k_gqa8": {"Hkv": 8, "rope_base": 500000.0}}
+
 DEFAULT_WORKLOAD = "fwd16k"
 
 
-def block_flops(S, d, inter, kind):
-    """Algorithmic flops: 8Sd^2 (Q,K,V,O) + 6SdI (SwiGLU) + 2S(S+1)d (causal pairs)."""
+def block_flops(S, d, inter, kind, dkv=None):
+    """Algorithmic flops: 8Sd^2 (Q,K,V,O) + 6SdI (SwiGLU) + 2S(S+1)d (causal pairs);
+    with K/V of width dkv < d the projections take 4Sd^2 + 4Sd*dkv."""
     if kind == "mlp":
         return 6.0 * S * d * inter
-    f = 8.0 * S * d * d + 6.0 * S * d * inter + 2.0 * S * (S + 1) * d
+    dkv = d if dkv is None else dkv
+    f = 4.0 * S * d * d + 4.0 * S * d * dkv + 6.0 * S * d * inter + 2.0 * S * (S + 1) * d
     return 3.0 * f if kind == "fwdbwd" else f
 
 
-def gemm_flops(name, S, d, inter):
+def gemm_flops(name, S, d, inter, dkv=None):
+    dkv = d if dkv is None else dkv
     table = {
-        "gemm_qkv": 2.0 * S * d * 3 * d,
+        "gemm_qkv": 2.0 * S * d * (d + 2 * dkv),
+        # grouped K/V heads: Q and K|V are separate GEMMs
+        "gemm_q": 2.0 * S * d * d,
+        "gemm_kv": 4.0 * S * d * dkv,
+        "gemm_wgrad_q": 2.0 * S * d * d,
+        "gemm_wgrad_kv": 4.0 * S * d * dkv,
         "gemm_oproj": 2.0 * S * d * d,
         "gemm_w13_swiglu": 4.0 * S * d * inter,
         "gemm_w2": 2.0 * S * d * inter,
@@ -80,8 +96,8 @@ def gemm_flops(name, S, d, inter):
         "gemm_dgrad_w13": 4.0 * S * d * inter,
         "gemm_wgrad_wo": 2.0 * S * d * d,
         "gemm_dgrad_wo": 2.0 * S * d * d,
-        "gemm_wgrad_qkv": 6.0 * S * d * d,
-        "gemm_dgrad_qkv": 6.0 * S * d * d,
+        "gemm_wgrad_qkv": 2.0 * S * d * (d + 2 * dkv),
+        "gemm_dgrad_qkv": 2.0 * S * d * (d + 2 * dkv),
         "attn_bwd": 5.0 * S * (S + 1) * d,
     }
     return table.get(name)
@@ -199,7 +215,7 @@ def reduce_max(value: float, world: int, device=None) -> float:
 _SAMPLE_CACHE = {}
 
 
-def oracle_sample(S_full, d, H, inter, D, kind, budget_rows):
+def oracle_sample(S_full, d, H, inter, D, kind, budget_rows, variant=None):
     """Time the float64 oracle on a causal prefix of the workload.
 
     The first `rows` tokens of a causal block only depend on each other, so
@@ -212,13 +228,17 @@ def oracle_sample(S_full, d, H, inter, D, kind, budget_rows):
     import oracle.tsp_oracle as O
     from folded_tensor_sequence_zigzag_gb300.inputs import BlockShape, make_block_inputs
     rows = budget_rows
-    key = (rows, d, H, inter, kind)
+    variant = variant or {}
+    key = (rows, d, H, inter, kind, tuple(sorted(variant.items())))
     if key not in _SAMPLE_CACHE:
-        shape = BlockShape(S=rows, d=d, H=H, inter=inter, D=1)
+        shape = BlockShape(S=rows, d=d, H=H, inter=inter, D=1, Hkv=variant.get("Hkv", 0))
         _SAMPLE_CACHE.clear()
         _SAMPLE_CACHE[key] = make_block_inputs(shape, torch.bfloat16, seed=0,
                                                with_dy=(kind == "fwdbwd"), mlp_only=(kind == "mlp"))
+        if variant.get("rope_base"):
+            _SAMPLE_CACHE[key]["rope_base"] = variant["rope_base"]
     inp = _SAMPLE_CACHE[key]
+    dkv = variant.get("Hkv", H) * (d // H)
     t0 = time.perf_counter()
     if kind == "mlp":
         O.mlp_fwd(inp["x"], inp, 1e-6, norm=False, residual=False)
@@ -227,7 +247,7 @@ def oracle_sample(S_full, d, H, inter, D, kind, budget_rows):
     else:
         O.block_bwd(inp["x"], inp, inp["dy"], H, 1e-6)
     dt = time.perf_counter() - t0
-    scale = block_flops(S_full, d, inter, kind) / block_flops(rows, d, inter, kind)
+    scale = block_flops(S_full, d, inter, kind, dkv) / block_flops(rows, d, inter, kind, dkv)
     desc = (f"oracle (numpy float64) on the first {rows} tokens of the workload "
             f"({kind}), scaled by algorithmic flops x{scale:.1f}")
     return dt * scale, dt, desc
@@ -250,11 +270,11 @@ def run_reference(args):
     L = LAYERS.get(args.workload, 1)
     rows = args.ref_rows or (256 if kind == "fwdbwd" else 512)
     for _ in range(args.warmup):
-        oracle_sample(S, d, H, inter, D, kind, rows)
+        oracle_sample(S, d, H, inter, D, kind, rows, VARIANTS.get(args.workload))
     times = []
     desc = ""
     for _ in range(args.steps):
-        est, _, desc = oracle_sample(S, d, H, inter, D, kind, rows)
+        est, _, desc = oracle_sample(S, d, H, inter, D, kind, rows, VARIANTS.get(args.workload))
         times.append(est * L)
     if L > 1:
         desc += f", x{L} layers"
@@ -284,9 +304,16 @@ def workload_config(name):
     L = LAYERS.get(name, 1)
     if L > 1:
         desc = f"{L}-layer stack of the {desc}"
+    var = VARIANTS.get(name, {})
+    extra = ""
+    if "Hkv" in var:
+        extra += f", grouped-query attention with {var['Hkv']} K/V heads"
+    if var.get("rope_base"):
+        extra += f", rotary embedding base {var['rope_base']:g}"
     return {"workload": f"{desc}, S={S}, D={D} zigzag virtual ranks, d_model={d}, "
-                        f"{H} heads x {d // H}, SwiGLU inter={inter}, causal",
-            "S": S, "D": D, "d_model": d, "heads": H, "inter": inter, "global_batch": 1,
+                        f"{H} heads x {d // H}, SwiGLU inter={inter}, causal{extra}",
+            "S": S, "D": D, "d_model": d, "heads": H, "kv_heads": var.get("Hkv", H),
+            "rope_base": var.get("rope_base", 0.0), "inter": inter, "global_batch": 1,
             "seq_len": S, "parallelism": "replicas (one TSP-emulated block per GPU)",
             "l2": "working set larger than L2 (no flush needed)"}
 
@@ -311,10 +338,13 @@ def run_gpu(args):
     tsp.load()
 
     S, D, d, H, inter, kind = WORKLOADS[args.workload]
-    shape = BlockShape(S=S, d=d, H=H, inter=inter, D=D)
+    var = VARIANTS.get(args.workload, {})
+    shape = BlockShape(S=S, d=d, H=H, inter=inter, D=D, Hkv=var.get("Hkv", 0))
     inp = make_block_inputs(shape, torch.bfloat16, seed=rank, with_dy=(kind == "fwdbwd"),
                             mlp_only=(kind == "mlp"))
-    cfg = tsp.make_cfg(S, d, H, inter, D, torch.bfloat16)
+    cfg = tsp.make_cfg(S, d, H, inter, D, torch.bfloat16, rope_base=var.get("rope_base", 0.0),
+                       Hkv=var.get("Hkv", 0))
+    dkv = shape.dkv
     if kind == "mlp":
         inp.update({k: torch.zeros(1, dtype=torch.bfloat16) for k in ("wq", "wk", "wv", "wo")})
     W = tsp.BlockWeights.from_dict(inp, dev)
@@ -324,7 +354,7 @@ def run_gpu(args):
     for _ in range(1, L):   # further layers drawn on the device, same distributions
         def rnd(*shp):
             return (torch.randn(*shp, generator=gen, device=dev) * 0.02).to(torch.bfloat16)
-        Ws.append(tsp.BlockWeights(rnd(d, d), rnd(d, d), rnd(d, d), rnd(d, d), rnd(inter, d),
+        Ws.append(tsp.BlockWeights(rnd(d, d), rnd(dkv, d), rnd(dkv, d), rnd(d, d), rnd(inter, d),
                                    rnd(inter, d), rnd(d, inter),
                                    torch.ones(d, dtype=torch.bfloat16, device=dev),
                                    torch.ones(d, dtype=torch.bfloat16, device=dev)))
@@ -470,7 +500,7 @@ def run_gpu(args):
     per_kernel = {}
     for ms, name, k in kernel_rows:
         per_launch_ms = ms / max(k, 1)
-        f = gemm_flops(name, S, d, inter)
+        f = gemm_flops(name, S, d, inter, dkv)
         entry = {"launches": k, "ms_per_launch": per_launch_ms}
         if f is not None and kind != "mlp":
             entry["tflops"] = f / (per_launch_ms / 1e3) / 1e12
@@ -491,7 +521,7 @@ def run_gpu(args):
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                 "frac": ach / peak, "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)",
                 "traffic": measured_traffic(dom, args.workload)}
-    flops = block_flops(S, d, inter, kind) * L
+    flops = block_flops(S, d, inter, kind, dkv) * L
     value = world * S / t_dev
     tflops = world * flops / t_dev / 1e12
     line = {
@@ -523,7 +553,7 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline:
         S_, D_, d_, H_, I_, kind_ = WORKLOADS[args.workload]
         rows = args.ref_rows or (512 if kind_ == "fwdbwd" else 8192)   # ~10 s on 16 cores
-        est, dt, desc = oracle_sample(S_, d_, H_, I_, D_, kind_, rows)
+        est, dt, desc = oracle_sample(S_, d_, H_, I_, D_, kind_, rows, var)
         if L > 1:
             est *= L
             desc += f", x{L} layers"

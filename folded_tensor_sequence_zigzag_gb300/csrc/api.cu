@@ -112,6 +112,11 @@ namespace {
 bool al16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// K/V heads, the width of K (and of V), and the row length of the Q|K|V buffer
+int kv_heads(const tsp_cfg* c) { return c->Hkv > 0 ? c->Hkv : c->H; }
+int64_t kv_dim(const tsp_cfg* c) { return (int64_t)kv_heads(c) * c->dh; }
+int64_t qkv_ld(const tsp_cfg* c) { return c->d + 2 * kv_dim(c); }
+
 tsp_status check_cfg(const tsp_cfg* c) {
   if (!c) return TSP_ERR_INVALID_ARG;
   if (c->S <= 0 || c->D < 1 || c->D > 64 || c->S % (2 * (int64_t)c->D) != 0)
@@ -121,6 +126,8 @@ tsp_status check_cfg(const tsp_cfg* c) {
   if (c->dtype != TSP_F32 && c->dtype != TSP_BF16) return TSP_ERR_INVALID_ARG;
   if (!(c->eps >= 0.f)) return TSP_ERR_INVALID_ARG;
   if (!(c->rope_base >= 0.f) || (c->rope_base > 0.f && c->dh % 2 != 0)) return TSP_ERR_INVALID_ARG;
+  if (c->Hkv < 0 || (c->Hkv > 0 && c->H % c->Hkv != 0)) return TSP_ERR_INVALID_ARG;
+  if (kv_dim(c) < c->D) return TSP_ERR_INVALID_ARG;
   if (c->S > (int64_t)1 << 31) return TSP_ERR_UNSUPPORTED;
   if (c->dtype == TSP_F32 && c->dh > 128) return TSP_ERR_UNSUPPORTED;
   return TSP_OK;
@@ -134,6 +141,7 @@ tsp_status check_bf16_mlp(const tsp_cfg* c) {
 tsp_status check_bf16_attn(const tsp_cfg* c) {
   if (c->dtype != TSP_BF16) return TSP_OK;
   if (c->d % 256 != 0 || c->dh != 128 || (c->S / (2 * c->D)) % 256 != 0) return TSP_ERR_UNSUPPORTED;
+  if (kv_dim(c) % 256 != 0) return TSP_ERR_UNSUPPORTED;
   return TSP_OK;
 }
 
@@ -162,7 +170,7 @@ Acts acts_layout(const tsp_cfg* c, int parts, uint8_t* base) {
     A.rstd1 = (float*)take(S * 4);
     A.lse = (float*)take(H * S * 4);
     A.a = take(S * d * e);
-    A.qkv = take(S * 3 * d * e);
+    A.qkv = take(S * (size_t)qkv_ld(c) * e);
     A.o = take(S * d * e);
     if (c->rope_base > 0.f) A.rope = (float2*)take(S * (size_t)(c->dh / 2) * sizeof(float2));
   }
@@ -205,7 +213,7 @@ BwdWs bwd_layout(const tsp_cfg* c, uint8_t* base) {
   W.dh_f32 = take(S * d * 4);
   if (c->dtype == TSP_BF16) W.dh_t = take(S * d * e);
   W.dO = take(S * d * e);
-  W.dqkv = take(S * 3 * d * e);
+  W.dqkv = take(S * (size_t)qkv_ld(c) * e);
   W.da = take(S * d * 4);
   W.delta = (float*)take(2 * H * S * 4);   // Delta [H, S], then (bf16 path) LSE*log2(e) - 8
   if (c->dtype == TSP_BF16) W.dq_acc = (float*)take(S * d * 4);
@@ -236,9 +244,10 @@ WCache wcache_layout(const tsp_cfg* c, int which, uint8_t* base) {
     return p;
   };
   if (which & WC_ATTN) {
+    const size_t dk = (size_t)kv_dim(c);
     W.wq = take(d * d * 2);
-    W.wk = take(d * d * 2);
-    W.wv = take(d * d * 2);
+    W.wk = take(dk * d * 2);
+    W.wv = take(dk * d * 2);
     W.wo = take(d * d * 2);
   }
   if (which & WC_MLP) {
@@ -264,9 +273,10 @@ tsp_status fill_wcache(const tsp_cfg* c, const WCache& W, const tsp_attn_w* aw, 
     ++k;
   };
   if (W.wq) {
+    const int64_t kd = kv_dim(c) * c->d;
     add(aw->wq, W.wq, dd);
-    add(aw->wk, W.wk, dd);
-    add(aw->wv, W.wv, dd);
+    add(aw->wk, W.wk, kd);
+    add(aw->wv, W.wv, kd);
     add(aw->wo, W.wo, dd);
   }
   if (W.w1) {
@@ -279,7 +289,7 @@ tsp_status fill_wcache(const tsp_cfg* c, const WCache& W, const tsp_attn_w* aw, 
 
 cudaStream_t S_(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// Rotary embedding of the Q and K column blocks of a [S, 3d] Q|K|V buffer
+// Rotary embedding of the Q and K column blocks of an [S, d + 2*Hkv*dh] Q|K|V buffer
 // (inverse = 1: the transposed rotation, which maps gradients of the rotated
 // Q, K back to gradients of the projections).  The forward fills the table of
 // (cos, sin) per zigzag row first; the backward reuses the saved one.
@@ -290,7 +300,8 @@ tsp_status rope_qk(const tsp_cfg* c, const Acts& A, void* qkv, int ty, int inver
   if (!inverse &&
       (r = launch_rope_table(A.rope, c->S, c->D, c->dh, c->rope_base, st)) != TSP_OK)
     return r;
-  return launch_rope(qkv, ty, c->S, 3 * c->d, c->d, c->H, c->dh, A.rope, inverse, st);
+  return launch_rope(qkv, ty, c->S, (int)qkv_ld(c), c->d, c->H, kv_heads(c), c->dh, A.rope,
+                     inverse, st);
 }
 
 // ----------------------------------------------------------------------------
@@ -310,16 +321,36 @@ tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, const
   if (c->dtype == TSP_BF16) {
     // Q|K|V: the N range is split into the W_Q, W_K, W_V segments; within a
     // segment the N tiles are the column shards C_k streamed one after another.
-    TcGemm g;
-    g.M = (int)S; g.N = 3 * d; g.K = d;
-    g.A[0] = A.a; g.lda[0] = d; g.kseg_len[0] = d;
-    g.B[0] = WC.wq; g.B[1] = WC.wk; g.B[2] = WC.wv;
-    g.ldb[0] = g.ldb[1] = g.ldb[2] = d;
-    g.nseg_n = d; g.name = "gemm_qkv";
-    g.epi = EPI_STORE; g.out_type = OUT_F16; g.out = A.qkv; g.ldo = 3 * d;
-    if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    const int64_t ld = qkv_ld(c), dk = kv_dim(c);
+    if (dk == d) {
+      TcGemm g;
+      g.M = (int)S; g.N = 3 * d; g.K = d;
+      g.A[0] = A.a; g.lda[0] = d; g.kseg_len[0] = d;
+      g.B[0] = WC.wq; g.B[1] = WC.wk; g.B[2] = WC.wv;
+      g.ldb[0] = g.ldb[1] = g.ldb[2] = d;
+      g.nseg_n = d; g.name = "gemm_qkv";
+      g.epi = EPI_STORE; g.out_type = OUT_F16; g.out = A.qkv; g.ldo = ld;
+      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    } else {
+      // grouped K/V heads: Q (d columns), then K|V (2 x kv_dim columns)
+      TcGemm q;
+      q.M = (int)S; q.N = d; q.K = d;
+      q.A[0] = A.a; q.lda[0] = d; q.kseg_len[0] = d;
+      q.B[0] = WC.wq; q.ldb[0] = d; q.name = "gemm_q";
+      q.epi = EPI_STORE; q.out_type = OUT_F16; q.out = A.qkv; q.ldo = ld;
+      if ((r = gemm_tc(q, st)) != TSP_OK) return r;
+      TcGemm kv;
+      kv.M = (int)S; kv.N = (int)(2 * dk); kv.K = d;
+      kv.A[0] = A.a; kv.lda[0] = d; kv.kseg_len[0] = d;
+      kv.B[0] = WC.wk; kv.B[1] = WC.wv; kv.ldb[0] = kv.ldb[1] = d;
+      kv.nseg_n = (int)dk; kv.name = "gemm_kv";
+      kv.epi = EPI_STORE; kv.out_type = OUT_F16; kv.out = (uint8_t*)A.qkv + (size_t)d * 2;
+      kv.ldo = ld;
+      if ((r = gemm_tc(kv, st)) != TSP_OK) return r;
+    }
     if ((r = rope_qk(c, A, A.qkv, TY_F16, 0, st)) != TSP_OK) return r;
-    if ((r = launch_attn_fwd_f16(A.qkv, A.o, A.lse, S, c->H, c->dh, D, st)) != TSP_OK) return r;
+    if ((r = launch_attn_fwd_f16(A.qkv, A.o, A.lse, S, c->H, kv_heads(c), c->dh, D, st)) != TSP_OK)
+      return r;
     // W_O: split-K over the shards C_k (k = 0..D-1, broadcast order), fp32
     // accumulation in TMEM, residual x added in the epilogue.
     TcGemm o;
@@ -333,17 +364,22 @@ tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, const
   // exact fp32 path: literal shard loop
   const float* a = (const float*)A.a;
   float* qkv = (float*)A.qkv;
+  const int ld = (int)qkv_ld(c), dk = (int)kv_dim(c);
   const float* W3[3] = {(const float*)w->wq, (const float*)w->wk, (const float*)w->wv};
+  const int width[3] = {d, dk, dk}, col0[3] = {0, d, d + dk};
   for (int k = 0; k < D; ++k) {
-    const int lo = (int)((int64_t)k * d / D), hi = (int)((int64_t)(k + 1) * d / D);
     for (int j = 0; j < 3; ++j) {
+      const int n = width[j];
+      const int lo = (int)((int64_t)k * n / D), hi = (int)((int64_t)(k + 1) * n / D);
       r = launch_gemm_f32((int)S, hi - lo, d, a, d, 1, W3[j] + (int64_t)lo * d, d, 1,
-                          qkv + j * d + lo, 3 * d, nullptr, 0, 0, st);
+                          qkv + col0[j] + lo, ld, nullptr, 0, 0, st);
       if (r != TSP_OK) return r;
     }
   }
   if ((r = rope_qk(c, A, qkv, TY_F32, 0, st)) != TSP_OK) return r;
-  if ((r = launch_attn_f32_fwd(qkv, S, c->H, c->dh, D, (float*)A.o, A.lse, st)) != TSP_OK) return r;
+  if ((r = launch_attn_f32_fwd(qkv, S, c->H, kv_heads(c), c->dh, D, (float*)A.o, A.lse, st)) !=
+      TSP_OK)
+    return r;
   for (int k = 0; k < D; ++k) {
     const int lo = (int)((int64_t)k * d / D), hi = (int)((int64_t)(k + 1) * d / D);
     r = launch_gemm_f32((int)S, d, hi - lo, (const float*)A.o + lo, d, 1, (const float*)w->wo + lo,
@@ -602,6 +638,7 @@ tsp_status tsp_pack_attn_shards(const tsp_cfg* cfg, const tsp_attn_w* w, void* d
   tsp_status r = check_cfg(cfg);
   if (r != TSP_OK) return r;
   if (!w || !w->wq || !w->wk || !w->wv || !w->wo || !dst) return TSP_ERR_INVALID_ARG;
+  if (kv_dim(cfg) != cfg->d) return TSP_ERR_UNSUPPORTED;   // the packed layout is for MHA
   return launch_pack_attn_shards(w->wq, w->wk, w->wv, w->wo, dst, cfg->d, cfg->D, cfg->dtype,
                                  S_(stream));
 }
@@ -742,31 +779,48 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
       g.epi = EPI_STORE; g.out_type = OUT_F16; g.out = W.dO; g.ldo = d; g.name = "gemm_dgrad_wo";
       if ((r = gemm_tc(g, st)) != TSP_OK) return r;
     }
-    if ((r = launch_attn_bwd_f16(A.qkv, A.o, W.dO, A.lse, W.delta, W.dq_acc, W.dqkv, S, H, dh, D,
-                                 st)) != TSP_OK)
+    if ((r = launch_attn_bwd_f16(A.qkv, A.o, W.dO, A.lse, W.delta, W.dq_acc, W.dqkv, S, H,
+                                 kv_heads(c), dh, D, st)) != TSP_OK)
       return r;
     // gradients of the rotated Q, K -> gradients of the projections
     if ((r = rope_qk(c, A, W.dqkv, TY_F16, 1, st)) != TSP_OK) return r;
     // dW_Q | dW_K | dW_V = [dQ | dK | dV]^T a
-    {
+    const int64_t ld = qkv_ld(c), dk = kv_dim(c);
+    if (dk == d) {
       TcGemm g;
       g.M = 3 * d; g.N = d; g.K = (int)S;
-      g.a_mn = true; g.A[0] = W.dqkv; g.lda[0] = 3 * (int64_t)d; g.kseg_len[0] = (int)S;
+      g.a_mn = true; g.A[0] = W.dqkv; g.lda[0] = ld; g.kseg_len[0] = (int)S;
       g.b_mn = true; g.B[0] = A.a; g.ldb[0] = d;
       g.epi = EPI_F32; g.ldo = d; g.m_seg = d; g.name = "gemm_wgrad_qkv";
       g.outs[0] = dwq; g.outs[1] = dwk; g.outs[2] = dwv;
       if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    } else {
+      TcGemm q;
+      q.M = d; q.N = d; q.K = (int)S;
+      q.a_mn = true; q.A[0] = W.dqkv; q.lda[0] = ld; q.kseg_len[0] = (int)S;
+      q.b_mn = true; q.B[0] = A.a; q.ldb[0] = d;
+      q.epi = EPI_F32; q.out = dwq; q.ldo = d; q.name = "gemm_wgrad_q";
+      if ((r = gemm_tc(q, st)) != TSP_OK) return r;
+      TcGemm kv;
+      kv.M = (int)(2 * dk); kv.N = d; kv.K = (int)S;
+      kv.a_mn = true; kv.A[0] = (uint8_t*)W.dqkv + (size_t)d * e; kv.lda[0] = ld;
+      kv.kseg_len[0] = (int)S;
+      kv.b_mn = true; kv.B[0] = A.a; kv.ldb[0] = d;
+      kv.epi = EPI_F32; kv.ldo = d; kv.m_seg = dk; kv.name = "gemm_wgrad_kv";
+      kv.outs[0] = dwk; kv.outs[1] = dwv;
+      if ((r = gemm_tc(kv, st)) != TSP_OK) return r;
     }
     // da = dQ W_Q + dK W_K + dV W_V (three K segments), fp32
     {
       TcGemm g;
-      g.M = (int)S; g.N = d; g.K = 3 * d;
+      g.M = (int)S; g.N = d; g.K = (int)ld;
       g.nks = 3;
       const void* ws3[3] = {WC.wq, WC.wk, WC.wv};
+      const int64_t seg[3] = {d, dk, dk}, col[3] = {0, d, d + dk};
       for (int j = 0; j < 3; ++j) {
-        g.A[j] = (uint8_t*)W.dqkv + (size_t)j * d * e;
-        g.lda[j] = 3 * (int64_t)d;
-        g.kseg_len[j] = d;
+        g.A[j] = (uint8_t*)W.dqkv + (size_t)col[j] * e;
+        g.lda[j] = ld;
+        g.kseg_len[j] = (int)seg[j];
         g.B[j] = ws3[j];
         g.ldb[j] = d;
       }
@@ -826,15 +880,17 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
     return r;
   float* dqkv = (float*)W.dqkv;
   if ((r = launch_attn_f32_bwd((const float*)A.qkv, (const float*)A.o, dO, A.lse, W.delta, dqkv, S,
-                               H, dh, D, st)) != TSP_OK)
+                               H, kv_heads(c), dh, D, st)) != TSP_OK)
     return r;
   if ((r = rope_qk(c, A, dqkv, TY_F32, 1, st)) != TSP_OK) return r;
   float* dws[3] = {dwq, dwk, dwv};
   const float* wts[3] = {(const float*)aw->wq, (const float*)aw->wk, (const float*)aw->wv};
+  const int ld = (int)qkv_ld(c), dk = (int)kv_dim(c);
+  const int width[3] = {d, dk, dk}, col0[3] = {0, d, d + dk};
   for (int j = 0; j < 3; ++j) {
     for (int rr = 0; rr < D; ++rr) {
       const int64_t r0 = rr * R;
-      if ((r = launch_gemm_f32(d, d, (int)R, dqkv + r0 * 3 * d + j * d, 1, 3 * d,
+      if ((r = launch_gemm_f32(width[j], d, (int)R, dqkv + r0 * ld + col0[j], 1, ld,
                                (const float*)A.a + r0 * d, 1, d, dws[j], d, nullptr, 0, rr > 0,
                                st)) != TSP_OK)
         return r;
@@ -842,8 +898,8 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
   }
   float* da = (float*)W.da;
   for (int j = 0; j < 3; ++j) {
-    if ((r = launch_gemm_f32((int)S, d, d, dqkv + j * d, 3 * d, 1, wts[j], 1, d, da, d, nullptr, 0,
-                             j > 0, st)) != TSP_OK)
+    if ((r = launch_gemm_f32((int)S, d, width[j], dqkv + col0[j], ld, 1, wts[j], 1, d, da, d,
+                             nullptr, 0, j > 0, st)) != TSP_OK)
       return r;
   }
   return launch_rmsnorm_bwd(da, x, TY_F32, aw->g_attn, A.rstd1, dhf, nullptr, dx, nullptr,

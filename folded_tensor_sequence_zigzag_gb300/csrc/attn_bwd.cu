@@ -85,14 +85,15 @@ constexpr int B_KV = 0, B_QFULL = 1, B_QEMPTY = B_QFULL + QSTAGES, B_DP = B_QEMP
 static_assert(N_BARS * 8 <= 160, "barriers overlap the TMEM slot");
 
 struct TcBwdArgs {
-  CUtensorMap tm_qkv;   // Q|K|V [S, 3d] fp16, box {64, 128}, 128B swizzle
+  CUtensorMap tm_qkv;   // Q|K|V [S, ld = d + 2*dkv] fp16, box {64, 128}, 128B swizzle
   CUtensorMap tm_do;    // dO [S, d] fp16, box {64, 128}, 128B swizzle
   const float* lse2;    // [H, S]: LSE * log2(e) - 8
   const float* delta;   // [H, S]
   float* dq_acc;        // [S, d] fp32, zeroed
-  ct_t* dqkv;           // [S, 3d]: dK, dV written here
-  int64_t S, c;
+  ct_t* dqkv;           // [S, ld]: dK, dV written here
+  int64_t S, c, ld;
   int D, d, n_kt;       // n_kt = c / 128
+  int G, dkv;           // query heads per K/V head; K/V width Hkv*dh
   float scale, scale_log2;
   int* status;
   uint64_t limit_ns;
@@ -145,7 +146,9 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
   }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
+  // one CTA per (K/V head g, key-tile pair); its query iterations run over the
+  // G query heads of the group, head-major, so dK and dV add up in TMEM
+  const int g = blockIdx.y;
   const int pair = blockIdx.x;
   const int r = pair / a.n_kt, t = pair - r * a.n_kt;
   int64_t k0s[2];
@@ -198,7 +201,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
     uint32_t q_issued = 0, kv_issued = 0;
     for (int tile = 0; tile < 2; ++tile) {
       const int64_t k0 = k0s[tile];
-      const int nq = (int)((a.S - k0) / BR);
+      const int nqh = (int)((a.S - k0) / BR);   // query tiles per head
+      const int nq = nqh * a.G;                  // query iterations of this key tile
       const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
       if (warp == WARP_PROD) {
         // ------------------------------------------------------------ producer
@@ -206,16 +210,18 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           mbar_arrive_expect_tx(kv_full, 2 * TILE_BYTES);
 #pragma unroll
           for (int jh = 0; jh < 2; ++jh) {
-            tma_load_2d(base + OFF_K + jh * BOX_BYTES, &a.tm_qkv, a.d + h * DH + 64 * jh, (int)krow0,
+            tma_load_2d(base + OFF_K + jh * BOX_BYTES, &a.tm_qkv, a.d + g * DH + 64 * jh, (int)krow0,
                         kv_full);
-            tma_load_2d(base + OFF_V + jh * BOX_BYTES, &a.tm_qkv, 2 * a.d + h * DH + 64 * jh,
+            tma_load_2d(base + OFF_V + jh * BOX_BYTES, &a.tm_qkv, a.d + a.dkv + g * DH + 64 * jh,
                         (int)krow0, kv_full);
           }
           ++kv_issued;
           for (int j = 0; j < nq; ++j) {
             const uint32_t cur = it + j, st = qst(cur);
             if (!mbar_wait(qd_empty(st), qph(cur) ^ 1u, a.status, abort_flag, a.limit_ns)) break;
-            const int64_t qrow = zz_row_of_pos(k0 + (int64_t)j * BR, a.c, a.D);
+            const int gi = j / nqh, jj = j - gi * nqh;
+            const int h = g * a.G + gi;
+            const int64_t qrow = zz_row_of_pos(k0 + (int64_t)jj * BR, a.c, a.D);
             const uint32_t fb = qd_full(st);
             mbar_arrive_expect_tx(fb, 2 * TILE_BYTES + 2 * BR * 4);
 #pragma unroll
@@ -323,8 +329,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(REG_DRAIN));
     for (int tile = 0; tile < 2; ++tile) {
       const int64_t k0 = k0s[tile];
-      const int nq = (int)((a.S - k0) / BR);
-      const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
+      const int nqh = (int)((a.S - k0) / BR);
+      const int nq = nqh * a.G;
       {
         // ------------------------------------------------------------ dQ drain (thread = dh)
         // all 128 query columns are read before the TMEM columns are released, so
@@ -346,8 +352,9 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(dq_empty);   // dQ^T(cur) read: its columns may take S^T(cur+1)
-          const int64_t qrow = zz_row_of_pos(k0 + (int64_t)j * BR, a.c, a.D);
-          float* dst = a.dq_acc + qrow * a.d + h * DH + dh;
+          const int gi = j / nqh, jj = j - gi * nqh;
+          const int64_t qrow = zz_row_of_pos(k0 + (int64_t)jj * BR, a.c, a.D);
+          float* dst = a.dq_acc + qrow * a.d + (g * a.G + gi) * DH + dh;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -362,7 +369,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
   } else {
     for (int tile = 0; tile < 2; ++tile) {
       const int64_t k0 = k0s[tile];
-      const int nq = (int)((a.S - k0) / BR);
+      const int nqh = (int)((a.S - k0) / BR);
+      const int nq = nqh * a.G;
       const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
       {
         // ------------------------------------------------------------ P, dS (thread = key)
@@ -379,7 +387,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           tc_fence_after();
           const float* L = sLD + st * 2 * BR;
           const float* Dl = L + BR;
-          const bool diag = j == 0;   // query tile == key tile: key index > query index is masked
+          // query tile == key tile (the first of each head): key index > query index is masked
+          const bool diag = j % nqh == 0;
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
             const int qb = half * 64 + ch * 32;    // this chunk's 32 query columns
@@ -430,9 +439,9 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
         bool eok = ok && mbar_wait(kv_done, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
         if (__all_sync(0xffffffffu, eok)) {
           tc_fence_after();
-          ct_t* dkrow = a.dqkv + (krow0 + row) * 3 * (int64_t)a.d + a.d + h * DH;
+          ct_t* dkrow = a.dqkv + (krow0 + row) * a.ld + a.d + g * DH;
           const float mul = half == 0 ? a.scale * kOperandUnscale : kOperandUnscale;
-          ct_t* out = dkrow + half * a.d;     // warps 0-3 write dK, warps 4-7 write dV
+          ct_t* out = dkrow + half * a.dkv;   // warps 0-3 write dK, warps 4-7 write dV
 #pragma unroll 1
           for (int q = 0; q < 4; ++q) {
             uint32_t v[32];
@@ -487,9 +496,9 @@ __global__ void attn_delta_kernel(const ct_t* __restrict__ o, const ct_t* __rest
   }
 }
 
-// dQKV[:, 0:d] = fp16(dq_acc)
+// dQKV[:, 0:d] = fp16(dq_acc); dQKV rows are ld elements apart
 __global__ void dq_convert_kernel(const float* __restrict__ acc, ct_t* __restrict__ dqkv,
-                                  int64_t S, int d) {
+                                  int64_t S, int d, int64_t ld) {
   const int64_t total4 = S * d / 4;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total4;
        t += (int64_t)gridDim.x * blockDim.x) {
@@ -500,7 +509,7 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, ct_t* __restric
     uint2 o;
     o.x = pack_f16(v.x, v.y);
     o.y = pack_f16(v.z, v.w);
-    *reinterpret_cast<uint2*>(dqkv + row * 3 * (int64_t)d + col) = o;
+    *reinterpret_cast<uint2*>(dqkv + row * ld + col) = o;
   }
 }
 
@@ -540,13 +549,15 @@ bool map_2d(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows) {
 }  // namespace
 
 tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, const float* lse,
-                               float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int dh,
-                               int D, cudaStream_t st) {
+                               float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int Hkv,
+                               int dh, int D, cudaStream_t st) {
   if (dh != DH) return TSP_ERR_UNSUPPORTED;
   const int64_t c = S / (2 * D);
   if (c % BC != 0 || S > (int64_t)INT32_MAX) return TSP_ERR_UNSUPPORTED;
   if (S % 4 != 0) return TSP_ERR_UNSUPPORTED;
-  const int d = H * dh;
+  if (Hkv < 1 || H % Hkv != 0) return TSP_ERR_INVALID_ARG;
+  const int d = H * dh, dkv = Hkv * dh;
+  const int64_t ld = d + 2 * (int64_t)dkv;
   if (((uintptr_t)qkv & 15u) || ((uintptr_t)dO & 15u) || ((uintptr_t)lse & 15u) ||
       ((uintptr_t)delta & 15u) || (S * 4) % 16 != 0)
     return TSP_ERR_INVALID_ARG;
@@ -560,7 +571,7 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
   TcBwdArgs* a = new TcBwdArgs();
   std::unique_ptr<TcBwdArgs> guard(a);
   memset(a, 0, sizeof(TcBwdArgs));
-  if (!map_2d(&a->tm_qkv, qkv, 3 * (int64_t)d, S) || !map_2d(&a->tm_do, dO, d, S))
+  if (!map_2d(&a->tm_qkv, qkv, ld, S) || !map_2d(&a->tm_do, dO, d, S))
     return TSP_ERR_CUDA;
   a->lse2 = delta + (int64_t)H * S;
   a->delta = delta;
@@ -570,6 +581,9 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
   a->c = c;
   a->D = D;
   a->d = d;
+  a->ld = ld;
+  a->G = H / Hkv;
+  a->dkv = dkv;
   a->n_kt = (int)(c / BC);
   a->scale = 1.0f / sqrtf((float)dh);
   a->scale_log2 = 1.4426950408889634f * a->scale;
@@ -588,14 +602,14 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
   // setmaxnreg.inc would wait forever if the split exceeded the launch allocation
   if ((int64_t)launch_regs * NTHR < (int64_t)launch_regs * 256 + 128 * (REG_DRAIN + REG_CTRL))
     return TSP_ERR_UNSUPPORTED;
-  dim3 grid((unsigned)(D * a->n_kt), (unsigned)H);
+  dim3 grid((unsigned)(D * a->n_kt), (unsigned)Hkv);
   {
     Prof prof("attn_bwd", st);
     attn_bwd_tc_kernel<<<grid, NTHR, SMEM, st>>>(*a);
     TSP_CUDA_TRY(cudaGetLastError());
   }
   Prof prof("attn_bwd_dq_convert", st);
-  dq_convert_kernel<<<num_sms() * 8, 256, 0, st>>>(dq_acc, (ct_t*)dqkv, S, d);
+  dq_convert_kernel<<<num_sms() * 8, 256, 0, st>>>(dq_acc, (ct_t*)dqkv, S, d, ld);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }

@@ -76,11 +76,12 @@ constexpr uint32_t TMEM_COLS = 512;              // S_A | S_B | O_A | O_B
 constexpr float RESCALE_LOG2 = 8.0f;             // lazy-rescale threshold (log2 units)
 
 struct TcAttnArgs {
-  CUtensorMap tm;       // Q|K|V buffer [S rows, 3d cols] fp16, box {64, 128}, 128B swizzle
+  CUtensorMap tm;       // Q|K|V buffer [S rows, d + 2*Hkv*dh cols] fp16, box {64, 128}, 128B swizzle
   ct_t* o;              // [S, d]
   float* lse;           // [H, S]
   int64_t S, c;
   int D, d, n_blocks;   // n_blocks = c / 256
+  int G, dkv;           // query heads per K/V head; K/V width Hkv*dh
   float scale_log2;
   int* status;
   uint64_t limit_ns;
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
                 break;
               }
               const uint32_t dst = base + OFF_KV + s * TILE_BYTES;
-              const int col = (kv + 1) * a.d + h * DH;
+              const int col = a.d + kv * a.dkv + (h / a.G) * DH;
               mbar_arrive_expect_tx(slot_full(s), TILE_BYTES);
               tma_load_2d(dst, &a.tm, col, krow, slot_full(s));
               tma_load_2d(dst + BOX_BYTES, &a.tm, col + 64, krow, slot_full(s));
@@ -456,21 +457,23 @@ EncodeTiledFn encode_fn_attn() {
 
 }  // namespace
 
-tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, int H, int dh,
-                               int D, cudaStream_t st) {
+tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, int H, int Hkv,
+                               int dh, int D, cudaStream_t st) {
   if (dh != DH) return TSP_ERR_UNSUPPORTED;
   const int64_t c = S / (2 * D);
   if (c % BLOCK != 0) return TSP_ERR_UNSUPPORTED;
   if (S > (int64_t)INT32_MAX) return TSP_ERR_UNSUPPORTED;
-  const int d = H * dh;
-  if (((uintptr_t)qkv & 15u) || ((3 * d * 2) % 16)) return TSP_ERR_INVALID_ARG;
+  if (Hkv < 1 || H % Hkv != 0) return TSP_ERR_INVALID_ARG;
+  const int d = H * dh, dkv = Hkv * dh;
+  const int64_t ld = d + 2 * (int64_t)dkv;
+  if (((uintptr_t)qkv & 15u) || ((ld * 2) % 16)) return TSP_ERR_INVALID_ARG;
   TcAttnArgs* a = new TcAttnArgs();
   std::unique_ptr<TcAttnArgs> guard(a);
   memset(a, 0, sizeof(TcAttnArgs));
   EncodeTiledFn fn = encode_fn_attn();
   if (!fn) return TSP_ERR_CUDA;
-  const cuuint64_t dims[2] = {(cuuint64_t)(3 * d), (cuuint64_t)S};
-  const cuuint64_t strides[1] = {(cuuint64_t)(3 * d * 2)};
+  const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)S};
+  const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
   const cuuint32_t box[2] = {64u, 128u};
   const cuuint32_t estr[2] = {1u, 1u};
   if (fn(&a->tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(qkv), dims, strides, box,
@@ -483,6 +486,8 @@ tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, 
   a->c = c;
   a->D = D;
   a->d = d;
+  a->G = H / Hkv;
+  a->dkv = dkv;
   a->n_blocks = (int)(c / BLOCK);
   a->scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
   a->status = status_word();

@@ -35,7 +35,8 @@ tsp_status launch_convert_f32_bf16(const float* src, void* dst, int64_t n, cudaS
 // pos(row) the global position of zigzag row `row`; then rotate the Q (cols
 // [0, d)) and K (cols [d, 2d)) blocks of a [S, ld] buffer of type ty in place
 tsp_status launch_rope_table(float2* table, int64_t S, int D, int dh, float base, cudaStream_t st);
-tsp_status launch_rope(void* qkv, int ty, int64_t S, int ld, int d, int H, int dh,
+// (Q: H heads at column 0; K: Hkv heads at column d)
+tsp_status launch_rope(void* qkv, int ty, int64_t S, int ld, int d, int H, int Hkv, int dh,
                        const float2* table, int inverse, cudaStream_t st);
 // up to kMaxConvert conversions (n[k] elements each, multiples of 8) in one launch
 constexpr int kMaxConvert = 8;
@@ -51,19 +52,20 @@ tsp_status launch_pack_attn_shards(const void* wq, const void* wk, const void* w
 tsp_status launch_gemm_f32(int M, int N, int K, const float* A, int64_t sam, int64_t sak,
                            const float* B, int64_t sbn, int64_t sbk, float* C, int64_t ldc,
                            const float* R, int64_t ldr, int acc, cudaStream_t st);
-tsp_status launch_attn_f32_fwd(const float* QKV, int64_t S, int H, int dh, int D, float* O,
+// QKV: [S, d + 2*Hkv*dh] (Q | K | V); query head h reads K/V head h / (H / Hkv)
+tsp_status launch_attn_f32_fwd(const float* QKV, int64_t S, int H, int Hkv, int dh, int D, float* O,
                                float* LSE, cudaStream_t st);
 tsp_status launch_attn_f32_bwd(const float* QKV, const float* O, const float* dO, const float* LSE,
-                               float* delta, float* dQKV, int64_t S, int H, int dh, int D,
+                               float* delta, float* dQKV, int64_t S, int H, int Hkv, int dh, int D,
                                cudaStream_t st);
 
 // attn_fwd.cu
-tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, int H, int dh,
+tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, int H, int Hkv, int dh,
                                 int D, cudaStream_t st);
 
 // attn_bwd.cu (delta: 2 x H x S fp32 scratch, Delta then the scaled LSE)
 tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, const float* lse,
-                                float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int dh,
+                                float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int Hkv, int dh,
                                 int D, cudaStream_t st);
 
 }  // namespace tsp

@@ -611,21 +611,21 @@ tsp_status launch_rope_table(float2* table, int64_t S, int D, int dh, float base
   return TSP_OK;
 }
 
-// one thread = one (row, Q or K, head, pair j); consecutive threads take
-// consecutive j of one head, so both halves of a head are read coalesced
+// one thread = one (row, head of Q or K, pair j); consecutive threads take
+// consecutive j of one head, so both halves of a head are read coalesced.
+// Heads 0..H-1 are Q's (column 0), heads H..H+Hkv-1 are K's (column d).
 template <typename T>
-__global__ void rope_kernel(T* __restrict__ qkv, int64_t S, int ld, int d, int H, int half,
-                            const float2* __restrict__ tab, float sgn) {
-  const int64_t per_row = 2LL * H * half;
+__global__ void rope_kernel(T* __restrict__ qkv, int64_t S, int ld, int d, int H, int Hkv,
+                            int half, const float2* __restrict__ tab, float sgn) {
+  const int64_t per_row = (int64_t)(H + Hkv) * half;
   const int64_t total = S * per_row;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t row = t / per_row;
-    int64_t rem = t - row * per_row;
-    const int which = (int)(rem / ((int64_t)H * half));   // 0: Q, 1: K
-    rem -= (int64_t)which * H * half;
-    const int h = (int)(rem / half), j = (int)(rem - (int64_t)h * half);
-    T* p = qkv + row * ld + (int64_t)which * d + (int64_t)h * 2 * half + j;
+    const int rem = (int)(t - row * per_row);
+    const int hh = rem / half, j = rem - hh * half;
+    const int64_t col = hh < H ? (int64_t)hh * 2 * half : d + (int64_t)(hh - H) * 2 * half;
+    T* p = qkv + row * ld + col + j;
     const float2 cs = tab[row * half + j];
     const float s = sgn * cs.y;
     const float x1 = to_f(p[0]), x2 = to_f(p[half]);
@@ -634,18 +634,18 @@ __global__ void rope_kernel(T* __restrict__ qkv, int64_t S, int ld, int d, int H
   }
 }
 
-tsp_status launch_rope(void* qkv, int ty, int64_t S, int ld, int d, int H, int dh,
+tsp_status launch_rope(void* qkv, int ty, int64_t S, int ld, int d, int H, int Hkv, int dh,
                        const float2* table, int inverse, cudaStream_t st) {
   const int half = dh / 2;
   if (!qkv || !table || half < 1) return TSP_ERR_INVALID_ARG;
   Prof prof("rope", st);
-  const int64_t total = S * 2LL * H * half;
+  const int64_t total = S * (int64_t)(H + Hkv) * half;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 8));
   const float sgn = inverse ? -1.f : 1.f;
   if (ty == TY_F16)
-    rope_kernel<__half><<<grid, 256, 0, st>>>((__half*)qkv, S, ld, d, H, half, table, sgn);
+    rope_kernel<__half><<<grid, 256, 0, st>>>((__half*)qkv, S, ld, d, H, Hkv, half, table, sgn);
   else if (ty == TY_F32)
-    rope_kernel<float><<<grid, 256, 0, st>>>((float*)qkv, S, ld, d, H, half, table, sgn);
+    rope_kernel<float><<<grid, 256, 0, st>>>((float*)qkv, S, ld, d, H, Hkv, half, table, sgn);
   else
     return TSP_ERR_UNSUPPORTED;
   TSP_CUDA_TRY(cudaGetLastError());

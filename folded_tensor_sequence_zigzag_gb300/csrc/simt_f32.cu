@@ -88,12 +88,13 @@ constexpr int kMaxDhPerLane = 4;  // dh <= 128
 __global__ void attn_f32_fwd_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                                     const float* __restrict__ V, int64_t ld, float* __restrict__ O,
                                     int64_t ldo, float* __restrict__ LSE, int64_t S, int H, int dh,
-                                    int64_t c, int D, float scale) {
+                                    int64_t c, int D, float scale, int G) {
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= S * H) return;
   const int64_t b = gw / H;
   const int h = (int)(gw - b * H);
+  const int hk = h / G;   // K/V head of query head h
   const int64_t p = zz_pos_of_row(b, c, D);
   float q[kMaxDhPerLane], o[kMaxDhPerLane];
 #pragma unroll
@@ -109,7 +110,7 @@ __global__ void attn_f32_fwd_kernel(const float* __restrict__ Q, const float* __
 #pragma unroll
     for (int j = 0; j < kMaxDhPerLane; ++j) {
       const int col = lane + 32 * j;
-      if (col < dh) s = fmaf(q[j], K[kb * ld + h * dh + col], s);
+      if (col < dh) s = fmaf(q[j], K[kb * ld + hk * dh + col], s);
     }
     s = warp_sum(s) * scale;
     const float mn = fmaxf(m, s);
@@ -119,7 +120,7 @@ __global__ void attn_f32_fwd_kernel(const float* __restrict__ Q, const float* __
 #pragma unroll
     for (int j = 0; j < kMaxDhPerLane; ++j) {
       const int col = lane + 32 * j;
-      if (col < dh) o[j] = o[j] * corr + e * V[kb * ld + h * dh + col];
+      if (col < dh) o[j] = o[j] * corr + e * V[kb * ld + hk * dh + col];
     }
     m = mn;
   }
@@ -152,12 +153,13 @@ __global__ void attn_f32_dq_kernel(const float* __restrict__ Q, const float* __r
                                    const float* __restrict__ dO, int64_t lddo,
                                    const float* __restrict__ LSE, const float* __restrict__ delta,
                                    float* __restrict__ dQ, int64_t lddq, int64_t S, int H, int dh,
-                                   int64_t c, int D, float scale) {
+                                   int64_t c, int D, float scale, int G) {
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= S * H) return;
   const int64_t b = gw / H;
   const int h = (int)(gw - b * H);
+  const int hk = h / G;
   const int64_t p = zz_pos_of_row(b, c, D);
   float q[kMaxDhPerLane], g[kMaxDhPerLane], dq[kMaxDhPerLane];
 #pragma unroll
@@ -175,8 +177,8 @@ __global__ void attn_f32_dq_kernel(const float* __restrict__ Q, const float* __r
     for (int j = 0; j < kMaxDhPerLane; ++j) {
       const int col = lane + 32 * j;
       if (col < dh) {
-        s = fmaf(q[j], K[kb * ld + h * dh + col], s);
-        dp = fmaf(g[j], V[kb * ld + h * dh + col], dp);
+        s = fmaf(q[j], K[kb * ld + hk * dh + col], s);
+        dp = fmaf(g[j], V[kb * ld + hk * dh + col], dp);
       }
     }
     s = warp_sum(s);
@@ -186,7 +188,7 @@ __global__ void attn_f32_dq_kernel(const float* __restrict__ Q, const float* __r
 #pragma unroll
     for (int j = 0; j < kMaxDhPerLane; ++j) {
       const int col = lane + 32 * j;
-      if (col < dh) dq[j] = fmaf(ds, K[kb * ld + h * dh + col], dq[j]);
+      if (col < dh) dq[j] = fmaf(ds, K[kb * ld + hk * dh + col], dq[j]);
     }
   }
 #pragma unroll
@@ -203,42 +205,47 @@ __global__ void attn_f32_dkdv_kernel(const float* __restrict__ Q, const float* _
                                      const float* __restrict__ LSE,
                                      const float* __restrict__ delta, float* __restrict__ dK,
                                      float* __restrict__ dV, int64_t lddkv, int64_t S, int H, int dh,
-                                     int64_t c, int D, float scale) {
+                                     int64_t c, int D, float scale, int G) {
+  // one warp per (key row, K/V head); the G query heads of the group add up
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (gw >= S * H) return;
-  const int64_t kb = gw / H;
-  const int h = (int)(gw - kb * H);
+  const int Hk = H / G;
+  if (gw >= S * Hk) return;
+  const int64_t kb = gw / Hk;
+  const int hk = (int)(gw - kb * Hk);
   const int64_t kpos = zz_pos_of_row(kb, c, D);
   float k[kMaxDhPerLane], v[kMaxDhPerLane], dk[kMaxDhPerLane], dv[kMaxDhPerLane];
 #pragma unroll
   for (int j = 0; j < kMaxDhPerLane; ++j) {
     const int col = lane + 32 * j;
-    k[j] = col < dh ? K[kb * ld + h * dh + col] : 0.f;
-    v[j] = col < dh ? V[kb * ld + h * dh + col] : 0.f;
+    k[j] = col < dh ? K[kb * ld + hk * dh + col] : 0.f;
+    v[j] = col < dh ? V[kb * ld + hk * dh + col] : 0.f;
     dk[j] = dv[j] = 0.f;
   }
-  for (int64_t qp = kpos; qp < S; ++qp) {
-    const int64_t qb = zz_row_of_pos(qp, c, D);
-    float s = 0.f, dp = 0.f;
+  for (int gi = 0; gi < G; ++gi) {
+    const int h = hk * G + gi;
+    for (int64_t qp = kpos; qp < S; ++qp) {
+      const int64_t qb = zz_row_of_pos(qp, c, D);
+      float s = 0.f, dp = 0.f;
 #pragma unroll
-    for (int j = 0; j < kMaxDhPerLane; ++j) {
-      const int col = lane + 32 * j;
-      if (col < dh) {
-        s = fmaf(Q[qb * ld + h * dh + col], k[j], s);
-        dp = fmaf(dO[qb * lddo + h * dh + col], v[j], dp);
+      for (int j = 0; j < kMaxDhPerLane; ++j) {
+        const int col = lane + 32 * j;
+        if (col < dh) {
+          s = fmaf(Q[qb * ld + h * dh + col], k[j], s);
+          dp = fmaf(dO[qb * lddo + h * dh + col], v[j], dp);
+        }
       }
-    }
-    s = warp_sum(s);
-    dp = warp_sum(dp);
-    const float P = expf(s * scale - LSE[(int64_t)h * S + qb]);
-    const float ds = P * (dp - delta[(int64_t)h * S + qb]) * scale;
+      s = warp_sum(s);
+      dp = warp_sum(dp);
+      const float P = expf(s * scale - LSE[(int64_t)h * S + qb]);
+      const float ds = P * (dp - delta[(int64_t)h * S + qb]) * scale;
 #pragma unroll
-    for (int j = 0; j < kMaxDhPerLane; ++j) {
-      const int col = lane + 32 * j;
-      if (col < dh) {
-        dv[j] = fmaf(P, dO[qb * lddo + h * dh + col], dv[j]);
-        dk[j] = fmaf(ds, Q[qb * ld + h * dh + col], dk[j]);
+      for (int j = 0; j < kMaxDhPerLane; ++j) {
+        const int col = lane + 32 * j;
+        if (col < dh) {
+          dv[j] = fmaf(P, dO[qb * lddo + h * dh + col], dv[j]);
+          dk[j] = fmaf(ds, Q[qb * ld + h * dh + col], dk[j]);
+        }
       }
     }
   }
@@ -246,42 +253,44 @@ __global__ void attn_f32_dkdv_kernel(const float* __restrict__ Q, const float* _
   for (int j = 0; j < kMaxDhPerLane; ++j) {
     const int col = lane + 32 * j;
     if (col < dh) {
-      dK[kb * lddkv + h * dh + col] = dk[j];
-      dV[kb * lddkv + h * dh + col] = dv[j];
+      dK[kb * lddkv + hk * dh + col] = dk[j];
+      dV[kb * lddkv + hk * dh + col] = dv[j];
     }
   }
 }
 
 static int warp_grid(int64_t warps) { return (int)((warps * 32 + 255) / 256); }
 
-tsp_status launch_attn_f32_fwd(const float* QKV, int64_t S, int H, int dh, int D, float* O,
+tsp_status launch_attn_f32_fwd(const float* QKV, int64_t S, int H, int Hkv, int dh, int D, float* O,
                                float* LSE, cudaStream_t st) {
-  const int d = H * dh;
+  const int d = H * dh, dk = Hkv * dh;
+  const int64_t ld = d + 2 * (int64_t)dk;
   const int64_t c = S / (2 * D);
   Prof prof("attn_f32_fwd", st);
-  attn_f32_fwd_kernel<<<warp_grid(S * H), 256, 0, st>>>(QKV, QKV + d, QKV + 2 * d, 3 * (int64_t)d,
-                                                         O, d, LSE, S, H, dh, c, D,
-                                                         1.0f / sqrtf((float)dh));
+  attn_f32_fwd_kernel<<<warp_grid(S * H), 256, 0, st>>>(QKV, QKV + d, QKV + d + dk, ld, O, d, LSE,
+                                                         S, H, dh, c, D, 1.0f / sqrtf((float)dh),
+                                                         H / Hkv);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }
 
 tsp_status launch_attn_f32_bwd(const float* QKV, const float* O, const float* dO, const float* LSE,
-                               float* delta, float* dQKV, int64_t S, int H, int dh, int D,
+                               float* delta, float* dQKV, int64_t S, int H, int Hkv, int dh, int D,
                                cudaStream_t st) {
-  const int d = H * dh;
+  const int d = H * dh, dk = Hkv * dh;
+  const int64_t ld = d + 2 * (int64_t)dk;
   const int64_t c = S / (2 * D);
   const float scale = 1.0f / sqrtf((float)dh);
   Prof prof("attn_f32_bwd", st, 3);
   attn_f32_delta_kernel<<<warp_grid(S * H), 256, 0, st>>>(O, dO, d, delta, S, H, dh);
   TSP_CUDA_TRY(cudaGetLastError());
-  attn_f32_dq_kernel<<<warp_grid(S * H), 256, 0, st>>>(QKV, QKV + d, QKV + 2 * d, 3 * (int64_t)d,
-                                                        dO, d, LSE, delta, dQKV, 3 * (int64_t)d, S,
-                                                        H, dh, c, D, scale);
+  attn_f32_dq_kernel<<<warp_grid(S * H), 256, 0, st>>>(QKV, QKV + d, QKV + d + dk, ld, dO, d, LSE,
+                                                        delta, dQKV, ld, S, H, dh, c, D, scale,
+                                                        H / Hkv);
   TSP_CUDA_TRY(cudaGetLastError());
-  attn_f32_dkdv_kernel<<<warp_grid(S * H), 256, 0, st>>>(
-      QKV, QKV + d, QKV + 2 * d, 3 * (int64_t)d, dO, d, LSE, delta, dQKV + d, dQKV + 2 * d,
-      3 * (int64_t)d, S, H, dh, c, D, scale);
+  attn_f32_dkdv_kernel<<<warp_grid(S * Hkv), 256, 0, st>>>(
+      QKV, QKV + d, QKV + d + dk, ld, dO, d, LSE, delta, dQKV + d, dQKV + d + dk, ld, S, H, dh, c,
+      D, scale, H / Hkv);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }

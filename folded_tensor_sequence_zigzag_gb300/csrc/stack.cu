@@ -128,8 +128,10 @@ tsp_status tsp_rank_memory(const tsp_cfg* cfg, int32_t L, int32_t training, int3
   memset(out, 0, sizeof(*out));
   const double D = cfg->D, S = (double)cfg->S, d = cfg->d, I = cfg->inter;
   const double e = (double)elt_of(cfg);
-  // weights of one layer: W_Q, W_K, W_V, W_O, W_1, W_3, W_2 and both gains
-  const double W = ((4.0 * d * d + 3.0 * d * I) + 2.0 * d) * e;
+  // K/V width: Hkv heads of dh (Hkv = H without grouped-query attention)
+  const double dkv = (cfg->Hkv > 0 ? (double)cfg->Hkv : (double)cfg->H) * cfg->dh;
+  // weights of one layer: W_Q, W_O (d x d), W_K, W_V (dkv x d), W_1, W_3, W_2 and both gains
+  const double W = ((2.0 * d * d + 2.0 * d * dkv + 3.0 * d * I) + 2.0 * d) * e;
   // activations one layer keeps per token for its backward: the block's
   // saved buffer plus the layer input (inference: the largest single layer's
   // forward workspace, which is all freed before the next layer)
@@ -149,7 +151,7 @@ tsp_status tsp_rank_memory(const tsp_cfg* cfg, int32_t L, int32_t training, int3
   // the fold's transients (one layer at a time): one broadcast attention
   // shard plus the gathered K/V of the whole sequence, or one MLP ring shard
   if (scheme == TSP_MEM_TSP) {
-    const double attn = 4.0 * d * d / D * e + 2.0 * S * d * e;
+    const double attn = (2.0 * d * d + 2.0 * d * dkv) / D * e + 2.0 * S * dkv * e;
     const double mlp = 3.0 * d * I / D * e;
     out->transient = attn > mlp ? attn : mlp;
   }

@@ -36,7 +36,8 @@ class TspError(RuntimeError):
 class Cfg(ctypes.Structure):
     _fields_ = [("S", ctypes.c_int64), ("d", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("dh", ctypes.c_int32), ("inter", ctypes.c_int32), ("D", ctypes.c_int32),
-                ("eps", ctypes.c_float), ("dtype", ctypes.c_int32), ("rope_base", ctypes.c_float)]
+                ("eps", ctypes.c_float), ("dtype", ctypes.c_int32), ("rope_base", ctypes.c_float),
+                ("Hkv", ctypes.c_int32)]
 
 
 class AttnW(ctypes.Structure):
@@ -155,9 +156,16 @@ class BlockWeights:
                     1 if residual else 0)
 
 
-def make_cfg(S, d, H, inter, D, dtype: torch.dtype, eps=1e-6, rope_base=0.0) -> Cfg:
+def make_cfg(S, d, H, inter, D, dtype: torch.dtype, eps=1e-6, rope_base=0.0, Hkv=0) -> Cfg:
     return Cfg(int(S), int(d), int(H), int(d // H), int(inter), int(D), float(eps),
-               TSP_BF16 if dtype == torch.bfloat16 else TSP_F32, float(rope_base))
+               TSP_BF16 if dtype == torch.bfloat16 else TSP_F32, float(rope_base), int(Hkv))
+
+
+def _grad_shapes(cfg: Cfg) -> dict:
+    d, I = cfg.d, cfg.inter
+    dkv = (cfg.Hkv if cfg.Hkv > 0 else cfg.H) * cfg.dh
+    return {"dwq": (d, d), "dwk": (dkv, d), "dwv": (dkv, d), "dwo": (d, d), "dw1": (I, d),
+            "dw3": (I, d), "dw2": (d, I), "dg_attn": (d,), "dg_mlp": (d,)}
 
 
 def workspace_bytes(cfg: Cfg, op: int) -> int:
@@ -240,9 +248,7 @@ def block_bwd(cfg: Cfg, x_z, dy_z, saved, W: BlockWeights, ws=None, stream=None)
     """Gradients of sum(dy * y), all fp32: dx_z (zigzag order) and the weight/gain grads."""
     _require_cuda(x_z, dy_z, saved)
     dev = x_z.device
-    d, I = cfg.d, cfg.inter
-    shapes = {"dwq": (d, d), "dwk": (d, d), "dwv": (d, d), "dwo": (d, d), "dw1": (I, d),
-              "dw3": (I, d), "dw2": (d, I), "dg_attn": (d,), "dg_mlp": (d,)}
+    shapes = _grad_shapes(cfg)
     g = {k: torch.empty(shapes[k], dtype=torch.float32, device=dev) for k in GRAD_NAMES}
     g["dx"] = torch.empty(x_z.shape, dtype=torch.float32, device=dev)
     ws = _ws(workspace_bytes(cfg, TSP_OP_BLOCK_BWD), dev) if ws is None else ws
@@ -288,9 +294,7 @@ def stack_bwd(cfg: Cfg, dy_z, saved, Ws, ws=None, stream=None):
     _require_cuda(dy_z, saved)
     dev = dy_z.device
     L = len(Ws)
-    d, I = cfg.d, cfg.inter
-    shapes = {"dwq": (d, d), "dwk": (d, d), "dwv": (d, d), "dwo": (d, d), "dw1": (I, d),
-              "dw3": (I, d), "dw2": (d, I), "dg_attn": (d,), "dg_mlp": (d,)}
+    shapes = _grad_shapes(cfg)
     grads = [{k: torch.empty(shapes[k], dtype=torch.float32, device=dev) for k in GRAD_NAMES}
              for _ in range(L)]
     ptrs = (ctypes.c_void_p * (9 * L))(*[g[k].data_ptr() for g in grads for k in GRAD_NAMES])

@@ -92,9 +92,15 @@ typedef struct {
    * frequencies rope_base^(-2j/dh), j < dh/2, at each token's global
    * position (the zigzag layout only moves rows).  Needs an even dh. */
   float rope_base;
+  /* K/V heads (grouped-query attention, a variant; not on the pages):
+   * 0 or H = multi-head attention; otherwise a divisor of H, and the H/Hkv
+   * query heads h = g*(H/Hkv) .. (g+1)*(H/Hkv)-1 share K/V head g.  W_K and
+   * W_V are then [Hkv*dh, d].  The bf16 kernels need Hkv*dh % 256 == 0. */
+  int32_t Hkv;
 } tsp_cfg;
 
-/* Attention-half weights: wq, wk, wv, wo [d, d]; g_attn [d]. */
+/* Attention-half weights: wq, wo [d, d]; wk, wv [Hkv*dh, d] ([d, d] for
+ * multi-head attention); g_attn [d]. */
 typedef struct {
   const void *wq, *wk, *wv, *wo, *g_attn;
 } tsp_attn_w;
@@ -256,7 +262,8 @@ tsp_status tsp_rank_memory(const tsp_cfg* cfg, int32_t L, int32_t training, int3
  * d/D, boundaries floor(k*d/D)) writes [W_Q[C_k,:]; W_K[C_k,:]; W_V[C_k,:];
  * W_O[:,C_k]^T] as a [4*|C_k|, d] block; shards follow each other in dst.
  * Elements of the cfg dtype; dst holds 4*d*d elements.  The forward kernels
- * read the unsharded weights directly and do not need this. */
+ * read the unsharded weights directly and do not need this.  Multi-head
+ * attention only (TSP_ERR_UNSUPPORTED with grouped K/V heads). */
 tsp_status tsp_pack_attn_shards(const tsp_cfg* cfg, const tsp_attn_w* w, void* dst, void* stream);
 
 /* Reads (and with reset != 0 clears) the sticky device status word.  Waits

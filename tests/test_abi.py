@@ -44,15 +44,16 @@ def test_strerror(lib):
 
 
 def _cfg(**kw):
-    base = dict(S=256, d=64, H=4, inter=128, D=4, dtype=tsp.TSP_F32, rope_base=0.0)
+    base = dict(S=256, d=64, H=4, inter=128, D=4, dtype=tsp.TSP_F32, rope_base=0.0, Hkv=0)
     base.update(kw)
     return tsp.Cfg(base["S"], base["d"], base["H"], base.get("dh", base["d"] // base["H"]),
-                   base["inter"], base["D"], 1e-6, base["dtype"], base["rope_base"])
+                   base["inter"], base["D"], 1e-6, base["dtype"], base["rope_base"], base["Hkv"])
 
 
 @pytest.mark.parametrize("bad", [dict(S=250), dict(D=0), dict(D=65), dict(d=66), dict(dh=8),
                                  dict(inter=0), dict(dtype=7), dict(S=0), dict(d=2, H=1, D=4),
-                                 dict(rope_base=-1.0), dict(d=60, H=4, rope_base=10000.0)])
+                                 dict(rope_base=-1.0), dict(d=60, H=4, rope_base=10000.0),
+                                 dict(Hkv=3), dict(Hkv=-1), dict(Hkv=8), dict(H=8, Hkv=1, D=16)])
 def test_invalid_cfg_rejected_without_launch(lib, bad):
     cfg = _cfg(**bad)
     assert lib.tsp_workspace_bytes(ctypes.byref(cfg), tsp.TSP_OP_BLOCK_FWD) == 0
@@ -104,6 +105,10 @@ def test_bf16_shapes_the_kernels_do_not_take_are_unsupported(lib):
     cfg = _cfg(S=512, d=256, H=2, inter=512, D=4, dtype=tsp.TSP_BF16)
     assert lib.tsp_attn_block_fwd(ctypes.byref(cfg), ok, ctypes.byref(aw), ok, ok, 1 << 40,
                                   None) == tsp.TSP_ERR_UNSUPPORTED
+    # grouped K/V of width 128 (the K|V GEMM's N tiles are 256 columns wide)
+    cfg = _cfg(S=2048, d=512, H=4, inter=512, D=4, dtype=tsp.TSP_BF16, Hkv=1)
+    assert lib.tsp_block_fwd(ctypes.byref(cfg), ok, ctypes.byref(aw), ctypes.byref(mw), ok,
+                             None, ok, 1 << 40, None) == tsp.TSP_ERR_UNSUPPORTED
     # the MLP alone takes it
     cfg = _cfg(S=500 * 8, d=256, H=2, inter=384, D=4, dtype=tsp.TSP_BF16)
     assert lib.tsp_workspace_bytes(ctypes.byref(cfg), tsp.TSP_OP_MLP_FWD) > 0

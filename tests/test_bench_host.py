@@ -34,6 +34,24 @@ def test_kernel_flop_table_adds_up():
     assert bench.gemm_flops("attn_bwd", S, d, I) == 2.5 * bench.gemm_flops("attn_fwd", S, d, I)
 
 
+def test_grouped_kv_flops():
+    """8 K/V heads of 128 (dkv = 1024): the K and V projections shrink by
+    d/dkv, attention does not; the kernel table still adds up."""
+    S, d, I, dkv = 8192, 4096, 11008, 1024
+    full = bench.block_flops(S, d, I, "fwd")
+    assert bench.block_flops(S, d, I, "fwd", dkv) == full - 4 * S * d * (d - dkv)
+    fwd = ["gemm_q", "gemm_kv", "gemm_oproj", "gemm_w13_swiglu", "gemm_w2", "attn_fwd"]
+    assert sum(bench.gemm_flops(k, S, d, I, dkv) for k in fwd) == bench.block_flops(S, d, I, "fwd", dkv)
+    assert bench.gemm_flops("gemm_q", S, d, I, dkv) + bench.gemm_flops("gemm_kv", S, d, I, dkv) == \
+        bench.gemm_flops("gemm_qkv", S, d, I, dkv)
+    bwd_gemms = ["gemm_dgrad_w2_swiglu", "gemm_wgrad_w2", "gemm_wgrad_w13", "gemm_dgrad_w13",
+                 "gemm_wgrad_wo", "gemm_dgrad_wo", "gemm_wgrad_q", "gemm_wgrad_kv", "gemm_dgrad_qkv"]
+    proj = sum(bench.gemm_flops(k, S, d, I, dkv) for k in fwd[:5])
+    assert sum(bench.gemm_flops(k, S, d, I, dkv) for k in bwd_gemms) == 2 * proj
+    cfg = bench.workload_config("fwd16k_gqa8")
+    assert cfg["kv_heads"] == 8 and cfg["rope_base"] > 0
+
+
 def test_traffic_figure_tracks_its_source(tmp_path, monkeypatch):
     """A stored ncu traffic figure is reported only while the kernel source
     it was taken on is unchanged."""

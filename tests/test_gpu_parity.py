@@ -30,7 +30,8 @@ def lib():
 def _run_block(shape: BlockShape, inp: dict, dtype, mode="block", norm=True, residual=True,
                rope_base=0.0):
     dev = "cuda"
-    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps, rope_base)
+    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps, rope_base,
+                       shape.Hkv)
     W = tsp.BlockWeights.from_dict(inp, dev)
     x = inp["x"].to(dev)
     xz = tsp.zigzag_permute(x, shape.D)
@@ -208,7 +209,8 @@ def test_7b_block_fwd_sampled_rows(S):
 
 def _run_bwd(shape, inp, dtype, rope_base=0.0):
     dev = "cuda"
-    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps, rope_base)
+    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps, rope_base,
+                       shape.Hkv)
     W = tsp.BlockWeights.from_dict(inp, dev)
     xz = tsp.zigzag_permute(inp["x"].to(dev), shape.D)
     dyz = tsp.zigzag_permute(inp["dy"].to(dev), shape.D)
@@ -345,3 +347,65 @@ def test_7b_rope_block_fwd_sampled_rows():
     rows = sample_rows(S, 8).numpy()
     ref = O.block_fwd_rows(inp["x"], _with_rope(inp, base), shape.H, shape.eps, rows)
     assert_bf16_close(y[rows], ref, "7B rope block S=16384")
+
+
+# ------------------------------------------------------------------ grouped-query attention (variant)
+
+@pytest.mark.parametrize("Hkv,base", [(2, 0.0), (1, 10000.0)])
+def test_tiny_fp32_gqa_forward_backward(Hkv, base):
+    shape = BlockShape(S=256, d=64, H=4, inter=128, D=4, Hkv=Hkv)
+    inp = make_block_inputs(shape, torch.float32, seed=20 + Hkv, with_dy=True)
+    y, g = _run_bwd(shape, inp, torch.float32, rope_base=base)
+    ref_in = _with_rope(inp, base)
+    yref, _ = O.block_fwd(inp["x"], ref_in, shape.H, shape.eps)
+    assert_f32_close(y, yref, f"gqa Hkv={Hkv} fwd")
+    ref = O.block_bwd(inp["x"], ref_in, inp["dy"], shape.H, shape.eps)
+    for k, v in ref.items():
+        assert g[k].shape == v.shape, k
+        scale = max(1.0, float(np.max(np.abs(v))))
+        assert_f32_close(g[k], v, f"gqa Hkv={Hkv} {k}", tol=1e-4 * scale)
+
+
+def test_fp32_gqa_backward_three_ranks_matches_sharded_oracle():
+    shape = BlockShape(S=2 * 3 * 16, d=64, H=4, inter=48, D=3, Hkv=2)
+    inp = make_block_inputs(shape, torch.float32, seed=33, with_dy=True)
+    _, g = _run_bwd(shape, inp, torch.float32)
+    ref = O.block_bwd_sharded(inp["x"], inp, inp["dy"], shape.H, shape.D, shape.eps)
+    for k, v in ref.items():
+        scale = max(1.0, float(np.max(np.abs(v))))
+        assert_f32_close(g[k], v, f"gqa D=3 {k}", tol=1e-4 * scale)
+
+
+@pytest.mark.parametrize("S,d,H,Hkv,D,base", [(2048, 512, 4, 2, 4, 0.0), (4096, 1024, 8, 2, 8, 10000.0),
+                                               (2048, 1024, 8, 8, 2, 0.0)])
+def test_bf16_gqa_forward_backward_small(S, d, H, Hkv, D, base):
+    shape = BlockShape(S=S, d=d, H=H, inter=512, D=D, Hkv=Hkv)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=7, with_dy=True)
+    y, g = _run_bwd(shape, inp, torch.bfloat16, rope_base=base)
+    ref_in = _with_rope(inp, base)
+    yref, _ = O.block_fwd(inp["x"], ref_in, H, shape.eps)
+    assert_bf16_close(y, yref, f"bf16 gqa y (H={H}, Hkv={Hkv})")
+    ref = O.block_bwd(inp["x"], ref_in, inp["dy"], H, shape.eps)
+    for k, v in ref.items():
+        assert g[k].shape == v.shape, k
+        assert_bf16_close(g[k], v, f"bf16 gqa {k} (H={H}, Hkv={Hkv})")
+
+
+def test_7b_gqa8_training_step_S8192_sampled():
+    """7B shapes with 8 K/V heads (four query heads per group), RoPE on:
+    y on 256 seeded rows and dx on the last 256 positions, both exact in the
+    oracle; every gradient finite and of the grouped shapes."""
+    S, D, base = 8192, 8, 500000.0
+    shape = BlockShape(S=S, d=4096, H=32, inter=11008, D=D, Hkv=8)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=3, with_dy=True)
+    y, g = _run_bwd(shape, inp, torch.bfloat16, rope_base=base)
+    ref_in = _with_rope(inp, base)
+    rows = sample_rows(S, D).numpy()
+    assert_bf16_close(y[rows], O.block_fwd_rows(inp["x"], ref_in, shape.H, shape.eps, rows),
+                      "gqa8 y (S=8192, sampled rows)")
+    n_tail = 256
+    dx_ref = O.block_bwd_tail(inp["x"], ref_in, inp["dy"], shape.H, shape.eps, n_tail)
+    assert_bf16_close(g["dx"][S - n_tail:], dx_ref, "gqa8 dx (S=8192, last 256 positions)")
+    assert g["dwk"].shape == (1024, 4096) and g["dwv"].shape == (1024, 4096)
+    for k in ("dwq", "dwk", "dwv", "dwo", "dw1", "dw3", "dw2", "dg_attn", "dg_mlp"):
+        assert torch.isfinite(g[k]).all(), k

@@ -48,6 +48,13 @@ def test_weights_closed_form():
     r32 = tsp.rank_memory(_cfg(S=256, d=64, H=4, I=128, D=4, dtype=torch.float32), 3, True,
                           tsp.TSP_MEM_DP)
     assert r32["weights"] == 3 * (4 * 64 * 64 + 3 * 64 * 128 + 2 * 64) * 4   # fp32
+    # grouped-query attention: W_K, W_V have Hkv*dh = 1024 rows
+    g = tsp.rank_memory(tsp.make_cfg(16384, d, 32, I, 8, torch.bfloat16, Hkv=8), L, True,
+                        tsp.TSP_MEM_DP)
+    assert g["weights"] == L * (2 * d * d + 2 * 1024 * d + 3 * d * I + 2 * d) * 2
+    # ... and its saved activations hold the narrower K|V columns
+    full = tsp.stack_saved_bytes(_cfg(), L)
+    assert tsp.stack_saved_bytes(tsp.make_cfg(16384, d, 32, I, 8, torch.bfloat16, Hkv=8), L) < full
 
 
 def test_training_activations_are_the_stack_record():
