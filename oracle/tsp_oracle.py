@@ -44,6 +44,13 @@ design notes of the repository.
       floor(h / (H / Hkv)), so consecutive query heads form a group.  The K/V
       head count follows from the shapes (W_K, W_V have Hkv*dh rows); Hkv = H
       is plain multi-head attention.
+  R14 Inference (a variant the pages name in their title but do not
+      detail): the prefill is the block forward over the prompt; the KV
+      cache keeps the prompt's K (after R12's rotation, if selected) and V
+      rows in zigzag row order, each virtual rank's 2c rows contiguous;
+      decoded tokens are appended after the prompt in position order (they
+      are not re-zigzagged).  A decode step's output is what the causal
+      block forward over the whole sequence gives at the new positions.
   R11 Stack of L layers: plain composition, each layer its own weights; a
       stack whose activations live in bf16 hands each layer's output (and, in
       the backward, each layer's input gradient) to the next layer rounded to
@@ -419,6 +426,44 @@ def block_fwd_rows(x, W, H, eps, rows, attn_only=False):
     if attn_only:
         return h
     return mlp_fwd(h, W, eps)[0]
+
+
+# ----------------------------------------------------------------------------
+# Inference: KV cache and decode (reading R14)
+# ----------------------------------------------------------------------------
+
+
+def kv_cache_zigzag(x, W, H, eps, D):
+    """Cache rows of a prompt x [S, d]: row i = [K | V] of the token at
+    position zigzag_positions(S, D)[i] ([TSP 2, attention bullet]: every rank
+    keeps the K/V of its own zigzag rows).  Returns [S, 2 * K-width]."""
+    x = f64(x)
+    S = x.shape[0]
+    a, _ = rmsnorm(x, _w(W, "g_attn"), eps)
+    K = rope(a @ _w(W, "wk").T, np.arange(S), _kv_heads(W, H), _rope_base(W))
+    V = a @ _w(W, "wv").T
+    pos = zigzag_positions(S, D)
+    return np.concatenate([K[pos], V[pos]], axis=1)
+
+
+def block_decode(x_prompt, steps, W, H, eps):
+    """Outputs of consecutive decode steps after a prompt.
+
+    ``steps`` is a list of [T_k, d] arrays: step k's tokens follow the prompt
+    and every earlier step's tokens.  Each step's output is the causal block
+    forward over the whole sequence so far, at the step's positions (reading
+    R14), evaluated row-wise with block_fwd_rows.  Returns a list of [T_k, d].
+    """
+    seq = [f64(x_prompt)]
+    n = seq[0].shape[0]
+    outs = []
+    for xs in steps:
+        xs = f64(xs)
+        seq.append(xs)
+        rows = np.arange(n, n + xs.shape[0])
+        outs.append(block_fwd_rows(np.concatenate(seq, axis=0), W, H, eps, rows))
+        n += xs.shape[0]
+    return outs
 
 
 # ----------------------------------------------------------------------------

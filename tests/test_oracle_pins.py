@@ -628,3 +628,57 @@ def test_gqa_with_rope_sharded_rows_and_tail_equal_unsharded(D):
         fd = (_loss(plus, shape.H, shape.eps) - _loss(minus, shape.H, shape.eps)) / (2 * step)
         an = float(np.sum(g[gname] * v.numpy()))
         assert abs(fd - an) <= 1e-6 * abs(an), (gname, fd, an)
+
+
+# ------------------------------------------------------------------ inference: KV cache, decode (variant)
+
+@pytest.mark.parametrize("Hkv,base", [(0, 0.0), (2, 500.0)])
+def test_kv_cache_rows_follow_the_zigzag_layout(Hkv, base):
+    """Cache row i holds K/V of the token the hand-worked zigzag map puts at
+    buffer row i; K and V are torch's own projections (rotated by the closed
+    form for RoPE)."""
+    shape, inp = _small(S=12, d=16, H=4, inter=24, D=3, seed=90, Hkv=Hkv)
+    inp = {k: v.to(torch.float64) for k, v in inp.items()}
+    if base:
+        inp["rope_base"] = base
+    cache = O.kv_cache_zigzag(inp["x"], inp, shape.H, shape.eps, 3)
+    a = F.rms_norm(inp["x"], (16,), inp["g_attn"], eps=shape.eps)
+    K = F.linear(a, inp["wk"]).numpy()
+    V = F.linear(a, inp["wv"]).numpy()
+    if base:
+        dh, half = 4, 2
+        for p in range(12):
+            for h in range(K.shape[1] // dh):
+                for j in range(half):
+                    ang = p * base ** (-2.0 * j / dh)
+                    x1, x2 = K[p, h * dh + j], K[p, h * dh + j + half]
+                    K[p, h * dh + j] = x1 * math.cos(ang) - x2 * math.sin(ang)
+                    K[p, h * dh + j + half] = x1 * math.sin(ang) + x2 * math.cos(ang)
+    # buffer row -> global position, from the hand-worked S=12, D=3 fixture
+    pos_of_row = {int(r[0]): int(r[1]) for r in _load("zigzag_S12_D3.txt")}
+    want = np.concatenate([K, V], axis=1)
+    for row in range(12):
+        assert np.allclose(cache[row], want[pos_of_row[row]], atol=1e-13), row
+
+
+@pytest.mark.parametrize("Hkv,base", [(0, 0.0), (2, 1000.0)])
+def test_decode_steps_match_torch_full_forward(Hkv, base):
+    """Decoding 1, 3 and 2 tokens after a prompt gives the rows of torch's
+    causal block forward over the whole sequence."""
+    S = 16
+    shape, inp = _small(S=S + 6, d=32, H=4, inter=24, D=2, seed=95, Hkv=Hkv)
+    inp = {k: v.to(torch.float64) for k, v in inp.items()}
+    if base:
+        inp["rope_base"] = base
+    x = inp["x"].numpy()
+    outs = O.block_decode(x[:S], [x[S:S + 1], x[S + 1:S + 4], x[S + 4:S + 6]], inp, shape.H,
+                          shape.eps)
+    if base:   # torch has no rotary block here: compare with the oracle's own full forward,
+        # itself pinned against torch with RoPE off and by the RoPE pins above
+        y, _ = O.block_fwd(x, inp, shape.H, shape.eps)
+    else:
+        y = _torch_block({k: v for k, v in inp.items() if k != "rope_base"}, shape.H,
+                         shape.eps)[0].detach().numpy()
+    got = np.concatenate(outs, axis=0)
+    assert got.shape == (6, 32)
+    assert np.max(np.abs(got - y[S:])) < 1e-11
