@@ -56,11 +56,32 @@ WORKLOADS = {
     # query heads per group) and rotary embedding
     "fwd16k_gqa8": (16384, 8, 4096, 32, 11008, "fwd"),
     "fwdbwd8k_gqa8": (8192, 8, 4096, 32, 11008, "fwdbwd"),
+    # inference: one new token per step after a 16384-token prompt held in the
+    # zigzag KV cache (the prefill runs once, untimed)
+    "decode16k": (16384, 8, 4096, 32, 11008, "decode"),
+    "decode16k_gqa8": (16384, 8, 4096, 32, 11008, "decode"),
 }
+DECODE_T = 1        # new tokens per decode call
+DECODE_GEN = 256    # decode calls per step: a step generates 256 tokens after the prompt
 LAYERS = {"stack32_16k": 32, "stack32train_16k": 32}   # other workloads: one block
 # block variants of a workload (default: multi-head attention, no positional encoding)
 VARIANTS = {"fwd16k_gqa8": {"Hkv": 8, "rope_base": 500000.0},
-            "fwdbwd8k_gqa8": {"Hkv": 8, "rope_base": 500000.0}}
+            "fwdbwd8k_gqa8": {"Hkv": 8, "rope_base": 500000.0},
+            "decode16k_gqa8": {"Hkv": 8, "rope_base": 500000.0}}
+
+
+def decode_bytes(name, d, inter, dkv, n_rows, T=DECODE_T):
+    """Algorithmic HBM bytes of one decode-step kernel: every bf16 weight
+    once, the fp16 K/V of every cached row once (the activations of T tokens
+    are negligible and left out)."""
+    table = {
+        "gemv_qkv": 2.0 * d * (d + 2 * dkv),
+        "gemv_oproj": 2.0 * d * d,
+        "gemv_w13_swiglu": 4.0 * d * inter,
+        "gemv_w2": 2.0 * d * inter,
+        "decode_attn": 2.0 * 2 * dkv * n_rows,
+    }
+    return table.get(name)
 
 DEFAULT_WORKLOAD = "fwd16k"
 
@@ -268,6 +289,8 @@ def run_reference(args):
             return
     S, D, d, H, inter, kind = WORKLOADS[args.workload]
     L = LAYERS.get(args.workload, 1)
+    if kind == "decode":
+        return run_reference_decode(args, rank, world)
     rows = args.ref_rows or (256 if kind == "fwdbwd" else 512)
     for _ in range(args.warmup):
         oracle_sample(S, d, H, inter, D, kind, rows, VARIANTS.get(args.workload))
@@ -297,10 +320,68 @@ def run_reference(args):
         dist.destroy_process_group()
 
 
+def oracle_decode_sample(S_full, d, H, inter, variant, prompt_rows):
+    """Time the oracle's decode of one token after a `prompt_rows` prompt.
+    The oracle keeps no cache (it recomputes the prefix's K/V), so its cost
+    grows with the prompt; the time is scaled to the workload's prompt by
+    the row ratio.  Returns (seconds estimate, seconds measured, description)."""
+    import torch
+    import oracle.tsp_oracle as O
+    from folded_tensor_sequence_zigzag_gb300.inputs import BlockShape, make_block_inputs
+    variant = variant or {}
+    key = ("decode", prompt_rows, d, H, inter, tuple(sorted(variant.items())))
+    if key not in _SAMPLE_CACHE:
+        shape = BlockShape(S=prompt_rows + 1, d=d, H=H, inter=inter, D=1, Hkv=variant.get("Hkv", 0))
+        _SAMPLE_CACHE.clear()
+        _SAMPLE_CACHE[key] = make_block_inputs(shape, torch.bfloat16, seed=0)
+        if variant.get("rope_base"):
+            _SAMPLE_CACHE[key]["rope_base"] = variant["rope_base"]
+    inp = _SAMPLE_CACHE[key]
+    x = inp["x"]
+    t0 = time.perf_counter()
+    O.block_decode(x[:prompt_rows], [x[prompt_rows:prompt_rows + 1]], inp, H, 1e-6)
+    dt = time.perf_counter() - t0
+    scale = (S_full + 1) / (prompt_rows + 1)
+    desc = (f"oracle (numpy float64) decoding one token after a {prompt_rows}-token prompt "
+            f"(it recomputes the prefix K/V), scaled to the {S_full}-token prompt by x{scale:.1f}")
+    return dt * scale, dt, desc
+
+
+def run_reference_decode(args, rank, world):
+    S, D, d, H, inter, kind = WORKLOADS[args.workload]
+    rows = args.ref_rows or 1024
+    var = VARIANTS.get(args.workload)
+    for _ in range(args.warmup):
+        oracle_decode_sample(S, d, H, inter, var, rows)
+    times, desc = [], ""
+    for _ in range(args.steps):
+        est, _, desc = oracle_decode_sample(S, d, H, inter, var, rows)
+        times.append(est)
+    t = statistics.median(times) * DECODE_GEN / DECODE_T     # one step: DECODE_GEN tokens
+    value = DECODE_GEN / t
+    line = {
+        "impl": "reference", "metric": "decode tokens/s", "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args.workload),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def workload_config(name):
     S, D, d, H, inter, kind = WORKLOADS[name]
     desc = {"fwd": "7B-shaped TSP block forward", "fwdbwd": "7B-shaped TSP block forward+backward",
-            "mlp": "sharded SwiGLU MLP only (no norm, no residual)"}[kind]
+            "mlp": "sharded SwiGLU MLP only (no norm, no residual)",
+            "decode": f"7B-shaped TSP block decode, {DECODE_GEN} tokens generated one at a time "
+                      f"after the prompt, against its zigzag KV cache"}[kind]
     L = LAYERS.get(name, 1)
     if L > 1:
         desc = f"{L}-layer stack of the {desc}"
@@ -338,6 +419,8 @@ def run_gpu(args):
     tsp.load()
 
     S, D, d, H, inter, kind = WORKLOADS[args.workload]
+    if kind == "decode":
+        return run_gpu_decode(args, rank, world, local, dev)
     var = VARIANTS.get(args.workload, {})
     shape = BlockShape(S=S, d=d, H=H, inter=inter, D=D, Hkv=var.get("Hkv", 0))
     inp = make_block_inputs(shape, torch.bfloat16, seed=rank, with_dy=(kind == "fwdbwd"),
@@ -558,6 +641,171 @@ def run_gpu(args):
             est *= L
             desc += f", x{L} layers"
         line["cpu_baseline"] = {"value": S_ / est, "unit": "tokens/s", "cores": cpu_cores(),
+                                "kind": "oracle", "sample": desc, "sample_seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_gpu_decode(args, rank, world, local, dev):
+    """A step generates DECODE_GEN tokens after a prefilled prompt, one
+    tsp_block_decode call of DECODE_T tokens at a time (positions S, S+1, ...).
+    The prompt runs once through tsp_block_prefill, untimed; every step starts
+    again from the prompt (the cache's decoded rows are overwritten), so all
+    steps do the same work."""
+    import torch
+    import torch.distributed as dist
+    from folded_tensor_sequence_zigzag_gb300 import tsp
+    from folded_tensor_sequence_zigzag_gb300.inputs import BlockShape, make_block_inputs
+
+    S, D, d, H, inter, kind = WORKLOADS[args.workload]
+    var = VARIANTS.get(args.workload, {})
+    T, n_gen = DECODE_T, DECODE_GEN
+    calls = n_gen // T
+    shape = BlockShape(S=S + n_gen, d=d, H=H, inter=inter, D=D, Hkv=var.get("Hkv", 0))
+    inp = make_block_inputs(shape, torch.bfloat16, seed=rank)
+    cfg = tsp.make_cfg(S, d, H, inter, D, torch.bfloat16, rope_base=var.get("rope_base", 0.0),
+                       Hkv=var.get("Hkv", 0))
+    dkv = shape.dkv
+    W = tsp.BlockWeights.from_dict(inp, dev)
+    cache = tsp.KVCache(cfg, S + n_gen, dev)
+    stream = torch.cuda.current_stream(dev)
+    xs_host = inp["x"][S:].contiguous()          # the generated tokens' inputs, position order
+    xs = xs_host.to(dev)
+    ys = torch.empty_like(xs)
+    ws = torch.empty(tsp.decode_workspace_bytes(cfg, T, cache.rows_cap), dtype=torch.uint8,
+                     device=dev)
+    ws_pre = torch.empty(tsp.workspace_bytes(cfg, tsp.TSP_OP_BLOCK_FWD), dtype=torch.uint8,
+                         device=dev)
+    xz = tsp.zigzag_permute(inp["x"][:S].to(dev), D)
+    tsp.block_prefill(cfg, xz, W, cache, ws=ws_pre)
+    del ws_pre, xz
+    xv = [xs[i * T:(i + 1) * T] for i in range(calls)]
+    yv = [ys[i * T:(i + 1) * T] for i in range(calls)]
+
+    def step(x_in=None, y_out=None):
+        xin = xv if x_in is None else [x_in[i * T:(i + 1) * T] for i in range(calls)]
+        yout = yv if y_out is None else [y_out[i * T:(i + 1) * T] for i in range(calls)]
+        cache.n = S
+        for i in range(calls):
+            tsp.block_decode(cfg, xin[i], W, cache, out=yout[i], ws=ws)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    if tsp.device_status() != tsp.TSP_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    # A step's DECODE_GEN calls always run at the same positions, so the step
+    # is captured once as a CUDA graph and replayed: the timed region has no
+    # host launch overhead between the ~2000 small kernels of a step.
+    graph = torch.cuda.CUDAGraph()
+    n_cap = tsp.launch_count()
+    with torch.cuda.graph(graph):
+        step()
+    graph_kernels = tsp.launch_count() - n_cap
+    torch.cuda.synchronize(dev)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    launches = graph_kernels * args.steps
+    t_dev = reduce_max(ev0.elapsed_time(ev1) / 1e3 / args.steps, world, dev if world > 1 else None)
+    n_rows_mid = S + (n_gen + 1) / 2           # cached rows an attention call reads, on average
+
+    # per-kernel durations: the same steps once more, eagerly, with CUDA events
+    # around every kernel on the launch stream (events cannot sit inside the
+    # replayed graph), and the eager step time beside them
+    tsp.profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    prof = tsp.profile_report()
+    tsp.profile_enable(False)
+    t_eager = e0.elapsed_time(e1) / 1e3 / args.steps
+
+    # end to end through the public API: every step uploads its tokens' inputs
+    # from pinned host memory into the buffer the graph reads, replays the
+    # step, and reads the outputs back
+    x_host = xs_host.pin_memory()
+    y_host = torch.empty(ys.shape, dtype=ys.dtype).pin_memory()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        xs.copy_(x_host, non_blocking=True)
+        graph.replay()
+        y_host.copy_(ys, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_e2e = reduce_max(e0.elapsed_time(e1) / 1e3 / args.steps, world, dev if world > 1 else None)
+    if tsp.device_status() != tsp.TSP_OK:
+        raise RuntimeError("device status not OK after the timed region")
+
+    peaks, peak_src = measured_peaks()
+    hbm = peaks.get("hbm_gbs")
+    per_kernel = {}
+    for name, (k, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
+        per_launch_ms = ms / max(k, 1)
+        entry = {"launches": k, "ms_per_launch": per_launch_ms}
+        b = decode_bytes(name, d, inter, dkv, n_rows_mid)
+        if b is not None:
+            entry["gbs"] = b / (per_launch_ms / 1e3) / 1e9
+        per_kernel[name] = entry
+    dom = next((n for n in per_kernel if "gbs" in per_kernel[n]), None)
+    roof = None
+    if dom is not None:
+        ach = per_kernel[dom]["gbs"]
+        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS.json)",
+                "traffic": measured_traffic(dom, args.workload)}
+    call_bytes = sum(decode_bytes(n, d, inter, dkv, n_rows_mid) for n in
+                     ("gemv_qkv", "gemv_oproj", "gemv_w13_swiglu", "gemv_w2", "decode_attn"))
+    line = {
+        "metric": "decode tokens/s", "value": world * n_gen / t_dev, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_dev * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (x~N(0,1), weights~N(0,0.02), gains 1)",
+        "config": dict(workload_config(args.workload), tokens_per_call=T, tokens_per_step=n_gen,
+                       l2="working set (weights + KV cache) larger than L2 (no flush needed)"),
+        "hbm_bytes_per_token": call_bytes / T,
+        "hbm_gbs_per_step": call_bytes * calls / t_dev / 1e9,
+        "frac_of_hbm_peak": call_bytes * calls / t_dev / 1e9 / hbm,
+        "e2e": {"value": world * n_gen / t_e2e, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 2),
+                "d2h_bytes_per_step": int(y_host.numel() * 2)},
+        "gpu_launches": int(launches),
+        "launches_per_step": launches / args.steps,
+        "timed_as": "CUDA graph of one step, replayed; kernels and eager_ms_per_step from an "
+                    "eager pass of the same steps with per-kernel CUDA events",
+        "eager_ms_per_step": t_eager * 1e3,
+        "kernels": per_kernel,
+        "roofline": roof,
+        "clocks": clk,
+        "memory": {"device_peak_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
+                   "kv_cache_gb": tsp.kv_cache_bytes(cfg, cache.rows_cap) / 1e9},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        rows = args.ref_rows or 1024
+        est, dt, desc = oracle_decode_sample(S, d, H, inter, var, rows)
+        line["cpu_baseline"] = {"value": T / est, "unit": "tokens/s", "cores": cpu_cores(),
                                 "kind": "oracle", "sample": desc, "sample_seconds": dt}
     if rank == 0:
         print(json.dumps(line), flush=True)

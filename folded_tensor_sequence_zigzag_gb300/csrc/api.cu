@@ -478,6 +478,101 @@ tsp_status check_mlp_w(const tsp_mlp_w* w, bool need_norm) {
   return TSP_OK;
 }
 
+// ----------------------------------------------------------------------------
+// Decode workspace: the T new tokens' activations and the attention splits'
+// partial results (sized for a cache of `cap` rows).
+// ----------------------------------------------------------------------------
+struct DecWs {
+  void *a, *qkv, *o, *g;   // a: the normalised rows (both norms in turn)
+  float *h, *rstd, *part_o;
+  float2* part_ml;
+  size_t bytes;
+};
+
+DecWs decode_layout(const tsp_cfg* c, int T, int64_t cap, uint8_t* base) {
+  const size_t e = c->dtype == TSP_BF16 ? 2 : 4;   // fp16 / fp32 internal element
+  const size_t d = (size_t)c->d, I = (size_t)c->inter, H = (size_t)c->H, dh = (size_t)c->dh;
+  DecWs W;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void* {
+    void* p = base ? base + off : nullptr;
+    off += up256(bytes);
+    return p;
+  };
+  W.a = take(T * d * e);
+  W.rstd = (float*)take(T * 4);
+  W.qkv = take(T * (size_t)qkv_ld(c) * e);
+  W.o = take(T * d * e);
+  W.g = take(T * I * e);
+  W.h = (float*)take(T * d * 4);
+  const size_t nsplit = (size_t)decode_splits(c->S, c->D, cap);
+  W.part_o = (float*)take(nsplit * H * T * dh * 4);
+  W.part_ml = (float2*)take(nsplit * H * T * sizeof(float2));
+  W.bytes = off;
+  return W;
+}
+
+tsp_status decode_impl(const tsp_cfg* c, const void* x, int T, int64_t n_cached,
+                       const tsp_attn_w* aw, const tsp_mlp_w* mw, void* y, void* kv,
+                       const DecWs& W, cudaStream_t st) {
+  const bool bf = c->dtype == TSP_BF16;
+  const int io_ty = bf ? TY_BF16 : TY_F32, ct = bf ? TY_F16 : TY_F32;
+  const int d = c->d, I = c->inter, dk = (int)kv_dim(c);
+  const int64_t ld = qkv_ld(c);
+  tsp_status r;
+  // a = rms(x; g_attn)
+  if ((r = launch_rmsnorm_fwd(x, io_ty, aw->g_attn, W.a, ct, W.rstd, T, d, c->eps, c->dtype,
+                              st)) != TSP_OK)
+    return r;
+  // q | k | v = a [W_Q; W_K; W_V]^T, Q and K rotated at their positions,
+  // K | V also appended to the cache rows n_cached ..
+  {
+    Gemv g;
+    g.epi = GEMV_QKV; g.dtype = c->dtype; g.x = W.a; g.ldx = d;
+    g.w[0] = aw->wq; g.w[1] = aw->wk; g.w[2] = aw->wv;
+    g.rows[0] = d; g.rows[1] = dk; g.rows[2] = dk; g.nseg = 3;
+    g.K = d; g.T = T; g.out = W.qkv; g.ldo = ld; g.out_ty = ct;
+    g.dh = c->dh; g.qk_heads = c->H + kv_heads(c); g.d = d; g.rope_base = c->rope_base;
+    g.pos0 = n_cached; g.kv = kv; g.ldkv = 2 * dk; g.name = "gemv_qkv";
+    if ((r = launch_gemv(g, st)) != TSP_OK) return r;
+  }
+  {
+    DecodeAttn a;
+    a.dtype = c->dtype; a.q = W.qkv; a.ldq = ld; a.kv = kv; a.o = W.o;
+    a.part_o = W.part_o; a.part_ml = W.part_ml;
+    a.S = c->S; a.n_cached = n_cached; a.D = c->D; a.T = T;
+    a.H = c->H; a.Hkv = kv_heads(c); a.dh = c->dh;
+    if ((r = launch_decode_attn(a, st)) != TSP_OK) return r;
+  }
+  // h = x + O W_O^T (fp32)
+  {
+    Gemv g;
+    g.epi = GEMV_RES; g.dtype = c->dtype; g.x = W.o; g.ldx = d;
+    g.w[0] = aw->wo; g.rows[0] = d; g.nseg = 1; g.K = d; g.T = T;
+    g.out = W.h; g.ldo = d; g.out_ty = TY_F32; g.res = x; g.ldr = d; g.res_ty = io_ty;
+    g.name = "gemv_oproj";
+    if ((r = launch_gemv(g, st)) != TSP_OK) return r;
+  }
+  // G = silu(b W_1^T) * (b W_3^T), b = rms(h; g_mlp)
+  if ((r = launch_rmsnorm_fwd(W.h, TY_F32, mw->g_mlp, W.a, ct, W.rstd, T, d, c->eps, c->dtype,
+                              st)) != TSP_OK)
+    return r;
+  {
+    Gemv g;
+    g.epi = GEMV_SWIGLU; g.dtype = c->dtype; g.x = W.a; g.ldx = d;
+    g.w[0] = mw->w1; g.w[1] = mw->w3; g.rows[0] = g.rows[1] = I; g.nseg = 2;
+    g.K = d; g.T = T; g.out = W.g; g.ldo = I; g.out_ty = ct; g.name = "gemv_w13_swiglu";
+    if ((r = launch_gemv(g, st)) != TSP_OK) return r;
+  }
+  // y = h + G W_2^T
+  Gemv g;
+  g.epi = GEMV_RES; g.dtype = c->dtype; g.x = W.g; g.ldx = I;
+  g.w[0] = mw->w2; g.rows[0] = d; g.nseg = 1; g.K = I; g.T = T;
+  g.out = y; g.ldo = d; g.out_ty = io_ty; g.res = W.h; g.ldr = d; g.res_ty = TY_F32;
+  g.name = "gemv_w2";
+  return launch_gemv(g, st);
+}
+
 }  // namespace
 
 // ----------------------------------------------------------------------------
@@ -632,6 +727,51 @@ tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z, 
   if (!al16(ws) || ws_bytes < tsp_workspace_bytes(cfg, TSP_OP_BLOCK_BWD)) return TSP_ERR_INVALID_ARG;
   return block_bwd_impl(cfg, x_z, dy_z, saved, aw, mw, dx_z, dwq, dwk, dwv, dwo, dw1, dw3, dw2,
                         dg_attn, dg_mlp, ws, S_(stream));
+}
+
+size_t tsp_kv_cache_bytes(const tsp_cfg* cfg, int64_t kv_rows_cap) {
+  if (check_cfg(cfg) != TSP_OK || kv_rows_cap < cfg->S) return 0;
+  const size_t e = cfg->dtype == TSP_BF16 ? 2 : 4;
+  return (size_t)kv_rows_cap * 2 * (size_t)kv_dim(cfg) * e;
+}
+
+size_t tsp_decode_workspace_bytes(const tsp_cfg* cfg, int32_t T, int64_t kv_rows_cap) {
+  if (check_cfg(cfg) != TSP_OK || T < 1 || T > TSP_DECODE_MAX_T || kv_rows_cap < cfg->S + T)
+    return 0;
+  return decode_layout(cfg, T, kv_rows_cap, nullptr).bytes;
+}
+
+tsp_status tsp_block_prefill(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* aw,
+                             const tsp_mlp_w* mw, void* y_z, void* kv, int64_t kv_rows_cap,
+                             void* ws, size_t ws_bytes, void* stream) {
+  tsp_status r = check_cfg(cfg);
+  if (r != TSP_OK) return r;
+  if (!al16(kv) || kv_rows_cap < cfg->S) return TSP_ERR_INVALID_ARG;
+  if ((r = tsp_block_fwd(cfg, x_z, aw, mw, y_z, nullptr, ws, ws_bytes, stream)) != TSP_OK) return r;
+  // the prompt's K (rotated) and V, still in the forward's Q|K|V buffer
+  const Acts A = acts_layout(cfg, fwd_parts(cfg, false), (uint8_t*)ws);
+  const size_t e = cfg->dtype == TSP_BF16 ? 2 : 4;
+  const size_t dk = (size_t)kv_dim(cfg);
+  TSP_CUDA_TRY(cudaMemcpy2DAsync(kv, 2 * dk * e, (const uint8_t*)A.qkv + (size_t)cfg->d * e,
+                                 (size_t)qkv_ld(cfg) * e, 2 * dk * e, (size_t)cfg->S,
+                                 cudaMemcpyDeviceToDevice, S_(stream)));
+  return TSP_OK;
+}
+
+tsp_status tsp_block_decode(const tsp_cfg* cfg, const void* x, int32_t T, int64_t n_cached,
+                            const tsp_attn_w* aw, const tsp_mlp_w* mw, void* y, void* kv,
+                            int64_t kv_rows_cap, void* ws, size_t ws_bytes, void* stream) {
+  tsp_status r = check_cfg(cfg);
+  if (r != TSP_OK) return r;
+  if ((r = check_attn_w(aw)) != TSP_OK) return r;
+  if ((r = check_mlp_w(mw, true)) != TSP_OK) return r;
+  if (T < 1 || T > TSP_DECODE_MAX_T) return TSP_ERR_INVALID_ARG;
+  if (n_cached < cfg->S || n_cached + T > kv_rows_cap) return TSP_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(y) || !al16(kv)) return TSP_ERR_INVALID_ARG;
+  if (!al16(ws) || ws_bytes < tsp_decode_workspace_bytes(cfg, T, kv_rows_cap))
+    return TSP_ERR_INVALID_ARG;
+  const DecWs W = decode_layout(cfg, T, kv_rows_cap, (uint8_t*)ws);
+  return decode_impl(cfg, x, T, n_cached, aw, mw, y, kv, W, S_(stream));
 }
 
 tsp_status tsp_pack_attn_shards(const tsp_cfg* cfg, const tsp_attn_w* w, void* dst, void* stream) {

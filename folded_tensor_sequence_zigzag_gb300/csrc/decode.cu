@@ -1,0 +1,732 @@
+// decode.cu -- inference decode of the TSP-folded block against the zigzag KV cache.
+//
+// "Folding Tensor and Sequence Parallelism for Memory-Efficient Transformer
+// Training & Inference", section 2 ("Runtime schedules", attention bullet):
+// every rank keeps the K/V of its own zigzag rows.  A decode step of T new
+// tokens is HBM-bound: it streams every weight once (a few hundred MB for the
+// 7B-shaped block) and the cached K/V of the whole sequence, against only
+// 2*T flops per weight.  So its kernels are plain SIMT streaming kernels
+// sized for bandwidth, not tensor-core GEMMs:
+//
+//  * gemv_kernel: y[T, N] = x[T, K] W[N, K]^T with fused epilogues (store,
+//    + residual, SiLU(W1 x) * (W3 x), and for Q|K|V the rotary embedding of
+//    Q and K plus the append of K|V to the cache).  A warp streams groups of
+//    NR output rows, walking K with 16-byte non-allocating loads (four in
+//    flight per row); x sits in shared memory.
+//  * decode_attn_kernel: one CTA per (K/V head, split of 128 cache rows).
+//    The splits never straddle a virtual rank's 2c zigzag rows, so each
+//    rank's partial attention over the K/V it owns is formed where that K/V
+//    lives (the decode counterpart of the prefill's K/V all-gather); the
+//    decoded tokens' own rows, appended after the prompt, form the last
+//    splits.  A lane owns a key: its K row and its V columns go straight to
+//    registers, and one CTA serves all G*T query rows of its K/V head group.
+//  * decode_combine_kernel: merges the splits' (max, sum, unnormalised O) by
+//    their log-sum-exp into O [T, d].
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tsp {
+namespace {
+
+constexpr int kGemvWarps = 8;
+constexpr int kRopeMaxHalf = 64;   // rotary pairs per head the fused Q|K|V epilogue takes (dh <= 128)
+constexpr int kAttnWarps = 4;
+constexpr int kSplitRows = 32 * kAttnWarps;   // cache rows per attention CTA (a lane per row)
+constexpr int kQB = 4;                        // query rows per compute pass
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// 16 bytes of weights -> floats
+template <typename WT> struct WVec;
+template <> struct WVec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void cvt(uint4 v, float (&w)[8]) {
+    w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x); w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
+    w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z); w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
+  }
+};
+template <> struct WVec<float> {
+  static constexpr int N = 4;
+  __device__ static void cvt(uint4 v, float (&w)[4]) {
+    w[0] = __uint_as_float(v.x); w[1] = __uint_as_float(v.y);
+    w[2] = __uint_as_float(v.z); w[3] = __uint_as_float(v.w);
+  }
+};
+// 16 bytes of activations (the same element count as WVec) -> floats
+template <typename XT> struct XVec;
+template <> struct XVec<__half> {
+  __device__ static void cvt(uint4 v, float (&x)[8]) {
+    x[0] = f16_lo(v.x); x[1] = f16_hi(v.x); x[2] = f16_lo(v.y); x[3] = f16_hi(v.y);
+    x[4] = f16_lo(v.z); x[5] = f16_hi(v.z); x[6] = f16_lo(v.w); x[7] = f16_hi(v.w);
+  }
+};
+template <> struct XVec<float> {
+  __device__ static void cvt(uint4 v, float (&x)[4]) { WVec<float>::cvt(v, x); }
+};
+
+__device__ __forceinline__ float load_any(const void* p, int64_t i, int ty) {
+  if (ty == TY_F32) return reinterpret_cast<const float*>(p)[i];
+  if (ty == TY_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+  return __half2float(reinterpret_cast<const __half*>(p)[i]);
+}
+__device__ __forceinline__ void store_any(void* p, int64_t i, int ty, float v) {
+  if (ty == TY_F32)
+    reinterpret_cast<float*>(p)[i] = v;
+  else if (ty == TY_BF16)
+    reinterpret_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<__half*>(p)[i] = __float2half_rn(v);
+}
+
+struct GemvArgs {
+  const void* x;
+  int64_t ldx;
+  const void* w[3];
+  int seg_end[3];   // cumulative rows
+  int nseg, N, K, T;
+  void* out;
+  int64_t ldo;
+  int out_ty;
+  const void* res;
+  int64_t ldr;
+  int res_ty;
+  // GEMV_QKV: head width, Q+K head count, K|V column start, rotary
+  // frequencies and the position of token 0; the cache rows pos0.. receive
+  // the K|V columns
+  int dh, qk_heads, d, rope;
+  int64_t pos0;
+  void* kv;
+  int64_t ldkv;
+  double freq[kRopeMaxHalf];   // base^(-2j/dh), formed on the host in fp64
+};
+
+// Output rows n0 .. n0+NR-1 of one warp (GEMV_SWIGLU: outputs n0.., each
+// from row n of W1 and row n of W3).
+template <typename WT, typename XT, int EPI, int NR>
+__global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(const __grid_constant__ GemvArgs a) {
+  constexpr int VEC = WVec<WT>::N;
+  constexpr bool PAIRED = EPI == GEMV_SWIGLU || EPI == GEMV_QKV;
+  constexpr int NW = PAIRED ? 2 * NR : NR;   // weight rows per warp
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  XT* xs = reinterpret_cast<XT*>(smem_raw);
+  const int T = a.T, K = a.K;
+  // x [T, K] -> shared memory (16-byte pieces)
+  {
+    const int per_row = K * (int)sizeof(XT) / 16;
+    for (int i = threadIdx.x; i < T * per_row; i += blockDim.x) {
+      const int t = i / per_row, v = i - t * per_row;
+      const uint4 val = *reinterpret_cast<const uint4*>(
+          reinterpret_cast<const uint8_t*>(a.x) + ((int64_t)t * a.ldx * (int64_t)sizeof(XT)) + v * 16);
+      reinterpret_cast<uint4*>(xs + (int64_t)t * K)[v] = val;
+    }
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // row groups are dealt out grid-stride: every warp streams several groups
+  for (int grp = blockIdx.x * kGemvWarps + warp; grp * NR < a.N; grp += gridDim.x * kGemvWarps) {
+    const int n0 = grp * NR;
+    const WT* rp[NW];
+    bool ok[NW];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      int n;
+      const WT* base;
+      if (EPI == GEMV_SWIGLU) {
+        n = n0 + (i >> 1);
+        base = reinterpret_cast<const WT*>(a.w[i & 1]);
+        ok[i] = n < a.N;
+      } else if (EPI == GEMV_QKV) {
+        // output pair n0 + (i >> 1) = (head hh, j < dh/2): rows hh*dh + j and + dh/2
+        const int half = a.dh >> 1;
+        const int pi = n0 + (i >> 1), hh = pi / half, j = pi - hh * half;
+        n = hh * a.dh + j + (i & 1) * half;
+        ok[i] = pi < a.N;
+        int s = 0, lo = 0;
+        while (s + 1 < a.nseg && n >= a.seg_end[s]) lo = a.seg_end[s++];
+        base = reinterpret_cast<const WT*>(a.w[s]);
+        n -= lo;
+      } else {
+        n = n0 + i;
+        ok[i] = n < a.N;
+        int s = 0, lo = 0;
+        while (s + 1 < a.nseg && n >= a.seg_end[s]) lo = a.seg_end[s++];
+        base = reinterpret_cast<const WT*>(a.w[s]);
+        n -= lo;
+      }
+      rp[i] = base + (int64_t)(ok[i] ? n : 0) * K;
+    }
+    float acc[NW][TSP_DECODE_MAX_T];
+#pragma unroll
+    for (int i = 0; i < NW; ++i)
+#pragma unroll
+      for (int t = 0; t < TSP_DECODE_MAX_T; ++t) acc[i][t] = 0.f;
+    // U 16-byte loads per weight row are issued before any of them is used,
+    // so every warp keeps U * NW * 512 bytes in flight
+    constexpr int U = 4, STEP = 32 * VEC;
+    auto fma_piece = [&](const uint4 (&wv)[NW], int k) {
+      float w[NW][VEC];
+#pragma unroll
+      for (int i = 0; i < NW; ++i) WVec<WT>::cvt(wv[i], w[i]);
+#pragma unroll
+      for (int t = 0; t < TSP_DECODE_MAX_T; ++t) {
+        if (t < T) {
+          float xv[VEC];
+          XVec<XT>::cvt(*reinterpret_cast<const uint4*>(xs + (int64_t)t * K + k), xv);
+#pragma unroll
+          for (int i = 0; i < NW; ++i)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[i][t] = fmaf(w[i][e], xv[e], acc[i][t]);
+        }
+      }
+    };
+    int k = lane * VEC;
+    for (; k + (U - 1) * STEP < K; k += U * STEP) {
+      uint4 wv[U][NW];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int i = 0; i < NW; ++i)
+          wv[u][i] = ok[i] ? ld_stream(rp[i] + k + u * STEP) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < U; ++u) fma_piece(wv[u], k + u * STEP);
+    }
+    for (; k < K; k += STEP) {
+      uint4 wv[NW];
+#pragma unroll
+      for (int i = 0; i < NW; ++i) wv[i] = ok[i] ? ld_stream(rp[i] + k) : make_uint4(0u, 0u, 0u, 0u);
+      fma_piece(wv, k);
+    }
+#pragma unroll
+    for (int i = 0; i < NW; ++i)
+#pragma unroll
+      for (int t = 0; t < TSP_DECODE_MAX_T; ++t)
+        if (t < T) acc[i][t] = warp_sum(acc[i][t]);
+    if (lane == 0) {
+      if (EPI == GEMV_QKV) {
+        const int half = a.dh >> 1;
+#pragma unroll
+        for (int jp = 0; jp < NR; ++jp) {
+          const int pi = n0 + jp;
+          if (pi >= a.N) continue;
+          const int hh = pi / half, j = pi - hh * half;
+          const int n1 = hh * a.dh + j, n2 = n1 + half;
+          const bool rot = a.rope && hh < a.qk_heads;
+          // the angle in fp64, reduced modulo 2 pi before the fp32 sine and
+          // cosine (an fp32 angle is off by ~0.06 rad at 1M positions)
+          const double f = rot ? a.freq[j] : 0.0;
+#pragma unroll
+          for (int t = 0; t < TSP_DECODE_MAX_T; ++t) {
+            if (t >= T) continue;
+            float v1 = acc[2 * jp][t], v2 = acc[2 * jp + 1][t];
+            if (rot) {
+              const double ang = (double)(a.pos0 + t) * f;
+              const double two_pi = 6.283185307179586476925287;
+              float sv, cv;
+              sincosf((float)(ang - two_pi * rint(ang / two_pi)), &sv, &cv);
+              const float r1 = v1 * cv - v2 * sv, r2 = v1 * sv + v2 * cv;
+              v1 = r1;
+              v2 = r2;
+            }
+            store_any(a.out, (int64_t)t * a.ldo + n1, a.out_ty, v1);
+            store_any(a.out, (int64_t)t * a.ldo + n2, a.out_ty, v2);
+            if (n1 >= a.d) {   // K or V: also the cache row of this token
+              store_any(a.kv, (a.pos0 + t) * a.ldkv + (n1 - a.d), a.out_ty, v1);
+              store_any(a.kv, (a.pos0 + t) * a.ldkv + (n2 - a.d), a.out_ty, v2);
+            }
+          }
+        }
+      } else if (EPI == GEMV_SWIGLU) {
+#pragma unroll
+        for (int j = 0; j < NR; ++j) {
+          const int n = n0 + j;
+          if (n >= a.N) continue;
+#pragma unroll
+          for (int t = 0; t < TSP_DECODE_MAX_T; ++t) {
+            if (t >= T) continue;
+            const float g1 = acc[2 * j][t], g3 = acc[2 * j + 1][t];
+            store_any(a.out, (int64_t)t * a.ldo + n, a.out_ty, g1 * sigmoidf_(g1) * g3);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+          const int n = n0 + i;
+          if (n >= a.N) continue;
+#pragma unroll
+          for (int t = 0; t < TSP_DECODE_MAX_T; ++t) {
+            if (t >= T) continue;
+            float v = acc[i][t];
+            if (EPI == GEMV_RES) v += load_any(a.res, (int64_t)t * a.ldr + n, a.res_ty);
+            store_any(a.out, (int64_t)t * a.ldo + n, a.out_ty, v);
+          }
+        }
+      }
+    }
+  }
+}
+
+template <typename WT, typename XT, int EPI, int NR>
+tsp_status gemv_launch(const GemvArgs& ga, const char* name, cudaStream_t st) {
+  const size_t smem = (size_t)ga.T * ga.K * sizeof(XT);
+  static size_t attr = 0;   // the dynamic shared memory size this instantiation allows
+  if (smem > 48 * 1024 && smem > attr) {
+    TSP_CUDA_TRY(cudaFuncSetAttribute(gemv_kernel<WT, XT, EPI, NR>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    attr = smem;
+  }
+  const int per_cta = kGemvWarps * NR;
+  // a few CTAs per SM, each warp looping over row groups (no partial last wave)
+  const int grid = (int)std::min<int64_t>((ga.N + per_cta - 1) / per_cta, 4 * (int64_t)num_sms());
+  Prof prof(name, st);
+  gemv_kernel<WT, XT, EPI, NR><<<grid, kGemvWarps * 32, smem, st>>>(ga);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+template <typename WT, typename XT, int EPI>
+tsp_status gemv_nr(const GemvArgs& ga, const char* name, cudaStream_t st) {
+  // two rows a warp halve the shared-memory reads of x per weight byte once
+  // several tokens share each weight
+  return ga.T > 2 ? gemv_launch<WT, XT, EPI, 2>(ga, name, st)
+                  : gemv_launch<WT, XT, EPI, 1>(ga, name, st);
+}
+
+template <typename WT, typename XT>
+tsp_status gemv_epi(const GemvArgs& ga, int epi, const char* name, cudaStream_t st) {
+  switch (epi) {
+    case GEMV_QKV: return gemv_nr<WT, XT, GEMV_QKV>(ga, name, st);
+    case GEMV_STORE: return gemv_nr<WT, XT, GEMV_STORE>(ga, name, st);
+    case GEMV_RES: return gemv_nr<WT, XT, GEMV_RES>(ga, name, st);
+    case GEMV_SWIGLU: return gemv_nr<WT, XT, GEMV_SWIGLU>(ga, name, st);
+  }
+  return TSP_ERR_INVALID_ARG;
+}
+
+// ----------------------------------------------------------------------------
+// Attention of the new tokens over the cache
+// ----------------------------------------------------------------------------
+
+struct AttnArgs {
+  const void* q;
+  int64_t ldq;
+  const void* kv;
+  int64_t ldkv;          // 2 * dkv
+  float* part_o;
+  float2* part_ml;
+  int64_t S, c, n_cached, n_total;
+  int D, spr, nsplit, T, H, G, dkv;   // spr: splits per rank
+  int nz, qpc;   // query-row groups per (K/V head, split); query rows per group
+  float scale_log2;
+};
+
+// cache rows [r0, r1) of split `s`: splits 0 .. D*spr-1 cut each rank's 2c
+// zigzag rows into pieces of kSplitRows; the rest cut the decoded rows [S, n_total).
+__device__ __forceinline__ void split_rows(const AttnArgs& a, int s, int64_t& r0, int64_t& r1) {
+  const int prompt_splits = a.D * a.spr;
+  if (s < prompt_splits) {
+    const int r = s / a.spr, j = s - r * a.spr;
+    const int64_t rank0 = (int64_t)r * 2 * a.c, rank1 = rank0 + 2 * a.c;
+    r0 = rank0 + (int64_t)j * kSplitRows;
+    r1 = min(r0 + kSplitRows, rank1);
+  } else {
+    r0 = a.S + (int64_t)(s - prompt_splits) * kSplitRows;
+    r1 = min(r0 + kSplitRows, a.n_total);
+  }
+}
+
+__device__ __forceinline__ uint4 ld_nc16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// V elements one lane holds for one key: VPL of type CT
+template <typename CT, int VPL> struct VReg;
+template <> struct VReg<__half, 4> {   // 8 bytes
+  uint2 r;
+  __device__ void load(const __half* p) { r = *reinterpret_cast<const uint2*>(p); }
+  __device__ void zero() { r = make_uint2(0u, 0u); }
+  __device__ void get(float (&v)[4]) const {
+    v[0] = f16_lo(r.x); v[1] = f16_hi(r.x); v[2] = f16_lo(r.y); v[3] = f16_hi(r.y);
+  }
+};
+template <> struct VReg<__half, 2> {   // 4 bytes
+  uint32_t r;
+  __device__ void load(const __half* p) { r = *reinterpret_cast<const uint32_t*>(p); }
+  __device__ void zero() { r = 0u; }
+  __device__ void get(float (&v)[2]) const { v[0] = f16_lo(r); v[1] = f16_hi(r); }
+};
+template <> struct VReg<float, 2> {
+  float2 r;
+  __device__ void load(const float* p) { r = *reinterpret_cast<const float2*>(p); }
+  __device__ void zero() { r = make_float2(0.f, 0.f); }
+  __device__ void get(float (&v)[2]) const { v[0] = r.x; v[1] = r.y; }
+};
+template <> struct VReg<float, 1> {
+  float r;
+  __device__ void load(const float* p) { r = *p; }
+  __device__ void zero() { r = 0.f; }
+  __device__ void get(float (&v)[1]) const { v[0] = r; }
+};
+
+// CTA = (K/V head g, split s of <= 128 cache rows, query group z); warp w
+// takes rows r0 + 32w .. r0 + 32w + 31.  Every lane issues its K pieces and
+// its V columns of the warp's 32 keys before any arithmetic, so a warp has
+// 16 KB of loads in flight, all coalesced: a K row is read by LPR lanes
+// (16 bytes each) and its dot products reduced across them; a V row by the
+// whole warp.  No shared-memory staging of K/V; the warps' partial softmax
+// results are merged in shared memory.
+template <typename CT, int DH>
+__global__ void __launch_bounds__(kAttnWarps * 32, 3) decode_attn_kernel(const __grid_constant__ AttnArgs a) {
+  constexpr int E = 16 / sizeof(CT);          // elements per 16-byte piece
+  constexpr int LPR = DH / E;                 // lanes per K row (a piece each)
+  constexpr int RPI = 32 / LPR;               // K rows per warp-wide load
+  constexpr int KIT = LPR;                    // loads covering the warp's 32 rows
+  constexpr int VPL = DH >= 32 ? DH / 32 : 1; // V columns per lane
+  constexpr int VLANES = DH / VPL;            // lanes holding V columns
+  __shared__ __align__(16) float qs[kQB][DH];
+  __shared__ __align__(16) float pw[kAttnWarps][kQB][32];
+  __shared__ __align__(16) float ro[kAttnWarps][kQB][DH];
+  __shared__ float2 rml[kAttnWarps][kQB];
+
+  // the nz CTAs of one (K/V head, split) are neighbours in x: they run
+  // together and share the K/V rows through L2
+  const int g = blockIdx.x / a.nz, z = blockIdx.x - g * a.nz, s = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int64_t r0, r1;
+  split_rows(a, s, r0, r1);
+  const int64_t wr0 = r0 + warp * 32;
+  const bool wactive = wr0 < r1;
+  const int64_t kr = wr0 + lane;              // this lane's key row
+  const bool kin = kr < r1;
+  const CT* base = reinterpret_cast<const CT*>(a.kv) + (int64_t)g * DH;
+
+  const int kl = lane % LPR, kh = lane / LPR;   // piece and row of this lane in a K load
+  uint4 kreg[KIT];
+  VReg<CT, VPL> vreg[32];
+  if (wactive) {
+#pragma unroll
+    for (int it = 0; it < KIT; ++it) {
+      const int64_t row = wr0 + it * RPI + kh;
+      kreg[it] = ld_nc16(base + (row < r1 ? row : r0) * a.ldkv + kl * E);
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int64_t row = wr0 + k < r1 ? wr0 + k : r0;   // rows past the split: p = 0
+      if (lane < VLANES)
+        vreg[k].load(base + row * a.ldkv + a.dkv + lane * VPL);
+      else
+        vreg[k].zero();
+    }
+  }
+
+  // query rows of this K/V head: qr = (head g*G + gi, token t), gi = qr / T;
+  // this CTA takes rows [z*qpc, min(QR, (z+1)*qpc))
+  const int QR = min(a.G * a.T, (z + 1) * a.qpc);
+  for (int qb = z * a.qpc; qb < QR; qb += kQB) {
+    const int nq = min(kQB, QR - qb);
+    for (int idx = threadIdx.x; idx < kQB * DH; idx += kAttnWarps * 32) {
+      const int i = idx / DH, j = idx - i * DH;
+      float v = 0.f;
+      if (i < nq) {
+        const int qr = qb + i, gi = qr / a.T, t = qr - gi * a.T;
+        v = to_f(reinterpret_cast<const CT*>(a.q)[(int64_t)t * a.ldq + (g * a.G + gi) * DH + j]);
+      }
+      qs[i][j] = v;
+    }
+    __syncthreads();
+    if (wactive) {
+      // sc[i] = q_i . K[row wr0 + lane]: per load, partial dot products over
+      // each row's LPR lanes, reduced, then handed to the lane that owns the row
+      float sc[kQB];
+#pragma unroll
+      for (int i = 0; i < kQB; ++i) sc[i] = 0.f;
+#pragma unroll
+      for (int i = 0; i < kQB; ++i) {
+        if (i < nq) {
+          float qv[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) qv[e] = qs[i][kl * E + e];
+#pragma unroll
+          for (int it = 0; it < KIT; ++it) {
+            float kf[E];
+            if constexpr (sizeof(CT) == 2) {
+              XVec<__half>::cvt(kreg[it], *reinterpret_cast<float(*)[8]>(kf));
+            } else {
+              XVec<float>::cvt(kreg[it], *reinterpret_cast<float(*)[4]>(kf));
+            }
+            float part = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) part = fmaf(qv[e], kf[e], part);
+#pragma unroll
+            for (int off = LPR / 2; off >= 1; off >>= 1)
+              part += __shfl_xor_sync(0xffffffffu, part, off);
+            // row it*RPI + h sits in lanes h*LPR ..; lane j owns row j
+            const float v = __shfl_sync(0xffffffffu, part, (lane % RPI) * LPR);
+            if (lane / RPI == it) sc[i] = v;
+          }
+        }
+      }
+      // softmax pieces over the warp's 32 keys
+#pragma unroll
+      for (int i = 0; i < kQB; ++i) {
+        if (i < nq) {
+          const int t = (qb + i) % a.T;
+          // prompt rows precede every new token; a new row is visible to the
+          // tokens at or after its own position
+          const bool vis = kin && (kr < a.S || kr <= a.n_cached + t);
+          const float x = vis ? sc[i] * a.scale_log2 : -INFINITY;
+          const float m = warp_max(x);
+          const float p = m == -INFINITY ? 0.f : exp2f(x - m);
+          const float l = warp_sum(p);
+          pw[warp][i][lane] = p;
+          if (lane == 0) rml[warp][i] = make_float2(m, l);
+        }
+      }
+      __syncwarp();
+      // O piece = P V over the warp's keys: lane = V columns
+      float o[kQB][VPL];
+#pragma unroll
+      for (int i = 0; i < kQB; ++i)
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) o[i][v] = 0.f;
+#pragma unroll
+      for (int k4 = 0; k4 < 32; k4 += 4) {
+        float vf[4][VPL];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) vreg[k4 + kk].get(vf[kk]);
+#pragma unroll
+        for (int i = 0; i < kQB; ++i) {
+          if (i < nq) {
+            const float4 p4 = *reinterpret_cast<const float4*>(&pw[warp][i][k4]);
+            const float pk[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+              for (int v = 0; v < VPL; ++v) o[i][v] = fmaf(pk[kk], vf[kk][v], o[i][v]);
+          }
+        }
+      }
+      if (lane < VLANES) {
+#pragma unroll
+        for (int i = 0; i < kQB; ++i)
+          if (i < nq)
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) ro[warp][i][lane * VPL + v] = o[i][v];
+      }
+    } else if (lane < kQB) {
+      rml[warp][lane] = make_float2(-INFINITY, 0.f);   // no rows: no contribution
+    }
+    __syncthreads();
+    // merge the warps: M = max m_w, O = sum 2^(m_w - M) o_w, L likewise
+    for (int idx = threadIdx.x; idx < nq * DH; idx += kAttnWarps * 32) {
+      const int i = idx / DH, j = idx - i * DH;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, rml[w][i].x);
+      float O = 0.f, L = 0.f;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) {
+        const float2 ml = rml[w][i];
+        const float sc = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+        O = fmaf(sc, ml.x == -INFINITY ? 0.f : ro[w][i][j], O);
+        L = fmaf(sc, ml.y, L);
+      }
+      const int qr = qb + i, gi = qr / a.T, t = qr - gi * a.T;
+      const int64_t slot = ((int64_t)s * a.H + g * a.G + gi) * a.T + t;
+      a.part_o[slot * DH + j] = O;
+      if (j == 0) a.part_ml[slot] = make_float2(M, L);
+    }
+    __syncthreads();
+  }
+}
+
+// CTA per (head, token): the maxima first (lane-parallel loads), then warp w
+// adds splits w, w + 8, ... with no branch between its loads; the warps merge
+// in shared memory:  O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+constexpr int kCombineWarps = 8;
+template <typename CT>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    decode_combine_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
+                          CT* __restrict__ o, int nsplit, int H, int T, int dh) {
+  __shared__ float acc_s[kCombineWarps][128];
+  __shared__ float red[kCombineWarps];
+  const int ht = blockIdx.x, h = ht / T, t = ht - h * T;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float M = -INFINITY;
+  for (int s = threadIdx.x; s < nsplit; s += kCombineWarps * 32)
+    M = fmaxf(M, part_ml[((int64_t)s * H + h) * T + t].x);
+  M = warp_max(M);
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();   // red is reused for the sums below
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float L = 0.f;
+#pragma unroll 8
+  for (int s = warp; s < nsplit; s += kCombineWarps) {
+    const int64_t idx = ((int64_t)s * H + h) * T + t;
+    const float2 ml = part_ml[idx];
+    const float* po = part_o + idx * dh;
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = lane + 32 * i < dh ? po[lane + 32 * i] : 0.f;
+    // a split with no visible row (m = -inf) adds nothing
+    const float sc = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+    L = fmaf(sc, ml.y, L);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, v[i], acc[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc_s[warp][lane + 32 * i] = acc[i];
+  if (lane == 0) red[warp] = L;
+  __syncthreads();
+  if (threadIdx.x < dh) {
+    float sum = 0.f, lt = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) {
+      sum += acc_s[w][threadIdx.x];
+      lt += red[w];
+    }
+    o[(int64_t)t * H * dh + h * dh + threadIdx.x] = from_f<CT>(sum / lt);
+  }
+}
+
+template <typename CT, int DH>
+tsp_status decode_attn_t(const AttnArgs& aa, cudaStream_t st) {
+  Prof prof("decode_attn", st);
+  // the K/V head varies fastest: CTAs running together read whole cache rows
+  dim3 grid((unsigned)(aa.H / aa.G * aa.nz), (unsigned)aa.nsplit);
+  decode_attn_kernel<CT, DH><<<grid, kAttnWarps * 32, 0, st>>>(aa);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+}  // namespace
+
+tsp_status launch_gemv(const Gemv& g, cudaStream_t st) {
+  if (g.T < 1 || g.T > TSP_DECODE_MAX_T || g.K <= 0 || g.nseg < 1 || g.nseg > 3)
+    return TSP_ERR_INVALID_ARG;
+  const bool bf = g.dtype == TSP_BF16;
+  const int xsz = bf ? 2 : 4;
+  // 16-byte pieces of every weight row and every x row
+  if ((g.K * xsz) % 16 != 0) return TSP_ERR_UNSUPPORTED;
+  if ((g.ldx * xsz) % 16 != 0 || ((uintptr_t)g.x & 15u)) return TSP_ERR_UNSUPPORTED;
+  if ((size_t)g.T * g.K * xsz > 200 * 1024) return TSP_ERR_UNSUPPORTED;
+  GemvArgs ga;
+  memset(&ga, 0, sizeof(ga));
+  ga.x = g.x;
+  ga.ldx = g.ldx;
+  int n = 0;
+  const int nseg = g.epi == GEMV_SWIGLU ? 2 : g.nseg;
+  for (int s = 0; s < nseg; ++s) {
+    if (!g.w[s] || ((uintptr_t)g.w[s] & 15u)) return TSP_ERR_INVALID_ARG;
+    ga.w[s] = g.w[s];
+    n += g.epi == GEMV_SWIGLU ? 0 : g.rows[s];
+    ga.seg_end[s] = n;
+  }
+  ga.nseg = nseg;
+  ga.N = g.epi == GEMV_SWIGLU ? g.rows[0] : g.epi == GEMV_QKV ? n / 2 : n;
+  if (g.epi == GEMV_QKV && (g.dh < 2 || g.dh % 2 != 0 || n % g.dh != 0)) return TSP_ERR_INVALID_ARG;
+  ga.dh = g.dh;
+  ga.qk_heads = g.qk_heads;
+  ga.d = g.d;
+  ga.pos0 = g.pos0;
+  if (g.epi == GEMV_QKV && g.rope_base > 0.f) {
+    if (g.dh / 2 > kRopeMaxHalf) return TSP_ERR_UNSUPPORTED;
+    ga.rope = 1;
+    for (int j = 0; j < g.dh / 2; ++j)
+      ga.freq[j] = std::pow((double)g.rope_base, -2.0 * j / (double)g.dh);
+  }
+  ga.kv = g.kv;
+  ga.ldkv = g.ldkv;
+  ga.K = g.K;
+  ga.T = g.T;
+  ga.out = g.out;
+  ga.ldo = g.ldo;
+  ga.out_ty = g.out_ty;
+  ga.res = g.res;
+  ga.ldr = g.ldr;
+  ga.res_ty = g.res_ty;
+  if (ga.N <= 0) return TSP_ERR_INVALID_ARG;
+  return bf ? gemv_epi<__nv_bfloat16, __half>(ga, g.epi, g.name, st)
+            : gemv_epi<float, float>(ga, g.epi, g.name, st);
+}
+
+int64_t decode_splits(int64_t S, int D, int64_t n_rows) {
+  const int64_t c2 = S / D;   // 2c rows per virtual rank
+  const int64_t spr = (c2 + kSplitRows - 1) / kSplitRows;
+  return D * spr + (n_rows - S + kSplitRows - 1) / kSplitRows;
+}
+
+tsp_status launch_decode_attn(const DecodeAttn& d, cudaStream_t st) {
+  if (d.T < 1 || d.T > TSP_DECODE_MAX_T || d.Hkv < 1 || d.H % d.Hkv != 0) return TSP_ERR_INVALID_ARG;
+  if (((uintptr_t)d.kv & 15u) || ((uintptr_t)d.q & 15u)) return TSP_ERR_INVALID_ARG;
+  AttnArgs aa;
+  memset(&aa, 0, sizeof(aa));
+  aa.q = d.q;
+  aa.ldq = d.ldq;
+  aa.kv = d.kv;
+  aa.dkv = d.Hkv * d.dh;
+  aa.ldkv = 2 * (int64_t)aa.dkv;
+  aa.part_o = d.part_o;
+  aa.part_ml = d.part_ml;
+  aa.S = d.S;
+  aa.D = d.D;
+  aa.c = d.S / (2 * d.D);
+  aa.n_cached = d.n_cached;
+  aa.n_total = d.n_cached + d.T;
+  aa.spr = (int)((2 * aa.c + kSplitRows - 1) / kSplitRows);
+  aa.nsplit = (int)decode_splits(d.S, d.D, aa.n_total);
+  aa.T = d.T;
+  aa.H = d.H;
+  aa.G = d.H / d.Hkv;
+  aa.scale_log2 = 1.4426950408889634f / sqrtf((float)d.dh);
+  // query-row groups: enough CTAs for ~4 waves of 3 per SM when the K/V
+  // heads and splits alone give fewer (grouped K/V heads, short caches)
+  {
+    const int QR = aa.G * aa.T;
+    const int64_t base_ctas = (int64_t)d.Hkv * aa.nsplit;
+    const int64_t want = 12 * (int64_t)num_sms();
+    const int nz = (int)std::min<int64_t>(QR, std::max<int64_t>(1, (want + base_ctas - 1) / base_ctas));
+    aa.qpc = (QR + nz - 1) / nz;
+    aa.nz = (QR + aa.qpc - 1) / aa.qpc;
+  }
+  tsp_status r = TSP_ERR_UNSUPPORTED;
+  if (d.dtype == TSP_BF16) {
+    if (d.dh == 128) r = decode_attn_t<__half, 128>(aa, st);
+    else if (d.dh == 64) r = decode_attn_t<__half, 64>(aa, st);
+  } else {
+    if (d.dh == 64) r = decode_attn_t<float, 64>(aa, st);
+    else if (d.dh == 32) r = decode_attn_t<float, 32>(aa, st);
+    else if (d.dh == 16) r = decode_attn_t<float, 16>(aa, st);
+  }
+  if (r != TSP_OK) return r;
+  Prof prof("decode_combine", st);
+  const int blocks = d.H * d.T;   // a CTA per (head, token)
+  if (d.dtype == TSP_BF16)
+    decode_combine_kernel<__half><<<blocks, kCombineWarps * 32, 0, st>>>(
+        aa.part_o, aa.part_ml, (__half*)d.o, aa.nsplit, d.H, d.T, d.dh);
+  else
+    decode_combine_kernel<float><<<blocks, kCombineWarps * 32, 0, st>>>(
+        aa.part_o, aa.part_ml, (float*)d.o, aa.nsplit, d.H, d.T, d.dh);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+}  // namespace tsp

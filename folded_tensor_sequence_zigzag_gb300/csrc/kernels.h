@@ -68,4 +68,49 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
                                 float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int Hkv, int dh,
                                 int D, cudaStream_t st);
 
+// decode.cu: inference decode against the zigzag KV cache
+enum { GEMV_STORE = 0, GEMV_RES = 1, GEMV_SWIGLU = 2, GEMV_QKV = 3 };
+struct Gemv {
+  int epi = GEMV_STORE;
+  int dtype = TSP_BF16;        // TSP_BF16: W bf16, x fp16; TSP_F32: W and x fp32
+  const void* x = nullptr;     // [T, K], row stride ldx elements
+  int64_t ldx = 0;
+  const void* w[3] = {nullptr, nullptr, nullptr};   // weight segments [rows[s], K], stacked
+  int rows[3] = {0, 0, 0};     // (GEMV_SWIGLU: w[0] = W1, w[1] = W3, both rows[0] rows)
+  int nseg = 1;
+  int K = 0, T = 0;
+  void* out = nullptr;         // [T, N], row stride ldo elements, type out_ty
+  int64_t ldo = 0;
+  int out_ty = TY_F16;
+  const void* res = nullptr;   // GEMV_RES: out = x W^T + res (type res_ty, stride ldr)
+  int64_t ldr = 0;
+  int res_ty = TY_F32;
+  // GEMV_QKV (segments W_Q, W_K, W_V): rows computed in pairs (j, j + dh/2) of
+  // one head; the first qk_heads heads (Q and K) are rotated at positions
+  // pos0 + t when rope_base > 0; columns >= d (K | V) are also written to the
+  // cache rows pos0 + t (row stride ldkv)
+  int dh = 0, qk_heads = 0, d = 0;
+  float rope_base = 0.f;
+  int64_t pos0 = 0;
+  void* kv = nullptr;
+  int64_t ldkv = 0;
+  const char* name = "gemv";
+};
+tsp_status launch_gemv(const Gemv& g, cudaStream_t st);
+// partial attention of the T new query rows over the cache rows, one split of
+// cache rows per CTA, then the log-sum-exp merge of the splits into O [T, d]
+struct DecodeAttn {
+  int dtype = TSP_BF16;        // cache / q / O element type: fp16 (TSP_BF16) or fp32
+  const void* q = nullptr;     // [T, ldq], query head h at column h*dh
+  int64_t ldq = 0;
+  const void* kv = nullptr;    // cache rows [K | V], row stride 2*Hkv*dh
+  void* o = nullptr;           // [T, d]
+  float* part_o = nullptr;     // [nsplit][H][T][dh]
+  float2* part_ml = nullptr;   // [nsplit][H][T] (max, sum) in log2 units
+  int64_t S = 0, n_cached = 0; // prompt rows (zigzag), rows cached before this call
+  int D = 1, T = 1, H = 1, Hkv = 1, dh = 0;
+};
+int64_t decode_splits(int64_t S, int D, int64_t n_rows);
+tsp_status launch_decode_attn(const DecodeAttn& a, cudaStream_t st);
+
 }  // namespace tsp

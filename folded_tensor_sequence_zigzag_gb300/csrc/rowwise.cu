@@ -582,6 +582,7 @@ struct RopeFreq {
   double f[kRopeMaxHalf];
 };
 
+// row `row` holds zigzag position zz_pos_of_row(row)
 __global__ void rope_table_kernel(float2* __restrict__ tab, int64_t S, int64_t c, int D, int half,
                                   const __grid_constant__ RopeFreq F) {
   const int64_t total = S * half;
@@ -600,7 +601,7 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, int64_t S, int64_t c
 
 tsp_status launch_rope_table(float2* table, int64_t S, int D, int dh, float base, cudaStream_t st) {
   const int half = dh / 2;
-  if (!table || half < 1 || half > kRopeMaxHalf) return TSP_ERR_UNSUPPORTED;
+  if (!table || half < 1 || half > kRopeMaxHalf || D < 1) return TSP_ERR_UNSUPPORTED;
   RopeFreq F;
   for (int j = 0; j < half; ++j) F.f[j] = std::pow((double)base, -2.0 * j / (double)dh);
   Prof prof("rope_table", st);

@@ -24,7 +24,9 @@ EXPORTED = ("tsp_zigzag_permute", "tsp_rmsnorm_fwd", "tsp_workspace_bytes", "tsp
             "tsp_pack_attn_shards", "tsp_device_status", "tsp_strerror", "tsp_num_sms",
             "tsp_profile_enable", "tsp_profile_report", "tsp_launch_count",
             "tsp_gated_mlp_fwd_noalloc", "tsp_stack_saved_bytes", "tsp_stack_workspace_bytes",
-            "tsp_stack_fwd", "tsp_stack_bwd", "tsp_rank_memory")
+            "tsp_stack_fwd", "tsp_stack_bwd", "tsp_rank_memory", "tsp_kv_cache_bytes",
+            "tsp_decode_workspace_bytes", "tsp_block_prefill", "tsp_block_decode")
+DECODE_MAX_T = 8   # TSP_DECODE_MAX_T
 
 
 class TspError(RuntimeError):
@@ -85,6 +87,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "tsp_stack_fwd": (i32, [P(Cfg), i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "tsp_stack_bwd": (i32, [P(Cfg), i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "tsp_rank_memory": (i32, [P(Cfg), i32, i32, i32, P(RankMem)]),
+        "tsp_kv_cache_bytes": (sz, [P(Cfg), i64]),
+        "tsp_decode_workspace_bytes": (sz, [P(Cfg), i32, i64]),
+        "tsp_block_prefill": (i32, [P(Cfg), vp, P(AttnW), P(MlpW), vp, vp, i64, vp, sz, vp]),
+        "tsp_block_decode": (i32, [P(Cfg), vp, i32, i64, P(AttnW), P(MlpW), vp, vp, i64, vp, sz,
+                                   vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -238,6 +245,63 @@ def block_fwd(cfg: Cfg, x_z, W: BlockWeights, saved=None, out=None, ws=None, str
     _check(load().tsp_block_fwd(ctypes.byref(cfg), _ptr(x_z), ctypes.byref(aw), ctypes.byref(mw),
                                 _ptr(out), _ptr(saved), _ptr(ws), 0 if ws is None else ws.numel(),
                                 _stream(stream)), "tsp_block_fwd")
+    return out
+
+
+def kv_cache_bytes(cfg: Cfg, rows_cap: int) -> int:
+    return int(load().tsp_kv_cache_bytes(ctypes.byref(cfg), int(rows_cap)))
+
+
+def decode_workspace_bytes(cfg: Cfg, T: int, rows_cap: int) -> int:
+    return int(load().tsp_decode_workspace_bytes(ctypes.byref(cfg), int(T), int(rows_cap)))
+
+
+class KVCache:
+    """Device KV cache of ``rows_cap`` rows for one block (layout in tsp.h):
+    the prompt's rows in zigzag order, then the decoded tokens'."""
+
+    def __init__(self, cfg: Cfg, rows_cap: int, device="cuda"):
+        nb = kv_cache_bytes(cfg, rows_cap)
+        if nb == 0:
+            raise ValueError("invalid configuration or capacity for a KV cache")
+        self.buf = torch.empty(nb, dtype=torch.uint8, device=device)
+        self.rows_cap = int(rows_cap)
+        self.n = 0          # rows filled
+
+    def view(self, cfg: Cfg) -> torch.Tensor:
+        """[rows_cap, 2*Hkv*dh] view in the internal element type (K | V)."""
+        dt = torch.float16 if cfg.dtype == TSP_BF16 else torch.float32
+        return self.buf.view(dt).view(self.rows_cap, -1)
+
+
+def block_prefill(cfg: Cfg, x_z, W: BlockWeights, cache: KVCache, out=None, ws=None, stream=None):
+    """Inference forward over the S prompt tokens (zigzag order) that also
+    fills cache rows [0, S) with their K and V."""
+    _require_cuda(x_z)
+    out = torch.empty_like(x_z) if out is None else out
+    if ws is None:
+        ws = _ws(workspace_bytes(cfg, TSP_OP_BLOCK_FWD), x_z.device)
+    aw, mw = W.attn(), W.mlp()
+    _check(load().tsp_block_prefill(ctypes.byref(cfg), _ptr(x_z), ctypes.byref(aw), ctypes.byref(mw),
+                                    _ptr(out), _ptr(cache.buf), cache.rows_cap, _ptr(ws), ws.numel(),
+                                    _stream(stream)), "tsp_block_prefill")
+    cache.n = cfg.S
+    return out
+
+
+def block_decode(cfg: Cfg, x, W: BlockWeights, cache: KVCache, out=None, ws=None, stream=None):
+    """y [T, d] of T new tokens (position order) at positions cache.n ..;
+    appends their K/V to the cache."""
+    _require_cuda(x)
+    T = x.shape[0]
+    out = torch.empty_like(x) if out is None else out
+    if ws is None:
+        ws = _ws(decode_workspace_bytes(cfg, T, cache.rows_cap), x.device)
+    aw, mw = W.attn(), W.mlp()
+    _check(load().tsp_block_decode(ctypes.byref(cfg), _ptr(x), T, cache.n, ctypes.byref(aw),
+                                   ctypes.byref(mw), _ptr(out), _ptr(cache.buf), cache.rows_cap,
+                                   _ptr(ws), ws.numel(), _stream(stream)), "tsp_block_decode")
+    cache.n += T
     return out
 
 

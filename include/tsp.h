@@ -198,7 +198,7 @@ tsp_status tsp_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* 
  * of the residual stream, kept in fp32 like the stream itself: at early
  * positions, which every later query attends, it reaches ~10x its RMS, where
  * a bf16 result would lose more than the bf16 path's error budget to its own
- * rounding) and the gradients dwq, dwk, dwv, dwo [d, d], dw1, dw3 [inter, d],
+ * rounding) and the gradients dwq, dwo [d, d], dwk, dwv [Hkv*dh, d], dw1, dw3 [inter, d],
  * dw2 [d, inter], dg_attn, dg_mlp [d] -- each the sum over the D virtual
  * ranks' token rows (the reduction TSP performs toward the shard owners).
  * ws: tsp_workspace_bytes(cfg, TSP_OP_BLOCK_BWD). */
@@ -207,6 +207,45 @@ tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z,
                          float* dx_z, float* dwq, float* dwk, float* dwv, float* dwo,
                          float* dw1, float* dw3, float* dw2, float* dg_attn, float* dg_mlp,
                          void* ws, size_t ws_bytes, void* stream);
+
+/* ---- Inference: prefill, then decode against the zigzag KV cache ----
+ * (section 2, attention bullet: each rank holds the K/V of its own zigzag
+ * rows; the pages' title names inference, their schedules describe the
+ * full-sequence pass, which is the prefill.)
+ *
+ * KV cache: kv_rows_cap rows of [K (Hkv*dh) | V (Hkv*dh)], row-major, in the
+ * internal element type (fp16 for TSP_BF16, fp32 for TSP_F32), K after the
+ * rotary embedding when cfg->rope_base > 0.  Rows [0, S) hold the prompt in
+ * zigzag row order (row i is the token at global position zz_pos(i); virtual
+ * rank r owns rows [r*2c, (r+1)*2c), c = S/(2D)); rows [S, n) hold decoded
+ * tokens, row = position.  The caller owns it.
+ *
+ * tsp_kv_cache_bytes: bytes of a cache of kv_rows_cap rows (0 if invalid).
+ * tsp_block_prefill: tsp_block_fwd(x_z -> y_z, inference) over the S prompt
+ *   tokens, then their K and V into cache rows [0, S).  ws as for
+ *   tsp_block_fwd (tsp_workspace_bytes(cfg, TSP_OP_BLOCK_FWD)).
+ * tsp_block_decode: T (1..TSP_DECODE_MAX_T) new tokens at positions
+ *   n_cached .. n_cached+T-1, where n_cached (S <= n_cached <=
+ *   kv_rows_cap - T) rows are already in the cache.  x, y: [T, d] in
+ *   position order (cfg dtype).  Appends the new tokens' K/V at rows
+ *   n_cached.., then each new token attends to every cached row at or
+ *   before its position: per virtual rank over the zigzag rows it owns,
+ *   merged by log-sum-exp.  y equals rows n_cached.. of the block forward
+ *   over the whole sequence.  Reads the weights directly (no converted
+ *   copies).  ws: tsp_decode_workspace_bytes(cfg, T, kv_rows_cap).
+ * Errors: TSP_ERR_INVALID_ARG for NULL/misaligned pointers, T out of range,
+ *   n_cached out of range, a short workspace or cache; TSP_ERR_UNSUPPORTED
+ *   for shapes the decode kernels do not take (dh not dividing 256 into
+ *   whole column pairs, d or inter not a multiple of 8 (bf16) / 4 (fp32)). */
+#define TSP_DECODE_MAX_T 8
+size_t tsp_kv_cache_bytes(const tsp_cfg* cfg, int64_t kv_rows_cap);
+size_t tsp_decode_workspace_bytes(const tsp_cfg* cfg, int32_t T, int64_t kv_rows_cap);
+tsp_status tsp_block_prefill(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* aw,
+                             const tsp_mlp_w* mw, void* y_z, void* kv, int64_t kv_rows_cap,
+                             void* ws, size_t ws_bytes, void* stream);
+tsp_status tsp_block_decode(const tsp_cfg* cfg, const void* x, int32_t T, int64_t n_cached,
+                            const tsp_attn_w* aw, const tsp_mlp_w* mw, void* y, void* kv,
+                            int64_t kv_rows_cap, void* ws, size_t ws_bytes, void* stream);
 
 /* ---- Stack of L blocks (the multi-layer model the fold is applied to) ----
  * y = B_{L-1}(... B_0(x)), B_l = the block above with weights aw[l], mw[l];

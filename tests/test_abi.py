@@ -127,3 +127,34 @@ def test_workspace_sizes_are_consistent(lib):
     assert saved >= acts + S * 2 * I * 2
     assert saved < acts + S * 2 * I * 2 + 64 * 256
     assert lib.tsp_workspace_bytes(ctypes.byref(cfg), tsp.TSP_OP_BLOCK_BWD) > 0
+
+
+def test_decode_arguments_checked_without_launch(lib):
+    cfg = _cfg()            # S=256, d=64, H=4, fp32
+    ok = ctypes.c_void_p(0x10000)
+    aw = tsp.AttnW(ok, ok, ok, ok, ok)
+    mw = tsp.MlpW(ok, ok, ok, ok, 1)
+    cap = 300
+    assert lib.tsp_kv_cache_bytes(ctypes.byref(cfg), cap) == cap * 2 * 64 * 4
+    assert lib.tsp_kv_cache_bytes(ctypes.byref(cfg), 255) == 0          # below the prompt
+    assert lib.tsp_decode_workspace_bytes(ctypes.byref(cfg), 0, cap) == 0
+    assert lib.tsp_decode_workspace_bytes(ctypes.byref(cfg), tsp.DECODE_MAX_T + 1, cap) == 0
+    ws = lib.tsp_decode_workspace_bytes(ctypes.byref(cfg), 4, cap)
+    assert ws > 0
+    # grouped K/V: a narrower cache
+    g = _cfg(Hkv=2)
+    assert lib.tsp_kv_cache_bytes(ctypes.byref(g), cap) == cap * 2 * 32 * 4
+    big = 1 << 40
+
+    def dec(T, n_cached, cap_=cap, x=ok, wsb=big):
+        return lib.tsp_block_decode(ctypes.byref(cfg), x, T, n_cached, ctypes.byref(aw),
+                                    ctypes.byref(mw), ok, ok, cap_, ok, wsb, None)
+    assert dec(0, 256) == tsp.TSP_ERR_INVALID_ARG
+    assert dec(tsp.DECODE_MAX_T + 1, 256) == tsp.TSP_ERR_INVALID_ARG
+    assert dec(1, 255) == tsp.TSP_ERR_INVALID_ARG              # inside the prompt
+    assert dec(4, 297) == tsp.TSP_ERR_INVALID_ARG              # past the cache
+    assert dec(1, 256, x=ctypes.c_void_p(0x10004)) == tsp.TSP_ERR_INVALID_ARG
+    assert dec(1, 256, wsb=16) == tsp.TSP_ERR_INVALID_ARG      # short workspace
+    # prefill: the cache must hold the prompt
+    assert lib.tsp_block_prefill(ctypes.byref(cfg), ok, ctypes.byref(aw), ctypes.byref(mw), ok, ok,
+                                 255, ok, big, None) == tsp.TSP_ERR_INVALID_ARG
