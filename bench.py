@@ -48,6 +48,9 @@ WORKLOADS = {
     "fwd512k": (524288, 8, 4096, 32, 11008, "fwd"),
     "fwd1m": (1048576, 8, 4096, 32, 11008, "fwd"),
     "fwdbwd512k": (524288, 8, 4096, 32, 11008, "fwdbwd"),
+    # beyond the untiled limit: the MLP in sequence tiles of 16384 rows, its
+    # G and pre-activations recomputed in the backward instead of kept
+    "fwdbwd768k_tiled": (786432, 8, 4096, 32, 11008, "fwdbwd"),
     "mlp16k": (16384, 4, 4096, 32, 11008, "mlp"),
     # 32-layer stacks of the 7B-shaped block (each layer its own weights)
     "stack32_16k": (16384, 8, 4096, 32, 11008, "fwd"),
@@ -67,7 +70,8 @@ LAYERS = {"stack32_16k": 32, "stack32train_16k": 32}   # other workloads: one bl
 # block variants of a workload (default: multi-head attention, no positional encoding)
 VARIANTS = {"fwd16k_gqa8": {"Hkv": 8, "rope_base": 500000.0},
             "fwdbwd8k_gqa8": {"Hkv": 8, "rope_base": 500000.0},
-            "decode16k_gqa8": {"Hkv": 8, "rope_base": 500000.0}}
+            "decode16k_gqa8": {"Hkv": 8, "rope_base": 500000.0},
+            "fwdbwd768k_tiled": {"mlp_tile": 16384}}
 
 
 def decode_bytes(name, d, inter, dkv, n_rows, T=DECODE_T):
@@ -114,6 +118,8 @@ def gemm_flops(name, S, d, inter, dkv=None):
         "gemm_dgrad_w2_swiglu": 2.0 * S * d * inter,
         "gemm_wgrad_w2": 2.0 * S * d * inter,
         "gemm_wgrad_w13": 4.0 * S * d * inter,
+        # MLP tiling: the backward recomputes G and A|B (work beyond the model's flops)
+        "gemm_w13_recompute": 4.0 * S * d * inter,
         "gemm_dgrad_w13": 4.0 * S * d * inter,
         "gemm_wgrad_wo": 2.0 * S * d * d,
         "gemm_dgrad_wo": 2.0 * S * d * d,
@@ -391,6 +397,8 @@ def workload_config(name):
         extra += f", grouped-query attention with {var['Hkv']} K/V heads"
     if var.get("rope_base"):
         extra += f", rotary embedding base {var['rope_base']:g}"
+    if var.get("mlp_tile"):
+        extra += f", MLP in sequence tiles of {var['mlp_tile']} rows (recomputed in the backward)"
     return {"workload": f"{desc}, S={S}, D={D} zigzag virtual ranks, d_model={d}, "
                         f"{H} heads x {d // H}, SwiGLU inter={inter}, causal{extra}",
             "S": S, "D": D, "d_model": d, "heads": H, "kv_heads": var.get("Hkv", H),
@@ -426,7 +434,7 @@ def run_gpu(args):
     inp = make_block_inputs(shape, torch.bfloat16, seed=rank, with_dy=(kind == "fwdbwd"),
                             mlp_only=(kind == "mlp"))
     cfg = tsp.make_cfg(S, d, H, inter, D, torch.bfloat16, rope_base=var.get("rope_base", 0.0),
-                       Hkv=var.get("Hkv", 0))
+                       Hkv=var.get("Hkv", 0), mlp_tile=var.get("mlp_tile", 0))
     dkv = shape.dkv
     if kind == "mlp":
         inp.update({k: torch.zeros(1, dtype=torch.bfloat16) for k in ("wq", "wk", "wv", "wo")})
@@ -583,10 +591,10 @@ def run_gpu(args):
     per_kernel = {}
     for ms, name, k in kernel_rows:
         per_launch_ms = ms / max(k, 1)
-        f = gemm_flops(name, S, d, inter, dkv)
+        f = gemm_flops(name, S, d, inter, dkv)   # one layer-step's flops over all its launches
         entry = {"launches": k, "ms_per_launch": per_launch_ms}
         if f is not None and kind != "mlp":
-            entry["tflops"] = f / (per_launch_ms / 1e3) / 1e12
+            entry["tflops"] = f * L * args.steps / (ms / 1e3) / 1e12
         elif name.startswith("gemm_w13") and kind == "mlp":
             entry["tflops"] = 4.0 * S * d * inter / (per_launch_ms / 1e3) / 1e12
         elif name.startswith("gemm_w2") and kind == "mlp":

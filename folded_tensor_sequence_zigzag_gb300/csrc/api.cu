@@ -128,6 +128,11 @@ tsp_status check_cfg(const tsp_cfg* c) {
   if (!(c->rope_base >= 0.f) || (c->rope_base > 0.f && c->dh % 2 != 0)) return TSP_ERR_INVALID_ARG;
   if (c->Hkv < 0 || (c->Hkv > 0 && c->H % c->Hkv != 0)) return TSP_ERR_INVALID_ARG;
   if (kv_dim(c) < c->D) return TSP_ERR_INVALID_ARG;
+  if (c->mlp_tile < 0) return TSP_ERR_INVALID_ARG;
+  if (c->mlp_tile > 0) {
+    if (c->mlp_tile % 128 != 0 || (c->S / c->D) % c->mlp_tile != 0) return TSP_ERR_INVALID_ARG;
+    if (c->dtype != TSP_BF16) return TSP_ERR_UNSUPPORTED;
+  }
   if (c->S > (int64_t)1 << 31) return TSP_ERR_UNSUPPORTED;
   if (c->dtype == TSP_F32 && c->dh > 128) return TSP_ERR_UNSUPPORTED;
   return TSP_OK;
@@ -153,7 +158,7 @@ struct Acts {
   size_t bytes;
 };
 
-enum { PART_ATTN = 1, PART_MLP = 2, PART_AB = 4 };
+enum { PART_ATTN = 1, PART_MLP = 2, PART_AB = 4, PART_NO_G = 8 };
 
 Acts acts_layout(const tsp_cfg* c, int parts, uint8_t* base) {
   const size_t e = c->dtype == TSP_BF16 ? 2 : 4;
@@ -178,7 +183,7 @@ Acts acts_layout(const tsp_cfg* c, int parts, uint8_t* base) {
     A.rstd2 = (float*)take(S * 4);
     A.h = (parts & PART_ATTN) ? take(S * d * 4) : nullptr;  // fp32 residual stream
     A.b = take(S * d * e);
-    A.g = take(S * I * e);
+    if (!(parts & PART_NO_G)) A.g = take(S * I * e);
     if (parts & PART_AB) A.ab = take(S * 2 * I * e);
   }
   A.bytes = off;
@@ -186,12 +191,21 @@ Acts acts_layout(const tsp_cfg* c, int parts, uint8_t* base) {
 }
 
 int fwd_parts(const tsp_cfg* c, bool training) {
+  // with MLP tiling the training record keeps neither G nor A|B (the
+  // backward recomputes them tile by tile from b)
+  if (training && c->mlp_tile > 0) return PART_ATTN | PART_MLP | PART_NO_G;
   // the fp32 path builds G from A|B, so it always keeps them
   return PART_ATTN | PART_MLP | ((training || c->dtype == TSP_F32) ? PART_AB : 0);
 }
 
+// bytes of one MLP tile's G (fp16) in the training forward's workspace
+size_t mlp_tile_g_bytes(const tsp_cfg* c) {
+  return c->mlp_tile > 0 ? up256((size_t)c->mlp_tile * c->inter * 2) : 0;
+}
+
 struct BwdWs {
   void *dab, *dg_f32, *db, *dh_f32, *dh_t, *dO, *dqkv, *da, *dy16;
+  void *gt, *abt;   // MLP tiling: one tile's recomputed G and A|B
   float *delta, *dq_acc, *dg_part;
   size_t bytes;
 };
@@ -207,7 +221,12 @@ BwdWs bwd_layout(const tsp_cfg* c, uint8_t* base) {
   };
   BwdWs W;
   memset(&W, 0, sizeof(W));
-  W.dab = take(S * 2 * I * e);
+  const size_t mrows = c->mlp_tile > 0 ? (size_t)c->mlp_tile : S;   // rows of the MLP buffers
+  W.dab = take(mrows * 2 * I * e);
+  if (c->mlp_tile > 0) {
+    W.gt = take(mrows * I * e);
+    W.abt = take(mrows * 2 * I * e);
+  }
   if (c->dtype == TSP_F32) W.dg_f32 = take(S * I * 4);
   W.db = take(S * d * 4);
   W.dh_f32 = take(S * d * 4);
@@ -390,8 +409,11 @@ tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, const
 }
 
 // hin_f32: the input h is fp32 (the block's residual stream), else the cfg dtype.
+// g_tile (training with cfg->mlp_tile): the MLP runs one row tile at a time
+// with G in this [mlp_tile, inter] buffer, and keeps no G or A|B.
 tsp_status mlp_half(const tsp_cfg* c, const void* hin, bool hin_f32, const tsp_mlp_w* w,
-                    const WCache& WC, void* y, const Acts& A, cudaStream_t st) {
+                    const WCache& WC, void* y, const Acts& A, cudaStream_t st,
+                    void* g_tile = nullptr) {
   const int64_t S = c->S;
   const int d = c->d, I = c->inter, D = c->D;
   const int64_t rows_per_rank = S / D;
@@ -409,6 +431,35 @@ tsp_status mlp_half(const tsp_cfg* c, const void* hin, bool hin_f32, const tsp_m
     if (hin_f32) return TSP_ERR_UNSUPPORTED;
     if ((r = launch_convert_bf16_f16(hin, A.b, S * d, st)) != TSP_OK) return r;
     b = A.b;
+  }
+  if (bf && g_tile) {
+    // sequence tiles (each inside one virtual rank's rows): the same two
+    // GEMMs as below on M = mlp_tile rows, G living only for its tile
+    const int64_t tile = c->mlp_tile;
+    for (int64_t t0 = 0; t0 < S; t0 += tile) {
+      TcGemm g;
+      g.M = (int)tile; g.N = I; g.K = d;
+      g.A[0] = (const uint8_t*)b + (size_t)t0 * d * 2; g.lda[0] = d; g.kseg_len[0] = d;
+      g.B[0] = WC.w1; g.B[1] = WC.w3; g.ldb[0] = g.ldb[1] = d;
+      g.paired = true; g.name = "gemm_w13_swiglu";
+      g.epi = EPI_SWIGLU; g.out = g_tile; g.ldo = I;
+      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+      TcGemm o;
+      o.M = (int)tile; o.N = d; o.K = I;
+      o.A[0] = g_tile; o.lda[0] = I; o.kseg_len[0] = I;
+      o.B[0] = WC.w2; o.ldb[0] = I;
+      o.rot_rows = (int)tile; o.rot_r0 = (int)(t0 / rows_per_rank); o.rot_D = D;
+      o.name = "gemm_w2";
+      o.out = (uint8_t*)y + (size_t)t0 * d * 2; o.ldo = d; o.out_type = OUT_BF16;
+      if (w->add_residual) {
+        o.epi = EPI_RES; o.res = (const uint8_t*)hin + (size_t)t0 * d * (hin_f32 ? 4 : 2);
+        o.ldr = d; o.res_f32 = hin_f32;
+      } else {
+        o.epi = EPI_STORE;
+      }
+      if ((r = gemm_tc(o, st)) != TSP_OK) return r;
+    }
+    return TSP_OK;
   }
   if (bf) {
     // W_1|W_3: one 256-wide B tile = 128 rows of W_1 and the same 128 rows of
@@ -635,6 +686,9 @@ size_t tsp_workspace_bytes(const tsp_cfg* cfg, int32_t op) {
              wcache_layout(cfg, WC_ATTN | WC_MLP, nullptr).bytes;
     case TSP_OP_BLOCK_BWD:
       return bwd_layout(cfg, nullptr).bytes + wcache_layout(cfg, WC_ATTN | WC_MLP, nullptr).bytes;
+    case TSP_OP_BLOCK_FWD_TRAIN:
+      return std::max<size_t>(256, wcache_layout(cfg, WC_ATTN | WC_MLP, nullptr).bytes +
+                                       mlp_tile_g_bytes(cfg));
   }
   return 0;
 }
@@ -690,11 +744,13 @@ tsp_status tsp_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* 
   const bool training = saved != nullptr;
   const int parts = fwd_parts(cfg, training);
   const size_t nwc = wcache_layout(cfg, WC_ATTN | WC_MLP, nullptr).bytes;
+  const size_t ntile = training ? mlp_tile_g_bytes(cfg) : 0;
   uint8_t *abase, *wbase;
   if (training) {
     // activations go to `saved`; the workspace holds the fp16 weight copies
+    // (and, with MLP tiling, one tile's G)
     if (!al16(saved)) return TSP_ERR_INVALID_ARG;
-    if (nwc > 0 && (!al16(ws) || ws_bytes < nwc)) return TSP_ERR_INVALID_ARG;
+    if (nwc + ntile > 0 && (!al16(ws) || ws_bytes < nwc + ntile)) return TSP_ERR_INVALID_ARG;
     abase = (uint8_t*)saved;
     wbase = (uint8_t*)ws;
   } else {
@@ -707,7 +763,7 @@ tsp_status tsp_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* 
   cudaStream_t st = S_(stream);
   if ((r = fill_wcache(cfg, WC, aw, mw, st)) != TSP_OK) return r;
   if ((r = attn_half(cfg, x_z, aw, WC, A.h, true, A, st)) != TSP_OK) return r;
-  return mlp_half(cfg, A.h, true, mw, WC, y_z, A, st);
+  return mlp_half(cfg, A.h, true, mw, WC, y_z, A, st, ntile ? wbase + nwc : nullptr);
 }
 
 tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z, const void* saved,
@@ -853,48 +909,96 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
     if ((r = fill_wcache(c, WC, aw, mw, st)) != TSP_OK) return r;
     // the upstream gradient in the internal fp16 operand type
     if ((r = launch_convert_bf16_f16(dy, W.dy16, S * d, st)) != TSP_OK) return r;
-    // dA|dB = SwiGLU'(dG), dG = dy W_2   (B operand W_2 read MN-major)
-    {
-      TcGemm g;
-      g.M = (int)S; g.N = I; g.K = d;
-      g.A[0] = W.dy16; g.lda[0] = d; g.kseg_len[0] = d;
-      g.b_mn = true; g.B[0] = WC.w2; g.ldb[0] = I;
-      g.epi = EPI_SWIGLU_BWD; g.name = "gemm_dgrad_w2_swiglu";
-      g.e1 = A.ab; g.e2 = (uint8_t*)A.ab + (size_t)I * e; g.lde = 2 * (int64_t)I;
-      g.out = W.dab; g.ldo = 2 * (int64_t)I;
-      g.out2 = (uint8_t*)W.dab + (size_t)I * e; g.ldo2 = 2 * (int64_t)I;
-      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
-    }
-    // dW_2 = dy^T G: K = tokens, i.e. every virtual rank's rows summed in fp32
-    {
-      TcGemm g;
-      g.M = d; g.N = I; g.K = (int)S;
-      g.a_mn = true; g.A[0] = W.dy16; g.lda[0] = d; g.kseg_len[0] = (int)S;
-      g.b_mn = true; g.B[0] = A.g; g.ldb[0] = I;
-      g.epi = EPI_F32; g.out = dw2; g.ldo = I; g.name = "gemm_wgrad_w2";
-      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
-    }
-    // dW_1 | dW_3 = [dA | dB]^T b (one launch, rows split between the outputs)
-    {
-      TcGemm g;
-      g.M = 2 * I; g.N = d; g.K = (int)S;
-      g.a_mn = true; g.A[0] = W.dab; g.lda[0] = 2 * (int64_t)I; g.kseg_len[0] = (int)S;
-      g.b_mn = true; g.B[0] = A.b; g.ldb[0] = d;
-      g.epi = EPI_F32; g.ldo = d; g.m_seg = I; g.name = "gemm_wgrad_w13";
-      g.outs[0] = dw1; g.outs[1] = dw3;
-      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
-    }
-    // db = dA W_1 + dB W_3 (two K segments), fp32
-    {
-      TcGemm g;
-      g.M = (int)S; g.N = d; g.K = 2 * I;
-      g.nks = 2;
-      g.A[0] = W.dab; g.A[1] = (uint8_t*)W.dab + (size_t)I * e;
-      g.lda[0] = g.lda[1] = 2 * (int64_t)I;
-      g.kseg_len[0] = g.kseg_len[1] = I;
-      g.b_mn = true; g.B[0] = WC.w1; g.B[1] = WC.w3; g.ldb[0] = g.ldb[1] = d;
-      g.epi = EPI_F32; g.out = W.db; g.ldo = d; g.name = "gemm_dgrad_w13";
-      if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+    // MLP backward, over the whole sequence or (cfg->mlp_tile) one row tile at
+    // a time; weight gradients sum over the tiles in fp32 (each tile lies in
+    // one virtual rank's rows, so this is still the sum over the ranks' rows)
+    const bool tiled = c->mlp_tile > 0;
+    const int64_t tile = tiled ? c->mlp_tile : S;
+    for (int64_t t0 = 0; t0 < S; t0 += tile) {
+      const bool first = t0 == 0;
+      const void* ab = A.ab;
+      const void* gg = A.g;
+      const uint8_t* b_t = (const uint8_t*)A.b + (size_t)t0 * d * e;
+      const uint8_t* dy_t = (const uint8_t*)W.dy16 + (size_t)t0 * d * e;
+      if (tiled) {
+        // recompute the tile's G and A|B from the saved b
+        TcGemm g;
+        g.M = (int)tile; g.N = I; g.K = d;
+        g.A[0] = b_t; g.lda[0] = d; g.kseg_len[0] = d;
+        g.B[0] = WC.w1; g.B[1] = WC.w3; g.ldb[0] = g.ldb[1] = d;
+        g.paired = true; g.name = "gemm_w13_recompute";
+        g.epi = EPI_SWIGLU; g.out = W.gt; g.ldo = I;
+        g.out2 = W.abt; g.ldo2 = 2 * (int64_t)I;
+        g.out3 = (uint8_t*)W.abt + (size_t)I * e; g.ldo3 = 2 * (int64_t)I;
+        if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+        ab = W.abt;
+        gg = W.gt;
+      }
+      // dA|dB = SwiGLU'(dG), dG = dy W_2   (B operand W_2 read MN-major)
+      {
+        TcGemm g;
+        g.M = (int)tile; g.N = I; g.K = d;
+        g.A[0] = dy_t; g.lda[0] = d; g.kseg_len[0] = d;
+        g.b_mn = true; g.B[0] = WC.w2; g.ldb[0] = I;
+        g.epi = EPI_SWIGLU_BWD; g.name = "gemm_dgrad_w2_swiglu";
+        g.e1 = ab; g.e2 = (const uint8_t*)ab + (size_t)I * e; g.lde = 2 * (int64_t)I;
+        g.out = W.dab; g.ldo = 2 * (int64_t)I;
+        g.out2 = (uint8_t*)W.dab + (size_t)I * e; g.ldo2 = 2 * (int64_t)I;
+        if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+      }
+      // a weight gradient of this tile: written by the first, added by the rest
+      auto wgrad_epi = [&](TcGemm& g, float* out, int64_t ldo) {
+        g.out = out; g.ldo = ldo;
+        if (first) {
+          g.epi = EPI_F32;
+        } else {
+          g.epi = EPI_RES; g.res = out; g.ldr = ldo; g.res_f32 = true; g.out_type = OUT_F32;
+        }
+      };
+      // dW_2 = dy^T G: K = tokens, i.e. every virtual rank's rows summed in fp32
+      {
+        TcGemm g;
+        g.M = d; g.N = I; g.K = (int)tile;
+        g.a_mn = true; g.A[0] = dy_t; g.lda[0] = d; g.kseg_len[0] = (int)tile;
+        g.b_mn = true; g.B[0] = gg; g.ldb[0] = I;
+        g.name = "gemm_wgrad_w2";
+        wgrad_epi(g, dw2, I);
+        if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+      }
+      if (!tiled) {
+        // dW_1 | dW_3 = [dA | dB]^T b (one launch, rows split between the outputs)
+        TcGemm g;
+        g.M = 2 * I; g.N = d; g.K = (int)S;
+        g.a_mn = true; g.A[0] = W.dab; g.lda[0] = 2 * (int64_t)I; g.kseg_len[0] = (int)S;
+        g.b_mn = true; g.B[0] = A.b; g.ldb[0] = d;
+        g.epi = EPI_F32; g.ldo = d; g.m_seg = I; g.name = "gemm_wgrad_w13";
+        g.outs[0] = dw1; g.outs[1] = dw3;
+        if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+      } else {
+        for (int part = 0; part < 2; ++part) {   // dW_1 from dA, dW_3 from dB
+          TcGemm g;
+          g.M = I; g.N = d; g.K = (int)tile;
+          g.a_mn = true; g.A[0] = (const uint8_t*)W.dab + (size_t)part * I * e;
+          g.lda[0] = 2 * (int64_t)I; g.kseg_len[0] = (int)tile;
+          g.b_mn = true; g.B[0] = b_t; g.ldb[0] = d;
+          g.name = "gemm_wgrad_w13";
+          wgrad_epi(g, part == 0 ? dw1 : dw3, d);
+          if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+        }
+      }
+      // db = dA W_1 + dB W_3 (two K segments), fp32
+      {
+        TcGemm g;
+        g.M = (int)tile; g.N = d; g.K = 2 * I;
+        g.nks = 2;
+        g.A[0] = W.dab; g.A[1] = (uint8_t*)W.dab + (size_t)I * e;
+        g.lda[0] = g.lda[1] = 2 * (int64_t)I;
+        g.kseg_len[0] = g.kseg_len[1] = I;
+        g.b_mn = true; g.B[0] = WC.w1; g.B[1] = WC.w3; g.ldb[0] = g.ldb[1] = d;
+        g.epi = EPI_F32; g.out = (float*)W.db + (size_t)t0 * d; g.ldo = d;
+        g.name = "gemm_dgrad_w13";
+        if ((r = gemm_tc(g, st)) != TSP_OK) return r;
+      }
     }
     // dh = dy + RMSNorm_2'(db)   (fp32, plus an fp16 copy for the GEMMs)
     if ((r = launch_rmsnorm_bwd((const float*)W.db, A.h, TY_F32, mw->g_mlp, A.rstd2, nullptr, dy,

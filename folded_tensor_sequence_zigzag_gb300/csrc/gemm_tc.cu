@@ -55,7 +55,7 @@ struct KParams {
   int nks;
   int kseg_kb[4];
   int nseg_n;
-  int rot_rows, rot_D;
+  int rot_rows, rot_D, rot_r0;
   int tiles_m, tiles_n, group_m;
   int n_tile;  // output columns per tile (256, or 128 for the paired SwiGLU tile)
   void* out;
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
         tile_of(p, t, mb, nb);
         const int m0 = mb * BM, n0 = nb * p.n_tile;
         int rank = 0;
-        if (p.rot_D > 0) rank = min(m0 / p.rot_rows, p.rot_D - 1);
+        if (p.rot_D > 0) rank = min(p.rot_r0 + m0 / p.rot_rows, p.rot_D - 1);
         int step = 0, sh = rank, kb = p.rot_D > 0 ? p.shard_kb[rank] : 0;
         for (int i = 0; i < p.nkb; ++i) {
           if (p.rot_D > 0) {
@@ -535,9 +535,11 @@ tsp_status gemm_tc(const TcGemm& g, cudaStream_t st) {
   // ring rotation over shard segments of K (k-block granularity: a block
   // that straddles a shard boundary belongs to the later shard)
   if (g.rot_D > 0) {
-    if (g.rot_D > 64 || g.rot_rows <= 0) return TSP_ERR_INVALID_ARG;
+    if (g.rot_D > 64 || g.rot_rows <= 0 || g.rot_r0 < 0 || g.rot_r0 >= g.rot_D)
+      return TSP_ERR_INVALID_ARG;
     kp->rot_D = g.rot_D;
     kp->rot_rows = g.rot_rows;
+    kp->rot_r0 = g.rot_r0;
     for (int s = 0; s <= g.rot_D; ++s) {
       const int64_t e = (int64_t)s * g.K / g.rot_D;
       kp->shard_kb[s] = (s == g.rot_D) ? kp->nkb : (int)(e / BK);
@@ -577,6 +579,8 @@ tsp_status gemm_tc(const TcGemm& g, cudaStream_t st) {
       break;
     case EPI_RES:
       if (!g.a_mn && !g.b_mn) return launch_t<EPI_RES, false, false, false>(*kp, grid, st, g.name);
+      // weight gradients added over sequence tiles (fp32 residual = the output)
+      if (g.a_mn && g.b_mn) return launch_t<EPI_RES, true, true, false>(*kp, grid, st, g.name);
       break;
     case EPI_SWIGLU:
       if (g.paired && !g.a_mn && !g.b_mn) return launch_t<EPI_SWIGLU, false, false, true>(*kp, grid, st, g.name);

@@ -17,9 +17,9 @@ enum { EPI_STORE = 0, EPI_RES = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_SWIGLU_BWD =
 // N range is split into segments of nseg_n columns with B pointer B[n / nseg_n]
 // (and one K segment).  paired: SwiGLU tile, B[0] = W_1 and B[1] = W_3, both
 // [N, K]; the output is G [M, N] = silu(A W_1^T) * (A W_3^T).
-// rot_D > 0: row tile of virtual rank r = m0 / rot_rows walks the K shards
-// (boundaries floor(s*K/rot_D), k-block granularity) in ring order
-// (r - t) mod rot_D.
+// rot_D > 0: row tile of virtual rank r = rot_r0 + m0 / rot_rows walks the K
+// shards (boundaries floor(s*K/rot_D), k-block granularity) in ring order
+// (r - t) mod rot_D (rot_r0: the rank of row 0, for a GEMM over a row tile).
 // Epilogues (out/out2/out3 row strides ldo/ldo2/ldo3, elements):
 //   EPI_STORE      out = C stored as out_type (OUT_F16 / OUT_BF16 / OUT_F32)
 //   EPI_RES        out = C + res, res bf16 or fp32 (res_f32), stored as out_type
@@ -39,7 +39,7 @@ struct TcGemm {
   int kseg_len[3] = {0, 0, 0};
   int nseg_n = 0;
   bool paired = false;
-  int rot_rows = 0, rot_D = 0;
+  int rot_rows = 0, rot_D = 0, rot_r0 = 0;
   int epi = EPI_STORE;
   void* out = nullptr;
   int64_t ldo = 0;

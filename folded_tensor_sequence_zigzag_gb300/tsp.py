@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libtsp.so")
 
 TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT = range(5)
 TSP_F32, TSP_BF16 = 0, 1
-TSP_OP_ATTN_FWD, TSP_OP_MLP_FWD, TSP_OP_BLOCK_FWD, TSP_OP_BLOCK_BWD = range(4)
+TSP_OP_ATTN_FWD, TSP_OP_MLP_FWD, TSP_OP_BLOCK_FWD, TSP_OP_BLOCK_BWD, TSP_OP_BLOCK_FWD_TRAIN = range(5)
 
 EXPORTED = ("tsp_zigzag_permute", "tsp_rmsnorm_fwd", "tsp_workspace_bytes", "tsp_saved_bytes",
             "tsp_attn_block_fwd", "tsp_gated_mlp_fwd", "tsp_block_fwd", "tsp_block_bwd",
@@ -39,7 +39,7 @@ class Cfg(ctypes.Structure):
     _fields_ = [("S", ctypes.c_int64), ("d", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("dh", ctypes.c_int32), ("inter", ctypes.c_int32), ("D", ctypes.c_int32),
                 ("eps", ctypes.c_float), ("dtype", ctypes.c_int32), ("rope_base", ctypes.c_float),
-                ("Hkv", ctypes.c_int32)]
+                ("Hkv", ctypes.c_int32), ("mlp_tile", ctypes.c_int32)]
 
 
 class AttnW(ctypes.Structure):
@@ -163,9 +163,11 @@ class BlockWeights:
                     1 if residual else 0)
 
 
-def make_cfg(S, d, H, inter, D, dtype: torch.dtype, eps=1e-6, rope_base=0.0, Hkv=0) -> Cfg:
+def make_cfg(S, d, H, inter, D, dtype: torch.dtype, eps=1e-6, rope_base=0.0, Hkv=0,
+             mlp_tile=0) -> Cfg:
     return Cfg(int(S), int(d), int(H), int(d // H), int(inter), int(D), float(eps),
-               TSP_BF16 if dtype == torch.bfloat16 else TSP_F32, float(rope_base), int(Hkv))
+               TSP_BF16 if dtype == torch.bfloat16 else TSP_F32, float(rope_base), int(Hkv),
+               int(mlp_tile))
 
 
 def _grad_shapes(cfg: Cfg) -> dict:
@@ -240,7 +242,8 @@ def block_fwd(cfg: Cfg, x_z, W: BlockWeights, saved=None, out=None, ws=None, str
     _require_cuda(x_z)
     out = torch.empty_like(x_z) if out is None else out
     if ws is None:
-        ws = _ws(workspace_bytes(cfg, TSP_OP_BLOCK_FWD), x_z.device)
+        op = TSP_OP_BLOCK_FWD if saved is None else TSP_OP_BLOCK_FWD_TRAIN
+        ws = _ws(workspace_bytes(cfg, op), x_z.device)
     aw, mw = W.attn(), W.mlp()
     _check(load().tsp_block_fwd(ctypes.byref(cfg), _ptr(x_z), ctypes.byref(aw), ctypes.byref(mw),
                                 _ptr(out), _ptr(saved), _ptr(ws), 0 if ws is None else ws.numel(),

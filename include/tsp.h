@@ -97,6 +97,15 @@ typedef struct {
    * query heads h = g*(H/Hkv) .. (g+1)*(H/Hkv)-1 share K/V head g.  W_K and
    * W_V are then [Hkv*dh, d].  The bf16 kernels need Hkv*dh % 256 == 0. */
   int32_t Hkv;
+  /* Sequence tiling of the gated MLP in the training step (TiledMLP-style;
+   * a variant, not on the pages): 0 = off; otherwise the rows per tile, a
+   * multiple of 128 that divides the 2c rows of a virtual rank.  The
+   * training forward then runs the MLP one tile at a time and keeps neither
+   * G nor the pre-activations for the backward, which recomputes them tile
+   * by tile from the saved normalised input, so the MLP's [S, inter]-sized
+   * buffers shrink to [tile, inter].  bf16 only (TSP_ERR_UNSUPPORTED for
+   * fp32). */
+  int32_t mlp_tile;
 } tsp_cfg;
 
 /* Attention-half weights: wq, wo [d, d]; wk, wv [Hkv*dh, d] ([d, d] for
@@ -112,8 +121,11 @@ typedef struct {
   int32_t add_residual;
 } tsp_mlp_w;
 
-/* Workspace queries (op selects the entry point). */
-enum { TSP_OP_ATTN_FWD = 0, TSP_OP_MLP_FWD = 1, TSP_OP_BLOCK_FWD = 2, TSP_OP_BLOCK_BWD = 3 };
+/* Workspace queries (op selects the entry point).  TSP_OP_BLOCK_FWD_TRAIN:
+ * the block forward with a `saved` buffer (activations go there; the
+ * workspace holds the weight copies and, with mlp_tile, one MLP tile). */
+enum { TSP_OP_ATTN_FWD = 0, TSP_OP_MLP_FWD = 1, TSP_OP_BLOCK_FWD = 2, TSP_OP_BLOCK_BWD = 3,
+       TSP_OP_BLOCK_FWD_TRAIN = 4 };
 
 /* Zigzag causal partitioning (section 2, attention bullet: "zigzag
  * partitioning balances the causal attention work").  Bit-exact row copy.
@@ -187,7 +199,9 @@ tsp_status tsp_gated_mlp_fwd_noalloc(const tsp_cfg* cfg, const void* h_z, const 
 /* Whole block forward: y_z = MLP-half(Attention-half(x_z)).  mlp_w->g_mlp
  * must be non-NULL and add_residual 1 (pre-norm block).  saved (nullable):
  * tsp_saved_bytes(cfg) bytes that receive the activations tsp_block_bwd
- * needs; NULL for inference.  ws: tsp_workspace_bytes(cfg, TSP_OP_BLOCK_FWD). */
+ * needs; NULL for inference.  ws: tsp_workspace_bytes(cfg, TSP_OP_BLOCK_FWD)
+ * for inference, tsp_workspace_bytes(cfg, TSP_OP_BLOCK_FWD_TRAIN) (or more)
+ * with `saved`. */
 tsp_status tsp_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* aw,
                          const tsp_mlp_w* mw, void* y_z, void* saved,
                          void* ws, size_t ws_bytes, void* stream);

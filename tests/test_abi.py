@@ -44,16 +44,20 @@ def test_strerror(lib):
 
 
 def _cfg(**kw):
-    base = dict(S=256, d=64, H=4, inter=128, D=4, dtype=tsp.TSP_F32, rope_base=0.0, Hkv=0)
+    base = dict(S=256, d=64, H=4, inter=128, D=4, dtype=tsp.TSP_F32, rope_base=0.0, Hkv=0,
+                mlp_tile=0)
     base.update(kw)
     return tsp.Cfg(base["S"], base["d"], base["H"], base.get("dh", base["d"] // base["H"]),
-                   base["inter"], base["D"], 1e-6, base["dtype"], base["rope_base"], base["Hkv"])
+                   base["inter"], base["D"], 1e-6, base["dtype"], base["rope_base"], base["Hkv"],
+                   base["mlp_tile"])
 
 
 @pytest.mark.parametrize("bad", [dict(S=250), dict(D=0), dict(D=65), dict(d=66), dict(dh=8),
                                  dict(inter=0), dict(dtype=7), dict(S=0), dict(d=2, H=1, D=4),
                                  dict(rope_base=-1.0), dict(d=60, H=4, rope_base=10000.0),
-                                 dict(Hkv=3), dict(Hkv=-1), dict(Hkv=8), dict(H=8, Hkv=1, D=16)])
+                                 dict(Hkv=3), dict(Hkv=-1), dict(Hkv=8), dict(H=8, Hkv=1, D=16),
+                                 dict(mlp_tile=-128), dict(mlp_tile=64, S=512, D=2),
+                                 dict(mlp_tile=384, S=2048, D=4, dtype=tsp.TSP_BF16)])
 def test_invalid_cfg_rejected_without_launch(lib, bad):
     cfg = _cfg(**bad)
     assert lib.tsp_workspace_bytes(ctypes.byref(cfg), tsp.TSP_OP_BLOCK_FWD) == 0
@@ -158,3 +162,26 @@ def test_decode_arguments_checked_without_launch(lib):
     # prefill: the cache must hold the prompt
     assert lib.tsp_block_prefill(ctypes.byref(cfg), ok, ctypes.byref(aw), ctypes.byref(mw), ok, ok,
                                  255, ok, big, None) == tsp.TSP_ERR_INVALID_ARG
+
+
+def test_mlp_tiling_configuration(lib):
+    """Tiles of 128-multiples that divide a virtual rank's rows; bf16 only;
+    the training record loses G and A|B, the backward workspace shrinks."""
+    big = dict(S=16384, d=4096, H=32, inter=11008, D=8, dtype=tsp.TSP_BF16)
+    plain, tiled = _cfg(**big), _cfg(mlp_tile=1024, **big)
+    S, I = 16384, 11008
+    saved_gap = lib.tsp_saved_bytes(ctypes.byref(plain)) - lib.tsp_saved_bytes(ctypes.byref(tiled))
+    assert saved_gap == S * I * 2 + S * 2 * I * 2            # G and A|B, fp16
+    bwd_plain = lib.tsp_workspace_bytes(ctypes.byref(plain), tsp.TSP_OP_BLOCK_BWD)
+    bwd_tiled = lib.tsp_workspace_bytes(ctypes.byref(tiled), tsp.TSP_OP_BLOCK_BWD)
+    assert bwd_plain - bwd_tiled == (S - 1024) * 2 * I * 2 - 1024 * 3 * I * 2
+    train = lib.tsp_workspace_bytes(ctypes.byref(tiled), tsp.TSP_OP_BLOCK_FWD_TRAIN)
+    assert train - lib.tsp_workspace_bytes(ctypes.byref(plain), tsp.TSP_OP_BLOCK_FWD_TRAIN) == 1024 * I * 2
+    # fp32: valid shape, not taken by the tiled path
+    f32 = _cfg(mlp_tile=128, S=1024, d=64, H=4, inter=128, D=4)
+    assert lib.tsp_saved_bytes(ctypes.byref(f32)) == 0
+    ok = ctypes.c_void_p(0x10000)
+    aw = tsp.AttnW(ok, ok, ok, ok, ok)
+    mw = tsp.MlpW(ok, ok, ok, ok, 1)
+    assert lib.tsp_block_fwd(ctypes.byref(f32), ok, ctypes.byref(aw), ctypes.byref(mw), ok, ok, ok,
+                             1 << 40, None) == tsp.TSP_ERR_UNSUPPORTED

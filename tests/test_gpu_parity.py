@@ -207,10 +207,10 @@ def test_7b_block_fwd_sampled_rows(S):
 
 # ------------------------------------------------------------------ backward
 
-def _run_bwd(shape, inp, dtype, rope_base=0.0):
+def _run_bwd(shape, inp, dtype, rope_base=0.0, mlp_tile=0):
     dev = "cuda"
     cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps, rope_base,
-                       shape.Hkv)
+                       shape.Hkv, mlp_tile)
     W = tsp.BlockWeights.from_dict(inp, dev)
     xz = tsp.zigzag_permute(inp["x"].to(dev), shape.D)
     dyz = tsp.zigzag_permute(inp["dy"].to(dev), shape.D)
@@ -262,15 +262,18 @@ def test_bf16_backward_small(S, d, H, I, D):
 
 def test_7b_fwd_bwd_S8192_all_outputs():
     """Config-5 shapes (d=4096, 32x128 heads, inter=11008, D=8) at S=8192:
-    every output of the training step against the dense float64 backward."""
+    every output of the training step against the dense float64 backward,
+    once as is and once with the MLP in sequence tiles of 512 rows
+    (recomputed in the backward, weight gradients summed over 16 tiles)."""
     shape = BlockShape(S=8192, d=4096, H=32, inter=11008, D=8)
     inp = make_block_inputs(shape, torch.bfloat16, seed=0, with_dy=True)
-    y, g = _run_bwd(shape, inp, torch.bfloat16)
     yref, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
-    assert_bf16_close(y, yref, "y (S=8192)")
     ref = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
-    for k, v in ref.items():
-        assert_bf16_close(g[k], v, f"{k} (S=8192)")
+    for tile in (0, 512):
+        y, g = _run_bwd(shape, inp, torch.bfloat16, mlp_tile=tile)
+        assert_bf16_close(y, yref, f"y (S=8192, mlp_tile={tile})")
+        for k, v in ref.items():
+            assert_bf16_close(g[k], v, f"{k} (S=8192, mlp_tile={tile})")
 
 
 def test_long_context_training_step_S262144_tail():
@@ -409,3 +412,20 @@ def test_7b_gqa8_training_step_S8192_sampled():
     assert g["dwk"].shape == (1024, 4096) and g["dwv"].shape == (1024, 4096)
     for k in ("dwq", "dwk", "dwv", "dwo", "dw1", "dw3", "dw2", "dg_attn", "dg_mlp"):
         assert torch.isfinite(g[k]).all(), k
+
+
+# ------------------------------------------------------------------ MLP sequence tiling (variant)
+
+@pytest.mark.parametrize("tile,base,Hkv", [(128, 0.0, 0), (256, 10000.0, 2)])
+def test_bf16_mlp_tiling_forward_backward(tile, base, Hkv):
+    """The training step with the MLP run in sequence tiles (recomputed in the
+    backward) against the oracle: every output."""
+    shape = BlockShape(S=4096, d=512, H=4, inter=768, D=8, Hkv=Hkv)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=12, with_dy=True)
+    y, g = _run_bwd(shape, inp, torch.bfloat16, rope_base=base, mlp_tile=tile)
+    ref_in = _with_rope(inp, base)
+    yref, _ = O.block_fwd(inp["x"], ref_in, shape.H, shape.eps)
+    assert_bf16_close(y, yref, f"tiled y (tile={tile})")
+    ref = O.block_bwd(inp["x"], ref_in, inp["dy"], shape.H, shape.eps)
+    for k, v in ref.items():
+        assert_bf16_close(g[k], v, f"tiled {k} (tile={tile})")
