@@ -352,19 +352,24 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
           }
           // probabilities first (fp16 pairs), so the scores' registers are free
           // before O is touched
+          // the exponent in fp32, rounded to fp16 pairs; 2^x of both halves in
+          // one MUFU operation, which is already the fp16 P the PV MMA takes
           const float neg_m = -m_used;
-          float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // partial row sums
+          uint32_t ps[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};   // partial row sums (fp16 pairs)
           uint32_t pk[2][32];   // column i of P_x holds keys 2i (low half) and 2i+1
 #pragma unroll
           for (int q = 0; q < 4; ++q)
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
-              const float p0v = ex2_approx(fmaf(__uint_as_float(sr[q][e]), a.scale_log2, neg_m));
-              const float p1v = ex2_approx(fmaf(__uint_as_float(sr[q][e + 1]), a.scale_log2, neg_m));
-              ps[(e >> 1) & 7] += p0v + p1v;
-              pk[q >> 1][(q & 1) * 16 + (e >> 1)] = pack_f16(p0v, p1v);
+              const float x0 = fmaf(__uint_as_float(sr[q][e]), a.scale_log2, neg_m);
+              const float x1 = fmaf(__uint_as_float(sr[q][e + 1]), a.scale_log2, neg_m);
+              const uint32_t p2 = ex2_approx_f16x2(pack_f16(x0, x1));
+              pk[q >> 1][(q & 1) * 16 + (e >> 1)] = p2;
+              ps[(e >> 1) & 7] = hadd2_u32(ps[(e >> 1) & 7], p2);   // 8 terms a partial
             }
-          const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+          float sum = 0.f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) sum += f16_lo(ps[k]) + f16_hi(ps[k]);
           // PV_x(j-1) must have finished before P_x is overwritten or O_x rescaled
           if (j > 0) {
             okl = mbar_wait(o_done(x), (c_now - 1) & 1u, a.status, abort_flag, a.limit_ns);
