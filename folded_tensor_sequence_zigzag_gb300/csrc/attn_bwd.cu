@@ -120,6 +120,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
+// GROUPED = false: one query head per K/V head (G = 1), the loops' group
+// arithmetic folded away at compile time
+template <bool GROUPED>
 __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_constant__ TcBwdArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
@@ -149,6 +152,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
   // one CTA per (K/V head g, key-tile pair); its query iterations run over the
   // G query heads of the group, head-major, so dK and dV add up in TMEM
   const int g = blockIdx.y;
+  const int G = GROUPED ? a.G : 1;
   const int pair = blockIdx.x;
   const int r = pair / a.n_kt, t = pair - r * a.n_kt;
   int64_t k0s[2];
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
     for (int tile = 0; tile < 2; ++tile) {
       const int64_t k0 = k0s[tile];
       const int nqh = (int)((a.S - k0) / BR);   // query tiles per head
-      const int nq = nqh * a.G;                  // query iterations of this key tile
+      const int nq = nqh * G;                  // query iterations of this key tile
       const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
       if (warp == WARP_PROD) {
         // ------------------------------------------------------------ producer
@@ -219,8 +223,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           for (int j = 0; j < nq; ++j) {
             const uint32_t cur = it + j, st = qst(cur);
             if (!mbar_wait(qd_empty(st), qph(cur) ^ 1u, a.status, abort_flag, a.limit_ns)) break;
-            const int gi = j / nqh, jj = j - gi * nqh;
-            const int h = g * a.G + gi;
+            const int gi = GROUPED ? j / nqh : 0, jj = j - gi * nqh;
+            const int h = g * G + gi;
             const int64_t qrow = zz_row_of_pos(k0 + (int64_t)jj * BR, a.c, a.D);
             const uint32_t fb = qd_full(st);
             mbar_arrive_expect_tx(fb, 2 * TILE_BYTES + 2 * BR * 4);
@@ -330,7 +334,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
     for (int tile = 0; tile < 2; ++tile) {
       const int64_t k0 = k0s[tile];
       const int nqh = (int)((a.S - k0) / BR);
-      const int nq = nqh * a.G;
+      const int nq = nqh * G;
       {
         // ------------------------------------------------------------ dQ drain (thread = dh)
         // all 128 query columns are read before the TMEM columns are released, so
@@ -352,9 +356,9 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(dq_empty);   // dQ^T(cur) read: its columns may take S^T(cur+1)
-          const int gi = j / nqh, jj = j - gi * nqh;
+          const int gi = GROUPED ? j / nqh : 0, jj = j - gi * nqh;
           const int64_t qrow = zz_row_of_pos(k0 + (int64_t)jj * BR, a.c, a.D);
-          float* dst = a.dq_acc + qrow * a.d + (g * a.G + gi) * DH + dh;
+          float* dst = a.dq_acc + qrow * a.d + (g * G + gi) * DH + dh;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -370,7 +374,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
     for (int tile = 0; tile < 2; ++tile) {
       const int64_t k0 = k0s[tile];
       const int nqh = (int)((a.S - k0) / BR);
-      const int nq = nqh * a.G;
+      const int nq = nqh * G;
       const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
       {
         // ------------------------------------------------------------ P, dS (thread = key)
@@ -388,7 +392,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           const float* L = sLD + st * 2 * BR;
           const float* Dl = L + BR;
           // query tile == key tile (the first of each head): key index > query index is masked
-          const bool diag = j % nqh == 0;
+          const bool diag = GROUPED ? j % nqh == 0 : j == 0;
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
             const int qb = half * 64 + ch * 32;    // this chunk's 32 query columns
@@ -589,23 +593,24 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
   a->scale_log2 = 1.4426950408889634f * a->scale;
   a->status = status_word();
   a->limit_ns = wait_limit_ns();
-  static bool attr = false;
-  static int launch_regs = 0;
-  if (!attr) {
-    TSP_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_tc_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM));
+  const bool grouped = Hkv != H;
+  auto kern = grouped ? attn_bwd_tc_kernel<true> : attn_bwd_tc_kernel<false>;
+  static bool attr[2] = {false, false};
+  static int launch_regs[2] = {0, 0};
+  if (!attr[grouped]) {
+    TSP_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM));
     cudaFuncAttributes fa;
-    TSP_CUDA_TRY(cudaFuncGetAttributes(&fa, attn_bwd_tc_kernel));
-    launch_regs = fa.numRegs;
-    attr = true;
+    TSP_CUDA_TRY(cudaFuncGetAttributes(&fa, kern));
+    launch_regs[grouped] = fa.numRegs;
+    attr[grouped] = true;
   }
   // setmaxnreg.inc would wait forever if the split exceeded the launch allocation
-  if ((int64_t)launch_regs * NTHR < (int64_t)launch_regs * 256 + 128 * (REG_DRAIN + REG_CTRL))
-    return TSP_ERR_UNSUPPORTED;
+  const int64_t lr = launch_regs[grouped];
+  if (lr * NTHR < lr * 256 + 128 * (REG_DRAIN + REG_CTRL)) return TSP_ERR_UNSUPPORTED;
   dim3 grid((unsigned)(D * a->n_kt), (unsigned)Hkv);
   {
     Prof prof("attn_bwd", st);
-    attn_bwd_tc_kernel<<<grid, NTHR, SMEM, st>>>(*a);
+    kern<<<grid, NTHR, SMEM, st>>>(*a);
     TSP_CUDA_TRY(cudaGetLastError());
   }
   Prof prof("attn_bwd_dq_convert", st);
