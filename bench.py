@@ -138,14 +138,17 @@ MEASURED_TRAFFIC = {
     # (kernel, workload): (bytes per launch, source file, sha256 of the source);
     # first (cold) launch of the process, from the captures summarised under profiles/
     ("gemm_w13_swiglu", "fwd16k"): (
-        1576974000 + 347252224, "folded_tensor_sequence_zigzag_gb300/csrc/gemm_tc.cu",
-        "6746a2f317f37a9b17dbeb4daeab63797c4d6d5208f6bb042b02d22c3a573bf4"),
+        1577046000 + 347930368, "folded_tensor_sequence_zigzag_gb300/csrc/gemm_tc.cu",
+        "3881b04ac6ec4b6d60b752665348644c2ab5d1b8a18012c11b284893e04bf2a6"),
     ("attn_fwd", "fwd16k"): (
-        423326976 + 119269888, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
-        "cf9ba7748c5011b937e86fd91099f1f659aa90ce593c79bc15d0b984fe17529e"),
+        425805056 + 119521536, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
+        "7edd34168c2d0a321503026701a6e2e8b7eaed540464f7320b618f4bb29f99c1"),
     ("attn_bwd", "fwdbwd8k"): (
-        408379392 + 229071616, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
-        "8173d044cd43f05ef9db6dab64e8a65e29e59339a80da34bc75f7d5cf7436d9d"),
+        408193536 + 229216512, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
+        "c1380ccc41c0897044340f2c6ba425bb3690f1b8f465510c50b42bc22ef0aeb0"),
+    ("decode_attn", "decode16k"): (
+        268706304 + 4893440, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
+        "324d3b64ef7cf435ebebb6a65ce5e1f784c76d7bd9f11e5d90f565bdf66432ba"),
 }
 
 

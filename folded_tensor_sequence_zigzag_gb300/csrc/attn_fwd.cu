@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
+  const int kcol = a.d + (h / a.G) * DH;   // K columns of this head's K/V head; V at + dkv
   const int pair = blockIdx.x;
   const int r = pair / a.n_blocks, t = pair - r * a.n_blocks;
   const int64_t p0_mirror =
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
                 break;
               }
               const uint32_t dst = base + OFF_KV + s * TILE_BYTES;
-              const int col = a.d + kv * a.dkv + (h / a.G) * DH;
+              const int col = kcol + kv * a.dkv;
               mbar_arrive_expect_tx(slot_full(s), TILE_BYTES);
               tma_load_2d(dst, &a.tm, col, krow, slot_full(s));
               tma_load_2d(dst + BOX_BYTES, &a.tm, col + 64, krow, slot_full(s));
