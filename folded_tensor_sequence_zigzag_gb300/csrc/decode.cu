@@ -345,6 +345,12 @@ __device__ __forceinline__ void split_rows(const AttnArgs& a, int s, int64_t& r0
   }
 }
 
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 fills zeros
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_nc16(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -390,7 +396,7 @@ template <> struct VReg<float, 1> {
 // whole warp.  No shared-memory staging of K/V; the warps' partial softmax
 // results are merged in shared memory.
 template <typename CT, int DH>
-__global__ void __launch_bounds__(kAttnWarps * 32, 3) decode_attn_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(kAttnWarps * 32, 4) decode_attn_kernel(const __grid_constant__ AttnArgs a) {
   constexpr int E = 16 / sizeof(CT);          // elements per 16-byte piece
   constexpr int LPR = DH / E;                 // lanes per K row (a piece each)
   constexpr int RPI = 32 / LPR;               // K rows per warp-wide load
@@ -400,6 +406,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) decode_attn_kernel(const _
   __shared__ __align__(16) float qs[kQB][DH];
   __shared__ __align__(16) float pw[kAttnWarps][kQB][32];
   __shared__ __align__(16) float ro[kAttnWarps][kQB][DH];
+  __shared__ __align__(16) CT vs[kAttnWarps][32][DH];   // each warp's V rows (cp.async)
   __shared__ float2 rml[kAttnWarps][kQB];
 
   // the nz CTAs of one (K/V head, split) are neighbours in x: they run
@@ -416,22 +423,23 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) decode_attn_kernel(const _
 
   const int kl = lane % LPR, kh = lane / LPR;   // piece and row of this lane in a K load
   uint4 kreg[KIT];
-  VReg<CT, VPL> vreg[32];
   if (wactive) {
 #pragma unroll
     for (int it = 0; it < KIT; ++it) {
       const int64_t row = wr0 + it * RPI + kh;
       kreg[it] = ld_nc16(base + (row < r1 ? row : r0) * a.ldkv + kl * E);
     }
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const int64_t row = wr0 + k < r1 ? wr0 + k : r0;   // rows past the split: p = 0
-      if (lane < VLANES)
-        vreg[k].load(base + row * a.ldkv + a.dkv + lane * VPL);
-      else
-        vreg[k].zero();
+    // V rows -> this warp's shared-memory slice without holding registers;
+    // rows past the split read as zeros (their p is 0)
+    for (int i = lane; i < 32 * LPR; i += 32) {
+      const int k = i / LPR, pc = i - k * LPR;
+      const bool in = wr0 + k < r1;
+      cp_async16(smem_u32(&vs[warp][k][pc * E]), base + (in ? wr0 + k : r0) * a.ldkv + a.dkv + pc * E,
+                 in ? 16u : 0u);
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
   }
+  bool v_ready = false;
 
   // query rows of this K/V head: qr = (head g*G + gi, token t), gi = qr / T;
   // this CTA takes rows [z*qpc, min(QR, (z+1)*qpc))
@@ -496,6 +504,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) decode_attn_kernel(const _
           if (lane == 0) rml[warp][i] = make_float2(m, l);
         }
       }
+      if (!v_ready) {   // this lane's V copies, then the whole warp's, are in place
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        v_ready = true;
+      }
       __syncwarp();
       // O piece = P V over the warp's keys: lane = V columns
       float o[kQB][VPL];
@@ -507,7 +519,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) decode_attn_kernel(const _
       for (int k4 = 0; k4 < 32; k4 += 4) {
         float vf[4][VPL];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) vreg[k4 + kk].get(vf[kk]);
+        for (int kk = 0; kk < 4; ++kk) {
+          VReg<CT, VPL> vr;
+          if (lane < VLANES)
+            vr.load(&vs[warp][k4 + kk][lane * VPL]);
+          else
+            vr.zero();
+          vr.get(vf[kk]);
+        }
 #pragma unroll
         for (int i = 0; i < kQB; ++i) {
           if (i < nq) {
