@@ -147,8 +147,8 @@ MEASURED_TRAFFIC = {
         408193536 + 229216512, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
         "c1380ccc41c0897044340f2c6ba425bb3690f1b8f465510c50b42bc22ef0aeb0"),
     ("decode_attn", "decode16k"): (
-        268706304 + 4893440, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
-        "324d3b64ef7cf435ebebb6a65ce5e1f784c76d7bd9f11e5d90f565bdf66432ba"),
+        268699136 + 4189184, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
+        "cb8b1e50beb6bc5f5bacb526fcf64e98f3c688cf02cc585e4d0aa51bcb4bc99c"),
 }
 
 
