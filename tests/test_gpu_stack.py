@@ -50,9 +50,10 @@ def _stack_inputs(shape, dtype, L, seed):
     return inp["x"], inp["dy"], layers
 
 
-def _run_stack(shape, dtype, x, dy, layers, training):
+def _run_stack(shape, dtype, x, dy, layers, training, rope_base=0.0, mlp_tile=0):
     dev = "cuda"
-    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps)
+    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, dtype, shape.eps,
+                       rope_base, shape.Hkv, mlp_tile)
     Ws = [tsp.BlockWeights.from_dict(w, dev) for w in layers]
     xz = tsp.zigzag_permute(x.to(dev), shape.D)
     L = len(layers)
@@ -106,6 +107,25 @@ def test_bf16_stack_matches_oracle(training):
             for k, v in g_ref[l].items():
                 assert_stack_bf16_close(got["grads"][l][k].cpu(), v, 2 * (L - 1),
                                         f"bf16 stack layer {l} {k}")
+
+
+def test_bf16_stack_with_every_variant_matches_oracle():
+    """Two layers with grouped K/V heads, rotary embedding and the MLP in
+    sequence tiles together: forward and every gradient."""
+    L, base = 2, 10000.0
+    shape = BlockShape(S=2048, d=512, H=4, inter=512, D=4, Hkv=2)
+    x, dy, layers = _stack_inputs(shape, torch.bfloat16, L, seed=21)
+    got = _run_stack(shape, torch.bfloat16, x, dy, layers, True, rope_base=base, mlp_tile=256)
+    ref_layers = [dict(w, rope_base=base) for w in layers]
+    yref = O.stack_fwd(x, ref_layers, shape.H, shape.eps, store="bf16")
+    assert_stack_bf16_close(got["y"].float().cpu(), yref, L - 1, "variant stack y")
+    dx_ref, g_ref = O.stack_bwd(x, ref_layers, dy, shape.H, shape.eps, store="bf16")
+    assert_stack_bf16_close(got["dx"].cpu(), dx_ref, 2 * (L - 1), "variant stack dx")
+    for l in range(L):
+        for k, v in g_ref[l].items():
+            assert got["grads"][l][k].shape == v.shape, (l, k)
+            assert_stack_bf16_close(got["grads"][l][k].cpu(), v, 2 * (L - 1),
+                                    f"variant stack layer {l} {k}")
 
 
 def test_stack_rejects_bad_arguments():
