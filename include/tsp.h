@@ -249,8 +249,10 @@ tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z,
  *   copies).  ws: tsp_decode_workspace_bytes(cfg, T, kv_rows_cap).
  * Errors: TSP_ERR_INVALID_ARG for NULL/misaligned pointers, T out of range,
  *   n_cached out of range, a short workspace or cache; TSP_ERR_UNSUPPORTED
- *   for shapes the decode kernels do not take (dh not dividing 256 into
- *   whole column pairs, d or inter not a multiple of 8 (bf16) / 4 (fp32)). */
+ *   for shapes the decode kernels do not take (head width dh other than 64
+ *   or 128 in bf16, or 16, 32 or 64 in fp32; d or inter not a multiple of 8
+ *   (bf16) / 4 (fp32); T * max(d, inter) elements above 200 KB of shared
+ *   memory). */
 #define TSP_DECODE_MAX_T 8
 size_t tsp_kv_cache_bytes(const tsp_cfg* cfg, int64_t kv_rows_cap);
 size_t tsp_decode_workspace_bytes(const tsp_cfg* cfg, int32_t T, int64_t kv_rows_cap);
