@@ -102,3 +102,16 @@ def test_7b_decode_after_16k_prompt(Hkv, base, steps):
         S, dict(d=4096, H=32, inter=11008, D=8, Hkv=Hkv), torch.bfloat16, steps, base, seed=11)
     for k, (got, want) in enumerate(zip(outs, _oracle_steps(ref_in, S, steps, shape.H, shape.eps))):
         assert_bf16_close(got, want, f"7B decode step {k} (T={steps[k]}, Hkv={Hkv or 32})")
+
+
+def test_fp32_decode_crosses_split_boundaries():
+    """130 tokens decoded 8 at a time (the last call 2) after a prompt whose
+    ranks own 64 rows each (D=8): the decoded rows cross the 128-row split
+    boundary of the appended region, with grouped K/V heads and RoPE on."""
+    S, steps = 512, [8] * 16 + [2]
+    shape, ref_in, _, outs, cache, cfg = _run(
+        S, dict(d=64, H=4, inter=128, D=8, Hkv=2), torch.float32, steps, 500.0, seed=77, spare=0)
+    assert cache.n == cache.rows_cap
+    want = _oracle_steps(ref_in, S, steps, shape.H, shape.eps)
+    for k, (got, w) in enumerate(zip(outs, want)):
+        assert_f32_close(got, w, f"decode step {k} (T={steps[k]})")
