@@ -18,9 +18,10 @@ activations > 1 GiB) is larger than L2, so no explicit flush is needed.
 With N > 1 (torchrun, one rank per GPU) every rank runs its own replica
 ("replicas only": the block has no data-path exchange on one node's GPUs in
 this form); value = all ranks' tokens / max-over-ranks time.
-The reference arm is the CPU float64 oracle, timed on this host's cores on a
-bounded prefix of the same workload and scaled to the full workload by the
-algorithmic flop ratio.
+The reference arm is the CPU float64 oracle, timed on this host's cores, one
+bounded sample of the same workload per step (cpu_sample: for the forward
+workloads a virtual rank's step of the TSP schedule on mirrored row pairs,
+which carry exactly the block's average work per token).
 """
 from __future__ import annotations
 
@@ -88,6 +89,7 @@ def decode_bytes(name, d, inter, dkv, n_rows, T=DECODE_T):
     return table.get(name)
 
 DEFAULT_WORKLOAD = "fwd16k"
+NOMINAL_BF16_TFLOPS = 2250.0   # GB300 rated dense bf16 (context; the measured peaks are the denominators)
 
 
 def block_flops(S, d, inter, kind, dkv=None):
@@ -244,43 +246,97 @@ def reduce_max(value: float, world: int, device=None) -> float:
 
 _SAMPLE_CACHE = {}
 
+# rows (mirrored pairs per sample: 2 * CPU_PAIRS tokens) of one oracle sample
+# of a forward workload, shared by the GPU arm's cpu_baseline and every step
+# of the reference arm so that the two legs time the same thing
+CPU_PAIRS = 512
+# causal prefix of a training-step sample (the oracle's backward is unsharded)
+CPU_PREFIX_BWD = 512
+# rows of an MLP-only sample (the MLP is row-local: every row costs the same)
+CPU_ROWS_MLP = 2048
 
-def oracle_sample(S_full, d, H, inter, D, kind, budget_rows, variant=None):
-    """Time the float64 oracle on a causal prefix of the workload.
 
-    The first `rows` tokens of a causal block only depend on each other, so
-    the oracle's block forward on that prefix is a self-contained slice of the
-    same workload; its time is scaled to the full workload by the algorithmic
-    flop ratio.  Returns (seconds_for_full_workload_estimate, description).
-    """
-    import numpy as np  # noqa: F401
+def _oracle_inputs(S, d, H, inter, kind, variant):
     import torch
-    import oracle.tsp_oracle as O
     from folded_tensor_sequence_zigzag_gb300.inputs import BlockShape, make_block_inputs
-    rows = budget_rows
     variant = variant or {}
-    key = (rows, d, H, inter, kind, tuple(sorted(variant.items())))
+    key = (S, d, H, inter, kind, tuple(sorted(variant.items())))
     if key not in _SAMPLE_CACHE:
-        shape = BlockShape(S=rows, d=d, H=H, inter=inter, D=1, Hkv=variant.get("Hkv", 0))
         _SAMPLE_CACHE.clear()
-        _SAMPLE_CACHE[key] = make_block_inputs(shape, torch.bfloat16, seed=0,
-                                               with_dy=(kind == "fwdbwd"), mlp_only=(kind == "mlp"))
+        shape = BlockShape(S=S, d=d, H=H, inter=inter, D=1, Hkv=variant.get("Hkv", 0))
+        inp = make_block_inputs(shape, torch.bfloat16, seed=0, with_dy=(kind == "fwdbwd"),
+                                mlp_only=(kind == "mlp"))
         if variant.get("rope_base"):
-            _SAMPLE_CACHE[key]["rope_base"] = variant["rope_base"]
-    inp = _SAMPLE_CACHE[key]
-    dkv = variant.get("Hkv", H) * (d // H)
-    t0 = time.perf_counter()
+            inp["rope_base"] = variant["rope_base"]
+        _SAMPLE_CACHE[key] = {"inp": inp}
+    return _SAMPLE_CACHE[key]
+
+
+def cpu_sample(S, D, d, H, inter, kind, variant, r=0):
+    """Time the float64 oracle on one bounded sample of the workload.
+
+    Returns (tokens, seconds, equiv_seconds, exact, description): the sample
+    took `seconds`; `equiv_seconds` is the time `tokens` of the workload's
+    tokens take at that rate, so tokens / equiv_seconds is the oracle's
+    throughput on the workload.  `exact`: the sampled tokens carry exactly the
+    workload's average work per token (equiv_seconds == seconds); otherwise
+    equiv_seconds is an estimate scaled by the algorithmic flop ratio.
+
+    Forward: virtual rank r's step of the TSP schedule on CPU_PAIRS mirrored
+    row pairs of its zigzag rows -- its own Q/K/V projection shard by shard,
+    causal attention against the gathered K/V of the whole sequence, the W_O
+    shard loop and the MLP ring.  Every mirrored pair attends S + 1 keys, so
+    the sample's work per token is the block's average exactly.  The gathered
+    K/V (what the other ranks' projections and the all-gather deliver) is
+    prepared once, untimed.
+    MLP only: the oracle's MLP on the first CPU_ROWS_MLP rows (row-local).
+    Forward + backward: the oracle's (unsharded) backward on a causal prefix
+    of CPU_PREFIX_BWD tokens, scaled by the algorithmic flop ratio (an
+    estimate, labelled as such).
+    """
+    import numpy as np
+    import oracle.tsp_oracle as O
+    variant = variant or {}
+    H_kv = variant.get("Hkv", H)
+    dkv = H_kv * (d // H)
+    c = S // (2 * D)
     if kind == "mlp":
+        ent = _oracle_inputs(CPU_ROWS_MLP, d, H, inter, kind, variant)
+        inp = ent["inp"]
+        t0 = time.perf_counter()
         O.mlp_fwd(inp["x"], inp, 1e-6, norm=False, residual=False)
-    elif kind == "fwd":
-        O.block_fwd(inp["x"], inp, H, 1e-6)
-    else:
+        dt = time.perf_counter() - t0
+        return CPU_ROWS_MLP, dt, dt, True, (f"oracle (numpy float64) MLP on {CPU_ROWS_MLP} rows "
+                                        f"(row-local: every row carries the same work)")
+    if kind == "fwdbwd":
+        rows = CPU_PREFIX_BWD
+        inp = _oracle_inputs(rows, d, H, inter, kind, variant)["inp"]
+        t0 = time.perf_counter()
         O.block_bwd(inp["x"], inp, inp["dy"], H, 1e-6)
+        dt = time.perf_counter() - t0
+        scale = block_flops(S, d, inter, kind, dkv) / block_flops(rows, d, inter, kind, dkv)
+        return rows, dt, dt * rows * scale / S, False, (
+            f"oracle (numpy float64) training step on the first {rows} tokens, time scaled to "
+            f"the workload by algorithmic flops x{scale:.1f} (an estimate)")
+    ent = _oracle_inputs(S, d, H, inter, kind, variant)
+    inp = ent["inp"]
+    if "x64" not in ent:
+        ent["x64"] = O.f64(inp["x"])
+        ent["kv"] = O.gather_kv(inp["x"], inp, H, D, 1e-6)
+    x64 = ent["x64"]
+    K_all, V_all = ent["kv"]
+    n = min(c, CPU_PAIRS)
+    p = O.mirrored_rows(S, D, r, n)
+    t0 = time.perf_counter()
+    Q_r, _, _ = O.rank_project(x64[p], p, inp, H, D, 1e-6)
+    O.rank_fwd(r, x64[p], p, Q_r, K_all, V_all, inp, H, D, 1e-6, c)
     dt = time.perf_counter() - t0
-    scale = block_flops(S_full, d, inter, kind, dkv) / block_flops(rows, d, inter, kind, dkv)
-    desc = (f"oracle (numpy float64) on the first {rows} tokens of the workload "
-            f"({kind}), scaled by algorithmic flops x{scale:.1f}")
-    return dt * scale, dt, desc
+    return 2 * n, dt, dt, True, (
+        f"oracle (numpy float64), virtual rank {r}'s step of the TSP schedule on {n} mirrored "
+        f"row pairs of its zigzag rows ({2 * n} tokens: own Q/K/V projection by shards, causal "
+        f"attention against the gathered K/V of all {S} tokens, W_O shard loop, MLP ring); each "
+        f"pair attends S+1 keys, so the sample carries the block's average work per token; "
+        f"gathered K/V prepared untimed")
 
 
 def cpu_cores():
@@ -300,26 +356,30 @@ def run_reference(args):
     L = LAYERS.get(args.workload, 1)
     if kind == "decode":
         return run_reference_decode(args, rank, world)
-    rows = args.ref_rows or (256 if kind == "fwdbwd" else 512)
-    for _ in range(args.warmup):
-        oracle_sample(S, d, H, inter, D, kind, rows, VARIANTS.get(args.workload))
-    times = []
-    desc = ""
-    for _ in range(args.steps):
-        est, _, desc = oracle_sample(S, d, H, inter, D, kind, rows, VARIANTS.get(args.workload))
-        times.append(est * L)
+    var = VARIANTS.get(args.workload)
+    # each step is one bounded sample (virtual rank = step mod D for the
+    # forward workloads); ms_per_step is the sample's own time
+    for i in range(args.warmup):
+        cpu_sample(S, D, d, H, inter, kind, var, r=i % D)
+    times, equiv, toks = [], [], 0
+    desc, exact = "", True
+    for i in range(args.steps):
+        n_tok, dt, dt_eq, exact, desc = cpu_sample(S, D, d, H, inter, kind, var, r=i % D)
+        times.append(dt)
+        equiv.append(dt_eq * L)
+        toks += n_tok
     if L > 1:
-        desc += f", x{L} layers"
-    t = statistics.median(times)
-    value = S / t
+        desc += f"; x{L} layers (each layer its own weights, same work)"
+    value = toks / sum(equiv)
     line = {
         "impl": "reference", "metric": "TSP-block tokens/s", "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": statistics.mean(times) * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(args.workload),
+        "step": f"one bounded sample of the workload: {desc}",
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "exact_work_per_token": exact},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -482,30 +542,48 @@ def run_gpu(args):
         dyz = torch.empty_like(dy)
         y = torch.empty(x.shape, dtype=torch.float32, device=dev)  # dx (fp32) in global order
 
-    def step(xin, yout=None):
+    # The block's weights in the fp16 operand type, converted once per weight
+    # update (tsp_block_weights_prepare): for a forward (inference) workload
+    # once before timing, as a deployment holds them; for a training step once
+    # per step, inside it, shared by the forward and the backward.  The
+    # workspaces above are sized for the calls that convert their own weights,
+    # which is more than the prepared calls need, so they serve both.
+    prep_mode = "per-step" if kind == "fwdbwd" else ("once" if kind == "fwd" else "none")
+    preps = None
+    if prep_mode != "none":
+        preps = [tsp.prepare_weights(cfg, Wl) for Wl in Ws]
+    if prep_mode == "per-step" and L == 1:
+        ws = torch.empty(tsp.workspace_bytes(cfg, tsp.TSP_OP_BLOCK_FWD_TRAIN | tsp.TSP_OP_PREPARED),
+                         dtype=torch.uint8, device=dev)
+
+    def step(xin, yout=None, convert_per_call=False):
         yout = y if yout is None else yout
         tsp.zigzag_permute(xin, D, out=xz)
+        pp = None if convert_per_call else preps
+        if prep_mode == "per-step":
+            for Wl, p in zip(Ws, preps):
+                tsp.prepare_weights(cfg, Wl, out=p)
         if L > 1 and kind == "fwd":
-            tsp.stack_fwd(cfg, xz, Ws, out=yz, ws=ws)
+            tsp.stack_fwd(cfg, xz, Ws, out=yz, ws=ws, preps=pp)
             tsp.zigzag_permute(yz, D, inverse=True, out=yout)
             return yout
         if L > 1:
-            tsp.stack_fwd(cfg, xz, Ws, saved=saved, out=yz, ws=ws)
+            tsp.stack_fwd(cfg, xz, Ws, saved=saved, out=yz, ws=ws, preps=preps)
             tsp.zigzag_permute(dy, D, out=dyz)
-            dx, _ = tsp.stack_bwd(cfg, dyz, saved, Ws, ws=wsb)
+            dx, _ = tsp.stack_bwd(cfg, dyz, saved, Ws, ws=wsb, preps=preps)
             tsp.zigzag_permute(dx, D, inverse=True, out=yout)
             return yout
         if kind == "fwd":
-            tsp.block_fwd(cfg, xz, W, out=yz, ws=ws)
+            tsp.block_fwd(cfg, xz, W, out=yz, ws=ws, prep=pp[0] if pp else None)
             tsp.zigzag_permute(yz, D, inverse=True, out=yout)
             return yout
         if kind == "mlp":
             tsp.gated_mlp_fwd(cfg, xz, W, norm=False, residual=False, out=yz, ws=ws)
             tsp.zigzag_permute(yz, D, inverse=True, out=yout)
             return yout
-        tsp.block_fwd(cfg, xz, W, saved=saved, out=yz)
+        tsp.block_fwd(cfg, xz, W, saved=saved, out=yz, ws=ws, prep=preps[0])
         tsp.zigzag_permute(dy, D, out=dyz)
-        g = tsp.block_bwd(cfg, xz, dyz, saved, W, ws=wsb)
+        g = tsp.block_bwd(cfg, xz, dyz, saved, W, ws=wsb, prep=preps[0])
         tsp.zigzag_permute(g["dx"], D, inverse=True, out=yout)
         return yout
 
@@ -541,6 +619,22 @@ def run_gpu(args):
     tsp.profile_enable(False)
     t_dev = ev0.elapsed_time(ev1) / 1e3 / args.steps
     t_dev = reduce_max(t_dev, world, dev if world > 1 else None)
+
+    # ---- the same step with the weights converted inside every call (the
+    # calls without prepared copies), for comparison
+    conv = None
+    if prep_mode == "once":
+        for _ in range(2):
+            step(x, convert_per_call=True)
+        torch.cuda.synchronize(dev)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(args.steps):
+            step(x, convert_per_call=True)
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_conv = reduce_max(c0.elapsed_time(c1) / 1e3 / args.steps, world, dev if world > 1 else None)
+        conv = {"value": world * S / t_conv, "unit": "tokens/s", "ms_per_step": t_conv * 1e3}
 
     # ---- end to end through the public API with host buffers: every step
     # uploads its input from pinned host memory and reads its result back.
@@ -609,12 +703,28 @@ def run_gpu(args):
         if "tflops" in per_kernel[name]:
             dom = name
             break
-    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    # the burst peak (cuBLAS timed alone) for a timed region shorter than a
+    # second, the sustained one (seconds-long loop under the power cap) beyond
+    timed_s = t_dev * args.steps
+    sustained = timed_s >= 1.0
+    peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops", peaks.get("bf16_tflops"))
+    peak_label = (f"{peak_src} bf16 {'sustained' if sustained else 'burst'} (MEASURED_PEAKS.json; "
+                  f"timed region {timed_s:.2f} s {'>=' if sustained else '<'} 1 s)")
+    # the tensor core's own rate at the clock the run saw: 8192 dense fp16/bf16
+    # flop per clock per SM (M=128, N=128, K=16 in 64 cycles) x SMs x the
+    # median sampled SM clock
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    clock_peak = (n_sm * 8192.0 * clk["sm_mhz"] * 1e6 / 1e12) if clk.get("sm_mhz") else None
     if dom is not None:
         ach = per_kernel[dom]["tflops"]
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                "frac": ach / peak, "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)",
-                "traffic": measured_traffic(dom, args.workload)}
+                "frac": ach / peak, "peak_source": peak_label,
+                "traffic": measured_traffic(dom, args.workload),
+                "clock_peak": clock_peak,
+                "frac_of_clock_peak": ach / clock_peak if clock_peak else None,
+                "clock_peak_source": f"{n_sm} SMs x 8192 flop/clk x median sampled SM clock",
+                "frac_of_nominal": ach / NOMINAL_BF16_TFLOPS,
+                "nominal_source": "GB300 rated dense bf16, 2.25 PFLOP/s"}
     flops = block_flops(S, d, inter, kind, dkv) * L
     value = world * S / t_dev
     tflops = world * flops / t_dev / 1e12
@@ -625,13 +735,22 @@ def run_gpu(args):
         "data": "synthetic (x~N(0,1), weights~N(0,0.02), gains 1)",
         "config": workload_config(args.workload),
         "tflops": tflops, "tflops_per_gpu": tflops / world,
-        "frac_of_peak": (tflops / world) / peaks.get("bf16_tflops", peak),
-        "peak_tflops": peaks.get("bf16_tflops"), "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)",
+        "frac_of_peak": (tflops / world) / peak,
+        "peak_tflops": peak, "peak_source": peak_label,
+        "frac_of_nominal": (tflops / world) / NOMINAL_BF16_TFLOPS,
+        "timed_region_s": timed_s,
         "e2e": {"value": world * S / t_e2e, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x.numel() * x.element_size()),
                 "d2h_bytes_per_step": int(y.numel() * y.element_size())},
         "gpu_launches": int(launches),
         "launches_per_step": launches / args.steps,
+        "weights": {"once": "bf16 weights converted to the fp16 tensor-core operand copies once, "
+                            "before the timed region (tsp_block_weights_prepare), as a deployment "
+                            "holds them",
+                    "per-step": "bf16 weights converted to the fp16 operand copies once per step, "
+                                "inside the timed region, shared by the forward and the backward",
+                    "none": "the MLP call converts its weights inside every call"}[prep_mode],
+        "with_weight_conversion_per_call": conv,
         "kernels": per_kernel,
         "roofline": roof,
         "clocks": clk,
@@ -645,14 +764,29 @@ def run_gpu(args):
                                             ("tp_sp_on_D2_devices", tsp.TSP_MEM_TP_SP))}},
     }
     if rank == 0 and not args.no_cpu_baseline:
-        S_, D_, d_, H_, I_, kind_ = WORKLOADS[args.workload]
-        rows = args.ref_rows or (512 if kind_ == "fwdbwd" else 8192)   # ~10 s on 16 cores
-        est, dt, desc = oracle_sample(S_, d_, H_, I_, D_, kind_, rows, var)
+        n_tok, dt, dt_eq, exact, desc = cpu_sample(S, D, d, H, inter, kind, var, r=0)
         if L > 1:
-            est *= L
-            desc += f", x{L} layers"
-        line["cpu_baseline"] = {"value": S_ / est, "unit": "tokens/s", "cores": cpu_cores(),
-                                "kind": "oracle", "sample": desc, "sample_seconds": dt}
+            desc += f"; x{L} layers (each layer its own weights, same work)"
+        line["cpu_baseline"] = {"value": n_tok / (dt_eq * L), "unit": "tokens/s", "cores": cpu_cores(),
+                                "kind": "oracle", "sample": desc, "sample_seconds": dt,
+                                "exact_work_per_token": exact}
+    if rank == 0 and args.cpu_full:
+        # the oracle's unsharded block forward over the whole workload, once
+        # (minutes of CPU time: a check of the bounded sample above, not part
+        # of the default run)
+        import oracle.tsp_oracle as O
+        ent = _oracle_inputs(S, d, H, inter, kind, var)
+        t0 = time.perf_counter()
+        if kind == "fwd":
+            O.block_fwd(ent["inp"]["x"], ent["inp"], H, 1e-6)
+        elif kind == "mlp":
+            O.mlp_fwd(ent["inp"]["x"], ent["inp"], 1e-6, norm=False, residual=False)
+        else:
+            O.block_bwd(ent["inp"]["x"], ent["inp"], ent["inp"]["dy"], H, 1e-6)
+        dt = time.perf_counter() - t0
+        line["cpu_full"] = {"value": S / dt, "unit": "tokens/s", "seconds": dt,
+                            "cores": cpu_cores(), "kind": "oracle",
+                            "what": f"oracle (numpy float64), whole workload ({kind}), one layer"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -832,7 +966,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    ap.add_argument("--ref-rows", type=int, default=0)
+    ap.add_argument("--ref-rows", type=int, default=0, help="prompt rows of the decode sample")
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="also time the oracle once on the whole workload (minutes)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.impl == "reference":

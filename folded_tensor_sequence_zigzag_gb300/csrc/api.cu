@@ -28,10 +28,26 @@ namespace tsp {
 
 __device__ int g_status_word = 0;
 
-int* status_word() {
-  static int* ptr[16] = {nullptr};
+int current_device() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  return dev;
+}
+
+namespace {
+std::atomic<int> g_debug_skip{0};
+}  // namespace
+
+bool take_debug_skip() {
+  int n = g_debug_skip.load(std::memory_order_relaxed);
+  while (n > 0 && !g_debug_skip.compare_exchange_weak(n, n - 1)) {
+  }
+  return n > 0;
+}
+
+int* status_word() {
+  static int* ptr[kMaxDevices] = {nullptr};
+  const int dev = current_device();
   if (!ptr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) ptr[dev] = (int*)p;
@@ -40,9 +56,8 @@ int* status_word() {
 }
 
 int num_sms() {
-  static int n[16] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
+  static int n[kMaxDevices] = {0};
+  const int dev = current_device();
   if (n[dev] == 0) {
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) v = 0;
@@ -327,13 +342,15 @@ tsp_status rope_qk(const tsp_cfg* c, const Acts& A, void* qkv, int ty, int inver
 // Forward halves
 // ----------------------------------------------------------------------------
 
+// x_f32: the input x is fp32 (a residual stream kept in fp32) instead of the cfg dtype.
 // h_f32: write h in fp32 (the block's residual stream) instead of the cfg dtype.
 // WC: fp16 weight copies (bf16 configuration; filled by the caller of this function).
-tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, const WCache& WC,
-                     void* h, bool h_f32, const Acts& A, cudaStream_t st) {
+tsp_status attn_half(const tsp_cfg* c, const void* x, bool x_f32, const tsp_attn_w* w,
+                     const WCache& WC, void* h, bool h_f32, const Acts& A, cudaStream_t st) {
   const int64_t S = c->S;
   const int d = c->d, D = c->D;
-  tsp_status r = launch_rmsnorm_fwd(x, c->dtype == TSP_BF16 ? TY_BF16 : TY_F32, w->g_attn, A.a,
+  const int x_ty = (c->dtype == TSP_BF16 && !x_f32) ? TY_BF16 : TY_F32;
+  tsp_status r = launch_rmsnorm_fwd(x, x_ty, w->g_attn, A.a,
                                     c->dtype == TSP_BF16 ? TY_F16 : TY_F32, A.rstd1, S, d, c->eps,
                                     c->dtype, st);
   if (r != TSP_OK) return r;
@@ -376,7 +393,7 @@ tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, const
     o.M = (int)S; o.N = d; o.K = d;
     o.A[0] = A.o; o.lda[0] = d; o.kseg_len[0] = d;
     o.B[0] = WC.wo; o.ldb[0] = d;
-    o.epi = EPI_RES; o.res = x; o.ldr = d; o.name = "gemm_oproj";
+    o.epi = EPI_RES; o.res = x; o.ldr = d; o.res_f32 = x_f32; o.name = "gemm_oproj";
     o.out = h; o.ldo = d; o.out_type = h_f32 ? OUT_F32 : OUT_BF16;
     return gemm_tc(o, st);
   }
@@ -409,10 +426,11 @@ tsp_status attn_half(const tsp_cfg* c, const void* x, const tsp_attn_w* w, const
 }
 
 // hin_f32: the input h is fp32 (the block's residual stream), else the cfg dtype.
+// y_f32: write y in fp32 instead of the cfg dtype (bf16 configuration).
 // g_tile (training with cfg->mlp_tile): the MLP runs one row tile at a time
 // with G in this [mlp_tile, inter] buffer, and keeps no G or A|B.
 tsp_status mlp_half(const tsp_cfg* c, const void* hin, bool hin_f32, const tsp_mlp_w* w,
-                    const WCache& WC, void* y, const Acts& A, cudaStream_t st,
+                    const WCache& WC, void* y, bool y_f32, const Acts& A, cudaStream_t st,
                     void* g_tile = nullptr) {
   const int64_t S = c->S;
   const int d = c->d, I = c->inter, D = c->D;
@@ -450,7 +468,8 @@ tsp_status mlp_half(const tsp_cfg* c, const void* hin, bool hin_f32, const tsp_m
       o.B[0] = WC.w2; o.ldb[0] = I;
       o.rot_rows = (int)tile; o.rot_r0 = (int)(t0 / rows_per_rank); o.rot_D = D;
       o.name = "gemm_w2";
-      o.out = (uint8_t*)y + (size_t)t0 * d * 2; o.ldo = d; o.out_type = OUT_BF16;
+      o.out = (uint8_t*)y + (size_t)t0 * d * (y_f32 ? 4 : 2); o.ldo = d;
+      o.out_type = y_f32 ? OUT_F32 : OUT_BF16;
       if (w->add_residual) {
         o.epi = EPI_RES; o.res = (const uint8_t*)hin + (size_t)t0 * d * (hin_f32 ? 4 : 2);
         o.ldr = d; o.res_f32 = hin_f32;
@@ -482,7 +501,7 @@ tsp_status mlp_half(const tsp_cfg* c, const void* hin, bool hin_f32, const tsp_m
     o.A[0] = A.g; o.lda[0] = I; o.kseg_len[0] = I;
     o.B[0] = WC.w2; o.ldb[0] = I;
     o.rot_rows = (int)rows_per_rank; o.rot_D = D; o.name = "gemm_w2";
-    o.out = y; o.ldo = d; o.out_type = OUT_BF16;
+    o.out = y; o.ldo = d; o.out_type = y_f32 ? OUT_F32 : OUT_BF16;
     if (w->add_residual) {
       o.epi = EPI_RES; o.res = hin; o.ldr = d; o.res_f32 = hin_f32;
     } else {
@@ -517,13 +536,16 @@ tsp_status mlp_half(const tsp_cfg* c, const void* hin, bool hin_f32, const tsp_m
   return TSP_OK;
 }
 
-tsp_status check_attn_w(const tsp_attn_w* w) {
-  if (!w || !al16(w->wq) || !al16(w->wk) || !al16(w->wv) || !al16(w->wo) || !al16(w->g_attn))
+// mats = false: the weight matrices are not read (their fp16 copies come
+// prepared), only the gains
+tsp_status check_attn_w(const tsp_attn_w* w, bool mats = true) {
+  if (!w || !al16(w->g_attn)) return TSP_ERR_INVALID_ARG;
+  if (mats && (!al16(w->wq) || !al16(w->wk) || !al16(w->wv) || !al16(w->wo)))
     return TSP_ERR_INVALID_ARG;
   return TSP_OK;
 }
-tsp_status check_mlp_w(const tsp_mlp_w* w, bool need_norm) {
-  if (!w || !al16(w->w1) || !al16(w->w3) || !al16(w->w2)) return TSP_ERR_INVALID_ARG;
+tsp_status check_mlp_w(const tsp_mlp_w* w, bool need_norm, bool mats = true) {
+  if (!w || (mats && (!al16(w->w1) || !al16(w->w3) || !al16(w->w2)))) return TSP_ERR_INVALID_ARG;
   if (w->g_mlp && !al16(w->g_mlp)) return TSP_ERR_INVALID_ARG;
   if (need_norm && (!w->g_mlp || !w->add_residual)) return TSP_ERR_INVALID_ARG;
   return TSP_OK;
@@ -629,10 +651,75 @@ tsp_status decode_impl(const tsp_cfg* c, const void* x, int T, int64_t n_cached,
 // ----------------------------------------------------------------------------
 // Backward (defined below the C entry points' helpers)
 // ----------------------------------------------------------------------------
-tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const void* saved,
-                          const tsp_attn_w* aw, const tsp_mlp_w* mw, float* dx, float* dwq,
+tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, bool x_f32, const void* dy,
+                          bool dy_f32, const void* saved, const tsp_attn_w* aw,
+                          const tsp_mlp_w* mw, const void* prep, float* dx, float* dwq,
                           float* dwk, float* dwv, float* dwo, float* dw1, float* dw3, float* dw2,
                           float* dg_attn, float* dg_mlp, void* ws, cudaStream_t st);
+
+
+tsp_status block_fwd_checked(const tsp_cfg* cfg, const void* x_z, bool x_f32, const tsp_attn_w* aw,
+                             const tsp_mlp_w* mw, const void* prep, void* y_z, bool y_f32,
+                             void* saved, void* ws, size_t ws_bytes, cudaStream_t st) {
+  tsp_status r = check_cfg(cfg);
+  if (r != TSP_OK) return r;
+  // bf16 with prepared fp16 copies: the matrices themselves are not read
+  const bool use_prep = prep != nullptr && cfg->dtype == TSP_BF16;
+  if (prep && !al16(prep)) return TSP_ERR_INVALID_ARG;
+  if ((r = check_attn_w(aw, !use_prep)) != TSP_OK) return r;
+  if ((r = check_mlp_w(mw, true, !use_prep)) != TSP_OK) return r;
+  if (!al16(x_z) || !al16(y_z)) return TSP_ERR_INVALID_ARG;
+  if ((r = check_bf16_attn(cfg)) != TSP_OK) return r;
+  if ((r = check_bf16_mlp(cfg)) != TSP_OK) return r;
+  const bool training = saved != nullptr;
+  const int parts = fwd_parts(cfg, training);
+  const size_t nwc = use_prep ? 0 : wcache_layout(cfg, WC_ATTN | WC_MLP, nullptr).bytes;
+  const int prep_flag = use_prep ? TSP_OP_PREPARED : 0;
+  const size_t ntile = training ? mlp_tile_g_bytes(cfg) : 0;
+  uint8_t *abase, *wbase;
+  if (training) {
+    // activations go to `saved`; the workspace holds the fp16 weight copies
+    // (and, with MLP tiling, one tile's G)
+    if (!al16(saved)) return TSP_ERR_INVALID_ARG;
+    if (nwc + ntile > 0 && (!al16(ws) || ws_bytes < nwc + ntile)) return TSP_ERR_INVALID_ARG;
+    abase = (uint8_t*)saved;
+    wbase = (uint8_t*)ws;
+  } else {
+    if (!al16(ws) || ws_bytes < tsp_workspace_bytes(cfg, TSP_OP_BLOCK_FWD | prep_flag))
+      return TSP_ERR_INVALID_ARG;
+    abase = (uint8_t*)ws;
+    wbase = (uint8_t*)ws + acts_layout(cfg, parts, nullptr).bytes;
+  }
+  const Acts A = acts_layout(cfg, parts, abase);
+  const WCache WC = wcache_layout(cfg, WC_ATTN | WC_MLP, use_prep ? (uint8_t*)prep : wbase);
+  if (!use_prep && (r = fill_wcache(cfg, WC, aw, mw, st)) != TSP_OK) return r;
+  if ((r = attn_half(cfg, x_z, x_f32, aw, WC, A.h, true, A, st)) != TSP_OK) return r;
+  return mlp_half(cfg, A.h, true, mw, WC, y_z, y_f32, A, st, ntile ? wbase + nwc : nullptr);
+}
+
+tsp_status block_bwd_checked(const tsp_cfg* cfg, const void* x_z, bool x_f32, const void* dy_z,
+                             bool dy_f32, const void* saved, const tsp_attn_w* aw,
+                             const tsp_mlp_w* mw, const void* prep, float* dx_z,
+                             float* const* grads, void* ws, size_t ws_bytes, cudaStream_t st) {
+  tsp_status r = check_cfg(cfg);
+  if (r != TSP_OK) return r;
+  const bool use_prep = prep != nullptr && cfg->dtype == TSP_BF16;
+  if (prep && !al16(prep)) return TSP_ERR_INVALID_ARG;
+  if ((r = check_attn_w(aw, !use_prep)) != TSP_OK) return r;
+  if ((r = check_mlp_w(mw, true, !use_prep)) != TSP_OK) return r;
+  if (!al16(x_z) || !al16(dy_z) || !al16(saved) || !al16(dx_z) || !grads) return TSP_ERR_INVALID_ARG;
+  for (int k = 0; k < 9; ++k)
+    if (!al16(grads[k])) return TSP_ERR_INVALID_ARG;
+  if ((r = check_bf16_attn(cfg)) != TSP_OK) return r;
+  if ((r = check_bf16_mlp(cfg)) != TSP_OK) return r;
+  if (!al16(ws) ||
+      ws_bytes < tsp_workspace_bytes(cfg, TSP_OP_BLOCK_BWD | (use_prep ? TSP_OP_PREPARED : 0)))
+    return TSP_ERR_INVALID_ARG;
+  const bool bf = cfg->dtype == TSP_BF16;
+  return block_bwd_impl(cfg, x_z, bf && x_f32, dy_z, bf && dy_f32, saved, aw, mw,
+                        use_prep ? prep : nullptr, dx_z, grads[0], grads[1], grads[2], grads[3],
+                        grads[4], grads[5], grads[6], grads[7], grads[8], ws, st);
+}
 
 }  // namespace tsp
 
@@ -647,6 +734,7 @@ const char* tsp_strerror(tsp_status s) {
     case TSP_ERR_UNSUPPORTED: return "shape not supported by the selected kernels";
     case TSP_ERR_CUDA: return "CUDA runtime error";
     case TSP_ERR_TIMEOUT: return "device pipeline wait exceeded its time limit";
+    case TSP_ERR_RANGE: return "a value held in fp16 inside the bf16 path was out of fp16 range";
   }
   return "unknown status";
 }
@@ -675,6 +763,15 @@ tsp_status tsp_rmsnorm_fwd(const void* u, const void* g, void* out, float* rstd,
 
 size_t tsp_workspace_bytes(const tsp_cfg* cfg, int32_t op) {
   if (check_cfg(cfg) != TSP_OK) return 0;
+  if (op & TSP_OP_PREPARED) {
+    // the whole-block calls with prepared fp16 weight copies: no copies in the workspace
+    const int base = op & ~TSP_OP_PREPARED;
+    const size_t nwc = wcache_layout(cfg, WC_ATTN | WC_MLP, nullptr).bytes;
+    if (base != TSP_OP_BLOCK_FWD && base != TSP_OP_BLOCK_BWD && base != TSP_OP_BLOCK_FWD_TRAIN)
+      return 0;
+    const size_t full = tsp_workspace_bytes(cfg, base);
+    return std::max<size_t>(256, full - nwc);
+  }
   switch (op) {
     case TSP_OP_ATTN_FWD:
       return acts_layout(cfg, PART_ATTN, nullptr).bytes + wcache_layout(cfg, WC_ATTN, nullptr).bytes;
@@ -711,7 +808,7 @@ tsp_status tsp_attn_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_att
   const WCache WC = wcache_layout(cfg, WC_ATTN, (uint8_t*)ws + na);
   cudaStream_t st = S_(stream);
   if ((r = fill_wcache(cfg, WC, w, nullptr, st)) != TSP_OK) return r;
-  return attn_half(cfg, x_z, w, WC, h_z, false, A, st);
+  return attn_half(cfg, x_z, false, w, WC, h_z, false, A, st);
 }
 
 tsp_status tsp_gated_mlp_fwd(const tsp_cfg* cfg, const void* h_z, const tsp_mlp_w* w, void* y_z,
@@ -728,61 +825,59 @@ tsp_status tsp_gated_mlp_fwd(const tsp_cfg* cfg, const void* h_z, const tsp_mlp_
   const WCache WC = wcache_layout(cfg, WC_MLP, (uint8_t*)ws + na);
   cudaStream_t st = S_(stream);
   if ((r = fill_wcache(cfg, WC, nullptr, w, st)) != TSP_OK) return r;
-  return mlp_half(cfg, h_z, false, w, WC, y_z, A, st);
+  return mlp_half(cfg, h_z, false, w, WC, y_z, false, A, st);
 }
 
 tsp_status tsp_block_fwd(const tsp_cfg* cfg, const void* x_z, const tsp_attn_w* aw,
                          const tsp_mlp_w* mw, void* y_z, void* saved, void* ws, size_t ws_bytes,
                          void* stream) {
+  return block_fwd_checked(cfg, x_z, false, aw, mw, nullptr, y_z, false, saved, ws, ws_bytes,
+                           S_(stream));
+}
+
+size_t tsp_block_weights_bytes(const tsp_cfg* cfg) {
+  if (check_cfg(cfg) != TSP_OK || cfg->dtype != TSP_BF16) return 0;
+  return wcache_layout(cfg, WC_ATTN | WC_MLP, nullptr).bytes;
+}
+
+tsp_status tsp_block_weights_prepare(const tsp_cfg* cfg, const tsp_attn_w* aw, const tsp_mlp_w* mw,
+                                     void* prep, void* stream) {
   tsp_status r = check_cfg(cfg);
   if (r != TSP_OK) return r;
   if ((r = check_attn_w(aw)) != TSP_OK) return r;
-  if ((r = check_mlp_w(mw, true)) != TSP_OK) return r;
-  if (!al16(x_z) || !al16(y_z)) return TSP_ERR_INVALID_ARG;
-  if ((r = check_bf16_attn(cfg)) != TSP_OK) return r;
-  if ((r = check_bf16_mlp(cfg)) != TSP_OK) return r;
-  const bool training = saved != nullptr;
-  const int parts = fwd_parts(cfg, training);
-  const size_t nwc = wcache_layout(cfg, WC_ATTN | WC_MLP, nullptr).bytes;
-  const size_t ntile = training ? mlp_tile_g_bytes(cfg) : 0;
-  uint8_t *abase, *wbase;
-  if (training) {
-    // activations go to `saved`; the workspace holds the fp16 weight copies
-    // (and, with MLP tiling, one tile's G)
-    if (!al16(saved)) return TSP_ERR_INVALID_ARG;
-    if (nwc + ntile > 0 && (!al16(ws) || ws_bytes < nwc + ntile)) return TSP_ERR_INVALID_ARG;
-    abase = (uint8_t*)saved;
-    wbase = (uint8_t*)ws;
-  } else {
-    if (!al16(ws) || ws_bytes < tsp_workspace_bytes(cfg, TSP_OP_BLOCK_FWD)) return TSP_ERR_INVALID_ARG;
-    abase = (uint8_t*)ws;
-    wbase = (uint8_t*)ws + acts_layout(cfg, parts, nullptr).bytes;
-  }
-  const Acts A = acts_layout(cfg, parts, abase);
-  const WCache WC = wcache_layout(cfg, WC_ATTN | WC_MLP, wbase);
-  cudaStream_t st = S_(stream);
-  if ((r = fill_wcache(cfg, WC, aw, mw, st)) != TSP_OK) return r;
-  if ((r = attn_half(cfg, x_z, aw, WC, A.h, true, A, st)) != TSP_OK) return r;
-  return mlp_half(cfg, A.h, true, mw, WC, y_z, A, st, ntile ? wbase + nwc : nullptr);
+  if ((r = check_mlp_w(mw, false)) != TSP_OK) return r;
+  if (cfg->dtype != TSP_BF16) return TSP_OK;   // the fp32 path reads the weights as they are
+  if (!al16(prep)) return TSP_ERR_INVALID_ARG;
+  return fill_wcache(cfg, wcache_layout(cfg, WC_ATTN | WC_MLP, (uint8_t*)prep), aw, mw, S_(stream));
+}
+
+tsp_status tsp_block_fwd_prepared(const tsp_cfg* cfg, const void* x_z, const void* prep,
+                                  const tsp_attn_w* aw, const tsp_mlp_w* mw, void* y_z, void* saved,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  if (cfg && cfg->dtype == TSP_BF16 && !prep) return TSP_ERR_INVALID_ARG;
+  return block_fwd_checked(cfg, x_z, false, aw, mw, prep, y_z, false, saved, ws, ws_bytes,
+                           S_(stream));
+}
+
+tsp_status tsp_block_bwd_prepared(const tsp_cfg* cfg, const void* x_z, const void* dy_z,
+                                  const void* saved, const void* prep, const tsp_attn_w* aw,
+                                  const tsp_mlp_w* mw, float* dx_z, float* dwq, float* dwk,
+                                  float* dwv, float* dwo, float* dw1, float* dw3, float* dw2,
+                                  float* dg_attn, float* dg_mlp, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  if (cfg && cfg->dtype == TSP_BF16 && !prep) return TSP_ERR_INVALID_ARG;
+  float* const grads[9] = {dwq, dwk, dwv, dwo, dw1, dw3, dw2, dg_attn, dg_mlp};
+  return block_bwd_checked(cfg, x_z, false, dy_z, false, saved, aw, mw, prep, dx_z, grads, ws,
+                           ws_bytes, S_(stream));
 }
 
 tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z, const void* saved,
                          const tsp_attn_w* aw, const tsp_mlp_w* mw, float* dx_z, float* dwq,
                          float* dwk, float* dwv, float* dwo, float* dw1, float* dw3, float* dw2,
                          float* dg_attn, float* dg_mlp, void* ws, size_t ws_bytes, void* stream) {
-  tsp_status r = check_cfg(cfg);
-  if (r != TSP_OK) return r;
-  if ((r = check_attn_w(aw)) != TSP_OK) return r;
-  if ((r = check_mlp_w(mw, true)) != TSP_OK) return r;
-  if (!al16(x_z) || !al16(dy_z) || !al16(saved) || !al16(dx_z)) return TSP_ERR_INVALID_ARG;
-  const float* gp[9] = {dwq, dwk, dwv, dwo, dw1, dw3, dw2, dg_attn, dg_mlp};
-  for (const float* p : gp)
-    if (!al16(p)) return TSP_ERR_INVALID_ARG;
-  if ((r = check_bf16_attn(cfg)) != TSP_OK) return r;
-  if ((r = check_bf16_mlp(cfg)) != TSP_OK) return r;
-  if (!al16(ws) || ws_bytes < tsp_workspace_bytes(cfg, TSP_OP_BLOCK_BWD)) return TSP_ERR_INVALID_ARG;
-  return block_bwd_impl(cfg, x_z, dy_z, saved, aw, mw, dx_z, dwq, dwk, dwv, dwo, dw1, dw3, dw2,
-                        dg_attn, dg_mlp, ws, S_(stream));
+  float* const grads[9] = {dwq, dwk, dwv, dwo, dw1, dw3, dw2, dg_attn, dg_mlp};
+  return block_bwd_checked(cfg, x_z, false, dy_z, false, saved, aw, mw, nullptr, dx_z, grads, ws,
+                           ws_bytes, S_(stream));
 }
 
 size_t tsp_kv_cache_bytes(const tsp_cfg* cfg, int64_t kv_rows_cap) {
@@ -874,6 +969,8 @@ int32_t tsp_profile_report(char* buf, int64_t bytes) {
 
 int64_t tsp_launch_count(void) { return g_launches.load(); }
 
+void tsp_debug_skip_stage(int32_t n) { g_debug_skip.store(n > 0 ? n : 0); }
+
 tsp_status tsp_device_status(void* stream, int32_t reset) {
   int* p = status_word();
   if (!p) return TSP_ERR_CUDA;
@@ -894,8 +991,9 @@ tsp_status tsp_device_status(void* stream, int32_t reset) {
 // ----------------------------------------------------------------------------
 namespace tsp {
 
-tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const void* saved,
-                          const tsp_attn_w* aw, const tsp_mlp_w* mw, float* dx, float* dwq,
+tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, bool x_f32, const void* dy,
+                          bool dy_f32, const void* saved, const tsp_attn_w* aw,
+                          const tsp_mlp_w* mw, const void* prep, float* dx, float* dwq,
                           float* dwk, float* dwv, float* dwo, float* dw1, float* dw3, float* dw2,
                           float* dg_attn, float* dg_mlp, void* ws, cudaStream_t st) {
   const int64_t S = c->S;
@@ -905,10 +1003,13 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
   tsp_status r;
   if (c->dtype == TSP_BF16) {
     const size_t e = 2;
-    const WCache WC = wcache_layout(c, WC_ATTN | WC_MLP, (uint8_t*)ws + W.bytes);
-    if ((r = fill_wcache(c, WC, aw, mw, st)) != TSP_OK) return r;
+    // the fp16 weight copies: prepared by the caller, or converted here
+    const WCache WC = wcache_layout(c, WC_ATTN | WC_MLP, prep ? (uint8_t*)prep : (uint8_t*)ws + W.bytes);
+    if (!prep && (r = fill_wcache(c, WC, aw, mw, st)) != TSP_OK) return r;
     // the upstream gradient in the internal fp16 operand type
-    if ((r = launch_convert_bf16_f16(dy, W.dy16, S * d, st)) != TSP_OK) return r;
+    r = dy_f32 ? launch_convert_f32_f16((const float*)dy, W.dy16, S * d, st)
+               : launch_convert_bf16_f16(dy, W.dy16, S * d, st);
+    if (r != TSP_OK) return r;
     // MLP backward, over the whole sequence or (cfg->mlp_tile) one row tile at
     // a time; weight gradients sum over the tiles in fp32 (each tile lies in
     // one virtual rank's rows, so this is still the sum over the ranks' rows)
@@ -1001,7 +1102,8 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
       }
     }
     // dh = dy + RMSNorm_2'(db)   (fp32, plus an fp16 copy for the GEMMs)
-    if ((r = launch_rmsnorm_bwd((const float*)W.db, A.h, TY_F32, mw->g_mlp, A.rstd2, nullptr, dy,
+    if ((r = launch_rmsnorm_bwd((const float*)W.db, A.h, TY_F32, mw->g_mlp, A.rstd2,
+                                dy_f32 ? (const float*)dy : nullptr, dy_f32 ? nullptr : dy,
                                 (float*)W.dh_f32, W.dh_t, TY_F16, dg_mlp, W.dg_part, S, d,
                                 c->dtype, st)) != TSP_OK)
       return r;
@@ -1073,9 +1175,9 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, const void* dy, const
       if ((r = gemm_tc(g, st)) != TSP_OK) return r;
     }
     // dx = dh + RMSNorm_1'(da), fp32
-    return launch_rmsnorm_bwd((const float*)W.da, x, TY_BF16, aw->g_attn, A.rstd1,
-                              (const float*)W.dh_f32, nullptr, dx, nullptr, TY_BF16, dg_attn,
-                              W.dg_part, S, d, c->dtype, st);
+    return launch_rmsnorm_bwd((const float*)W.da, x, x_f32 ? TY_F32 : TY_BF16, aw->g_attn, A.rstd1,
+                              (const float*)W.dh_f32, nullptr, dx, nullptr,
+                              x_f32 ? TY_F16 : TY_BF16, dg_attn, W.dg_part, S, d, c->dtype, st);
   }
 
   // ------------------------------------------------------------ exact fp32
@@ -1199,5 +1301,5 @@ extern "C" tsp_status tsp_gated_mlp_fwd_noalloc(const tsp_cfg* cfg, const void* 
   const WCache WC = wcache_layout(cfg, WC_MLP, scratch + na);
   cudaStream_t st = S_(stream);
   if ((r = fill_wcache(cfg, WC, nullptr, w, st)) != TSP_OK) return r;
-  return mlp_half(cfg, h_z, false, w, WC, y_z, A, st);
+  return mlp_half(cfg, h_z, false, w, WC, y_z, false, A, st);
 }

@@ -80,8 +80,8 @@ constexpr float kOperandLog2Scale = 8.f;         // P, dS scaled by 2^8 into fp1
 constexpr float kOperandUnscale = 1.f / 256.f;
 // mbarrier indices
 constexpr int B_KV = 0, B_QFULL = 1, B_QEMPTY = B_QFULL + QSTAGES, B_DP = B_QEMPTY + QSTAGES,
-              B_P = B_DP + 1, B_DQF = B_P + 1, B_DQE = B_DQF + 1, B_KVDONE = B_DQE + 1,
-              B_DRAIN = B_KVDONE + 1, N_BARS = B_DRAIN + 1;
+              B_P = B_DP + 1 /* two: query halves A and B */, B_DQF = B_P + 2, B_DQE = B_DQF + 1,
+              B_KVDONE = B_DQE + 1, B_DRAIN = B_KVDONE + 1, N_BARS = B_DRAIN + 1;
 static_assert(N_BARS * 8 <= 160, "barriers overlap the TMEM slot");
 
 struct TcBwdArgs {
@@ -132,7 +132,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
   auto qd_full = [&](uint32_t s) { return bars + 8u * (B_QFULL + s); };
   auto qd_empty = [&](uint32_t s) { return bars + 8u * (B_QEMPTY + s); };
   const uint32_t dp_full = bars + 8u * B_DP;     // S^T(c), dP^T(c) and all earlier MMAs done
-  const uint32_t p_full = bars + 8u * B_P;       // P^T(c) in TMEM, dS^T(c) in shared memory
+  // P^T(c) in TMEM and dS^T(c) in shared memory for query half X (queries 64X .. 64X+63)
+  auto p_full = [&](int X) { return bars + 8u * (B_P + X); };
   const uint32_t dq_full = bars + 8u * B_DQF;
   const uint32_t dq_empty = bars + 8u * B_DQE;
   const uint32_t kv_done = bars + 8u * B_KVDONE;
@@ -140,7 +141,10 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 160);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_BAR + 168);
 
-  if (*(volatile int*)a.status != 0) return;  // an earlier device error skips the work
+  // an earlier device error skips the work; thread 0 alone reads the word and
+  // the barrier hands every thread the same answer, so the CTA leaves whole
+  // or not at all (the word can change while the CTA starts)
+  if (__syncthreads_or(threadIdx.x == 0 && *(volatile int*)a.status != 0)) return;
   // the 128-byte-swizzled tiles need a 1024-byte aligned base; the layout has
   // no slack to realign it
   if (base & 1023u) {
@@ -166,7 +170,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
       mbar_init(qd_empty(s), 1);
     }
     mbar_init(dp_full, 1);
-    mbar_init(p_full, 256);
+    mbar_init(p_full(0), 256);
+    mbar_init(p_full(1), 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(kv_done, 1);
@@ -246,7 +251,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
         if (lane == 0 && !*abort_flag) {
           constexpr uint32_t id_f = idesc_f16_f32(128, 128, false, false, false);  // S^T, dP^T
           constexpr uint32_t id_kv = idesc_f16_f32(128, 128, false, true, false);  // dV, dK
-          constexpr uint32_t id_q = idesc_f16_f32(128, 128, true, true, false);    // dQ^T
+          constexpr uint32_t id_q64 = idesc_f16_f32(128, 64, true, true, false);   // dQ^T half
           // base descriptors, computed once: the issue loops only add constants
           const uint64_t dK_k = sdesc_sw128(base + OFF_K, 16, 1024);           // K, K-major
           const uint64_t dV_k = sdesc_sw128(base + OFF_V, 16, 1024);           // V, K-major
@@ -277,27 +282,39 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           }
           for (int j = 0; j < nq && ok; ++j) {
             const uint32_t cur = it + j, so = qst(cur) * TILE_BYTES;
-            if (!(ok = mbar_wait(p_full, cur & 1u, a.status, abort_flag, a.limit_ns))) break;
-            tc_fence_after();
-            // dK += dS^T Q: M = 128 keys, N = 128 dh, K = 128 queries
             const uint64_t bdo = sdesc_add(dDO_mn, so), bq = sdesc_add(dQ_mn, so);
             const uint32_t acc0 = j > 0 ? 1u : 0u;
+            // The query tile in two halves X = A, B (queries 64X .. 64X+63): the
+            // MMAs of half A run while the P/dS warps work on half B.
 #pragma unroll
-            for (int kk = 0; kk < BR / 16; ++kk)
-              umma_f16_ss_hot(tmem + TM_DK,
-                              sdesc_add(dDS_k, (kk >> 2) * BOX_BYTES + (kk & 3) * 32),
-                              sdesc_add(bq, kk * 2048), id_kv, kk > 0 ? 1u : acc0);
-            // dQ^T(cur) = K^T dS^T: M = 128 dh, N = 128 queries, K = 128 keys
+            for (int X = 0; X < 2; ++X) {
+              if (!(ok = mbar_wait(p_full(X), cur & 1u, a.status, abort_flag, a.limit_ns))) break;
+              tc_fence_after();
+              // dK += dS^T Q over the half's queries: M = 128 keys, N = 128 dh, K = 64
 #pragma unroll
-            for (int kk = 0; kk < BC / 16; ++kk)
-              umma_f16_ss_hot(tmem + TM_SQ, sdesc_add(dK_mn, kk * 2048), sdesc_add(dDS_mn, kk * 2048),
-                              id_q, kk > 0 ? 1u : 0u);
-            umma_commit(dq_full);
-            // dV += P^T dO (A = P^T from TMEM: queries 64g + 16m.. at column 64g + 8m)
+              for (int k4 = 0; k4 < 4; ++k4) {
+                const int kk = 4 * X + k4;
+                umma_f16_ss_hot(tmem + TM_DK, sdesc_add(dDS_k, X * BOX_BYTES + k4 * 32),
+                                sdesc_add(bq, kk * 2048), id_kv, kk > 0 ? 1u : acc0);
+              }
+              // dQ^T of the half = K^T dS^T: M = 128 dh, N = 64 queries, K = 128 keys,
+              // into S^T's columns of the same queries (the half has read them)
 #pragma unroll
-            for (int kk = 0; kk < BR / 16; ++kk)
-              umma_f16_ts_hot(tmem + TM_DV, tmem + TM_DPP + 64 * (kk >> 2) + 8 * (kk & 3),
-                              sdesc_add(bdo, kk * 2048), id_kv, kk > 0 ? 1u : acc0);
+              for (int kk = 0; kk < BC / 16; ++kk)
+                umma_f16_ss_hot(tmem + TM_SQ + 64 * X, sdesc_add(dK_mn, kk * 2048),
+                                sdesc_add(dDS_mn, X * BOX_BYTES + kk * 2048), id_q64,
+                                kk > 0 ? 1u : 0u);
+              if (X == 1) umma_commit(dq_full);
+              // dV += P^T dO over the half (A = P^T from TMEM: queries 16kk .. 16kk+15
+              // at column 32 (kk / 2) + 8 (kk % 2))
+#pragma unroll
+              for (int k4 = 0; k4 < 4; ++k4) {
+                const int kk = 4 * X + k4;
+                umma_f16_ts_hot(tmem + TM_DV, tmem + TM_DPP + 32 * (kk >> 1) + 8 * (kk & 1),
+                                sdesc_add(bdo, kk * 2048), id_kv, kk > 0 ? 1u : acc0);
+              }
+            }
+            if (!ok) break;
             umma_commit(qd_empty(qst(cur)));
             if (j + 1 < nq) {
               const uint32_t nx = cur + 1, so1 = qst(nx) * TILE_BYTES;
@@ -381,7 +398,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        uint8_t* drow = gbase + OFF_DS + half * BOX_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
+        uint8_t* drow = gbase + OFF_DS + (row >> 3) * 1024 + (row & 7) * 128;
         bool ok = true;
         for (int j = 0; j < nq; ++j) {
           const uint32_t cur = it + j, st = qst(cur);
@@ -393,9 +410,11 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           const float* Dl = L + BR;
           // query tile == key tile (the first of each head): key index > query index is masked
           const bool diag = GROUPED ? j % nqh == 0 : j == 0;
+          // query half X (queries 64X .. 64X+63) by all eight warps, A then B:
+          // warps w and w+4 share a key and take 32 queries of the half each
 #pragma unroll
-          for (int ch = 0; ch < 2; ++ch) {
-            const int qb = half * 64 + ch * 32;    // this chunk's 32 query columns
+          for (int X = 0; X < 2; ++X) {
+            const int qb = X * 64 + half * 32;     // this thread's 32 query columns
             uint32_t sv[32], dv[32];
             tmem_ld32(lane_base + TM_SQ + qb, sv);
             tmem_ld32(lane_base + TM_DPP + qb, dv);
@@ -424,20 +443,21 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
                 dk[c8 * 4 + (e >> 1)] = pack_f16(dd[0], dd[1]);
               }
             }
-            // P^T over this thread's own dP^T columns: queries qb.. -> column half*64 + ch*16
-            tmem_st16(lane_base + TM_DPP + half * 64 + ch * 16, pk);
-            // dS^T row `row`, queries qb.. -> box `half`, 16-byte chunks 4*ch .. 4*ch+3
+            // P^T over dP^T columns this thread has read: queries qb .. qb+31 ->
+            // columns qb .. qb+15 (query chunk kk at 32 (kk / 2) + 8 (kk % 2))
+            tmem_st16(lane_base + TM_DPP + qb, pk);
+            // dS^T row `row`, queries qb.. -> box X, 16-byte chunks 4*half .. 4*half+3
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-              const int chunk = ch * 4 + c;
-              *reinterpret_cast<uint4*>(drow + ((chunk ^ (row & 7)) << 4)) =
+              const int chunk = half * 4 + c;
+              *reinterpret_cast<uint4*>(drow + X * BOX_BYTES + ((chunk ^ (row & 7)) << 4)) =
                   make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
             }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(p_full(X));
           }
-          tmem_wait_st();
-          fence_proxy_async_smem();
-          tc_fence_before();
-          mbar_arrive(p_full);
         }
         // dK, dV of this key tile -> fp16 rows
         bool eok = ok && mbar_wait(kv_done, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
@@ -447,19 +467,25 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           const float mul = half == 0 ? a.scale * kOperandUnscale : kOperandUnscale;
           ct_t* out = dkrow + half * a.dkv;   // warps 0-3 write dK, warps 4-7 write dV
 #pragma unroll 1
+          // (a dS beyond fp16 range makes dK and dQ non-finite, so the checks
+          // of the dK, dV rows here and of dQ in dq_convert_kernel cover it)
+          bool bad = false;
           for (int q = 0; q < 4; ++q) {
             uint32_t v[32];
             tmem_ld32(lane_base + (half == 0 ? TM_DK : TM_DV) + q * 32, v);
             tmem_wait_ld();
+            float f[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
+            bad |= f16_bad_n<32>(f);
             uint4* dst = reinterpret_cast<uint4*>(out + q * 32);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              dst[c] = make_uint4(
-                  pack_f16(__uint_as_float(v[8 * c]) * mul, __uint_as_float(v[8 * c + 1]) * mul),
-                  pack_f16(__uint_as_float(v[8 * c + 2]) * mul, __uint_as_float(v[8 * c + 3]) * mul),
-                  pack_f16(__uint_as_float(v[8 * c + 4]) * mul, __uint_as_float(v[8 * c + 5]) * mul),
-                  pack_f16(__uint_as_float(v[8 * c + 6]) * mul, __uint_as_float(v[8 * c + 7]) * mul));
+              dst[c] = make_uint4(pack_f16(f[8 * c], f[8 * c + 1]), pack_f16(f[8 * c + 2], f[8 * c + 3]),
+                                  pack_f16(f[8 * c + 4], f[8 * c + 5]),
+                                  pack_f16(f[8 * c + 6], f[8 * c + 7]));
           }
+          if (bad) report_status(a.status, (int)TSP_ERR_RANGE);
         }
         tc_fence_before();
       }
@@ -502,19 +528,22 @@ __global__ void attn_delta_kernel(const ct_t* __restrict__ o, const ct_t* __rest
 
 // dQKV[:, 0:d] = fp16(dq_acc); dQKV rows are ld elements apart
 __global__ void dq_convert_kernel(const float* __restrict__ acc, ct_t* __restrict__ dqkv,
-                                  int64_t S, int d, int64_t ld) {
+                                  int64_t S, int d, int64_t ld, int* __restrict__ status) {
   const int64_t total4 = S * d / 4;
+  bool bad = false;   // an fp16 output out of range
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total4;
        t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t e = t * 4;
     const int64_t row = e / d;
     const int col = (int)(e - row * d);
     const float4 v = reinterpret_cast<const float4*>(acc)[t];
+    bad |= f16_bad(v.x) | f16_bad(v.y) | f16_bad(v.z) | f16_bad(v.w);
     uint2 o;
     o.x = pack_f16(v.x, v.y);
     o.y = pack_f16(v.z, v.w);
     *reinterpret_cast<uint2*>(dqkv + row * ld + col) = o;
   }
+  if (bad) report_status(status, (int)TSP_ERR_RANGE);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -595,14 +624,15 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
   a->limit_ns = wait_limit_ns();
   const bool grouped = Hkv != H;
   auto kern = grouped ? attn_bwd_tc_kernel<true> : attn_bwd_tc_kernel<false>;
-  static bool attr[2] = {false, false};
+  static bool attr[kMaxDevices][2] = {};   // the attribute holds for one device
   static int launch_regs[2] = {0, 0};
-  if (!attr[grouped]) {
+  const int dev = current_device();
+  if (!attr[dev][grouped]) {
     TSP_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM));
     cudaFuncAttributes fa;
     TSP_CUDA_TRY(cudaFuncGetAttributes(&fa, kern));
     launch_regs[grouped] = fa.numRegs;
-    attr[grouped] = true;
+    attr[dev][grouped] = true;
   }
   // setmaxnreg.inc would wait forever if the split exceeded the launch allocation
   const int64_t lr = launch_regs[grouped];
@@ -614,7 +644,7 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
     TSP_CUDA_TRY(cudaGetLastError());
   }
   Prof prof("attn_bwd_dq_convert", st);
-  dq_convert_kernel<<<num_sms() * 8, 256, 0, st>>>(dq_acc, (ct_t*)dqkv, S, d, ld);
+  dq_convert_kernel<<<num_sms() * 8, 256, 0, st>>>(dq_acc, (ct_t*)dqkv, S, d, ld, a->status);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }

@@ -115,7 +115,10 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 160);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_BAR + 168);
 
-  if (*(volatile int*)a.status != 0) return;  // an earlier device error skips the work
+  // an earlier device error skips the work; thread 0 alone reads the word and
+  // the barrier hands every thread the same answer, so the CTA leaves whole
+  // or not at all (the word can change while the CTA starts)
+  if (__syncthreads_or(threadIdx.x == 0 && *(volatile int*)a.status != 0)) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
@@ -498,15 +501,16 @@ tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, 
   a->scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
   a->status = status_word();
   a->limit_ns = wait_limit_ns();
-  static bool attr = false;
+  static bool attr[kMaxDevices] = {};   // the attribute holds for one device
   static int launch_regs = 0;
-  if (!attr) {
+  const int dev = current_device();
+  if (!attr[dev]) {
     TSP_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_tc_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM));
     cudaFuncAttributes fa;
     TSP_CUDA_TRY(cudaFuncGetAttributes(&fa, attn_fwd_tc_kernel));
     launch_regs = fa.numRegs;
-    attr = true;
+    attr[dev] = true;
   }
   // setmaxnreg.inc would wait forever if the split exceeded the launch allocation
   if ((int64_t)launch_regs * NTHR < (int64_t)REG_TOTAL) return TSP_ERR_UNSUPPORTED;

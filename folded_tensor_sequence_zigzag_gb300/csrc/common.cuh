@@ -23,6 +23,13 @@ namespace tsp {
 // it as a parameter; they write TSP_ERR_TIMEOUT there and never trap.
 int* status_word();
 int num_sms();
+// Ordinal of the current device (0 if it cannot be read).  Per-device state
+// (function attributes, symbol addresses) is kept in arrays of kMaxDevices.
+constexpr int kMaxDevices = 64;
+int current_device();
+// Failure-detection knob (tsp_debug_skip_stage): true for each of the next n
+// tensor-core GEMM launches after tsp_debug_skip_stage(n).
+bool take_debug_skip();
 // Default limit of one pipeline wait, in nanoseconds of %globaltimer.
 uint64_t wait_limit_ns();
 
@@ -70,6 +77,20 @@ __device__ __forceinline__ void report_timeout(int* status) {
 // Records `code` in the sticky status word unless an error is already there.
 __device__ __forceinline__ void report_status(int* status, int code) {
   atomicCAS(status, 0, code);
+}
+
+// fp16 range of the internal tensor-core operands: a value becomes a finite
+// fp16 only if |v| < 65520 (the largest fp16, 65504, plus half its spacing);
+// anything else -- NaN included -- turns into inf or NaN.  Kernels that store
+// an fp16 operand OR this test over the values they store and record
+// TSP_ERR_RANGE once.
+__device__ __forceinline__ bool f16_bad(float v) { return !(fabsf(v) < 65520.f); }
+template <int N>
+__device__ __forceinline__ bool f16_bad_n(const float* f) {
+  bool b = false;
+#pragma unroll
+  for (int j = 0; j < N; ++j) b |= f16_bad(f[j]);
+  return b;
 }
 
 // ---- mbarrier -------------------------------------------------------------

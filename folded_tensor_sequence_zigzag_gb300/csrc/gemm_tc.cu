@@ -25,6 +25,7 @@
 // that runs out records TSP_ERR_TIMEOUT, drains the CTA's copies and MMAs,
 // frees TMEM and returns.
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <memory>
@@ -56,7 +57,7 @@ struct KParams {
   int kseg_kb[4];
   int nseg_n;
   int rot_rows, rot_D, rot_r0;
-  int tiles_m, tiles_n, group_m;
+  int tiles_m, tiles_n, group_m, group_n;   // tile order: see slab_order()
   int n_tile;  // output columns per tile (256, or 128 for the paired SwiGLU tile)
   void* out;
   int64_t ldo;
@@ -78,7 +79,22 @@ struct KParams {
   int shard_kb[65];
 };
 
+// Output tile of tile index t.  The output is walked in slabs: group_m
+// M-tiles across every N-tile (group_n == 0), or group_n N-tiles across every
+// M-tile; inside a slab the slab's own dimension varies fastest, so the tiles
+// that run at the same time on the persistent CTAs share the slab's operand
+// tiles and every wave touches all of them.
 __device__ __forceinline__ void tile_of(const KParams& p, int t, int& mb, int& nb) {
+  if (p.group_n > 0) {
+    const int per_group = p.group_n * p.tiles_m;
+    const int g = t / per_group;
+    const int first = g * p.group_n;
+    const int gs = min(p.tiles_n - first, p.group_n);
+    const int r = t - g * per_group;
+    nb = first + r % gs;
+    mb = r / gs;
+    return;
+  }
   const int per_group = p.group_m * p.tiles_n;
   const int g = t / per_group;
   const int first = g * p.group_m;
@@ -153,8 +169,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // a device error recorded earlier (sticky until the host resets it) skips the work
-  if (*(volatile int*)p.status != 0) return;
+  // a device error recorded earlier (sticky until the host resets it) skips the
+  // work; thread 0 alone reads the word and the barrier hands every thread the
+  // same answer, so the CTA leaves whole or not at all
+  if (__syncthreads_or(threadIdx.x == 0 && *(volatile int*)p.status != 0)) return;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
@@ -326,6 +344,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
     int acc = 0;
     uint32_t acc_phase = 0;
     const int row = warp * 32 + lane;
+    bool bad = false;   // an fp16 output out of range
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       int mb, nb;
       tile_of(p, t, mb, nb);
@@ -351,6 +370,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
               fb[j] = __uint_as_float(vb[j]);
               g[j] = fa[j] * sigmoidf_(fa[j]) * fb[j];
             }
+            bad |= f16_bad_n<32>(g);
+            if (p.out2) bad |= f16_bad_n<32>(fa) | f16_bad_n<32>(fb);
             store16x32((ct_t*)p.out + (int64_t)m * p.ldo + n, g);
             if (p.out2) store16x32((ct_t*)p.out2 + (int64_t)m * p.ldo2 + n, fa);
             if (p.out3) store16x32((ct_t*)p.out3 + (int64_t)m * p.ldo3 + n, fb);
@@ -368,6 +389,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
 #pragma unroll
           for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
           if constexpr (EPI == EPI_STORE) {
+            if (p.out_type == OUT_F16) bad |= f16_bad_n<32>(f);
             store_any32(p.out, (int64_t)m * p.ldo + n, f, p.out_type);
           } else if constexpr (EPI == EPI_RES) {
             float r[32];
@@ -384,6 +406,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) f[j] += r[j];
+            if (p.out_type == OUT_F16) bad |= f16_bad_n<32>(f);
             store_any32(p.out, (int64_t)m * p.ldo + n, f, p.out_type);
           } else if constexpr (EPI == EPI_F32) {
             float* dst;
@@ -405,6 +428,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
               da[j] = f[j] * b[j] * s * (1.f + a[j] * (1.f - s));
               db[j] = f[j] * a[j] * s;
             }
+            bad |= f16_bad_n<32>(da) | f16_bad_n<32>(db);
             store16x32((ct_t*)p.out + (int64_t)m * p.ldo + n, da);
             store16x32((ct_t*)p.out2 + (int64_t)m * p.ldo2 + n, db);
           }
@@ -418,6 +442,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
         acc_phase ^= 1u;
       }
     }
+    if (bad) report_status(p.status, (int)TSP_ERR_RANGE);
   }
 
   tc_fence_before();
@@ -470,11 +495,12 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int
 template <int EPI, bool A_MN, bool B_MN, bool PAIRED>
 tsp_status launch_t(const KParams& kp, int grid, cudaStream_t st, const char* name) {
   Prof prof(name, st);
-  static bool attr_set = false;
+  static bool attr_set[kMaxDevices] = {};   // the attribute holds for one device
   auto kern = gemm_tc_kernel<EPI, A_MN, B_MN, PAIRED>;
-  if (!attr_set) {
+  const int dev = current_device();
+  if (!attr_set[dev]) {
     TSP_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-    attr_set = true;
+    attr_set[dev] = true;
   }
   kern<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(kp);
   TSP_CUDA_TRY(cudaGetLastError());
@@ -482,6 +508,51 @@ tsp_status launch_t(const KParams& kp, int grid, cudaStream_t st, const char* na
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// L2 share (bytes) that the resident operand slab of a GEMM may take: the
+// rest of the 129 MB L2 holds the streamed operand's tiles in flight and the
+// output lines being written back.  Measured on the 7B-shaped block forward
+// (S=16384): 48 MB beats the fixed 16-M-tile order (W_1|W_3 -3.5%, W_2 and
+// W_O -1.5%), while 64 MB and 96 MB slabs were 7% and 16% slower -- lines
+// read by SMs of both dies seem to occupy L2 space on both, so only about
+// half of the L2 is there for a resident slab.  TSP_GEMM_SLAB_MB (read once) overrides
+// the default for tuning runs; 0 keeps the fixed order of 16-M-tile slabs.
+size_t slab_budget() {
+  static size_t v = [] {
+    const char* e = getenv("TSP_GEMM_SLAB_MB");
+    size_t mb = 48;
+    if (e && atoll(e) >= 0 && *e) mb = (size_t)atoll(e);
+    return mb << 20;
+  }();
+  return v;
+}
+
+// Tile order of a GEMM: which operand slab stays in L2.  A slab of g M-tiles
+// (BM rows of A, all of K each) is read once and every wave of the slab
+// touches all of it, so it stays resident while the B tiles stream past; B
+// is then read once per slab.  DRAM reads of the operands:
+//   M slabs of g tiles: A + B * ceil(tiles_m / g)
+//   N slabs of g tiles: B + A * ceil(tiles_n / g)
+// with g as large as the slab budget allows; the cheaper order wins.  For a
+// very long K (the weight gradients, K = tokens) a slab holds few tiles and
+// the reuse inside one wave dominates; those keep slabs of 16 M-tiles.
+void slab_order(KParams* kp, int K) {
+  const double a_tile = (double)BM * K * 2, b_tile = 256.0 * K * 2;   // fp16 operand bytes
+  const double A = a_tile * kp->tiles_m, B = b_tile * kp->tiles_n;
+  kp->group_n = 0;
+  kp->group_m = std::min(16, kp->tiles_m);
+  const double budget = (double)slab_budget();
+  if (K > 16384 || budget <= 0) return;
+  const int gm = (int)std::max(1.0, std::min((double)kp->tiles_m, std::floor(budget / a_tile)));
+  const int gn = (int)std::max(1.0, std::min((double)kp->tiles_n, std::floor(budget / b_tile)));
+  const double via_m = A + B * std::ceil((double)kp->tiles_m / gm);
+  const double via_n = B + A * std::ceil((double)kp->tiles_n / gn);
+  if (via_n < via_m) {
+    kp->group_n = gn;
+  } else {
+    kp->group_m = gm;
+  }
+}
 
 }  // namespace
 
@@ -510,7 +581,7 @@ tsp_status gemm_tc(const TcGemm& g, cudaStream_t st) {
   kp->n_tile = g.paired ? 128 : BN;
   kp->tiles_m = (g.M + BM - 1) / BM;
   kp->tiles_n = (g.N + kp->n_tile - 1) / kp->n_tile;
-  kp->group_m = std::min(16, kp->tiles_m);
+  slab_order(kp, g.K);
   // operand maps
   for (int s = 0; s < g.nks; ++s) {
     const int klen = g.kseg_len[s];
@@ -562,14 +633,10 @@ tsp_status gemm_tc(const TcGemm& g, cudaStream_t st) {
   for (int i = 0; i < 3; ++i) kp->outs[i] = g.outs[i];
   kp->status = status_word();
   kp->limit_ns = wait_limit_ns();
-  {
-    // TSP_DEBUG_SKIP_STAGE=1 (read on every call): CTA 0 of the next GEMM never
-    // fills its first pipeline stage, which exercises the bounded-wait path
-    // (TSP_ERR_TIMEOUT in the status word after TSP_WAIT_LIMIT_MS) without a
-    // fault or a hang.  Used by the failure-detection test only.
-    const char* e = getenv("TSP_DEBUG_SKIP_STAGE");
-    kp->debug_skip = (e && atoi(e) > 0) ? 1 : 0;
-  }
+  // tsp_debug_skip_stage: CTA 0 of this GEMM never fills its first pipeline
+  // stage, which exercises the bounded-wait path (TSP_ERR_TIMEOUT in the status
+  // word after TSP_WAIT_LIMIT_MS) without a fault or a hang
+  kp->debug_skip = take_debug_skip() ? 1 : 0;
   const int tiles = kp->tiles_m * kp->tiles_n;
   const int grid = std::min(tiles, num_sms());
   switch (g.epi) {

@@ -30,7 +30,7 @@ tsp_status launch_rmsnorm_bwd(const float* dout, const void* u, int u_ty, const 
                               float* out_f32, void* out_t, int out_ty, float* dg, float* dg_part,
                               int64_t rows, int n, int dtype, cudaStream_t st);
 tsp_status launch_convert_bf16_f16(const void* src, void* dst, int64_t n, cudaStream_t st);
-tsp_status launch_convert_f32_bf16(const float* src, void* dst, int64_t n, cudaStream_t st);
+tsp_status launch_convert_f32_f16(const float* src, void* dst, int64_t n, cudaStream_t st);
 // rotary embedding: table[row][j] = (cos, sin) of pos(row) * base^(-2j/dh), j < dh/2,
 // pos(row) the global position of zigzag row `row`; then rotate the Q (cols
 // [0, d)) and K (cols [d, 2d)) blocks of a [S, ld] buffer of type ty in place
@@ -112,5 +112,21 @@ struct DecodeAttn {
 };
 int64_t decode_splits(int64_t S, int D, int64_t n_rows);
 tsp_status launch_decode_attn(const DecodeAttn& a, cudaStream_t st);
+
+// api.cu: the block forward and backward with the residual stream's element
+// type chosen per call (the C entry points pass the cfg dtype; the stack keeps
+// the stream between layers in fp32).  In a bf16 configuration x_f32 / y_f32 /
+// dy_f32 select fp32 for x, y and dy; in an fp32 configuration everything is
+// fp32 and the flags are ignored.  prep (nullable): fp16 weight copies made
+// by tsp_block_weights_prepare (bf16 only), used instead of converting the
+// weights in the call.  Arguments are checked as by tsp_block_fwd /
+// tsp_block_bwd (and their _prepared forms).
+tsp_status block_fwd_checked(const tsp_cfg* cfg, const void* x_z, bool x_f32, const tsp_attn_w* aw,
+                             const tsp_mlp_w* mw, const void* prep, void* y_z, bool y_f32,
+                             void* saved, void* ws, size_t ws_bytes, cudaStream_t st);
+tsp_status block_bwd_checked(const tsp_cfg* cfg, const void* x_z, bool x_f32, const void* dy_z,
+                             bool dy_f32, const void* saved, const tsp_attn_w* aw,
+                             const tsp_mlp_w* mw, const void* prep, float* dx_z,
+                             float* const* grads, void* ws, size_t ws_bytes, cudaStream_t st);
 
 }  // namespace tsp

@@ -9,6 +9,8 @@
 #include <cmath>
 #include <cstring>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -100,8 +102,10 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const Tin* __restrict_
                                                           const Tg* __restrict__ g,
                                                           T* __restrict__ out,
                                                           float* __restrict__ rstd_out,
-                                                          int64_t rows, int n, float eps) {
+                                                          int64_t rows, int n, float eps,
+                                                          int* __restrict__ status) {
   const int lane = threadIdx.x & 31;
+  bool bad = false;   // an fp16 output out of range
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int nu = n >> 3;  // 8-element units per row
   for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
@@ -130,10 +134,12 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const Tin* __restrict_
         load8(g + idx * 8, gf);
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[i][e] = v[i][e] * r * gf[e];
+        if constexpr (std::is_same<T, __half>::value) bad |= f16_bad_n<8>(v[i]);
         store8(dst + idx * 8, v[i]);
       }
     }
   }
+  if (bad) report_status(status, (int)TSP_ERR_RANGE);
 }
 
 // Row-per-CTA variant for n % 512 == 0, n <= 16384: n/16 threads, 16 elements
@@ -146,8 +152,10 @@ __global__ void __launch_bounds__(1024) rmsnorm_fwd_cta_kernel(const Tin* __rest
                                                                const Tg* __restrict__ g,
                                                                T* __restrict__ out,
                                                                float* __restrict__ rstd_out,
-                                                               int64_t rows, int n, float eps) {
+                                                               int64_t rows, int n, float eps,
+                                                               int* __restrict__ status) {
   __shared__ float part[2][32];
+  bool bad = false;   // an fp16 output out of range
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nw = blockDim.x >> 5;
   const int c0 = t * 8, c1 = (t + blockDim.x) * 8;   // this thread's two units
   float gf0[8], gf1[8];
@@ -175,17 +183,20 @@ __global__ void __launch_bounds__(1024) rmsnorm_fwd_cta_kernel(const Tin* __rest
       v1[e] = v1[e] * r * gf1[e];
     }
     T* dst = out + row * n;
+    if constexpr (std::is_same<T, __half>::value) bad |= f16_bad_n<8>(v0) | f16_bad_n<8>(v1);
     store8(dst + c0, v0);
     store8(dst + c1, v1);
   }
+  if (bad) report_status(status, (int)TSP_ERR_RANGE);
 }
 
 // Scalar fallback for rows whose length is not a multiple of 8 (or unaligned).
 template <typename Tin, typename Tg, typename T>
 __global__ void rmsnorm_fwd_scalar_kernel(const Tin* __restrict__ u, const Tg* __restrict__ g,
                                           T* __restrict__ out, float* __restrict__ rstd_out,
-                                          int64_t rows, int n, float eps) {
+                                          int64_t rows, int n, float eps, int* __restrict__ status) {
   const int lane = threadIdx.x & 31;
+  bool bad = false;   // an fp16 output out of range
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
        row += warps) {
@@ -197,9 +208,13 @@ __global__ void rmsnorm_fwd_scalar_kernel(const Tin* __restrict__ u, const Tg* _
     ss = warp_sum(ss);
     const float r = rsqrtf(ss / (float)n + eps);
     if (lane == 0 && rstd_out) rstd_out[row] = r;
-    for (int i = lane; i < n; i += 32)
-      out[row * n + i] = from_f<T>(to_f(u[row * n + i]) * r * to_f(g[i]));
+    for (int i = lane; i < n; i += 32) {
+      const float o = to_f(u[row * n + i]) * r * to_f(g[i]);
+      if constexpr (std::is_same<T, __half>::value) bad |= f16_bad(o);
+      out[row * n + i] = from_f<T>(o);
+    }
   }
+  if (bad) report_status(status, (int)TSP_ERR_RANGE);
 }
 
 template <typename Tin, typename Tg, typename T>
@@ -210,20 +225,21 @@ static tsp_status rmsnorm_fwd_t(const Tin* u, const Tg* g, T* out, float* rstd, 
   const bool vec_ok = (n % 8 == 0) && ((uintptr_t)u % 16 == 0) && ((uintptr_t)g % 16 == 0) &&
                       ((uintptr_t)out % 16 == 0);
   const int nu = n / 8;
+  int* status = status_word();
   Prof prof("rmsnorm_fwd", st);
   if (vec_ok && n % 512 == 0 && n <= 16384) {
     const int threads = n / 16;
     const int per_sm = std::max(1, 2048 / threads);
     const int grid2 = (int)std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)num_sms() * per_sm));
-    rmsnorm_fwd_cta_kernel<Tin, Tg, T><<<grid2, threads, 0, st>>>(u, g, out, rstd, rows, n, eps);
+    rmsnorm_fwd_cta_kernel<Tin, Tg, T><<<grid2, threads, 0, st>>>(u, g, out, rstd, rows, n, eps, status);
   } else if (vec_ok && nu <= 32)
-    rmsnorm_fwd_kernel<Tin, Tg, T, 1><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
+    rmsnorm_fwd_kernel<Tin, Tg, T, 1><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps, status);
   else if (vec_ok && nu <= 128)
-    rmsnorm_fwd_kernel<Tin, Tg, T, 4><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
+    rmsnorm_fwd_kernel<Tin, Tg, T, 4><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps, status);
   else if (vec_ok && nu <= 512)
-    rmsnorm_fwd_kernel<Tin, Tg, T, 16><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
+    rmsnorm_fwd_kernel<Tin, Tg, T, 16><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps, status);
   else
-    rmsnorm_fwd_scalar_kernel<Tin, Tg, T><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps);
+    rmsnorm_fwd_scalar_kernel<Tin, Tg, T><<<grid, 256, 0, st>>>(u, g, out, rstd, rows, n, eps, status);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }
@@ -480,15 +496,24 @@ tsp_status launch_rmsnorm_bwd(const float* dout, const void* u, int u_ty, const 
   return TSP_ERR_UNSUPPORTED;
 }
 
+// Eight bf16 values -> fp16 (exact whenever in range); `bad` collects values
+// fp16 cannot hold.
+__device__ __forceinline__ uint4 cvt8_bf16_f16(const uint4 v, bool& bad) {
+  float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+  bad |= f16_bad_n<8>(f);
+  return make_uint4(pack_f16(f[0], f[1]), pack_f16(f[2], f[3]), pack_f16(f[4], f[5]),
+                    pack_f16(f[6], f[7]));
+}
+
 // bf16 -> fp16, 8 elements per thread-iteration (n % 8 == 0, 16-byte aligned)
 __global__ void convert_bf16_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                        int64_t n8) {
+                                        int64_t n8, int* __restrict__ status) {
+  bool bad = false;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n8;
-       t += (int64_t)gridDim.x * blockDim.x) {
-    const uint4 v = src[t];
-    dst[t] = make_uint4(pack_f16(bf16_lo(v.x), bf16_hi(v.x)), pack_f16(bf16_lo(v.y), bf16_hi(v.y)),
-                        pack_f16(bf16_lo(v.z), bf16_hi(v.z)), pack_f16(bf16_lo(v.w), bf16_hi(v.w)));
-  }
+       t += (int64_t)gridDim.x * blockDim.x)
+    dst[t] = cvt8_bf16_f16(src[t], bad);
+  if (bad) report_status(status, (int)TSP_ERR_RANGE);
 }
 
 tsp_status launch_convert_bf16_f16(const void* src, void* dst, int64_t n, cudaStream_t st) {
@@ -496,7 +521,7 @@ tsp_status launch_convert_bf16_f16(const void* src, void* dst, int64_t n, cudaSt
   Prof prof("convert_bf16_f16", st);
   const int64_t n8 = n / 8;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((n8 + 255) / 256, (int64_t)num_sms() * 8));
-  convert_bf16_f16_kernel<<<grid, 256, 0, st>>>((const uint4*)src, (uint4*)dst, n8);
+  convert_bf16_f16_kernel<<<grid, 256, 0, st>>>((const uint4*)src, (uint4*)dst, n8, status_word());
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }
@@ -511,17 +536,18 @@ struct ConvertList {
   int count;
 };
 
-__global__ void convert_bf16_f16_many_kernel(const __grid_constant__ ConvertList L) {
+__global__ void convert_bf16_f16_many_kernel(const __grid_constant__ ConvertList L,
+                                             int* __restrict__ status) {
   const int64_t total = L.end8[L.count - 1];
   int seg = 0;
+  bool bad = false;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
     while (t >= L.end8[seg]) ++seg;
     const int64_t i = t - (seg > 0 ? L.end8[seg - 1] : 0);
-    const uint4 v = L.src[seg][i];
-    L.dst[seg][i] = make_uint4(pack_f16(bf16_lo(v.x), bf16_hi(v.x)), pack_f16(bf16_lo(v.y), bf16_hi(v.y)),
-                               pack_f16(bf16_lo(v.z), bf16_hi(v.z)), pack_f16(bf16_lo(v.w), bf16_hi(v.w)));
+    L.dst[seg][i] = cvt8_bf16_f16(L.src[seg][i], bad);
   }
+  if (bad) report_status(status, (int)TSP_ERR_RANGE);
 }
 
 tsp_status launch_convert_bf16_f16_many(const void* const* src, void* const* dst, const int64_t* n,
@@ -542,28 +568,32 @@ tsp_status launch_convert_bf16_f16_many(const void* const* src, void* const* dst
   if (acc == 0) return TSP_OK;
   Prof prof("convert_bf16_f16", st);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((acc + 255) / 256, (int64_t)num_sms() * 8));
-  convert_bf16_f16_many_kernel<<<grid, 256, 0, st>>>(L);
+  convert_bf16_f16_many_kernel<<<grid, 256, 0, st>>>(L, status_word());
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }
 
-// fp32 -> bf16 (round to nearest), 8 elements per thread-iteration
-__global__ void convert_f32_bf16_kernel(const float4* __restrict__ src, uint4* __restrict__ dst,
-                                        int64_t n8) {
+// fp32 -> fp16 (round to nearest), 8 elements per thread-iteration
+__global__ void convert_f32_f16_kernel(const float4* __restrict__ src, uint4* __restrict__ dst,
+                                       int64_t n8, int* __restrict__ status) {
+  bool bad = false;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n8;
        t += (int64_t)gridDim.x * blockDim.x) {
     const float4 a = src[2 * t], b = src[2 * t + 1];
-    dst[t] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
-                        pack_bf16(b.z, b.w));
+    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    bad |= f16_bad_n<8>(f);
+    dst[t] = make_uint4(pack_f16(a.x, a.y), pack_f16(a.z, a.w), pack_f16(b.x, b.y),
+                        pack_f16(b.z, b.w));
   }
+  if (bad) report_status(status, (int)TSP_ERR_RANGE);
 }
 
-tsp_status launch_convert_f32_bf16(const float* src, void* dst, int64_t n, cudaStream_t st) {
+tsp_status launch_convert_f32_f16(const float* src, void* dst, int64_t n, cudaStream_t st) {
   if (n % 8 != 0 || ((uintptr_t)src & 15u) || ((uintptr_t)dst & 15u)) return TSP_ERR_UNSUPPORTED;
-  Prof prof("convert_f32_bf16", st);
+  Prof prof("convert_f32_f16", st);
   const int64_t n8 = n / 8;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((n8 + 255) / 256, (int64_t)num_sms() * 8));
-  convert_f32_bf16_kernel<<<grid, 256, 0, st>>>((const float4*)src, (uint4*)dst, n8);
+  convert_f32_f16_kernel<<<grid, 256, 0, st>>>((const float4*)src, (uint4*)dst, n8, status_word());
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }
@@ -617,9 +647,11 @@ tsp_status launch_rope_table(float2* table, int64_t S, int D, int dh, float base
 // Heads 0..H-1 are Q's (column 0), heads H..H+Hkv-1 are K's (column d).
 template <typename T>
 __global__ void rope_kernel(T* __restrict__ qkv, int64_t S, int ld, int d, int H, int Hkv,
-                            int half, const float2* __restrict__ tab, float sgn) {
+                            int half, const float2* __restrict__ tab, float sgn,
+                            int* __restrict__ status) {
   const int64_t per_row = (int64_t)(H + Hkv) * half;
   const int64_t total = S * per_row;
+  bool bad = false;   // an fp16 output out of range
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t row = t / per_row;
@@ -630,9 +662,12 @@ __global__ void rope_kernel(T* __restrict__ qkv, int64_t S, int ld, int d, int H
     const float2 cs = tab[row * half + j];
     const float s = sgn * cs.y;
     const float x1 = to_f(p[0]), x2 = to_f(p[half]);
-    p[0] = from_f<T>(x1 * cs.x - x2 * s);
-    p[half] = from_f<T>(x1 * s + x2 * cs.x);
+    const float y1 = x1 * cs.x - x2 * s, y2 = x1 * s + x2 * cs.x;
+    if constexpr (std::is_same<T, __half>::value) bad |= f16_bad(y1) | f16_bad(y2);
+    p[0] = from_f<T>(y1);
+    p[half] = from_f<T>(y2);
   }
+  if (bad) report_status(status, (int)TSP_ERR_RANGE);
 }
 
 tsp_status launch_rope(void* qkv, int ty, int64_t S, int ld, int d, int H, int Hkv, int dh,
@@ -644,9 +679,11 @@ tsp_status launch_rope(void* qkv, int ty, int64_t S, int ld, int d, int H, int H
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 8));
   const float sgn = inverse ? -1.f : 1.f;
   if (ty == TY_F16)
-    rope_kernel<__half><<<grid, 256, 0, st>>>((__half*)qkv, S, ld, d, H, Hkv, half, table, sgn);
+    rope_kernel<__half><<<grid, 256, 0, st>>>((__half*)qkv, S, ld, d, H, Hkv, half, table, sgn,
+                                              status_word());
   else if (ty == TY_F32)
-    rope_kernel<float><<<grid, 256, 0, st>>>((float*)qkv, S, ld, d, H, Hkv, half, table, sgn);
+    rope_kernel<float><<<grid, 256, 0, st>>>((float*)qkv, S, ld, d, H, Hkv, half, table, sgn,
+                                             status_word());
   else
     return TSP_ERR_UNSUPPORTED;
   TSP_CUDA_TRY(cudaGetLastError());

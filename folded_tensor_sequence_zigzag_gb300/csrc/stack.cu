@@ -6,9 +6,12 @@
 // every rank holds 1/D of the parameters and 1/D of the tokens of every
 // layer, and the fold is the only layout of the compared ones that cuts both
 // weight and activation memory by D without D^2 devices.  The stack here is
-// the plain composition y = B_{L-1}(... B_0(x)); each block is tsp_block_fwd /
-// tsp_block_bwd with its own weights, so every step still runs in the block's
-// kernels.
+// the plain composition y = B_{L-1}(... B_0(x)); each block is the block
+// forward / backward of tsp_block_fwd / tsp_block_bwd with its own weights, so
+// every step still runs in the block's kernels.  The residual stream between
+// layers stays in fp32, as it does inside a block (h): layer outputs and the
+// gradient handed down to the layer below are fp32; only x and y (cfg dtype)
+// and dx (fp32) are the stack's own input and outputs.
 #include <cstring>
 
 #include "common.cuh"
@@ -19,12 +22,16 @@ namespace {
 
 size_t up256(size_t b) { return (b + 255) & ~(size_t)255; }
 size_t elt_of(const tsp_cfg* c) { return c->dtype == TSP_BF16 ? 2 : 4; }
-size_t act_bytes(const tsp_cfg* c) { return up256((size_t)c->S * c->d * elt_of(c)); }
+// one layer's input or output between layers: the residual stream, kept in
+// fp32 across the whole stack as it is inside the block (only the stack's own
+// input x and output y are in the cfg dtype)
+size_t stream_bytes(const tsp_cfg* c) { return up256((size_t)c->S * c->d * 4); }
 bool al16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
 
 // per-layer slot of the training record: the layer's input, then the block's
-// saved activations
-size_t layer_slot(const tsp_cfg* c) { return act_bytes(c) + up256(tsp_saved_bytes(c)); }
+// saved activations.  Layer 0's input is the caller's x (cfg dtype); the
+// others are fp32.
+size_t layer_slot(const tsp_cfg* c) { return stream_bytes(c) + up256(tsp_saved_bytes(c)); }
 
 }  // namespace
 }  // namespace tsp
@@ -40,84 +47,121 @@ size_t tsp_stack_saved_bytes(const tsp_cfg* cfg, int32_t L) {
 
 size_t tsp_stack_workspace_bytes(const tsp_cfg* cfg, int32_t L, int32_t op) {
   if (L < 1) return 0;
+  const int base = op & ~TSP_OP_PREPARED;
+  if (base != TSP_OP_BLOCK_FWD && base != TSP_OP_BLOCK_BWD) return 0;
   const size_t w = tsp_workspace_bytes(cfg, op);
   if (w == 0) return 0;
-  if (op == TSP_OP_BLOCK_FWD) return up256(w) + 2 * act_bytes(cfg);   // + ping-pong layer outputs
-  if (op == TSP_OP_BLOCK_BWD)                                         // + fp32 dx, dy in cfg dtype
-    return up256(w) + up256((size_t)cfg->S * cfg->d * 4) + act_bytes(cfg);
-  return 0;
+  // + two fp32 stream buffers: ping-pong layer outputs (forward) or the
+  // gradient handed down between layers (backward)
+  return up256(w) + 2 * stream_bytes(cfg);
 }
 
-tsp_status tsp_stack_fwd(const tsp_cfg* cfg, int32_t L, const void* x_z, const tsp_attn_w* aw,
-                         const tsp_mlp_w* mw, void* y_z, void* saved, void* ws, size_t ws_bytes,
-                         void* stream) {
+}  // extern "C"
+
+namespace tsp {
+namespace {
+
+// prep: nullable host array of L prepared weight buffers
+tsp_status stack_fwd(const tsp_cfg* cfg, int32_t L, const void* x_z, const void* const* prep,
+                     const tsp_attn_w* aw, const tsp_mlp_w* mw, void* y_z, void* saved, void* ws,
+                     size_t ws_bytes, void* stream) {
   if (L < 1 || !aw || !mw || !al16(x_z) || !al16(y_z) || !al16(ws)) return TSP_ERR_INVALID_ARG;
-  const size_t need = tsp_stack_workspace_bytes(cfg, L, TSP_OP_BLOCK_FWD);
+  const int pf = prep ? TSP_OP_PREPARED : 0;
+  const size_t need = tsp_stack_workspace_bytes(cfg, L, TSP_OP_BLOCK_FWD | pf);
   if (need == 0 || ws_bytes < need) return TSP_ERR_INVALID_ARG;
   if (saved && !al16(saved)) return TSP_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const size_t blk_ws = up256(tsp_workspace_bytes(cfg, TSP_OP_BLOCK_FWD));
-  const size_t nbytes = (size_t)cfg->S * cfg->d * elt_of(cfg);
+  const size_t blk_ws = up256(tsp_workspace_bytes(cfg, TSP_OP_BLOCK_FWD | pf));
   uint8_t* w = (uint8_t*)ws;
   tsp_status r = TSP_OK;
   if (saved) {
     // training: layer l's input sits at the head of its slot, so the backward
     // has every layer's input; each layer writes the next layer's input slot
-    const size_t slot = layer_slot(cfg), ab = act_bytes(cfg);
+    const size_t slot = layer_slot(cfg), sb = stream_bytes(cfg);
+    const size_t xbytes = (size_t)cfg->S * cfg->d * elt_of(cfg);
     uint8_t* sv = (uint8_t*)saved;
-    if (cudaMemcpyAsync(sv, x_z, nbytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    if (cudaMemcpyAsync(sv, x_z, xbytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
       return TSP_ERR_CUDA;
     for (int l = 0; l < L && r == TSP_OK; ++l) {
       uint8_t* in = sv + (size_t)l * slot;
-      void* out = l == L - 1 ? y_z : (void*)(sv + (size_t)(l + 1) * slot);
-      r = tsp_block_fwd(cfg, in, &aw[l], &mw[l], out, in + ab, w, blk_ws, stream);
+      const bool last = l == L - 1;
+      void* out = last ? y_z : (void*)(sv + (size_t)(l + 1) * slot);
+      r = block_fwd_checked(cfg, in, l > 0, &aw[l], &mw[l], prep ? prep[l] : nullptr, out, !last,
+                            in + sb, w, blk_ws, st);
     }
     return r;
   }
-  uint8_t* buf[2] = {w + blk_ws, w + blk_ws + act_bytes(cfg)};
+  uint8_t* buf[2] = {w + blk_ws, w + blk_ws + stream_bytes(cfg)};
   for (int l = 0; l < L && r == TSP_OK; ++l) {
+    const bool last = l == L - 1;
     const void* in = l == 0 ? x_z : buf[(l - 1) & 1];
-    void* out = l == L - 1 ? y_z : buf[l & 1];
-    r = tsp_block_fwd(cfg, in, &aw[l], &mw[l], out, nullptr, w, blk_ws, stream);
+    void* out = last ? y_z : buf[l & 1];
+    r = block_fwd_checked(cfg, in, l > 0, &aw[l], &mw[l], prep ? prep[l] : nullptr, out, !last,
+                          nullptr, w, blk_ws, st);
   }
   return r;
+}
+
+tsp_status stack_bwd(const tsp_cfg* cfg, int32_t L, const void* dy_z, const void* saved,
+                     const void* const* prep, const tsp_attn_w* aw, const tsp_mlp_w* mw,
+                     float* dx_z, float* const* grads, void* ws, size_t ws_bytes, void* stream) {
+  if (L < 1 || !aw || !mw || !grads || !al16(dy_z) || !al16(saved) || !al16(dx_z) || !al16(ws))
+    return TSP_ERR_INVALID_ARG;
+  const int pf = prep ? TSP_OP_PREPARED : 0;
+  const size_t need = tsp_stack_workspace_bytes(cfg, L, TSP_OP_BLOCK_BWD | pf);
+  if (need == 0 || ws_bytes < need) return TSP_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t blk_ws = up256(tsp_workspace_bytes(cfg, TSP_OP_BLOCK_BWD | pf));
+  const size_t slot = layer_slot(cfg), sb = stream_bytes(cfg);
+  uint8_t* w = (uint8_t*)ws;
+  // the gradient of layer l's input is the upstream gradient of layer l - 1:
+  // fp32, ping-ponged between two buffers
+  float* gbuf[2] = {(float*)(w + blk_ws), (float*)(w + blk_ws + sb)};
+  const uint8_t* sv = (const uint8_t*)saved;
+  for (int l = L - 1; l >= 0; --l) {
+    const uint8_t* in = sv + (size_t)l * slot;
+    const bool top = l == L - 1;
+    const void* dy = top ? dy_z : (const void*)gbuf[(l + 1) & 1];
+    float* dx = l == 0 ? dx_z : gbuf[l & 1];
+    tsp_status r = block_bwd_checked(cfg, in, l > 0, dy, !top, in + sb, &aw[l], &mw[l],
+                                     prep ? prep[l] : nullptr, dx, grads + 9 * (size_t)l, w,
+                                     blk_ws, st);
+    if (r != TSP_OK) return r;
+  }
+  return TSP_OK;
+}
+
+}  // namespace
+}  // namespace tsp
+
+extern "C" {
+
+tsp_status tsp_stack_fwd(const tsp_cfg* cfg, int32_t L, const void* x_z, const tsp_attn_w* aw,
+                         const tsp_mlp_w* mw, void* y_z, void* saved, void* ws, size_t ws_bytes,
+                         void* stream) {
+  return stack_fwd(cfg, L, x_z, nullptr, aw, mw, y_z, saved, ws, ws_bytes, stream);
+}
+
+tsp_status tsp_stack_fwd_prepared(const tsp_cfg* cfg, int32_t L, const void* x_z,
+                                  const void* const* prep, const tsp_attn_w* aw,
+                                  const tsp_mlp_w* mw, void* y_z, void* saved, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  if (!prep) return TSP_ERR_INVALID_ARG;
+  return stack_fwd(cfg, L, x_z, prep, aw, mw, y_z, saved, ws, ws_bytes, stream);
 }
 
 tsp_status tsp_stack_bwd(const tsp_cfg* cfg, int32_t L, const void* dy_z, const void* saved,
                          const tsp_attn_w* aw, const tsp_mlp_w* mw, float* dx_z,
                          float* const* grads, void* ws, size_t ws_bytes, void* stream) {
-  if (L < 1 || !aw || !mw || !grads || !al16(dy_z) || !al16(saved) || !al16(dx_z) || !al16(ws))
-    return TSP_ERR_INVALID_ARG;
-  const size_t need = tsp_stack_workspace_bytes(cfg, L, TSP_OP_BLOCK_BWD);
-  if (need == 0 || ws_bytes < need) return TSP_ERR_INVALID_ARG;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const size_t blk_ws = up256(tsp_workspace_bytes(cfg, TSP_OP_BLOCK_BWD));
-  const size_t slot = layer_slot(cfg), ab = act_bytes(cfg);
-  const int64_t n = cfg->S * (int64_t)cfg->d;
-  uint8_t* w = (uint8_t*)ws;
-  float* dxbuf = (float*)(w + blk_ws);
-  uint8_t* dybuf = w + blk_ws + up256((size_t)n * 4);
-  const uint8_t* sv = (const uint8_t*)saved;
-  for (int l = L - 1; l >= 0; --l) {
-    const uint8_t* in = sv + (size_t)l * slot;
-    const void* dy = l == L - 1 ? dy_z : (const void*)dybuf;
-    float* dx = l == 0 ? dx_z : dxbuf;
-    float* const* G = grads + 9 * (size_t)l;
-    tsp_status r = tsp_block_bwd(cfg, in, dy, in + ab, &aw[l], &mw[l], dx, G[0], G[1], G[2], G[3],
-                                 G[4], G[5], G[6], G[7], G[8], w, blk_ws, stream);
-    if (r != TSP_OK) return r;
-    if (l > 0) {
-      // the gradient handed to the layer below is in the storage dtype, as
-      // the block's dy input is
-      if (cfg->dtype == TSP_BF16) {
-        if ((r = launch_convert_f32_bf16(dxbuf, dybuf, n, st)) != TSP_OK) return r;
-      } else if (cudaMemcpyAsync(dybuf, dxbuf, (size_t)n * 4, cudaMemcpyDeviceToDevice, st) !=
-                 cudaSuccess) {
-        return TSP_ERR_CUDA;
-      }
-    }
-  }
-  return TSP_OK;
+  return stack_bwd(cfg, L, dy_z, saved, nullptr, aw, mw, dx_z, grads, ws, ws_bytes, stream);
+}
+
+tsp_status tsp_stack_bwd_prepared(const tsp_cfg* cfg, int32_t L, const void* dy_z,
+                                  const void* saved, const void* const* prep,
+                                  const tsp_attn_w* aw, const tsp_mlp_w* mw, float* dx_z,
+                                  float* const* grads, void* ws, size_t ws_bytes, void* stream) {
+  if (!prep) return TSP_ERR_INVALID_ARG;
+  return stack_bwd(cfg, L, dy_z, saved, prep, aw, mw, dx_z, grads, ws, ws_bytes, stream);
 }
 
 tsp_status tsp_rank_memory(const tsp_cfg* cfg, int32_t L, int32_t training, int32_t scheme,
@@ -133,9 +177,10 @@ tsp_status tsp_rank_memory(const tsp_cfg* cfg, int32_t L, int32_t training, int3
   // weights of one layer: W_Q, W_O (d x d), W_K, W_V (dkv x d), W_1, W_3, W_2 and both gains
   const double W = ((2.0 * d * d + 2.0 * d * dkv + 3.0 * d * I) + 2.0 * d) * e;
   // activations one layer keeps per token for its backward: the block's
-  // saved buffer plus the layer input (inference: the largest single layer's
-  // forward workspace, which is all freed before the next layer)
-  const double A_tok = training ? ((double)saved + (double)act_bytes(cfg)) / S
+  // saved buffer plus the layer input, a slot of the fp32 residual stream
+  // (inference: the largest single layer's forward workspace, which is all
+  // freed before the next layer)
+  const double A_tok = training ? ((double)saved + (double)stream_bytes(cfg)) / S
                                 : (double)tsp_workspace_bytes(cfg, TSP_OP_BLOCK_FWD) / S;
   const double A = (training ? L : 1) * A_tok * S;   // whole sequence
   double w_share = 1.0, a_share = 1.0;

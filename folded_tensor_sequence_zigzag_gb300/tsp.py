@@ -15,9 +15,10 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libtsp.so")
 
-TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT = range(5)
+TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT, TSP_ERR_RANGE = range(6)
 TSP_F32, TSP_BF16 = 0, 1
 TSP_OP_ATTN_FWD, TSP_OP_MLP_FWD, TSP_OP_BLOCK_FWD, TSP_OP_BLOCK_BWD, TSP_OP_BLOCK_FWD_TRAIN = range(5)
+TSP_OP_PREPARED = 16
 
 EXPORTED = ("tsp_zigzag_permute", "tsp_rmsnorm_fwd", "tsp_workspace_bytes", "tsp_saved_bytes",
             "tsp_attn_block_fwd", "tsp_gated_mlp_fwd", "tsp_block_fwd", "tsp_block_bwd",
@@ -25,7 +26,10 @@ EXPORTED = ("tsp_zigzag_permute", "tsp_rmsnorm_fwd", "tsp_workspace_bytes", "tsp
             "tsp_profile_enable", "tsp_profile_report", "tsp_launch_count",
             "tsp_gated_mlp_fwd_noalloc", "tsp_stack_saved_bytes", "tsp_stack_workspace_bytes",
             "tsp_stack_fwd", "tsp_stack_bwd", "tsp_rank_memory", "tsp_kv_cache_bytes",
-            "tsp_decode_workspace_bytes", "tsp_block_prefill", "tsp_block_decode")
+            "tsp_decode_workspace_bytes", "tsp_block_prefill", "tsp_block_decode",
+            "tsp_debug_skip_stage", "tsp_block_weights_bytes", "tsp_block_weights_prepare",
+            "tsp_block_fwd_prepared", "tsp_block_bwd_prepared", "tsp_stack_fwd_prepared",
+            "tsp_stack_bwd_prepared")
 DECODE_MAX_T = 8   # TSP_DECODE_MAX_T
 
 
@@ -81,6 +85,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "tsp_profile_enable": (None, [i32]),
         "tsp_profile_report": (i32, [ctypes.c_char_p, i64]),
         "tsp_launch_count": (i64, []),
+        "tsp_debug_skip_stage": (None, [i32]),
+        "tsp_block_weights_bytes": (sz, [P(Cfg)]),
+        "tsp_block_weights_prepare": (i32, [P(Cfg), P(AttnW), P(MlpW), vp, vp]),
+        "tsp_block_fwd_prepared": (i32, [P(Cfg), vp, vp, P(AttnW), P(MlpW), vp, vp, vp, sz, vp]),
+        "tsp_block_bwd_prepared": (i32, [P(Cfg), vp, vp, vp, vp, P(AttnW), P(MlpW), vp] + [vp] * 9
+                                   + [vp, sz, vp]),
+        "tsp_stack_fwd_prepared": (i32, [P(Cfg), i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "tsp_stack_bwd_prepared": (i32, [P(Cfg), i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "tsp_gated_mlp_fwd_noalloc": (i32, [P(Cfg), vp, P(MlpW), vp, vp]),
         "tsp_stack_saved_bytes": (sz, [P(Cfg), i32]),
         "tsp_stack_workspace_bytes": (sz, [P(Cfg), i32, i32]),
@@ -185,15 +197,34 @@ def saved_bytes(cfg: Cfg) -> int:
     return int(load().tsp_saved_bytes(ctypes.byref(cfg)))
 
 
+# Poison mode (for tests): every buffer the binding allocates -- outputs,
+# gradients, workspaces, caches -- starts as all-ones bytes (NaN in fp32,
+# bf16 and fp16) instead of whatever the caching allocator hands back, so an
+# element the library fails to write cannot pass as a previous call's value.
+POISON = False
+
+
+def empty(shape, dtype, device) -> torch.Tensor:
+    """An uninitialised buffer, or a poisoned one while POISON is set."""
+    t = torch.empty(shape, dtype=dtype, device=device)
+    if POISON:
+        t.view(torch.uint8).fill_(0xFF)
+    return t
+
+
+def empty_like(t: torch.Tensor) -> torch.Tensor:
+    return empty(t.shape, t.dtype, t.device)
+
+
 def _ws(nbytes: int, device) -> torch.Tensor:
-    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    return empty(max(nbytes, 256), torch.uint8, device)
 
 
 def zigzag_permute(src: torch.Tensor, D: int, inverse: bool = False, out=None, stream=None):
     """Rows of src (global order) -> zigzag rank-major order (or back)."""
     _require_cuda(src)
     src = src.contiguous()
-    out = torch.empty_like(src) if out is None else out
+    out = empty_like(src) if out is None else out
     S = src.shape[0]
     row_bytes = src.numel() // max(S, 1) * src.element_size()
     _check(load().tsp_zigzag_permute(_ptr(src), _ptr(out), S, D, row_bytes, 1 if inverse else 0,
@@ -203,8 +234,8 @@ def zigzag_permute(src: torch.Tensor, D: int, inverse: bool = False, out=None, s
 
 def rmsnorm_fwd(u: torch.Tensor, g: torch.Tensor, eps: float = 1e-6, with_rstd=False, stream=None):
     _require_cuda(u, g)
-    out = torch.empty_like(u)
-    rstd = torch.empty(u.shape[0], dtype=torch.float32, device=u.device) if with_rstd else None
+    out = empty_like(u)
+    rstd = empty(u.shape[0], torch.float32, u.device) if with_rstd else None
     dt = TSP_BF16 if u.dtype == torch.bfloat16 else TSP_F32
     _check(load().tsp_rmsnorm_fwd(_ptr(u), _ptr(g), _ptr(out), _ptr(rstd), u.shape[0], u.shape[1],
                                   eps, dt, _stream(stream)), "tsp_rmsnorm_fwd")
@@ -213,7 +244,7 @@ def rmsnorm_fwd(u: torch.Tensor, g: torch.Tensor, eps: float = 1e-6, with_rstd=F
 
 def attn_block_fwd(cfg: Cfg, x_z, W: BlockWeights, out=None, ws=None, stream=None):
     _require_cuda(x_z)
-    out = torch.empty_like(x_z) if out is None else out
+    out = empty_like(x_z) if out is None else out
     nb = workspace_bytes(cfg, TSP_OP_ATTN_FWD)
     ws = _ws(nb, x_z.device) if ws is None else ws
     aw = W.attn()
@@ -225,7 +256,7 @@ def attn_block_fwd(cfg: Cfg, x_z, W: BlockWeights, out=None, ws=None, stream=Non
 def gated_mlp_fwd(cfg: Cfg, h_z, W: BlockWeights, norm=True, residual=True, out=None, ws=None,
                   stream=None):
     _require_cuda(h_z)
-    out = torch.empty_like(h_z) if out is None else out
+    out = empty_like(h_z) if out is None else out
     nb = workspace_bytes(cfg, TSP_OP_MLP_FWD)
     ws = _ws(nb, h_z.device) if ws is None else ws
     mw = W.mlp(norm, residual)
@@ -234,17 +265,44 @@ def gated_mlp_fwd(cfg: Cfg, h_z, W: BlockWeights, norm=True, residual=True, out=
     return out
 
 
-def block_fwd(cfg: Cfg, x_z, W: BlockWeights, saved=None, out=None, ws=None, stream=None):
-    """y_z = block(x_z).  Pass ``saved`` (uint8, saved_bytes(cfg)) to keep activations for bwd.
+def block_weights_bytes(cfg: Cfg) -> int:
+    return int(load().tsp_block_weights_bytes(ctypes.byref(cfg)))
 
-    The workspace always holds the fp16 operand copies of the weights; without
-    ``saved`` it also holds the activations."""
+
+def prepare_weights(cfg: Cfg, W: BlockWeights, out=None, stream=None):
+    """The block's fp16 operand copies, converted once (bf16 configurations;
+    None for fp32, which reads the weights as they are).  ``out``: a buffer of
+    block_weights_bytes(cfg) bytes to refill instead of a new one."""
+    nb = block_weights_bytes(cfg)
+    if nb == 0:
+        return None
+    prep = _ws(nb, W.wq.device) if out is None else out
+    aw, mw = W.attn(), W.mlp()
+    _check(load().tsp_block_weights_prepare(ctypes.byref(cfg), ctypes.byref(aw), ctypes.byref(mw),
+                                            _ptr(prep), _stream(stream)), "tsp_block_weights_prepare")
+    return prep
+
+
+def block_fwd(cfg: Cfg, x_z, W: BlockWeights, saved=None, out=None, ws=None, stream=None,
+              prep=None):
+    """y_z = block(x_z).  Pass ``saved`` (uint8, saved_bytes(cfg)) to keep activations for bwd,
+    ``prep`` (prepare_weights) to use weights converted once.
+
+    Without ``prep`` the workspace holds the fp16 operand copies of the weights;
+    without ``saved`` it also holds the activations."""
     _require_cuda(x_z)
-    out = torch.empty_like(x_z) if out is None else out
+    out = empty_like(x_z) if out is None else out
+    pf = TSP_OP_PREPARED if prep is not None else 0
     if ws is None:
         op = TSP_OP_BLOCK_FWD if saved is None else TSP_OP_BLOCK_FWD_TRAIN
-        ws = _ws(workspace_bytes(cfg, op), x_z.device)
+        ws = _ws(workspace_bytes(cfg, op | pf), x_z.device)
     aw, mw = W.attn(), W.mlp()
+    if prep is not None:
+        _check(load().tsp_block_fwd_prepared(ctypes.byref(cfg), _ptr(x_z), _ptr(prep),
+                                             ctypes.byref(aw), ctypes.byref(mw), _ptr(out),
+                                             _ptr(saved), _ptr(ws), ws.numel(), _stream(stream)),
+               "tsp_block_fwd_prepared")
+        return out
     _check(load().tsp_block_fwd(ctypes.byref(cfg), _ptr(x_z), ctypes.byref(aw), ctypes.byref(mw),
                                 _ptr(out), _ptr(saved), _ptr(ws), 0 if ws is None else ws.numel(),
                                 _stream(stream)), "tsp_block_fwd")
@@ -267,7 +325,7 @@ class KVCache:
         nb = kv_cache_bytes(cfg, rows_cap)
         if nb == 0:
             raise ValueError("invalid configuration or capacity for a KV cache")
-        self.buf = torch.empty(nb, dtype=torch.uint8, device=device)
+        self.buf = empty(nb, torch.uint8, device)
         self.rows_cap = int(rows_cap)
         self.n = 0          # rows filled
 
@@ -281,7 +339,7 @@ def block_prefill(cfg: Cfg, x_z, W: BlockWeights, cache: KVCache, out=None, ws=N
     """Inference forward over the S prompt tokens (zigzag order) that also
     fills cache rows [0, S) with their K and V."""
     _require_cuda(x_z)
-    out = torch.empty_like(x_z) if out is None else out
+    out = empty_like(x_z) if out is None else out
     if ws is None:
         ws = _ws(workspace_bytes(cfg, TSP_OP_BLOCK_FWD), x_z.device)
     aw, mw = W.attn(), W.mlp()
@@ -297,7 +355,7 @@ def block_decode(cfg: Cfg, x, W: BlockWeights, cache: KVCache, out=None, ws=None
     appends their K/V to the cache."""
     _require_cuda(x)
     T = x.shape[0]
-    out = torch.empty_like(x) if out is None else out
+    out = empty_like(x) if out is None else out
     if ws is None:
         ws = _ws(decode_workspace_bytes(cfg, T, cache.rows_cap), x.device)
     aw, mw = W.attn(), W.mlp()
@@ -311,15 +369,24 @@ def block_decode(cfg: Cfg, x, W: BlockWeights, cache: KVCache, out=None, ws=None
 GRAD_NAMES = ("dwq", "dwk", "dwv", "dwo", "dw1", "dw3", "dw2", "dg_attn", "dg_mlp")
 
 
-def block_bwd(cfg: Cfg, x_z, dy_z, saved, W: BlockWeights, ws=None, stream=None) -> dict:
+def block_bwd(cfg: Cfg, x_z, dy_z, saved, W: BlockWeights, ws=None, stream=None,
+              prep=None) -> dict:
     """Gradients of sum(dy * y), all fp32: dx_z (zigzag order) and the weight/gain grads."""
     _require_cuda(x_z, dy_z, saved)
     dev = x_z.device
     shapes = _grad_shapes(cfg)
-    g = {k: torch.empty(shapes[k], dtype=torch.float32, device=dev) for k in GRAD_NAMES}
-    g["dx"] = torch.empty(x_z.shape, dtype=torch.float32, device=dev)
-    ws = _ws(workspace_bytes(cfg, TSP_OP_BLOCK_BWD), dev) if ws is None else ws
+    g = {k: empty(shapes[k], torch.float32, dev) for k in GRAD_NAMES}
+    g["dx"] = empty(x_z.shape, torch.float32, dev)
+    pf = TSP_OP_PREPARED if prep is not None else 0
+    ws = _ws(workspace_bytes(cfg, TSP_OP_BLOCK_BWD | pf), dev) if ws is None else ws
     aw, mw = W.attn(), W.mlp()
+    if prep is not None:
+        _check(load().tsp_block_bwd_prepared(ctypes.byref(cfg), _ptr(x_z), _ptr(dy_z), _ptr(saved),
+                                             _ptr(prep), ctypes.byref(aw), ctypes.byref(mw),
+                                             _ptr(g["dx"]), *[_ptr(g[k]) for k in GRAD_NAMES],
+                                             _ptr(ws), ws.numel(), _stream(stream)),
+               "tsp_block_bwd_prepared")
+        return g
     _check(load().tsp_block_bwd(ctypes.byref(cfg), _ptr(x_z), _ptr(dy_z), _ptr(saved),
                                 ctypes.byref(aw), ctypes.byref(mw), _ptr(g["dx"]),
                                 *[_ptr(g[k]) for k in GRAD_NAMES], _ptr(ws), ws.numel(),
@@ -342,33 +409,50 @@ def _weight_arrays(Ws):
     return aws, mws
 
 
-def stack_fwd(cfg: Cfg, x_z, Ws, saved=None, out=None, ws=None, stream=None):
+def _prep_array(preps):
+    return (ctypes.c_void_p * len(preps))(*[p.data_ptr() for p in preps])
+
+
+def stack_fwd(cfg: Cfg, x_z, Ws, saved=None, out=None, ws=None, stream=None, preps=None):
     """y_z of the L-block stack with weights Ws[0..L-1].  ``saved`` (uint8,
-    stack_saved_bytes(cfg, L)) keeps every layer's input and activations."""
+    stack_saved_bytes(cfg, L)) keeps every layer's input and activations;
+    ``preps``: every layer's prepare_weights buffer (weights converted once)."""
     _require_cuda(x_z)
     L = len(Ws)
-    out = torch.empty_like(x_z) if out is None else out
+    out = empty_like(x_z) if out is None else out
+    pf = TSP_OP_PREPARED if preps is not None else 0
     if ws is None:
-        ws = _ws(stack_workspace_bytes(cfg, L, TSP_OP_BLOCK_FWD), x_z.device)
+        ws = _ws(stack_workspace_bytes(cfg, L, TSP_OP_BLOCK_FWD | pf), x_z.device)
     aws, mws = _weight_arrays(Ws)
+    if preps is not None:
+        _check(load().tsp_stack_fwd_prepared(ctypes.byref(cfg), L, _ptr(x_z), _prep_array(preps), aws,
+                                             mws, _ptr(out), _ptr(saved), _ptr(ws), ws.numel(),
+                                             _stream(stream)), "tsp_stack_fwd_prepared")
+        return out
     _check(load().tsp_stack_fwd(ctypes.byref(cfg), L, _ptr(x_z), aws, mws, _ptr(out), _ptr(saved),
                                 _ptr(ws), ws.numel(), _stream(stream)), "tsp_stack_fwd")
     return out
 
 
-def stack_bwd(cfg: Cfg, dy_z, saved, Ws, ws=None, stream=None):
+def stack_bwd(cfg: Cfg, dy_z, saved, Ws, ws=None, stream=None, preps=None):
     """Gradients of sum(dy * y) through the stack: (dx_z fp32, [grads of layer l])."""
     _require_cuda(dy_z, saved)
     dev = dy_z.device
     L = len(Ws)
     shapes = _grad_shapes(cfg)
-    grads = [{k: torch.empty(shapes[k], dtype=torch.float32, device=dev) for k in GRAD_NAMES}
+    grads = [{k: empty(shapes[k], torch.float32, dev) for k in GRAD_NAMES}
              for _ in range(L)]
     ptrs = (ctypes.c_void_p * (9 * L))(*[g[k].data_ptr() for g in grads for k in GRAD_NAMES])
-    dx = torch.empty(dy_z.shape, dtype=torch.float32, device=dev)
+    dx = empty(dy_z.shape, torch.float32, dev)
+    pf = TSP_OP_PREPARED if preps is not None else 0
     if ws is None:
-        ws = _ws(stack_workspace_bytes(cfg, L, TSP_OP_BLOCK_BWD), dev)
+        ws = _ws(stack_workspace_bytes(cfg, L, TSP_OP_BLOCK_BWD | pf), dev)
     aws, mws = _weight_arrays(Ws)
+    if preps is not None:
+        _check(load().tsp_stack_bwd_prepared(ctypes.byref(cfg), L, _ptr(dy_z), _ptr(saved),
+                                             _prep_array(preps), aws, mws, _ptr(dx), ptrs, _ptr(ws),
+                                             ws.numel(), _stream(stream)), "tsp_stack_bwd_prepared")
+        return dx, grads
     _check(load().tsp_stack_bwd(ctypes.byref(cfg), L, _ptr(dy_z), _ptr(saved), aws, mws, _ptr(dx),
                                 ptrs, _ptr(ws), ws.numel(), _stream(stream)), "tsp_stack_bwd")
     return dx, grads
@@ -383,7 +467,7 @@ def rank_memory(cfg: Cfg, L: int, training: bool, scheme: int) -> dict:
 
 
 def pack_attn_shards(cfg: Cfg, W: BlockWeights, stream=None):
-    out = torch.empty((4 * cfg.d, cfg.d), dtype=W.wq.dtype, device=W.wq.device)
+    out = empty((4 * cfg.d, cfg.d), W.wq.dtype, W.wq.device)
     aw = W.attn()
     _check(load().tsp_pack_attn_shards(ctypes.byref(cfg), ctypes.byref(aw), _ptr(out),
                                        _stream(stream)), "tsp_pack_attn_shards")
@@ -413,6 +497,12 @@ def profile_report() -> dict:
 
 def launch_count() -> int:
     return int(load().tsp_launch_count())
+
+
+def debug_skip_stage(n: int):
+    """Failure-detection knob: the next n GEMM launches each leave one pipeline
+    stage unfilled so a bounded wait runs out (TSP_ERR_TIMEOUT, no fault)."""
+    load().tsp_debug_skip_stage(int(n))
 
 
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024

@@ -46,8 +46,16 @@
  *  - Errors a host can detect (bad sizes, NULL or misaligned pointers, short
  *    workspace, shapes the bf16 kernels do not take) are returned at once and
  *    nothing is launched.  Launch failures return TSP_ERR_CUDA.  Errors the
- *    device detects (a pipeline wait that exceeded its time limit) set a
- *    sticky device status word read by tsp_device_status; kernels never trap.
+ *    device detects set a sticky device status word read by
+ *    tsp_device_status; kernels never trap.  They are: a pipeline wait that
+ *    exceeded its time limit (TSP_ERR_TIMEOUT), and, in the bf16
+ *    configuration, a value that the tensor-core path holds in fp16 -- the
+ *    weights, the normalised activations, Q/K/V, G, the SwiGLU
+ *    pre-activations, the upstream gradient and the backward's fp16
+ *    operands -- that is not finite or too large for fp16 (|v| >= 65520,
+ *    which fp16 rounds to infinity): TSP_ERR_RANGE.  The result of such a
+ *    call is not valid.  (Magnitudes below 6.1e-5 are kept as fp16
+ *    subnormals with fewer significant bits; that is not reported.)
  *    While the word holds an error, the tensor-core kernels return without
  *    doing their work, until tsp_device_status(stream, 1) clears it.
  *  - All pointers must be 16-byte aligned; row strides are dense.
@@ -67,7 +75,8 @@ typedef enum {
   TSP_ERR_INVALID_ARG = 1,   /* bad size, NULL or misaligned pointer, short buffer */
   TSP_ERR_UNSUPPORTED = 2,   /* valid shape that the selected kernels do not take */
   TSP_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed               */
-  TSP_ERR_TIMEOUT = 4        /* a device pipeline wait exceeded its time limit     */
+  TSP_ERR_TIMEOUT = 4,       /* a device pipeline wait exceeded its time limit     */
+  TSP_ERR_RANGE = 5          /* a value the bf16 path holds in fp16 was out of fp16 range */
 } tsp_status;
 
 typedef enum { TSP_F32 = 0, TSP_BF16 = 1 } tsp_dtype;
@@ -123,9 +132,12 @@ typedef struct {
 
 /* Workspace queries (op selects the entry point).  TSP_OP_BLOCK_FWD_TRAIN:
  * the block forward with a `saved` buffer (activations go there; the
- * workspace holds the weight copies and, with mlp_tile, one MLP tile). */
+ * workspace holds the weight copies and, with mlp_tile, one MLP tile).
+ * OR TSP_OP_PREPARED into TSP_OP_BLOCK_FWD, TSP_OP_BLOCK_BWD or
+ * TSP_OP_BLOCK_FWD_TRAIN for the _prepared entry points, whose workspace
+ * holds no weight copies (other ops with the flag: 0). */
 enum { TSP_OP_ATTN_FWD = 0, TSP_OP_MLP_FWD = 1, TSP_OP_BLOCK_FWD = 2, TSP_OP_BLOCK_BWD = 3,
-       TSP_OP_BLOCK_FWD_TRAIN = 4 };
+       TSP_OP_BLOCK_FWD_TRAIN = 4, TSP_OP_PREPARED = 16 };
 
 /* Zigzag causal partitioning (section 2, attention bullet: "zigzag
  * partitioning balances the causal attention work").  Bit-exact row copy.
@@ -222,6 +234,39 @@ tsp_status tsp_block_bwd(const tsp_cfg* cfg, const void* x_z, const void* dy_z,
                          float* dw1, float* dw3, float* dw2, float* dg_attn, float* dg_mlp,
                          void* ws, size_t ws_bytes, void* stream);
 
+/* ---- Weights converted once (not on the pages: an implementation choice) ----
+ * The bf16 path's tensor-core operands are fp16 (10-bit mantissa), so every
+ * whole-block call first converts the bf16 weight matrices it reads into fp16
+ * copies in its workspace (4 bytes of traffic per weight element, every
+ * call).  A caller whose weights stay the same across calls -- inference, or
+ * the forward and backward of one training step between two optimizer
+ * updates -- converts them once into a buffer it owns and passes that
+ * instead.
+ * tsp_block_weights_bytes: bytes of one block's fp16 copies (W_Q, W_K, W_V,
+ *   W_O, W_1, W_3, W_2, 256-byte aligned pieces); 0 for TSP_F32 (which reads
+ *   the weights as they are) or an invalid cfg.
+ * tsp_block_weights_prepare: writes them into prep (16-byte aligned, that
+ *   many bytes).  A weight that fp16 cannot hold sets TSP_ERR_RANGE in the
+ *   device status word.  The copies are valid until the caller changes the
+ *   weights; they are not tracked.  TSP_F32: nothing to do, TSP_OK.
+ * tsp_block_fwd_prepared / tsp_block_bwd_prepared: tsp_block_fwd /
+ *   tsp_block_bwd reading the weight matrices from prep (bf16: required; the
+ *   matrix pointers in aw, mw may then be NULL, the gains and add_residual
+ *   are still read from them; TSP_F32: prep is ignored).  Workspace:
+ *   tsp_workspace_bytes(cfg, op | TSP_OP_PREPARED). */
+size_t tsp_block_weights_bytes(const tsp_cfg* cfg);
+tsp_status tsp_block_weights_prepare(const tsp_cfg* cfg, const tsp_attn_w* aw, const tsp_mlp_w* mw,
+                                     void* prep, void* stream);
+tsp_status tsp_block_fwd_prepared(const tsp_cfg* cfg, const void* x_z, const void* prep,
+                                  const tsp_attn_w* aw, const tsp_mlp_w* mw, void* y_z, void* saved,
+                                  void* ws, size_t ws_bytes, void* stream);
+tsp_status tsp_block_bwd_prepared(const tsp_cfg* cfg, const void* x_z, const void* dy_z,
+                                  const void* saved, const void* prep, const tsp_attn_w* aw,
+                                  const tsp_mlp_w* mw, float* dx_z, float* dwq, float* dwk,
+                                  float* dwv, float* dwo, float* dw1, float* dw3, float* dw2,
+                                  float* dg_attn, float* dg_mlp, void* ws, size_t ws_bytes,
+                                  void* stream);
+
 /* ---- Inference: prefill, then decode against the zigzag KV cache ----
  * (section 2, attention bullet: each rank holds the K/V of its own zigzag
  * rows; the pages' title names inference, their schedules describe the
@@ -265,11 +310,16 @@ tsp_status tsp_block_decode(const tsp_cfg* cfg, const void* x, int32_t T, int64_
 
 /* ---- Stack of L blocks (the multi-layer model the fold is applied to) ----
  * y = B_{L-1}(... B_0(x)), B_l = the block above with weights aw[l], mw[l];
- * every layer runs tsp_block_fwd / tsp_block_bwd, so the kernels are the
- * block's.  aw, mw: host arrays of L weight sets (each as for tsp_block_fwd).
+ * every layer runs the block's forward / backward, so the kernels are the
+ * block's.  The residual stream between layers stays in fp32, as it does
+ * inside a block: each layer's output, and in the backward the gradient each
+ * layer hands to the one below, are fp32 (no rounding to the cfg dtype
+ * between layers).  aw, mw: host arrays of L weight sets (each as for
+ * tsp_block_fwd).
  *
- * tsp_stack_saved_bytes: training record of L layers (each layer's input
- *   plus its block's saved activations); 0 if cfg is invalid or L < 1.
+ * tsp_stack_saved_bytes: training record of L layers (each layer's input,
+ *   in an fp32-sized slot, plus its block's saved activations); 0 if cfg is
+ *   invalid or L < 1.
  * tsp_stack_workspace_bytes: op = TSP_OP_BLOCK_FWD (forward, with or without
  *   the training record) or TSP_OP_BLOCK_BWD; 0 if invalid.
  * tsp_stack_fwd: x_z, y_z [S, d] zigzag (cfg dtype); saved = NULL for
@@ -278,8 +328,7 @@ tsp_status tsp_block_decode(const tsp_cfg* cfg, const void* x, int32_t T, int64_
  *   (cfg dtype), saved as filled by tsp_stack_fwd, dx_z [S, d] fp32 out.
  *   grads: host array of 9*L fp32 device pointers, layer l at 9*l in the
  *   order dwq, dwk, dwv, dwo, dw1, dw3, dw2, dg_attn, dg_mlp (each sized as
- *   for tsp_block_bwd, overwritten).  The gradient between layers is passed
- *   in the cfg dtype (bf16 for bf16 configurations), as the block's dy is.
+ *   for tsp_block_bwd, overwritten).  The gradient between layers is fp32.
  * Errors: TSP_ERR_INVALID_ARG for L < 1, NULL or misaligned pointers or a
  *   short workspace; otherwise as for the block calls, stopping at the first
  *   failing layer. */
@@ -291,6 +340,18 @@ tsp_status tsp_stack_fwd(const tsp_cfg* cfg, int32_t L, const void* x_z, const t
 tsp_status tsp_stack_bwd(const tsp_cfg* cfg, int32_t L, const void* dy_z, const void* saved,
                          const tsp_attn_w* aw, const tsp_mlp_w* mw, float* dx_z,
                          float* const* grads, void* ws, size_t ws_bytes, void* stream);
+/* The same with every layer's weights converted once (see
+ * tsp_block_weights_prepare): prep is a host array of L device pointers,
+ * layer l's fp16 copies at prep[l].  Workspace: tsp_stack_workspace_bytes(cfg,
+ * L, op | TSP_OP_PREPARED). */
+tsp_status tsp_stack_fwd_prepared(const tsp_cfg* cfg, int32_t L, const void* x_z,
+                                  const void* const* prep, const tsp_attn_w* aw,
+                                  const tsp_mlp_w* mw, void* y_z, void* saved, void* ws,
+                                  size_t ws_bytes, void* stream);
+tsp_status tsp_stack_bwd_prepared(const tsp_cfg* cfg, int32_t L, const void* dy_z,
+                                  const void* saved, const void* const* prep,
+                                  const tsp_attn_w* aw, const tsp_mlp_w* mw, float* dx_z,
+                                  float* const* grads, void* ws, size_t ws_bytes, void* stream);
 
 /* ---- Per-rank memory account (sections 1-3: the fold cuts both weight and
  * activation memory per rank by D; TP cuts only weights, SP only
@@ -323,7 +384,7 @@ tsp_status tsp_pack_attn_shards(const tsp_cfg* cfg, const tsp_attn_w* w, void* d
 
 /* Reads (and with reset != 0 clears) the sticky device status word.  Waits
  * for `stream` to finish.  Returns TSP_OK or the first device error seen
- * (TSP_ERR_TIMEOUT). */
+ * (TSP_ERR_TIMEOUT or TSP_ERR_RANGE). */
 tsp_status tsp_device_status(void* stream, int32_t reset);
 
 /* Static string for a status code. */
@@ -344,6 +405,14 @@ int32_t tsp_num_sms(void);
 void tsp_profile_enable(int32_t on);
 int32_t tsp_profile_report(char* buf, int64_t bytes);
 int64_t tsp_launch_count(void);
+
+/* Failure-detection test knob (not on the pages): the next n tensor-core GEMM
+ * launches each leave one pipeline stage of their first CTA unfilled, so that
+ * CTA's bounded wait runs out (after TSP_WAIT_LIMIT_MS, an environment
+ * variable read once, default 4000) and the call reports TSP_ERR_TIMEOUT
+ * through tsp_device_status -- without a fault or a hang.  n <= 0 turns it
+ * off.  Never needed in normal use. */
+void tsp_debug_skip_stage(int32_t n);
 
 #ifdef __cplusplus
 }

@@ -51,14 +51,13 @@ design notes of the repository.
       decoded tokens are appended after the prompt in position order (they
       are not re-zigzagged).  A decode step's output is what the causal
       block forward over the whole sequence gives at the new positions.
-  R11 Stack of L layers: plain composition, each layer its own weights; a
-      stack whose activations live in bf16 hands each layer's output (and, in
-      the backward, each layer's input gradient) to the next layer rounded to
-      bf16.
+  R11 Stack of L layers: plain composition, each layer its own weights.  The
+      residual stream between layers is not rounded to the storage dtype (it
+      stays fp32 on the GPU, as inside one block), so in this float64 oracle
+      the stack is the exact composition of the blocks.
 
 Every floating-point step runs in numpy float64; inputs are converted
-exactly from their bf16/fp32 storage.  No step here rounds to bf16, except
-the stack's explicit bf16 storage between layers (R11, ``store="bf16"``).
+exactly from their bf16/fp32 storage.  No step here rounds to bf16.
 
 Parity pins: every function below is pinned by tests under tests/ against
 closed forms, invariants, brute force and an independent library
@@ -311,72 +310,125 @@ def block_fwd(x, W, H, eps):
 # ----------------------------------------------------------------------------
 
 
+def rank_project(x_r, pos_r, W, H, D, eps):
+    """Step 2 of the attention schedule for one rank's rows x_r (global
+    positions pos_r): a_r = rms(x_r; g_attn), then shard k = 0..D-1 of the
+    packed W_Q/W_K/W_V columns arrives and the rank projects its own rows
+    with it (K/V columns cut the same way over their own width, which is d
+    unless reading R13 applies); Q and K are rotated at the rows' global
+    positions when reading R12 applies.  Returns (Q_r, K_r, V_r)."""
+    x_r = f64(x_r)
+    wq, wk, wv = (_w(W, n) for n in ("wq", "wk", "wv"))
+    d, dkv = wq.shape[0], wk.shape[0]
+    Cb, Kb = shard_bounds(d, D), shard_bounds(dkv, D)
+    a_r = rmsnorm(x_r, _w(W, "g_attn"), eps)[0]
+    Q = np.zeros((x_r.shape[0], d)); K = np.zeros((x_r.shape[0], dkv)); V = np.zeros_like(K)
+    for k in range(D):
+        C, Ck = slice(Cb[k], Cb[k + 1]), slice(Kb[k], Kb[k + 1])
+        Q[:, C] = a_r @ wq[C].T
+        K[:, Ck] = a_r @ wk[Ck].T
+        V[:, Ck] = a_r @ wv[Ck].T
+    Q = rope(Q, pos_r, H, _rope_base(W))
+    K = rope(K, pos_r, _kv_heads(W, H), _rope_base(W))
+    return Q, K, V
+
+
+def rank_fwd(r, x_r, pos_r, Q_r, K_all, V_all, W, H, D, eps, c, parts=("attn", "mlp")):
+    """Steps 4-6 of the schedule for virtual rank r, given the gathered K/V.
+
+    x_r, pos_r: the rank's rows and their global positions; Q_r from
+    rank_project; K_all, V_all: the all-gathered keys and values of the whole
+    sequence, row p holding position p.  Attention of the rank's rows runs
+    chunk by chunk (chunk length c) against the keys at positions <= each
+    query's own; the rank accumulates O[:, C_k] W_O[:, C_k]^T shard by shard
+    onto its residual rows; then the MLP ring hands it shard (r - t) mod D of
+    W_1/W_3 (rows) and W_2 (columns) at step t and it accumulates
+    G[:, I_k] W_2[:, I_k]^T onto its rows.  ``parts`` selects the halves.
+    Returns y_r (h_r if only the attention half runs)."""
+    x_r = f64(x_r)
+    pos_r = np.asarray(pos_r)
+    h_r = x_r.copy()
+    if "attn" in parts:
+        wo = _w(W, "wo")
+        Cb = shard_bounds(wo.shape[0], D)
+        O_r = np.zeros_like(Q_r)
+        kpos = np.arange(K_all.shape[0])
+        for ch in np.unique(pos_r // c):        # each chunk's rows have ascending positions
+            sel = np.nonzero(pos_r // c == ch)[0]
+            O_r[sel], _ = causal_attention(Q_r[sel], K_all, V_all, H, q_pos=pos_r[sel], k_pos=kpos)
+        for k in range(D):
+            C = slice(Cb[k], Cb[k + 1])
+            h_r += O_r[:, C] @ wo[:, C].T
+    y_r = h_r.copy()
+    if "mlp" in parts:
+        w1, w3, w2 = (_w(W, n) for n in ("w1", "w3", "w2"))
+        Ib = shard_bounds(w1.shape[0], D)
+        b_r = rmsnorm(h_r, _w(W, "g_mlp"), eps)[0]
+        for t in range(D):
+            k = (r - t) % D
+            I = slice(Ib[k], Ib[k + 1])
+            G = silu(b_r @ w1[I].T) * (b_r @ w3[I].T)
+            y_r += G @ w2[:, I].T
+    return y_r
+
+
+def gather_kv(x, W, H, D, eps):
+    """The K/V all-gather: every rank projects its own zigzag rows
+    (rank_project) and the rows are placed at their global positions.
+    Returns (K_all, V_all) in position order."""
+    x = f64(x)
+    S = x.shape[0]
+    c = S // (2 * D)
+    pos = zigzag_positions(S, D)
+    dkv = W["wk"].shape[0]
+    K_all = np.zeros((S, dkv)); V_all = np.zeros((S, dkv))
+    for r in range(D):
+        R = pos[r * 2 * c:(r + 1) * 2 * c]
+        _, K_all[R], V_all[R] = rank_project(x[R], R, W, H, D, eps)
+    return K_all, V_all
+
+
 def block_fwd_sharded(x, W, H, D, eps, parts=("attn", "mlp")):
     """The TSP schedule, one virtual rank at a time, in float64.
 
-    1. zigzag-partition the tokens (reading R5);
-    2. attention broadcast loop: shard k = 0..D-1 of the packed W_Q/W_K/W_V
-       columns C_k arrives (K/V columns cut the same way over their own
-       width, which is d unless reading R13 applies); every rank projects its
-       own rows with it;
-    3. "all-gather" of K/V: concatenate every rank's K/V rows with their
-       global positions;
-    4. causal attention of rank r's rows against the gathered K/V;
-    5. W_O: each rank accumulates O[:, C_k] W_O[:, C_k]^T shard by shard onto
-       its residual rows;
-    6. MLP ring: at step t rank r holds shard I_k, k = (r - t) mod D, of
-       W_1/W_3 (rows) and W_2 (columns) and accumulates the partial
-       G[:, I_k] W_2[:, I_k]^T onto its rows;
+    1. zigzag-partition the tokens (reading R5): rank r holds chunks r and
+       2D-1-r;
+    2. attention broadcast loop: every rank projects its own rows with each
+       arriving shard (rank_project);
+    3. "all-gather" of K/V: every rank's K/V rows placed at their global
+       positions (gather_kv);
+    4.-6. per rank: causal attention of its rows against the gathered K/V,
+       the W_O shard loop onto its residual rows, the MLP ring (rank_fwd);
     7. un-permute.
     ``parts`` selects which half runs (both by default); the MLP half keeps
     its norm and residual.
     """
     x = f64(x)
-    S, d = x.shape
+    S = x.shape[0]
     c = S // (2 * D)
     pos = zigzag_positions(S, D)
-    xz = x[pos]
-    rows = [slice(r * 2 * c, (r + 1) * 2 * c) for r in range(D)]
-    Cb = shard_bounds(d, D)
-    hz = xz.copy()
+    K_all = V_all = None
     if "attn" in parts:
-        g1 = _w(W, "g_attn")
-        wq, wk, wv, wo = (_w(W, n) for n in ("wq", "wk", "wv", "wo"))
-        dkv = wk.shape[0]
-        Kb = shard_bounds(dkv, D)
-        Qz = np.zeros((S, d)); Kz = np.zeros((S, dkv)); Vz = np.zeros((S, dkv))
-        az = np.zeros((S, d))
-        for r in range(D):
-            az[rows[r]] = rmsnorm(xz[rows[r]], g1, eps)[0]
-        for k in range(D):                      # shard k is broadcast ...
-            C = slice(Cb[k], Cb[k + 1])
-            Ck = slice(Kb[k], Kb[k + 1])
-            for r in range(D):                  # ... and every rank projects
-                Qz[rows[r], C] = az[rows[r]] @ wq[C].T
-                Kz[rows[r], Ck] = az[rows[r]] @ wk[Ck].T
-                Vz[rows[r], Ck] = az[rows[r]] @ wv[Ck].T
-        Qz = rope(Qz, pos, H, _rope_base(W))        # whole heads, global positions
-        Kz = rope(Kz, pos, _kv_heads(W, H), _rope_base(W))
-        for r in range(D):
-            O_r, _ = causal_attention(Qz[rows[r]], Kz, Vz, H, q_pos=pos[rows[r]], k_pos=pos)
-            for k in range(D):
-                C = slice(Cb[k], Cb[k + 1])
-                hz[rows[r]] += O_r[:, C] @ wo[:, C].T
-    yz = hz.copy()
-    if "mlp" in parts:
-        g2 = _w(W, "g_mlp")
-        w1, w3, w2 = (_w(W, n) for n in ("w1", "w3", "w2"))
-        Ib = shard_bounds(w1.shape[0], D)
-        for r in range(D):
-            b_r = rmsnorm(hz[rows[r]], g2, eps)[0]
-            for t in range(D):
-                k = (r - t) % D
-                I = slice(Ib[k], Ib[k + 1])
-                G = silu(b_r @ w1[I].T) * (b_r @ w3[I].T)
-                yz[rows[r]] += G @ w2[:, I].T
-    out = np.empty_like(yz)
-    out[pos] = yz
+        K_all, V_all = gather_kv(x, W, H, D, eps)
+    out = np.empty_like(x)
+    for r in range(D):
+        R = pos[r * 2 * c:(r + 1) * 2 * c]
+        Q_r = rank_project(x[R], R, W, H, D, eps)[0] if "attn" in parts else None
+        out[R] = rank_fwd(r, x[R], R, Q_r, K_all, V_all, W, H, D, eps, c, parts)
     return out
+
+
+def mirrored_rows(S, D, r, n):
+    """n mirrored row pairs of virtual rank r, as global positions: the first
+    n rows of chunk r and the last n rows of chunk 2D-1-r.  Row i of chunk r
+    (position r*c + i) attends r*c + i + 1 keys and its mirror (position
+    (2D-r)*c - 1 - i) attends (2D-r)*c - i, so every pair attends S + 1 keys:
+    a set of mirrored pairs carries exactly the block's average work per
+    token (the balance the zigzag layout is built for)."""
+    c = S // (2 * D)
+    lo = r * c + np.arange(n)
+    hi = (2 * D - 1 - r) * c + c - n + np.arange(n)
+    return np.concatenate([lo, hi])
 
 
 def mlp_fwd_sharded(h, W, D, eps, norm=True, residual=True):
@@ -522,47 +574,29 @@ def causal_attention_bwd(Q, K, V, O, dO, H, q_pos=None, k_pos=None, row_block=51
     return dQ, dK, dV
 
 
-def _store(v, store):
-    """A value the way the stack stores it between layers: unchanged (None)
-    or rounded to bfloat16 ("bf16", the storage dtype of the bf16 API)."""
-    if store is None:
-        return v
-    if store == "bf16":
-        return torch.from_numpy(np.ascontiguousarray(v)).to(torch.bfloat16).to(torch.float64).numpy()
-    raise ValueError(store)
-
-
-def stack_fwd(x, Ws, H, eps, store=None):
+def stack_fwd(x, Ws, H, eps):
     """y of an L-layer stack: the blocks applied in order, each with its own
     weights Ws[l] ([TSP] sections 1-3: the fold is applied to every layer of
-    the model; the stack is plain composition).  ``store="bf16"`` rounds each
-    layer's output to bfloat16 before the next layer reads it, as a stack
-    whose activations are stored in bf16 does (reading R11)."""
+    the model; the stack is plain composition, reading R11)."""
     y = f64(x)
-    for l, W in enumerate(Ws):
+    for W in Ws:
         y, _ = block_fwd(y, W, H, eps)
-        if l + 1 < len(Ws):
-            y = _store(y, store)
     return y
 
 
-def stack_bwd(x, Ws, dy, H, eps, store=None):
+def stack_bwd(x, Ws, dy, H, eps):
     """dx and per-layer gradients of L = sum(dy * y), y = stack_fwd(x): the
     chain rule through the layers, the dx of layer l being the dy of layer
-    l - 1 (rounded to bfloat16 with ``store="bf16"``, like the forward's
-    layer outputs).  Returns (dx, [dict of layer l's weight and gain
-    gradients])."""
+    l - 1.  Returns (dx, [dict of layer l's weight and gain gradients])."""
     xs = [f64(x)]
     for W in Ws[:-1]:
-        xs.append(_store(block_fwd(xs[-1], W, H, eps)[0], store))
+        xs.append(block_fwd(xs[-1], W, H, eps)[0])
     g = f64(dy)
     grads = [None] * len(Ws)
     for l in range(len(Ws) - 1, -1, -1):
         gl = block_bwd(xs[l], Ws[l], g, H, eps)
         g = gl.pop("dx")
         grads[l] = gl
-        if l > 0:
-            g = _store(g, store)
     return g, grads
 
 

@@ -38,9 +38,10 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_strerror(lib):
-    for code in range(5):
-        assert lib.tsp_strerror(code)
+    for code in range(6):
+        assert lib.tsp_strerror(code) and lib.tsp_strerror(code) != b"unknown status"
     assert b"invalid" in lib.tsp_strerror(tsp.TSP_ERR_INVALID_ARG)
+    assert b"fp16" in lib.tsp_strerror(tsp.TSP_ERR_RANGE)
 
 
 def _cfg(**kw):
@@ -185,3 +186,26 @@ def test_mlp_tiling_configuration(lib):
     mw = tsp.MlpW(ok, ok, ok, ok, 1)
     assert lib.tsp_block_fwd(ctypes.byref(f32), ok, ctypes.byref(aw), ctypes.byref(mw), ok, ok, ok,
                              1 << 40, None) == tsp.TSP_ERR_UNSUPPORTED
+
+
+def test_prepared_weights_sizes(lib):
+    """Prepared fp16 copies: one block's seven matrices in fp16; the whole-block
+    workspaces shrink by exactly that; fp32 has nothing to prepare; the
+    prepared calls reject a missing buffer on the host."""
+    d, I = 4096, 11008
+    cfg = _cfg(S=16384, d=d, H=32, inter=I, D=8, dtype=tsp.TSP_BF16)
+    nb = lib.tsp_block_weights_bytes(ctypes.byref(cfg))
+    assert 2 * (4 * d * d + 3 * d * I) <= nb < 2 * (4 * d * d + 3 * d * I) + 7 * 256
+    for op in (tsp.TSP_OP_BLOCK_FWD, tsp.TSP_OP_BLOCK_BWD):
+        full = lib.tsp_workspace_bytes(ctypes.byref(cfg), op)
+        assert lib.tsp_workspace_bytes(ctypes.byref(cfg), op | tsp.TSP_OP_PREPARED) == full - nb
+    assert lib.tsp_workspace_bytes(ctypes.byref(cfg), tsp.TSP_OP_MLP_FWD | tsp.TSP_OP_PREPARED) == 0
+    L = 4
+    assert (lib.tsp_stack_workspace_bytes(ctypes.byref(cfg), L, tsp.TSP_OP_BLOCK_FWD)
+            - lib.tsp_stack_workspace_bytes(ctypes.byref(cfg), L,
+                                             tsp.TSP_OP_BLOCK_FWD | tsp.TSP_OP_PREPARED)) == nb
+    assert lib.tsp_block_weights_bytes(ctypes.byref(_cfg())) == 0      # fp32
+    assert lib.tsp_block_fwd_prepared(ctypes.byref(cfg), None, None, None, None, None, None, None,
+                                      0, None) == tsp.TSP_ERR_INVALID_ARG
+    assert lib.tsp_stack_fwd_prepared(ctypes.byref(cfg), 2, None, None, None, None, None, None,
+                                      None, 0, None) == tsp.TSP_ERR_INVALID_ARG

@@ -1,6 +1,6 @@
 """Failure detection on the GPU without a fault: a pipeline wait that can never
 be satisfied (one stage of one CTA is deliberately left unfilled, through the
-TSP_DEBUG_SKIP_STAGE knob) must run out after TSP_WAIT_LIMIT_MS, be reported as
+tsp_debug_skip_stage knob) must run out after TSP_WAIT_LIMIT_MS, be reported as
 TSP_ERR_TIMEOUT by tsp_device_status, and leave the context usable: after the
 status is cleared the same call gives the correct result again.  Runs in a
 child process so the short wait limit applies to nothing else."""
@@ -30,12 +30,11 @@ cfg = tsp.make_cfg(512, 256, 2, 384, 4, torch.bfloat16)
 h = tsp.zigzag_permute(inp["x"].cuda(), 4)
 good = tsp.gated_mlp_fwd(cfg, h, W, norm=False, residual=False)
 assert tsp.device_status(reset=True) == tsp.TSP_OK
-os.environ["TSP_DEBUG_SKIP_STAGE"] = "1"
+tsp.debug_skip_stage(1)
 t0 = time.time()
 tsp.gated_mlp_fwd(cfg, h, W, norm=False, residual=False)
 st = tsp.device_status(reset=True)
 dt = time.time() - t0
-del os.environ["TSP_DEBUG_SKIP_STAGE"]
 assert st == tsp.TSP_ERR_TIMEOUT, st
 assert dt < 30, dt
 again = tsp.gated_mlp_fwd(cfg, h, W, norm=False, residual=False)
@@ -49,7 +48,6 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     if not torch.cuda.is_available():
         pytest.fail("CUDA device required for -m gpu tests")
     env = dict(os.environ, TSP_WAIT_LIMIT_MS="300", TSP_ROOT=ROOT)
-    env.pop("TSP_DEBUG_SKIP_STAGE", None)
     out = subprocess.run([sys.executable, "-c", CHILD], capture_output=True, text=True,
                          timeout=300, env=env, cwd=ROOT)
     assert out.returncode == 0, out.stdout + out.stderr

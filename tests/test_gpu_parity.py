@@ -214,7 +214,7 @@ def _run_bwd(shape, inp, dtype, rope_base=0.0, mlp_tile=0):
     W = tsp.BlockWeights.from_dict(inp, dev)
     xz = tsp.zigzag_permute(inp["x"].to(dev), shape.D)
     dyz = tsp.zigzag_permute(inp["dy"].to(dev), shape.D)
-    saved = torch.empty(tsp.saved_bytes(cfg), dtype=torch.uint8, device=dev)
+    saved = tsp.empty(tsp.saved_bytes(cfg), torch.uint8, dev)
     yz = tsp.block_fwd(cfg, xz, W, saved=saved)
     g = tsp.block_bwd(cfg, xz, dyz, saved, W)
     g["dx"] = tsp.zigzag_permute(g["dx"], shape.D, inverse=True)

@@ -7,25 +7,8 @@ import torch
 import oracle.tsp_oracle as O
 from folded_tensor_sequence_zigzag_gb300 import tsp
 from folded_tensor_sequence_zigzag_gb300.inputs import BlockShape, TINY_FP32, make_block_inputs
-from tests.helpers import BF16_MAX_REL_RMS, BF16_MEAN_REL, assert_f32_close, bf16_metrics, to64
+from tests.helpers import assert_bf16_close, assert_f32_close
 
-
-def assert_stack_bf16_close(got, ref, boundaries, what=""):
-    """The block's bf16 bounds, with the max-error bound widened by one bf16
-    ulp of the largest reference value per stored layer boundary: a value
-    within rounding distance of a bf16 tie can round to different neighbours
-    on the GPU (fp32 before rounding) and in the oracle (fp64), and the
-    residual path carries that one-ulp step to the output.  The mean relative
-    bound is unchanged."""
-    ref64 = to64(ref)
-    rms = float(np.sqrt(np.mean(ref64 ** 2)))
-    top = float(np.max(np.abs(ref64)))
-    ulp = 2.0 ** (np.floor(np.log2(top)) - 7) if top > 0 else 0.0
-    mx, mean = bf16_metrics(got, ref)
-    bound = BF16_MAX_REL_RMS + boundaries * ulp / rms
-    assert np.all(np.isfinite(to64(got))), f"{what}: non-finite output"
-    assert mx <= bound and mean <= BF16_MEAN_REL, \
-        f"{what}: max|err|/RMS={mx:.3e} (<= {bound:.3e}), mean rel={mean:.3e} (<= {BF16_MEAN_REL})"
 
 pytestmark = pytest.mark.gpu
 
@@ -59,7 +42,7 @@ def _run_stack(shape, dtype, x, dy, layers, training, rope_base=0.0, mlp_tile=0)
     L = len(layers)
     saved = None
     if training:
-        saved = torch.empty(tsp.stack_saved_bytes(cfg, L), dtype=torch.uint8, device=dev)
+        saved = tsp.empty(tsp.stack_saved_bytes(cfg, L), torch.uint8, dev)
     yz = tsp.stack_fwd(cfg, xz, Ws, saved=saved)
     y = tsp.zigzag_permute(yz, shape.D, inverse=True)
     out = {"y": y}
@@ -96,17 +79,19 @@ def test_bf16_stack_matches_oracle(training):
     shape = BlockShape(S=2048, d=256, H=2, inter=512, D=4)
     x, dy, layers = _stack_inputs(shape, torch.bfloat16, L, seed=9)
     got = _run_stack(shape, torch.bfloat16, x, dy, layers, training)
-    # the stack stores activations (and the gradient between layers) in bf16
-    yref = O.stack_fwd(x, layers, shape.H, shape.eps, store="bf16")
-    assert_stack_bf16_close(got["y"].float().cpu(), yref, L - 1, "bf16 stack y")
+    # the residual stream between layers stays fp32, so the stack is held to
+    # the block's own bf16 bounds (2e-2 * RMS max, 5e-3 mean relative)
+    yref = O.stack_fwd(x, layers, shape.H, shape.eps)
+    report = [("y",) + assert_bf16_close(got["y"].float().cpu(), yref, "bf16 stack y")]
     if training:
-        dx_ref, g_ref = O.stack_bwd(x, layers, dy, shape.H, shape.eps, store="bf16")
-        # dx crosses the L-1 forward boundaries and the L-1 gradient boundaries
-        assert_stack_bf16_close(got["dx"].cpu(), dx_ref, 2 * (L - 1), "bf16 stack dx")
+        dx_ref, g_ref = O.stack_bwd(x, layers, dy, shape.H, shape.eps)
+        report.append(("dx",) + assert_bf16_close(got["dx"].cpu(), dx_ref, "bf16 stack dx"))
         for l in range(L):
             for k, v in g_ref[l].items():
-                assert_stack_bf16_close(got["grads"][l][k].cpu(), v, 2 * (L - 1),
-                                        f"bf16 stack layer {l} {k}")
+                report.append((f"{l}.{k}",) + assert_bf16_close(got["grads"][l][k].cpu(), v,
+                                                                 f"bf16 stack layer {l} {k}"))
+    for name, mx, mean in report:
+        print(f"bf16 stack {name}: max|err|/RMS {mx:.3e}  mean rel {mean:.3e}")
 
 
 def test_bf16_stack_with_every_variant_matches_oracle():
@@ -117,15 +102,14 @@ def test_bf16_stack_with_every_variant_matches_oracle():
     x, dy, layers = _stack_inputs(shape, torch.bfloat16, L, seed=21)
     got = _run_stack(shape, torch.bfloat16, x, dy, layers, True, rope_base=base, mlp_tile=256)
     ref_layers = [dict(w, rope_base=base) for w in layers]
-    yref = O.stack_fwd(x, ref_layers, shape.H, shape.eps, store="bf16")
-    assert_stack_bf16_close(got["y"].float().cpu(), yref, L - 1, "variant stack y")
-    dx_ref, g_ref = O.stack_bwd(x, ref_layers, dy, shape.H, shape.eps, store="bf16")
-    assert_stack_bf16_close(got["dx"].cpu(), dx_ref, 2 * (L - 1), "variant stack dx")
+    yref = O.stack_fwd(x, ref_layers, shape.H, shape.eps)
+    assert_bf16_close(got["y"].float().cpu(), yref, "variant stack y")
+    dx_ref, g_ref = O.stack_bwd(x, ref_layers, dy, shape.H, shape.eps)
+    assert_bf16_close(got["dx"].cpu(), dx_ref, "variant stack dx")
     for l in range(L):
         for k, v in g_ref[l].items():
             assert got["grads"][l][k].shape == v.shape, (l, k)
-            assert_stack_bf16_close(got["grads"][l][k].cpu(), v, 2 * (L - 1),
-                                    f"variant stack layer {l} {k}")
+            assert_bf16_close(got["grads"][l][k].cpu(), v, f"variant stack layer {l} {k}")
 
 
 def test_stack_rejects_bad_arguments():

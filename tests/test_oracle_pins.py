@@ -445,25 +445,25 @@ def test_stack_backward_central_finite_differences():
             assert abs(fd - an) <= 1e-6 * max(abs(an), 1e-8), (l, gname, fd, an)
 
 
-def test_stack_bf16_storage_rounds_only_between_layers():
-    """With bf16 storage a one-layer stack is still the block exactly, and an
-    identity layer after a block returns exactly the block's output rounded
-    to bf16 (the rounding happens at the layer boundary and nowhere else)."""
+def test_two_layer_stack_backward_is_the_composition_of_block_backwards():
+    """The gradient handed from layer 1 to layer 0 is layer 1's dx, unrounded:
+    a two-layer stack's dx and every gradient equal two block backwards
+    chained by hand, and layer 1 sees layer 0's exact output as its input."""
     shape, inp = _small(S=24, d=16, H=2, inter=24, D=3, seed=46)
-    ident = dict(inp)
-    ident["wo"] = torch.zeros_like(inp["wo"])
-    ident["w2"] = torch.zeros_like(inp["w2"])
-    yb, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
-    y1 = O.stack_fwd(inp["x"], [inp], shape.H, shape.eps, store="bf16")
-    assert np.array_equal(y1, yb)
-    y2 = O.stack_fwd(inp["x"], [inp, ident], shape.H, shape.eps, store="bf16")
-    rounded = torch.from_numpy(yb).to(torch.bfloat16).to(torch.float64).numpy()
-    assert np.array_equal(y2, rounded)
-    assert not np.array_equal(y2, yb)
-    # backward: the gradient handed down is rounded, the top layer's is not
-    dx1, _ = O.stack_bwd(inp["x"], [inp], inp["dy"], shape.H, shape.eps, store="bf16")
-    g = O.block_bwd(inp["x"], inp, inp["dy"], shape.H, shape.eps)
-    assert np.array_equal(dx1, g["dx"])
+    W0 = inp
+    W1 = _layers(shape, [47])[0]
+    x, dy = inp["x"], inp["dy"]
+    dx, grads = O.stack_bwd(x, [W0, W1], dy, shape.H, shape.eps)
+    y0, _ = O.block_fwd(x, W0, shape.H, shape.eps)
+    g1 = O.block_bwd(y0, W1, dy, shape.H, shape.eps)
+    g0 = O.block_bwd(x, W0, g1["dx"], shape.H, shape.eps)
+    assert np.array_equal(dx, g0["dx"])
+    for k in grads[0]:
+        assert np.array_equal(grads[0][k], g0[k]), k
+        assert np.array_equal(grads[1][k], g1[k]), k
+    # and the forward: layer 1 reads layer 0's output as it is
+    y = O.stack_fwd(x, [W0, W1], shape.H, shape.eps)
+    assert np.array_equal(y, O.block_fwd(y0, W1, shape.H, shape.eps)[0])
 
 
 # ------------------------------------------------------------------ rotary embedding (variant)
@@ -682,3 +682,46 @@ def test_decode_steps_match_torch_full_forward(Hkv, base):
     got = np.concatenate(outs, axis=0)
     assert got.shape == (6, 32)
     assert np.max(np.abs(got - y[S:])) < 1e-11
+
+
+# ------------------------------------------------------------------ per-rank steps of the schedule
+
+def test_mirrored_row_pairs_each_attend_S_plus_1_keys():
+    """Closed form: position p attends p + 1 keys; a mirrored pair of virtual
+    rank r attends S + 1 keys in all, and n = c pairs are exactly rank r's
+    zigzag rows."""
+    for S, D in ((48, 3), (256, 4), (16384, 8)):
+        c = S // (2 * D)
+        for r in range(D):
+            n = min(c, 5)
+            p = O.mirrored_rows(S, D, r, n)
+            keys = p + 1
+            assert np.all(keys[:n] + keys[n:][::-1] == S + 1)
+            full = O.mirrored_rows(S, D, r, c)
+            zz = O.zigzag_positions(S, D)[r * 2 * c:(r + 1) * 2 * c]
+            assert np.array_equal(np.sort(full), np.sort(zz))
+
+
+def test_gather_kv_is_the_unsharded_projection():
+    shape, inp = _small(S=48, d=24, H=3, inter=40, D=3, seed=61)
+    K_all, V_all = O.gather_kv(inp["x"], inp, shape.H, shape.D, shape.eps)
+    _, s = O.attn_block_fwd(inp["x"], inp, shape.H, shape.eps)
+    assert np.max(np.abs(K_all - s["K"])) <= 1e-12 * np.max(np.abs(s["K"]))
+    assert np.max(np.abs(V_all - s["V"])) <= 1e-12 * np.max(np.abs(s["V"]))
+
+
+@pytest.mark.parametrize("D,n", [(3, 2), (4, 8), (2, 1)])
+def test_rank_step_on_mirrored_rows_is_the_block_at_those_rows(D, n):
+    """One virtual rank's step on a subset of its rows (its own Q/K/V
+    projection, attention against the gathered K/V, the W_O loop and the MLP
+    ring) gives the unsharded block's output at exactly those positions."""
+    shape, inp = _small(S=2 * D * 8, d=16, H=2, inter=24, D=D, seed=62 + D)
+    S, c = shape.S, shape.S // (2 * D)
+    yb, _ = O.block_fwd(inp["x"], inp, shape.H, shape.eps)
+    K_all, V_all = O.gather_kv(inp["x"], inp, shape.H, D, shape.eps)
+    x = O.f64(inp["x"])
+    for r in range(D):
+        p = O.mirrored_rows(S, D, r, n)
+        Q_r, _, _ = O.rank_project(x[p], p, inp, shape.H, D, shape.eps)
+        y_r = O.rank_fwd(r, x[p], p, Q_r, K_all, V_all, inp, shape.H, D, shape.eps, c)
+        assert np.max(np.abs(y_r - yb[p])) <= 1e-12 * np.max(np.abs(yb)), r
