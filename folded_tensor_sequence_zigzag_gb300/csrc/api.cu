@@ -658,6 +658,8 @@ tsp_status block_bwd_impl(const tsp_cfg* c, const void* x, bool x_f32, const voi
                           float* dg_attn, float* dg_mlp, void* ws, cudaStream_t st);
 
 
+tsp_status cfg_status(const tsp_cfg* cfg) { return check_cfg(cfg); }
+
 tsp_status block_fwd_checked(const tsp_cfg* cfg, const void* x_z, bool x_f32, const tsp_attn_w* aw,
                              const tsp_mlp_w* mw, const void* prep, void* y_z, bool y_f32,
                              void* saved, void* ws, size_t ws_bytes, cudaStream_t st) {

@@ -76,11 +76,18 @@ constexpr uint32_t TMEM_COLS = 512;              // S_A | S_B | O_A | O_B
 constexpr float RESCALE_LOG2 = 8.0f;             // lazy-rescale threshold (log2 units)
 
 struct TcAttnArgs {
-  CUtensorMap tm;       // Q|K|V buffer [S rows, d + 2*Hkv*dh cols] fp16, box {64, 128}, 128B swizzle
-  ct_t* o;              // [S, d]
-  float* lse;           // [H, S]
-  int64_t S, c;
+  // K/V: rows in zigzag order over all S positions, K of K/V head g at columns
+  // kv_col0 + g*dh, V at kv_col0 + dkv + g*dh (fp16, box {64, 128}, 128B swizzle)
+  CUtensorMap tm;
+  // Q: query head h at columns q_col0 + h*dh of the rows of zigzag row
+  // index - q_row_off (the whole Q|K|V buffer, or one rank's own rows)
+  CUtensorMap tm_q;
+  ct_t* o;              // O row (zigzag row index - o_row_off), row stride ldo
+  float* lse;           // [H][lse_ld] at (zigzag row index - o_row_off)
+  int64_t S, c, q_row_off, o_row_off, ldo, lse_ld;
   int D, d, n_blocks;   // n_blocks = c / 256
+  int rank0;            // virtual rank of blockIdx.x / n_blocks == 0
+  int q_col0, kv_col0;
   int G, dkv;           // query heads per K/V head; K/V width Hkv*dh
   float scale_log2;
   int* status;
@@ -122,9 +129,10 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
-  const int kcol = a.d + (h / a.G) * DH;   // K columns of this head's K/V head; V at + dkv
+  const int kcol = a.kv_col0 + (h / a.G) * DH;   // K columns of this head's K/V head; V at + dkv
   const int pair = blockIdx.x;
-  const int r = pair / a.n_blocks, t = pair - r * a.n_blocks;
+  const int rl = pair / a.n_blocks, t = pair - rl * a.n_blocks;
+  const int r = a.rank0 + rl;
   const int64_t p0_mirror =
       (int64_t)(2 * a.D - 1 - r) * a.c + (int64_t)(a.n_blocks - 1 - t) * BLOCK;
   const int64_t p0_own = (int64_t)r * a.c + (int64_t)t * BLOCK;
@@ -149,7 +157,10 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == WARP_PROD && lane == 0) tma_prefetch_desc(&a.tm);
+  if (warp == WARP_PROD && lane == 0) {
+    tma_prefetch_desc(&a.tm);
+    tma_prefetch_desc(&a.tm_q);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -178,9 +189,10 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
           mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
-            tma_load_2d(base + OFF_Q + x * TILE_BYTES, &a.tm, h * DH, (int)(qrow0 + x * BQ), q_full);
-            tma_load_2d(base + OFF_Q + x * TILE_BYTES + BOX_BYTES, &a.tm, h * DH + 64,
-                        (int)(qrow0 + x * BQ), q_full);
+            const int qr = (int)(qrow0 - a.q_row_off + x * BQ);
+            tma_load_2d(base + OFF_Q + x * TILE_BYTES, &a.tm_q, a.q_col0 + h * DH, qr, q_full);
+            tma_load_2d(base + OFF_Q + x * TILE_BYTES + BOX_BYTES, &a.tm_q, a.q_col0 + h * DH + 64,
+                        qr, q_full);
           }
           ++q_issued;
           bool ok = true;
@@ -331,20 +343,24 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
               for (int e = 0; e < 32; ++e)
                 if (q * 32 + e > row) sr[q][e] = __float_as_uint(-INFINITY);
           }
-          // row max over 16 independent partial maxima (short dependency chains)
+          // row max over 16 independent partial maxima (short dependency
+          // chains), three scores an instruction: 72 max instructions a row
+          // instead of 127
+          auto S_ = [&](int i) { return __uint_as_float(sr[i >> 5][i & 31]); };
           float mp[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            mp[k] = fmaxf(__uint_as_float(sr[0][k]), __uint_as_float(sr[0][k + 16]));
+          for (int k = 0; k < 16; ++k) mp[k] = fmax3f(S_(k), S_(k + 16), S_(k + 32));
 #pragma unroll
-          for (int q = 1; q < 4; ++q)
+          for (int k = 0; k < 16; ++k) {   // scores 48 + k + 16 i, i = 0..4
+            mp[k] = fmax3f(mp[k], S_(48 + k), S_(64 + k));
+            mp[k] = fmax3f(mp[k], S_(80 + k), S_(96 + k));
+            mp[k] = fmaxf(mp[k], S_(112 + k));
+          }
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mp[e & 15] = fmaxf(mp[e & 15], __uint_as_float(sr[q][e]));
-#pragma unroll
-          for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-            for (int k = 0; k < w; ++k) mp[k] = fmaxf(mp[k], mp[k + w]);
-          const float mx = mp[0] * a.scale_log2;
+          for (int k = 0; k < 5; ++k) mp[k] = fmax3f(mp[k], mp[k + 5], mp[k + 10]);
+          mp[0] = fmax3f(mp[0], mp[1], mp[15]);
+          mp[2] = fmax3f(mp[2], mp[3], mp[4]);
+          const float mx = fmaxf(mp[0], mp[2]) * a.scale_log2;
           const bool mine = mx > m_used + RESCALE_LOG2;
           const bool resc = __any_sync(0xffffffffu, mine);
           float alpha = 1.f;
@@ -411,8 +427,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
         if (__all_sync(0xffffffffu, eok)) {
           tc_fence_after();
           const float inv = 1.f / l;
-          const int64_t orow_i = qrow0 + x * BQ + row;
-          ct_t* orow = a.o + orow_i * (int64_t)a.d + h * DH;
+          const int64_t orow_i = qrow0 - a.o_row_off + x * BQ + row;
+          ct_t* orow = a.o + orow_i * a.ldo + h * DH;
 #pragma unroll 1
           for (int q = 0; q < 4; ++q) {
             uint32_t ov[32];
@@ -428,7 +444,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
                   pack_f16(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv));
           }
           constexpr float LN2 = 0.69314718055994530942f;
-          a.lse[(int64_t)h * a.S + orow_i] = (m_used + __log2f(l)) * LN2;
+          a.lse[(int64_t)h * a.lse_ld + orow_i] = (m_used + __log2f(l)) * LN2;
         }
         tc_fence_before();
           }
@@ -466,38 +482,31 @@ EncodeTiledFn encode_fn_attn() {
 
 }  // namespace
 
-tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, int H, int Hkv,
-                               int dh, int D, cudaStream_t st) {
-  if (dh != DH) return TSP_ERR_UNSUPPORTED;
-  const int64_t c = S / (2 * D);
-  if (c % BLOCK != 0) return TSP_ERR_UNSUPPORTED;
-  if (S > (int64_t)INT32_MAX) return TSP_ERR_UNSUPPORTED;
-  if (Hkv < 1 || H % Hkv != 0) return TSP_ERR_INVALID_ARG;
-  const int d = H * dh, dkv = Hkv * dh;
-  const int64_t ld = d + 2 * (int64_t)dkv;
-  if (((uintptr_t)qkv & 15u) || ((ld * 2) % 16)) return TSP_ERR_INVALID_ARG;
-  TcAttnArgs* a = new TcAttnArgs();
-  std::unique_ptr<TcAttnArgs> guard(a);
-  memset(a, 0, sizeof(TcAttnArgs));
+namespace {
+
+// fp16 [rows, cols] row-major, box {64 columns, 128 rows}, 128-byte swizzle
+bool attn_map(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows) {
   EncodeTiledFn fn = encode_fn_attn();
-  if (!fn) return TSP_ERR_CUDA;
-  const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)S};
-  const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
   const cuuint32_t box[2] = {64u, 128u};
   const cuuint32_t estr[2] = {1u, 1u};
-  if (fn(&a->tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(qkv), dims, strides, box,
-         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return TSP_ERR_CUDA;
-  a->o = (ct_t*)o;
-  a->lse = lse;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// a: maps, pointers and offsets filled in; the common fields, checks and launch
+tsp_status attn_launch(TcAttnArgs* a, int64_t S, int H, int Hkv, int dh, int D, int nranks,
+                       cudaStream_t st) {
   a->S = S;
-  a->c = c;
+  a->c = S / (2 * D);
   a->D = D;
-  a->d = d;
+  a->d = H * dh;
   a->G = H / Hkv;
-  a->dkv = dkv;
-  a->n_blocks = (int)(c / BLOCK);
+  a->dkv = Hkv * dh;
+  a->n_blocks = (int)(a->c / BLOCK);
   a->scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
   a->status = status_word();
   a->limit_ns = wait_limit_ns();
@@ -514,11 +523,61 @@ tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, 
   }
   // setmaxnreg.inc would wait forever if the split exceeded the launch allocation
   if ((int64_t)launch_regs * NTHR < (int64_t)REG_TOTAL) return TSP_ERR_UNSUPPORTED;
-  dim3 grid((unsigned)(D * a->n_blocks), (unsigned)H);
+  dim3 grid((unsigned)(nranks * a->n_blocks), (unsigned)H);
   Prof prof("attn_fwd", st);
   attn_fwd_tc_kernel<<<grid, NTHR, SMEM, st>>>(*a);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
+}
+
+}  // namespace
+
+tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, int H, int Hkv,
+                               int dh, int D, cudaStream_t st) {
+  if (dh != DH) return TSP_ERR_UNSUPPORTED;
+  const int64_t c = S / (2 * D);
+  if (c % BLOCK != 0) return TSP_ERR_UNSUPPORTED;
+  if (S > (int64_t)INT32_MAX) return TSP_ERR_UNSUPPORTED;
+  if (Hkv < 1 || H % Hkv != 0) return TSP_ERR_INVALID_ARG;
+  const int d = H * dh, dkv = Hkv * dh;
+  const int64_t ld = d + 2 * (int64_t)dkv;
+  if (((uintptr_t)qkv & 15u) || ((ld * 2) % 16)) return TSP_ERR_INVALID_ARG;
+  TcAttnArgs* a = new TcAttnArgs();
+  std::unique_ptr<TcAttnArgs> guard(a);
+  memset(a, 0, sizeof(TcAttnArgs));
+  // Q, K and V all in the one Q|K|V buffer: Q at column 0, K at d, V at d + dkv
+  if (!attn_map(&a->tm, qkv, ld, S)) return TSP_ERR_CUDA;
+  a->tm_q = a->tm;
+  a->kv_col0 = d;
+  a->o = (ct_t*)o;
+  a->ldo = d;
+  a->lse = lse;
+  a->lse_ld = S;
+  return attn_launch(a, S, H, Hkv, dh, D, D, st);
+}
+
+tsp_status launch_attn_fwd_rank_f16(const void* q, int64_t ldq, const void* kv, int64_t ldkv,
+                                    void* o, int64_t ldo, float* lse, int64_t S, int H, int dh,
+                                    int D, int r, cudaStream_t st) {
+  if (dh != DH) return TSP_ERR_UNSUPPORTED;
+  const int64_t c = S / (2 * D);
+  if (c % BLOCK != 0 || S > (int64_t)INT32_MAX) return TSP_ERR_UNSUPPORTED;
+  if (r < 0 || r >= D || H < 1) return TSP_ERR_INVALID_ARG;
+  if (((uintptr_t)q & 15u) || ((uintptr_t)kv & 15u) || ((ldq * 2) % 16) || ((ldkv * 2) % 16) ||
+      ldq < (int64_t)H * dh || ldkv < 2 * (int64_t)H * dh)
+    return TSP_ERR_INVALID_ARG;
+  TcAttnArgs* a = new TcAttnArgs();
+  std::unique_ptr<TcAttnArgs> guard(a);
+  memset(a, 0, sizeof(TcAttnArgs));
+  // the rank's own 2c rows of Q; the gathered K|V of all S rows (K at 0, V at H*dh)
+  if (!attn_map(&a->tm_q, q, ldq, 2 * c) || !attn_map(&a->tm, kv, ldkv, S)) return TSP_ERR_CUDA;
+  a->q_row_off = a->o_row_off = (int64_t)r * 2 * c;
+  a->rank0 = r;
+  a->o = (ct_t*)o;
+  a->ldo = ldo;
+  a->lse = lse;
+  a->lse_ld = 2 * c;
+  return attn_launch(a, S, H, H, dh, D, 1, st);
 }
 
 }  // namespace tsp

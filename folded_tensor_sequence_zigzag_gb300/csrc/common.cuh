@@ -79,6 +79,13 @@ __device__ __forceinline__ void report_status(int* status, int code) {
   atomicCAS(status, 0, code);
 }
 
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later)
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // fp16 range of the internal tensor-core operands: a value becomes a finite
 // fp16 only if |v| < 65520 (the largest fp16, 65504, plus half its spacing);
 // anything else -- NaN included -- turns into inf or NaN.  Kernels that store

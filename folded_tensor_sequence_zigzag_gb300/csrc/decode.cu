@@ -13,14 +13,15 @@
 //    Q and K plus the append of K|V to the cache).  A warp streams groups of
 //    NR output rows, walking K with 16-byte non-allocating loads (four in
 //    flight per row); x sits in shared memory.
-//  * decode_attn_kernel: work item = (K/V head, split of 128 cache rows).
+//  * decode_attn_kernel: one CTA per (K/V head, split of 128 cache rows).
 //    The splits never straddle a virtual rank's 2c zigzag rows, so each
 //    rank's partial attention over the K/V it owns is formed where that K/V
 //    lives (the decode counterpart of the prefill's K/V all-gather); the
 //    decoded tokens' own rows, appended after the prompt, form the last
-//    splits.  One persistent CTA per SM walks its items while cp.async
-//    stages the next items' K|V rows in shared memory, and an item serves
-//    all G*T query rows of its K/V head group (every cache row is read once).
+//    splits.  A lane owns a key: its K row goes straight to registers (read
+//    16 bytes a lane, coalesced) while the warp's V rows are staged in its
+//    shared-memory slice by cp.async; the query rows of a K/V head group are
+//    split over a few CTAs when the heads and splits alone give too few.
 //  * decode_combine_kernel: merges the splits' (max, sum, unnormalised O) by
 //    their log-sum-exp into O [T, d].
 #include <cuda_bf16.h>
@@ -338,6 +339,7 @@ struct AttnArgs {
   float2* part_ml;
   int64_t S, c, n_cached, n_total;
   int D, spr, nsplit, T, H, G, dkv;   // spr: splits per rank
+  int nz, qpc;   // query-row groups per (K/V head, split); query rows per group
   float scale_log2;
 };
 
@@ -360,6 +362,14 @@ __device__ __forceinline__ void split_rows(const AttnArgs& a, int s, int64_t& r0
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_nc16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
 }
 
 // V elements one lane holds for one key: VPL of type CT
@@ -391,230 +401,189 @@ template <> struct VReg<float, 1> {
   __device__ void get(float (&v)[1]) const { v[0] = r; }
 };
 
-// Shared-memory stage of one work item: the K and V rows of one K/V head
-// over one split, [kSplitRows][K (DH) | V (DH)], each row padded by 16 bytes
-// so that lanes reading the same 16-byte piece of different rows fall in
-// different banks.
+// CTA = (K/V head g, split s of <= 128 cache rows, query group z); warp w
+// takes rows r0 + 32w .. r0 + 32w + 31.  Every lane issues its K pieces and
+// its V columns of the warp's 32 keys before any arithmetic, so a warp has
+// 16 KB of loads in flight, all coalesced: a K row is read by LPR lanes
+// (16 bytes each) and its dot products reduced across them; a V row by the
+// whole warp.  No shared-memory staging of K/V; the warps' partial softmax
+// results are merged in shared memory.
 template <typename CT, int DH>
-struct Stage {
-  static constexpr int ROW = 2 * DH * (int)sizeof(CT) + 16;   // bytes per staged row
-  static constexpr int BYTES = kSplitRows * ROW;
-  static constexpr int CPR = 2 * DH * (int)sizeof(CT) / 16;   // 16-byte pieces per row
-  // as many stages as fit next to the static buffers: 3 for the fp16 128-wide heads
-  static constexpr int N = (3 * BYTES <= 200 * 1024) ? 3 : 2;
-};
-
-// Persistent CTA, one per SM: work item = (K/V head g, split s of <= 128
-// cache rows), items strided over the grid.  While the CTA computes item i
-// from its shared-memory stage, the K|V rows of the next Stage::N - 1 items
-// are already on their way by cp.async, so every SM keeps a steady stream of
-// loads in flight instead of loading, computing and exiting per split.  An
-// item serves all G*T query rows of its K/V head group, so each cache row is
-// read from memory once.  Per item: warp w takes rows 32w .. 32w+31; a K row
-// is read by LPR lanes (16 bytes each) and its dot products reduced across
-// them; V rows are read by the whole warp (lane = V columns); the warps'
-// partial softmax results are merged in shared memory.
-template <typename CT, int DH>
-__global__ void __launch_bounds__(kAttnWarps * 32, 1) decode_attn_kernel(const __grid_constant__ AttnArgs a) {
-  using St = Stage<CT, DH>;
+__global__ void __launch_bounds__(kAttnWarps * 32, 4) decode_attn_kernel(const __grid_constant__ AttnArgs a) {
   constexpr int E = 16 / sizeof(CT);          // elements per 16-byte piece
   constexpr int LPR = DH / E;                 // lanes per K row (a piece each)
   constexpr int RPI = 32 / LPR;               // K rows per warp-wide load
   constexpr int KIT = LPR;                    // loads covering the warp's 32 rows
   constexpr int VPL = DH >= 32 ? DH / 32 : 1; // V columns per lane
   constexpr int VLANES = DH / VPL;            // lanes holding V columns
-  constexpr int NST = St::N;
-  extern __shared__ __align__(16) uint8_t stage_raw[];
   __shared__ __align__(16) float qs[kQB][DH];
   __shared__ __align__(16) float pw[kAttnWarps][kQB][32];
   __shared__ __align__(16) float ro[kAttnWarps][kQB][DH];
+  __shared__ __align__(16) CT vs[kAttnWarps][32][DH];   // each warp's V rows (cp.async)
   __shared__ float2 rml[kAttnWarps][kQB];
 
+  // the nz CTAs of one (K/V head, split) are neighbours in x: they run
+  // together and share the K/V rows through L2
+  const int g = blockIdx.x / a.nz, z = blockIdx.x - g * a.nz, s = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Hkv = a.H / a.G;
-  const int n_items = Hkv * a.nsplit;
-  const int kl = lane % LPR, kh = lane / LPR;   // piece and row of this lane in a K load
+  int64_t r0, r1;
+  split_rows(a, s, r0, r1);
+  const int64_t wr0 = r0 + warp * 32;
+  const bool wactive = wr0 < r1;
+  const int64_t kr = wr0 + lane;              // this lane's key row
+  const bool kin = kr < r1;
+  const CT* base = reinterpret_cast<const CT*>(a.kv) + (int64_t)g * DH;
 
-  // item -> (K/V head, split); the head varies fastest, so the CTAs running
-  // together read neighbouring heads of the same cache rows
-  auto issue = [&](int item, int st) {
-    const int g = item % Hkv, s = item / Hkv;
-    int64_t r0, r1;
-    split_rows(a, s, r0, r1);
-    const CT* kvb = reinterpret_cast<const CT*>(a.kv);
-    const uint32_t dst0 = smem_u32(stage_raw) + (uint32_t)(st * St::BYTES);
-    for (int i = threadIdx.x; i < kSplitRows * St::CPR; i += kAttnWarps * 32) {
-      const int row = i / St::CPR, pc = i - row * St::CPR;
-      const bool in = r0 + row < r1;
-      // pieces [0, CPR/2): K of head g; [CPR/2, CPR): V of head g
-      const int half = pc >= St::CPR / 2;
-      const int64_t col = (half ? a.dkv : 0) + (int64_t)g * DH + (int64_t)(pc - half * (St::CPR / 2)) * E;
-      cp_async16(dst0 + (uint32_t)(row * St::ROW + pc * 16),
-                 kvb + (in ? r0 + row : r0) * a.ldkv + col, in ? 16u : 0u);
+  const int kl = lane % LPR, kh = lane / LPR;   // piece and row of this lane in a K load
+  uint4 kreg[KIT];
+  if (wactive) {
+#pragma unroll
+    for (int it = 0; it < KIT; ++it) {
+      const int64_t row = wr0 + it * RPI + kh;
+      kreg[it] = ld_nc16(base + (row < r1 ? row : r0) * a.ldkv + kl * E);
     }
-  };
-  for (int p = 0; p < NST - 1; ++p) {
-    const int item = blockIdx.x + p * gridDim.x;
-    if (item < n_items) issue(item, p);
+    // V rows -> this warp's shared-memory slice without holding registers;
+    // rows past the split read as zeros (their p is 0)
+    for (int i = lane; i < 32 * LPR; i += 32) {
+      const int k = i / LPR, pc = i - k * LPR;
+      const bool in = wr0 + k < r1;
+      cp_async16(smem_u32(&vs[warp][k][pc * E]), base + (in ? wr0 + k : r0) * a.ldkv + a.dkv + pc * E,
+                 in ? 16u : 0u);
+    }
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
+  bool v_ready = false;
 
-  for (int it = 0;; ++it) {
-    const int item = blockIdx.x + it * gridDim.x;
-    if (item >= n_items) break;
-    {
-      const int pre = item + (NST - 1) * gridDim.x;
-      if (pre < n_items) issue(pre, (it + NST - 1) % NST);
-      asm volatile("cp.async.commit_group;" ::: "memory");
-    }
-    // this thread's copies of `item` are done; the barrier makes everyone's visible
-    asm volatile("cp.async.wait_group %0;" ::"n"(NST - 1) : "memory");
-    __syncthreads();
-
-    const int g = item % Hkv, s = item / Hkv;
-    int64_t r0, r1;
-    split_rows(a, s, r0, r1);
-    const uint8_t* stg = stage_raw + (it % NST) * St::BYTES;
-    const int64_t wr0 = r0 + warp * 32;
-    const bool wactive = wr0 < r1;
-    const int64_t kr = wr0 + lane;              // this lane's key row
-    const bool kin = kr < r1;
-
-    uint4 kreg[KIT];
-    if (wactive) {
-#pragma unroll
-      for (int i = 0; i < KIT; ++i)
-        kreg[i] = *reinterpret_cast<const uint4*>(stg + (warp * 32 + i * RPI + kh) * St::ROW + kl * 16);
-    }
-
-    // query rows of this K/V head: qr = (head g*G + gi, token t), gi = qr / T
-    const int QR = a.G * a.T;
-    for (int qb = 0; qb < QR; qb += kQB) {
-      const int nq = min(kQB, QR - qb);
-      for (int idx = threadIdx.x; idx < kQB * DH; idx += kAttnWarps * 32) {
-        const int i = idx / DH, j = idx - i * DH;
-        float v = 0.f;
-        if (i < nq) {
-          const int qr = qb + i, gi = qr / a.T, t = qr - gi * a.T;
-          v = to_f(reinterpret_cast<const CT*>(a.q)[(int64_t)t * a.ldq + (g * a.G + gi) * DH + j]);
-        }
-        qs[i][j] = v;
+  // query rows of this K/V head: qr = (head g*G + gi, token t), gi = qr / T;
+  // this CTA takes rows [z*qpc, min(QR, (z+1)*qpc))
+  const int QR = min(a.G * a.T, (z + 1) * a.qpc);
+  for (int qb = z * a.qpc; qb < QR; qb += kQB) {
+    const int nq = min(kQB, QR - qb);
+    for (int idx = threadIdx.x; idx < kQB * DH; idx += kAttnWarps * 32) {
+      const int i = idx / DH, j = idx - i * DH;
+      float v = 0.f;
+      if (i < nq) {
+        const int qr = qb + i, gi = qr / a.T, t = qr - gi * a.T;
+        v = to_f(reinterpret_cast<const CT*>(a.q)[(int64_t)t * a.ldq + (g * a.G + gi) * DH + j]);
       }
-      __syncthreads();
-      if (wactive) {
-        // sc[i] = q_i . K[row wr0 + lane]: per load, partial dot products over
-        // each row's LPR lanes, reduced, then handed to the lane that owns the row
-        float sc[kQB];
+      qs[i][j] = v;
+    }
+    __syncthreads();
+    if (wactive) {
+      // sc[i] = q_i . K[row wr0 + lane]: per load, partial dot products over
+      // each row's LPR lanes, reduced, then handed to the lane that owns the row
+      float sc[kQB];
 #pragma unroll
-        for (int i = 0; i < kQB; ++i) sc[i] = 0.f;
+      for (int i = 0; i < kQB; ++i) sc[i] = 0.f;
 #pragma unroll
-        for (int i = 0; i < kQB; ++i) {
-          if (i < nq) {
-            float qv[E];
+      for (int i = 0; i < kQB; ++i) {
+        if (i < nq) {
+          float qv[E];
 #pragma unroll
-            for (int e = 0; e < E; ++e) qv[e] = qs[i][kl * E + e];
+          for (int e = 0; e < E; ++e) qv[e] = qs[i][kl * E + e];
 #pragma unroll
-            for (int k = 0; k < KIT; ++k) {
-              float kf[E];
-              if constexpr (sizeof(CT) == 2) {
-                XVec<__half>::cvt(kreg[k], *reinterpret_cast<float(*)[8]>(kf));
-              } else {
-                XVec<float>::cvt(kreg[k], *reinterpret_cast<float(*)[4]>(kf));
-              }
-              float part = 0.f;
-#pragma unroll
-              for (int e = 0; e < E; ++e) part = fmaf(qv[e], kf[e], part);
-#pragma unroll
-              for (int off = LPR / 2; off >= 1; off >>= 1)
-                part += __shfl_xor_sync(0xffffffffu, part, off);
-              // row k*RPI + h sits in lanes h*LPR ..; lane j owns row j
-              const float v = __shfl_sync(0xffffffffu, part, (lane % RPI) * LPR);
-              if (lane / RPI == k) sc[i] = v;
+          for (int it = 0; it < KIT; ++it) {
+            float kf[E];
+            if constexpr (sizeof(CT) == 2) {
+              XVec<__half>::cvt(kreg[it], *reinterpret_cast<float(*)[8]>(kf));
+            } else {
+              XVec<float>::cvt(kreg[it], *reinterpret_cast<float(*)[4]>(kf));
             }
+            float part = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) part = fmaf(qv[e], kf[e], part);
+#pragma unroll
+            for (int off = LPR / 2; off >= 1; off >>= 1)
+              part += __shfl_xor_sync(0xffffffffu, part, off);
+            // row it*RPI + h sits in lanes h*LPR ..; lane j owns row j
+            const float v = __shfl_sync(0xffffffffu, part, (lane % RPI) * LPR);
+            if (lane / RPI == it) sc[i] = v;
           }
         }
-        // softmax pieces over the warp's 32 keys
+      }
+      // softmax pieces over the warp's 32 keys
+#pragma unroll
+      for (int i = 0; i < kQB; ++i) {
+        if (i < nq) {
+          const int t = (qb + i) % a.T;
+          // prompt rows precede every new token; a new row is visible to the
+          // tokens at or after its own position
+          const bool vis = kin && (kr < a.S || kr <= a.n_cached + t);
+          const float x = vis ? sc[i] * a.scale_log2 : -INFINITY;
+          const float m = warp_max(x);
+          const float p = m == -INFINITY ? 0.f : exp2f(x - m);
+          const float l = warp_sum(p);
+          pw[warp][i][lane] = p;
+          if (lane == 0) rml[warp][i] = make_float2(m, l);
+        }
+      }
+      if (!v_ready) {   // this lane's V copies, then the whole warp's, are in place
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        v_ready = true;
+      }
+      __syncwarp();
+      // O piece = P V over the warp's keys: lane = V columns
+      float o[kQB][VPL];
+#pragma unroll
+      for (int i = 0; i < kQB; ++i)
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) o[i][v] = 0.f;
+#pragma unroll
+      for (int k4 = 0; k4 < 32; k4 += 4) {
+        float vf[4][VPL];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          VReg<CT, VPL> vr;
+          if (lane < VLANES)
+            vr.load(&vs[warp][k4 + kk][lane * VPL]);
+          else
+            vr.zero();
+          vr.get(vf[kk]);
+        }
 #pragma unroll
         for (int i = 0; i < kQB; ++i) {
           if (i < nq) {
-            const int t = (qb + i) % a.T;
-            // prompt rows precede every new token; a new row is visible to the
-            // tokens at or after its own position
-            const bool vis = kin && (kr < a.S || kr <= a.n_cached + t);
-            const float x = vis ? sc[i] * a.scale_log2 : -INFINITY;
-            const float m = warp_max(x);
-            const float p = m == -INFINITY ? 0.f : exp2f(x - m);
-            const float l = warp_sum(p);
-            pw[warp][i][lane] = p;
-            if (lane == 0) rml[warp][i] = make_float2(m, l);
+            const float4 p4 = *reinterpret_cast<const float4*>(&pw[warp][i][k4]);
+            const float pk[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+              for (int v = 0; v < VPL; ++v) o[i][v] = fmaf(pk[kk], vf[kk][v], o[i][v]);
           }
         }
-        __syncwarp();
-        // O piece = P V over the warp's keys: lane = V columns
-        float o[kQB][VPL];
+      }
+      if (lane < VLANES) {
 #pragma unroll
         for (int i = 0; i < kQB; ++i)
+          if (i < nq)
 #pragma unroll
-          for (int v = 0; v < VPL; ++v) o[i][v] = 0.f;
-        const uint8_t* vbase = stg + warp * 32 * St::ROW + DH * (int)sizeof(CT);
-#pragma unroll
-        for (int k4 = 0; k4 < 32; k4 += 4) {
-          float vf[4][VPL];
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            VReg<CT, VPL> vr;
-            if (lane < VLANES)
-              vr.load(reinterpret_cast<const CT*>(vbase + (k4 + kk) * St::ROW) + lane * VPL);
-            else
-              vr.zero();
-            vr.get(vf[kk]);
-          }
-#pragma unroll
-          for (int i = 0; i < kQB; ++i) {
-            if (i < nq) {
-              const float4 p4 = *reinterpret_cast<const float4*>(&pw[warp][i][k4]);
-              const float pk[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                for (int v = 0; v < VPL; ++v) o[i][v] = fmaf(pk[kk], vf[kk][v], o[i][v]);
-            }
-          }
-        }
-        if (lane < VLANES) {
-#pragma unroll
-          for (int i = 0; i < kQB; ++i)
-            if (i < nq)
-#pragma unroll
-              for (int v = 0; v < VPL; ++v) ro[warp][i][lane * VPL + v] = o[i][v];
-        }
-      } else if (lane < kQB) {
-        rml[warp][lane] = make_float2(-INFINITY, 0.f);   // no rows: no contribution
+            for (int v = 0; v < VPL; ++v) ro[warp][i][lane * VPL + v] = o[i][v];
       }
-      __syncthreads();
-      // merge the warps: M = max m_w, O = sum 2^(m_w - M) o_w, L likewise
-      for (int idx = threadIdx.x; idx < nq * DH; idx += kAttnWarps * 32) {
-        const int i = idx / DH, j = idx - i * DH;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, rml[w][i].x);
-        float O = 0.f, L = 0.f;
-#pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w) {
-          const float2 ml = rml[w][i];
-          const float sc = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-          O = fmaf(sc, ml.x == -INFINITY ? 0.f : ro[w][i][j], O);
-          L = fmaf(sc, ml.y, L);
-        }
-        const int qr = qb + i, gi = qr / a.T, t = qr - gi * a.T;
-        const int64_t slot = ((int64_t)s * a.H + g * a.G + gi) * a.T + t;
-        a.part_o[slot * DH + j] = O;
-        if (j == 0) a.part_ml[slot] = make_float2(M, L);
-      }
-      __syncthreads();
+    } else if (lane < kQB) {
+      rml[warp][lane] = make_float2(-INFINITY, 0.f);   // no rows: no contribution
     }
+    __syncthreads();
+    // merge the warps: M = max m_w, O = sum 2^(m_w - M) o_w, L likewise
+    for (int idx = threadIdx.x; idx < nq * DH; idx += kAttnWarps * 32) {
+      const int i = idx / DH, j = idx - i * DH;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, rml[w][i].x);
+      float O = 0.f, L = 0.f;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) {
+        const float2 ml = rml[w][i];
+        const float sc = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+        O = fmaf(sc, ml.x == -INFINITY ? 0.f : ro[w][i][j], O);
+        L = fmaf(sc, ml.y, L);
+      }
+      const int qr = qb + i, gi = qr / a.T, t = qr - gi * a.T;
+      const int64_t slot = ((int64_t)s * a.H + g * a.G + gi) * a.T + t;
+      a.part_o[slot * DH + j] = O;
+      if (j == 0) a.part_ml[slot] = make_float2(M, L);
+    }
+    __syncthreads();
   }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 // CTA per (head, token): the maxima first (lane-parallel loads), then warp w
@@ -672,19 +641,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 
 template <typename CT, int DH>
 tsp_status decode_attn_t(const AttnArgs& aa, cudaStream_t st) {
-  using St = Stage<CT, DH>;
-  const size_t smem = (size_t)St::N * St::BYTES;
-  static bool attr[kMaxDevices] = {};   // the attribute holds for one device
-  const int dev = current_device();
-  if (!attr[dev]) {
-    TSP_CUDA_TRY(cudaFuncSetAttribute(decode_attn_kernel<CT, DH>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    attr[dev] = true;
-  }
-  const int64_t items = (int64_t)(aa.H / aa.G) * aa.nsplit;
-  const int grid = (int)std::min<int64_t>(items, num_sms());   // one persistent CTA per SM
   Prof prof("decode_attn", st);
-  decode_attn_kernel<CT, DH><<<grid, kAttnWarps * 32, smem, st>>>(aa);
+  // the K/V head varies fastest: CTAs running together read whole cache rows
+  dim3 grid((unsigned)(aa.H / aa.G * aa.nz), (unsigned)aa.nsplit);
+  decode_attn_kernel<CT, DH><<<grid, kAttnWarps * 32, 0, st>>>(aa);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }
@@ -770,6 +730,16 @@ tsp_status launch_decode_attn(const DecodeAttn& d, cudaStream_t st) {
   aa.H = d.H;
   aa.G = d.H / d.Hkv;
   aa.scale_log2 = 1.4426950408889634f / sqrtf((float)d.dh);
+  // query-row groups: enough CTAs for ~4 waves of 3 per SM when the K/V
+  // heads and splits alone give fewer (grouped K/V heads, short caches)
+  {
+    const int QR = aa.G * aa.T;
+    const int64_t base_ctas = (int64_t)d.Hkv * aa.nsplit;
+    const int64_t want = 12 * (int64_t)num_sms();
+    const int nz = (int)std::min<int64_t>(QR, std::max<int64_t>(1, (want + base_ctas - 1) / base_ctas));
+    aa.qpc = (QR + nz - 1) / nz;
+    aa.nz = (QR + aa.qpc - 1) / aa.qpc;
+  }
   tsp_status r = TSP_ERR_UNSUPPORTED;
   if (d.dtype == TSP_BF16) {
     if (d.dh == 128) r = decode_attn_t<__half, 128>(aa, st);

@@ -646,6 +646,8 @@ tsp_status gemm_tc(const TcGemm& g, cudaStream_t st) {
       break;
     case EPI_RES:
       if (!g.a_mn && !g.b_mn) return launch_t<EPI_RES, false, false, false>(*kp, grid, st, g.name);
+      // one rank's W_O / W_2 shard, stored transposed in the packed shard
+      if (!g.a_mn && g.b_mn) return launch_t<EPI_RES, false, true, false>(*kp, grid, st, g.name);
       // weight gradients added over sequence tiles (fp32 residual = the output)
       if (g.a_mn && g.b_mn) return launch_t<EPI_RES, true, true, false>(*kp, grid, st, g.name);
       break;

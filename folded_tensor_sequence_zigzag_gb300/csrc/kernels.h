@@ -47,6 +47,8 @@ tsp_status launch_swiglu_bwd_f32(const float* dG, const float* AB, float* dAB, i
                                  cudaStream_t st);
 tsp_status launch_pack_attn_shards(const void* wq, const void* wk, const void* wv, const void* wo,
                                    void* dst, int d, int D, int dtype, cudaStream_t st);
+tsp_status launch_pack_mlp_shards(const void* w1, const void* w3, const void* w2, void* dst, int d,
+                                  int I, int D, int dtype, cudaStream_t st);
 
 // simt_f32.cu
 tsp_status launch_gemm_f32(int M, int N, int K, const float* A, int64_t sam, int64_t sak,
@@ -62,6 +64,12 @@ tsp_status launch_attn_f32_bwd(const float* QKV, const float* O, const float* dO
 // attn_fwd.cu
 tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, int H, int Hkv, int dh,
                                 int D, cudaStream_t st);
+// one virtual rank r's query rows (multi-head, H heads of width dh): q [2c, ldq]
+// its own rows (head h at column h*dh), kv [S, ldkv] the gathered K|V in zigzag
+// row order (K head h at h*dh, V at H*dh + h*dh); o [2c, ldo], lse [H, 2c]
+tsp_status launch_attn_fwd_rank_f16(const void* q, int64_t ldq, const void* kv, int64_t ldkv,
+                                    void* o, int64_t ldo, float* lse, int64_t S, int H, int dh,
+                                    int D, int r, cudaStream_t st);
 
 // attn_bwd.cu (delta: 2 x H x S fp32 scratch, Delta then the scaled LSE)
 tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, const float* lse,
@@ -112,6 +120,9 @@ struct DecodeAttn {
 };
 int64_t decode_splits(int64_t S, int D, int64_t n_rows);
 tsp_status launch_decode_attn(const DecodeAttn& a, cudaStream_t st);
+
+// api.cu: TSP_OK if the configuration is valid (the entry points' common check)
+tsp_status cfg_status(const tsp_cfg* cfg);
 
 // api.cu: the block forward and backward with the residual stream's element
 // type chosen per call (the C entry points pass the cfg dtype; the stack keeps

@@ -764,6 +764,48 @@ __global__ void pack_attn_shards_kernel(const T* __restrict__ wq, const T* __res
   }
 }
 
+// Packed MLP shards, what one step of the ring hands on: shard k (rows I_k of
+// W_1 and W_3, boundaries floor(k*I/D)) is [W_1[I_k,:]; W_3[I_k,:]; W_2[:,I_k]^T],
+// a [3*|I_k|, d] block; shards follow each other.
+template <typename T>
+__global__ void pack_mlp_shards_kernel(const T* __restrict__ w1, const T* __restrict__ w3,
+                                       const T* __restrict__ w2, T* __restrict__ dst, int d, int I,
+                                       int D) {
+  const int64_t total = (int64_t)3 * I * d;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t orow = t / d;  // row of dst
+    const int col = (int)(t - orow * d);
+    // shard k with 3*lo(k) <= orow < 3*lo(k+1)
+    int k = (int)((orow / 3) * D / I);
+    while (k > 0 && 3 * ((int64_t)k * I / D) > orow) --k;
+    while (k + 1 < D && 3 * ((int64_t)(k + 1) * I / D) <= orow) ++k;
+    const int64_t lo = (int64_t)k * I / D, w = (int64_t)(k + 1) * I / D - lo;
+    const int64_t rr = orow - 3 * lo;
+    const int part = (int)(rr / w);
+    const int64_t ii = lo + (rr - part * w);
+    T v;
+    if (part == 0) v = w1[ii * d + col];
+    else if (part == 1) v = w3[ii * d + col];
+    else v = w2[(int64_t)col * I + ii];
+    dst[t] = v;
+  }
+}
+
+tsp_status launch_pack_mlp_shards(const void* w1, const void* w3, const void* w2, void* dst, int d,
+                                  int I, int D, int dtype, cudaStream_t st) {
+  Prof prof("pack_mlp_shards", st);
+  if (dtype == TSP_BF16)
+    pack_mlp_shards_kernel<__nv_bfloat16><<<num_sms() * 4, 256, 0, st>>>(
+        (const __nv_bfloat16*)w1, (const __nv_bfloat16*)w3, (const __nv_bfloat16*)w2,
+        (__nv_bfloat16*)dst, d, I, D);
+  else
+    pack_mlp_shards_kernel<float><<<num_sms() * 4, 256, 0, st>>>(
+        (const float*)w1, (const float*)w3, (const float*)w2, (float*)dst, d, I, D);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
 tsp_status launch_pack_attn_shards(const void* wq, const void* wk, const void* wv, const void* wo,
                                    void* dst, int d, int D, int dtype, cudaStream_t st) {
   Prof prof("pack_attn_shards", st);

@@ -29,7 +29,8 @@ EXPORTED = ("tsp_zigzag_permute", "tsp_rmsnorm_fwd", "tsp_workspace_bytes", "tsp
             "tsp_decode_workspace_bytes", "tsp_block_prefill", "tsp_block_decode",
             "tsp_debug_skip_stage", "tsp_block_weights_bytes", "tsp_block_weights_prepare",
             "tsp_block_fwd_prepared", "tsp_block_bwd_prepared", "tsp_stack_fwd_prepared",
-            "tsp_stack_bwd_prepared")
+            "tsp_stack_bwd_prepared", "tsp_pack_mlp_shards", "tsp_rank_workspace_bytes",
+            "tsp_rank_attn_project", "tsp_rank_attn_heads", "tsp_rank_mlp_step")
 DECODE_MAX_T = 8   # TSP_DECODE_MAX_T
 
 
@@ -93,6 +94,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                    + [vp, sz, vp]),
         "tsp_stack_fwd_prepared": (i32, [P(Cfg), i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "tsp_stack_bwd_prepared": (i32, [P(Cfg), i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "tsp_pack_mlp_shards": (i32, [P(Cfg), P(MlpW), vp, vp]),
+        "tsp_rank_workspace_bytes": (sz, [P(Cfg)]),
+        "tsp_rank_attn_project": (i32, [P(Cfg), i32, i32, vp, vp, vp, vp, vp, sz, vp]),
+        "tsp_rank_attn_heads": (i32, [P(Cfg), i32, i32, vp, vp, vp, vp, sz, vp]),
+        "tsp_rank_mlp_step": (i32, [P(Cfg), i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "tsp_gated_mlp_fwd_noalloc": (i32, [P(Cfg), vp, P(MlpW), vp, vp]),
         "tsp_stack_saved_bytes": (sz, [P(Cfg), i32]),
         "tsp_stack_workspace_bytes": (sz, [P(Cfg), i32, i32]),
@@ -472,6 +478,37 @@ def pack_attn_shards(cfg: Cfg, W: BlockWeights, stream=None):
     _check(load().tsp_pack_attn_shards(ctypes.byref(cfg), ctypes.byref(aw), _ptr(out),
                                        _stream(stream)), "tsp_pack_attn_shards")
     return out
+
+
+def pack_mlp_shards(cfg: Cfg, W: BlockWeights, stream=None):
+    """[3*inter, d]: shard k = [W_1[I_k]; W_3[I_k]; W_2[:, I_k]^T], shards in order."""
+    out = empty((3 * cfg.inter, cfg.d), W.w1.dtype, W.w1.device)
+    mw = W.mlp()
+    _check(load().tsp_pack_mlp_shards(ctypes.byref(cfg), ctypes.byref(mw), _ptr(out),
+                                      _stream(stream)), "tsp_pack_mlp_shards")
+    return out
+
+
+def rank_workspace_bytes(cfg: Cfg) -> int:
+    return int(load().tsp_rank_workspace_bytes(ctypes.byref(cfg)))
+
+
+def rank_attn_project(cfg: Cfg, r: int, k: int, x_r, g_attn, shard_k, kv_k, ws, stream=None):
+    _check(load().tsp_rank_attn_project(ctypes.byref(cfg), r, k, _ptr(x_r), _ptr(g_attn),
+                                        _ptr(shard_k), _ptr(kv_k), _ptr(ws), ws.numel(),
+                                        _stream(stream)), "tsp_rank_attn_project")
+
+
+def rank_attn_heads(cfg: Cfg, r: int, k: int, x_r, kv_all_k, h_r, ws, stream=None):
+    _check(load().tsp_rank_attn_heads(ctypes.byref(cfg), r, k, _ptr(x_r), _ptr(kv_all_k),
+                                      _ptr(h_r), _ptr(ws), ws.numel(), _stream(stream)),
+           "tsp_rank_attn_heads")
+
+
+def rank_mlp_step(cfg: Cfg, r: int, t: int, h_r, g_mlp, shard, y_r, y_out, ws, stream=None):
+    _check(load().tsp_rank_mlp_step(ctypes.byref(cfg), r, t, _ptr(h_r), _ptr(g_mlp), _ptr(shard),
+                                    _ptr(y_r), _ptr(y_out), _ptr(ws), ws.numel(), _stream(stream)),
+           "tsp_rank_mlp_step")
 
 
 def device_status(reset: bool = True, stream=None) -> int:

@@ -382,6 +382,58 @@ tsp_status tsp_rank_memory(const tsp_cfg* cfg, int32_t L, int32_t training, int3
  * attention only (TSP_ERR_UNSUPPORTED with grouped K/V heads). */
 tsp_status tsp_pack_attn_shards(const tsp_cfg* cfg, const tsp_attn_w* w, void* dst, void* stream);
 
+/* Packed MLP shards, what one step of the ring schedule hands on (section 2,
+ * gated-MLP bullet: W_1, W_2, W_3 shards rotate around the ranks): shard k
+ * (rows I_k of W_1 and W_3, boundaries floor(k*inter/D)) is written as
+ * [W_1[I_k,:]; W_3[I_k,:]; W_2[:,I_k]^T], a [3*|I_k|, d] block; shards
+ * follow each other in dst (3*inter*d elements of the cfg dtype). */
+tsp_status tsp_pack_mlp_shards(const tsp_cfg* cfg, const tsp_mlp_w* w, void* dst, void* stream);
+
+/* ---- One rank's steps of the forward schedule (section 2, "Runtime
+ * schedules") ----
+ * Where the other entry points run all D ranks at once on one GPU, these
+ * compute what one rank r computes between two exchanges of the schedule,
+ * from the data that rank holds; the caller moves the data between ranks.
+ * A forward of the block is, for every rank r:
+ *   for k = 0..D-1 (attention shard k broadcast by its owner):
+ *     tsp_rank_attn_project(r, k, x_r, g_attn, shard_k, kv_k[r])
+ *     all-gather: kv_all_k = kv_k[0] ; kv_k[1] ; ... ; kv_k[D-1] (rows stacked)
+ *     tsp_rank_attn_heads(r, k, x_r, kv_all_k, h_r)
+ *   for t = 0..D-1 (MLP shard (r - t) mod D received from rank r - 1):
+ *     tsp_rank_mlp_step(r, t, h_r, g_mlp, mlp_shard_{(r-t) mod D}, y_r, y_out_r)
+ * Shards are head-aligned (D divides H), so broadcast step k carries whole
+ * heads and its attention needs only that shard's K/V: every shard's weights
+ * are used once, while they are held.
+ * Buffers (rows = 2c = S/D, rank r's zigzag rows, chunk r then chunk 2D-1-r):
+ *   x_r      [2c, d] cfg dtype: the rank's input rows;
+ *   shard_k  [4*|C_k|, d] cfg dtype: block k of tsp_pack_attn_shards;
+ *   kv_k     [2c, 2*|C_k|] fp16: the rank's K | V of shard k's heads (out);
+ *   kv_all_k [S, 2*|C_k|] fp16: every rank's kv_k, rank q's at rows q*2c;
+ *   h_r      [2c, d] fp32: residual stream after the attention half
+ *            (written at k = 0 as x_r + ..., accumulated at k > 0);
+ *   mlp shard [3*|I_s|, d] cfg dtype: block s of tsp_pack_mlp_shards;
+ *   y_r      [2c, d] fp32: MLP accumulator (t = 0 starts from h_r);
+ *   y_out_r  [2c, d] cfg dtype (nullable): at t = D-1 the block output goes
+ *            here instead of y_r;
+ *   ws       tsp_rank_workspace_bytes(cfg) bytes, one per rank, passed to
+ *            all of that rank's calls of the layer in the order above (it
+ *            keeps the normalised rows, the received shard and Q between
+ *            calls).
+ * Shapes: TSP_BF16, multi-head attention without rotary embedding, dh = 128,
+ * D divides H with H/D >= 2, c a multiple of 256, d a multiple of 256,
+ * inter a multiple of 32*D; otherwise TSP_ERR_UNSUPPORTED (and
+ * tsp_rank_workspace_bytes returns 0).  Errors as for the block calls. */
+size_t tsp_rank_workspace_bytes(const tsp_cfg* cfg);
+tsp_status tsp_rank_attn_project(const tsp_cfg* cfg, int32_t r, int32_t k, const void* x_r,
+                                 const void* g_attn, const void* shard_k, void* kv_k, void* ws,
+                                 size_t ws_bytes, void* stream);
+tsp_status tsp_rank_attn_heads(const tsp_cfg* cfg, int32_t r, int32_t k, const void* x_r,
+                               const void* kv_all_k, float* h_r, void* ws, size_t ws_bytes,
+                               void* stream);
+tsp_status tsp_rank_mlp_step(const tsp_cfg* cfg, int32_t r, int32_t t, const float* h_r,
+                             const void* g_mlp, const void* shard, float* y_r, void* y_out,
+                             void* ws, size_t ws_bytes, void* stream);
+
 /* Reads (and with reset != 0 clears) the sticky device status word.  Waits
  * for `stream` to finish.  Returns TSP_OK or the first device error seen
  * (TSP_ERR_TIMEOUT or TSP_ERR_RANGE). */
