@@ -140,17 +140,20 @@ MEASURED_TRAFFIC = {
     # (kernel, workload): (bytes per launch, source file, sha256 of the source);
     # first (cold) launch of the process, from the captures summarised under profiles/
     ("gemm_w13_swiglu", "fwd16k"): (
-        1577046000 + 347930368, "folded_tensor_sequence_zigzag_gb300/csrc/gemm_tc.cu",
-        "3881b04ac6ec4b6d60b752665348644c2ab5d1b8a18012c11b284893e04bf2a6"),
+        1087107000 + 350731008, "folded_tensor_sequence_zigzag_gb300/csrc/gemm_tc.cu",
+        "ce2f297aab4cb1e40f5466009a187677b6f2508e1bf47cfb84a81454284b26f0"),
     ("attn_fwd", "fwd16k"): (
-        425805056 + 119521536, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
-        "7edd34168c2d0a321503026701a6e2e8b7eaed540464f7320b618f4bb29f99c1"),
+        423540480 + 118739456, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
+        "51c3428d7e86a4951317067fe2380ef5ec8a5f32ebc8dc546212f8ad46981586"),
     ("attn_bwd", "fwdbwd8k"): (
-        408193536 + 229216512, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
-        "c1380ccc41c0897044340f2c6ba425bb3690f1b8f465510c50b42bc22ef0aeb0"),
+        408808960 + 229822720, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
+        "c3c78393009a39a72ff72f7a1b51c0a6853a57916bb51052e2cc8270530f2822"),
     ("decode_attn", "decode16k"): (
-        268699136 + 4189184, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
-        "cb8b1e50beb6bc5f5bacb526fcf64e98f3c688cf02cc585e4d0aa51bcb4bc99c"),
+        268643072 + 4099072, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
+        "4ce5083cf3fa964a6a574593a8ec31526cb830396298ee6baf842441ced73d8a"),
+    ("decode_attn", "decode16k_gqa8"): (
+        67179520 + 1200896, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
+        "4ce5083cf3fa964a6a574593a8ec31526cb830396298ee6baf842441ced73d8a"),
 }
 
 

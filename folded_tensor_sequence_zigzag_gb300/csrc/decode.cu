@@ -374,20 +374,6 @@ __device__ __forceinline__ uint4 ld_nc16(const void* p) {
 
 // V elements one lane holds for one key: VPL of type CT
 template <typename CT, int VPL> struct VReg;
-template <> struct VReg<__half, 4> {   // 8 bytes
-  uint2 r;
-  __device__ void load(const __half* p) { r = *reinterpret_cast<const uint2*>(p); }
-  __device__ void zero() { r = make_uint2(0u, 0u); }
-  __device__ void get(float (&v)[4]) const {
-    v[0] = f16_lo(r.x); v[1] = f16_hi(r.x); v[2] = f16_lo(r.y); v[3] = f16_hi(r.y);
-  }
-};
-template <> struct VReg<__half, 2> {   // 4 bytes
-  uint32_t r;
-  __device__ void load(const __half* p) { r = *reinterpret_cast<const uint32_t*>(p); }
-  __device__ void zero() { r = 0u; }
-  __device__ void get(float (&v)[2]) const { v[0] = f16_lo(r); v[1] = f16_hi(r); }
-};
 template <> struct VReg<float, 2> {
   float2 r;
   __device__ void load(const float* p) { r = *reinterpret_cast<const float2*>(p); }
@@ -586,6 +572,208 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 4) decode_attn_kernel(const _
   }
 }
 
+// ---- the fp16 kernel: dot products and P V on the tensor cores (mma.sync) ----
+//
+// CTA = (K/V head g, split s of <= 128 cache rows, query group z), warp w takes
+// rows 32w .. 32w+31 as above.  The warp stages its K and V rows in its
+// shared-memory slice by cp.async (rows padded by 16 bytes so the 8x8 matrix
+// loads hit distinct banks), then for each pass of up to kQB query rows
+// (padded to the MMA's 16 rows with zeros) computes S = Q K^T over its 32 keys
+// with m16n8k16 MMAs (fp16 in, fp32 accumulate), the softmax pieces on the
+// accumulator fragments, and O = P V with P taken straight from those
+// fragments as the A operand.  A cache row costs a few tensor-core
+// instructions instead of the scalar dot products and lane shuffles of the
+// fp32 kernel, so the CTA's time is its loads.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A B + C, m16n8k16, A row-major fp16, B column-major fp16, fp32 C/D
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int DH>
+struct MmaSmem {
+  static constexpr int RB = DH * 2 + 16;                  // bytes per staged row (padded)
+  static constexpr int WARP_BYTES = 2 * 32 * RB;          // a warp's K rows, then its V rows
+  static constexpr int Q_BYTES = 16 * RB;                 // 16 query rows (fp16, padded)
+  static constexpr int BYTES = kAttnWarps * WARP_BYTES + Q_BYTES;
+};
+
+template <int DH>
+__global__ void __launch_bounds__(kAttnWarps * 32, 2) decode_attn_mma_kernel(const __grid_constant__ AttnArgs a) {
+  using L = MmaSmem<DH>;
+  constexpr int CPR = DH * 2 / 16;              // 16-byte pieces per K (or V) row
+  constexpr int NT = DH / 8;                    // n8 tiles of O (dh)
+  extern __shared__ __align__(16) uint8_t mma_smem[];
+  __shared__ __align__(16) float ro[kAttnWarps][kQB][DH];
+  __shared__ float2 rml[kAttnWarps][kQB];
+
+  const int g = blockIdx.x / a.nz, z = blockIdx.x - g * a.nz, s = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;      // MMA fragment row group and thread in it
+  int64_t r0, r1;
+  split_rows(a, s, r0, r1);
+  const int64_t wr0 = r0 + warp * 32;
+  const bool wactive = wr0 < r1;
+  const __half* base = reinterpret_cast<const __half*>(a.kv) + (int64_t)g * DH;
+  const uint32_t ks = smem_u32(mma_smem) + (uint32_t)(warp * L::WARP_BYTES);   // K rows
+  const uint32_t vs = ks + 32 * L::RB;                                          // V rows
+  const uint32_t qsm = smem_u32(mma_smem) + (uint32_t)(kAttnWarps * L::WARP_BYTES);
+  __half* qh = reinterpret_cast<__half*>(mma_smem + kAttnWarps * L::WARP_BYTES);
+
+  if (wactive) {
+    // K and V rows of the warp -> its slice; rows past the split read as zeros
+    for (int i = lane; i < 2 * 32 * CPR; i += 32) {
+      const int kv = i / (32 * CPR), k = (i / CPR) & 31, pc = i % CPR;
+      const bool in = wr0 + k < r1;
+      cp_async16(ks + (uint32_t)(kv * 32 * L::RB + k * L::RB + pc * 16),
+                 base + (in ? wr0 + k : r0) * a.ldkv + kv * a.dkv + pc * 8, in ? 16u : 0u);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  bool kv_ready = false;
+
+  const int QR = min(a.G * a.T, (z + 1) * a.qpc);
+  for (int qb = z * a.qpc; qb < QR; qb += kQB) {
+    const int nq = min(kQB, QR - qb);
+    // query rows qb .. qb+nq-1 into rows 0..nq-1 of the MMA's 16 (the rest zero)
+    for (int idx = threadIdx.x; idx < 16 * (DH / 8); idx += kAttnWarps * 32) {
+      const int i = idx / (DH / 8), pc = idx - i * (DH / 8);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (i < nq) {
+        const int qr = qb + i, gi = qr / a.T, t = qr - gi * a.T;
+        v = *reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(a.q) +
+                                            (int64_t)t * a.ldq + (g * a.G + gi) * DH + pc * 8);
+      }
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(qh) + i * L::RB + pc * 16) = v;
+    }
+    __syncthreads();
+    if (wactive) {
+      if (!kv_ready) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncwarp();
+        kv_ready = true;
+      }
+      // S[16 query rows x 32 keys] = Q K^T: four n8 tiles of keys, DH/16 k-steps
+      float sc[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < DH / 16; ++kk) {
+        uint32_t qa[4];
+        ldsm_x4(qsm + (uint32_t)((lane & 15) * L::RB + (kk * 16 + (lane >> 4) * 8) * 2), qa[0], qa[1],
+                qa[2], qa[3]);
+#pragma unroll
+        for (int nt = 0; nt < 4; nt += 2) {
+          // matrices: (keys nt*8.., dh lo), (nt*8.., dh hi), ((nt+1)*8.., lo), ((nt+1)*8.., hi)
+          const int m = lane >> 3;
+          const uint32_t addr = ks + (uint32_t)(((nt + (m >> 1)) * 8 + (lane & 7)) * L::RB +
+                                                (kk * 16 + (m & 1) * 8) * 2);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma16816(sc[nt], qa, b0, b1);
+          mma16816(sc[nt + 1], qa, b2, b3);
+        }
+      }
+      // softmax pieces of rows gq (sc[.][0..1]) over the warp's keys nt*8 + 2 tq + {0, 1};
+      // rows gq + 8 (sc[.][2..3]) are padding
+      const int t_row = (qb + gq) % a.T;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int64_t kr = wr0 + nt * 8 + 2 * tq + e;
+          // prompt rows precede every new token; a new row is visible to the
+          // tokens at or after its own position
+          const bool vis = kr < r1 && (kr < a.S || kr <= a.n_cached + t_row);
+          sc[nt][e] = vis ? sc[nt][e] * a.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, sc[nt][e]);
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      float l = 0.f;
+      uint32_t pa[2][4];   // P as the A operand of P V: k-steps of 16 keys
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float p0 = mx == -INFINITY ? 0.f : exp2f(sc[nt][0] - mx);
+        const float p1 = mx == -INFINITY ? 0.f : exp2f(sc[nt][1] - mx);
+        l += p0 + p1;
+        pa[nt >> 1][(nt & 1) * 2] = pack_f16(p0, p1);   // rows gq: a0 (keys lo) / a2 (keys hi)
+        pa[nt >> 1][(nt & 1) * 2 + 1] = 0u;             // rows gq + 8: padding
+      }
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      // O[16 x DH] = P V: V read transposed (k = keys, n = dh)
+      float o[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+        for (int nt = 0; nt < NT; nt += 2) {
+          // matrices: (keys kk*16 + 0..7, dh nt*8..), (keys +8..15, nt), (0..7, nt+1), (8..15, nt+1)
+          const int m = lane >> 3;
+          const uint32_t addr = vs + (uint32_t)((kk * 16 + (m & 1) * 8 + (lane & 7)) * L::RB +
+                                                (nt + (m >> 1)) * 8 * 2);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(addr, b0, b1, b2, b3);
+          mma16816(o[nt], pa[kk], b0, b1);
+          mma16816(o[nt + 1], pa[kk], b2, b3);
+        }
+      }
+      if (gq < nq) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          *reinterpret_cast<float2*>(&ro[warp][gq][nt * 8 + 2 * tq]) = make_float2(o[nt][0], o[nt][1]);
+        if (tq == 0) rml[warp][gq] = make_float2(mx, l);
+      }
+    } else if (lane < kQB) {
+      rml[warp][lane] = make_float2(-INFINITY, 0.f);   // no rows: no contribution
+    }
+    __syncthreads();
+    // merge the warps: M = max m_w, O = sum 2^(m_w - M) o_w, L likewise
+    for (int idx = threadIdx.x; idx < nq * DH; idx += kAttnWarps * 32) {
+      const int i = idx / DH, j = idx - i * DH;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, rml[w][i].x);
+      float O = 0.f, L2 = 0.f;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) {
+        const float2 ml = rml[w][i];
+        const float sc = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+        O = fmaf(sc, ml.x == -INFINITY ? 0.f : ro[w][i][j], O);
+        L2 = fmaf(sc, ml.y, L2);
+      }
+      const int qr = qb + i, gi = qr / a.T, t = qr - gi * a.T;
+      const int64_t slot = ((int64_t)s * a.H + g * a.G + gi) * a.T + t;
+      a.part_o[slot * DH + j] = O;
+      if (j == 0) a.part_ml[slot] = make_float2(M, L2);
+    }
+    __syncthreads();
+  }
+}
+
 // CTA per (head, token): the maxima first (lane-parallel loads), then warp w
 // adds splits w, w + 8, ... with no branch between its loads; the warps merge
 // in shared memory:  O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
@@ -637,6 +825,24 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     }
     o[(int64_t)t * H * dh + h * dh + threadIdx.x] = from_f<CT>(sum / lt);
   }
+}
+
+template <int DH>
+tsp_status decode_attn_mma(const AttnArgs& aa, cudaStream_t st) {
+  const size_t smem = MmaSmem<DH>::BYTES;
+  static bool attr[kMaxDevices] = {};   // the attribute holds for one device
+  const int dev = current_device();
+  if (!attr[dev]) {
+    TSP_CUDA_TRY(cudaFuncSetAttribute(decode_attn_mma_kernel<DH>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    attr[dev] = true;
+  }
+  Prof prof("decode_attn", st);
+  // the K/V head varies fastest: CTAs running together read whole cache rows
+  dim3 grid((unsigned)(aa.H / aa.G * aa.nz), (unsigned)aa.nsplit);
+  decode_attn_mma_kernel<DH><<<grid, kAttnWarps * 32, smem, st>>>(aa);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
 }
 
 template <typename CT, int DH>
@@ -730,20 +936,26 @@ tsp_status launch_decode_attn(const DecodeAttn& d, cudaStream_t st) {
   aa.H = d.H;
   aa.G = d.H / d.Hkv;
   aa.scale_log2 = 1.4426950408889634f / sqrtf((float)d.dh);
-  // query-row groups: enough CTAs for ~4 waves of 3 per SM when the K/V
-  // heads and splits alone give fewer (grouped K/V heads, short caches)
+  // query-row groups.  The fp16 kernel (dot products on the tensor cores)
+  // serves all G*T query rows of a K/V head in one CTA, so every cache row is
+  // read once.  The fp32 kernel's scalar arithmetic grows with the rows, so
+  // it splits them over enough CTAs for ~4 waves of 3 per SM when the K/V
+  // heads and splits alone give fewer (grouped K/V heads, short caches).
   {
     const int QR = aa.G * aa.T;
-    const int64_t base_ctas = (int64_t)d.Hkv * aa.nsplit;
-    const int64_t want = 12 * (int64_t)num_sms();
-    const int nz = (int)std::min<int64_t>(QR, std::max<int64_t>(1, (want + base_ctas - 1) / base_ctas));
+    int nz = 1;
+    if (d.dtype != TSP_BF16) {
+      const int64_t base_ctas = (int64_t)d.Hkv * aa.nsplit;
+      const int64_t want = 12 * (int64_t)num_sms();
+      nz = (int)std::min<int64_t>(QR, std::max<int64_t>(1, (want + base_ctas - 1) / base_ctas));
+    }
     aa.qpc = (QR + nz - 1) / nz;
     aa.nz = (QR + aa.qpc - 1) / aa.qpc;
   }
   tsp_status r = TSP_ERR_UNSUPPORTED;
   if (d.dtype == TSP_BF16) {
-    if (d.dh == 128) r = decode_attn_t<__half, 128>(aa, st);
-    else if (d.dh == 64) r = decode_attn_t<__half, 64>(aa, st);
+    if (d.dh == 128) r = decode_attn_mma<128>(aa, st);
+    else if (d.dh == 64) r = decode_attn_mma<64>(aa, st);
   } else {
     if (d.dh == 64) r = decode_attn_t<float, 64>(aa, st);
     else if (d.dh == 32) r = decode_attn_t<float, 32>(aa, st);
