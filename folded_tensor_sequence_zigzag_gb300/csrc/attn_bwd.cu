@@ -31,14 +31,15 @@
 // P/dS warps wait: a tcgen05.mma issue needs scheduler slots that those warps
 // would otherwise take.
 //   warps 0-7  P/dS: thread = key = TMEM lane, warps w and w+4 share 32 keys
-//              and take 64 query columns each: 2^8 P = 2^(s*scale*log2e - L2)
-//              with L2 = LSE*log2e - 8 precomputed per query (the 2^8 keeps
-//              small probabilities in fp16's normal range), dS = P (dP - Delta)
+//              and take 64 query columns each: P = 2^(s*scale*log2e - L2)
+//              with L2 = LSE*log2e precomputed per query, two probabilities a
+//              MUFU operation (fp16 pairs), scaled by 2^8 (which keeps small
+//              probabilities in fp16's normal range), dS = P (dP - Delta)
 //              at the same scale; P^T into TMEM, dS^T into swizzled shared memory (the
 //              K-major A operand of dK and the MN-major B operand of dQ^T);
 //              at the end of a key tile dK (warps 0-3), dV (4-7) -> fp16 rows;
 //   warps 8-11 dQ drain (thread = dh = TMEM lane): dQ^T(c) into the fp32 dQ
-//              accumulator with warp-coalesced atomics;
+//              accumulator with warp-coalesced reductions, paced;
 //   warp 12    TMA producer: K, V once per key tile; Q_c, dO_c (+ LSE_c,
 //              Delta_c by bulk copy) through a 2-stage ring;
 //   warp 13    TMEM allocator + MMA issuer.
@@ -76,8 +77,7 @@ constexpr int SMEM = OFF_BAR + 256;        // the dynamic base must be 1024-byte
 static_assert(SMEM <= 232448, "shared memory above the per-block limit");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_SQ = 0, TM_DPP = 128, TM_DV = 256, TM_DK = 384;
-constexpr float kOperandLog2Scale = 8.f;         // P, dS scaled by 2^8 into fp16's normal range
-constexpr float kOperandUnscale = 1.f / 256.f;
+constexpr float kOperandUnscale = 1.f / 256.f;   // P, dS carry 2^8 (fp16's normal range)
 // mbarrier indices
 constexpr int B_KV = 0, B_QFULL = 1, B_QEMPTY = B_QFULL + QSTAGES, B_DP = B_QEMPTY + QSTAGES,
               B_P = B_DP + 1 /* two: query halves A and B */, B_DQF = B_P + 2, B_DQE = B_DQF + 1,
@@ -87,7 +87,7 @@ static_assert(N_BARS * 8 <= 160, "barriers overlap the TMEM slot");
 struct TcBwdArgs {
   CUtensorMap tm_qkv;   // Q|K|V [S, ld = d + 2*dkv] fp16, box {64, 128}, 128B swizzle
   CUtensorMap tm_do;    // dO [S, d] fp16, box {64, 128}, 128B swizzle
-  const float* lse2;    // [H, S]: LSE * log2(e) - 8
+  const float* lse2;    // [H, S]: LSE * log2(e)
   const float* delta;   // [H, S]
   float* dq_acc;        // [S, d] fp32, zeroed
   ct_t* dqkv;           // [S, ld]: dK, dV written here
@@ -111,6 +111,44 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // barrier `id` over `nthreads` threads (whole warps), independent of barrier 0
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// 2^8 P and 2^8 dS of 32 consecutive queries of one key, as fp16 pairs.
+// P = 2^(s*scale*log2e - LSE*log2e): the exponents (<= 0) are rounded to fp16
+// pairs and one MUFU operation gives both probabilities (fp16 resolves the
+// exponents of the large probabilities to 2^-11 or better); 2^8 P is exact
+// from there and keeps small probabilities in fp16's normal range;
+// dS = 2^8 P * (dP - Delta) with dP - Delta in fp32 first.  MASK: queries
+// before the key (x < kx) get P = 0 through an exponent of -inf.
+template <bool MASK>
+__device__ __forceinline__ void p_ds_32(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
+                                        const float* L, const float* Dl, float scale_log2, int kx,
+                                        uint32_t (&pk)[16], uint32_t (&dk)[16]) {
+  const uint32_t k256 = 0x5C005C00u;   // (256, 256) in fp16
+#pragma unroll
+  for (int c8 = 0; c8 < 4; ++c8) {
+    const float4 l0 = *reinterpret_cast<const float4*>(L + c8 * 8);
+    const float4 l1 = *reinterpret_cast<const float4*>(L + c8 * 8 + 4);
+    const float4 d0 = *reinterpret_cast<const float4*>(Dl + c8 * 8);
+    const float4 d1 = *reinterpret_cast<const float4*>(Dl + c8 * 8 + 4);
+    const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+    const float dlv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const int x = c8 * 8 + e;
+      float x0 = fmaf(__uint_as_float(sv[x]), scale_log2, -lv[e]);
+      float x1 = fmaf(__uint_as_float(sv[x + 1]), scale_log2, -lv[e + 1]);
+      if (MASK) {
+        if (kx > x) x0 = -INFINITY;
+        if (kx > x + 1) x1 = -INFINITY;
+      }
+      const uint32_t p2 = hmul2_u32(ex2_approx_f16x2(pack_f16(x0, x1)), k256);
+      const uint32_t g2 =
+          pack_f16(__uint_as_float(dv[x]) - dlv[e], __uint_as_float(dv[x + 1]) - dlv[e + 1]);
+      pk[x >> 1] = p2;
+      dk[x >> 1] = hmul2_u32(p2, g2);
+    }
+  }
 }
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -376,11 +414,22 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           const int gi = GROUPED ? j / nqh : 0, jj = j - gi * nqh;
           const int64_t qrow = zz_row_of_pos(k0 + (int64_t)jj * BR, a.c, a.D);
           float* dst = a.dq_acc + qrow * a.d + (g * G + gi) * DH + dh;
+          // The reductions leave in 8 groups of 16 with a short sleep between
+          // them: at ~24 bytes a clock an SM's reductions drain slower than the
+          // warps issue them, and a full queue holds up the P/dS warps' shared
+          // memory loads and stores behind it (the tile took ~8% longer with
+          // the reductions issued in one burst).
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
+          for (int q = 0; q < 4; ++q) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              atomicAdd(dst + (int64_t)(q * 32 + e) * a.d, __uint_as_float(v[q][e]) * sc);
+            for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                atomicAdd(dst + (int64_t)(q * 32 + h2 * 16 + e) * a.d,
+                          __uint_as_float(v[q][h2 * 16 + e]) * sc);
+              __nanosleep(250);
+            }
+          }
         }
         tc_fence_before();
       }
@@ -420,29 +469,10 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
             tmem_ld32(lane_base + TM_DPP + qb, dv);
             tmem_wait_ld();
             uint32_t pk[16], dk[16];
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-              const float4 l0 = *reinterpret_cast<const float4*>(L + qb + c8 * 8);
-              const float4 l1 = *reinterpret_cast<const float4*>(L + qb + c8 * 8 + 4);
-              const float4 d0 = *reinterpret_cast<const float4*>(Dl + qb + c8 * 8);
-              const float4 d1 = *reinterpret_cast<const float4*>(Dl + qb + c8 * 8 + 4);
-              const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-              const float dlv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-#pragma unroll
-              for (int e = 0; e < 8; e += 2) {
-                float pp[2], dd[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                  const int x = c8 * 8 + e + u;
-                  float p = ex2_approx(fmaf(__uint_as_float(sv[x]), a.scale_log2, -lv[e + u]));
-                  if (diag && row > qb + x) p = 0.f;
-                  pp[u] = p;
-                  dd[u] = p * (__uint_as_float(dv[x]) - dlv[e + u]);
-                }
-                pk[c8 * 4 + (e >> 1)] = pack_f16(pp[0], pp[1]);
-                dk[c8 * 4 + (e >> 1)] = pack_f16(dd[0], dd[1]);
-              }
-            }
+            if (diag)
+              p_ds_32<true>(sv, dv, L + qb, Dl + qb, a.scale_log2, row - qb, pk, dk);
+            else
+              p_ds_32<false>(sv, dv, L + qb, Dl + qb, a.scale_log2, row - qb, pk, dk);
             // P^T over dP^T columns this thread has read: queries qb .. qb+31 ->
             // columns qb .. qb+15 (query chunk kk at 32 (kk / 2) + 8 (kk % 2))
             tmem_st16(lane_base + TM_DPP + qb, pk);
@@ -466,10 +496,10 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           ct_t* dkrow = a.dqkv + (krow0 + row) * a.ld + a.d + g * DH;
           const float mul = half == 0 ? a.scale * kOperandUnscale : kOperandUnscale;
           ct_t* out = dkrow + half * a.dkv;   // warps 0-3 write dK, warps 4-7 write dV
-#pragma unroll 1
           // (a dS beyond fp16 range makes dK and dQ non-finite, so the checks
           // of the dK, dV rows here and of dQ in dq_convert_kernel cover it)
           bool bad = false;
+#pragma unroll 1
           for (int q = 0; q < 4; ++q) {
             uint32_t v[32];
             tmem_ld32(lane_base + (half == 0 ? TM_DK : TM_DV) + q * 32, v);
@@ -503,7 +533,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
 }
 
 // Delta[h][row] = dO[row, head h] . O[row, head h] and
-// L2[h][row] = LSE[h][row] * log2(e) - 8 (the exponent offset of 2^8 P)
+// L2[h][row] = LSE[h][row] * log2(e) (the exponent offset of P)
 // (warp per row and head)
 __global__ void attn_delta_kernel(const ct_t* __restrict__ o, const ct_t* __restrict__ dO,
                                   const float* __restrict__ lse, float* __restrict__ delta,
@@ -520,8 +550,7 @@ __global__ void attn_delta_kernel(const ct_t* __restrict__ o, const ct_t* __rest
     s = warp_sum(s);
     if (lane == 0) {
       delta[(int64_t)h * S + row] = s;
-      lse2[(int64_t)h * S + row] =
-          fmaf(lse[(int64_t)h * S + row], 1.4426950408889634f, -kOperandLog2Scale);
+      lse2[(int64_t)h * S + row] = lse[(int64_t)h * S + row] * 1.4426950408889634f;
     }
   }
 }
