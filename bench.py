@@ -146,8 +146,8 @@ MEASURED_TRAFFIC = {
         423540480 + 118739456, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
         "51c3428d7e86a4951317067fe2380ef5ec8a5f32ebc8dc546212f8ad46981586"),
     ("attn_bwd", "fwdbwd8k"): (
-        408808960 + 229822720, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
-        "c3c78393009a39a72ff72f7a1b51c0a6853a57916bb51052e2cc8270530f2822"),
+        408622592 + 229798656, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
+        "a7729c67a8b19ad2b8a99f7828f59eb792be50f2e977afd6f00cbf7a7e0ca68d"),
     ("decode_attn", "decode16k"): (
         268643072 + 4099072, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
         "4ce5083cf3fa964a6a574593a8ec31526cb830396298ee6baf842441ced73d8a"),

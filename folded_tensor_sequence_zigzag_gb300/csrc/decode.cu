@@ -576,9 +576,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 4) decode_attn_kernel(const _
 //
 // CTA = (K/V head g, split s of <= 128 cache rows, query group z), warp w takes
 // rows 32w .. 32w+31 as above.  The warp stages its K and V rows in its
-// shared-memory slice by cp.async (rows padded by 16 bytes so the 8x8 matrix
-// loads hit distinct banks), then for each pass of up to kQB query rows
-// (padded to the MMA's 16 rows with zeros) computes S = Q K^T over its 32 keys
+// shared-memory slice by cp.async (the 16-byte pieces of row r swizzled by
+// r mod 8, so the 8x8 matrix loads hit distinct banks without padding, and
+// three CTAs fit an SM), then for each pass of up to kQB query rows (the
+// MMA's other rows read one shared zero row) computes S = Q K^T over its 32 keys
 // with m16n8k16 MMAs (fp16 in, fp32 accumulate), the softmax pieces on the
 // accumulator fragments, and O = P V with P taken straight from those
 // fragments as the A operand.  A cache row costs a few tensor-core
@@ -608,14 +609,18 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 
 template <int DH>
 struct MmaSmem {
-  static constexpr int RB = DH * 2 + 16;                  // bytes per staged row (padded)
+  static constexpr int RB = DH * 2;                       // bytes per staged row
   static constexpr int WARP_BYTES = 2 * 32 * RB;          // a warp's K rows, then its V rows
-  static constexpr int Q_BYTES = 16 * RB;                 // 16 query rows (fp16, padded)
+  static constexpr int Q_BYTES = (kQB + 1) * RB;          // kQB query rows and a zero row
   static constexpr int BYTES = kAttnWarps * WARP_BYTES + Q_BYTES;
+  // byte offset of 16-byte piece `c` of staged row `r`
+  static __device__ __forceinline__ uint32_t at(int r, int c) {
+    return (uint32_t)(r * RB + ((c ^ (r & 7)) << 4));
+  }
 };
 
 template <int DH>
-__global__ void __launch_bounds__(kAttnWarps * 32, 2) decode_attn_mma_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(kAttnWarps * 32, 3) decode_attn_mma_kernel(const __grid_constant__ AttnArgs a) {
   using L = MmaSmem<DH>;
   constexpr int CPR = DH * 2 / 16;              // 16-byte pieces per K (or V) row
   constexpr int NT = DH / 8;                    // n8 tiles of O (dh)
@@ -641,7 +646,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) decode_attn_mma_kernel(con
     for (int i = lane; i < 2 * 32 * CPR; i += 32) {
       const int kv = i / (32 * CPR), k = (i / CPR) & 31, pc = i % CPR;
       const bool in = wr0 + k < r1;
-      cp_async16(ks + (uint32_t)(kv * 32 * L::RB + k * L::RB + pc * 16),
+      cp_async16(ks + (uint32_t)(kv * 32 * L::RB) + L::at(k, pc),
                  base + (in ? wr0 + k : r0) * a.ldkv + kv * a.dkv + pc * 8, in ? 16u : 0u);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -651,8 +656,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) decode_attn_mma_kernel(con
   const int QR = min(a.G * a.T, (z + 1) * a.qpc);
   for (int qb = z * a.qpc; qb < QR; qb += kQB) {
     const int nq = min(kQB, QR - qb);
-    // query rows qb .. qb+nq-1 into rows 0..nq-1 of the MMA's 16 (the rest zero)
-    for (int idx = threadIdx.x; idx < 16 * (DH / 8); idx += kAttnWarps * 32) {
+    // query rows qb .. qb+nq-1 into staged rows 0..nq-1; rows nq..kQB are zero
+    // (row kQB stands in for the MMA's rows kQB..15)
+    for (int idx = threadIdx.x; idx < (kQB + 1) * (DH / 8); idx += kAttnWarps * 32) {
       const int i = idx / (DH / 8), pc = idx - i * (DH / 8);
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (i < nq) {
@@ -660,7 +666,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) decode_attn_mma_kernel(con
         v = *reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(a.q) +
                                             (int64_t)t * a.ldq + (g * a.G + gi) * DH + pc * 8);
       }
-      *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(qh) + i * L::RB + pc * 16) = v;
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(qh) + L::at(i, pc)) = v;
     }
     __syncthreads();
     if (wactive) {
@@ -678,14 +684,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) decode_attn_mma_kernel(con
 #pragma unroll
       for (int kk = 0; kk < DH / 16; ++kk) {
         uint32_t qa[4];
-        ldsm_x4(qsm + (uint32_t)((lane & 15) * L::RB + (kk * 16 + (lane >> 4) * 8) * 2), qa[0], qa[1],
-                qa[2], qa[3]);
+        const int qrow = (lane & 15) < kQB ? (lane & 15) : kQB;
+        ldsm_x4(qsm + L::at(qrow, 2 * kk + (lane >> 4)), qa[0], qa[1], qa[2], qa[3]);
 #pragma unroll
         for (int nt = 0; nt < 4; nt += 2) {
           // matrices: (keys nt*8.., dh lo), (nt*8.., dh hi), ((nt+1)*8.., lo), ((nt+1)*8.., hi)
           const int m = lane >> 3;
-          const uint32_t addr = ks + (uint32_t)(((nt + (m >> 1)) * 8 + (lane & 7)) * L::RB +
-                                                (kk * 16 + (m & 1) * 8) * 2);
+          const uint32_t addr = ks + L::at((nt + (m >> 1)) * 8 + (lane & 7), 2 * kk + (m & 1));
           uint32_t b0, b1, b2, b3;
           ldsm_x4(addr, b0, b1, b2, b3);
           mma16816(sc[nt], qa, b0, b1);
@@ -733,8 +738,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) decode_attn_mma_kernel(con
         for (int nt = 0; nt < NT; nt += 2) {
           // matrices: (keys kk*16 + 0..7, dh nt*8..), (keys +8..15, nt), (0..7, nt+1), (8..15, nt+1)
           const int m = lane >> 3;
-          const uint32_t addr = vs + (uint32_t)((kk * 16 + (m & 1) * 8 + (lane & 7)) * L::RB +
-                                                (nt + (m >> 1)) * 8 * 2);
+          const uint32_t addr = vs + L::at(kk * 16 + (m & 1) * 8 + (lane & 7), nt + (m >> 1));
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(addr, b0, b1, b2, b3);
           mma16816(o[nt], pa[kk], b0, b1);
