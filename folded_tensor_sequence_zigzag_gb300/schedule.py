@@ -110,53 +110,51 @@ class LocalComm:
 
 
 class GpuRankOps:
-    """One rank's computation in the library's kernels: x_z holds every
-    local rank's rows (rank r's at rows r * 2c, the zigzag layout); each rank
-    keeps its own workspace, K|V part, fp32 residual and MLP accumulator."""
+    """One rank's computation in the library's kernels, for the ranks in
+    `x_rows` ({rank: that rank's 2c zigzag rows of x}); each rank keeps its own
+    workspace, K|V part, fp32 residual and MLP accumulator."""
 
-    def __init__(self, cfg, W: tsp.BlockWeights, x_z, stream=None):
+    def __init__(self, cfg, W: tsp.BlockWeights, x_rows: dict, stream=None):
         self.cfg, self.W, self.stream = cfg, W, stream
         self.rows = cfg.S // cfg.D
-        self.x = x_z
-        dev = x_z.device
+        self.x = dict(x_rows)
+        dev = next(iter(self.x.values())).device
         nb = tsp.rank_workspace_bytes(cfg)
         if nb == 0:
             raise tsp.TspError(tsp.TSP_ERR_UNSUPPORTED, "tsp_rank_workspace_bytes")
-        wC = max(b - a for a, b in zip(shard_bounds(cfg.d, cfg.D)[:-1], shard_bounds(cfg.d, cfg.D)[1:]))
-        self.ws = [tsp.empty(nb, torch.uint8, dev) for _ in range(cfg.D)]
-        self.kv = [tsp.empty((self.rows, 2 * wC), torch.float16, dev) for _ in range(cfg.D)]
-        self.h = tsp.empty((cfg.S, cfg.d), torch.float32, dev)
-        self.y = tsp.empty((cfg.S, cfg.d), torch.float32, dev)
-        self.out = tsp.empty(x_z.shape, x_z.dtype, dev)
-
-    def _rows(self, t, r):
-        return t[r * self.rows:(r + 1) * self.rows]
+        b = shard_bounds(cfg.d, cfg.D)
+        wC = max(hi - lo for lo, hi in zip(b[:-1], b[1:]))
+        dt = next(iter(self.x.values())).dtype
+        self.ws = {r: tsp.empty(nb, torch.uint8, dev) for r in self.x}
+        self.kv = {r: tsp.empty((self.rows, 2 * wC), torch.float16, dev) for r in self.x}
+        self.h = {r: tsp.empty((self.rows, cfg.d), torch.float32, dev) for r in self.x}
+        self.y = {r: tsp.empty((self.rows, cfg.d), torch.float32, dev) for r in self.x}
+        self.out = {r: tsp.empty((self.rows, cfg.d), dt, dev) for r in self.x}
 
     def attn_project(self, r, k, shard):
         Ck = shard.shape[0] // 4
         kv = self.kv[r].view(-1)[:self.rows * 2 * Ck].view(self.rows, 2 * Ck)
-        tsp.rank_attn_project(self.cfg, r, k, self._rows(self.x, r), self.W.g_attn, shard, kv,
-                              self.ws[r], self.stream)
+        tsp.rank_attn_project(self.cfg, r, k, self.x[r], self.W.g_attn, shard, kv, self.ws[r],
+                              self.stream)
         return kv
 
     def attn_heads(self, r, k, kv_all):
-        tsp.rank_attn_heads(self.cfg, r, k, self._rows(self.x, r), kv_all, self._rows(self.h, r),
-                            self.ws[r], self.stream)
+        tsp.rank_attn_heads(self.cfg, r, k, self.x[r], kv_all, self.h[r], self.ws[r], self.stream)
 
     def mlp_step(self, r, t, shard):
         last = t == self.cfg.D - 1
-        tsp.rank_mlp_step(self.cfg, r, t, self._rows(self.h, r), self.W.g_mlp, shard,
-                          self._rows(self.y, r), self._rows(self.out, r) if last else None,
-                          self.ws[r], self.stream)
+        tsp.rank_mlp_step(self.cfg, r, t, self.h[r], self.W.g_mlp, shard, self.y[r],
+                          self.out[r] if last else None, self.ws[r], self.stream)
 
     def output(self, r):
-        return self._rows(self.out, r)
+        return self.out[r]
 
 
 def block_fwd_by_schedule(cfg, x_z, W: tsp.BlockWeights, stream=None):
     """y_z of the block computed rank by rank by the schedule, all D virtual
     ranks on this GPU (the same value tsp_block_fwd computes in one pass)."""
+    rows = cfg.S // cfg.D
     comm = LocalComm(cfg, W, stream)
-    ops = GpuRankOps(cfg, W, x_z, stream)
-    forward(comm, ops, cfg.D)
-    return ops.out
+    ops = GpuRankOps(cfg, W, {r: x_z[r * rows:(r + 1) * rows] for r in range(cfg.D)}, stream)
+    y = forward(comm, ops, cfg.D)
+    return torch.cat([y[r] for r in range(cfg.D)], 0)
