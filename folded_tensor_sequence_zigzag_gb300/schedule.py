@@ -56,24 +56,53 @@ def forward(comm, ops, D: int):
 
 
 class LocalComm:
-    """All D virtual ranks in this process, on one GPU.  The broadcast shard is
-    copied into one receive buffer that every local rank reads; the all-gather
-    copies each rank's K|V rows into one gathered buffer (rank q's rows at
-    q * 2c, the zigzag row order); the ring copies each held MLP shard into the
-    next rank's receive buffer (two buffers a rank, alternating)."""
+    """All D virtual ranks in this process, on one GPU.  The broadcast copies
+    the owner's packed shard into a receive buffer that every local rank
+    reads; the all-gather copies each rank's K|V rows into one gathered buffer
+    (rank q's rows at q * 2c, the zigzag row order); the ring copies each held
+    MLP shard into the next rank's receive buffer.  Receive buffers come in
+    pairs, alternating by step.
 
-    def __init__(self, cfg, W: tsp.BlockWeights, stream=None):
+    overlap=True moves the weight transfers (broadcast and ring) to a copy
+    stream, the single-GPU picture of the pages' transfer hidden behind the
+    shard GEMMs: shard k + 1 is copied while step k computes, and the compute
+    stream waits for a copy only where it reads the buffer.  The K|V
+    all-gather stays on the compute stream (its data is made by the same
+    step)."""
+
+    def __init__(self, cfg, W: tsp.BlockWeights, stream=None, overlap=False):
         self.cfg, self.D = cfg, cfg.D
-        self.attn_packed = tsp.pack_attn_shards(cfg, W, stream=stream)   # [4d, d]
-        self.mlp_packed = tsp.pack_mlp_shards(cfg, W, stream=stream)     # [3I, d]
+        dev = W.wq.device
+        self.dev, self._stream = dev, stream
+        self.attn_packed = tsp.pack_attn_shards(cfg, W, stream=self.stream)   # [4d, d]
+        self.mlp_packed = tsp.pack_mlp_shards(cfg, W, stream=self.stream)     # [3I, d]
         self.Cb = shard_bounds(cfg.d, cfg.D)
         self.Ib = shard_bounds(cfg.inter, cfg.D)
-        dev, dt = W.wq.device, W.wq.dtype
+        dt = W.wq.dtype
         wC = max(self.Cb[k + 1] - self.Cb[k] for k in range(self.D))
         wI = max(self.Ib[k + 1] - self.Ib[k] for k in range(self.D))
-        self.attn_rx = tsp.empty((4 * wC, cfg.d), dt, dev)
+        self.attn_rx = [tsp.empty((4 * wC, cfg.d), dt, dev) for _ in range(2)]
         self.kv_all = tsp.empty((cfg.S, 2 * wC), torch.float16, dev)
         self.mlp_rx = [[tsp.empty((3 * wI, cfg.d), dt, dev) for _ in range(2)] for _ in range(self.D)]
+        self.overlap = overlap
+        self._copy = torch.cuda.Stream(dev) if overlap else None
+        if overlap:
+            self._copy.wait_stream(self.stream)   # the packed shards are written
+        # per receive slot: the copy into it is done / the compute reading it is done
+        self.a_copied = [torch.cuda.Event() for _ in range(2)]
+        self.a_used = [torch.cuda.Event() for _ in range(2)]
+        self.m_copied = [torch.cuda.Event() for _ in range(2)]
+        self.m_used = [torch.cuda.Event() for _ in range(2)]
+
+    @property
+    def stream(self):
+        """The compute stream: the one given, else the current one at each call
+        (so a CUDA-graph capture records the exchanges too)."""
+        return self._stream if self._stream is not None else torch.cuda.current_stream(self.dev)
+
+    @property
+    def copy(self):
+        return self._copy if self.overlap else self.stream
 
     def local_ranks(self):
         return list(range(self.D))
@@ -81,10 +110,31 @@ class LocalComm:
     def attn_shard(self, k):
         return self.attn_packed[4 * self.Cb[k]:4 * self.Cb[k + 1]]
 
-    def broadcast_attn_shard(self, k):
+    def _copy_attn(self, k):
+        b = k & 1
         src = self.attn_shard(k)
-        dst = self.attn_rx[:src.shape[0]]
-        dst.copy_(src)
+        dst = self.attn_rx[b][:src.shape[0]]
+        with torch.cuda.stream(self.copy):
+            if self.overlap and k >= 2:
+                self.copy.wait_event(self.a_used[b])   # step k - 2 has read the slot
+            dst.copy_(src)
+            self.a_copied[b].record(self.copy)
+        return dst
+
+    def broadcast_attn_shard(self, k):
+        b = k & 1
+        if k >= 1:
+            self.a_used[(k - 1) & 1].record(self.stream)   # step k - 1 is fully issued
+        elif self.overlap:
+            self.copy.wait_stream(self.stream)   # fork the copy stream from this point
+        if not self.overlap or k == 0:
+            dst = self._copy_attn(k)
+        else:
+            dst = self.attn_rx[b][:self.attn_shard(k).shape[0]]
+        if self.overlap:
+            self.stream.wait_event(self.a_copied[b])
+            if k + 1 < self.D:
+                self._copy_attn(k + 1)   # runs while step k computes
         return dst
 
     def all_gather_kv(self, k, parts):
@@ -92,20 +142,32 @@ class LocalComm:
         w = 2 * (self.Cb[k + 1] - self.Cb[k])
         out = self.kv_all[:, :w] if w == self.kv_all.shape[1] else \
             self.kv_all.view(-1)[:self.cfg.S * w].view(self.cfg.S, w)
-        for r, p in parts.items():
-            out[r * rows:(r + 1) * rows].copy_(p)
+        with torch.cuda.stream(self.stream):
+            for r, p in parts.items():
+                out[r * rows:(r + 1) * rows].copy_(p)
         return out
 
     def own_mlp_shard(self, r):
         return self.mlp_packed[3 * self.Ib[r]:3 * self.Ib[r + 1]]
 
     def ring_pass(self, t, held):
+        b = (t + 1) & 1
+        self.m_used[t & 1].record(self.stream)   # step t is fully issued
         out = {}
-        for r in range(self.D):
-            src = held[(r - 1) % self.D]
-            dst = self.mlp_rx[r][t & 1][:src.shape[0]]
-            dst.copy_(src)
-            out[r] = dst
+        with torch.cuda.stream(self.copy):
+            # the held shards are the packed ones (t = 0) or this stream's own
+            # earlier copies, so only the slots being overwritten need a wait
+            if self.overlap and t >= 1:
+                self.copy.wait_event(self.m_used[b])   # step t - 1 has read the slots
+            for r in self.local_ranks():
+                src = held[(r - 1) % self.D]
+                dst = self.mlp_rx[r][b][:src.shape[0]]
+                dst.copy_(src)
+                out[r] = dst
+            self.m_copied[b].record(self.copy)
+        if self.overlap:
+            # the copy runs beside step t's kernels, queued before this wait
+            self.stream.wait_event(self.m_copied[b])
         return out
 
 
@@ -150,11 +212,114 @@ class GpuRankOps:
         return self.out[r]
 
 
-def block_fwd_by_schedule(cfg, x_z, W: tsp.BlockWeights, stream=None):
+def block_fwd_by_schedule(cfg, x_z, W: tsp.BlockWeights, stream=None, overlap=False):
     """y_z of the block computed rank by rank by the schedule, all D virtual
     ranks on this GPU (the same value tsp_block_fwd computes in one pass)."""
     rows = cfg.S // cfg.D
-    comm = LocalComm(cfg, W, stream)
+    comm = LocalComm(cfg, W, stream, overlap=overlap)
     ops = GpuRankOps(cfg, W, {r: x_z[r * rows:(r + 1) * rows] for r in range(cfg.D)}, stream)
     y = forward(comm, ops, cfg.D)
     return torch.cat([y[r] for r in range(cfg.D)], 0)
+
+
+class OneRankComm(LocalComm):
+    """Rank r0 alone, as one GPU of a D-GPU deployment sees the schedule: the
+    broadcast shard and the ring shard arrive by copies into its receive
+    buffers, and the all-gather copies every rank's K|V of the shard into the
+    gathered buffer -- the other ranks' parts taken from `kv_shards` (each
+    shard's K|V of all S rows, computed beforehand)."""
+
+    def __init__(self, cfg, W, r0, kv_shards, overlap=False):
+        super().__init__(cfg, W, overlap=overlap)
+        self.r0, self.kv_shards = r0, kv_shards
+
+    def local_ranks(self):
+        return [self.r0]
+
+    def all_gather_kv(self, k, parts):
+        rows = self.cfg.S // self.D
+        out = super().all_gather_kv(k, {})
+        with torch.cuda.stream(self.stream):
+            out.copy_(self.kv_shards[k])
+            out[self.r0 * rows:(self.r0 + 1) * rows].copy_(parts[self.r0])
+        return out
+
+    def ring_pass(self, t, held):
+        full = {r: self.own_mlp_shard(ring_shard(r, t, self.D)) for r in range(self.D)}
+        full[self.r0] = held[self.r0]
+        out = super().ring_pass(t, full)
+        return {self.r0: out[self.r0]}
+
+
+def _time_main():
+    """Times the 7B-shaped block forward on this GPU and prints one JSON line:
+    the one-pass tsp_block_fwd (all D ranks' work), and one rank's schedule
+    (what one GPU of a D-GPU deployment computes: 1/D of the work) replayed
+    from a CUDA graph, with its weight transfers on the compute stream and on
+    a copy stream.  python -m folded_tensor_sequence_zigzag_gb300.schedule"""
+    import argparse
+    import json
+
+    from .inputs import BlockShape, make_block_inputs
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--S", type=int, default=16384)
+    ap.add_argument("--D", type=int, default=8)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    a = ap.parse_args()
+    shape = BlockShape(S=a.S, d=4096, H=32, inter=11008, D=a.D)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=0)
+    cfg = tsp.make_cfg(shape.S, shape.d, shape.H, shape.inter, shape.D, torch.bfloat16, shape.eps)
+    W = tsp.BlockWeights.from_dict(inp, "cuda")
+    xz = tsp.zigzag_permute(inp["x"].cuda(), a.D)
+    rows = a.S // a.D
+
+    def timed(fn, graph):
+        for _ in range(a.warmup):
+            fn()
+        torch.cuda.synchronize()
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            fn = g.replay
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(a.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / a.steps
+
+    # every shard's K|V of all rows, from one full run of the schedule
+    class Keep(LocalComm):
+        kept = []
+
+        def all_gather_kv(self, k, parts):
+            out = super().all_gather_kv(k, parts)
+            self.kept.append(out.clone())
+            return out
+
+    all_ops = GpuRankOps(cfg, W, {r: xz[r * rows:(r + 1) * rows] for r in range(a.D)})
+    forward(Keep(cfg, W), all_ops, a.D)
+    kv_shards = Keep.kept
+
+    res = {"workload": f"7B-shaped block forward, S={a.S}, D={a.D}",
+           "one_pass_ms": timed(lambda: tsp.block_fwd(cfg, xz, W), False)}
+    res["one_pass_per_rank_ms"] = res["one_pass_ms"] / a.D
+    y_ref = all_ops.output(0).clone()
+    for overlap in (False, True):
+        comm = OneRankComm(cfg, W, 0, kv_shards, overlap=overlap)
+        ops = GpuRankOps(cfg, W, {0: xz[:rows]})
+        key = "one_rank_overlap_ms" if overlap else "one_rank_serial_ms"
+        res[key] = timed(lambda: forward(comm, ops, a.D), True)
+        if not torch.equal(ops.output(0), y_ref):
+            raise RuntimeError("one rank's schedule differs from the full run")
+    if tsp.device_status() != tsp.TSP_OK:
+        raise RuntimeError("device status not OK")
+    print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    _time_main()
