@@ -149,11 +149,11 @@ MEASURED_TRAFFIC = {
         408622592 + 229798656, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
         "a7729c67a8b19ad2b8a99f7828f59eb792be50f2e977afd6f00cbf7a7e0ca68d"),
     ("decode_attn", "decode16k"): (
-        268643072 + 4099072, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
-        "4ce5083cf3fa964a6a574593a8ec31526cb830396298ee6baf842441ced73d8a"),
+        268650240 + 4473856, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
+        "6085f2b2a1f1e130cccd798dc95f30b6719464d221e8c54f5dedb3db16dedb82"),
     ("decode_attn", "decode16k_gqa8"): (
-        67179520 + 1200896, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
-        "4ce5083cf3fa964a6a574593a8ec31526cb830396298ee6baf842441ced73d8a"),
+        67186176 + 188928, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
+        "6085f2b2a1f1e130cccd798dc95f30b6719464d221e8c54f5dedb3db16dedb82"),
 }
 
 
