@@ -638,6 +638,69 @@ def block_bwd(x, W, dy, H, eps):
                 dw2=dw2, dg_attn=dg_attn, dg_mlp=dg_mlp)
 
 
+def block_bwd_rows(x, W, dy_rows, rows, H, eps):
+    """All gradients of L = sum over the given positions of dy_rows * y, that
+    is block_bwd with dy zero at every other position, computed exactly
+    without the forward of the other rows.
+
+    The MLP, W_O and the query side of attention are row-local, so they run on
+    the given rows only; the keys and values at positions <= max(rows) are
+    projected for all of those positions, and the attention backward of the
+    given query rows reaches every one of them (dK, dV), so the K/V weight
+    gradients, the first RMSNorm's backward and dx cover positions
+    0 .. max(rows).  Returns the dict of block_bwd (dx over all S positions).
+    """
+    x = f64(x)
+    dy_r = f64(dy_rows)
+    rows = np.asarray(rows, dtype=np.int64)
+    S = x.shape[0]
+    kmax = int(rows.max()) + 1
+    keys = np.arange(kmax)
+    g1, g2 = _w(W, "g_attn"), _w(W, "g_mlp")
+    wq, wk, wv, wo = (_w(W, n) for n in ("wq", "wk", "wv", "wo"))
+    w1, w3, w2 = _w(W, "w1"), _w(W, "w3"), _w(W, "w2")
+    Hk = _kv_heads(W, H)
+    # forward: keys and values of positions < kmax, the rest at the rows
+    a_all, rstd1 = rmsnorm(x[:kmax], g1, eps)
+    K = rope(a_all @ wk.T, keys, Hk, _rope_base(W))
+    V = a_all @ wv.T
+    a_r = a_all[rows]
+    Q_r = rope(a_r @ wq.T, rows, H, _rope_base(W))
+    O_r, _ = causal_attention(Q_r, K, V, H, q_pos=rows, k_pos=keys)
+    h_r = x[rows] + O_r @ wo.T
+    b_r, rstd2 = rmsnorm(h_r, g2, eps)
+    A = b_r @ w1.T
+    B = b_r @ w3.T
+    sA = sigmoid(A)
+    G = A * sA * B
+    # MLP backward at the rows
+    dw2 = dy_r.T @ G
+    dG = dy_r @ w2
+    dA = dG * B * sA * (1.0 + A * (1.0 - sA))
+    dB = dG * A * sA
+    dw1 = dA.T @ b_r
+    dw3 = dB.T @ b_r
+    du2, dg_mlp = rmsnorm_bwd(dA @ w1 + dB @ w3, h_r, g2, rstd2)
+    dh_r = dy_r + du2
+    # attention backward: the rows' queries against every key they see
+    dwo = dh_r.T @ O_r
+    dO_r = dh_r @ wo
+    dQ_r, dK, dV = causal_attention_bwd(Q_r, K, V, O_r, dO_r, H, q_pos=rows, k_pos=keys)
+    dQ_r = rope(dQ_r, rows, H, _rope_base(W), inverse=True)
+    dK = rope(dK, keys, Hk, _rope_base(W), inverse=True)
+    dwq = dQ_r.T @ a_r
+    dwk = dK.T @ a_all
+    dwv = dV.T @ a_all
+    da = dK @ wk + dV @ wv
+    da[rows] += dQ_r @ wq
+    du1, dg_attn = rmsnorm_bwd(da, x[:kmax], g1, rstd1)
+    dx = np.zeros_like(x)
+    dx[:kmax] = du1
+    dx[rows] += dh_r
+    return dict(dx=dx, dwq=dwq, dwk=dwk, dwv=dwv, dwo=dwo, dw1=dw1, dw3=dw3,
+                dw2=dw2, dg_attn=dg_attn, dg_mlp=dg_mlp)
+
+
 def block_bwd_sharded(x, W, dy, H, D, eps):
     """Backward in the D-virtual-rank layout.
 

@@ -308,6 +308,41 @@ def test_7b_fwd_bwd_S32768_sampled():
         assert torch.isfinite(g[k]).all(), k
 
 
+def test_7b_fwd_bwd_S32768_sparse_dy_every_gradient():
+    """Config 5 at full size (S=32768, D=8) with dy non-zero on 256 seeded rows
+    only: every output of the backward (dx at all positions, all weight and
+    gain gradients) against the float64 oracle, which needs the forward only
+    at those rows (block_bwd_rows).  The kernels run at the full size: every
+    key tile, every query tile, the whole dQ reduction stream."""
+    S, D = 32768, 8
+    shape = BlockShape(S=S, d=4096, H=32, inter=11008, D=D)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=3, with_dy=True)
+    rows = np.sort(sample_rows(S, D).numpy())
+    dy = inp["dy"].clone()
+    keep = torch.zeros(S, dtype=torch.bool)
+    keep[torch.from_numpy(rows)] = True
+    dy[~keep] = 0
+    inp_s = dict(inp)
+    inp_s["dy"] = dy
+    _, g = _run_bwd(shape, inp_s, torch.bfloat16)
+    ref = O.block_bwd_rows(inp["x"], inp, O.f64(dy)[rows], rows, shape.H, shape.eps)
+    # dx is dy-sized on the 256 rows and only the attention's share elsewhere,
+    # and that share falls off along the sequence (the first keys are seen by
+    # every sampled query): the rows of dy against their own RMS, every other
+    # row (one position's gradient) against its own RMS at the same 2e-2 bound
+    dx, dx_ref = g.pop("dx"), ref.pop("dx")
+    assert_bf16_close(dx[rows], dx_ref[rows], "dx at the dy rows (S=32768)")
+    other = np.setdiff1d(np.arange(S), rows)
+    a, b = O.f64(dx)[other], dx_ref[other]
+    row_rms = np.sqrt(np.mean(b * b, axis=1))
+    floor = 1e-6 * float(np.sqrt(np.mean(b * b)))   # rows past the last dy row are zero
+    worst = float(np.max(np.abs(a - b).max(axis=1) / (row_rms + floor)))
+    assert worst <= 2e-2, ("dx elsewhere: max over rows of max|err|/row RMS", worst)
+    assert float(np.abs(a - b).sum() / np.abs(b).sum()) <= 5e-3, "dx elsewhere: mean rel"
+    for k, v in ref.items():
+        assert_bf16_close(g[k], v, f"{k} (S=32768, dy on 256 rows)")
+
+
 # ------------------------------------------------------------------ rotary embedding (variant)
 
 def _with_rope(inp, base):

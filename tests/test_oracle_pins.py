@@ -725,3 +725,24 @@ def test_rank_step_on_mirrored_rows_is_the_block_at_those_rows(D, n):
         Q_r, _, _ = O.rank_project(x[p], p, inp, shape.H, D, shape.eps)
         y_r = O.rank_fwd(r, x[p], p, Q_r, K_all, V_all, inp, shape.H, D, shape.eps, c)
         assert np.max(np.abs(y_r - yb[p])) <= 1e-12 * np.max(np.abs(yb)), r
+
+
+@pytest.mark.parametrize("Hkv,base", [(0, 0.0), (2, 10000.0)])
+def test_backward_of_sparse_dy_is_the_dense_backward(Hkv, base):
+    """block_bwd_rows (the gradients when dy is non-zero on a few rows only,
+    computed without the other rows' forward) against the dense block_bwd
+    with the same dy, including grouped K/V heads and the rotary embedding;
+    a key reached only by later rows, and the last position, are among the
+    cases."""
+    shape = BlockShape(S=64, d=32, H=4, inter=48, D=2, Hkv=Hkv)
+    inp = make_block_inputs(shape, torch.float32, seed=5 + Hkv, with_dy=True)
+    if base:
+        inp["rope_base"] = base
+    for rows in (np.array([3, 17, 40, 63]), np.array([0, 31, 32, 50])):
+        dy = O.f64(inp["dy"])
+        dys = np.zeros_like(dy)
+        dys[rows] = dy[rows]
+        ref = O.block_bwd(inp["x"], inp, dys, shape.H, shape.eps)
+        got = O.block_bwd_rows(inp["x"], inp, dy[rows], rows, shape.H, shape.eps)
+        for k, v in ref.items():
+            assert np.max(np.abs(got[k] - v)) <= 1e-12 * max(1e-30, np.max(np.abs(v))), (k, rows)
