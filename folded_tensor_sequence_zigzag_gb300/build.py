@@ -21,6 +21,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtsp.so")
+# checked build: every computed global index tested before its access
+BUILD_CHECK = os.path.join(ROOT, "_build_check")
+LIB_CHECK = os.path.join(PKG, "libtsp_check.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -38,15 +41,18 @@ def _newest(paths):
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(verbose: bool = False, jobs: int | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, jobs: int | None = None, check: bool = False) -> str:
+    """libtsp.so, or with check=True libtsp_check.so (compiled with TSP_CHECK)."""
+    out_dir, lib = (BUILD_CHECK, LIB_CHECK) if check else (BUILD, LIB)
+    flags = NVCC_FLAGS + (["-DTSP_CHECK"] if check else [])
+    os.makedirs(out_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
                      + glob.glob(os.path.join(INCLUDE, "*.h")))
     hdr_time = _newest(headers) if headers else 0.0
     objs, todo = [], []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src) + ".o")
         objs.append(obj)
         if not os.path.exists(obj) or os.path.getmtime(obj) < max(os.path.getmtime(src), hdr_time):
             todo.append((src, obj))
@@ -54,7 +60,7 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
 
     def compile_one(pair):
         src, obj = pair
-        cmd = [exe, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [exe, *ARCH, *flags, "-c", src, "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{res.stderr}")
@@ -65,15 +71,15 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
     if todo:
         with cf.ThreadPoolExecutor(max_workers=jobs or min(len(todo), os.cpu_count() or 4)) as ex:
             list(ex.map(compile_one, todo))
-    if todo or not os.path.exists(LIB) or os.path.getmtime(LIB) < _newest(objs):
-        tmp = LIB + ".tmp"
+    if todo or not os.path.exists(lib) or os.path.getmtime(lib) < _newest(objs):
+        tmp = lib + ".tmp"
         cmd = [exe, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64", "-o", tmp, *objs]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv))
+    print(build(verbose="-v" in sys.argv, check="--check" in sys.argv))

@@ -587,7 +587,7 @@ DecWs decode_layout(const tsp_cfg* c, int T, int64_t cap, uint8_t* base) {
 
 tsp_status decode_impl(const tsp_cfg* c, const void* x, int T, int64_t n_cached,
                        const tsp_attn_w* aw, const tsp_mlp_w* mw, void* y, void* kv,
-                       const DecWs& W, cudaStream_t st) {
+                       int64_t kv_rows, const DecWs& W, cudaStream_t st) {
   const bool bf = c->dtype == TSP_BF16;
   const int io_ty = bf ? TY_BF16 : TY_F32, ct = bf ? TY_F16 : TY_F32;
   const int d = c->d, I = c->inter, dk = (int)kv_dim(c);
@@ -606,7 +606,7 @@ tsp_status decode_impl(const tsp_cfg* c, const void* x, int T, int64_t n_cached,
     g.rows[0] = d; g.rows[1] = dk; g.rows[2] = dk; g.nseg = 3;
     g.K = d; g.T = T; g.out = W.qkv; g.ldo = ld; g.out_ty = ct;
     g.dh = c->dh; g.qk_heads = c->H + kv_heads(c); g.d = d; g.rope_base = c->rope_base;
-    g.pos0 = n_cached; g.kv = kv; g.ldkv = 2 * dk; g.name = "gemv_qkv";
+    g.pos0 = n_cached; g.kv = kv; g.ldkv = 2 * dk; g.kv_rows = kv_rows; g.name = "gemv_qkv";
     if ((r = launch_gemv(g, st)) != TSP_OK) return r;
   }
   {
@@ -737,6 +737,7 @@ const char* tsp_strerror(tsp_status s) {
     case TSP_ERR_CUDA: return "CUDA runtime error";
     case TSP_ERR_TIMEOUT: return "device pipeline wait exceeded its time limit";
     case TSP_ERR_RANGE: return "a value held in fp16 inside the bf16 path was out of fp16 range";
+    case TSP_ERR_BOUNDS: return "a computed index failed its bounds check (checked build)";
   }
   return "unknown status";
 }
@@ -924,7 +925,7 @@ tsp_status tsp_block_decode(const tsp_cfg* cfg, const void* x, int32_t T, int64_
   if (!al16(ws) || ws_bytes < tsp_decode_workspace_bytes(cfg, T, kv_rows_cap))
     return TSP_ERR_INVALID_ARG;
   const DecWs W = decode_layout(cfg, T, kv_rows_cap, (uint8_t*)ws);
-  return decode_impl(cfg, x, T, n_cached, aw, mw, y, kv, W, S_(stream));
+  return decode_impl(cfg, x, T, n_cached, aw, mw, y, kv, kv_rows_cap, W, S_(stream));
 }
 
 tsp_status tsp_pack_attn_shards(const tsp_cfg* cfg, const tsp_attn_w* w, void* dst, void* stream) {

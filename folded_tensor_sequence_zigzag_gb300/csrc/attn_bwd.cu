@@ -254,6 +254,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
       if (warp == WARP_PROD) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && !*abort_flag) {
+          (void)TSP_INB(krow0 >= 0 && krow0 + BC <= a.S, a.status);   // tensor copies: report only
           mbar_arrive_expect_tx(kv_full, 2 * TILE_BYTES);
 #pragma unroll
           for (int jh = 0; jh < 2; ++jh) {
@@ -268,7 +269,10 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
             if (!mbar_wait(qd_empty(st), qph(cur) ^ 1u, a.status, abort_flag, a.limit_ns)) break;
             const int gi = GROUPED ? j / nqh : 0, jj = j - gi * nqh;
             const int h = g * G + gi;
-            const int64_t qrow = zz_row_of_pos(k0 + (int64_t)jj * BR, a.c, a.D);
+            int64_t qrow = zz_row_of_pos(k0 + (int64_t)jj * BR, a.c, a.D);
+            // a failed check reads row 0 instead: the copy still lands, so the
+            // pipeline's byte counts hold
+            if (!TSP_INB(qrow >= 0 && qrow + BR <= a.S, a.status)) qrow = 0;
             const uint32_t fb = qd_full(st);
             mbar_arrive_expect_tx(fb, 2 * TILE_BYTES + 2 * BR * 4);
 #pragma unroll
@@ -413,6 +417,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           mbar_arrive(dq_empty);   // dQ^T(cur) read: its columns may take S^T(cur+1)
           const int gi = GROUPED ? j / nqh : 0, jj = j - gi * nqh;
           const int64_t qrow = zz_row_of_pos(k0 + (int64_t)jj * BR, a.c, a.D);
+          const bool q_in = TSP_INB(qrow >= 0 && qrow + BR <= a.S, a.status);
           float* dst = a.dq_acc + qrow * a.d + (g * G + gi) * DH + dh;
           // The reductions leave in 8 groups of 16 with a short sleep between
           // them: at ~24 bytes a clock an SM's reductions drain slower than the
@@ -425,7 +430,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
             for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
               for (int e = 0; e < 16; ++e)
-                atomicAdd(dst + (int64_t)(q * 32 + h2 * 16 + e) * a.d,
+                if (q_in) atomicAdd(dst + (int64_t)(q * 32 + h2 * 16 + e) * a.d,
                           __uint_as_float(v[q][h2 * 16 + e]) * sc);
               __nanosleep(250);
             }
@@ -493,6 +498,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
         bool eok = ok && mbar_wait(kv_done, (uint32_t)tile & 1u, a.status, abort_flag, a.limit_ns);
         if (__all_sync(0xffffffffu, eok)) {
           tc_fence_after();
+          const bool k_in = TSP_INB(krow0 >= 0 && krow0 + row < a.S, a.status);
           ct_t* dkrow = a.dqkv + (krow0 + row) * a.ld + a.d + g * DH;
           const float mul = half == 0 ? a.scale * kOperandUnscale : kOperandUnscale;
           ct_t* out = dkrow + half * a.dkv;   // warps 0-3 write dK, warps 4-7 write dV
@@ -511,7 +517,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
             uint4* dst = reinterpret_cast<uint4*>(out + q * 32);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              dst[c] = make_uint4(pack_f16(f[8 * c], f[8 * c + 1]), pack_f16(f[8 * c + 2], f[8 * c + 3]),
+              if (k_in) dst[c] = make_uint4(pack_f16(f[8 * c], f[8 * c + 1]), pack_f16(f[8 * c + 2], f[8 * c + 3]),
                                   pack_f16(f[8 * c + 4], f[8 * c + 5]),
                                   pack_f16(f[8 * c + 6], f[8 * c + 7]));
           }

@@ -190,6 +190,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
             const int qr = (int)(qrow0 - a.q_row_off + x * BQ);
+            // a tensor copy reads the fill value past its map, so the check reports only
+            (void)TSP_INB(qr >= 0 && qr + BQ <= a.lse_ld, a.status);
             tma_load_2d(base + OFF_Q + x * TILE_BYTES, &a.tm_q, a.q_col0 + h * DH, qr, q_full);
             tma_load_2d(base + OFF_Q + x * TILE_BYTES + BOX_BYTES, &a.tm_q, a.q_col0 + h * DH + 64,
                         qr, q_full);
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
           bool ok = true;
           for (int j = 0; j < nB && ok; ++j) {
             const int krow = (int)zz_row_of_pos((int64_t)j * BKV, a.c, a.D);
+            (void)TSP_INB(krow >= 0 && krow + BKV <= a.S, a.status);
 #pragma unroll 1
             for (int kv = 0; kv < 2; ++kv) {   // K_j then V_j
               const uint32_t n = n_loads, s = n % NSLOT;
@@ -428,6 +431,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
           tc_fence_after();
           const float inv = 1.f / l;
           const int64_t orow_i = qrow0 - a.o_row_off + x * BQ + row;
+          const bool o_in = TSP_INB(orow_i >= 0 && orow_i < a.lse_ld, a.status);
           ct_t* orow = a.o + orow_i * a.ldo + h * DH;
 #pragma unroll 1
           for (int q = 0; q < 4; ++q) {
@@ -437,14 +441,14 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
             uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              dst[c] = make_uint4(
+              if (o_in) dst[c] = make_uint4(
                   pack_f16(__uint_as_float(ov[8 * c + 0]) * inv, __uint_as_float(ov[8 * c + 1]) * inv),
                   pack_f16(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv),
                   pack_f16(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv),
                   pack_f16(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv));
           }
           constexpr float LN2 = 0.69314718055994530942f;
-          a.lse[(int64_t)h * a.lse_ld + orow_i] = (m_used + __log2f(l)) * LN2;
+          if (o_in) a.lse[(int64_t)h * a.lse_ld + orow_i] = (m_used + __log2f(l)) * LN2;
         }
         tc_fence_before();
           }

@@ -79,6 +79,21 @@ __device__ __forceinline__ void report_status(int* status, int code) {
   atomicCAS(status, 0, code);
 }
 
+// ---- checked build -------------------------------------------------------------
+// Compiled with -DTSP_CHECK, TSP_INB(cond, status) tests a computed index before
+// the global access it guards: when cond fails it records TSP_ERR_BOUNDS in the
+// sticky status word and the caller skips the access.  In the normal build it
+// is the constant true and compiles away.
+#ifdef TSP_CHECK
+__device__ __forceinline__ bool tsp_inb(bool ok, int* status) {
+  if (!ok) report_status(status, (int)TSP_ERR_BOUNDS);
+  return ok;
+}
+#define TSP_INB(cond, status) ::tsp::tsp_inb((cond), (status))
+#else
+#define TSP_INB(cond, status) true
+#endif
+
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 and later)
 __device__ __forceinline__ float fmax3f(float a, float b, float c) {
   float r;

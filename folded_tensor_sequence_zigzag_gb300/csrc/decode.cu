@@ -117,6 +117,7 @@ struct GemvArgs {
   void* kv;
   int64_t ldkv;
   int* status;   // sticky device status word (TSP_ERR_RANGE)
+  int64_t kv_rows;   // rows of the cache (the appended rows must fall inside)
   double freq[kRopeMaxHalf];   // base^(-2j/dh), formed on the host in fp64
 };
 
@@ -250,7 +251,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(const __grid_cons
             }
             store_chk(a.out, (int64_t)t * a.ldo + n1, a.out_ty, v1, bad);
             store_chk(a.out, (int64_t)t * a.ldo + n2, a.out_ty, v2, bad);
-            if (n1 >= a.d) {   // K or V: also the cache row of this token
+            if (n1 >= a.d &&   // K or V: also the cache row of this token
+                TSP_INB(a.pos0 + t >= 0 && a.pos0 + t < a.kv_rows, a.status)) {
               store_chk(a.kv, (a.pos0 + t) * a.ldkv + (n1 - a.d), a.out_ty, v1, bad);
               store_chk(a.kv, (a.pos0 + t) * a.ldkv + (n2 - a.d), a.out_ty, v2, bad);
             }
@@ -341,6 +343,7 @@ struct AttnArgs {
   int D, spr, nsplit, T, H, G, dkv;   // spr: splits per rank
   int nz, qpc;   // query-row groups per (K/V head, split); query rows per group
   float scale_log2;
+  int* status;   // sticky device status word (checked build: TSP_ERR_BOUNDS)
 };
 
 // cache rows [r0, r1) of split `s`: splits 0 .. D*spr-1 cut each rank's 2c
@@ -414,10 +417,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 4) decode_attn_kernel(const _
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int64_t r0, r1;
   split_rows(a, s, r0, r1);
+  const bool rows_in = TSP_INB(r0 >= 0 && r0 <= r1 && r1 <= a.n_total, a.status);
   const int64_t wr0 = r0 + warp * 32;
-  const bool wactive = wr0 < r1;
+  const bool wactive = rows_in && wr0 < r1;
   const int64_t kr = wr0 + lane;              // this lane's key row
-  const bool kin = kr < r1;
+  const bool kin = rows_in && kr < r1;
   const CT* base = reinterpret_cast<const CT*>(a.kv) + (int64_t)g * DH;
 
   const int kl = lane % LPR, kh = lane / LPR;   // piece and row of this lane in a K load
@@ -565,6 +569,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 4) decode_attn_kernel(const _
       }
       const int qr = qb + i, gi = qr / a.T, t = qr - gi * a.T;
       const int64_t slot = ((int64_t)s * a.H + g * a.G + gi) * a.T + t;
+      if (!TSP_INB(slot >= 0 && slot < (int64_t)a.nsplit * a.H * a.T, a.status)) continue;
       a.part_o[slot * DH + j] = O;
       if (j == 0) a.part_ml[slot] = make_float2(M, L);
     }
@@ -633,8 +638,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) decode_attn_mma_kernel(con
   const int gq = lane >> 2, tq = lane & 3;      // MMA fragment row group and thread in it
   int64_t r0, r1;
   split_rows(a, s, r0, r1);
+  const bool rows_in = TSP_INB(r0 >= 0 && r0 <= r1 && r1 <= a.n_total, a.status);
   const int64_t wr0 = r0 + warp * 32;
-  const bool wactive = wr0 < r1;
+  const bool wactive = rows_in && wr0 < r1;
   const __half* base = reinterpret_cast<const __half*>(a.kv) + (int64_t)g * DH;
   const uint32_t ks = smem_u32(mma_smem) + (uint32_t)(warp * L::WARP_BYTES);   // K rows
   const uint32_t vs = ks + 32 * L::RB;                                          // V rows
@@ -771,6 +777,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) decode_attn_mma_kernel(con
       }
       const int qr = qb + i, gi = qr / a.T, t = qr - gi * a.T;
       const int64_t slot = ((int64_t)s * a.H + g * a.G + gi) * a.T + t;
+      if (!TSP_INB(slot >= 0 && slot < (int64_t)a.nsplit * a.H * a.T, a.status)) continue;
       a.part_o[slot * DH + j] = O;
       if (j == 0) a.part_ml[slot] = make_float2(M, L2);
     }
@@ -898,6 +905,7 @@ tsp_status launch_gemv(const Gemv& g, cudaStream_t st) {
   }
   ga.kv = g.kv;
   ga.ldkv = g.ldkv;
+  ga.kv_rows = g.kv_rows;
   ga.K = g.K;
   ga.T = g.T;
   ga.out = g.out;
@@ -934,6 +942,7 @@ tsp_status launch_decode_attn(const DecodeAttn& d, cudaStream_t st) {
   aa.c = d.S / (2 * d.D);
   aa.n_cached = d.n_cached;
   aa.n_total = d.n_cached + d.T;
+  aa.status = status_word();
   aa.spr = (int)((2 * aa.c + kSplitRows - 1) / kSplitRows);
   aa.nsplit = (int)decode_splits(d.S, d.D, aa.n_total);
   aa.T = d.T;

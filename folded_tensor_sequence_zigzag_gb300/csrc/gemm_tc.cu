@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
         for (int i = 0; i < p.nkb; ++i) {
           if (p.rot_D > 0) {
             while (kb >= p.shard_kb[sh + 1]) {
+              if (!TSP_INB(step + 1 < p.rot_D, p.status)) break;   // shard table exhausted
               ++step;
               sh = (rank - step + p.rot_D) % p.rot_D;
               kb = p.shard_kb[sh];
@@ -412,6 +413,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
             float* dst;
             if (p.m_seg > 0) {
               const int sgi = (int)(m / p.m_seg);
+              if (!TSP_INB(sgi >= 0 && sgi < 3 && p.outs[sgi] != nullptr, p.status)) continue;
               dst = (float*)p.outs[sgi] + (int64_t)(m - sgi * p.m_seg) * p.ldo + n;
             } else {
               dst = (float*)p.out + (int64_t)m * p.ldo + n;

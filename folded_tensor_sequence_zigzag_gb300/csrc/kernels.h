@@ -102,6 +102,7 @@ struct Gemv {
   int64_t pos0 = 0;
   void* kv = nullptr;
   int64_t ldkv = 0;
+  int64_t kv_rows = 0;         // rows of the cache (bound of the appended rows)
   const char* name = "gemv";
 };
 tsp_status launch_gemv(const Gemv& g, cudaStream_t st);

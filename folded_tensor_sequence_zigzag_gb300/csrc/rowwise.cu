@@ -25,11 +25,12 @@ template <typename V>
 __global__ void __launch_bounds__(256) zigzag_permute_kernel(const V* __restrict__ src,
                                                              V* __restrict__ dst, int64_t S,
                                                              int64_t c, int D, int64_t vpr,
-                                                             int inverse) {
+                                                             int inverse, int* status) {
   for (int64_t row = blockIdx.x; row < S; row += gridDim.x) {
     // forward: dst zigzag row <- src global row pos(row)
     // inverse: dst global row <- src zigzag row row_of_pos(row)
     const int64_t srow = inverse ? zz_row_of_pos(row, c, D) : zz_pos_of_row(row, c, D);
+    if (!TSP_INB(srow >= 0 && srow < S, status)) continue;
     const V* s = src + srow * vpr;
     V* d = dst + row * vpr;
     int64_t v = threadIdx.x;
@@ -51,13 +52,13 @@ tsp_status launch_zigzag_permute(const void* src, void* dst, int64_t S, int D, i
   Prof prof(inverse ? "zigzag_unpermute" : "zigzag_permute", st);
   if (row_bytes % 16 == 0) {
     zigzag_permute_kernel<uint4><<<grid, 256, 0, st>>>((const uint4*)src, (uint4*)dst, S, c, D,
-                                                       row_bytes / 16, inverse);
+                                                       row_bytes / 16, inverse, status_word());
   } else if (row_bytes % 4 == 0) {
     zigzag_permute_kernel<uint32_t><<<grid, 256, 0, st>>>((const uint32_t*)src, (uint32_t*)dst, S,
-                                                          c, D, row_bytes / 4, inverse);
+                                                          c, D, row_bytes / 4, inverse, status_word());
   } else {
     zigzag_permute_kernel<uint8_t><<<grid, 256, 0, st>>>((const uint8_t*)src, (uint8_t*)dst, S, c,
-                                                         D, row_bytes, inverse);
+                                                         D, row_bytes, inverse, status_word());
   }
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;

@@ -14,8 +14,12 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libtsp.so")
+# the checked build (build.build(check=True)): the same library with every
+# computed global index tested before its access (TSP_ERR_BOUNDS)
+CHECK_LIB_PATH = os.path.join(_PKG, "libtsp_check.so")
 
-TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT, TSP_ERR_RANGE = range(6)
+(TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT, TSP_ERR_RANGE,
+ TSP_ERR_BOUNDS) = range(7)
 TSP_F32, TSP_BF16 = 0, 1
 TSP_OP_ATTN_FWD, TSP_OP_MLP_FWD, TSP_OP_BLOCK_FWD, TSP_OP_BLOCK_BWD, TSP_OP_BLOCK_FWD_TRAIN = range(5)
 TSP_OP_PREPARED = 16

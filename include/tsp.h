@@ -55,7 +55,12 @@
  *    operands -- that is not finite or too large for fp16 (|v| >= 65520,
  *    which fp16 rounds to infinity): TSP_ERR_RANGE.  The result of such a
  *    call is not valid.  (Magnitudes below 6.1e-5 are kept as fp16
- *    subnormals with fewer significant bits; that is not reported.)
+ *    subnormals with fewer significant bits; that is not reported.)  The
+ *    checked build (libtsp_check.so, compiled with TSP_CHECK) also tests the
+ *    global indices the kernels compute -- zigzag rows, shard and segment
+ *    indices, tile rows, cache rows, partial slots -- before each access and
+ *    skips an access that fails, recording TSP_ERR_BOUNDS; the normal build
+ *    carries none of these tests.
  *    While the word holds an error, the tensor-core kernels return without
  *    doing their work, until tsp_device_status(stream, 1) clears it.
  *  - All pointers must be 16-byte aligned; row strides are dense.
@@ -76,7 +81,8 @@ typedef enum {
   TSP_ERR_UNSUPPORTED = 2,   /* valid shape that the selected kernels do not take */
   TSP_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed               */
   TSP_ERR_TIMEOUT = 4,       /* a device pipeline wait exceeded its time limit     */
-  TSP_ERR_RANGE = 5          /* a value the bf16 path holds in fp16 was out of fp16 range */
+  TSP_ERR_RANGE = 5,         /* a value the bf16 path holds in fp16 was out of fp16 range */
+  TSP_ERR_BOUNDS = 6         /* checked build only: a computed index failed its bounds check */
 } tsp_status;
 
 typedef enum { TSP_F32 = 0, TSP_BF16 = 1 } tsp_dtype;

@@ -38,10 +38,22 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_strerror(lib):
-    for code in range(6):
+    for code in range(7):
         assert lib.tsp_strerror(code) and lib.tsp_strerror(code) != b"unknown status"
     assert b"invalid" in lib.tsp_strerror(tsp.TSP_ERR_INVALID_ARG)
     assert b"fp16" in lib.tsp_strerror(tsp.TSP_ERR_RANGE)
+    assert b"bounds" in lib.tsp_strerror(tsp.TSP_ERR_BOUNDS)
+
+
+def test_checked_build_exports_the_same_entry_points():
+    """The checked build (TSP_CHECK: every computed global index tested
+    before its access) is the same library otherwise: it builds from the same
+    sources and exports every declared entry point."""
+    from folded_tensor_sequence_zigzag_gb300 import build
+    path = build.build(check=True)
+    chk = ctypes.CDLL(path)
+    for n in _declared():
+        assert hasattr(chk, n), n
 
 
 def _cfg(**kw):
