@@ -55,6 +55,48 @@ def forward(comm, ops, D: int):
     return {r: ops.output(r) for r in local}
 
 
+def backward(comm, ops, D: int):
+    """One block backward by the schedule, after `forward` ran with the same
+    `ops` (which keeps what each rank's forward left).  Returns {rank: dx
+    rows} for the ranks `comm` holds; each shard's weight gradient ends at its
+    owner (comm keeps it) and the gain gradients are all-reduced.
+
+    The pages describe the forward only; this is its reverse, moving the same
+    shards (reading R17):
+      * MLP: the ring again, rank r holding shard (r - t) mod D at step t; the
+        shard's weight gradient travels with it, each rank adding its rows'
+        part, and one more hop after the last step brings it to its owner;
+      * attention: the owners broadcast their packed shards again; every rank
+        recomputes its K|V of the shard and the K|V is all-gathered; each rank
+        back-propagates its own query rows through the shard's heads, which
+        gives dK|dV for every key, and a reduce-scatter returns to each rank
+        the sum over all query ranks for its own rows; the shard's weight
+        gradient (summed over ranks) goes to its owner;
+      * the RMSNorm gains are replicated, so their gradients are all-reduced.
+    """
+    local = comm.local_ranks()
+    held = {r: comm.own_mlp_shard(r) for r in local}
+    grad = {r: None for r in local}                 # running gradient of the held shard
+    for t in range(D):
+        for r in local:
+            grad[r] = ops.mlp_bwd_step(r, t, held[r], grad[r])
+        held, grad = comm.ring_pass_with_grad(t, held, grad)
+    comm.keep_mlp_grads(grad)                       # rank r: the gradient of its own shard
+    for r in local:
+        ops.mlp_bwd_finish(r)
+    for k in range(D):
+        shard = comm.broadcast_attn_shard(k)
+        parts = {r: ops.attn_project(r, k, shard) for r in local}
+        kv_all = comm.all_gather_kv(k, parts)
+        dkv = {r: ops.attn_bwd_heads(r, k, kv_all) for r in local}   # every key's dK|dV
+        dkv_own = comm.reduce_scatter_kv(k, dkv)                      # own rows, all query ranks
+        comm.reduce_attn_grad(k, {r: ops.attn_bwd_weights(r, k, dkv_own[r]) for r in local})
+    for r in local:
+        ops.attn_bwd_finish(r)
+    comm.all_reduce_gains({r: ops.gain_grads(r) for r in local})
+    return {r: ops.dx(r) for r in local}
+
+
 class LocalComm:
     """All D virtual ranks in this process, on one GPU.  The broadcast copies
     the owner's packed shard into a receive buffer that every local rank
