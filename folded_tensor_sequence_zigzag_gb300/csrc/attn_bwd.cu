@@ -84,20 +84,58 @@ constexpr int B_KV = 0, B_QFULL = 1, B_QEMPTY = B_QFULL + QSTAGES, B_DP = B_QEMP
               B_KVDONE = B_DQE + 1, B_DRAIN = B_KVDONE + 1, N_BARS = B_DRAIN + 1;
 static_assert(N_BARS * 8 <= 160, "barriers overlap the TMEM slot");
 
+// Fp16 operands through 128-byte-swizzled maps (box {64, 128}).  The query
+// side (Q, dO, LSE, Delta, dQ) is indexed by query row = zigzag row - q_row_off;
+// the batched call passes the whole sequence (q_row_off 0), the one-rank call
+// its own 2c rows (q_row_off = r * 2c).
 struct TcBwdArgs {
-  CUtensorMap tm_qkv;   // Q|K|V [S, ld = d + 2*dkv] fp16, box {64, 128}, 128B swizzle
-  CUtensorMap tm_do;    // dO [S, d] fp16, box {64, 128}, 128B swizzle
-  const float* lse2;    // [H, S]: LSE * log2(e)
-  const float* delta;   // [H, S]
-  float* dq_acc;        // [S, d] fp32, zeroed
-  ct_t* dqkv;           // [S, ld]: dK, dV written here
-  int64_t S, c, ld;
-  int D, d, n_kt;       // n_kt = c / 128
+  CUtensorMap tm_q;     // Q: query head h at columns q_col0 + h*dh
+  CUtensorMap tm_kv;    // K at columns kv_col0 + g*dh, V at kv_col0 + dkv + g*dh; all S rows
+  CUtensorMap tm_do;    // dO: query head h at columns h*dh
+  const float* lse2;    // [H][lse_ld]: LSE * log2(e)
+  const float* delta;   // [H][lse_ld]
+  float* dq_acc;        // [query rows][dq_ld] fp32, zeroed
+  ct_t* out;            // dK at (zigzag row, out_col0 + g*dh), dV out_dkv columns further
+  int64_t S, c, out_ld, q_row_off, q_rows, lse_ld, dq_ld;
+  int q_col0, kv_col0, out_col0, out_dkv;
+  int D, n_kt;          // n_kt = c / 128
   int G, dkv;           // query heads per K/V head; K/V width Hkv*dh
+  int rank;             // one-rank call: the rank whose query rows are back-propagated
   float scale, scale_log2;
   int* status;
   uint64_t limit_ns;
 };
+
+// The query tiles a key tile at position k0 meets, per query head: every tile
+// from k0 on (batched), or the one rank's tiles from k0 on -- the rest of its
+// chunk r, then the rest of its chunk 2D-1-r (RANK).
+struct QTiles {
+  int nqh;              // per query head
+  int nA;               // RANK: tiles from chunk r
+  int64_t a0, b0;       // RANK: first positions in chunks r and 2D-1-r
+};
+template <bool RANK>
+__device__ __forceinline__ QTiles qtiles(const TcBwdArgs& a, int64_t k0) {
+  QTiles q;
+  if (!RANK) {
+    q.nqh = (int)((a.S - k0) / BR);
+    q.nA = 0; q.a0 = q.b0 = 0;
+    return q;
+  }
+  const int64_t ca = (int64_t)a.rank * a.c, cb = (int64_t)(2 * a.D - 1 - a.rank) * a.c;
+  q.a0 = k0 > ca ? k0 : ca;
+  q.b0 = k0 > cb ? k0 : cb;
+  q.nA = q.a0 < ca + a.c ? (int)((ca + a.c - q.a0) / BR) : 0;
+  const int nB = q.b0 < cb + a.c ? (int)((cb + a.c - q.b0) / BR) : 0;
+  q.nqh = q.nA + nB;
+  return q;
+}
+// position of query tile jj (0 .. nqh-1) of one head
+template <bool RANK>
+__device__ __forceinline__ int64_t qpos(const QTiles& q, int64_t k0, int jj) {
+  if (!RANK) return k0 + (int64_t)jj * BR;
+  return jj < q.nA ? q.a0 + (int64_t)jj * BR : q.b0 + (int64_t)(jj - q.nA) * BR;
+}
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
@@ -159,8 +197,11 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 }
 
 // GROUPED = false: one query head per K/V head (G = 1), the loops' group
-// arithmetic folded away at compile time
-template <bool GROUPED>
+// arithmetic folded away at compile time.  RANK: one rank's query rows
+// against every key tile (one key tile per CTA, blockIdx.x = its index; a
+// key tile no query of the rank reaches is skipped, its output rows having
+// been zeroed by the caller).
+template <bool GROUPED, bool RANK>
 __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_constant__ TcBwdArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
@@ -197,9 +238,15 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
   const int G = GROUPED ? a.G : 1;
   const int pair = blockIdx.x;
   const int r = pair / a.n_kt, t = pair - r * a.n_kt;
+  constexpr int NTILE = RANK ? 1 : 2;   // key tiles per CTA
   int64_t k0s[2];
-  k0s[0] = (int64_t)r * a.c + (int64_t)t * BC;                                      // long range
-  k0s[1] = (int64_t)(2 * a.D - 1 - r) * a.c + (int64_t)(a.n_kt - 1 - t) * BC;      // mirror
+  if (RANK) {
+    k0s[0] = (int64_t)blockIdx.x * BC;
+    k0s[1] = 0;
+  } else {
+    k0s[0] = (int64_t)r * a.c + (int64_t)t * BC;                                    // long range
+    k0s[1] = (int64_t)(2 * a.D - 1 - r) * a.c + (int64_t)(a.n_kt - 1 - t) * BC;    // mirror
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -223,7 +270,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
     tmem_relinquish();
   }
   if (warp == WARP_PROD && lane == 0) {
-    tma_prefetch_desc(&a.tm_qkv);
+    tma_prefetch_desc(&a.tm_q);
+    tma_prefetch_desc(&a.tm_kv);
     tma_prefetch_desc(&a.tm_do);
   }
   tc_fence_before();
@@ -246,10 +294,12 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
   if (warp >= WARP_PROD) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(REG_CTRL));
     uint32_t q_issued = 0, kv_issued = 0;
-    for (int tile = 0; tile < 2; ++tile) {
+    for (int tile = 0; tile < NTILE; ++tile) {
       const int64_t k0 = k0s[tile];
-      const int nqh = (int)((a.S - k0) / BR);   // query tiles per head
+      const QTiles qt = qtiles<RANK>(a, k0);
+      const int nqh = qt.nqh;                  // query tiles per head
       const int nq = nqh * G;                  // query iterations of this key tile
+      if (RANK && nq == 0) continue;           // every role skips it alike
       const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
       if (warp == WARP_PROD) {
         // ------------------------------------------------------------ producer
@@ -258,9 +308,9 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           mbar_arrive_expect_tx(kv_full, 2 * TILE_BYTES);
 #pragma unroll
           for (int jh = 0; jh < 2; ++jh) {
-            tma_load_2d(base + OFF_K + jh * BOX_BYTES, &a.tm_qkv, a.d + g * DH + 64 * jh, (int)krow0,
+            tma_load_2d(base + OFF_K + jh * BOX_BYTES, &a.tm_kv, a.kv_col0 + g * DH + 64 * jh, (int)krow0,
                         kv_full);
-            tma_load_2d(base + OFF_V + jh * BOX_BYTES, &a.tm_qkv, a.d + a.dkv + g * DH + 64 * jh,
+            tma_load_2d(base + OFF_V + jh * BOX_BYTES, &a.tm_kv, a.kv_col0 + a.dkv + g * DH + 64 * jh,
                         (int)krow0, kv_full);
           }
           ++kv_issued;
@@ -269,22 +319,22 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
             if (!mbar_wait(qd_empty(st), qph(cur) ^ 1u, a.status, abort_flag, a.limit_ns)) break;
             const int gi = GROUPED ? j / nqh : 0, jj = j - gi * nqh;
             const int h = g * G + gi;
-            int64_t qrow = zz_row_of_pos(k0 + (int64_t)jj * BR, a.c, a.D);
+            int64_t qrow = zz_row_of_pos(qpos<RANK>(qt, k0, jj), a.c, a.D) - a.q_row_off;
             // a failed check reads row 0 instead: the copy still lands, so the
             // pipeline's byte counts hold
-            if (!TSP_INB(qrow >= 0 && qrow + BR <= a.S, a.status)) qrow = 0;
+            if (!TSP_INB(qrow >= 0 && qrow + BR <= a.q_rows, a.status)) qrow = 0;
             const uint32_t fb = qd_full(st);
             mbar_arrive_expect_tx(fb, 2 * TILE_BYTES + 2 * BR * 4);
 #pragma unroll
             for (int jh = 0; jh < 2; ++jh) {
-              tma_load_2d(base + OFF_Q + st * TILE_BYTES + jh * BOX_BYTES, &a.tm_qkv,
-                          h * DH + 64 * jh, (int)qrow, fb);
+              tma_load_2d(base + OFF_Q + st * TILE_BYTES + jh * BOX_BYTES, &a.tm_q,
+                          a.q_col0 + h * DH + 64 * jh, (int)qrow, fb);
               tma_load_2d(base + OFF_DO + st * TILE_BYTES + jh * BOX_BYTES, &a.tm_do,
                           h * DH + 64 * jh, (int)qrow, fb);
             }
             const uint32_t sl = smem_u32(sLD + st * 2 * BR);
-            bulk_load(sl, a.lse2 + (int64_t)h * a.S + qrow, BR * 4, fb);
-            bulk_load(sl + BR * 4, a.delta + (int64_t)h * a.S + qrow, BR * 4, fb);
+            bulk_load(sl, a.lse2 + (int64_t)h * a.lse_ld + qrow, BR * 4, fb);
+            bulk_load(sl + BR * 4, a.delta + (int64_t)h * a.lse_ld + qrow, BR * 4, fb);
             ++q_issued;
           }
         }
@@ -390,10 +440,12 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
     }
   } else if (warp >= WARP_DRAIN) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(REG_DRAIN));
-    for (int tile = 0; tile < 2; ++tile) {
+    for (int tile = 0; tile < NTILE; ++tile) {
       const int64_t k0 = k0s[tile];
-      const int nqh = (int)((a.S - k0) / BR);
+      const QTiles qt = qtiles<RANK>(a, k0);
+      const int nqh = qt.nqh;
       const int nq = nqh * G;
+      if (RANK && nq == 0) continue;
       {
         // ------------------------------------------------------------ dQ drain (thread = dh)
         // all 128 query columns are read before the TMEM columns are released, so
@@ -416,9 +468,9 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           tc_fence_before();
           mbar_arrive(dq_empty);   // dQ^T(cur) read: its columns may take S^T(cur+1)
           const int gi = GROUPED ? j / nqh : 0, jj = j - gi * nqh;
-          const int64_t qrow = zz_row_of_pos(k0 + (int64_t)jj * BR, a.c, a.D);
-          const bool q_in = TSP_INB(qrow >= 0 && qrow + BR <= a.S, a.status);
-          float* dst = a.dq_acc + qrow * a.d + (g * G + gi) * DH + dh;
+          const int64_t qrow = zz_row_of_pos(qpos<RANK>(qt, k0, jj), a.c, a.D) - a.q_row_off;
+          const bool q_in = TSP_INB(qrow >= 0 && qrow + BR <= a.q_rows, a.status);
+          float* dst = a.dq_acc + qrow * a.dq_ld + (g * G + gi) * DH + dh;
           // The reductions leave in 8 groups of 16 with a short sleep between
           // them: at ~24 bytes a clock an SM's reductions drain slower than the
           // warps issue them, and a full queue holds up the P/dS warps' shared
@@ -430,7 +482,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
             for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
               for (int e = 0; e < 16; ++e)
-                if (q_in) atomicAdd(dst + (int64_t)(q * 32 + h2 * 16 + e) * a.d,
+                if (q_in) atomicAdd(dst + (int64_t)(q * 32 + h2 * 16 + e) * a.dq_ld,
                           __uint_as_float(v[q][h2 * 16 + e]) * sc);
               __nanosleep(250);
             }
@@ -442,10 +494,12 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
       tile_sync();
     }
   } else {
-    for (int tile = 0; tile < 2; ++tile) {
+    for (int tile = 0; tile < NTILE; ++tile) {
       const int64_t k0 = k0s[tile];
-      const int nqh = (int)((a.S - k0) / BR);
+      const QTiles qt = qtiles<RANK>(a, k0);
+      const int nqh = qt.nqh;
       const int nq = nqh * G;
+      if (RANK && nq == 0) continue;
       const int64_t krow0 = zz_row_of_pos(k0, a.c, a.D);
       {
         // ------------------------------------------------------------ P, dS (thread = key)
@@ -463,7 +517,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           const float* L = sLD + st * 2 * BR;
           const float* Dl = L + BR;
           // query tile == key tile (the first of each head): key index > query index is masked
-          const bool diag = GROUPED ? j % nqh == 0 : j == 0;
+          const bool diag = RANK ? qpos<RANK>(qt, k0, j) == k0 : (GROUPED ? j % nqh == 0 : j == 0);
           // query half X (queries 64X .. 64X+63) by all eight warps, A then B:
           // warps w and w+4 share a key and take 32 queries of the half each
 #pragma unroll
@@ -499,9 +553,9 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
         if (__all_sync(0xffffffffu, eok)) {
           tc_fence_after();
           const bool k_in = TSP_INB(krow0 >= 0 && krow0 + row < a.S, a.status);
-          ct_t* dkrow = a.dqkv + (krow0 + row) * a.ld + a.d + g * DH;
+          ct_t* dkrow = a.out + (krow0 + row) * a.out_ld + a.out_col0 + g * DH;
           const float mul = half == 0 ? a.scale * kOperandUnscale : kOperandUnscale;
-          ct_t* out = dkrow + half * a.dkv;   // warps 0-3 write dK, warps 4-7 write dV
+          ct_t* out = dkrow + half * a.out_dkv;   // warps 0-3 write dK, warps 4-7 write dV
           // (a dS beyond fp16 range makes dK and dQ non-finite, so the checks
           // of the dK, dV rows here and of dQ in dq_convert_kernel cover it)
           bool bad = false;
@@ -616,6 +670,34 @@ bool map_2d(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows) {
 
 }  // namespace
 
+namespace {
+
+// The backward kernel with its shared-memory attribute (once per device) and
+// the register-split check; grid (key-tile units, K/V heads).
+template <bool GROUPED, bool RANK>
+tsp_status launch_bwd_kernel(const TcBwdArgs& a, dim3 grid, cudaStream_t st) {
+  auto kern = attn_bwd_tc_kernel<GROUPED, RANK>;
+  static bool attr[kMaxDevices] = {};   // the attribute holds for one device
+  static int launch_regs = 0;
+  const int dev = current_device();
+  if (!attr[dev]) {
+    TSP_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM));
+    cudaFuncAttributes fa;
+    TSP_CUDA_TRY(cudaFuncGetAttributes(&fa, kern));
+    launch_regs = fa.numRegs;
+    attr[dev] = true;
+  }
+  // setmaxnreg.inc would wait forever if the split exceeded the launch allocation
+  const int64_t lr = launch_regs;
+  if (lr * NTHR < lr * 256 + 128 * (REG_DRAIN + REG_CTRL)) return TSP_ERR_UNSUPPORTED;
+  Prof prof(RANK ? "rank_attn_bwd" : "attn_bwd", st);
+  kern<<<grid, NTHR, SMEM, st>>>(a);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+}  // namespace
+
 tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, const float* lse,
                                float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int Hkv,
                                int dh, int D, cudaStream_t st) {
@@ -639,47 +721,96 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
   TcBwdArgs* a = new TcBwdArgs();
   std::unique_ptr<TcBwdArgs> guard(a);
   memset(a, 0, sizeof(TcBwdArgs));
-  if (!map_2d(&a->tm_qkv, qkv, ld, S) || !map_2d(&a->tm_do, dO, d, S))
-    return TSP_ERR_CUDA;
+  if (!map_2d(&a->tm_q, qkv, ld, S) || !map_2d(&a->tm_do, dO, d, S)) return TSP_ERR_CUDA;
+  a->tm_kv = a->tm_q;
+  a->q_col0 = 0;
+  a->kv_col0 = d;
   a->lse2 = delta + (int64_t)H * S;
   a->delta = delta;
   a->dq_acc = dq_acc;
-  a->dqkv = (ct_t*)dqkv;
+  a->dq_ld = d;
+  a->out = (ct_t*)dqkv;
+  a->out_ld = ld;
+  a->out_col0 = d;
+  a->out_dkv = dkv;
   a->S = S;
   a->c = c;
   a->D = D;
-  a->d = d;
-  a->ld = ld;
+  a->q_row_off = 0;
+  a->q_rows = S;
+  a->lse_ld = S;
   a->G = H / Hkv;
   a->dkv = dkv;
   a->n_kt = (int)(c / BC);
+  a->rank = -1;
   a->scale = 1.0f / sqrtf((float)dh);
   a->scale_log2 = 1.4426950408889634f * a->scale;
   a->status = status_word();
   a->limit_ns = wait_limit_ns();
-  const bool grouped = Hkv != H;
-  auto kern = grouped ? attn_bwd_tc_kernel<true> : attn_bwd_tc_kernel<false>;
-  static bool attr[kMaxDevices][2] = {};   // the attribute holds for one device
-  static int launch_regs[2] = {0, 0};
-  const int dev = current_device();
-  if (!attr[dev][grouped]) {
-    TSP_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM));
-    cudaFuncAttributes fa;
-    TSP_CUDA_TRY(cudaFuncGetAttributes(&fa, kern));
-    launch_regs[grouped] = fa.numRegs;
-    attr[dev][grouped] = true;
-  }
-  // setmaxnreg.inc would wait forever if the split exceeded the launch allocation
-  const int64_t lr = launch_regs[grouped];
-  if (lr * NTHR < lr * 256 + 128 * (REG_DRAIN + REG_CTRL)) return TSP_ERR_UNSUPPORTED;
-  dim3 grid((unsigned)(D * a->n_kt), (unsigned)Hkv);
-  {
-    Prof prof("attn_bwd", st);
-    kern<<<grid, NTHR, SMEM, st>>>(*a);
-    TSP_CUDA_TRY(cudaGetLastError());
-  }
+  const dim3 grid((unsigned)(D * a->n_kt), (unsigned)Hkv);
+  const tsp_status r = Hkv != H ? launch_bwd_kernel<true, false>(*a, grid, st)
+                                : launch_bwd_kernel<false, false>(*a, grid, st);
+  if (r != TSP_OK) return r;
   Prof prof("attn_bwd_dq_convert", st);
   dq_convert_kernel<<<num_sms() * 8, 256, 0, st>>>(dq_acc, (ct_t*)dqkv, S, d, ld, a->status);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+tsp_status launch_attn_bwd_rank_f16(const void* q, const void* kv, const void* o, const void* dO,
+                                    const float* lse, float* delta, float* dq_acc, void* dq,
+                                    void* dkv, int64_t S, int Hk, int dh, int D, int r,
+                                    cudaStream_t st) {
+  if (dh != DH) return TSP_ERR_UNSUPPORTED;
+  const int64_t c = S / (2 * D), rows = 2 * c;
+  if (c % BC != 0 || S > (int64_t)INT32_MAX || r < 0 || r >= D) return TSP_ERR_UNSUPPORTED;
+  const int Ck = Hk * dh;
+  const void* ptrs[9] = {q, kv, o, dO, lse, delta, dq_acc, dq, dkv};
+  for (const void* p : ptrs)
+    if (!p || ((uintptr_t)p & 15u)) return TSP_ERR_INVALID_ARG;
+  {
+    Prof prof("rank_attn_bwd_prep", st);
+    attn_delta_kernel<<<num_sms() * 8, 256, 0, st>>>((const ct_t*)o, (const ct_t*)dO, lse, delta,
+                                                     delta + (int64_t)Hk * rows, rows, Hk, Ck);
+    TSP_CUDA_TRY(cudaGetLastError());
+    TSP_CUDA_TRY(cudaMemsetAsync(dq_acc, 0, (size_t)rows * Ck * sizeof(float), st));
+    // key tiles none of the rank's queries reach keep these zeros
+    TSP_CUDA_TRY(cudaMemsetAsync(dkv, 0, (size_t)S * 2 * Ck * sizeof(ct_t), st));
+  }
+  TcBwdArgs* a = new TcBwdArgs();
+  std::unique_ptr<TcBwdArgs> guard(a);
+  memset(a, 0, sizeof(TcBwdArgs));
+  if (!map_2d(&a->tm_q, q, Ck, rows) || !map_2d(&a->tm_kv, kv, 2 * (int64_t)Ck, S) ||
+      !map_2d(&a->tm_do, dO, Ck, rows))
+    return TSP_ERR_CUDA;
+  a->q_col0 = 0;
+  a->kv_col0 = 0;
+  a->lse2 = delta + (int64_t)Hk * rows;
+  a->delta = delta;
+  a->dq_acc = dq_acc;
+  a->dq_ld = Ck;
+  a->out = (ct_t*)dkv;
+  a->out_ld = 2 * Ck;
+  a->out_col0 = 0;
+  a->out_dkv = Ck;
+  a->S = S;
+  a->c = c;
+  a->D = D;
+  a->q_row_off = (int64_t)r * rows;
+  a->q_rows = rows;
+  a->lse_ld = rows;
+  a->G = 1;
+  a->dkv = Ck;
+  a->n_kt = (int)(c / BC);
+  a->rank = r;
+  a->scale = 1.0f / sqrtf((float)dh);
+  a->scale_log2 = 1.4426950408889634f * a->scale;
+  a->status = status_word();
+  a->limit_ns = wait_limit_ns();
+  const tsp_status res = launch_bwd_kernel<false, true>(*a, dim3((unsigned)(S / BC), (unsigned)Hk), st);
+  if (res != TSP_OK) return res;
+  Prof prof("rank_attn_bwd_dq_convert", st);
+  dq_convert_kernel<<<num_sms() * 8, 256, 0, st>>>(dq_acc, (ct_t*)dq, rows, Ck, Ck, a->status);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }

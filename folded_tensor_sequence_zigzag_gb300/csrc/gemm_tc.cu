@@ -658,6 +658,8 @@ tsp_status gemm_tc(const TcGemm& g, cudaStream_t st) {
       break;
     case EPI_SWIGLU_BWD:
       if (!g.a_mn && g.b_mn) return launch_t<EPI_SWIGLU_BWD, false, true, false>(*kp, grid, st, g.name);
+      // one rank's W_2 shard, stored transposed in the packed ring shard
+      if (!g.a_mn && !g.b_mn) return launch_t<EPI_SWIGLU_BWD, false, false, false>(*kp, grid, st, g.name);
       break;
     case EPI_F32:
       if (!g.a_mn && g.b_mn) return launch_t<EPI_F32, false, true, false>(*kp, grid, st, g.name);

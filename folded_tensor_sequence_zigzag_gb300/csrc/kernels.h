@@ -75,6 +75,15 @@ tsp_status launch_attn_fwd_rank_f16(const void* q, int64_t ldq, const void* kv, 
 tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, const float* lse,
                                 float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int Hkv, int dh,
                                 int D, cudaStream_t st);
+// One rank's query rows (2c rows: Q, O, dO [2c, Hk*dh] fp16, LSE [Hk][2c]) of
+// Hk heads against the gathered K|V [S, 2*Hk*dh] (zigzag row order): dQ
+// [2c, Hk*dh] fp16, and dK|dV [S, 2*Hk*dh] fp16 for every key (the rank's
+// queries' share; zero where none reaches).  delta: 2*Hk*2c fp32 scratch,
+// dq_acc: 2c*Hk*dh fp32 scratch.
+tsp_status launch_attn_bwd_rank_f16(const void* q, const void* kv, const void* o, const void* dO,
+                                    const float* lse, float* delta, float* dq_acc, void* dq,
+                                    void* dkv, int64_t S, int Hk, int dh, int D, int r,
+                                    cudaStream_t st);
 
 // decode.cu: inference decode against the zigzag KV cache
 enum { GEMV_STORE = 0, GEMV_RES = 1, GEMV_SWIGLU = 2, GEMV_QKV = 3 };

@@ -43,6 +43,10 @@ int64_t bound(int64_t k, int64_t n, int D) { return k * n / D; }   // shard boun
 struct RankWs {
   void *a, *shard, *q, *o, *b, *g;
   float* lse;
+  // backward: rstd of both norms, dy and dh in fp16, the MLP shard's A|B and
+  // dA|dB, dO and dQ of the attention shard, and fp32 scratch
+  float *rstd1, *rstd2, *delta, *dq_acc, *dg_part;
+  void *dy16, *dh16, *ab, *dab, *dO, *dq;
   size_t bytes;
 };
 
@@ -63,6 +67,17 @@ RankWs rank_layout(const tsp_cfg* c, uint8_t* base) {
   W.lse = (float*)take(maxC / (size_t)c->dh * rows * 4);
   W.b = take(rows * d * 2);                                       // rms(h_r), fp16
   W.g = take(rows * maxI * 2);                                    // G of the held MLP shard
+  W.rstd1 = (float*)take(rows * 4);
+  W.rstd2 = (float*)take(rows * 4);
+  W.dy16 = take(rows * d * 2);
+  W.dh16 = take(rows * d * 2);
+  W.ab = take(rows * 2 * maxI * 2);                               // A | B of the held shard
+  W.dab = take(rows * 2 * maxI * 2);                              // dA | dB
+  W.dO = take(rows * maxC * 2);
+  W.dq = take(rows * maxC * 2);
+  W.delta = (float*)take(2 * (maxC / (size_t)c->dh) * rows * 4);  // Delta and LSE*log2(e)
+  W.dq_acc = (float*)take(rows * maxC * 4);
+  W.dg_part = (float*)take((size_t)rmsnorm_bwd_blocks((int64_t)rows) * d * 4);
   W.bytes = off;
   return W;
 }
@@ -203,6 +218,214 @@ tsp_status tsp_rank_mlp_step(const tsp_cfg* cfg, int32_t r, int32_t t, const flo
   o.out = last ? y_out : (void*)y_r; o.out_type = last ? OUT_BF16 : OUT_F32; o.ldo = d;
   o.name = "rank_gemm_w2";
   return gemm_tc(o, s);
+}
+
+// ---------------------------------------------------------------------------
+// The backward of the schedule (reading R17): the same shards in reverse.
+// ---------------------------------------------------------------------------
+
+tsp_status tsp_rank_mlp_bwd_step(const tsp_cfg* cfg, int32_t r, int32_t t, const float* h_r,
+                                 const void* g_mlp, const void* shard, const void* dy_r,
+                                 float* grad, float* db_r, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  tsp_status st = check_rank_cfg(cfg);
+  if (st != TSP_OK) return st;
+  if (r < 0 || r >= cfg->D || t < 0 || t >= cfg->D) return TSP_ERR_INVALID_ARG;
+  if (!al16(h_r) || !al16(g_mlp) || !al16(shard) || !al16(dy_r) || !al16(grad) || !al16(db_r))
+    return TSP_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, ws, ws_bytes)) != TSP_OK) return st;
+  const RankWs W = rank_layout(cfg, (uint8_t*)ws);
+  cudaStream_t s = S_(stream);
+  const int64_t rows = cfg->S / cfg->D;
+  const int d = cfg->d, I = cfg->inter, D = cfg->D;
+  const int sh = ((r - t) % D + D) % D;   // the shard rank r holds at ring step t
+  const int Is = (int)(bound(sh + 1, I, D) - bound(sh, I, D));
+  const size_t e = 2;
+  if (t == 0) {
+    if ((st = launch_rmsnorm_fwd(h_r, TY_F32, g_mlp, W.b, TY_F16, W.rstd2, rows, d, cfg->eps,
+                                 cfg->dtype, s)) != TSP_OK)
+      return st;
+    if ((st = launch_convert_bf16_f16(dy_r, W.dy16, rows * d, s)) != TSP_OK) return st;
+  }
+  if ((st = launch_convert_bf16_f16(shard, W.shard, (int64_t)3 * Is * d, s)) != TSP_OK) return st;
+  const uint8_t* w1s = (const uint8_t*)W.shard;
+  const uint8_t* w2t = w1s + (size_t)2 * Is * d * e;   // W_2[:, I_s]^T, [I_s, d]
+  {   // G and the pre-activations A | B of the held shard (recomputed)
+    TcGemm g;
+    g.M = (int)rows; g.N = Is; g.K = d;
+    g.A[0] = W.b; g.lda[0] = d; g.kseg_len[0] = d;
+    g.B[0] = w1s; g.B[1] = w1s + (size_t)Is * d * e; g.ldb[0] = g.ldb[1] = d;
+    g.paired = true; g.epi = EPI_SWIGLU; g.out = W.g; g.ldo = Is;
+    g.out2 = W.ab; g.ldo2 = 2 * (int64_t)Is;
+    g.out3 = (uint8_t*)W.ab + (size_t)Is * e; g.ldo3 = 2 * (int64_t)Is;
+    g.name = "rank_gemm_w13_recompute";
+    if ((st = gemm_tc(g, s)) != TSP_OK) return st;
+  }
+  {   // dG = dy W_2[:, I_s] -> dA | dB through the SwiGLU derivative
+    TcGemm g;
+    g.M = (int)rows; g.N = Is; g.K = d;
+    g.A[0] = W.dy16; g.lda[0] = d; g.kseg_len[0] = d;
+    g.B[0] = w2t; g.ldb[0] = d;
+    g.epi = EPI_SWIGLU_BWD; g.e1 = W.ab; g.e2 = (const uint8_t*)W.ab + (size_t)Is * e;
+    g.lde = 2 * (int64_t)Is;
+    g.out = W.dab; g.ldo = 2 * (int64_t)Is;
+    g.out2 = (uint8_t*)W.dab + (size_t)Is * e; g.ldo2 = 2 * (int64_t)Is;
+    g.name = "rank_gemm_dgrad_w2_swiglu";
+    if ((st = gemm_tc(g, s)) != TSP_OK) return st;
+  }
+  {   // db (+)= [dA | dB] [W_1[I_s]; W_3[I_s]]
+    TcGemm g;
+    g.M = (int)rows; g.N = d; g.K = 2 * Is;
+    g.A[0] = W.dab; g.lda[0] = 2 * Is; g.kseg_len[0] = 2 * Is;
+    g.b_mn = true; g.B[0] = w1s; g.ldb[0] = d;
+    if (t == 0) {
+      g.epi = EPI_F32;
+    } else {
+      g.epi = EPI_RES; g.res = db_r; g.res_f32 = true; g.ldr = d; g.out_type = OUT_F32;
+    }
+    g.out = db_r; g.ldo = d; g.name = "rank_gemm_dgrad_w13";
+    if ((st = gemm_tc(g, s)) != TSP_OK) return st;
+  }
+  {   // the shard's gradient (+)= this rank's rows: [dA | dB]^T b, then G^T dy
+    TcGemm g;
+    g.M = 2 * Is; g.N = d; g.K = (int)rows;
+    g.a_mn = true; g.A[0] = W.dab; g.lda[0] = 2 * Is; g.kseg_len[0] = (int)rows;
+    g.b_mn = true; g.B[0] = W.b; g.ldb[0] = d;
+    g.epi = EPI_RES; g.res = grad; g.res_f32 = true; g.ldr = d; g.out_type = OUT_F32;
+    g.out = grad; g.ldo = d; g.name = "rank_gemm_wgrad_w13";
+    if ((st = gemm_tc(g, s)) != TSP_OK) return st;
+    TcGemm g2;
+    float* g2out = grad + (size_t)2 * Is * d;
+    g2.M = Is; g2.N = d; g2.K = (int)rows;
+    g2.a_mn = true; g2.A[0] = W.g; g2.lda[0] = Is; g2.kseg_len[0] = (int)rows;
+    g2.b_mn = true; g2.B[0] = W.dy16; g2.ldb[0] = d;
+    g2.epi = EPI_RES; g2.res = g2out; g2.res_f32 = true; g2.ldr = d; g2.out_type = OUT_F32;
+    g2.out = g2out; g2.ldo = d; g2.name = "rank_gemm_wgrad_w2";
+    return gemm_tc(g2, s);
+  }
+}
+
+tsp_status tsp_rank_mlp_bwd_finish(const tsp_cfg* cfg, int32_t r, const float* h_r,
+                                   const void* g_mlp, const float* db_r, const void* dy_r,
+                                   float* dh_r, float* dg_mlp, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  tsp_status st = check_rank_cfg(cfg);
+  if (st != TSP_OK) return st;
+  if (r < 0 || r >= cfg->D) return TSP_ERR_INVALID_ARG;
+  if (!al16(h_r) || !al16(g_mlp) || !al16(db_r) || !al16(dy_r) || !al16(dh_r) || !al16(dg_mlp))
+    return TSP_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, ws, ws_bytes)) != TSP_OK) return st;
+  const RankWs W = rank_layout(cfg, (uint8_t*)ws);
+  const int64_t rows = cfg->S / cfg->D;
+  // dh = dy + RMSNorm_2 backward of db (fp32, and fp16 for the attention GEMMs)
+  return launch_rmsnorm_bwd(db_r, h_r, TY_F32, g_mlp, W.rstd2, nullptr, dy_r, dh_r, W.dh16, TY_F16,
+                            dg_mlp, W.dg_part, rows, cfg->d, cfg->dtype, S_(stream));
+}
+
+tsp_status tsp_rank_attn_bwd_heads(const tsp_cfg* cfg, int32_t r, int32_t k,
+                                   const void* kv_all_k, float* grad_k, void* dkv_k, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  tsp_status st = check_rank_cfg(cfg);
+  if (st != TSP_OK) return st;
+  if (r < 0 || r >= cfg->D || k < 0 || k >= cfg->D) return TSP_ERR_INVALID_ARG;
+  if (!al16(kv_all_k) || !al16(grad_k) || !al16(dkv_k)) return TSP_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, ws, ws_bytes)) != TSP_OK) return st;
+  const RankWs W = rank_layout(cfg, (uint8_t*)ws);
+  cudaStream_t s = S_(stream);
+  const int64_t rows = cfg->S / cfg->D;
+  const int d = cfg->d;
+  const int Ck = (int)(bound(k + 1, d, cfg->D) - bound(k, d, cfg->D));
+  const size_t e = 2;
+  // O and LSE of the rank's rows for shard k's heads (recomputed)
+  if ((st = launch_attn_fwd_rank_f16(W.q, Ck, kv_all_k, 2 * (int64_t)Ck, W.o, Ck, W.lse, cfg->S,
+                                     Ck / cfg->dh, cfg->dh, cfg->D, r, s)) != TSP_OK)
+    return st;
+  const uint8_t* wot = (const uint8_t*)W.shard + (size_t)3 * Ck * d * e;   // W_O[:, C_k]^T
+  {   // dO = dh W_O[:, C_k]
+    TcGemm g;
+    g.M = (int)rows; g.N = Ck; g.K = d;
+    g.A[0] = W.dh16; g.lda[0] = d; g.kseg_len[0] = d;
+    g.B[0] = wot; g.ldb[0] = d;
+    g.epi = EPI_STORE; g.out_type = OUT_F16; g.out = W.dO; g.ldo = Ck; g.name = "rank_gemm_dgrad_wo";
+    if ((st = gemm_tc(g, s)) != TSP_OK) return st;
+  }
+  {   // this rank's part of the gradient of W_O[:, C_k]^T: O^T dh
+    TcGemm g;
+    g.M = Ck; g.N = d; g.K = (int)rows;
+    g.a_mn = true; g.A[0] = W.o; g.lda[0] = Ck; g.kseg_len[0] = (int)rows;
+    g.b_mn = true; g.B[0] = W.dh16; g.ldb[0] = d;
+    g.epi = EPI_F32; g.out = grad_k + (size_t)3 * Ck * d; g.ldo = d; g.name = "rank_gemm_wgrad_wo";
+    if ((st = gemm_tc(g, s)) != TSP_OK) return st;
+  }
+  // the rank's query rows back-propagated: dQ (kept), dK | dV of every key
+  return launch_attn_bwd_rank_f16(W.q, kv_all_k, W.o, W.dO, W.lse, W.delta, W.dq_acc, W.dq, dkv_k,
+                                  cfg->S, Ck / cfg->dh, cfg->dh, cfg->D, r, s);
+}
+
+tsp_status tsp_rank_attn_bwd_weights(const tsp_cfg* cfg, int32_t r, int32_t k,
+                                     const void* dkv_own, float* grad_k, float* da_r, void* ws,
+                                     size_t ws_bytes, void* stream) {
+  tsp_status st = check_rank_cfg(cfg);
+  if (st != TSP_OK) return st;
+  if (r < 0 || r >= cfg->D || k < 0 || k >= cfg->D) return TSP_ERR_INVALID_ARG;
+  if (!al16(dkv_own) || !al16(grad_k) || !al16(da_r)) return TSP_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, ws, ws_bytes)) != TSP_OK) return st;
+  const RankWs W = rank_layout(cfg, (uint8_t*)ws);
+  cudaStream_t s = S_(stream);
+  const int64_t rows = cfg->S / cfg->D;
+  const int d = cfg->d;
+  const int Ck = (int)(bound(k + 1, d, cfg->D) - bound(k, d, cfg->D));
+  const size_t e = 2;
+  {   // this rank's part of the gradients of W_Q[C_k], then W_K[C_k] | W_V[C_k]
+    TcGemm g;
+    g.M = Ck; g.N = d; g.K = (int)rows;
+    g.a_mn = true; g.A[0] = W.dq; g.lda[0] = Ck; g.kseg_len[0] = (int)rows;
+    g.b_mn = true; g.B[0] = W.a; g.ldb[0] = d;
+    g.epi = EPI_F32; g.out = grad_k; g.ldo = d; g.name = "rank_gemm_wgrad_q";
+    if ((st = gemm_tc(g, s)) != TSP_OK) return st;
+    TcGemm g2;
+    g2.M = 2 * Ck; g2.N = d; g2.K = (int)rows;
+    g2.a_mn = true; g2.A[0] = dkv_own; g2.lda[0] = 2 * Ck; g2.kseg_len[0] = (int)rows;
+    g2.b_mn = true; g2.B[0] = W.a; g2.ldb[0] = d;
+    g2.epi = EPI_F32; g2.out = grad_k + (size_t)Ck * d; g2.ldo = d; g2.name = "rank_gemm_wgrad_kv";
+    if ((st = gemm_tc(g2, s)) != TSP_OK) return st;
+  }
+  // da (+)= dQ W_Q[C_k] + [dK | dV] [W_K[C_k]; W_V[C_k]]: two K segments
+  TcGemm g;
+  g.M = (int)rows; g.N = d; g.K = 3 * Ck; g.nks = 2;
+  g.A[0] = W.dq; g.lda[0] = Ck; g.kseg_len[0] = Ck;
+  g.A[1] = dkv_own; g.lda[1] = 2 * Ck; g.kseg_len[1] = 2 * Ck;
+  g.b_mn = true; g.B[0] = W.shard; g.B[1] = (const uint8_t*)W.shard + (size_t)Ck * d * e;
+  g.ldb[0] = g.ldb[1] = d;
+  if (k == 0) {
+    g.epi = EPI_F32;
+  } else {
+    g.epi = EPI_RES; g.res = da_r; g.res_f32 = true; g.ldr = d; g.out_type = OUT_F32;
+  }
+  g.out = da_r; g.ldo = d; g.name = "rank_gemm_dgrad_qkv";
+  return gemm_tc(g, s);
+}
+
+tsp_status tsp_rank_attn_bwd_finish(const tsp_cfg* cfg, int32_t r, const void* x_r,
+                                    const void* g_attn, const float* da_r, const float* dh_r,
+                                    float* dx_r, float* dg_attn, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  tsp_status st = check_rank_cfg(cfg);
+  if (st != TSP_OK) return st;
+  if (r < 0 || r >= cfg->D) return TSP_ERR_INVALID_ARG;
+  if (!al16(x_r) || !al16(g_attn) || !al16(da_r) || !al16(dh_r) || !al16(dx_r) || !al16(dg_attn))
+    return TSP_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, ws, ws_bytes)) != TSP_OK) return st;
+  const RankWs W = rank_layout(cfg, (uint8_t*)ws);
+  cudaStream_t s = S_(stream);
+  const int64_t rows = cfg->S / cfg->D;
+  // rstd of the first norm (the forward kept only its output)
+  if ((st = launch_rmsnorm_fwd(x_r, TY_BF16, g_attn, W.a, TY_F16, W.rstd1, rows, cfg->d, cfg->eps,
+                               cfg->dtype, s)) != TSP_OK)
+    return st;
+  // dx = dh + RMSNorm_1 backward of da
+  return launch_rmsnorm_bwd(da_r, x_r, TY_BF16, g_attn, W.rstd1, dh_r, nullptr, dx_r, nullptr,
+                            TY_BF16, dg_attn, W.dg_part, rows, cfg->d, cfg->dtype, s);
 }
 
 }  // extern "C"

@@ -212,6 +212,50 @@ class LocalComm:
             self.stream.wait_event(self.m_copied[b])
         return out
 
+    # --- backward exchanges (on this GPU: copies, and the sums the collectives form)
+    def ring_pass_with_grad(self, t, held, grad):
+        if not hasattr(self, "grad_rx"):
+            wI = max(self.Ib[s + 1] - self.Ib[s] for s in range(self.D))
+            dev = self.attn_packed.device
+            self.grad_rx = [[tsp.empty((3 * wI, self.cfg.d), torch.float32, dev) for _ in range(2)]
+                            for _ in range(self.D)]
+        b = (t + 1) & 1
+        out_s, out_g = {}, {}
+        with torch.cuda.stream(self.stream):
+            for r in self.local_ranks():
+                src, gsrc = held[(r - 1) % self.D], grad[(r - 1) % self.D]
+                dst = self.mlp_rx[r][b][:src.shape[0]]
+                gdst = self.grad_rx[r][b][:gsrc.shape[0]]
+                dst.copy_(src)
+                gdst.copy_(gsrc)
+                out_s[r], out_g[r] = dst, gdst
+        return out_s, out_g
+
+    def keep_mlp_grads(self, grad):
+        self.mlp_grads = {r: g.clone() for r, g in grad.items()}   # rank r: its own shard's gradient
+
+    def reduce_scatter_kv(self, k, dkv):
+        rows = self.cfg.S // self.D
+        with torch.cuda.stream(self.stream):
+            total = None
+            for p in dkv.values():
+                total = p.float() if total is None else total + p.float()
+            return {r: total[r * rows:(r + 1) * rows].to(torch.float16).contiguous()
+                    for r in self.local_ranks()}
+
+    def reduce_attn_grad(self, k, gparts):
+        if not hasattr(self, "attn_grads"):
+            self.attn_grads = {}
+        with torch.cuda.stream(self.stream):
+            acc = None
+            for g in gparts.values():
+                acc = g.clone() if acc is None else acc + g
+            self.attn_grads[k] = acc        # summed at the owner, rank k
+
+    def all_reduce_gains(self, g):
+        with torch.cuda.stream(self.stream):
+            self.gains = sum(v for v in g.values())
+
 
 class GpuRankOps:
     """One rank's computation in the library's kernels, for the ranks in
@@ -253,6 +297,59 @@ class GpuRankOps:
     def output(self, r):
         return self.out[r]
 
+    # --- backward (schedule.backward), after the forward ran on this object
+    def set_dy(self, r, dy_r):
+        if not hasattr(self, "dy"):
+            dev, cfg = self.x[r].device, self.cfg
+            b = shard_bounds(cfg.d, cfg.D)
+            wC = max(hi - lo for lo, hi in zip(b[:-1], b[1:]))
+            bi = shard_bounds(cfg.inter, cfg.D)
+            wI = max(hi - lo for lo, hi in zip(bi[:-1], bi[1:]))
+            f32 = torch.float32
+            mk = lambda shape, dt=f32: {q: tsp.empty(shape, dt, dev) for q in self.x}
+            self.dy = {}
+            self.db, self.dh, self.da, self.dxr = (mk((self.rows, cfg.d)) for _ in range(4))
+            self.dgm, self.dga = mk((cfg.d,)), mk((cfg.d,))
+            self.dkv = mk((cfg.S, 2 * wC), torch.float16)
+            self.gk = mk((4 * wC, cfg.d))
+            self.g0 = mk((3 * wI, cfg.d))
+        self.dy[r] = dy_r
+
+    def mlp_bwd_step(self, r, t, shard, g):
+        if g is None:                        # the first holder starts the shard's gradient
+            g = self.g0[r][:shard.shape[0]]
+            g.zero_()
+        tsp.rank_mlp_bwd_step(self.cfg, r, t, self.h[r], self.W.g_mlp, shard, self.dy[r], g,
+                              self.db[r], self.ws[r], self.stream)
+        return g
+
+    def mlp_bwd_finish(self, r):
+        tsp.rank_mlp_bwd_finish(self.cfg, r, self.h[r], self.W.g_mlp, self.db[r], self.dy[r],
+                                self.dh[r], self.dgm[r], self.ws[r], self.stream)
+
+    def attn_bwd_heads(self, r, k, kv_all):
+        Ck = kv_all.shape[1] // 2
+        dkv = self.dkv[r].view(-1)[:self.cfg.S * 2 * Ck].view(self.cfg.S, 2 * Ck)
+        gk = self.gk[r].view(-1)[:4 * Ck * self.cfg.d].view(4 * Ck, self.cfg.d)
+        tsp.rank_attn_bwd_heads(self.cfg, r, k, kv_all, gk, dkv, self.ws[r], self.stream)
+        return dkv
+
+    def attn_bwd_weights(self, r, k, dkv_own):
+        Ck = dkv_own.shape[1] // 2
+        gk = self.gk[r].view(-1)[:4 * Ck * self.cfg.d].view(4 * Ck, self.cfg.d)
+        tsp.rank_attn_bwd_weights(self.cfg, r, k, dkv_own, gk, self.da[r], self.ws[r], self.stream)
+        return gk
+
+    def attn_bwd_finish(self, r):
+        tsp.rank_attn_bwd_finish(self.cfg, r, self.x[r], self.W.g_attn, self.da[r], self.dh[r],
+                                 self.dxr[r], self.dga[r], self.ws[r], self.stream)
+
+    def gain_grads(self, r):
+        return torch.cat([self.dga[r], self.dgm[r]])
+
+    def dx(self, r):
+        return self.dxr[r]
+
 
 def block_fwd_by_schedule(cfg, x_z, W: tsp.BlockWeights, stream=None, overlap=False):
     """y_z of the block computed rank by rank by the schedule, all D virtual
@@ -291,6 +388,35 @@ class OneRankComm(LocalComm):
         full[self.r0] = held[self.r0]
         out = super().ring_pass(t, full)
         return {self.r0: out[self.r0]}
+
+
+def block_bwd_by_schedule(cfg, x_z, dy_z, W: tsp.BlockWeights, stream=None):
+    """The block's gradients computed rank by rank by the forward and backward
+    schedule, all D virtual ranks on this GPU: the same dict as tsp.block_bwd
+    (dx_z fp32 in the zigzag layout, weight and gain gradients fp32), each
+    shard's weight gradient taken from its owner."""
+    D, d, rows = cfg.D, cfg.d, cfg.S // cfg.D
+    comm = LocalComm(cfg, W, stream)
+    ops = GpuRankOps(cfg, W, {r: x_z[r * rows:(r + 1) * rows] for r in range(D)}, stream)
+    forward(comm, ops, D)
+    for r in range(D):
+        ops.set_dy(r, dy_z[r * rows:(r + 1) * rows])
+    dx = backward(comm, ops, D)
+    dev = x_z.device
+    g = {n: torch.zeros(shape, dtype=torch.float32, device=dev) for n, shape in
+         (("dwq", (d, d)), ("dwk", (d, d)), ("dwv", (d, d)), ("dwo", (d, d)),
+          ("dw1", (cfg.inter, d)), ("dw3", (cfg.inter, d)), ("dw2", (d, cfg.inter)))}
+    Cb, Ib = shard_bounds(d, D), shard_bounds(cfg.inter, D)
+    for k in range(D):
+        n, C, a = Cb[k + 1] - Cb[k], slice(Cb[k], Cb[k + 1]), comm.attn_grads[k]
+        g["dwq"][C], g["dwk"][C], g["dwv"][C] = a[:n], a[n:2 * n], a[2 * n:3 * n]
+        g["dwo"][:, C] = a[3 * n:4 * n].T
+        m, I, b = Ib[k + 1] - Ib[k], slice(Ib[k], Ib[k + 1]), comm.mlp_grads[k]
+        g["dw1"][I], g["dw3"][I] = b[:m], b[m:2 * m]
+        g["dw2"][:, I] = b[2 * m:3 * m].T
+    g["dg_attn"], g["dg_mlp"] = comm.gains[:d].clone(), comm.gains[d:].clone()
+    g["dx"] = torch.cat([dx[r] for r in range(D)], 0)
+    return g
 
 
 def _time_main():

@@ -34,7 +34,9 @@ EXPORTED = ("tsp_zigzag_permute", "tsp_rmsnorm_fwd", "tsp_workspace_bytes", "tsp
             "tsp_debug_skip_stage", "tsp_block_weights_bytes", "tsp_block_weights_prepare",
             "tsp_block_fwd_prepared", "tsp_block_bwd_prepared", "tsp_stack_fwd_prepared",
             "tsp_stack_bwd_prepared", "tsp_pack_mlp_shards", "tsp_rank_workspace_bytes",
-            "tsp_rank_attn_project", "tsp_rank_attn_heads", "tsp_rank_mlp_step")
+            "tsp_rank_attn_project", "tsp_rank_attn_heads", "tsp_rank_mlp_step",
+            "tsp_rank_mlp_bwd_step", "tsp_rank_mlp_bwd_finish", "tsp_rank_attn_bwd_heads",
+            "tsp_rank_attn_bwd_weights", "tsp_rank_attn_bwd_finish")
 DECODE_MAX_T = 8   # TSP_DECODE_MAX_T
 
 
@@ -103,6 +105,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "tsp_rank_attn_project": (i32, [P(Cfg), i32, i32, vp, vp, vp, vp, vp, sz, vp]),
         "tsp_rank_attn_heads": (i32, [P(Cfg), i32, i32, vp, vp, vp, vp, sz, vp]),
         "tsp_rank_mlp_step": (i32, [P(Cfg), i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "tsp_rank_mlp_bwd_step": (i32, [P(Cfg), i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "tsp_rank_mlp_bwd_finish": (i32, [P(Cfg), i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "tsp_rank_attn_bwd_heads": (i32, [P(Cfg), i32, i32, vp, vp, vp, vp, sz, vp]),
+        "tsp_rank_attn_bwd_weights": (i32, [P(Cfg), i32, i32, vp, vp, vp, vp, sz, vp]),
+        "tsp_rank_attn_bwd_finish": (i32, [P(Cfg), i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "tsp_gated_mlp_fwd_noalloc": (i32, [P(Cfg), vp, P(MlpW), vp, vp]),
         "tsp_stack_saved_bytes": (sz, [P(Cfg), i32]),
         "tsp_stack_workspace_bytes": (sz, [P(Cfg), i32, i32]),
@@ -513,6 +520,39 @@ def rank_mlp_step(cfg: Cfg, r: int, t: int, h_r, g_mlp, shard, y_r, y_out, ws, s
     _check(load().tsp_rank_mlp_step(ctypes.byref(cfg), r, t, _ptr(h_r), _ptr(g_mlp), _ptr(shard),
                                     _ptr(y_r), _ptr(y_out), _ptr(ws), ws.numel(), _stream(stream)),
            "tsp_rank_mlp_step")
+
+
+def rank_mlp_bwd_step(cfg: Cfg, r: int, t: int, h_r, g_mlp, shard, dy_r, grad, db_r, ws,
+                      stream=None):
+    _check(load().tsp_rank_mlp_bwd_step(ctypes.byref(cfg), r, t, _ptr(h_r), _ptr(g_mlp),
+                                        _ptr(shard), _ptr(dy_r), _ptr(grad), _ptr(db_r), _ptr(ws),
+                                        ws.numel(), _stream(stream)), "tsp_rank_mlp_bwd_step")
+
+
+def rank_mlp_bwd_finish(cfg: Cfg, r: int, h_r, g_mlp, db_r, dy_r, dh_r, dg_mlp, ws, stream=None):
+    _check(load().tsp_rank_mlp_bwd_finish(ctypes.byref(cfg), r, _ptr(h_r), _ptr(g_mlp), _ptr(db_r),
+                                          _ptr(dy_r), _ptr(dh_r), _ptr(dg_mlp), _ptr(ws),
+                                          ws.numel(), _stream(stream)), "tsp_rank_mlp_bwd_finish")
+
+
+def rank_attn_bwd_heads(cfg: Cfg, r: int, k: int, kv_all_k, grad_k, dkv_k, ws, stream=None):
+    _check(load().tsp_rank_attn_bwd_heads(ctypes.byref(cfg), r, k, _ptr(kv_all_k), _ptr(grad_k),
+                                          _ptr(dkv_k), _ptr(ws), ws.numel(), _stream(stream)),
+           "tsp_rank_attn_bwd_heads")
+
+
+def rank_attn_bwd_weights(cfg: Cfg, r: int, k: int, dkv_own, grad_k, da_r, ws, stream=None):
+    _check(load().tsp_rank_attn_bwd_weights(ctypes.byref(cfg), r, k, _ptr(dkv_own), _ptr(grad_k),
+                                            _ptr(da_r), _ptr(ws), ws.numel(), _stream(stream)),
+           "tsp_rank_attn_bwd_weights")
+
+
+def rank_attn_bwd_finish(cfg: Cfg, r: int, x_r, g_attn, da_r, dh_r, dx_r, dg_attn, ws,
+                         stream=None):
+    _check(load().tsp_rank_attn_bwd_finish(ctypes.byref(cfg), r, _ptr(x_r), _ptr(g_attn),
+                                           _ptr(da_r), _ptr(dh_r), _ptr(dx_r), _ptr(dg_attn),
+                                           _ptr(ws), ws.numel(), _stream(stream)),
+           "tsp_rank_attn_bwd_finish")
 
 
 def device_status(reset: bool = True, stream=None) -> int:

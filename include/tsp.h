@@ -440,6 +440,59 @@ tsp_status tsp_rank_mlp_step(const tsp_cfg* cfg, int32_t r, int32_t t, const flo
                              const void* g_mlp, const void* shard, float* y_r, void* y_out,
                              void* ws, size_t ws_bytes, void* stream);
 
+/* ---- The backward of the per-rank schedule ----------------------------------
+ * The pages describe the forward only; the backward moves the same shards in
+ * reverse (same page, section 2, read as follows).  Per block, after the
+ * forward calls above ran for rank r with the same `ws`:
+ *
+ *   for t = 0 .. D-1:   (the ring again; the shard's gradient travels with it)
+ *     tsp_rank_mlp_bwd_step(r, t, h_r, g_mlp, mlp_shard_{(r-t) mod D}, dy_r, grad, db_r)
+ *     pass (shard, grad) to rank r+1       (D passes: the last one home)
+ *   tsp_rank_mlp_bwd_finish(r, h_r, g_mlp, db_r, dy_r -> dh_r, dg_mlp part)
+ *   for k = 0 .. D-1:   (the attention shards broadcast again)
+ *     tsp_rank_attn_project(r, k, x_r, g_attn, attn_shard_k -> kv_k)   (as forward)
+ *     all-gather kv_k -> kv_all_k
+ *     tsp_rank_attn_bwd_heads(r, k, kv_all_k -> grad_k[W_O part], dkv_k)
+ *     reduce-scatter the ranks' dkv_k -> dkv_own_r (own rows, summed)
+ *     tsp_rank_attn_bwd_weights(r, k, dkv_own_r -> grad_k[Q|K|V parts], da_r)
+ *     reduce grad_k to its owner, rank k
+ *   tsp_rank_attn_bwd_finish(r, x_r, g_attn, da_r, dh_r -> dx_r, dg_attn part)
+ *   all-reduce the gain gradients
+ *
+ * Shapes and layouts (rows = 2c, Ck / Is the shard widths, fp32 unless noted):
+ *   dy_r [rows, d] bf16;  db_r, dh_r, da_r, dx_r [rows, d];
+ *   grad (MLP shard gradient, packed like the shard) [3*Is, d]: rows 0..Is-1
+ *     dW_1[I_s], then dW_3[I_s], then dW_2[:, I_s]^T; ACCUMULATED into (the
+ *     first holder's buffer must be zero);  db_r written at t = 0, then
+ *     accumulated;
+ *   grad_k (attention shard gradient, packed like the shard) [4*Ck, d]:
+ *     dW_Q[C_k], dW_K[C_k], dW_V[C_k], dW_O[:, C_k]^T, this rank's rows' part,
+ *     OVERWRITTEN (the W_O part by ..._heads, the rest by ..._weights);
+ *   dkv_k [S, 2*Ck] fp16, zigzag row order: dK | dV of every key from this
+ *     rank's queries (zero where none reaches);  dkv_own_r [rows, 2*Ck]
+ *     fp16: the sum over all ranks of their dkv_k at rank r's rows;
+ *   da_r written at k = 0, then accumulated;  dg_mlp, dg_attn [d]: this
+ *     rank's part (sum over ranks for the gain gradient).
+ * Errors as for the forward per-rank calls. */
+tsp_status tsp_rank_mlp_bwd_step(const tsp_cfg* cfg, int32_t r, int32_t t, const float* h_r,
+                                 const void* g_mlp, const void* shard, const void* dy_r,
+                                 float* grad, float* db_r, void* ws, size_t ws_bytes,
+                                 void* stream);
+tsp_status tsp_rank_mlp_bwd_finish(const tsp_cfg* cfg, int32_t r, const float* h_r,
+                                   const void* g_mlp, const float* db_r, const void* dy_r,
+                                   float* dh_r, float* dg_mlp, void* ws, size_t ws_bytes,
+                                   void* stream);
+tsp_status tsp_rank_attn_bwd_heads(const tsp_cfg* cfg, int32_t r, int32_t k,
+                                   const void* kv_all_k, float* grad_k, void* dkv_k, void* ws,
+                                   size_t ws_bytes, void* stream);
+tsp_status tsp_rank_attn_bwd_weights(const tsp_cfg* cfg, int32_t r, int32_t k,
+                                     const void* dkv_own, float* grad_k, float* da_r, void* ws,
+                                     size_t ws_bytes, void* stream);
+tsp_status tsp_rank_attn_bwd_finish(const tsp_cfg* cfg, int32_t r, const void* x_r,
+                                    const void* g_attn, const float* da_r, const float* dh_r,
+                                    float* dx_r, float* dg_attn, void* ws, size_t ws_bytes,
+                                    void* stream);
+
 /* Reads (and with reset != 0 clears) the sticky device status word.  Waits
  * for `stream` to finish.  Returns TSP_OK or the first device error seen
  * (TSP_ERR_TIMEOUT or TSP_ERR_RANGE). */

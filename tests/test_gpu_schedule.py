@@ -96,3 +96,59 @@ def test_rank_calls_reject_what_they_do_not_take():
         tsp.rank_attn_project(bf, 0, 0, x, x, x, x, ws)                # workspace too small
     assert e.value.code == tsp.TSP_ERR_INVALID_ARG
     assert np.isfinite(tsp.rank_workspace_bytes(bf))
+
+
+@pytest.mark.parametrize("S,d,H,I,D", [(4096, 1024, 8, 2048, 4), (2048, 512, 4, 1024, 2),
+                                       (4096, 1024, 8, 2048, 1)])
+def test_backward_schedule_by_rank_matches_oracle(S, d, H, I, D):
+    """The training step rank by rank: the forward schedule, then its reverse
+    (schedule.backward: the MLP ring carrying each shard's gradient home, the
+    attention shards re-broadcast, the K|V re-gathered, the dK|dV
+    reduce-scatter, each shard's gradient summed at its owner, the gains
+    all-reduced), every rank's steps in the tsp_rank_* kernels including the
+    one-rank attention backward.  Every gradient against the dense float64
+    backward."""
+    shape = BlockShape(S=S, d=d, H=H, inter=I, D=D)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=S + D + 1, with_dy=True)
+    cfg = tsp.make_cfg(S, d, H, I, D, torch.bfloat16, shape.eps)
+    W = tsp.BlockWeights.from_dict(inp, "cuda")
+    xz = tsp.zigzag_permute(inp["x"].cuda(), D)
+    dyz = tsp.zigzag_permute(inp["dy"].cuda(), D)
+    g = schedule.block_bwd_by_schedule(cfg, xz, dyz, W)
+    g["dx"] = tsp.zigzag_permute(g["dx"], D, inverse=True)
+    torch.cuda.synchronize()
+    assert tsp.device_status() == tsp.TSP_OK
+    ref = O.block_bwd(inp["x"], inp, inp["dy"], H, shape.eps)
+    for k, v in ref.items():
+        assert_bf16_close(g[k].cpu(), v, f"{k} by rank (S={S}, D={D})")
+
+
+def test_backward_schedule_by_rank_7b_shapes_S8192_sparse_dy():
+    """d=4096, 32 heads x 128, inter=11008, D=8 (4 heads and 1376 MLP rows a
+    shard) at S=8192, with dy on 256 seeded rows: every gradient of the
+    rank-by-rank training step against the oracle's exact backward for such a
+    dy (block_bwd_rows); dx row by row off the dy rows, as in the batched
+    full-size test."""
+    S, D = 8192, 8
+    shape = BlockShape(S=S, d=4096, H=32, inter=11008, D=D)
+    inp = make_block_inputs(shape, torch.bfloat16, seed=11, with_dy=True)
+    rows = np.sort(sample_rows(S, D).numpy())
+    dy = torch.zeros_like(inp["dy"])
+    dy[torch.from_numpy(rows)] = inp["dy"][torch.from_numpy(rows)]
+    cfg = tsp.make_cfg(S, shape.d, shape.H, shape.inter, D, torch.bfloat16, shape.eps)
+    W = tsp.BlockWeights.from_dict(inp, "cuda")
+    g = schedule.block_bwd_by_schedule(cfg, tsp.zigzag_permute(inp["x"].cuda(), D),
+                                       tsp.zigzag_permute(dy.cuda(), D), W)
+    g["dx"] = tsp.zigzag_permute(g["dx"], D, inverse=True)
+    torch.cuda.synchronize()
+    assert tsp.device_status() == tsp.TSP_OK
+    ref = O.block_bwd_rows(inp["x"], inp, O.f64(dy)[rows], rows, shape.H, shape.eps)
+    dx, dx_ref = O.f64(g.pop("dx").cpu()), ref.pop("dx")
+    assert_bf16_close(torch.from_numpy(dx[rows]), dx_ref[rows], "dx at the dy rows, by rank")
+    other = np.setdiff1d(np.arange(S), rows)
+    a, b = dx[other], dx_ref[other]
+    row_rms = np.sqrt(np.mean(b * b, axis=1))
+    floor = 1e-6 * float(np.sqrt(np.mean(b * b)))
+    assert float(np.max(np.abs(a - b).max(axis=1) / (row_rms + floor))) <= 2e-2
+    for k, v in ref.items():
+        assert_bf16_close(g[k].cpu(), v, f"{k} by rank, 7B shapes, dy on 256 rows")
