@@ -484,6 +484,20 @@ def _time_main():
         res[key] = timed(lambda: forward(comm, ops, a.D), True)
         if not torch.equal(ops.output(0), y_ref):
             raise RuntimeError("one rank's schedule differs from the full run")
+    # the training step: one pass (tsp_block_fwd + tsp_block_bwd) against all D
+    # ranks' schedule steps run one after another on this GPU (so 1/D of it is
+    # one rank's work), both replayed from CUDA graphs
+    dyz = tsp.zigzag_permute(make_block_inputs(shape, torch.bfloat16, seed=1, with_dy=True)["dy"]
+                             .cuda(), a.D)
+    saved = tsp.empty(tsp.saved_bytes(cfg), torch.uint8, "cuda")
+
+    def one_pass_train():
+        tsp.block_fwd(cfg, xz, W, saved=saved)
+        tsp.block_bwd(cfg, xz, dyz, saved, W)
+
+    res["train_one_pass_per_rank_ms"] = timed(one_pass_train, True) / a.D
+    res["train_by_rank_per_rank_ms"] = timed(
+        lambda: block_bwd_by_schedule(cfg, xz, dyz, W), True) / a.D
     if tsp.device_status() != tsp.TSP_OK:
         raise RuntimeError("device status not OK")
     print(json.dumps(res))
