@@ -32,6 +32,12 @@ int current_device();
 bool take_debug_skip();
 // Default limit of one pipeline wait, in nanoseconds of %globaltimer.
 uint64_t wait_limit_ns();
+// Tensor map of a row-major fp16 matrix [outer, inner] with row stride ld
+// elements: box {64 inner, box_outer}, 128-byte swizzle, zero fill out of
+// bounds (cuTensorMapEncodeTiled, looked up once from the driver).  False if
+// the driver lacks the call or rejects the layout.
+bool tma_map_f16(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld,
+                 int box_outer);
 
 // Launch accounting (api.cu): counts the kernels of one launch site and,
 // while profiling is enabled (tsp_profile_enable), brackets them with CUDA

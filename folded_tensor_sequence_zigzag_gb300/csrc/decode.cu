@@ -13,15 +13,22 @@
 //    Q and K plus the append of K|V to the cache).  A warp streams groups of
 //    NR output rows, walking K with 16-byte non-allocating loads (four in
 //    flight per row); x sits in shared memory.
-//  * decode_attn_kernel: one CTA per (K/V head, split of 128 cache rows).
+//  * attention of the new tokens over the cache, in splits of 128 cache rows.
 //    The splits never straddle a virtual rank's 2c zigzag rows, so each
 //    rank's partial attention over the K/V it owns is formed where that K/V
 //    lives (the decode counterpart of the prefill's K/V all-gather); the
 //    decoded tokens' own rows, appended after the prompt, form the last
-//    splits.  A lane owns a key: its K row goes straight to registers (read
-//    16 bytes a lane, coalesced) while the warp's V rows are staged in its
-//    shared-memory slice by cp.async; the query rows of a K/V head group are
-//    split over a few CTAs when the heads and splits alone give too few.
+//    splits.  Three kernels:
+//    - decode_attn_stream_kernel (fp16 cache, at most 4 query rows per K/V
+//      head): one wave of CTAs, each walking a slice of the splits with its
+//      warps' rows staged by cp.async three splits deep, the dot products on
+//      the tensor cores (mma.sync) and an online softmax;
+//    - decode_attn_mma_kernel (fp16 cache, more query rows): a CTA per
+//      (K/V head, split), the head group's query rows all in that CTA, so
+//      every cache row is read once;
+//    - decode_attn_kernel (fp32 cache): a lane per key, K read to registers,
+//      V staged by cp.async; the query rows of a K/V head group are split
+//      over a few CTAs when the heads and splits alone give too few.
 //  * decode_combine_kernel: merges the splits' (max, sum, unnormalised O) by
 //    their log-sum-exp into O [T, d].
 #include <cuda_bf16.h>
@@ -333,6 +340,7 @@ tsp_status gemv_epi(const GemvArgs& ga, int epi, const char* name, cudaStream_t 
 // ----------------------------------------------------------------------------
 
 struct AttnArgs {
+  CUtensorMap tm;        // streaming kernel: the cache [n_total, ldkv], box {64, 32}, 128B swizzle
   const void* q;
   int64_t ldq;
   const void* kv;
@@ -342,8 +350,10 @@ struct AttnArgs {
   int64_t S, c, n_cached, n_total;
   int D, spr, nsplit, T, H, G, dkv;   // spr: splits per rank
   int nz, qpc;   // query-row groups per (K/V head, split); query rows per group
+  int nslice;    // streaming kernel: CTAs per K/V head, each over a slice of the splits
   float scale_log2;
   int* status;   // sticky device status word (checked build: TSP_ERR_BOUNDS)
+  uint64_t limit_ns;   // bound of one wait (streaming kernel)
 };
 
 // cache rows [r0, r1) of split `s`: splits 0 .. D*spr-1 cut each rank's 2c
@@ -785,6 +795,293 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) decode_attn_mma_kernel(con
   }
 }
 
+// Streaming variant for at most kQB query rows per K/V head (one decoded
+// token, or a few with grouped heads): the grid is one wave, nslice CTAs per
+// K/V head (a CTA an SM), and CTA p walks the splits
+// [p*nsplit/nslice, (p+1)*nsplit/nslice).  Each warp takes its 32 rows of
+// every split in turn through a ring of kStreamStages shared-memory stages
+// that one lane fills with tensor copies (TMA: 64-column boxes of 32 rows,
+// 128-byte swizzle, an mbarrier a stage), kStreamStages - 1 splits ahead of
+// the one its MMAs work on, and keeps a running (max, sum, O) per query row
+// -- the online softmax of the flash-attention forward.  The cache streams
+// without CTAs starting and ending in waves, and a warp spends no issue slots
+// on copy addresses.  Every CTA writes one partial per query row; the combine
+// kernel merges the nslice partials.
+constexpr int kStreamStages = 3;
+template <int DH>
+struct StreamSmem {
+  static constexpr int BOX_BYTES = 32 * 128;                  // 32 rows x 64 fp16 columns
+  static constexpr int KV_BYTES = (DH / 64) * BOX_BYTES;      // a warp's K (or V) rows
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;            // K boxes, then V boxes
+  static constexpr int WARP_BYTES = kStreamStages * STAGE_BYTES;
+  static constexpr int OFF_Q = kAttnWarps * WARP_BYTES;       // staged query rows (MmaSmem layout)
+  static constexpr int OFF_BAR = OFF_Q + MmaSmem<DH>::Q_BYTES;
+  static constexpr int BYTES = OFF_BAR + kAttnWarps * kStreamStages * 8 + 1024;  // + alignment
+  // byte offset of 16-byte piece c (of DH/8) of staged row r in a K or V part
+  static __device__ __forceinline__ uint32_t at(int r, int c) {
+    return (uint32_t)((c >> 3) * BOX_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+  }
+};
+
+// Waits for phase `parity` of a stage's barrier for at most limit_ns; on
+// time-out records TSP_ERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, int* status,
+                                           uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > limit_ns) {
+      report_timeout(status);
+      return false;
+    }
+  }
+  return true;
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kAttnWarps * 32, 1)
+    decode_attn_stream_kernel(const __grid_constant__ AttnArgs a) {
+  using L = MmaSmem<DH>;
+  using SL = StreamSmem<DH>;
+  constexpr int NT = DH / 8;                    // n8 tiles of O (dh)
+  extern __shared__ __align__(16) uint8_t mma_smem[];
+  __shared__ __align__(16) float ro[kAttnWarps][kQB][DH];
+  __shared__ float2 rml[kAttnWarps][kQB];
+
+  const int g = blockIdx.x, p = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;      // MMA fragment row group and thread in it
+  const int s_lo = (int)((int64_t)p * a.nsplit / a.nslice);
+  const int s_hi = (int)((int64_t)(p + 1) * a.nsplit / a.nslice);
+  const int nq = a.G * a.T;                     // <= kQB (host-checked)
+  // the 128-byte swizzle repeats every 1024 bytes: boxes start on that boundary
+  const uint32_t raw = smem_u32(mma_smem);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = mma_smem + (sbase - raw);
+  const uint32_t wsm = sbase + (uint32_t)(warp * SL::WARP_BYTES);
+  const uint32_t qsm = sbase + (uint32_t)SL::OFF_Q;
+  const uint32_t wbar = sbase + (uint32_t)SL::OFF_BAR + (uint32_t)(warp * kStreamStages * 8);
+  if (lane == 0) {
+    for (int st = 0; st < kStreamStages; ++st) mbar_init(wbar + 8u * st, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  // split cursors: (s, rank, piece) walked forward one split at a time, so
+  // the rows of a split cost no division; a warp with no rows in a split
+  // neither loads nor waits for it
+  struct Cur {
+    int s, r, j;
+  };
+  auto start = [&](int s) {
+    Cur c{s, a.D, 0};
+    if (s < a.D * a.spr) {
+      c.r = s / a.spr;
+      c.j = s - c.r * a.spr;
+    }
+    return c;
+  };
+  auto next = [&](Cur& c) {
+    ++c.s;
+    if (c.r < a.D && ++c.j == a.spr) {
+      c.j = 0;
+      ++c.r;
+    }
+  };
+  auto rows_of = [&](const Cur& c, int64_t& r0, int64_t& r1) -> bool {
+    if (c.r < a.D) {
+      const int64_t rank0 = (int64_t)c.r * 2 * a.c;
+      r0 = rank0 + (int64_t)c.j * kSplitRows;
+      r1 = min(r0 + kSplitRows, rank0 + 2 * a.c);
+    } else {
+      r0 = a.S + (int64_t)(c.s - a.D * a.spr) * kSplitRows;
+      r1 = min(r0 + kSplitRows, a.n_total);
+    }
+    return c.s < s_hi && TSP_INB(r0 >= 0 && r0 <= r1 && r1 <= a.n_total, a.status) &&
+           r0 + warp * 32 < r1;
+  };
+  uint32_t pending = 0;   // bit st: stage st has a fill not yet waited for
+  auto load = [&](const Cur& c, int stage) {
+    int64_t r0, r1;
+    if (!rows_of(c, r0, r1)) return;
+    pending |= 1u << stage;
+    if (lane != 0) return;
+    const uint32_t dst = wsm + (uint32_t)(stage * SL::STAGE_BYTES), bar = wbar + 8u * stage;
+    const int y = (int)(r0 + warp * 32);        // rows past the cache read as zeros
+    mbar_arrive_expect_tx(bar, (uint32_t)SL::STAGE_BYTES);
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+      for (int b = 0; b < DH / 64; ++b)
+        tma_load_2d(dst + (uint32_t)(kv * SL::KV_BYTES + b * SL::BOX_BYTES), &a.tm,
+                    kv * a.dkv + g * DH + b * 64, y, bar);
+  };
+  Cur cl = start(s_lo);   // next split to load
+#pragma unroll
+  for (int i = 0; i < kStreamStages - 1; ++i) {
+    load(cl, i);
+    next(cl);
+  }
+
+  // the query rows into staged rows 0..nq-1; rows nq..kQB are zero (row kQB
+  // stands in for the MMA's rows kQB..15)
+  uint8_t* qh = gbase + SL::OFF_Q;
+  for (int idx = threadIdx.x; idx < (kQB + 1) * (DH / 8); idx += kAttnWarps * 32) {
+    const int i = idx / (DH / 8), pc = idx - i * (DH / 8);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (i < nq) {
+      const int gi = i / a.T, t = i - gi * a.T;
+      v = *reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(a.q) +
+                                          (int64_t)t * a.ldq + (g * a.G + gi) * DH + pc * 8);
+    }
+    *reinterpret_cast<uint4*>(qh + L::at(i, pc)) = v;
+  }
+  __syncthreads();
+  // the query fragments (A operand of S = Q K^T), the same for every split
+  uint32_t qa[DH / 16][4];
+  {
+    const int qrow = (lane & 15) < kQB ? (lane & 15) : kQB;
+#pragma unroll
+    for (int kk = 0; kk < DH / 16; ++kk)
+      ldsm_x4(qsm + L::at(qrow, 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+  }
+
+  const int t_row = gq % a.T;                   // token of fragment row gq (rows >= nq unused)
+  const int64_t new_lim = a.n_cached + t_row + 1;   // decoded rows row gq may see: below this
+  float m_run = -INFINITY, l_run = 0.f;         // row gq's running max (log2 units) and sum
+  float o[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+  uint32_t phase = 0;     // bit st: parity of stage st's next fill
+  bool ok = true;         // false after a timed-out wait (warp-uniform)
+
+  Cur cc = start(s_lo);   // split consumed
+  for (int it = 0; cc.s < s_hi; ++it, next(cc)) {
+    if (ok) {
+      load(cl, (it + kStreamStages - 1) % kStreamStages);
+      next(cl);
+    }
+    int64_t r0, r1;
+    if (!rows_of(cc, r0, r1)) continue;         // warp-uniform
+    const int st = it % kStreamStages;
+    if (ok) {
+      ok = __all_sync(0xffffffffu, stage_wait(wbar + 8u * st, (phase >> st) & 1u, a.status,
+                                              a.limit_ns));
+      if (ok) {
+        phase ^= 1u << st;
+        pending &= ~(1u << st);
+      }
+    }
+    if (!ok) continue;
+    const int64_t wr0 = r0 + warp * 32;
+    // keys wr0 + k with k < vis_n are visible to row gq: prompt rows below r1;
+    // decoded rows also at or before the row's own position
+    const int64_t lim = r0 >= a.S ? min(r1, new_lim) : r1;
+    const int vis_n = (int)max((int64_t)0, min((int64_t)32, lim - wr0));
+    const uint32_t ks = wsm + (uint32_t)(st * SL::STAGE_BYTES);
+    const uint32_t vs = ks + (uint32_t)SL::KV_BYTES;
+    // S[16 query rows x 32 keys] = Q K^T: four n8 tiles of keys, DH/16 k-steps
+    float sc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < DH / 16; ++kk) {
+#pragma unroll
+      for (int nt = 0; nt < 4; nt += 2) {
+        const int m = lane >> 3;
+        const uint32_t addr = ks + SL::at((nt + (m >> 1)) * 8 + (lane & 7), 2 * kk + (m & 1));
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(addr, b0, b1, b2, b3);
+        mma16816(sc[nt], qa[kk], b0, b1);
+        mma16816(sc[nt + 1], qa[kk], b2, b3);
+      }
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        sc[nt][e] = nt * 8 + 2 * tq + e < vis_n ? sc[nt][e] * a.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sc[nt][e]);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run, mx);
+    // the earlier rows' share 2^(m_run - m_new); nothing seen yet -> O and l are 0
+    const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+    float l = 0.f;
+    uint32_t pa[2][4];   // P as the A operand of P V: k-steps of 16 keys
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const float p0 = m_new == -INFINITY ? 0.f : exp2f(sc[nt][0] - m_new);
+      const float p1 = m_new == -INFINITY ? 0.f : exp2f(sc[nt][1] - m_new);
+      l += p0 + p1;
+      pa[nt >> 1][(nt & 1) * 2] = pack_f16(p0, p1);
+      pa[nt >> 1][(nt & 1) * 2 + 1] = 0u;
+    }
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    l_run = fmaf(l_run, alpha, l);
+    m_run = m_new;
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {   // O rescaled only when a max grew
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[nt][e] *= alpha;
+    }
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+      for (int nt = 0; nt < NT; nt += 2) {
+        const int m = lane >> 3;
+        const uint32_t addr = vs + SL::at(kk * 16 + (m & 1) * 8 + (lane & 7), nt + (m >> 1));
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(addr, b0, b1, b2, b3);
+        mma16816(o[nt], pa[kk], b0, b1);
+        mma16816(o[nt + 1], pa[kk], b2, b3);
+      }
+    }
+    __syncwarp();   // the stage just read is refilled by a later iteration's load
+  }
+  // after a wait ran out (the status word carries the error and the merge
+  // below still runs), wait -- bounded again -- for the copies in flight
+#pragma unroll
+  for (int st = 0; st < kStreamStages; ++st)
+    if (pending & (1u << st)) (void)stage_wait(wbar + 8u * st, (phase >> st) & 1u, a.status, a.limit_ns);
+
+  if (gq < nq) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      *reinterpret_cast<float2*>(&ro[warp][gq][nt * 8 + 2 * tq]) = make_float2(o[nt][0], o[nt][1]);
+    if (tq == 0) rml[warp][gq] = make_float2(m_run, l_run);
+  }
+  __syncthreads();
+  // merge the warps: M = max m_w, O = sum 2^(m_w - M) o_w, L likewise
+  for (int idx = threadIdx.x; idx < nq * DH; idx += kAttnWarps * 32) {
+    const int i = idx / DH, j = idx - i * DH;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, rml[w][i].x);
+    float O = 0.f, L2 = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float2 ml = rml[w][i];
+      const float sc = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+      O = fmaf(sc, ml.x == -INFINITY ? 0.f : ro[w][i][j], O);
+      L2 = fmaf(sc, ml.y, L2);
+    }
+    const int gi = i / a.T, t = i - gi * a.T;
+    const int64_t slot = ((int64_t)p * a.H + g * a.G + gi) * a.T + t;
+    if (!TSP_INB(slot >= 0 && slot < (int64_t)a.nslice * a.H * a.T, a.status)) continue;
+    a.part_o[slot * DH + j] = O;
+    if (j == 0) a.part_ml[slot] = make_float2(M, L2);
+  }
+}
+
 // CTA per (head, token): the maxima first (lane-parallel loads), then warp w
 // adds splits w, w + 8, ... with no branch between its loads; the warps merge
 // in shared memory:  O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
@@ -852,6 +1149,23 @@ tsp_status decode_attn_mma(const AttnArgs& aa, cudaStream_t st) {
   // the K/V head varies fastest: CTAs running together read whole cache rows
   dim3 grid((unsigned)(aa.H / aa.G * aa.nz), (unsigned)aa.nsplit);
   decode_attn_mma_kernel<DH><<<grid, kAttnWarps * 32, smem, st>>>(aa);
+  TSP_CUDA_TRY(cudaGetLastError());
+  return TSP_OK;
+}
+
+template <int DH>
+tsp_status decode_attn_stream(const AttnArgs& aa, cudaStream_t st) {
+  const size_t smem = StreamSmem<DH>::BYTES;
+  static bool attr[kMaxDevices] = {};   // the attribute holds for one device
+  const int dev = current_device();
+  if (!attr[dev]) {
+    TSP_CUDA_TRY(cudaFuncSetAttribute(decode_attn_stream_kernel<DH>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    attr[dev] = true;
+  }
+  Prof prof("decode_attn", st);
+  dim3 grid((unsigned)(aa.H / aa.G), (unsigned)aa.nslice);
+  decode_attn_stream_kernel<DH><<<grid, kAttnWarps * 32, smem, st>>>(aa);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }
@@ -966,9 +1280,25 @@ tsp_status launch_decode_attn(const DecodeAttn& d, cudaStream_t st) {
     aa.nz = (QR + aa.qpc - 1) / aa.qpc;
   }
   tsp_status r = TSP_ERR_UNSUPPORTED;
+  int n_part = aa.nsplit;   // partials per query row the combine kernel merges
   if (d.dtype == TSP_BF16) {
-    if (d.dh == 128) r = decode_attn_mma<128>(aa, st);
-    else if (d.dh == 64) r = decode_attn_mma<64>(aa, st);
+    // a few query rows per K/V head (one token; grouped heads): one wave of
+    // streaming CTAs, each over a slice of the splits, when the K/V heads
+    // leave room for at least two slices a head
+    const int sms = num_sms();
+    if (aa.G * aa.T <= kQB && 2 * d.Hkv <= sms && (d.dh == 128 || d.dh == 64)) {
+      aa.nslice = std::min(aa.nsplit, sms / d.Hkv);
+      aa.limit_ns = wait_limit_ns();
+      n_part = aa.nslice;
+      // x of every box (a multiple of 64 columns) is 16-byte aligned; the
+      // row extent n_total makes rows past the cache read as zeros
+      if (!tma_map_f16(&aa.tm, d.kv, aa.ldkv, aa.n_total, aa.ldkv, 32)) return TSP_ERR_CUDA;
+      r = d.dh == 128 ? decode_attn_stream<128>(aa, st) : decode_attn_stream<64>(aa, st);
+    } else if (d.dh == 128) {
+      r = decode_attn_mma<128>(aa, st);
+    } else if (d.dh == 64) {
+      r = decode_attn_mma<64>(aa, st);
+    }
   } else {
     if (d.dh == 64) r = decode_attn_t<float, 64>(aa, st);
     else if (d.dh == 32) r = decode_attn_t<float, 32>(aa, st);
@@ -979,7 +1309,7 @@ tsp_status launch_decode_attn(const DecodeAttn& d, cudaStream_t st) {
   const int blocks = d.H * d.T;   // a CTA per (head, token)
   if (d.dtype == TSP_BF16)
     decode_combine_kernel<__half><<<blocks, kCombineWarps * 32, 0, st>>>(
-        aa.part_o, aa.part_ml, (__half*)d.o, aa.nsplit, d.H, d.T, d.dh);
+        aa.part_o, aa.part_ml, (__half*)d.o, n_part, d.H, d.T, d.dh);
   else
     decode_combine_kernel<float><<<blocks, kCombineWarps * 32, 0, st>>>(
         aa.part_o, aa.part_ml, (float*)d.o, aa.nsplit, d.H, d.T, d.dh);

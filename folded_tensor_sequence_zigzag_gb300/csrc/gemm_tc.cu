@@ -29,7 +29,6 @@
 #include <cstdlib>
 #include <cstring>
 #include <memory>
-#include <mutex>
 
 #include "common.cuh"
 #include "gemm_tc.h"
@@ -460,40 +459,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
 // Host side
 // ---------------------------------------------------------------------------
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// Row-major fp16 matrix [outer, inner] with row stride ld elements; box
-// {box_inner = 64, box_outer}; 128-byte swizzle; zero fill out of bounds.
-bool make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld,
-              int box_outer) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-  const cuuint32_t box[2] = {64u, (cuuint32_t)box_outer};
-  const cuuint32_t estr[2] = {1u, 1u};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int EPI, bool A_MN, bool B_MN, bool PAIRED>
 tsp_status launch_t(const KParams& kp, int grid, cudaStream_t st, const char* name) {
   Prof prof(name, st);
@@ -588,8 +553,8 @@ tsp_status gemm_tc(const TcGemm& g, cudaStream_t st) {
   for (int s = 0; s < g.nks; ++s) {
     const int klen = g.kseg_len[s];
     if (!aligned16(g.A[s]) || (g.lda[s] * 2) % 16 != 0) return TSP_ERR_INVALID_ARG;
-    bool ok = g.a_mn ? make_map(&kp->ta[s], g.A[s], g.M, klen, g.lda[s], 64)
-                     : make_map(&kp->ta[s], g.A[s], klen, g.M, g.lda[s], BM);
+    bool ok = g.a_mn ? tma_map_f16(&kp->ta[s], g.A[s], g.M, klen, g.lda[s], 64)
+                     : tma_map_f16(&kp->ta[s], g.A[s], klen, g.M, g.lda[s], BM);
     if (!ok) return TSP_ERR_CUDA;
   }
   const int nb_maps = g.paired ? 2 : (g.nseg_n > 0 ? (g.N + g.nseg_n - 1) / g.nseg_n : g.nks);
@@ -600,9 +565,9 @@ tsp_status gemm_tc(const TcGemm& g, cudaStream_t st) {
     const int klen = (g.nseg_n > 0 || g.paired) ? g.K : g.kseg_len[s];
     const int nlen = g.paired ? g.N : (g.nseg_n > 0 ? g.nseg_n : g.N);
     bool ok;
-    if (g.paired) ok = make_map(&kp->tb[s], g.B[s], klen, nlen, g.ldb[s], 128);
-    else if (g.b_mn) ok = make_map(&kp->tb[s], g.B[s], nlen, klen, g.ldb[s], 64);
-    else ok = make_map(&kp->tb[s], g.B[s], klen, nlen, g.ldb[s], BN);
+    if (g.paired) ok = tma_map_f16(&kp->tb[s], g.B[s], klen, nlen, g.ldb[s], 128);
+    else if (g.b_mn) ok = tma_map_f16(&kp->tb[s], g.B[s], nlen, klen, g.ldb[s], 64);
+    else ok = tma_map_f16(&kp->tb[s], g.B[s], klen, nlen, g.ldb[s], BN);
     if (!ok) return TSP_ERR_CUDA;
   }
   // ring rotation over shard segments of K (k-block granularity: a block

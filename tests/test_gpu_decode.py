@@ -115,3 +115,18 @@ def test_fp32_decode_crosses_split_boundaries():
     want = _oracle_steps(ref_in, S, steps, shape.H, shape.eps)
     for k, (got, w) in enumerate(zip(outs, want)):
         assert_f32_close(got, w, f"decode step {k} (T={steps[k]})")
+
+
+def test_bf16_decode_streaming_across_split_boundaries():
+    """Calls of 4 tokens (then 3) with one query head per K/V head: at most
+    four query rows per K/V head, the streaming kernel's case, for 131 tokens
+    after a 1024-token prompt over D=2 ranks; the appended rows cross the
+    128-row split boundary, with RoPE on.  (The 16K-prompt 7B cases above
+    give that kernel slices of many splits each.)"""
+    S, steps = 1024, [4] * 32 + [3]
+    shape, ref_in, _, outs, cache, cfg = _run(
+        S, dict(d=256, H=2, inter=512, D=2), torch.bfloat16, steps, 10000.0, seed=21, spare=0)
+    assert cache.n == cache.rows_cap
+    want = _oracle_steps(ref_in, S, steps, shape.H, shape.eps)
+    for k, (got, w) in enumerate(zip(outs, want)):
+        assert_bf16_close(got, w, f"bf16 decode step {k} (T={steps[k]})")
