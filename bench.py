@@ -59,6 +59,10 @@ WORKLOADS = {
     # the 7B-shaped block with grouped-query attention (8 K/V heads, four
     # query heads per group) and rotary embedding
     "fwd16k_gqa8": (16384, 8, 4096, 32, 11008, "fwd"),
+    # the same forward computed rank by rank by the TSP schedule: every virtual
+    # rank's per-rank calls in turn (tsp_rank_*), the shard broadcast, K/V
+    # all-gather and MLP ring as device copies on a copy stream
+    "fwd16k_by_rank": (16384, 8, 4096, 32, 11008, "fwd"),
     "fwdbwd8k_gqa8": (8192, 8, 4096, 32, 11008, "fwdbwd"),
     # inference: one new token per step after a 16384-token prompt held in the
     # zigzag KV cache (the prefill runs once, untimed)
@@ -72,7 +76,8 @@ LAYERS = {"stack32_16k": 32, "stack32train_16k": 32}   # other workloads: one bl
 VARIANTS = {"fwd16k_gqa8": {"Hkv": 8, "rope_base": 500000.0},
             "fwdbwd8k_gqa8": {"Hkv": 8, "rope_base": 500000.0},
             "decode16k_gqa8": {"Hkv": 8, "rope_base": 500000.0},
-            "fwdbwd768k_tiled": {"mlp_tile": 16384}}
+            "fwdbwd768k_tiled": {"mlp_tile": 16384},
+            "fwd16k_by_rank": {"by_rank": True}}
 
 
 def decode_bytes(name, d, inter, dkv, n_rows, T=DECODE_T):
@@ -114,6 +119,13 @@ def gemm_flops(name, S, d, inter, dkv=None):
         "gemm_oproj": 2.0 * S * d * d,
         "gemm_w13_swiglu": 4.0 * S * d * inter,
         "gemm_w2": 2.0 * S * d * inter,
+        # the per-rank calls of the schedule: every rank's launches of a step
+        # together do the block's work
+        "rank_gemm_q": 2.0 * S * d * d,
+        "rank_gemm_kv": 4.0 * S * d * dkv,
+        "rank_gemm_oproj": 2.0 * S * d * d,
+        "rank_gemm_w13_swiglu": 4.0 * S * d * inter,
+        "rank_gemm_w2": 2.0 * S * d * inter,
         "attn_fwd": 2.0 * S * (S + 1) * d,
         # backward: dgrad and wgrad of every projection, and the attention
         # backward's five causal products (S recomputed, dP, dV, dK, dQ)
@@ -465,6 +477,10 @@ def workload_config(name):
         extra += f", rotary embedding base {var['rope_base']:g}"
     if var.get("mlp_tile"):
         extra += f", MLP in sequence tiles of {var['mlp_tile']} rows (recomputed in the backward)"
+    if var.get("by_rank"):
+        extra += (", computed rank by rank by the TSP schedule (each virtual rank's per-rank "
+                  "calls in turn; shard broadcast, K/V all-gather and MLP ring as device copies "
+                  "on a copy stream)")
     return {"workload": f"{desc}, S={S}, D={D} zigzag virtual ranks, d_model={d}, "
                         f"{H} heads x {d // H}, SwiGLU inter={inter}, causal{extra}",
             "S": S, "D": D, "d_model": d, "heads": H, "kv_heads": var.get("Hkv", H),
@@ -552,6 +568,15 @@ def run_gpu(args):
     # workspaces above are sized for the calls that convert their own weights,
     # which is more than the prepared calls need, so they serve both.
     prep_mode = "per-step" if kind == "fwdbwd" else ("once" if kind == "fwd" else "none")
+    sched = None
+    if var.get("by_rank"):
+        # packed shards once before timing (what the broadcast and the ring
+        # carry); each rank's calls convert the shard they hold as it arrives
+        from folded_tensor_sequence_zigzag_gb300 import schedule
+        prep_mode = "shards"
+        rows = S // D
+        sched = (schedule.LocalComm(cfg, W, overlap=True),
+                 schedule.GpuRankOps(cfg, W, {r: xz[r * rows:(r + 1) * rows] for r in range(D)}))
     preps = None
     if prep_mode != "none":
         preps = [tsp.prepare_weights(cfg, Wl) for Wl in Ws]
@@ -563,6 +588,13 @@ def run_gpu(args):
         yout = y if yout is None else yout
         tsp.zigzag_permute(xin, D, out=xz)
         pp = None if convert_per_call else preps
+        if sched is not None:
+            comm, ops = sched
+            schedule.forward(comm, ops, D)
+            for r in range(D):
+                yz[r * rows:(r + 1) * rows].copy_(ops.output(r))
+            tsp.zigzag_permute(yz, D, inverse=True, out=yout)
+            return yout
         if prep_mode == "per-step":
             for Wl, p in zip(Ws, preps):
                 tsp.prepare_weights(cfg, Wl, out=p)
@@ -752,7 +784,11 @@ def run_gpu(args):
                             "holds them",
                     "per-step": "bf16 weights converted to the fp16 operand copies once per step, "
                                 "inside the timed region, shared by the forward and the backward",
-                    "none": "the MLP call converts its weights inside every call"}[prep_mode],
+                    "none": "the MLP call converts its weights inside every call",
+                    "shards": "bf16 weights packed into the schedule's shards once, before the "
+                              "timed region (tsp_pack_attn_shards, tsp_pack_mlp_shards); each "
+                              "rank's calls convert the shard they hold to fp16 as it "
+                              "arrives"}[prep_mode],
         "with_weight_conversion_per_call": conv,
         "kernels": per_kernel,
         "roofline": roof,

@@ -92,7 +92,64 @@ struct TcAttnArgs {
   float scale_log2;
   int* status;
   uint64_t limit_ns;
+  // one-rank split mode (split_lc > 0): a CTA per chunk of split_lc key tiles
+  // of one of the rank's 256-row blocks (the last chunk takes the block's last
+  // two tiles, its diagonals), writing O / l in fp32 and log2-sum-exp to the
+  // partials [H][n_items][256][DH] and [H][n_items][256] that
+  // attn_split_merge_kernel merges
+  int split_lc, n_items;
+  float* part_o;
+  float* part_lse;
 };
+
+// The work of blockIdx.x = `pair`, item `blk` of the CTA: the block's first
+// query position p0 and its key tiles [j0, j1) of the block's nB = p0/128 + 2
+// (tile A reads [j0, min(j1, nB - 1)), its diagonal tile nB - 2; tile B reads
+// up to its own diagonal nB - 1).  Without a split: block `blk` of the
+// mirrored pair `pair` (blk 0 in chunk 2D-1-r, blk 1 in chunk r), every tile.
+struct Item {
+  int64_t p0;
+  int j0, j1;
+};
+// blocks of one rank in split mode: b < nb are chunk r's blocks in order,
+// b >= nb chunk 2D-1-r's, mirrored (b = nb + t has block nb-1-t)
+__device__ __forceinline__ int64_t split_block_p0(const TcAttnArgs& a, int b) {
+  const int nb = a.n_blocks;
+  return b < nb ? (int64_t)a.rank0 * a.c + (int64_t)b * BLOCK
+                : (int64_t)(2 * a.D - 1 - a.rank0) * a.c + (int64_t)(2 * nb - 1 - b) * BLOCK;
+}
+// chunks of a block with nB key tiles: split_lc tiles each, the last one up
+// to split_lc + 1 (never fewer than the two diagonal tiles)
+__device__ __forceinline__ int split_chunks(int nB, int lc) { return (nB - 2) / lc + 1; }
+
+__device__ __forceinline__ Item item_of(const TcAttnArgs& a, int pair, int blk) {
+  Item it;
+  if (a.split_lc == 0) {
+    const int rl = pair / a.n_blocks, t = pair - rl * a.n_blocks;
+    const int r = a.rank0 + rl;
+    it.p0 = blk == 0 ? (int64_t)(2 * a.D - 1 - r) * a.c + (int64_t)(a.n_blocks - 1 - t) * BLOCK
+                     : (int64_t)r * a.c + (int64_t)t * BLOCK;
+    it.j0 = 0;
+    it.j1 = (int)(it.p0 / BKV) + 2;
+    return it;
+  }
+  int rem = pair;
+  for (int b = 0; b < 2 * a.n_blocks; ++b) {
+    const int64_t pb = split_block_p0(a, b);
+    const int nB = (int)(pb / BKV) + 2;
+    const int nch = split_chunks(nB, a.split_lc);
+    if (rem < nch) {
+      it.p0 = pb;
+      it.j0 = rem * a.split_lc;
+      it.j1 = rem == nch - 1 ? nB : it.j0 + a.split_lc;
+      return it;
+    }
+    rem -= nch;
+  }
+  it.p0 = 0;
+  it.j0 = it.j1 = 0;   // past the last item: no work
+  return it;
+}
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer();
@@ -131,11 +188,10 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
   const int h = blockIdx.y;
   const int kcol = a.kv_col0 + (h / a.G) * DH;   // K columns of this head's K/V head; V at + dkv
   const int pair = blockIdx.x;
-  const int rl = pair / a.n_blocks, t = pair - rl * a.n_blocks;
-  const int r = a.rank0 + rl;
-  const int64_t p0_mirror =
-      (int64_t)(2 * a.D - 1 - r) * a.c + (int64_t)(a.n_blocks - 1 - t) * BLOCK;
-  const int64_t p0_own = (int64_t)r * a.c + (int64_t)t * BLOCK;
+  const int n_it = a.split_lc ? 1 : 2;   // items (blocks, or chunks of one) of this CTA
+  // a split-mode CTA past the last chunk has nothing to do (every thread
+  // computes the same answer before any barrier or TMEM is set up)
+  if (a.split_lc && item_of(a, pair, 0).j1 == 0) return;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -178,10 +234,11 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
     uint32_t n_cons = 0;           // MMA: ring loads consumed
     uint32_t cnt_a = 0, cnt_b = 0; // MMA: PV rounds of tile A / tile B so far
     uint32_t q_issued = 0;
-    for (int blk = 0; blk < 2; ++blk) {
-      const int64_t p0 = blk == 0 ? p0_mirror : p0_own;
+    for (int blk = 0; blk < n_it; ++blk) {
+      const Item itm = item_of(a, pair, blk);
+      const int64_t p0 = itm.p0;
       const int nA = (int)(p0 / BKV) + 1;     // KV tiles of tile A (last one diagonal)
-      const int nB = nA + 1;                  // tile B has one more, its own diagonal
+      const int j0 = itm.j0, j1 = itm.j1;     // this item's tiles; tile B's last is nA
       const int64_t qrow0 = zz_row_of_pos(p0, a.c, a.D);   // 256 rows, contiguous
       if (warp == WARP_PROD) {
         // ------------------------------------------------------------ producer
@@ -198,7 +255,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
           }
           ++q_issued;
           bool ok = true;
-          for (int j = 0; j < nB && ok; ++j) {
+          for (int j = j0; j < j1 && ok; ++j) {
             const int krow = (int)zz_row_of_pos((int64_t)j * BKV, a.c, a.D);
             (void)TSP_INB(krow >= 0 && krow + BKV <= a.S, a.status);
 #pragma unroll 1
@@ -272,13 +329,13 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
             mma_s(1, kslot);
             umma_commit(slot_empty(kslot));
           }
-          for (int j = 0; j < nB && ok; ++j) {
+          for (int j = j0; j < j1 && ok; ++j) {
             vslot = n_cons % NSLOT;
             if (!(ok = take())) break;
             uint32_t kn = 0;
-            const bool next_k = j + 1 < nB;
+            const bool next_k = j + 1 < j1;
             if (j < nA) {
-              if (!(ok = mma_pv(0, vslot, j == 0))) break;
+              if (!(ok = mma_pv(0, vslot, j == j0))) break;
               if (next_k) {
                 kn = n_cons % NSLOT;
                 if (!(ok = take())) break;
@@ -288,7 +345,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
               kn = n_cons % NSLOT;
               if (!(ok = take())) break;
             }
-            if (!(ok = mma_pv(1, vslot, j == 0))) break;
+            if (!(ok = mma_pv(1, vslot, j == j0))) break;
             umma_commit(slot_empty(vslot));
             if (next_k) {
               mma_s(1, kn);
@@ -313,8 +370,9 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(REG_SOFT));
     uint32_t rounds = 0;           // rounds (S, P, PV) of this thread's tile so far
-    for (int blk = 0; blk < 2; ++blk) {
-      const int64_t p0 = blk == 0 ? p0_mirror : p0_own;
+    for (int blk = 0; blk < n_it; ++blk) {
+      const Item itm = item_of(a, pair, blk);
+      const int64_t p0 = itm.p0;
       const int nA = (int)(p0 / BKV) + 1;     // KV tiles of tile A (last one diagonal)
       const int nB = nA + 1;                  // tile B has one more, its own diagonal
       const int64_t qrow0 = zz_row_of_pos(p0, a.c, a.D);   // 256 rows, contiguous
@@ -327,7 +385,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
         const uint32_t tm_s = lane_base + x * 128, tm_o = lane_base + 256 + x * 128;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < nX; ++j) {
+        const int jx1 = min(itm.j1, nX);
+        for (int j = itm.j0; j < jx1; ++j) {
           const uint32_t c_now = rounds;
           bool okl = mbar_wait(s_full(x), c_now & 1u, a.status, abort_flag, a.limit_ns);
           if (!__all_sync(0xffffffffu, okl)) {
@@ -394,7 +453,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
 #pragma unroll
           for (int k = 0; k < 8; ++k) sum += f16_lo(ps[k]) + f16_hi(ps[k]);
           // PV_x(j-1) must have finished before P_x is overwritten or O_x rescaled
-          if (j > 0) {
+          if (j > itm.j0) {
             okl = mbar_wait(o_done(x), (c_now - 1) & 1u, a.status, abort_flag, a.limit_ns);
             if (!__all_sync(0xffffffffu, okl)) {
               ok = false;
@@ -427,7 +486,26 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
         // epilogue: O / l -> fp16 rows, LSE (after the last PV of this tile)
         const bool eok =
             ok && mbar_wait(o_done(x), (rounds - 1) & 1u, a.status, abort_flag, a.limit_ns);
-        if (__all_sync(0xffffffffu, eok)) {
+        if (__all_sync(0xffffffffu, eok) && a.split_lc) {
+          // split mode: this chunk's O / l (fp32) and log2 of its sum
+          tc_fence_after();
+          const float inv = 1.f / l;
+          const int64_t prow = ((int64_t)h * a.n_items + pair) * BLOCK + x * BQ + row;
+          const bool p_in = TSP_INB(pair < a.n_items, a.status);
+          float4* dst = reinterpret_cast<float4*>(a.part_o + prow * DH);
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            uint32_t ov[32];
+            tmem_ld32(tm_o + q * 32, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              if (p_in) dst[q * 8 + c] = make_float4(
+                  __uint_as_float(ov[4 * c + 0]) * inv, __uint_as_float(ov[4 * c + 1]) * inv,
+                  __uint_as_float(ov[4 * c + 2]) * inv, __uint_as_float(ov[4 * c + 3]) * inv);
+          }
+          if (p_in) a.part_lse[prow] = m_used + __log2f(l);
+        } else if (__all_sync(0xffffffffu, eok)) {
           tc_fence_after();
           const float inv = 1.f / l;
           const int64_t orow_i = qrow0 - a.o_row_off + x * BQ + row;
@@ -464,7 +542,68 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
   }
 }
 
+// Split mode: merges the chunks of every query row of the rank by their
+// log-sum-exp, O = sum 2^(s_i - M) O_i / sum 2^(s_i - M) with s_i = log2 of
+// chunk i's sum and M = max s_i, and LSE = (M + log2 sum) ln 2.  A warp per
+// (rank-local row, head); each lane holds four of the DH columns.
+__global__ void __launch_bounds__(256) attn_split_merge_kernel(const __grid_constant__ TcAttnArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t rr = (int64_t)blockIdx.x * 8 + warp;   // rank-local row: chunk r, then 2D-1-r
+  const int h = blockIdx.y;
+  if (rr >= 2 * a.c) return;
+  const int nb = a.n_blocks;
+  const int64_t within = rr < a.c ? rr : rr - a.c;
+  const int k = (int)(within / BLOCK), i = (int)(within - (int64_t)k * BLOCK);
+  const int b = rr < a.c ? k : 2 * nb - 1 - k;       // the row's block (split_block_p0 order)
+  int first = 0;                                      // its first chunk
+  for (int bb = 0; bb < b; ++bb)
+    first += split_chunks((int)(split_block_p0(a, bb) / BKV) + 2, a.split_lc);
+  const int64_t p0 = split_block_p0(a, b);
+  const int nch = split_chunks((int)(p0 / BKV) + 2, a.split_lc);
+  const int64_t orow = zz_row_of_pos(p0, a.c, a.D) - a.o_row_off + i;
+  if (!TSP_INB(first + nch <= a.n_items && orow >= 0 && orow < a.lse_ld, a.status)) return;
+  const int64_t base = ((int64_t)h * a.n_items + first) * BLOCK + i;
+  float M = -INFINITY;
+  for (int s = 0; s < nch; ++s) M = fmaxf(M, a.part_lse[base + (int64_t)s * BLOCK]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f;
+  for (int s = 0; s < nch; ++s) {
+    const int64_t pr = base + (int64_t)s * BLOCK;
+    const float w = exp2f(a.part_lse[pr] - M);
+    const float4 v = reinterpret_cast<const float4*>(a.part_o + pr * DH)[lane];
+    L += w;
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  }
+  const float inv = 1.f / L;
+  *reinterpret_cast<uint2*>(a.o + orow * a.ldo + h * DH + lane * 4) =
+      make_uint2(pack_f16(acc.x * inv, acc.y * inv), pack_f16(acc.z * inv, acc.w * inv));
+  constexpr float LN2 = 0.69314718055994530942f;
+  if (lane == 0) a.lse[(int64_t)h * a.lse_ld + orow] = (M + __log2f(L)) * LN2;
+}
+
 }  // namespace
+
+// The one-rank split plan for a launch of H heads: no split while the rank's
+// 256-row block pairs and heads give at least kSplitBelow CTAs (half of the
+// 152 SMs); else chunks of lc key tiles, lc sized for about kSplitCtas CTAs.
+// n_items_max bounds the chunks of one head over the rank's blocks for every
+// rank: with T the key tiles of a rank's blocks (the same for every rank:
+// mirrored blocks' counts add up to a constant), sum (nB_b - 2) / lc + 1 is at
+// most T / lc + 2 nb.
+void attn_rank_split_plan(int64_t S, int D, int H, int* lc, int* n_items_max) {
+  constexpr int kSplitBelow = 76, kSplitCtas = 304;
+  const int64_t c = S / (2 * D), nb = c / BLOCK;
+  *lc = 0;
+  *n_items_max = 0;
+  if (nb < 1 || nb * H >= kSplitBelow) return;
+  const int64_t T = nb * (((2 * (int64_t)D - 1) * c + (nb - 1) * BLOCK) / BKV + 4);
+  const int64_t l = std::max<int64_t>(2, (T * H + kSplitCtas - 1) / kSplitCtas);
+  *lc = (int)l;
+  *n_items_max = (int)(T / l + 2 * nb);
+}
 
 namespace {
 
@@ -499,10 +638,18 @@ tsp_status attn_launch(TcAttnArgs* a, int64_t S, int H, int Hkv, int dh, int D, 
   }
   // setmaxnreg.inc would wait forever if the split exceeded the launch allocation
   if ((int64_t)launch_regs * NTHR < (int64_t)REG_TOTAL) return TSP_ERR_UNSUPPORTED;
-  dim3 grid((unsigned)(nranks * a->n_blocks), (unsigned)H);
-  Prof prof("attn_fwd", st);
-  attn_fwd_tc_kernel<<<grid, NTHR, SMEM, st>>>(*a);
-  TSP_CUDA_TRY(cudaGetLastError());
+  dim3 grid((unsigned)(a->split_lc ? a->n_items : nranks * a->n_blocks), (unsigned)H);
+  {
+    Prof prof("attn_fwd", st);
+    attn_fwd_tc_kernel<<<grid, NTHR, SMEM, st>>>(*a);
+    TSP_CUDA_TRY(cudaGetLastError());
+  }
+  if (a->split_lc) {
+    Prof prof("attn_split_merge", st);
+    dim3 mgrid((unsigned)((2 * a->c + 7) / 8), (unsigned)H);
+    attn_split_merge_kernel<<<mgrid, 256, 0, st>>>(*a);
+    TSP_CUDA_TRY(cudaGetLastError());
+  }
   return TSP_OK;
 }
 
@@ -533,8 +680,9 @@ tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, 
 }
 
 tsp_status launch_attn_fwd_rank_f16(const void* q, int64_t ldq, const void* kv, int64_t ldkv,
-                                    void* o, int64_t ldo, float* lse, int64_t S, int H, int dh,
-                                    int D, int r, cudaStream_t st) {
+                                    void* o, int64_t ldo, float* lse, float* part_o,
+                                    float* part_lse, int64_t S, int H, int dh, int D, int r,
+                                    cudaStream_t st) {
   if (dh != DH) return TSP_ERR_UNSUPPORTED;
   const int64_t c = S / (2 * D);
   if (c % BLOCK != 0 || S > (int64_t)INT32_MAX) return TSP_ERR_UNSUPPORTED;
@@ -553,6 +701,24 @@ tsp_status launch_attn_fwd_rank_f16(const void* q, int64_t ldq, const void* kv, 
   a->ldo = ldo;
   a->lse = lse;
   a->lse_ld = 2 * c;
+  int lc = 0, n_max = 0;
+  attn_rank_split_plan(S, D, H, &lc, &n_max);
+  if (lc > 0) {
+    // this rank's chunk count (at most the plan's bound, which sized the partials)
+    const int nb = (int)(c / BLOCK);
+    int n = 0;
+    for (int b = 0; b < 2 * nb; ++b) {
+      const int64_t pb = b < nb ? (int64_t)r * c + (int64_t)b * BLOCK
+                                : (int64_t)(2 * D - 1 - r) * c + (int64_t)(2 * nb - 1 - b) * BLOCK;
+      n += (int)((pb / BKV + 2 - 2) / lc + 1);
+    }
+    if (n > n_max || !part_o || !part_lse || ((uintptr_t)part_o & 15u))
+      return TSP_ERR_INVALID_ARG;
+    a->split_lc = lc;
+    a->n_items = n;
+    a->part_o = part_o;
+    a->part_lse = part_lse;
+  }
   return attn_launch(a, S, H, H, dh, D, 1, st);
 }
 

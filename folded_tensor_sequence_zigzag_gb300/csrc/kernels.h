@@ -66,10 +66,17 @@ tsp_status launch_attn_fwd_f16(const void* qkv, void* o, float* lse, int64_t S, 
                                 int D, cudaStream_t st);
 // one virtual rank r's query rows (multi-head, H heads of width dh): q [2c, ldq]
 // its own rows (head h at column h*dh), kv [S, ldkv] the gathered K|V in zigzag
-// row order (K head h at h*dh, V at H*dh + h*dh); o [2c, ldo], lse [H, 2c]
+// row order (K head h at h*dh, V at H*dh + h*dh); o [2c, ldo], lse [H, 2c].
+// When the rank's blocks alone would fill too few SMs the key range is split
+// into chunks merged by log-sum-exp: part_o / part_lse, fp32 scratch of
+// H * n_items_max * 256 * (dh + 1) floats (attn_rank_split_plan), then hold
+// the chunks' partials (null when the plan has no split).
 tsp_status launch_attn_fwd_rank_f16(const void* q, int64_t ldq, const void* kv, int64_t ldkv,
-                                    void* o, int64_t ldo, float* lse, int64_t S, int H, int dh,
-                                    int D, int r, cudaStream_t st);
+                                    void* o, int64_t ldo, float* lse, float* part_o,
+                                    float* part_lse, int64_t S, int H, int dh, int D, int r,
+                                    cudaStream_t st);
+// lc = key tiles per chunk (0: no split) and the bound on one head's chunks
+void attn_rank_split_plan(int64_t S, int D, int H, int* lc, int* n_items_max);
 
 // attn_bwd.cu (delta: 2 x H x S fp32 scratch, Delta then the scaled LSE)
 tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, const float* lse,

@@ -47,6 +47,7 @@ struct RankWs {
   // dA|dB, dO and dQ of the attention shard, and fp32 scratch
   float *rstd1, *rstd2, *delta, *dq_acc, *dg_part;
   void *dy16, *dh16, *ab, *dab, *dO, *dq;
+  float *part_o, *part_lse;   // the attention's chunk partials (split plan; may be empty)
   size_t bytes;
 };
 
@@ -78,6 +79,11 @@ RankWs rank_layout(const tsp_cfg* c, uint8_t* base) {
   W.delta = (float*)take(2 * (maxC / (size_t)c->dh) * rows * 4);  // Delta and LSE*log2(e)
   W.dq_acc = (float*)take(rows * maxC * 4);
   W.dg_part = (float*)take((size_t)rmsnorm_bwd_blocks((int64_t)rows) * d * 4);
+  int lc = 0, n_items = 0;
+  attn_rank_split_plan(c->S, c->D, (int)(maxC / (size_t)c->dh), &lc, &n_items);
+  const size_t part_rows = maxC / (size_t)c->dh * (size_t)n_items * 256;
+  W.part_o = lc ? (float*)take(part_rows * (size_t)c->dh * 4) : nullptr;
+  W.part_lse = lc ? (float*)take(part_rows * 4) : nullptr;
   W.bytes = off;
   return W;
 }
@@ -166,7 +172,8 @@ tsp_status tsp_rank_attn_heads(const tsp_cfg* cfg, int32_t r, int32_t k, const v
   const int64_t rows = cfg->S / cfg->D;
   const int d = cfg->d;
   const int Ck = (int)(bound(k + 1, d, cfg->D) - bound(k, d, cfg->D));
-  if ((st = launch_attn_fwd_rank_f16(W.q, Ck, kv_all_k, 2 * (int64_t)Ck, W.o, Ck, W.lse, cfg->S,
+  if ((st = launch_attn_fwd_rank_f16(W.q, Ck, kv_all_k, 2 * (int64_t)Ck, W.o, Ck, W.lse, W.part_o,
+                                     W.part_lse, cfg->S,
                                      Ck / cfg->dh, cfg->dh, cfg->D, r, s)) != TSP_OK)
     return st;
   // h_r (+)= O_k W_O[:, C_k]^T; W_O[:, C_k]^T sits in the shard as [C_k, d]
@@ -337,7 +344,8 @@ tsp_status tsp_rank_attn_bwd_heads(const tsp_cfg* cfg, int32_t r, int32_t k,
   const int Ck = (int)(bound(k + 1, d, cfg->D) - bound(k, d, cfg->D));
   const size_t e = 2;
   // O and LSE of the rank's rows for shard k's heads (recomputed)
-  if ((st = launch_attn_fwd_rank_f16(W.q, Ck, kv_all_k, 2 * (int64_t)Ck, W.o, Ck, W.lse, cfg->S,
+  if ((st = launch_attn_fwd_rank_f16(W.q, Ck, kv_all_k, 2 * (int64_t)Ck, W.o, Ck, W.lse, W.part_o,
+                                     W.part_lse, cfg->S,
                                      Ck / cfg->dh, cfg->dh, cfg->D, r, s)) != TSP_OK)
     return st;
   const uint8_t* wot = (const uint8_t*)W.shard + (size_t)3 * Ck * d * e;   // W_O[:, C_k]^T

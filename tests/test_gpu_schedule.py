@@ -26,16 +26,20 @@ def lib():
 
 def _assert_same_up_to_bf16_rounding(y, y_other, what):
     """Two bf16 outputs of the same block computed with the work cut
-    differently: their fp32 values before the final rounding agree to fp32
-    summation order and the internal fp16 roundings, so every element is
-    within one bf16 spacing (2^-7 of its magnitude) of the other, up to a
-    tiny absolute term for elements near zero, and on average far closer."""
+    differently.  Their fp32 values before the final rounding differ by the
+    summation order and by the internal fp16 roundings -- the attention's P
+    among them, which a rank whose key range is split into chunks (a short
+    sequence: too few 256-row blocks to fill the GPU) forms against each
+    chunk's own running maximum and merges by log-sum-exp -- so every element
+    is within two bf16 spacings (2^-6 of its magnitude) of the other, up to a
+    small absolute term for elements near zero, and on average far closer."""
     a, b = O.f64(y), O.f64(y_other)
     rms = float(np.sqrt(np.mean(b * b)))
     diff = np.abs(a - b)
-    bound = 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 1e-3 * rms
-    assert np.all(diff <= bound), (what, float((diff / bound).max()))
-    assert float(diff.sum() / np.abs(b).sum()) <= 1e-3, what
+    bound = 2.0 ** -6 * np.maximum(np.abs(a), np.abs(b)) + 2e-3 * rms
+    mean_rel = float(diff.sum() / np.abs(b).sum())
+    assert np.all(diff <= bound), (what, float((diff / bound).max()), mean_rel)
+    assert mean_rel <= 1e-3, (what, mean_rel)
 
 
 def _run(shape, seed):
@@ -75,6 +79,10 @@ def test_schedule_by_rank_7b_shapes_S16384():
     ref = O.block_fwd_rows(inp["x"], inp, shape.H, shape.eps, rows)
     assert_bf16_close(y[rows], ref, "schedule by rank, 7B shapes")
     _assert_same_up_to_bf16_rounding(y, y_batched, "schedule vs one-pass block, 7B shapes")
+    # the rank path (its attention split into chunks here) is as close to the
+    # oracle as the one-pass block on the sampled rows
+    err = lambda v: float(np.abs(O.f64(v[rows]) - ref).max())
+    assert err(y) <= 1.25 * err(y_batched), (err(y), err(y_batched))
 
 
 def test_rank_calls_reject_what_they_do_not_take():
