@@ -121,6 +121,7 @@ def gemm_flops(name, S, d, inter, dkv=None):
         "gemm_w2": 2.0 * S * d * inter,
         # the per-rank calls of the schedule: every rank's launches of a step
         # together do the block's work
+        "rank_gemm_qkv": 2.0 * S * d * (d + 2 * dkv),
         "rank_gemm_q": 2.0 * S * d * d,
         "rank_gemm_kv": 4.0 * S * d * dkv,
         "rank_gemm_oproj": 2.0 * S * d * d,

@@ -72,6 +72,7 @@ struct KParams {
   int64_t lde;
   int64_t m_seg;
   void* outs[3];
+  int n_split;   // EPI_STORE: columns from here on go to out2
   int* status;
   uint64_t limit_ns;
   int debug_skip;  // failure-detection test: CTA 0 never loads its first stage
@@ -390,7 +391,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
           for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
           if constexpr (EPI == EPI_STORE) {
             if (p.out_type == OUT_F16) bad |= f16_bad_n<32>(f);
-            store_any32(p.out, (int64_t)m * p.ldo + n, f, p.out_type);
+            if (p.n_split > 0 && n >= p.n_split)
+              store_any32(p.out2, (int64_t)m * p.ldo2 + (n - p.n_split), f, p.out_type);
+            else
+              store_any32(p.out, (int64_t)m * p.ldo + n, f, p.out_type);
           } else if constexpr (EPI == EPI_RES) {
             float r[32];
             if (p.res_f32) {
@@ -587,6 +591,10 @@ tsp_status gemm_tc(const TcGemm& g, cudaStream_t st) {
   kp->ldo = g.ldo;
   kp->out2 = g.out2;
   kp->ldo2 = g.ldo2;
+  if (g.n_split < 0 || (g.n_split > 0 && (g.epi != EPI_STORE || g.n_split % BN != 0 ||
+                                          g.n_split >= g.N || !g.out2)))
+    return TSP_ERR_INVALID_ARG;
+  kp->n_split = g.n_split;
   kp->out3 = g.out3;
   kp->ldo3 = g.ldo3;
   kp->res = g.res;

@@ -21,7 +21,9 @@ enum { EPI_STORE = 0, EPI_RES = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_SWIGLU_BWD =
 // shards (boundaries floor(s*K/rot_D), k-block granularity) in ring order
 // (r - t) mod rot_D (rot_r0: the rank of row 0, for a GEMM over a row tile).
 // Epilogues (out/out2/out3 row strides ldo/ldo2/ldo3, elements):
-//   EPI_STORE      out = C stored as out_type (OUT_F16 / OUT_BF16 / OUT_F32)
+//   EPI_STORE      out = C stored as out_type (OUT_F16 / OUT_BF16 / OUT_F32); with
+//                  n_split > 0 (a multiple of 256) columns n >= n_split go to
+//                  out2 at column n - n_split instead
 //   EPI_RES        out = C + res, res bf16 or fp32 (res_f32), stored as out_type
 //   EPI_F32        out = C (fp32); with m_seg > 0 rows go to outs[m / m_seg]
 //   EPI_SWIGLU     out = f16(silu(C_1) * C_3); out2/out3 (nullable) = f16(C_1), f16(C_3)
@@ -56,6 +58,7 @@ struct TcGemm {
   int64_t lde = 0;
   int64_t m_seg = 0;
   void* outs[3] = {nullptr, nullptr, nullptr};
+  int n_split = 0;
 };
 
 tsp_status gemm_tc(const TcGemm& g, cudaStream_t st);

@@ -145,6 +145,18 @@ tsp_status tsp_rank_attn_project(const tsp_cfg* cfg, int32_t r, int32_t k, const
     return st;
   // the received shard (Q, K, V rows, then W_O^T rows) in the fp16 operand type
   if ((st = launch_convert_bf16_f16(shard_k, W.shard, (int64_t)4 * Ck * d, s)) != TSP_OK) return st;
+  if (Ck % 256 == 0) {
+    // one GEMM over the shard's Q, K and V rows: Q of the shard's heads for
+    // the rank's rows into the workspace, K | V (the rank's part of the
+    // all-gather) into kv_k
+    TcGemm g;
+    g.M = (int)rows; g.N = 3 * Ck; g.K = d;
+    g.A[0] = W.a; g.lda[0] = d; g.kseg_len[0] = d;
+    g.B[0] = W.shard; g.ldb[0] = d;
+    g.epi = EPI_STORE; g.out_type = OUT_F16; g.out = W.q; g.ldo = Ck;
+    g.n_split = Ck; g.out2 = kv_k; g.ldo2 = 2 * Ck; g.name = "rank_gemm_qkv";
+    return gemm_tc(g, s);
+  }
   TcGemm q;   // Q of the shard's heads for the rank's rows
   q.M = (int)rows; q.N = Ck; q.K = d;
   q.A[0] = W.a; q.lda[0] = d; q.kseg_len[0] = d;

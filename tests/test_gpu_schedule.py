@@ -60,7 +60,10 @@ def _run(shape, seed):
 
 
 @pytest.mark.parametrize("S,d,H,I,D", [(4096, 1024, 8, 2048, 4), (2048, 512, 4, 1024, 2),
-                                       (4096, 1024, 8, 2048, 1)])
+                                       (4096, 1024, 8, 2048, 1),
+                                       # three heads a shard (384 columns): Q and K|V
+                                       # projected by two GEMMs instead of one
+                                       (2048, 1536, 12, 1024, 4)])
 def test_schedule_by_rank_matches_oracle(S, d, H, I, D):
     shape = BlockShape(S=S, d=d, H=H, inter=I, D=D)
     inp, y, y_batched = _run(shape, seed=S + D)
