@@ -96,7 +96,11 @@ struct TcBwdArgs {
   const float* delta;   // [H][lse_ld]
   float* dq_acc;        // [query rows][dq_ld] fp32, zeroed
   ct_t* out;            // dK at (zigzag row, out_col0 + g*dh), dV out_dkv columns further
-  int64_t S, c, out_ld, q_row_off, q_rows, lse_ld, dq_ld;
+  int64_t S, c, out_ld, q_row_off, q_rows, lse_ld;
+  // 32-bit: the dQ drain forms one address per reduction, and a 32-bit
+  // stride keeps that a single wide multiply-add (a 64-bit one costs the
+  // drain warps, which share the MMA issuer's schedulers, ~16% of the kernel)
+  int dq_ld;
   int q_col0, kv_col0, out_col0, out_dkv;
   int D, n_kt;          // n_kt = c / 128
   int G, dkv;           // query heads per K/V head; K/V width Hkv*dh
