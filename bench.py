@@ -153,20 +153,20 @@ MEASURED_TRAFFIC = {
     # (kernel, workload): (bytes per launch, source file, sha256 of the source);
     # first (cold) launch of the process, from the captures summarised under profiles/
     ("gemm_w13_swiglu", "fwd16k"): (
-        1087107000 + 350731008, "folded_tensor_sequence_zigzag_gb300/csrc/gemm_tc.cu",
-        "ce2f297aab4cb1e40f5466009a187677b6f2508e1bf47cfb84a81454284b26f0"),
+        944034816 + 348202240, "folded_tensor_sequence_zigzag_gb300/csrc/gemm_tc.cu",
+        "e83ee7a870f45b96341ece6c71e6c262d62c017a8ea9d8649962054a2391ec7b"),
     ("attn_fwd", "fwd16k"): (
-        423540480 + 118739456, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
-        "51c3428d7e86a4951317067fe2380ef5ec8a5f32ebc8dc546212f8ad46981586"),
+        424954368 + 115012096, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
+        "1a361e7b2a4150ecd8f0cf420564b80009244418a1564e42aa53eec45db84239"),
     ("attn_bwd", "fwdbwd8k"): (
-        408622592 + 229798656, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
-        "a7729c67a8b19ad2b8a99f7828f59eb792be50f2e977afd6f00cbf7a7e0ca68d"),
+        408550144 + 228360448, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
+        "ab1db0604a37f2c4d273a283460f2cec011a2c7fe73c6cc0b0ff6f292de8bcf8"),
     ("decode_attn", "decode16k"): (
-        268650240 + 4473856, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
-        "6085f2b2a1f1e130cccd798dc95f30b6719464d221e8c54f5dedb3db16dedb82"),
+        268713728 + 2905600, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
+        "f18fb1543642fef5e3c46c60d884bcc4fec2def3a9b08aa0a04305815fe27910"),
     ("decode_attn", "decode16k_gqa8"): (
-        67186176 + 188928, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
-        "6085f2b2a1f1e130cccd798dc95f30b6719464d221e8c54f5dedb3db16dedb82"),
+        67188224 + 7424, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
+        "f18fb1543642fef5e3c46c60d884bcc4fec2def3a9b08aa0a04305815fe27910"),
 }
 
 
