@@ -94,13 +94,9 @@ struct TcBwdArgs {
   CUtensorMap tm_do;    // dO: query head h at columns h*dh
   const float* lse2;    // [H][lse_ld]: LSE * log2(e)
   const float* delta;   // [H][lse_ld]
-  float* dq_acc;        // [query rows][dq_ld] fp32, zeroed
+  float* dq_acc;        // [query head][query rows][dh] fp32 (head-major), zeroed
   ct_t* out;            // dK at (zigzag row, out_col0 + g*dh), dV out_dkv columns further
   int64_t S, c, out_ld, q_row_off, q_rows, lse_ld;
-  // 32-bit: the dQ drain forms one address per reduction, and a 32-bit
-  // stride keeps that a single wide multiply-add (a 64-bit one costs the
-  // drain warps, which share the MMA issuer's schedulers, ~16% of the kernel)
-  int dq_ld;
   int q_col0, kv_col0, out_col0, out_dkv;
   int D, n_kt;          // n_kt = c / 128
   int G, dkv;           // query heads per K/V head; K/V width Hkv*dh
@@ -323,7 +319,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
             if (!mbar_wait(qd_empty(st), qph(cur) ^ 1u, a.status, abort_flag, a.limit_ns)) break;
             const int gi = GROUPED ? j / nqh : 0, jj = j - gi * nqh;
             const int h = g * G + gi;
-            int64_t qrow = zz_row_of_pos(qpos<RANK>(qt, k0, jj), a.c, a.D) - a.q_row_off;
+            int64_t qrow = zz_row_of_pos32((int)qpos<RANK>(qt, k0, jj), (int)a.c, a.D) - a.q_row_off;
             // a failed check reads row 0 instead: the copy still lands, so the
             // pipeline's byte counts hold
             if (!TSP_INB(qrow >= 0 && qrow + BR <= a.q_rows, a.status)) qrow = 0;
@@ -458,7 +454,6 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
         const int quarter = warp & 3;
         const int dh = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const float sc = a.scale * kOperandUnscale;
         bool ok = true;
         for (int j = 0; j < nq; ++j) {
           const uint32_t cur = it + j;
@@ -472,9 +467,17 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           tc_fence_before();
           mbar_arrive(dq_empty);   // dQ^T(cur) read: its columns may take S^T(cur+1)
           const int gi = GROUPED ? j / nqh : 0, jj = j - gi * nqh;
-          const int64_t qrow = zz_row_of_pos(qpos<RANK>(qt, k0, jj), a.c, a.D) - a.q_row_off;
+          const int64_t qrow =
+              zz_row_of_pos32((int)qpos<RANK>(qt, k0, jj), (int)a.c, a.D) - a.q_row_off;
           const bool q_in = TSP_INB(qrow >= 0 && qrow + BR <= a.q_rows, a.status);
-          float* dst = a.dq_acc + qrow * a.dq_ld + (g * G + gi) * DH + dh;
+          // head-major accumulator: the tile's 128 query rows of this head are
+          // DH floats apart, so every reduction's address is dst plus a
+          // constant (no per-reduction address arithmetic in the drain, whose
+          // warps share the MMA issuer's schedulers)
+          float* dst = a.dq_acc + ((int64_t)(g * G + gi) * a.q_rows + qrow) * DH + dh;
+          // dQ^T leaves unscaled (scale * 2^-8 is applied once per element by
+          // dq_convert_kernel): a multiply per reduction would take issue slots
+          // from the schedulers the MMA-issuing thread shares.
           // The reductions leave in 8 groups of 16 with a short sleep between
           // them: at ~24 bytes a clock an SM's reductions drain slower than the
           // warps issue them, and a full queue holds up the P/dS warps' shared
@@ -486,8 +489,8 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
             for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
               for (int e = 0; e < 16; ++e)
-                if (q_in) atomicAdd(dst + (int64_t)(q * 32 + h2 * 16 + e) * a.dq_ld,
-                          __uint_as_float(v[q][h2 * 16 + e]) * sc);
+                if (q_in) atomicAdd(dst + (q * 32 + h2 * 16 + e) * DH,
+                                    __uint_as_float(v[q][h2 * 16 + e]));
               __nanosleep(250);
             }
           }
@@ -620,8 +623,12 @@ __global__ void attn_delta_kernel(const ct_t* __restrict__ o, const ct_t* __rest
 }
 
 // dQKV[:, 0:d] = fp16(dq_acc); dQKV rows are ld elements apart
+// dQ = mul * acc (mul = softmax scale * 2^-8: the accumulator holds the dQ^T
+// MMA outputs unscaled), acc head-major [d / DH][S][DH] -> fp16 rows of
+// stride ld, head h at columns h*DH
 __global__ void dq_convert_kernel(const float* __restrict__ acc, ct_t* __restrict__ dqkv,
-                                  int64_t S, int d, int64_t ld, int* __restrict__ status) {
+                                  int64_t S, int d, int64_t ld, float mul,
+                                  int* __restrict__ status) {
   const int64_t total4 = S * d / 4;
   bool bad = false;   // an fp16 output out of range
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total4;
@@ -629,7 +636,12 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, ct_t* __restric
     const int64_t e = t * 4;
     const int64_t row = e / d;
     const int col = (int)(e - row * d);
-    const float4 v = reinterpret_cast<const float4*>(acc)[t];
+    const int hh = col / DH, j = col - hh * DH;
+    float4 v = *reinterpret_cast<const float4*>(acc + ((int64_t)hh * S + row) * DH + j);
+    v.x *= mul;
+    v.y *= mul;
+    v.z *= mul;
+    v.w *= mul;
     bad |= f16_bad(v.x) | f16_bad(v.y) | f16_bad(v.z) | f16_bad(v.w);
     uint2 o;
     o.x = pack_f16(v.x, v.y);
@@ -704,7 +716,6 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
   a->lse2 = delta + (int64_t)H * S;
   a->delta = delta;
   a->dq_acc = dq_acc;
-  a->dq_ld = d;
   a->out = (ct_t*)dqkv;
   a->out_ld = ld;
   a->out_col0 = d;
@@ -728,7 +739,8 @@ tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, c
                                 : launch_bwd_kernel<false, false>(*a, grid, st);
   if (r != TSP_OK) return r;
   Prof prof("attn_bwd_dq_convert", st);
-  dq_convert_kernel<<<num_sms() * 8, 256, 0, st>>>(dq_acc, (ct_t*)dqkv, S, d, ld, a->status);
+  dq_convert_kernel<<<num_sms() * 8, 256, 0, st>>>(dq_acc, (ct_t*)dqkv, S, d, ld,
+                                                    a->scale * kOperandUnscale, a->status);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }
@@ -764,7 +776,6 @@ tsp_status launch_attn_bwd_rank_f16(const void* q, const void* kv, const void* o
   a->lse2 = delta + (int64_t)Hk * rows;
   a->delta = delta;
   a->dq_acc = dq_acc;
-  a->dq_ld = Ck;
   a->out = (ct_t*)dkv;
   a->out_ld = 2 * Ck;
   a->out_col0 = 0;
@@ -786,7 +797,8 @@ tsp_status launch_attn_bwd_rank_f16(const void* q, const void* kv, const void* o
   const tsp_status res = launch_bwd_kernel<false, true>(*a, dim3((unsigned)(S / BC), (unsigned)Hk), st);
   if (res != TSP_OK) return res;
   Prof prof("rank_attn_bwd_dq_convert", st);
-  dq_convert_kernel<<<num_sms() * 8, 256, 0, st>>>(dq_acc, (ct_t*)dq, rows, Ck, Ck, a->status);
+  dq_convert_kernel<<<num_sms() * 8, 256, 0, st>>>(dq_acc, (ct_t*)dq, rows, Ck, Ck,
+                                                    a->scale * kOperandUnscale, a->status);
   TSP_CUDA_TRY(cudaGetLastError());
   return TSP_OK;
 }

@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
           ++q_issued;
           bool ok = true;
           for (int j = j0; j < j1 && ok; ++j) {
-            const int krow = (int)zz_row_of_pos((int64_t)j * BKV, a.c, a.D);
+            const int krow = zz_row_of_pos32(j * BKV, (int)a.c, a.D);
             (void)TSP_INB(krow >= 0 && krow + BKV <= a.S, a.status);
 #pragma unroll 1
             for (int kv = 0; kv < 2; ++kv) {   // K_j then V_j

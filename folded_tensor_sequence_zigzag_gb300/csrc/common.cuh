@@ -442,6 +442,13 @@ __host__ __device__ __forceinline__ int64_t zz_row_of_pos(int64_t p, int64_t c, 
   int64_t j = p / c, off = p - j * c;
   return j < D ? j * 2 * c + off : (2 * D - 1 - j) * 2 * c + c + off;
 }
+// The same for sequences of at most INT32_MAX positions (every row index then
+// fits 32 bits): a 32-bit division, for kernels that map a row per tile in
+// warps sharing schedulers with a tensor-core issuing thread.
+__device__ __forceinline__ int zz_row_of_pos32(int p, int c, int D) {
+  const int j = p / c, off = p - j * c;
+  return j < D ? j * 2 * c + off : (2 * D - 1 - j) * 2 * c + c + off;
+}
 // Global position held at buffer row b.
 __host__ __device__ __forceinline__ int64_t zz_pos_of_row(int64_t b, int64_t c, int D) {
   int64_t r = b / (2 * c), rem = b - r * 2 * c;
