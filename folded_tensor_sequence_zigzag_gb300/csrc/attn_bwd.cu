@@ -92,8 +92,8 @@ struct TcBwdArgs {
   CUtensorMap tm_q;     // Q: query head h at columns q_col0 + h*dh
   CUtensorMap tm_kv;    // K at columns kv_col0 + g*dh, V at kv_col0 + dkv + g*dh; all S rows
   CUtensorMap tm_do;    // dO: query head h at columns h*dh
-  const float* lse2;    // [H][lse_ld]: LSE * log2(e)
-  const float* delta;   // [H][lse_ld]
+  const float* lse2;    // [H][lse_ld]: -LSE * log2(e)
+  const float* delta;   // [H][lse_ld]: -Delta
   float* dq_acc;        // [query head][query rows][dh] fp32 (head-major), zeroed
   ct_t* out;            // dK at (zigzag row, out_col0 + g*dh), dV out_dkv columns further
   int64_t S, c, out_ld, q_row_off, q_rows, lse_ld;
@@ -174,15 +174,17 @@ __device__ __forceinline__ void p_ds_32(const uint32_t (&sv)[32], const uint32_t
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
       const int x = c8 * 8 + e;
-      float x0 = fmaf(__uint_as_float(sv[x]), scale_log2, -lv[e]);
-      float x1 = fmaf(__uint_as_float(sv[x + 1]), scale_log2, -lv[e + 1]);
+      // L and Delta arrive negated, so both pairs are one .f32x2 operation each
+      float2 xx = ffma2(make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1])),
+                        make_float2(scale_log2, scale_log2), make_float2(lv[e], lv[e + 1]));
       if (MASK) {
-        if (kx > x) x0 = -INFINITY;
-        if (kx > x + 1) x1 = -INFINITY;
+        if (kx > x) xx.x = -INFINITY;
+        if (kx > x + 1) xx.y = -INFINITY;
       }
-      const uint32_t p2 = hmul2_u32(ex2_approx_f16x2(pack_f16(x0, x1)), k256);
-      const uint32_t g2 =
-          pack_f16(__uint_as_float(dv[x]) - dlv[e], __uint_as_float(dv[x + 1]) - dlv[e + 1]);
+      const uint32_t p2 = hmul2_u32(ex2_approx_f16x2(pack_f16(xx.x, xx.y)), k256);
+      const float2 gg = fadd2(make_float2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1])),
+                              make_float2(dlv[e], dlv[e + 1]));
+      const uint32_t g2 = pack_f16(gg.x, gg.y);
       pk[x >> 1] = p2;
       dk[x >> 1] = hmul2_u32(p2, g2);
     }
@@ -616,8 +618,10 @@ __global__ void attn_delta_kernel(const ct_t* __restrict__ o, const ct_t* __rest
               f16_lo(ov.y) * f16_lo(gv.y) + f16_hi(ov.y) * f16_hi(gv.y);
     s = warp_sum(s);
     if (lane == 0) {
-      delta[(int64_t)h * S + row] = s;
-      lse2[(int64_t)h * S + row] = lse[(int64_t)h * S + row] * 1.4426950408889634f;
+      // both negated: the P/dS warps add them (x = s * scale log2e - L2,
+      // dP - Delta) with two-lane fp32 operations that take no negation
+      delta[(int64_t)h * S + row] = -s;
+      lse2[(int64_t)h * S + row] = -lse[(int64_t)h * S + row] * 1.4426950408889634f;
     }
   }
 }

@@ -443,9 +443,10 @@ __global__ void __launch_bounds__(NTHR, 1) attn_fwd_tc_kernel(const __grid_const
           for (int q = 0; q < 4; ++q)
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
-              const float x0 = fmaf(__uint_as_float(sr[q][e]), a.scale_log2, neg_m);
-              const float x1 = fmaf(__uint_as_float(sr[q][e + 1]), a.scale_log2, neg_m);
-              const uint32_t p2 = ex2_approx_f16x2(pack_f16(x0, x1));
+              const float2 xx =
+                  ffma2(make_float2(__uint_as_float(sr[q][e]), __uint_as_float(sr[q][e + 1])),
+                        make_float2(a.scale_log2, a.scale_log2), make_float2(neg_m, neg_m));
+              const uint32_t p2 = ex2_approx_f16x2(pack_f16(xx.x, xx.y));
               pk[q >> 1][(q & 1) * 16 + (e >> 1)] = p2;
               ps[(e >> 1) & 7] = hadd2_u32(ps[(e >> 1) & 7], p2);   // 8 terms a partial
             }

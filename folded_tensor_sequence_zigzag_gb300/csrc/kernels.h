@@ -78,7 +78,7 @@ tsp_status launch_attn_fwd_rank_f16(const void* q, int64_t ldq, const void* kv, 
 // lc = key tiles per chunk (0: no split) and the bound on one head's chunks
 void attn_rank_split_plan(int64_t S, int D, int H, int* lc, int* n_items_max);
 
-// attn_bwd.cu (delta: 2 x H x S fp32 scratch, Delta then the scaled LSE)
+// attn_bwd.cu (delta: 2 x H x S fp32 scratch, -Delta then -LSE*log2(e))
 tsp_status launch_attn_bwd_f16(const void* qkv, const void* o, const void* dO, const float* lse,
                                 float* delta, float* dq_acc, void* dqkv, int64_t S, int H, int Hkv, int dh,
                                 int D, cudaStream_t st);

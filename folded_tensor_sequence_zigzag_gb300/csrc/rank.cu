@@ -76,7 +76,7 @@ RankWs rank_layout(const tsp_cfg* c, uint8_t* base) {
   W.dab = take(rows * 2 * maxI * 2);                              // dA | dB
   W.dO = take(rows * maxC * 2);
   W.dq = take(rows * maxC * 2);
-  W.delta = (float*)take(2 * (maxC / (size_t)c->dh) * rows * 4);  // Delta and LSE*log2(e)
+  W.delta = (float*)take(2 * (maxC / (size_t)c->dh) * rows * 4);  // -Delta and -LSE*log2(e)
   W.dq_acc = (float*)take(rows * maxC * 4);
   W.dg_part = (float*)take((size_t)rmsnorm_bwd_blocks((int64_t)rows) * d * 4);
   int lc = 0, n_items = 0;
