@@ -156,11 +156,11 @@ MEASURED_TRAFFIC = {
         944034816 + 348202240, "folded_tensor_sequence_zigzag_gb300/csrc/gemm_tc.cu",
         "e83ee7a870f45b96341ece6c71e6c262d62c017a8ea9d8649962054a2391ec7b"),
     ("attn_fwd", "fwd16k"): (
-        424954368 + 115012096, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
-        "1a361e7b2a4150ecd8f0cf420564b80009244418a1564e42aa53eec45db84239"),
+        424335872 + 114846720, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
+        "5530b6e00aaa2438b504c61075f93ecdbef0833ca6be8814e57c58b43cc512e5"),
     ("attn_bwd", "fwdbwd8k"): (
-        408550144 + 228360448, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
-        "ab1db0604a37f2c4d273a283460f2cec011a2c7fe73c6cc0b0ff6f292de8bcf8"),
+        408130048 + 228092928, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
+        "c3b1465131c661c1aee91598730842064e8f38babfff5f509589c047a818eff9"),
     ("decode_attn", "decode16k"): (
         268713728 + 2905600, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
         "f18fb1543642fef5e3c46c60d884bcc4fec2def3a9b08aa0a04305815fe27910"),
