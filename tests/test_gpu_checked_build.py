@@ -67,6 +67,14 @@ cfg = tsp.make_cfg(4096, 1024, 8, 2048, 4, torch.bfloat16, shape.eps)
 W = tsp.BlockWeights.from_dict(inp, "cuda")
 out["sched/y"] = schedule.block_fwd_by_schedule(cfg, tsp.zigzag_permute(inp["x"].cuda(), 4), W).cpu()
 check("schedule")
+# and its training step rank by rank (the one-rank attention backward among them)
+inp = make_block_inputs(shape, torch.bfloat16, seed=10, with_dy=True)
+W = tsp.BlockWeights.from_dict(inp, "cuda")
+g = schedule.block_bwd_by_schedule(cfg, tsp.zigzag_permute(inp["x"].cuda(), 4),
+                                   tsp.zigzag_permute(inp["dy"].cuda(), 4), W)
+for k, v in g.items():
+    out["sched_bwd/" + k] = v.cpu()
+check("schedule backward")
 torch.save(out, sys.argv[2])
 """
 
