@@ -424,7 +424,10 @@ tsp_status tsp_pack_mlp_shards(const tsp_cfg* cfg, const tsp_mlp_w* w, void* dst
  *   ws       tsp_rank_workspace_bytes(cfg) bytes, one per rank, passed to
  *            all of that rank's calls of the layer in the order above (it
  *            keeps the normalised rows, the received shard and Q between
- *            calls).
+ *            calls; at short sequences, where a rank's 256-row blocks would
+ *            fill too few SMs, it also holds the attention's per-chunk
+ *            partial outputs: the key range is split into chunks whose
+ *            results are merged by their log-sum-exp).
  * Shapes: TSP_BF16, multi-head attention without rotary embedding, dh = 128,
  * D divides H with H/D >= 2, c a multiple of 256, d a multiple of 256,
  * inter a multiple of 32*D; otherwise TSP_ERR_UNSUPPORTED (and
