@@ -159,8 +159,8 @@ MEASURED_TRAFFIC = {
         424335872 + 114846720, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
         "5530b6e00aaa2438b504c61075f93ecdbef0833ca6be8814e57c58b43cc512e5"),
     ("attn_bwd", "fwdbwd8k"): (
-        408130048 + 228092928, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
-        "c3b1465131c661c1aee91598730842064e8f38babfff5f509589c047a818eff9"),
+        407518976 + 227177216, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
+        "6153d18e49ffa1c13d3bd1855a0b850efe2e96017d7d90ce197a4972184c4fc6"),
     ("decode_attn", "decode16k"): (
         268713728 + 2905600, "folded_tensor_sequence_zigzag_gb300/csrc/decode.cu",
         "f18fb1543642fef5e3c46c60d884bcc4fec2def3a9b08aa0a04305815fe27910"),

@@ -484,7 +484,9 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
           // them: at ~24 bytes a clock an SM's reductions drain slower than the
           // warps issue them, and a full queue holds up the P/dS warps' shared
           // memory loads and stores behind it (the tile took ~8% longer with
-          // the reductions issued in one burst).
+          // the reductions issued in one burst).  The sleeps must stay well
+          // inside a tile's time (~2.5 us): at 8 x 400 ns the drain became the
+          // bottleneck (+55%); 150 and 250 ns time alike.
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
 #pragma unroll
@@ -493,7 +495,7 @@ __global__ void __launch_bounds__(NTHR, 1) attn_bwd_tc_kernel(const __grid_const
               for (int e = 0; e < 16; ++e)
                 if (q_in) atomicAdd(dst + (q * 32 + h2 * 16 + e) * DH,
                                     __uint_as_float(v[q][h2 * 16 + e]));
-              __nanosleep(250);
+              __nanosleep(150);
             }
           }
         }
