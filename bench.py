@@ -127,6 +127,16 @@ def gemm_flops(name, S, d, inter, dkv=None):
         "rank_gemm_oproj": 2.0 * S * d * d,
         "rank_gemm_w13_swiglu": 4.0 * S * d * inter,
         "rank_gemm_w2": 2.0 * S * d * inter,
+        "rank_gemm_w13_recompute": 4.0 * S * d * inter,   # the backward's ring recomputes G, A|B
+        "rank_gemm_dgrad_w2_swiglu": 2.0 * S * d * inter,
+        "rank_gemm_dgrad_w13": 4.0 * S * d * inter,
+        "rank_gemm_wgrad_w13": 4.0 * S * d * inter,
+        "rank_gemm_wgrad_w2": 2.0 * S * d * inter,
+        "rank_gemm_dgrad_wo": 2.0 * S * d * d,
+        "rank_gemm_wgrad_wo": 2.0 * S * d * d,
+        "rank_gemm_wgrad_q": 2.0 * S * d * d,
+        "rank_gemm_wgrad_kv": 4.0 * S * d * dkv,
+        "rank_gemm_dgrad_qkv": 2.0 * S * d * (d + 2 * dkv),
         "attn_fwd": 2.0 * S * (S + 1) * d,
         # backward: dgrad and wgrad of every projection, and the attention
         # backward's five causal products (S recomputed, dP, dV, dK, dQ)

@@ -52,6 +52,31 @@ def test_grouped_kv_flops():
     assert cfg["kv_heads"] == 8 and cfg["rope_base"] > 0
 
 
+def test_rank_schedule_flops_cover_its_launches():
+    """The rank-by-rank workload: every per-rank GEMM launch name the library
+    labels has a flop count, and the forward ones (one Q|K|V GEMM, or Q and
+    K|V apart) add up, with the attention, to the block's forward flops."""
+    import re
+    src = open(os.path.join(ROOT, "folded_tensor_sequence_zigzag_gb300", "csrc", "rank.cu")).read()
+    names = set(re.findall(r'name = "(rank_gemm_\w+)"', src))
+    assert names, "no rank GEMM labels found"
+    S, d, I = 16384, 4096, 11008
+    for n in names:
+        assert bench.gemm_flops(n, S, d, I) is not None, n
+    fused = ["rank_gemm_qkv", "rank_gemm_oproj", "rank_gemm_w13_swiglu", "rank_gemm_w2", "attn_fwd"]
+    apart = ["rank_gemm_q", "rank_gemm_kv"] + fused[1:]
+    for ks in (fused, apart):
+        assert sum(bench.gemm_flops(k, S, d, I) for k in ks) == bench.block_flops(S, d, I, "fwd")
+    bwd = ["rank_gemm_dgrad_w2_swiglu", "rank_gemm_wgrad_w2", "rank_gemm_dgrad_w13",
+           "rank_gemm_wgrad_w13", "rank_gemm_dgrad_wo", "rank_gemm_wgrad_wo", "rank_gemm_wgrad_q",
+           "rank_gemm_wgrad_kv", "rank_gemm_dgrad_qkv"]
+    proj = sum(bench.gemm_flops(k, S, d, I) for k in fused[:4])
+    assert sum(bench.gemm_flops(k, S, d, I) for k in bwd) == 2 * proj
+    S_, D, d_, H, I_, kind = bench.WORKLOADS["fwd16k_by_rank"]
+    assert kind == "fwd" and bench.VARIANTS["fwd16k_by_rank"].get("by_rank")
+    assert "rank by rank" in bench.workload_config("fwd16k_by_rank")["workload"]
+
+
 def test_traffic_figure_tracks_its_source(tmp_path, monkeypatch):
     """A stored ncu traffic figure is reported only while the kernel source
     it was taken on is unchanged."""
