@@ -166,8 +166,8 @@ MEASURED_TRAFFIC = {
         944034816 + 348202240, "folded_tensor_sequence_zigzag_gb300/csrc/gemm_tc.cu",
         "e83ee7a870f45b96341ece6c71e6c262d62c017a8ea9d8649962054a2391ec7b"),
     ("attn_fwd", "fwd16k"): (
-        424335872 + 114846720, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
-        "5530b6e00aaa2438b504c61075f93ecdbef0833ca6be8814e57c58b43cc512e5"),
+        422576384 + 114971648, "folded_tensor_sequence_zigzag_gb300/csrc/attn_fwd.cu",
+        "e15ab810a491d18f59761817c11bd61ea0997429e80e87acca851d2c5e0afd5a"),
     ("attn_bwd", "fwdbwd8k"): (
         407518976 + 227177216, "folded_tensor_sequence_zigzag_gb300/csrc/attn_bwd.cu",
         "6153d18e49ffa1c13d3bd1855a0b850efe2e96017d7d90ce197a4972184c4fc6"),

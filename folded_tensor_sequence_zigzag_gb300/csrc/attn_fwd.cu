@@ -589,13 +589,15 @@ __global__ void __launch_bounds__(256) attn_split_merge_kernel(const __grid_cons
 
 // The one-rank split plan for a launch of H heads: no split while the rank's
 // 256-row block pairs and heads give at least kSplitBelow CTAs (half of the
-// 152 SMs); else chunks of lc key tiles, lc sized for about kSplitCtas CTAs.
+// 152 SMs); else chunks of lc key tiles, lc sized for about kSplitCtas CTAs
+// (one wave: 304 CTAs took 1% longer, their extra partials costing the merge
+// more than the finer chunks saved; 456 took 3% longer).
 // n_items_max bounds the chunks of one head over the rank's blocks for every
 // rank: with T the key tiles of a rank's blocks (the same for every rank:
 // mirrored blocks' counts add up to a constant), sum (nB_b - 2) / lc + 1 is at
 // most T / lc + 2 nb.
 void attn_rank_split_plan(int64_t S, int D, int H, int* lc, int* n_items_max) {
-  constexpr int kSplitBelow = 76, kSplitCtas = 304;
+  constexpr int kSplitBelow = 76, kSplitCtas = 152;
   const int64_t c = S / (2 * D), nb = c / BLOCK;
   *lc = 0;
   *n_items_max = 0;
