@@ -63,6 +63,9 @@ WORKLOADS = {
     # rank's per-rank calls in turn (tsp_rank_*), the shard broadcast, K/V
     # all-gather and MLP ring as device copies on a copy stream
     "fwd16k_by_rank": (16384, 8, 4096, 32, 11008, "fwd"),
+    # ... and the training step that way (the backward schedule's exchanges
+    # as device copies and sums; each shard's gradient left at its owner)
+    "fwdbwd16k_by_rank": (16384, 8, 4096, 32, 11008, "fwdbwd"),
     "fwdbwd8k_gqa8": (8192, 8, 4096, 32, 11008, "fwdbwd"),
     # inference: one new token per step after a 16384-token prompt held in the
     # zigzag KV cache (the prefill runs once, untimed)
@@ -77,7 +80,8 @@ VARIANTS = {"fwd16k_gqa8": {"Hkv": 8, "rope_base": 500000.0},
             "fwdbwd8k_gqa8": {"Hkv": 8, "rope_base": 500000.0},
             "decode16k_gqa8": {"Hkv": 8, "rope_base": 500000.0},
             "fwdbwd768k_tiled": {"mlp_tile": 16384},
-            "fwd16k_by_rank": {"by_rank": True}}
+            "fwd16k_by_rank": {"by_rank": True},
+            "fwdbwd16k_by_rank": {"by_rank": True}}
 
 
 def decode_bytes(name, d, inter, dkv, n_rows, T=DECODE_T):
@@ -137,6 +141,7 @@ def gemm_flops(name, S, d, inter, dkv=None):
         "rank_gemm_wgrad_q": 2.0 * S * d * d,
         "rank_gemm_wgrad_kv": 4.0 * S * d * dkv,
         "rank_gemm_dgrad_qkv": 2.0 * S * d * (d + 2 * dkv),
+        "rank_attn_bwd": 5.0 * S * (S + 1) * d,
         "attn_fwd": 2.0 * S * (S + 1) * d,
         # backward: dgrad and wgrad of every projection, and the attention
         # backward's five causal products (S recomputed, dP, dV, dK, dQ)
@@ -588,6 +593,10 @@ def run_gpu(args):
         rows = S // D
         sched = (schedule.LocalComm(cfg, W, overlap=True),
                  schedule.GpuRankOps(cfg, W, {r: xz[r * rows:(r + 1) * rows] for r in range(D)}))
+        if kind == "fwdbwd":
+            for r in range(D):   # each rank's dy rows: views of the step's permuted dy
+                sched[1].set_dy(r, dyz[r * rows:(r + 1) * rows])
+            dxz = torch.empty(x.shape, dtype=torch.float32, device=dev)
     preps = None
     if prep_mode != "none":
         preps = [tsp.prepare_weights(cfg, Wl) for Wl in Ws]
@@ -602,6 +611,13 @@ def run_gpu(args):
         if sched is not None:
             comm, ops = sched
             schedule.forward(comm, ops, D)
+            if kind == "fwdbwd":
+                tsp.zigzag_permute(dy, D, out=dyz)
+                dx = schedule.backward(comm, ops, D)
+                for r in range(D):
+                    dxz[r * rows:(r + 1) * rows].copy_(dx[r])
+                tsp.zigzag_permute(dxz, D, inverse=True, out=yout)
+                return yout
             for r in range(D):
                 yz[r * rows:(r + 1) * rows].copy_(ops.output(r))
             tsp.zigzag_permute(yz, D, inverse=True, out=yout)
@@ -772,6 +788,9 @@ def run_gpu(args):
     for ms, name, k in kernel_rows:
         per_launch_ms = ms / max(k, 1)
         f = gemm_flops(name, S, d, inter, dkv)   # one layer-step's flops over all its launches
+        if (f is not None and sched is not None and kind == "fwdbwd" and
+                name in ("attn_fwd", "rank_gemm_qkv", "rank_gemm_q", "rank_gemm_kv")):
+            f *= 2   # rank by rank the backward recomputes each rank's Q, K|V, O and LSE
         entry = {"launches": k, "ms_per_launch": per_launch_ms}
         if f is not None and kind != "mlp":
             entry["tflops"] = f * L * args.steps / (ms / 1e3) / 1e12
